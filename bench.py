@@ -1,0 +1,552 @@
+#!/usr/bin/env python
+"""FP32 GEMM benchmark: TFLOP/s (2MNK / CUDA-event time) per shape and % of roofline.
+
+Headline workload: the large squares 4096x4096x4096 and 8192x8192x8192 (A, B
+uniform[-1,1) from seeded SplitMix64).  One step = one GEMM of each shape
+through the C-ABI (gemm_f32_run), inputs resident in HBM; both shapes' operands
+exceed the 129 MB L2, so no flush is needed between steps.  `value` is
+2*sum(MNK) per step over the device-timed step (CUDA events, max over ranks),
+times the number of ranks.
+
+Also printed, in the same JSON line:
+  roofline      the dominant kernel (tcgen05 main GEMM) timed live with CUDA
+                events recorded by the library around each launch (tracing
+                API), against the 3xTF32-effective tensor peak;
+  per_shape     every shape of every configuration: TFLOP/s, roofline fraction,
+                chosen kernel, max normalised error against the CPU oracle;
+  e2e           the same metric through gemm_f32_run_host with pinned host
+                buffers (host->device copies of A, B and the copy of C back
+                inside the timed region);
+  cpu_baseline  the CPU oracle timed on a bounded sample of the workload.
+
+`--impl reference` times the CPU oracle itself (the reference arm: there is no
+runnable reference implementation for this GPU) on the same workload.
+With torchrun (N > 1) every rank runs an independent replica (weak scaling);
+there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP32 GEMM TFLOP/s (2MNK/CUDA-event time) per shape; % of roofline"
+HEADLINE = "large_squares"
+TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense TF32 : BF16 tensor ratio
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "measured"
+    try:
+        with open(path) as f:
+            p = json.load(f)
+    except (OSError, ValueError):
+        p, src = dict(FALLBACK), "fallback"
+    hbm = float(p.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+    bf16 = float(p.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    bf16s = float(p.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
+    return {
+        "source": src,
+        "hbm_gbs": hbm,
+        # 3xTF32-effective FP32 peak = dense TF32 peak / 3, the TF32 peak taken
+        # as the measured BF16 peak times the nominal TF32:BF16 ratio.
+        "f32_3xtf32_tflops_burst": bf16 * TF32_OVER_BF16 / 3.0,
+        "f32_3xtf32_tflops_sustained": bf16s * TF32_OVER_BF16 / 3.0,
+        # FP32 SIMT: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz (nominal).
+        "f32_simt_tflops_nominal": 152 * 128 * 2 * 2.07e9 / 1e12,
+    }
+
+
+def shapes_of(workload, shape=None):
+    """The (name, M, N, K, dist, seed_A, seed_B) entries of a workload, or a
+    single M x N x K shape (uniform inputs) when `shape` is given."""
+    from software_pipelined_gb300 import inputs
+    if shape:
+        M, N, K = (int(v) for v in shape.lower().split("x"))
+        return [(f"{M}x{N}x{K}", M, N, K, "uniform", 5001, 5002)]
+    return inputs.WORKLOADS[workload]
+
+
+def algorithmic_bytes(M, N, K):
+    return 4 * (M * K + K * N + M * N)
+
+
+# ---------------------------------------------------------------------------
+# Clocks sampled during the timed region.
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm).
+# ---------------------------------------------------------------------------
+
+def oracle_rows_rate(A, B, rows):
+    """Time the oracle on the first `rows` rows of A*B; returns (seconds, flops)."""
+    import oracle
+    Asub = np.ascontiguousarray(A[:rows])
+    t0 = time.perf_counter()
+    oracle.gemm_f64(Asub, B, with_scale=False)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * B.shape[1] * A.shape[1]
+
+
+def oracle_sample(A, B, target_s):
+    """Largest row block (a multiple of the thread count) the oracle finishes in
+    about target_s seconds, timed; returns (tflops, rows, seconds, threads)."""
+    import oracle
+    threads = oracle.get_threads()
+    cal = max(threads, 1)
+    dt, fl = oracle_rows_rate(A, B, cal)
+    rows = int(max(cal, min(A.shape[0], cal * max(1, round(target_s / max(dt, 1e-6))))))
+    rows = max(threads, rows // threads * threads) if rows >= threads else rows
+    dt, fl = oracle_rows_rate(A, B, rows)
+    return fl / dt / 1e12, rows, dt, threads
+
+
+# ---------------------------------------------------------------------------
+# GPU arm.
+# ---------------------------------------------------------------------------
+
+def time_batches(plan_run, stream, target_ms=20.0, batches=5, warm_ms=100.0):
+    """Median per-run time (ms) over batches of back-to-back runs, CUDA events."""
+    import torch
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one timed run to size the batch
+    for _ in range(3):
+        plan_run()
+    ev0.record(stream)
+    plan_run()
+    ev1.record(stream)
+    ev1.synchronize()
+    one = max(ev0.elapsed_time(ev1), 1e-3)
+    reps = int(max(1, min(2000, target_ms / one)))
+    t_end = time.perf_counter() + warm_ms / 1e3
+    while time.perf_counter() < t_end:
+        for _ in range(reps):
+            plan_run()
+        torch.cuda.synchronize()
+    res = []
+    for _ in range(batches):
+        ev0.record(stream)
+        for _ in range(reps):
+            plan_run()
+        ev1.record(stream)
+        ev1.synchronize()
+        res.append(ev0.elapsed_time(ev1) / reps)
+    return statistics.median(res), min(res), max(res), reps
+
+
+def make_device_operands(M, N, K, dist, sa, sb):
+    import torch
+    from software_pipelined_gb300 import inputs
+    A, B = inputs.make_operands(M, N, K, dist, sa, sb)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    return A, B, dA, dB, dC
+
+
+def parity(A, B, Cd, full_limit=2 ** 31):
+    """Max normalised error of the GPU result against the oracle: the full
+    output for moderate sizes, sampled outputs beyond."""
+    import oracle
+    M, K = A.shape
+    N = B.shape[1]
+    C = Cd.cpu().numpy()
+    if M * N * K <= full_limit:
+        Cr, S = oracle.gemm_f64(A, B)
+        return oracle.normalised_error(C, Cr, S, K), "full"
+    rng = np.random.default_rng(12345)
+    rows = np.concatenate([[0, M - 1, 0, M - 1], rng.integers(0, M, 1024)])
+    cols = np.concatenate([[0, 0, N - 1, N - 1], rng.integers(0, N, 1024)])
+    c, s = oracle.gemm_f64_entries(A, B, rows, cols)
+    return oracle.normalised_error(C[rows, cols], c, s, K), "sampled-1028"
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_src_hash):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, only if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "tcgen05_main_dram_traffic.txt")
+    try:
+        with open(path) as f:
+            lines = [l.split("#")[0].strip() for l in f]
+    except OSError:
+        return None, "no ncu traffic summary"
+    kv = dict(l.split("=", 1) for l in lines if "=" in l)
+    if kv.get("kernel_source_sha256_16") != kernel_src_hash:
+        return None, "kernel changed since the ncu capture"
+    try:
+        return {k[len("bytes_per_launch_"):]: float(v) for k, v in kv.items()
+                if k.startswith("bytes_per_launch_")}, "ncu"
+    except ValueError:
+        return None, "unreadable ncu summary"
+
+
+def run_gpu_arm(args):
+    import torch
+    import software_pipelined_gb300 as g
+    from software_pipelined_gb300 import build as gbuild
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        gbuild.build()
+    if dist:
+        dist.barrier()
+    g.load()
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    dev_name = torch.cuda.get_device_name(local)
+
+    # ---- headline: the large squares, one GEMM of each per step -------------
+    work = []
+    for (name, M, N, K, dist_name, sa, sb) in shapes_of(args.workload, args.shape):
+        A, B, dA, dB, dC = make_device_operands(M, N, K, dist_name, sa, sb)
+        plan = g.Plan(M, N, K)
+        plan.trace_enable(args.steps)
+        work.append(dict(name=name, M=M, N=N, K=K, A=A, B=B, dA=dA, dB=dB, dC=dC, plan=plan,
+                         run=(lambda p=plan, a=dA, b=dB, c=dC: p.run_ptr(a.data_ptr(), b.data_ptr(),
+                                                                         c.data_ptr(), sptr))))
+    flops_step = sum(2.0 * w["M"] * w["N"] * w["K"] for w in work)
+
+    def step():
+        for w in work:
+            s = w["run"]()
+            if s != g.OK:
+                raise g.GemmError(s, "gemm_f32_run")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for w in work:  # drop warm-up traces; the timed region records afresh
+        w["plan"].trace_read(args.steps)
+        w["plan"].trace_enable(args.steps)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.1)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    for w in work:
+        s = w["plan"].check()
+        if s != g.OK:
+            raise g.GemmError(s, "gemm_f32_check")
+
+    # per-kernel durations in the timed region (library-recorded CUDA events)
+    main_fl, main_ms, split_ms, red_ms, per_kernel = 0.0, 0.0, 0.0, 0.0, {}
+    for w in work:
+        runs = w["plan"].trace_read(args.steps)
+        sp = sum(r[0] for r in runs) / len(runs)
+        mn = sum(r[1] for r in runs) / len(runs)
+        rd = sum(r[2] for r in runs) / len(runs)
+        main_fl += 2.0 * w["M"] * w["N"] * w["K"]
+        main_ms += mn
+        split_ms += sp
+        red_ms += rd
+        per_kernel[w["name"]] = {"plan": w["plan"].describe(), "split_ms": round(sp, 4),
+                                 "main_ms": round(mn, 4), "reduce_ms": round(rd, 4),
+                                 "main_tflops": round(2.0 * w["M"] * w["N"] * w["K"] / (mn * 1e-3) / 1e12, 2)}
+    achieved = main_fl / (main_ms * 1e-3) / 1e12
+    peak = pk["f32_3xtf32_tflops_sustained"]
+    kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", "tc_gemm.cu")])
+    traffic, traffic_src = traffic_for(kern_hash)
+    traffic_per_launch = None
+    if traffic:
+        tot = [traffic.get(w["name"]) for w in work]
+        if all(t is not None for t in tot):
+            traffic_per_launch = sum(tot) / len(tot)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic_per_launch,
+                "kernel": "tc_gemm_kernel (tcgen05 3xTF32 main GEMM)",
+                "peak_basis": f"of {pk['source']}: sustained bf16 x {TF32_OVER_BF16:.4f} (nominal tf32/bf16) / 3",
+                "frac_of_burst_peak": round(achieved / pk["f32_3xtf32_tflops_burst"], 4),
+                "traffic_source": traffic_src, "kernel_source_sha256_16": kern_hash,
+                "share_of_step": round(main_ms / ms_step, 4),
+                "split_pass_share_of_step": round(split_ms / ms_step, 4),
+                "per_shape": per_kernel}
+    launches = args.steps * sum(w["plan"].kernel_launches for w in work)
+
+    # headline parity (sampled against the oracle)
+    headline_parity = {}
+    if rank == 0 and not args.quick:
+        for w in work:
+            err, how = parity(w["A"], w["B"], w["dC"], full_limit=0)
+            headline_parity[w["name"]] = {"max_normalised_error": round(err, 4), "checked": how}
+
+    # ---- e2e: through the C-ABI host-buffer call ------------------------------
+    e2e = None
+    if not args.no_e2e:
+        hbufs = []
+        for w in work:
+            hA = torch.from_numpy(w["A"]).pin_memory()
+            hB = torch.from_numpy(w["B"]).pin_memory()
+            hC = torch.empty((w["M"], w["N"]), dtype=torch.float32).pin_memory()
+            hbufs.append((w, hA, hB, hC))
+
+        def e2e_step():
+            for (w, hA, hB, hC) in hbufs:
+                s = w["plan"].run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
+                if s != g.OK:
+                    raise g.GemmError(s, "gemm_f32_run_host")
+        for w in work:
+            w["plan"].trace_enable(0)
+        e2e_step()
+        n_e2e = max(3, args.steps // 10)
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        dt = (time.perf_counter() - t0) / n_e2e
+        if dist:
+            t = torch.tensor([dt], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": round(world * flops_step / dt / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(sum(4 * (w["M"] * w["K"] + w["K"] * w["N"]) for w in work)),
+               "d2h_bytes_per_step": int(sum(4 * w["M"] * w["N"] for w in work)),
+               "ms_per_step": round(dt * 1e3, 3), "steps": n_e2e,
+               "call": "gemm_f32_run_host (pinned host A, B, C; copies and sync inside the call)"}
+        del hbufs
+
+    # ---- per shape: every configuration's shapes ----------------------------
+    per_shape = None
+    floors = None
+    if rank == 0 and not args.no_per_shape:
+        per_shape = []
+        from software_pipelined_gb300 import inputs
+        for key in ("tiny_32", "small_ragged", "tall_skinny", "square_1024", "large_squares"):
+            for (name, M, N, K, dist_name, sa, sb) in inputs.WORKLOADS[key]:
+                if key == args.workload and not args.shape:
+                    w = next(x for x in work if x["name"] == name)
+                    A, B, dA, dB, dC, plan = w["A"], w["B"], w["dA"], w["dB"], w["dC"], w["plan"]
+                else:
+                    A, B, dA, dB, dC = make_device_operands(M, N, K, dist_name, sa, sb)
+                    plan = g.Plan(M, N, K)
+                run = (lambda p=plan, a=dA, b=dB, c=dC: p.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), sptr))
+                med, lo, hi, reps = time_batches(run, stream)
+                fl = 2.0 * M * N * K
+                byts = algorithmic_bytes(M, N, K)
+                P = pk["f32_3xtf32_tflops_burst"]
+                t_roof = max(fl / (P * 1e12), byts / (pk["hbm_gbs"] * 1e9))
+                t_roof_simt = max(fl / (pk["f32_simt_tflops_nominal"] * 1e12), byts / (pk["hbm_gbs"] * 1e9))
+                err, how = (None, None) if args.quick else parity(A, B, dC)
+                per_shape.append({
+                    "config": key, "shape": name, "plan": plan.describe(),
+                    "us": round(med * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                    "tflops": round(fl / (med * 1e-3) / 1e12, 3),
+                    "roofline_frac": round(t_roof / (med * 1e-3), 4),
+                    "roofline_frac_vs_simt_peak": round(t_roof_simt / (med * 1e-3), 4),
+                    "max_normalised_error": None if err is None else round(err, 4), "checked": how,
+                    "l2": "warm (back-to-back)" if byts < 100e6 else "inputs larger than L2",
+                    "runs_per_batch": reps})
+                if key != args.workload or args.shape:
+                    plan.close()
+                    del dA, dB, dC
+        # launch/event floors on this stream
+        ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(50):
+            ev_a.record(stream)
+            ev_b.record(stream)
+            ev_b.synchronize()
+            ts.append(ev_a.elapsed_time(ev_b))
+        z = torch.empty((1, 1), dtype=torch.float32, device="cuda")
+        zp = g.Plan(1, 1, 0, 1, 1, 1)
+        med, _, _, _ = time_batches(lambda: zp.run_ptr(0, 0, z.data_ptr(), sptr), stream)
+        zp.close()
+        floors = {"event_pair_us": round(statistics.median(ts) * 1e3, 3),
+                  "smallest_kernel_us": round(med * 1e3, 3),
+                  "note": "smallest kernel = this library's 1x1 zero-fill, back-to-back launches"}
+
+    # ---- CPU baseline: the oracle on a bounded sample ------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        big = max(work, key=lambda w: w["M"] * w["N"] * w["K"])
+        tf, rows, dt, threads = oracle_sample(big["A"], big["B"], args.cpu_seconds)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} rows of {big['name']} ({rows}x{big['N']}x{big['K']}), "
+                         f"FP64 i-k-j triple loop, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64, uniform[-1,1))",
+            "config": {"workload": ("large squares: 4096x4096x4096 + 8192x8192x8192 FP32 GEMM, row-major, "
+                                    "tight leading dimensions, one GEMM of each per step") if not args.shape
+                       else f"single shape {args.shape} FP32 GEMM, row-major, tight leading dimensions",
+                       "shapes": [w["name"] for w in work],
+                       "l2": "inputs larger than L2 (no flush needed)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk, "headline_parity": headline_parity, "per_shape": per_shape, "floors": floors,
+            "peaks": pk, "device": dev_name,
+            "library_sha256_16": source_hash([g.LIB_PATH]),
+        }
+        print(json.dumps(line), flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                json.dump(line, f, indent=1)
+    for w in work:
+        w["plan"].close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the same workload.
+# ---------------------------------------------------------------------------
+
+def run_reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from software_pipelined_gb300 import inputs
+    oracle.build()
+    big = max(shapes_of(args.workload), key=lambda w: w[1] * w[2] * w[3])
+    name, M, N, K, dist_name, sa, sb = big
+    A, B = inputs.make_operands(M, N, K, dist_name, sa, sb)
+    threads = oracle.get_threads()
+    # size one step so that warmup + steps take about two minutes in all
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    _, rows, _, _ = oracle_sample(A, B, budget)
+    for _ in range(args.warmup):
+        oracle_rows_rate(A, B, rows)
+    times = []
+    fl = 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_rows_rate(A, B, rows)
+        times.append(dt)
+    dt = sum(times) / len(times)
+    v = fl / dt / 1e12
+    sample = f"first {rows} rows of {name} ({rows}x{N}x{K}) per step, FP64 i-k-j triple loop"
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64, uniform[-1,1))",
+            "config": {"workload": "large squares: 4096x4096x4096 + 8192x8192x8192 FP32 GEMM, row-major",
+                       "sample": sample},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--shape", default=None, help="time one MxNxK shape instead of the workload")
+    ap.add_argument("--no-per-shape", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip the parity checks inside the bench")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--json-out", default=None)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference_arm(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * gemm_f32 — FP32 matrix multiply C = A*B on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the tiled dense FP32 GEMM whose K-loop stages tiles of A
+ * and B through on-chip memory with a double-buffered / multi-stage prefetch
+ * ("Double Buffering" technique page; "Case Study: The Double-Buffered GEMM",
+ * the sync_copy_db listing and the paragraph on the single barrier's double
+ * duty).  Three kernels sit behind this interface:
+ *
+ *   - a tcgen05 tensor-core kernel: a TMA producer warp fills an N-stage
+ *     mbarrier ring in shared memory, an MMA warp accumulates into TMEM with an
+ *     error-compensated 3xTF32 split, an epilogue warpgroup drains TMEM;
+ *   - a SIMT FFMA kernel with cp.async double/multi-stage buffering, for tiny,
+ *     latency-bound shapes;
+ *   - a deterministic split-K reduction.
+ *
+ * A per-shape dispatcher chooses kernel, tile, stage count and split-K
+ * ("Double Buffering" page, last paragraph, and the case study's first
+ * paragraph: no single kernel is fastest; libraries dispatch per shape).
+ *
+ * Conventions (every entry point):
+ *   - Row-major.  A is M x K with lda >= K, B is K x N with ldb >= N, C is
+ *     M x N with ldc >= N; leading dimensions are in elements.
+ *   - C is overwritten and never read (no alpha/beta): NaN in C before the
+ *     call does not propagate.
+ *   - M == 0 or N == 0: nothing to do, GEMM_F32_OK.  K == 0: C is filled with
+ *     zeros (the empty sum).
+ *   - A and B must not overlap C.  This is not checked.
+ *   - Any base-pointer alignment and any leading dimension is accepted; the
+ *     dispatcher routes around what a kernel cannot take.
+ *   - Accuracy: every element satisfies |C - C_exact| <= 2*K*2^-24*sum_k|A_ik||B_kj|
+ *     for finite inputs.  The tensor-core path splits each operand into two
+ *     TF32 pieces (22 significand bits), whose per-product error of about
+ *     3*2^-22*|a||b| meets that bound only for K of about 10 and up, so it
+ *     takes K >= 16 only; smaller K always runs on the SIMT kernel.  With non-finite inputs the affected outputs are
+ *     non-finite, but not necessarily the IEEE value (the 3xTF32 split turns
+ *     +-Inf into NaN).
+ *   - Errors are returned as status codes; nothing calls exit or abort.
+ *   - A plan is bound to the CUDA device that was current when it was made and
+ *     must run with that device current.  One plan may be used from one stream
+ *     at a time: it owns scratch memory (split-K partials, split operands).
+ */
+#ifndef GEMM_F32_H_
+#define GEMM_F32_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_F32_API __attribute__((visibility("default")))
+#else
+#define GEMM_F32_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque plan.  Created by gemm_f32_plan / gemm_f32_plan_ex, owned by the
+ * caller, released by gemm_f32_plan_destroy. */
+typedef struct gemm_f32_plan_s* gemm_f32_plan_t;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* gemm_f32_stream_t;
+
+typedef enum {
+    GEMM_F32_OK = 0,
+    GEMM_F32_ERR_INVALID_ARG = 1, /* bad size, leading dimension, NULL pointer or option */
+    GEMM_F32_ERR_UNSUPPORTED = 2, /* forced variant cannot run this problem; no GPU of the right kind */
+    GEMM_F32_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, copy, tensor map) */
+    GEMM_F32_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out; the result is not valid */
+    GEMM_F32_ERR_OOM = 5          /* device or pinned host allocation failed */
+} gemm_f32_status;
+
+typedef enum {
+    GEMM_F32_VARIANT_AUTO = 0,     /* dispatcher's choice */
+    GEMM_F32_VARIANT_SIMT = 1,     /* FFMA, cp.async multi-stage */
+    GEMM_F32_VARIANT_TCGEN05 = 2   /* tcgen05 3xTF32 with TMA/mbarrier pipeline */
+} gemm_f32_variant;
+
+/* Options for gemm_f32_plan_ex.  Zero means "dispatcher's choice" for every
+ * field; gemm_f32_opts_init fills the defaults. */
+typedef struct {
+    int32_t variant;        /* gemm_f32_variant */
+    int32_t tile_m;         /* output tile rows (SIMT: 32/64/128; TC: 128) */
+    int32_t tile_n;         /* output tile cols (SIMT: 32/64/128; TC: 64/128/256) */
+    int32_t stages;         /* pipeline depth (SIMT: 1..4; TC: 2..8) */
+    int32_t split_k;        /* K splits, 1 = none (max 64) */
+    int32_t tf32_terms;     /* TC only: 3 = 3xTF32 (default); 1 = single TF32 product,
+                               a deliberately inaccurate negative control for tests */
+    int64_t wait_timeout_cycles; /* TC only: limit of every device-side wait, in SM clock
+                                    cycles; 0 = default (about 2^32 cycles) */
+    int32_t debug_withhold_stage; /* TC only, test hook: >0 makes the producer skip the
+                                     load of that pipeline fill (1-based), so the MMA
+                                     warp's bounded wait runs out and the run reports
+                                     GEMM_F32_ERR_TIMEOUT through gemm_f32_check */
+    int32_t reserved[7];
+} gemm_f32_opts;
+
+/* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */
+GEMM_F32_API gemm_f32_status gemm_f32_opts_init(gemm_f32_opts* opts);
+
+/*
+ * Make a plan for C[M x N] = A[M x K] * B[K x N] with the given leading
+ * dimensions.  Chooses the kernel and its configuration, allocates the plan's
+ * scratch memory on the current device (cudaMalloc) and prepares the tensor
+ * maps of that scratch.  Pointers to A, B and C are given only at run time.
+ *
+ * INVALID_ARG: M, N or K negative; lda < K, ldb < N or ldc < N (when the
+ * matrix is non-empty); leading dimension < 1; plan NULL.
+ * UNSUPPORTED: no CUDA device, or the device is not sm_103.
+ * OOM: scratch allocation failed.  On any error *plan is set to NULL.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_plan(int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_f32_plan_t* plan);
+
+/* As gemm_f32_plan, with options (NULL = defaults).  A forced variant or
+ * configuration that cannot run the problem gives UNSUPPORTED or INVALID_ARG. */
+GEMM_F32_API gemm_f32_status gemm_f32_plan_ex(int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldc,
+                                 const gemm_f32_opts* opts, gemm_f32_plan_t* plan);
+
+/*
+ * Enqueue C = A*B on `stream`.  A, B, C are device pointers with the plan's
+ * shapes and leading dimensions.  Asynchronous: returns after the launches are
+ * queued; nothing is synchronised.  INVALID_ARG for a NULL plan or a NULL
+ * pointer with non-empty work; CUDA if a launch fails.  A device-side timeout
+ * is reported later by gemm_f32_check.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_run(gemm_f32_plan_t plan, const float* A, const float* B,
+                             float* C, gemm_f32_stream_t stream);
+
+/*
+ * C = A*B with HOST operands: copies A and B to device buffers the plan owns
+ * (allocated on first use), runs, copies C back to host memory and
+ * synchronises `stream`.  For pinned host memory the copies are asynchronous
+ * DMA; pageable memory works but is slower.  Returns the run's status, or
+ * TIMEOUT if a device-side wait ran out.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t plan, const float* A_host,
+                                  const float* B_host, float* C_host,
+                                  gemm_f32_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device status word.
+ * TIMEOUT if a kernel of an earlier run gave up a bounded wait (that run's C
+ * is not valid); CUDA if the stream reports an error; OK otherwise.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_check(gemm_f32_plan_t plan, gemm_f32_stream_t stream);
+
+/* Release the plan and its scratch memory.  NULL is a no-op.  The caller must
+ * make sure no run of this plan is still executing. */
+GEMM_F32_API void gemm_f32_plan_destroy(gemm_f32_plan_t plan);
+
+/* Write a one-line, NUL-terminated description of the chosen configuration
+ * (variant, tile, stages, split-K, scratch bytes) into buf[0..n-1].
+ * INVALID_ARG for a NULL plan or buffer or n == 0. */
+GEMM_F32_API gemm_f32_status gemm_f32_plan_describe(gemm_f32_plan_t plan, char* buf, size_t n);
+
+/* Bytes of device scratch the plan holds (0 for none). */
+GEMM_F32_API size_t gemm_f32_plan_workspace_bytes(gemm_f32_plan_t plan);
+
+/* Number of kernels one gemm_f32_run of this plan launches (0 for an empty
+ * problem), or -1 for a NULL plan. */
+GEMM_F32_API int gemm_f32_plan_kernel_launches(gemm_f32_plan_t plan);
+
+/*
+ * Kernel-level timing with CUDA events (tracing).  After
+ * gemm_f32_trace_enable(plan, capacity) each of the next `capacity` runs
+ * records four events on its stream, at the boundaries of its three phases:
+ * operand split (tensor-core path only), main GEMM kernel, split-K reduction.
+ * gemm_f32_trace_read waits for the recorded events, writes the phase
+ * durations in milliseconds to ms[3*i + 0..2] for run i (0 for a phase the
+ * run does not have), sets *n_runs, and empties the record.  capacity 0
+ * disables tracing.  The plan creates the events (cudaEventCreate) when
+ * tracing is enabled.  INVALID_ARG for a NULL plan, a negative capacity or
+ * NULL outputs; CUDA if an event call fails.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_trace_enable(gemm_f32_plan_t plan, int capacity);
+GEMM_F32_API gemm_f32_status gemm_f32_trace_read(gemm_f32_plan_t plan, float* ms, int max_runs,
+                                                 int* n_runs);
+
+/* Static, NUL-terminated name of a status code. */
+GEMM_F32_API const char* gemm_f32_status_string(gemm_f32_status s);
+
+/* Library version: major*10000 + minor*100 + patch. */
+GEMM_F32_API int gemm_f32_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F32_H_ */

@@ -1,0 +1,512 @@
+// C-ABI of the library: plans, the per-shape dispatcher, runs, status codes.
+//
+// The dispatcher follows the pages' standing lesson that no single kernel is
+// fastest ("Double Buffering" technique page, last paragraph; "Case Study: The
+// Double-Buffered GEMM", first paragraph): it picks the kernel, its tile, the
+// stage count and split-K per problem shape, from a table of timings measured on
+// GB300 (dispatch_table.inc) with a rule for shapes the table does not cover.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+using namespace gemm_f32;
+
+namespace {
+
+enum PlanKind : int { kNoop = 0, kZeroFill = 1, kSimt = 2, kTc = 3 };
+
+// Smallest K the tensor-core path accepts (accuracy of the 3xTF32 split).
+constexpr int64_t kTcMinK = 16;
+
+struct DispatchChoice {
+    int variant;   // GEMM_F32_VARIANT_SIMT / _TCGEN05
+    int tile_m, tile_n, stages, split_k;
+};
+
+#include "dispatch_table.inc"
+
+}  // namespace
+
+struct gemm_f32_plan_s {
+    int64_t M = 0, N = 0, K = 0, lda = 0, ldb = 0, ldc = 0;
+    gemm_f32_opts opts{};
+    int device = -1;
+    int kind = kNoop;
+    int num_sms = 0;
+    // SIMT path
+    int simt_id = -1;
+    int split_k = 1;
+    int64_t k_chunk = 0;
+    float* partial = nullptr;
+    int64_t ldp = 0;
+    // tensor-core path
+    TcPlanState tc;
+    // scratch: one device allocation carved into the buffers above
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    int* d_status = nullptr;
+    // device staging for gemm_f32_run_host (allocated on first use)
+    float* hA = nullptr;
+    float* hB = nullptr;
+    float* hC = nullptr;
+    char desc[256] = {0};
+    // tracing: 4 events per recorded run
+    std::vector<cudaEvent_t> trace_ev;
+    int trace_cap = 0;
+    int trace_n = 0;
+};
+
+namespace {
+
+gemm_f32_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return GEMM_F32_OK;
+    if (e == cudaErrorMemoryAllocation) return GEMM_F32_ERR_OOM;
+    return GEMM_F32_ERR_CUDA;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+gemm_f32_status validate_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0) return GEMM_F32_ERR_INVALID_ARG;
+    if (lda < 1 || ldb < 1 || ldc < 1) return GEMM_F32_ERR_INVALID_ARG;
+    if (M > 0 && K > 0 && lda < K) return GEMM_F32_ERR_INVALID_ARG;
+    if (K > 0 && N > 0 && ldb < N) return GEMM_F32_ERR_INVALID_ARG;
+    if (M > 0 && N > 0 && ldc < N) return GEMM_F32_ERR_INVALID_ARG;
+    // Keep every index comfortably inside int64 and the grid limits.
+    const int64_t lim = int64_t(1) << 31;
+    if (M >= lim || N >= lim || K >= lim || lda >= lim || ldb >= lim || ldc >= lim)
+        return GEMM_F32_ERR_INVALID_ARG;
+    return GEMM_F32_OK;
+}
+
+gemm_f32_status validate_opts(const gemm_f32_opts& o)
+{
+    if (o.variant < 0 || o.variant > GEMM_F32_VARIANT_TCGEN05) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.tile_m < 0 || o.tile_n < 0 || o.stages < 0 || o.split_k < 0 || o.split_k > 64)
+        return GEMM_F32_ERR_INVALID_ARG;
+    if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
+    return GEMM_F32_OK;
+}
+
+// Pick a split-K factor so that tiles*split roughly fills the SMs once, with at
+// least `min_k_per_split` of K per split.
+int auto_split(int64_t tiles, int64_t K, int64_t min_k_per_split, int sms)
+{
+    if (tiles >= sms / 2) return 1;
+    int64_t s = sms / (tiles > 0 ? tiles : 1);
+    const int64_t kmax = K / min_k_per_split;
+    if (s > kmax) s = kmax;
+    if (s > 16) s = 16;
+    return s < 1 ? 1 : (int)s;
+}
+
+DispatchChoice choose(int64_t M, int64_t N, int64_t K, int sms)
+{
+    DispatchChoice c{};
+    if (table_lookup(M, N, K, c)) return c;
+    // Shapes outside the measured table: tensor cores once the product is big
+    // enough to amortise the operand split; SIMT below that.
+    const double macs = double(M) * double(N) * double(K);
+    if (macs >= 6.0e7 && K >= 32) {  // K >= kTcMinK with margin
+        c.variant = GEMM_F32_VARIANT_TCGEN05;
+        c.tile_m = 128;
+        c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
+        c.stages = 0;  // the depth compiled for that tile width
+        const int64_t tiles = ((M + 127) / 128) * ((N + c.tile_n - 1) / c.tile_n);
+        c.split_k = auto_split(tiles, K, 256, sms);
+        return c;
+    }
+    c.variant = GEMM_F32_VARIANT_SIMT;
+    c.stages = 2;
+    const int64_t t128 = ((M + 127) / 128) * ((N + 127) / 128);
+    const int64_t t64 = ((M + 63) / 64) * ((N + 63) / 64);
+    if (t128 >= sms) { c.tile_m = c.tile_n = 128; }
+    else if (t64 >= sms / 4 || M * N > 64 * 64 * 4) { c.tile_m = c.tile_n = 64; }
+    else { c.tile_m = c.tile_n = 32; }
+    const int64_t tiles = ((M + c.tile_m - 1) / c.tile_m) * ((N + c.tile_n - 1) / c.tile_n);
+    c.split_k = auto_split(tiles, K, 64, sms);
+    return c;
+}
+
+gemm_f32_status device_check(int* dev, int* sms)
+{
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
+        cudaGetLastError();
+        return GEMM_F32_ERR_UNSUPPORTED;
+    }
+    if (cudaGetDevice(dev) != cudaSuccess) return GEMM_F32_ERR_CUDA;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev);
+    if (major != 10 || minor != 3) return GEMM_F32_ERR_UNSUPPORTED;
+    cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev);
+    return GEMM_F32_OK;
+}
+
+gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                          int64_t ldc, const gemm_f32_opts* opts_in, gemm_f32_plan_t* out)
+{
+    if (!out) return GEMM_F32_ERR_INVALID_ARG;
+    *out = nullptr;
+    gemm_f32_status st = validate_dims(M, N, K, lda, ldb, ldc);
+    if (st != GEMM_F32_OK) return st;
+    gemm_f32_opts o{};
+    if (opts_in) o = *opts_in;
+    if ((st = validate_opts(o)) != GEMM_F32_OK) return st;
+
+    gemm_f32_plan_s* p = new (std::nothrow) gemm_f32_plan_s();
+    if (!p) return GEMM_F32_ERR_OOM;
+    p->M = M; p->N = N; p->K = K; p->lda = lda; p->ldb = ldb; p->ldc = ldc;
+    p->opts = o;
+
+    if (M == 0 || N == 0) {
+        p->kind = kNoop;
+        snprintf(p->desc, sizeof p->desc, "noop M=%lld N=%lld K=%lld", (long long)M,
+                 (long long)N, (long long)K);
+        *out = p;
+        return GEMM_F32_OK;
+    }
+    if ((st = device_check(&p->device, &p->num_sms)) != GEMM_F32_OK) {
+        delete p;
+        return st;
+    }
+
+    size_t status_off = 0, part_off = 0, ahi_off = 0, alo_off = 0, bhi_off = 0, blo_off = 0;
+    size_t bytes = align256(sizeof(int));
+    status_off = 0;
+
+    if (K == 0) {
+        p->kind = kZeroFill;
+        snprintf(p->desc, sizeof p->desc, "zero-fill M=%lld N=%lld K=0", (long long)M, (long long)N);
+    } else {
+        DispatchChoice c = choose(M, N, K, p->num_sms);
+        if (o.variant != GEMM_F32_VARIANT_AUTO && o.variant != c.variant) {
+            // A forced variant starts from that variant's own rule.
+            c.variant = o.variant;
+            if (c.variant == GEMM_F32_VARIANT_SIMT) {
+                c.tile_m = c.tile_n = 64; c.stages = 2; c.split_k = 1;
+            } else {
+                c.tile_m = 128; c.tile_n = 128; c.stages = 0;
+                const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+                c.split_k = auto_split(tiles, K, 256, p->num_sms);
+            }
+        }
+        if (o.tile_m) c.tile_m = o.tile_m;
+        if (o.tile_n) c.tile_n = o.tile_n;
+        if (o.stages) c.stages = o.stages;
+        if (o.split_k) c.split_k = o.split_k;
+
+        if (c.variant == GEMM_F32_VARIANT_SIMT) {
+            p->kind = kSimt;
+            p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages);
+            if (p->simt_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            const int bk = simt_config(p->simt_id).bk;
+            int64_t split = c.split_k < 1 ? 1 : c.split_k;
+            int64_t chunk = round_up((K + split - 1) / split, bk);
+            split = (K + chunk - 1) / chunk;  // no empty splits
+            p->split_k = (int)split;
+            p->k_chunk = chunk;
+            if (split > 1) {
+                p->ldp = round_up(N, 4);
+                part_off = bytes;
+                bytes += align256(size_t(split) * size_t(M) * size_t(p->ldp) * sizeof(float));
+            }
+            const SimtConfig& sc = simt_config(p->simt_id);
+            snprintf(p->desc, sizeof p->desc,
+                     "simt tile=%dx%dx%d thread=%dx%d stages=%d split_k=%d", sc.bm, sc.bn, sc.bk,
+                     sc.tm, sc.tn, sc.stages, p->split_k);
+        } else {
+            // The two-piece TF32 split keeps 22 of FP32's 24 significand bits, so
+            // each product carries an error up to about 3*2^-22*|a||b|; against the
+            // bound 2*K*2^-24*sum|a||b| that fits only once K is about 10 or more.
+            if (K < kTcMinK) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            p->kind = kTc;
+            TcPlanState& t = p->tc;
+            t.config_id = tc_find_config(c.tile_n, c.stages);
+            if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            const TcConfig& tcfg = tc_config(t.config_id);
+            t.terms = o.tf32_terms ? o.tf32_terms : 3;
+            t.kp = round_up(K, 32);
+            int64_t kblocks = t.kp / tcfg.bk;
+            int64_t split = c.split_k < 1 ? 1 : c.split_k;
+            if (split > kblocks) split = kblocks;
+            int64_t kb_per = (kblocks + split - 1) / split;
+            split = (kblocks + kb_per - 1) / kb_per;
+            t.split_k = (int)split;
+            t.kb_per_split = (int)kb_per;
+            t.num_sms = p->num_sms;
+            t.timeout_cycles = o.wait_timeout_cycles;
+            t.withhold_stage = o.debug_withhold_stage;
+            ahi_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
+            alo_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
+            bhi_off = bytes; bytes += align256(size_t(N) * size_t(t.kp) * sizeof(float));
+            blo_off = bytes; bytes += align256(size_t(N) * size_t(t.kp) * sizeof(float));
+            if (t.split_k > 1) {
+                t.ldp = round_up(N, 4);
+                part_off = bytes;
+                bytes += align256(size_t(t.split_k) * size_t(M) * size_t(t.ldp) * sizeof(float));
+            }
+            snprintf(p->desc, sizeof p->desc,
+                     "tcgen05 3xtf32 terms=%d tile=%dx%dx%d stages=%d split_k=%d kp=%lld",
+                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.split_k, (long long)t.kp);
+        }
+    }
+
+    cudaError_t e = cudaMalloc(&p->ws, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return from_cuda(e);
+    }
+    p->ws_bytes = bytes;
+    char* base = static_cast<char*>(p->ws);
+    p->d_status = reinterpret_cast<int*>(base + status_off);
+    e = cudaMemset(p->d_status, 0, sizeof(int));
+    if (p->kind == kSimt && p->split_k > 1) p->partial = reinterpret_cast<float*>(base + part_off);
+    if (p->kind == kTc) {
+        TcPlanState& t = p->tc;
+        t.a_hi = reinterpret_cast<float*>(base + ahi_off);
+        t.a_lo = reinterpret_cast<float*>(base + alo_off);
+        t.b_hi = reinterpret_cast<float*>(base + bhi_off);
+        t.b_lo = reinterpret_cast<float*>(base + blo_off);
+        if (t.split_k > 1) t.partial = reinterpret_cast<float*>(base + part_off);
+        if (e == cudaSuccess) e = tc_prepare(t, M, N, K);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->ws);
+        delete p;
+        return from_cuda(e);
+    }
+    size_t len = strlen(p->desc);
+    snprintf(p->desc + len, sizeof p->desc - len, " ws=%zu", p->ws_bytes);
+    *out = p;
+    return GEMM_F32_OK;
+}
+
+bool current_device_is(int dev)
+{
+    int d = -1;
+    return cudaGetDevice(&d) == cudaSuccess && d == dev;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_f32_status gemm_f32_opts_init(gemm_f32_opts* opts)
+{
+    if (!opts) return GEMM_F32_ERR_INVALID_ARG;
+    memset(opts, 0, sizeof *opts);
+    return GEMM_F32_OK;
+}
+
+gemm_f32_status gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              int64_t ldc, gemm_f32_plan_t* plan)
+{
+    return make_plan(M, N, K, lda, ldb, ldc, nullptr, plan);
+}
+
+gemm_f32_status gemm_f32_plan_ex(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t ldc, const gemm_f32_opts* opts, gemm_f32_plan_t* plan)
+{
+    return make_plan(M, N, K, lda, ldb, ldc, opts, plan);
+}
+
+gemm_f32_status gemm_f32_run(gemm_f32_plan_t p, const float* A, const float* B, float* C,
+                             gemm_f32_stream_t stream)
+{
+    if (!p) return GEMM_F32_ERR_INVALID_ARG;
+    if (p->kind == kNoop) return GEMM_F32_OK;
+    if (!C || (p->K > 0 && (!A || !B))) return GEMM_F32_ERR_INVALID_ARG;
+    if (!current_device_is(p->device)) return GEMM_F32_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    cudaEvent_t* ev = nullptr;
+    if (p->trace_n < p->trace_cap) ev = &p->trace_ev[4 * size_t(p->trace_n++)];
+    switch (p->kind) {
+    case kZeroFill:
+        if (ev) { cudaEventRecord(ev[0], s); cudaEventRecord(ev[1], s); }
+        e = zero_fill_launch(C, p->M, p->N, p->ldc, s);
+        if (ev) { cudaEventRecord(ev[2], s); cudaEventRecord(ev[3], s); }
+        break;
+    case kSimt: {
+        SimtArgs a{};
+        a.M = p->M; a.N = p->N; a.K = p->K;
+        a.A = A; a.lda = p->lda; a.B = B; a.ldb = p->ldb; a.C = C; a.ldc = p->ldc;
+        a.split_k = p->split_k; a.k_chunk = p->k_chunk; a.partial = p->partial; a.ldp = p->ldp;
+        if (ev) { cudaEventRecord(ev[0], s); cudaEventRecord(ev[1], s); }
+        e = simt_launch(p->simt_id, a, s);
+        if (ev) cudaEventRecord(ev[2], s);
+        if (e == cudaSuccess && p->split_k > 1)
+            e = splitk_reduce_launch(p->partial, p->split_k, p->M, p->N, p->ldp, C, p->ldc, s);
+        if (ev) cudaEventRecord(ev[3], s);
+        break;
+    }
+    case kTc:
+        e = tc_launch(p->tc, p->M, p->N, p->K, A, p->lda, B, p->ldb, C, p->ldc, p->d_status, s, ev);
+        break;
+    default:
+        return GEMM_F32_ERR_INVALID_ARG;
+    }
+    return from_cuda(e);
+}
+
+gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t p, const float* A_host, const float* B_host,
+                                  float* C_host, gemm_f32_stream_t stream)
+{
+    if (!p) return GEMM_F32_ERR_INVALID_ARG;
+    if (p->kind == kNoop) return GEMM_F32_OK;
+    if (!C_host || (p->K > 0 && (!A_host || !B_host))) return GEMM_F32_ERR_INVALID_ARG;
+    if (!current_device_is(p->device)) return GEMM_F32_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t a_bytes = p->K > 0 ? size_t(p->M) * size_t(p->lda) * sizeof(float) : 0;
+    const size_t b_bytes = p->K > 0 ? size_t(p->K) * size_t(p->ldb) * sizeof(float) : 0;
+    const size_t c_bytes = size_t(p->M) * size_t(p->ldc) * sizeof(float);
+    cudaError_t e = cudaSuccess;
+    if (!p->hC) {
+        if (a_bytes && (e = cudaMalloc(&p->hA, a_bytes)) != cudaSuccess) goto fail;
+        if (b_bytes && (e = cudaMalloc(&p->hB, b_bytes)) != cudaSuccess) goto fail;
+        if ((e = cudaMalloc(&p->hC, c_bytes)) != cudaSuccess) goto fail;
+    }
+    if (p->K > 0) {
+        e = cudaMemcpy2DAsync(p->hA, p->lda * sizeof(float), A_host, p->lda * sizeof(float),
+                              p->K * sizeof(float), p->M, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = cudaMemcpy2DAsync(p->hB, p->ldb * sizeof(float), B_host, p->ldb * sizeof(float),
+                              p->N * sizeof(float), p->K, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    {
+        gemm_f32_status st = gemm_f32_run(p, p->hA, p->hB, p->hC, stream);
+        if (st != GEMM_F32_OK) return st;
+    }
+    e = cudaMemcpy2DAsync(C_host, p->ldc * sizeof(float), p->hC, p->ldc * sizeof(float),
+                          p->N * sizeof(float), p->M, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return gemm_f32_check(p, stream);
+fail:
+    cudaGetLastError();
+    cudaFree(p->hA); cudaFree(p->hB); cudaFree(p->hC);
+    p->hA = p->hB = p->hC = nullptr;
+    return from_cuda(e);
+}
+
+gemm_f32_status gemm_f32_check(gemm_f32_plan_t p, gemm_f32_stream_t stream)
+{
+    if (!p) return GEMM_F32_ERR_INVALID_ARG;
+    if (p->kind == kNoop) return GEMM_F32_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return from_cuda(e);
+    int h = 0;
+    e = cudaMemcpy(&h, p->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (h != kStatusOk) {
+        e = cudaMemset(p->d_status, 0, sizeof(int));
+        if (e != cudaSuccess) return from_cuda(e);
+        return GEMM_F32_ERR_TIMEOUT;
+    }
+    return GEMM_F32_OK;
+}
+
+void gemm_f32_plan_destroy(gemm_f32_plan_t p)
+{
+    if (!p) return;
+    for (cudaEvent_t e : p->trace_ev) cudaEventDestroy(e);
+    if (p->ws) cudaFree(p->ws);
+    if (p->hA) cudaFree(p->hA);
+    if (p->hB) cudaFree(p->hB);
+    if (p->hC) cudaFree(p->hC);
+    delete p;
+}
+
+gemm_f32_status gemm_f32_plan_describe(gemm_f32_plan_t p, char* buf, size_t n)
+{
+    if (!p || !buf || n == 0) return GEMM_F32_ERR_INVALID_ARG;
+    snprintf(buf, n, "%s", p->desc);
+    return GEMM_F32_OK;
+}
+
+size_t gemm_f32_plan_workspace_bytes(gemm_f32_plan_t p) { return p ? p->ws_bytes : 0; }
+
+int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
+{
+    if (!p) return -1;
+    switch (p->kind) {
+    case kZeroFill: return 1;
+    case kSimt: return p->split_k > 1 ? 2 : 1;
+    case kTc: return 3 + (p->tc.split_k > 1 ? 1 : 0);
+    default: return 0;
+    }
+}
+
+gemm_f32_status gemm_f32_trace_enable(gemm_f32_plan_t p, int capacity)
+{
+    if (!p || capacity < 0) return GEMM_F32_ERR_INVALID_ARG;
+    for (cudaEvent_t e : p->trace_ev) cudaEventDestroy(e);
+    p->trace_ev.clear();
+    p->trace_cap = p->trace_n = 0;
+    if (capacity == 0 || p->kind == kNoop) return GEMM_F32_OK;
+    try {
+        p->trace_ev.resize(4 * size_t(capacity), nullptr);
+    } catch (...) {
+        return GEMM_F32_ERR_OOM;
+    }
+    for (cudaEvent_t& e : p->trace_ev) {
+        cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) {
+            cudaGetLastError();
+            for (cudaEvent_t x : p->trace_ev)
+                if (x) cudaEventDestroy(x);
+            p->trace_ev.clear();
+            return from_cuda(r);
+        }
+    }
+    p->trace_cap = capacity;
+    return GEMM_F32_OK;
+}
+
+gemm_f32_status gemm_f32_trace_read(gemm_f32_plan_t p, float* ms, int max_runs, int* n_runs)
+{
+    if (!p || !n_runs || max_runs < 0 || (max_runs > 0 && !ms)) return GEMM_F32_ERR_INVALID_ARG;
+    const int n = p->trace_n < max_runs ? p->trace_n : max_runs;
+    for (int i = 0; i < n; ++i) {
+        cudaEvent_t* ev = &p->trace_ev[4 * size_t(i)];
+        cudaError_t r = cudaEventSynchronize(ev[3]);
+        for (int j = 0; j < 3 && r == cudaSuccess; ++j) r = cudaEventElapsedTime(&ms[3 * i + j], ev[j], ev[j + 1]);
+        if (r != cudaSuccess) return from_cuda(r);
+    }
+    *n_runs = n;
+    p->trace_n = 0;
+    return GEMM_F32_OK;
+}
+
+const char* gemm_f32_status_string(gemm_f32_status s)
+{
+    switch (s) {
+    case GEMM_F32_OK: return "GEMM_F32_OK";
+    case GEMM_F32_ERR_INVALID_ARG: return "GEMM_F32_ERR_INVALID_ARG";
+    case GEMM_F32_ERR_UNSUPPORTED: return "GEMM_F32_ERR_UNSUPPORTED";
+    case GEMM_F32_ERR_CUDA: return "GEMM_F32_ERR_CUDA";
+    case GEMM_F32_ERR_TIMEOUT: return "GEMM_F32_ERR_TIMEOUT";
+    case GEMM_F32_ERR_OOM: return "GEMM_F32_ERR_OOM";
+    }
+    return "GEMM_F32_ERR_UNKNOWN";
+}
+
+int gemm_f32_version(void) { return 100; }
+
+}  // extern "C"

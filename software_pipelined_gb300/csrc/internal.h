@@ -1,0 +1,84 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gemm_f32.h"
+
+namespace gemm_f32 {
+
+// ---- SIMT FFMA kernel (simt_gemm.cu) --------------------------------------
+struct SimtConfig {
+    int bm, bn, bk;   // CTA tile
+    int tm, tn;       // per-thread register tile
+    int stages;       // cp.async ring depth (1 = single buffer, 2 = double, ...)
+};
+// Configurations compiled into the library; `id` indexes this table.
+int simt_num_configs();
+const SimtConfig& simt_config(int id);
+int simt_find_config(int bm, int bn, int stages);  // -1 if none
+
+struct SimtArgs {
+    int64_t M, N, K;
+    const float* A; int64_t lda;
+    const float* B; int64_t ldb;
+    float* C; int64_t ldc;
+    int split_k;          // >1: write partials to `partial`
+    int64_t k_chunk;      // K per split (multiple of bk)
+    float* partial;       // split_k x M x ldp
+    int64_t ldp;
+};
+cudaError_t simt_launch(int config_id, const SimtArgs& a, cudaStream_t s);
+
+// Deterministic split-K reduction: C[i][j] = sum_{z=0}^{splits-1} P[z][i][j]
+// in ascending z (splitk_reduce.cu).
+cudaError_t splitk_reduce_launch(const float* P, int splits, int64_t M, int64_t N, int64_t ldp,
+                                 float* C, int64_t ldc, cudaStream_t s);
+// C = 0 (the K == 0 case).
+cudaError_t zero_fill_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t s);
+
+// ---- tcgen05 3xTF32 kernel (tc_gemm.cu) -----------------------------------
+struct TcConfig {
+    int bm, bn, bk;  // CTA tile (bm = 128 rows = TMEM lanes; bk = 32 fp32 = 128 B)
+    int stages;      // smem ring depth
+};
+int tc_num_configs();
+const TcConfig& tc_config(int id);
+int tc_find_config(int bn, int stages);
+
+// Plan-time state of the tensor-core path: split-operand scratch and the
+// tensor maps that describe it.
+struct TcPlanState {
+    int config_id = -1;
+    int split_k = 1;
+    int kb_per_split = 0;  // k-blocks of 32 per split
+    int terms = 3;
+    int64_t kp = 0;            // padded K (row length of split operands), multiple of 32
+    float* a_hi = nullptr;     // M x kp
+    float* a_lo = nullptr;
+    float* b_hi = nullptr;     // N x kp (B transposed: K-major)
+    float* b_lo = nullptr;
+    float* partial = nullptr;  // split_k x M x ldp (split_k > 1)
+    int64_t ldp = 0;
+    alignas(64) unsigned char tmap_a_hi[128];
+    alignas(64) unsigned char tmap_a_lo[128];
+    alignas(64) unsigned char tmap_b_hi[128];
+    alignas(64) unsigned char tmap_b_lo[128];
+    int num_sms = 0;
+    int64_t timeout_cycles = 0;
+    int withhold_stage = 0;
+};
+// Allocates nothing: encodes tensor maps over already-allocated split buffers.
+cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K);
+// ev: NULL, or four events recorded before the split, before the main kernel,
+// after the main kernel and after the split-K reduction.
+cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K,
+                      const float* A, int64_t lda, const float* B, int64_t ldb,
+                      float* C, int64_t ldc, int* status, cudaStream_t s,
+                      cudaEvent_t* ev = nullptr);
+
+// Device status word values written by kernels.
+enum : int { kStatusOk = 0, kStatusTimeout = 1 };
+
+}  // namespace gemm_f32
