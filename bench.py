@@ -336,22 +336,29 @@ def run_gpu_arm(args):
         per_kernel[w["name"]] = {"plan": w["plan"].describe(), "split_ms": round(sp, 4),
                                  "main_ms": round(mn, 4), "reduce_ms": round(rd, 4),
                                  "main_tflops": round(2.0 * w["M"] * w["N"] * w["K"] / (mn * 1e-3) / 1e12, 2)}
-    achieved = main_fl / (main_ms * 1e-3) / 1e12
-    peak = pk["f32_3xtf32_tflops_sustained"]
+    # The dominant kernel: the tcgen05 main GEMM of the largest shape (the
+    # biggest share of the step).  Its peak is the 3xTF32-effective tensor peak
+    # from the burst BF16 measurement: the kernel runs at full SM clock with no
+    # power-cap reason (see clocks), which is the burst regime.
+    big = max(work, key=lambda w: w["M"] * w["N"] * w["K"])
+    bk = per_kernel[big["name"]]
+    achieved = bk["main_tflops"]
+    peak = pk["f32_3xtf32_tflops_burst"]
     kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", "tc_gemm.cu")])
     traffic, traffic_src = traffic_for(kern_hash)
-    traffic_per_launch = None
-    if traffic:
-        tot = [traffic.get(w["name"]) for w in work]
-        if all(t is not None for t in tot):
-            traffic_per_launch = sum(tot) / len(tot)
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic_per_launch,
-                "kernel": "tc_gemm_kernel (tcgen05 3xTF32 main GEMM)",
-                "peak_basis": f"of {pk['source']}: sustained bf16 x {TF32_OVER_BF16:.4f} (nominal tf32/bf16) / 3",
-                "frac_of_burst_peak": round(achieved / pk["f32_3xtf32_tflops_burst"], 4),
+    for w in work:
+        t = traffic.get(w["name"]) if traffic else None
+        per_kernel[w["name"]]["dram_bytes_per_launch"] = t
+        per_kernel[w["name"]]["frac"] = round(per_kernel[w["name"]]["main_tflops"] / peak, 4)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": round(peak, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": per_kernel[big["name"]]["dram_bytes_per_launch"],
+                "kernel": f"tc_gemm_kernel (tcgen05 3xTF32 main GEMM), {big['name']} launches",
+                "peak_basis": f"of {pk['source']}: burst bf16 x {TF32_OVER_BF16:.4f} (nominal tf32/bf16) / 3",
+                "frac_of_sustained_peak": round(achieved / pk["f32_3xtf32_tflops_sustained"], 4),
+                "algorithmic_flops_per_launch": 2.0 * big["M"] * big["N"] * big["K"],
+                "algorithmic_bytes_per_launch": algorithmic_bytes(big["M"], big["N"], big["K"]),
                 "traffic_source": traffic_src, "kernel_source_sha256_16": kern_hash,
-                "share_of_step": round(main_ms / ms_step, 4),
+                "main_kernel_share_of_step": round(main_ms / ms_step, 4),
                 "split_pass_share_of_step": round(split_ms / ms_step, 4),
                 "per_shape": per_kernel}
     launches = args.steps * sum(w["plan"].kernel_launches for w in work)
