@@ -181,6 +181,44 @@ GEMM_F32_API gemm_f32_status gemm_f32_trace_enable(gemm_f32_plan_t plan, int cap
 GEMM_F32_API gemm_f32_status gemm_f32_trace_read(gemm_f32_plan_t plan, float* ms, int max_runs,
                                                  int* n_runs);
 
+/*
+ * C = A*B without allocating anything.  (An addition of this library; the
+ * pages have no counterpart.)
+ *
+ * For callers that cannot allocate device memory when they need the product:
+ * code running while an allocator or memory pool is being set up or torn down,
+ * code whose device memory all comes from an arena it manages itself, or a
+ * latency-critical path that must not take the allocator's locks.
+ * gemm_f32_plan allocates its scratch with cudaMalloc; this call does not.
+ *
+ * It runs the SIMT FFMA kernel with K split into `split_k` slices (2..64; the
+ * slices are rounded to whole K-tiles, so fewer may run) followed by the
+ * deterministic split-K reduction.  The partial products live in one fixed
+ * 8 MiB array inside the library image, which every GPU that loads the
+ * library holds until the process exits; the call needs
+ * split_k * M * round_up(N, 4) floats of it and returns INVALID_ARG when that
+ * exceeds 2^21 floats (8 MiB).  Nothing in the call runs cudaMalloc, cudaFree
+ * or any other allocating routine.
+ *
+ * A, B, C are device pointers with the layout of the conventions above; the
+ * call is asynchronous on `stream`.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls share the one
+ * array and each overwrites what the last one left; every partial is written
+ * in full before it is read, so nothing has to start at zero.  Calls whose
+ * executions overlap on the GPU (different streams, or several host threads)
+ * race on the array and give wrong results: serialise them.
+ *
+ * INVALID_ARG: bad sizes or leading dimensions, split_k outside 2..64, NULL
+ * pointers with non-empty work, or partials larger than the array.
+ * UNSUPPORTED: the current device is not sm_103.  CUDA: a launch failed.
+ * M == 0 or N == 0 returns OK at once; K == 0 writes zeros to C.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_run_splitk_noalloc(int64_t M, int64_t N, int64_t K,
+                                                         int64_t lda, int64_t ldb, int64_t ldc,
+                                                         const float* A, const float* B, float* C,
+                                                         int32_t split_k, gemm_f32_stream_t stream);
+
 /* Static, NUL-terminated name of a status code. */
 GEMM_F32_API const char* gemm_f32_status_string(gemm_f32_status s);
 

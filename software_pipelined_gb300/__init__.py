@@ -26,7 +26,7 @@ EXPORTED = ("gemm_f32_opts_init", "gemm_f32_plan", "gemm_f32_plan_ex", "gemm_f32
             "gemm_f32_run_host", "gemm_f32_check", "gemm_f32_plan_destroy",
             "gemm_f32_plan_describe", "gemm_f32_plan_workspace_bytes", "gemm_f32_status_string",
             "gemm_f32_version", "gemm_f32_plan_kernel_launches", "gemm_f32_trace_enable",
-            "gemm_f32_trace_read")
+            "gemm_f32_trace_read", "gemm_f32_run_splitk_noalloc")
 
 
 class GemmError(RuntimeError):
@@ -87,6 +87,9 @@ def load(path: str | None = None):
         lib.gemm_f32_trace_enable.restype = st
         lib.gemm_f32_trace_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), st, ctypes.POINTER(st)]
         lib.gemm_f32_trace_read.restype = st
+        lib.gemm_f32_run_splitk_noalloc.argtypes = [i64, i64, i64, i64, i64, i64, vp, vp, vp,
+                                                    ctypes.c_int32, vp]
+        lib.gemm_f32_run_splitk_noalloc.restype = st
         _lib = lib
         return lib
 
@@ -155,6 +158,12 @@ def gemm_f32_trace_read(plan, max_runs: int):
     n = ctypes.c_int(0)
     s = load().gemm_f32_trace_read(plan, buf, max_runs, ctypes.byref(n))
     return s, [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n.value)]
+
+
+def gemm_f32_run_splitk_noalloc(M, N, K, lda, ldb, ldc, A, B, C, split_k, stream=0) -> int:
+    """Split-K GEMM whose scratch is the library's fixed device array: no
+    allocation at all (see the header for the size limit and the sharing rule)."""
+    return load().gemm_f32_run_splitk_noalloc(M, N, K, lda, ldb, ldc, A, B, C, split_k, stream)
 
 
 def gemm_f32_status_string(s: int) -> str:

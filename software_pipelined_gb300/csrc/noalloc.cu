@@ -1,0 +1,102 @@
+// Split-K GEMM that allocates nothing: gemm_f32_run_splitk_noalloc.
+//
+// Some callers cannot allocate device memory at the point where they need a
+// GEMM: code that runs while a memory pool or allocator is being set up or
+// torn down, code under a strict no-allocation budget or arena (the caller owns
+// all device memory and hands out only the operands), or a real-time path that
+// must not take the allocator's locks or risk its latency.  gemm_f32_plan
+// cannot serve them, because a plan allocates its scratch with cudaMalloc.
+//
+// This entry point runs the SIMT FFMA kernel in split-K mode and keeps the
+// per-split partial products in one fixed array that is part of the library
+// image (a file-scope __device__ array).  Every GPU that loads the library
+// holds that array, kNoAllocScratchBytes of it, until the process exits.
+// Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace gemm_f32 {
+namespace {
+
+// 8 MiB of partial sums: split_k * M * round_up(N, 4) floats must fit.
+constexpr int64_t kNoAllocScratchFloats = int64_t(2) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+std::mutex g_setup_mutex;
+float* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+cudaError_t scratch_for_current_device(float** out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace gemm_f32
+
+using namespace gemm_f32;
+
+extern "C" gemm_f32_status gemm_f32_run_splitk_noalloc(int64_t M, int64_t N, int64_t K, int64_t lda,
+                                                       int64_t ldb, int64_t ldc, const float* A,
+                                                       const float* B, float* C, int32_t split_k,
+                                                       gemm_f32_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < 1 || ldb < 1 || ldc < 1) return GEMM_F32_ERR_INVALID_ARG;
+    if ((M > 0 && K > 0 && lda < K) || (K > 0 && N > 0 && ldb < N) || (M > 0 && N > 0 && ldc < N))
+        return GEMM_F32_ERR_INVALID_ARG;
+    if (split_k < 2 || split_k > 64) return GEMM_F32_ERR_INVALID_ARG;
+    const int64_t lim = int64_t(1) << 31;
+    if (M >= lim || N >= lim || K >= lim) return GEMM_F32_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_F32_OK;
+    if (!C || (K > 0 && (!A || !B))) return GEMM_F32_ERR_INVALID_ARG;
+
+    int dev = -1, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_F32_ERR_UNSUPPORTED;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return GEMM_F32_ERR_UNSUPPORTED;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_fill_launch(C, M, N, ldc, s) == cudaSuccess ? GEMM_F32_OK : GEMM_F32_ERR_CUDA;
+
+    const int cfg = simt_find_config(64, 64, 2);
+    if (cfg < 0) return GEMM_F32_ERR_UNSUPPORTED;
+    const int64_t bk = simt_config(cfg).bk;
+    int64_t chunk = ((K + split_k - 1) / split_k + bk - 1) / bk * bk;
+    const int64_t splits = (K + chunk - 1) / chunk;  // no empty K-slice
+    const int64_t ldp = (N + 3) / 4 * 4;
+    if (splits * M * ldp > kNoAllocScratchFloats) return GEMM_F32_ERR_INVALID_ARG;
+
+    float* scratch = nullptr;
+    if (scratch_for_current_device(&scratch) != cudaSuccess) return GEMM_F32_ERR_CUDA;
+
+    SimtArgs a{};
+    a.M = M; a.N = N; a.K = K;
+    a.A = A; a.lda = lda; a.B = B; a.ldb = ldb; a.C = C; a.ldc = ldc;
+    a.split_k = (int)splits;
+    a.k_chunk = chunk;
+    a.partial = scratch;  // every partial is written in full before it is read
+    a.ldp = ldp;
+    cudaError_t e = simt_launch(cfg, a, s);
+    if (e == cudaSuccess && splits > 1) e = splitk_reduce_launch(scratch, (int)splits, M, N, ldp, C, ldc, s);
+    return e == cudaSuccess ? GEMM_F32_OK : GEMM_F32_ERR_CUDA;
+}
