@@ -422,6 +422,13 @@ def run_gpu_arm(args):
                     plan = g.Plan(M, N, K)
                 run = (lambda p=plan, a=dA, b=dB, c=dC: p.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), sptr))
                 med, lo, hi, reps = time_batches(run, stream)
+                # phase breakdown of a few more runs (library-recorded events)
+                plan.trace_enable(8)
+                for _ in range(8):
+                    run()
+                phases = plan.trace_read(8)
+                plan.trace_enable(0)
+                ph = [round(sum(r[i] for r in phases) / len(phases) * 1e3, 3) for i in range(3)]
                 fl = 2.0 * M * N * K
                 byts = algorithmic_bytes(M, N, K)
                 P = pk["f32_3xtf32_tflops_burst"]
@@ -431,6 +438,7 @@ def run_gpu_arm(args):
                 per_shape.append({
                     "config": key, "shape": name, "plan": plan.describe(),
                     "us": round(med * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                    "phases_us_split_main_reduce": ph,
                     "tflops": round(fl / (med * 1e-3) / 1e12, 3),
                     "roofline_frac": round(t_roof / (med * 1e-3), 4),
                     "roofline_frac_vs_simt_peak": round(t_roof_simt / (med * 1e-3), 4),

@@ -124,7 +124,7 @@ DispatchChoice choose(int64_t M, int64_t N, int64_t K, int sms)
         c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
         c.stages = 0;  // the depth compiled for that tile width
         const int64_t tiles = ((M + 127) / 128) * ((N + c.tile_n - 1) / c.tile_n);
-        c.split_k = auto_split(tiles, K, 256, sms);
+        c.split_k = tiles >= sms / 2 ? 0 : auto_split(tiles, K, 256, sms);
         return c;
     }
     c.variant = GEMM_F32_VARIANT_SIMT;
@@ -200,7 +200,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             } else {
                 c.tile_m = 128; c.tile_n = 128; c.stages = 0;
                 const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
-                c.split_k = auto_split(tiles, K, 256, p->num_sms);
+                c.split_k = tiles >= p->num_sms / 2 ? 0 : auto_split(tiles, K, 256, p->num_sms);
             }
         }
         if (o.tile_m) c.tile_m = o.tile_m;
@@ -238,29 +238,22 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             const TcConfig& tcfg = tc_config(t.config_id);
             t.terms = o.tf32_terms ? o.tf32_terms : 3;
-            t.kp = round_up(K, 32);
-            int64_t kblocks = t.kp / tcfg.bk;
-            int64_t split = c.split_k < 1 ? 1 : c.split_k;
-            if (split > kblocks) split = kblocks;
-            int64_t kb_per = (kblocks + split - 1) / split;
-            split = (kblocks + kb_per - 1) / kb_per;
-            t.split_k = (int)split;
-            t.kb_per_split = (int)kb_per;
             t.num_sms = p->num_sms;
             t.timeout_cycles = o.wait_timeout_cycles;
             t.withhold_stage = o.debug_withhold_stage;
+            tc_configure(t, M, N, K, c.split_k);
             ahi_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             alo_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             bhi_off = bytes; bytes += align256(size_t(N) * size_t(t.kp) * sizeof(float));
             blo_off = bytes; bytes += align256(size_t(N) * size_t(t.kp) * sizeof(float));
-            if (t.split_k > 1) {
-                t.ldp = round_up(N, 4);
+            if (t.partial_bytes) {
                 part_off = bytes;
-                bytes += align256(size_t(t.split_k) * size_t(M) * size_t(t.ldp) * sizeof(float));
+                bytes += align256(t.partial_bytes);
             }
             snprintf(p->desc, sizeof p->desc,
-                     "tcgen05 3xtf32 terms=%d tile=%dx%dx%d stages=%d split_k=%d kp=%lld",
-                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.split_k, (long long)t.kp);
+                     "tcgen05 3xtf32 terms=%d tile=%dx%dx%d stages=%d tiles=%d whole=%d split=%dx%d kp=%lld",
+                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m * t.tiles_n, t.dp_tiles,
+                     t.split_tiles, t.splits, (long long)t.kp);
         }
     }
 
@@ -281,7 +274,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         t.a_lo = reinterpret_cast<float*>(base + alo_off);
         t.b_hi = reinterpret_cast<float*>(base + bhi_off);
         t.b_lo = reinterpret_cast<float*>(base + blo_off);
-        if (t.split_k > 1) t.partial = reinterpret_cast<float*>(base + part_off);
+        if (t.partial_bytes) t.partial = reinterpret_cast<float*>(base + part_off);
         if (e == cudaSuccess) e = tc_prepare(t, M, N, K);
     }
     if (e != cudaSuccess) {
@@ -448,7 +441,7 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
     switch (p->kind) {
     case kZeroFill: return 1;
     case kSimt: return p->split_k > 1 ? 2 : 1;
-    case kTc: return 3 + (p->tc.split_k > 1 ? 1 : 0);
+    case kTc: return 2 + (p->tc.split_tiles > 0 ? 1 : 0);
     default: return 0;
     }
 }

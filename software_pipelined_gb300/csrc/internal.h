@@ -48,19 +48,30 @@ const TcConfig& tc_config(int id);
 int tc_find_config(int bn, int stages);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
-// tensor maps that describe it.
+// tensor maps that describe it, and the work decomposition.
+//
+// The output tiles are taken in the kernel's tile order.  The first dp_tiles
+// are computed whole and written straight to C.  The remaining split_tiles are
+// computed as `splits` K-slices each, written as dense 128 x BN partial tiles to
+// `partial`, and summed in slice order by the tile reduction.  With a global
+// split-K request every tile is a split tile; with the automatic policy only
+// the tiles of a partial last wave are split, so that they finish in a
+// fraction of a tile's time instead of leaving most SMs idle.
 struct TcPlanState {
     int config_id = -1;
-    int split_k = 1;
-    int kb_per_split = 0;  // k-blocks of 32 per split
     int terms = 3;
     int64_t kp = 0;            // padded K (row length of split operands), multiple of 32
+    int tiles_m = 0, tiles_n = 0;
+    int dp_tiles = 0;
+    int split_tiles = 0;
+    int splits = 1;            // K-slices per split tile
+    int kb_per_split = 0;      // k-blocks of 32 per slice
     float* a_hi = nullptr;     // M x kp
     float* a_lo = nullptr;
     float* b_hi = nullptr;     // N x kp (B transposed: K-major)
     float* b_lo = nullptr;
-    float* partial = nullptr;  // split_k x M x ldp (split_k > 1)
-    int64_t ldp = 0;
+    float* partial = nullptr;  // split_tiles x splits x 128 x BN
+    size_t partial_bytes = 0;
     alignas(64) unsigned char tmap_a_hi[128];
     alignas(64) unsigned char tmap_a_lo[128];
     alignas(64) unsigned char tmap_b_hi[128];
@@ -69,6 +80,10 @@ struct TcPlanState {
     int64_t timeout_cycles = 0;
     int withhold_stage = 0;
 };
+// Work decomposition for config t.config_id: split_request 0 = automatic
+// (split the tiles of a partial last wave), 1 = none, >= 2 = every tile in that
+// many K-slices.  Sets kp, tiles, dp/split tiles, splits and partial_bytes.
+void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_request);
 // Allocates nothing: encodes tensor maps over already-allocated split buffers.
 cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K);
 // ev: NULL, or four events recorded before the split, before the main kernel,

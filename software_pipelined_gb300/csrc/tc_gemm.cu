@@ -40,6 +40,7 @@
 // freed before the CTA exits.
 #include <cstdint>
 #include <cstdio>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -58,18 +59,50 @@ constexpr int64_t kDefaultTimeout = int64_t(1) << 32;  // SM clock cycles
 
 struct TcArgs {
     int64_t M, N;
-    int64_t ldc, ldp;
+    int64_t ldc;
     float* C;
-    float* partial;
+    float* partial;      // split units' dense 128 x BN partial tiles
     int* status;
     int64_t timeout;
     int tiles_m, tiles_n;
     int num_kb;          // k-blocks of 32 in the padded K
+    int dp_tiles;        // tiles computed whole, written to C
+    int split_tiles;     // tiles computed in `splits` K-slices each
+    int splits;
     int kb_per_split;
-    int split_k;
     int terms;           // 3 = 3xTF32, 1 = hi*hi only
     int withhold;        // test hook: 1-based fill index the producer skips (0 = none)
 };
+
+// One unit of work of the persistent kernel: a whole tile, or one K-slice of a
+// split tile.
+struct Unit {
+    int tile;            // index in tile order
+    int kb0, kb1;        // k-block range
+    int slot;            // -1: write C; else index of the dense partial tile
+};
+
+__device__ __forceinline__ Unit decode_unit(int w, const TcArgs& a)
+{
+    Unit u;
+    if (w < a.dp_tiles) {
+        u.tile = w;
+        u.kb0 = 0;
+        u.kb1 = a.num_kb;
+        u.slot = -1;
+    } else {
+        const int t = w - a.dp_tiles;
+        const int z = t % a.splits;
+        u.tile = a.dp_tiles + t / a.splits;
+        u.kb0 = z * a.kb_per_split;
+        u.kb1 = min(a.num_kb, u.kb0 + a.kb_per_split);
+        u.slot = t;
+    }
+    return u;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Operand split pre-pass.
@@ -91,62 +124,83 @@ __device__ __forceinline__ void split3(float x, float& hi, float& lo)
     lo = tf32_rne(x - hi);  // x - hi is exact in FP32
 }
 
-// A (M x K, lda) -> a_hi, a_lo (M x kp, K-major, zero for k >= K).
-__global__ void __launch_bounds__(256)
-split_a_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t lda, int64_t kp,
-               float4* __restrict__ hi, float4* __restrict__ lo, int vec)
-{
-    const int64_t kp4 = kp / 4;
-    const int64_t total = M * kp4;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = idx / kp4, k = (idx % kp4) * 4;
-        const float* row = A + i * lda;
-        float v[4];
-        if (vec && k + 3 < K) {
-            const float4 t = __ldg(reinterpret_cast<const float4*>(row + k));
-            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = (k + j < K) ? __ldg(row + k + j) : 0.f;
-        }
-        float h[4], l[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) split3(v[j], h[j], l[j]);
-        hi[idx] = make_float4(h[0], h[1], h[2], h[3]);
-        lo[idx] = make_float4(l[0], l[1], l[2], l[3]);
-    }
-}
+constexpr int kSplitBK = 32;    // k rows per B tile of the split pre-pass
+constexpr int kSplitBN = 128;   // n columns per B tile
 
-// B (K x N, ldb) -> b_hi, b_lo (N x kp, i.e. B transposed, K-major), through a
-// 32x32 shared-memory tile so both the read (along n) and the write (along k)
-// are coalesced.  Grid: x over the kp/32 k-blocks, y strides over n-blocks.
+// One launch splits both operands.  Blocks [0, a_blocks) stream A (M x K, lda)
+// into a_hi, a_lo (M x kp, K-major, zero for k >= K), 16 bytes at a time where
+// the rows allow.  The remaining blocks each take a 32 (k) x 128 (n) tile of B
+// (K x N, ldb), stage it in shared memory and write it transposed to b_hi,
+// b_lo (N x kp): reads are coalesced along n, writes along k.  The last thing
+// each block does is allow the dependent GEMM launch to start its prologue.
 __global__ void __launch_bounds__(256)
-split_bt_kernel(const float* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int64_t kp,
-                float* __restrict__ hi, float* __restrict__ lo)
+split_operands_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t lda, int vec_a,
+                      const float* __restrict__ B, int64_t N, int64_t ldb, int vec_b, int64_t kp,
+                      float4* __restrict__ a_hi, float4* __restrict__ a_lo,
+                      float* __restrict__ b_hi, float* __restrict__ b_lo, int a_blocks)
 {
-    __shared__ float tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-    const int64_t k0 = (int64_t)blockIdx.x * 32;
-    for (int64_t n0 = (int64_t)blockIdx.y * 32; n0 < N; n0 += (int64_t)gridDim.y * 32) {
+    if ((int)blockIdx.x < a_blocks) {
+        const int64_t kp4 = kp / 4;
+        const int64_t total = M * kp4;
+        for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+             idx += (int64_t)a_blocks * blockDim.x) {
+            const int64_t i = idx / kp4, k = (idx % kp4) * 4;
+            const float* row = A + i * lda;
+            float v[4];
+            if (vec_a && k + 3 < K) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(row + k));
+                v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+            } else {
 #pragma unroll
-        for (int r = ty; r < 32; r += 8) {
-            const int64_t k = k0 + r, n = n0 + tx;
-            tile[r][tx] = (k < K && n < N) ? __ldg(B + k * ldb + n) : 0.f;
+                for (int j = 0; j < 4; ++j) v[j] = (k + j < K) ? __ldg(row + k + j) : 0.f;
+            }
+            float h[4], l[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) split3(v[j], h[j], l[j]);
+            a_hi[idx] = make_float4(h[0], h[1], h[2], h[3]);
+            a_lo[idx] = make_float4(l[0], l[1], l[2], l[3]);
+        }
+    } else {
+        __shared__ float tile[kSplitBK][kSplitBN + 1];
+        const int64_t kblocks = kp / kSplitBK;
+        const int64_t b = (int64_t)blockIdx.x - a_blocks;
+        const int64_t k0 = (b % kblocks) * kSplitBK;
+        const int64_t n0 = (b / kblocks) * kSplitBN;
+        // read: 32 rows x 32 float4, four per thread, a warp per row
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int f = threadIdx.x + 256 * i;
+            const int r = f >> 5, c = (f & 31) * 4;
+            const int64_t k = k0 + r, n = n0 + c;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (k < K) {
+                const float* src = B + k * ldb + n;
+                if (vec_b && n + 3 < N) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = (n + j < N) ? __ldg(src + j) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tile[r][c + j] = v[j];
         }
         __syncthreads();
-#pragma unroll
-        for (int r = ty; r < 32; r += 8) {
-            const int64_t n = n0 + r, k = k0 + tx;
+        // write: warp w takes columns n = 16w .. 16w+15, lane = k
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll 4
+        for (int c = w * 16; c < w * 16 + 16; ++c) {
+            const int64_t n = n0 + c;
             if (n < N) {
                 float h, l;
-                split3(tile[tx][r], h, l);
-                hi[n * kp + k] = h;
-                lo[n * kp + k] = l;
+                split3(tile[lane][c], h, l);
+                b_hi[n * kp + k0 + lane] = h;
+                b_lo[n * kp + k0 + lane] = l;
             }
         }
-        __syncthreads();
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -277,9 +331,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above overlaps the split pre-pass; its outputs are read only
+    // after this point.
+    pdl_wait();
 
-    const int num_tiles = args.tiles_m * args.tiles_n;
-    const int num_work = num_tiles * args.split_k;
+    const int num_work = args.dp_tiles + args.split_tiles * args.splits;
     const int64_t limit = args.timeout;
 
     if (warp == 0) {
@@ -290,12 +346,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             uint32_t fills = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
-                const int z = w / num_tiles;
+                const Unit u = decode_unit(w, args);
                 int tm, tn;
-                tile_coords(w % num_tiles, args.tiles_m, args.tiles_n, tm, tn);
-                const int kb0 = z * args.kb_per_split;
-                const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, limit, abort_flag, args.status)) {
                         stop = true;
                         break;
@@ -338,9 +392,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             int iter = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x, ++iter) {
-                const int z = w / num_tiles;
-                const int kb0 = z * args.kb_per_split;
-                const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
+                const Unit u = decode_unit(w, args);
+                const int kb0 = u.kb0, kb1 = u.kb1;
                 const int buf = iter & 1;
                 const uint32_t tphase = (iter >> 1) & 1;
                 if (!wait_phase(tempty_bar(buf), tphase ^ 1u, limit, abort_flag, args.status)) break;
@@ -387,37 +440,41 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
         const int row_in_tile = quad * 32 + lane;
         int iter = 0;
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++iter) {
-            const int z = w / num_tiles;
+            const Unit u = decode_unit(w, args);
             int tm, tn;
-            tile_coords(w % num_tiles, args.tiles_m, args.tiles_n, tm, tn);
+            tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
             const int buf = iter & 1;
             const uint32_t tphase = (iter >> 1) & 1;
             if (!wait_phase(tfull_bar(buf), tphase, limit, abort_flag, args.status)) break;
             ptx::tc_fence_after();
-            float* out;
-            int64_t ld;
-            bool vec;
-            if (args.split_k > 1) {
-                out = args.partial + (int64_t)z * args.M * args.ldp;
-                ld = args.ldp;
-                vec = true;
+            // Whole tiles go to C (guarded); K-slices to a dense 128 x BN partial
+            // tile, all of it (rows past M hold the zero-filled operands' zeros).
+            float* orow;
+            int64_t col0, ncols;
+            bool vec, row_ok;
+            if (u.slot < 0) {
+                const int64_t grow = (int64_t)tm * kBM + row_in_tile;
+                row_ok = grow < args.M;
+                orow = args.C + (row_ok ? grow : 0) * args.ldc;
+                col0 = (int64_t)tn * BN;
+                ncols = args.N;
+                vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
             } else {
-                out = args.C;
-                ld = args.ldc;
-                vec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+                row_ok = true;
+                orow = args.partial + ((int64_t)u.slot * kBM + row_in_tile) * BN;
+                col0 = 0;
+                ncols = BN;
+                vec = true;
             }
-            const int64_t grow = (int64_t)tm * kBM + row_in_tile;
-            const bool row_ok = grow < args.M;
-            float* orow = out + (row_ok ? grow : 0) * ld;
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 16) {
                 uint32_t r[16];
                 ptx::tmem_ld_32x32b_x16(taddr + c, r);
                 ptx::tmem_wait_ld();
-                const int64_t gn = (int64_t)tn * BN + c;
+                const int64_t gn = col0 + c;
                 if (row_ok) {
-                    if (vec && gn + 15 < args.N) {
+                    if (vec && gn + 15 < ncols) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
                             *reinterpret_cast<float4*>(orow + gn + j) =
@@ -426,7 +483,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
                     } else {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (gn + j < args.N) orow[gn + j] = __uint_as_float(r[j]);
+                            if (gn + j < ncols) orow[gn + j] = __uint_as_float(r[j]);
                     }
                 }
             }
@@ -438,9 +495,47 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
 
     ptx::tc_fence_before();
     __syncthreads();
+    pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// Sum the K-slices of every split tile in slice order and write the tile to C
+// (guarded).  Grid-stride over split_tiles x 128 x BN/4 float4 positions.
+template <int BN>
+__global__ void __launch_bounds__(256)
+tile_reduce_kernel(const float4* __restrict__ partial, int dp_tiles, int split_tiles, int splits,
+                   int tiles_m, int tiles_n, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
+{
+    pdl_wait();
+    constexpr int Q = BN / 4;                 // float4 per partial row
+    constexpr int PER_TILE = kBM * Q;
+    const bool vec = ((ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    const int64_t total = (int64_t)split_tiles * PER_TILE;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(idx / PER_TILE);
+        const int rem = (int)(idx % PER_TILE);
+        const int r = rem / Q, c = (rem % Q) * 4;
+        int tm, tn;
+        tile_coords(dp_tiles + j, tiles_m, tiles_n, tm, tn);
+        const int64_t grow = (int64_t)tm * kBM + r, gcol = (int64_t)tn * BN + c;
+        if (grow >= M || gcol >= N) continue;
+        const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
+        float4 acc = __ldg(p);
+        for (int z = 1; z < splits; ++z) {
+            const float4 t = __ldg(p + (int64_t)z * PER_TILE);
+            acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+        }
+        float* dst = C + grow * ldc + gcol;
+        if (vec && gcol + 3 < N) {
+            *reinterpret_cast<float4*>(dst) = acc;
+        } else {
+            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int q = 0; q < 4 && gcol + q < N; ++q) dst[q] = v[q];
+        }
     }
 }
 
@@ -483,6 +578,33 @@ cudaError_t encode_kmajor(void* out, float* base, int64_t rows, int64_t kp, int 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream finishes, and waits for it (griddepcontrol)
+// before touching that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+int grid_cap(int64_t work, int sms)
+{
+    const int64_t blocks = (work + 255) / 256;
+    const int64_t cap = (int64_t)sms * 8;
+    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
 template <int BN, int STAGES>
 cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
 {
@@ -494,31 +616,35 @@ cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    const int work = a.tiles_m * a.tiles_n * a.split_k;
+    const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
-    kern<<<grid, kThreads, L::SMEM_BYTES, s>>>(
-        *reinterpret_cast<const CUtensorMap*>(st.tmap_a_hi), *reinterpret_cast<const CUtensorMap*>(st.tmap_a_lo),
-        *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi), *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::SMEM_BYTES, s,
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_a_hi),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_a_lo),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), a);
 }
 
-using MainFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
+template <int BN>
+cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
+{
+    const int64_t total = (int64_t)a.split_tiles * kBM * (BN / 4);
+    return launch_pdl(tile_reduce_kernel<BN>, dim3(grid_cap(total, st.num_sms)), dim3(256), 0, s,
+                      reinterpret_cast<const float4*>(a.partial), a.dp_tiles, a.split_tiles, a.splits,
+                      a.tiles_m, a.tiles_n, a.M, a.N, a.C, a.ldc);
+}
+
+using LaunchFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
 struct TcEntry {
     TcConfig cfg;
-    MainFn fn;
+    LaunchFn main;
+    LaunchFn reduce;
 };
 const TcEntry kTc[] = {
-    {{128, 128, 32, 3}, launch_main<128, 3>},
-    {{128, 256, 32, 2}, launch_main<256, 2>},
-    {{128, 64, 32, 4}, launch_main<64, 4>},
+    {{128, 128, 32, 3}, launch_main<128, 3>, launch_reduce<128>},
+    {{128, 256, 32, 2}, launch_main<256, 2>, launch_reduce<256>},
+    {{128, 64, 32, 4}, launch_main<64, 4>, launch_reduce<64>},
 };
-
-int grid_cap(int64_t work, int sms)
-{
-    const int64_t blocks = (work + 255) / 256;
-    const int64_t cap = (int64_t)sms * 8;
-    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-}
 
 }  // namespace
 
@@ -533,6 +659,51 @@ int tc_find_config(int bn, int stages)
         for (int i = 0; i < tc_num_configs(); ++i)
             if (kTc[i].cfg.bn == bn) return i;
     return -1;
+}
+
+void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_request)
+{
+    const TcConfig& c = kTc[t.config_id].cfg;
+    t.kp = (K + kBK - 1) / kBK * kBK;
+    const int num_kb = (int)(t.kp / kBK);
+    t.tiles_m = (int)((M + kBM - 1) / kBM);
+    t.tiles_n = (int)((N + c.bn - 1) / c.bn);
+    const int tiles = t.tiles_m * t.tiles_n;
+    const int sms = t.num_sms > 0 ? t.num_sms : 1;
+    t.dp_tiles = tiles;
+    t.split_tiles = 0;
+    t.splits = 1;
+    int want = 1;
+    if (split_request >= 2) {
+        // every tile in split_request K-slices
+        want = split_request;
+        t.dp_tiles = 0;
+        t.split_tiles = tiles;
+    } else if (split_request == 0 && tiles > sms && tiles % sms != 0) {
+        // split the tiles of the partial last wave so they fill the machine once
+        const int rem = tiles % sms;
+        want = sms / rem;
+        if (want > 8) want = 8;
+        if (want > num_kb / 4) want = num_kb / 4;
+        if (want >= 2) {
+            t.dp_tiles = tiles - rem;
+            t.split_tiles = rem;
+        }
+    }
+    if (t.split_tiles > 0) {
+        if (want > num_kb) want = num_kb;
+        int kb_per = (num_kb + want - 1) / want;
+        int splits = (num_kb + kb_per - 1) / kb_per;  // no empty slice
+        if (splits < 2) {
+            t.dp_tiles = tiles;
+            t.split_tiles = 0;
+        } else {
+            t.splits = splits;
+            t.kb_per_split = kb_per;
+        }
+    }
+    if (t.split_tiles == 0) t.kb_per_split = num_kb;
+    t.partial_bytes = t.split_tiles ? size_t(t.split_tiles) * t.splits * kBM * c.bn * sizeof(float) : 0;
 }
 
 cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K)
@@ -551,38 +722,39 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
                       const float* B, int64_t ldb, float* C, int64_t ldc, int* status, cudaStream_t s,
                       cudaEvent_t* ev)
 {
-    const TcConfig& c = kTc[st.config_id].cfg;
     if (ev) cudaEventRecord(ev[0], s);
-    // 1. Split the operands (and transpose B) into the plan's scratch.
+    // 1. Split both operands (B transposed) into the plan's scratch, one launch.
     {
-        const int vec = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
-        split_a_kernel<<<grid_cap(M * (st.kp / 4), st.num_sms), 256, 0, s>>>(
-            A, M, K, lda, st.kp, reinterpret_cast<float4*>(st.a_hi), reinterpret_cast<float4*>(st.a_lo), vec);
+        const int vec_a = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
+        const int vec_b = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
+        const int a_blocks = grid_cap(M * (st.kp / 4), st.num_sms);
+        const int64_t b_blocks = (st.kp / kSplitBK) * ((N + kSplitBN - 1) / kSplitBN);
+        split_operands_kernel<<<(unsigned)(a_blocks + b_blocks), 256, 0, s>>>(
+            A, M, K, lda, vec_a, B, N, ldb, vec_b, st.kp, reinterpret_cast<float4*>(st.a_hi),
+            reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        const int64_t nb = (N + 31) / 32;
-        dim3 g((unsigned)(st.kp / 32), (unsigned)(nb < 65535 ? nb : 65535));
-        split_bt_kernel<<<g, 256, 0, s>>>(B, K, N, ldb, st.kp, st.b_hi, st.b_lo);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // 2. The pipelined tensor-core GEMM.
+    // 2. The pipelined tensor-core GEMM (and the reduction of split tiles).
     TcArgs a{};
-    a.M = M; a.N = N; a.ldc = ldc; a.ldp = st.ldp; a.C = C; a.partial = st.partial;
+    a.M = M; a.N = N; a.ldc = ldc; a.C = C; a.partial = st.partial;
     a.status = status;
     a.timeout = st.timeout_cycles > 0 ? st.timeout_cycles : kDefaultTimeout;
-    a.tiles_m = (int)((M + kBM - 1) / kBM);
-    a.tiles_n = (int)((N + c.bn - 1) / c.bn);
+    a.tiles_m = st.tiles_m;
+    a.tiles_n = st.tiles_n;
     a.num_kb = (int)(st.kp / kBK);
-    a.split_k = st.split_k;
+    a.dp_tiles = st.dp_tiles;
+    a.split_tiles = st.split_tiles;
+    a.splits = st.splits;
     a.kb_per_split = st.kb_per_split;
     a.terms = st.terms;
     a.withhold = st.withhold_stage;
     if (ev) cudaEventRecord(ev[1], s);
-    cudaError_t e = kTc[st.config_id].fn(st, a, s);
+    cudaError_t e = kTc[st.config_id].main(st, a, s);
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);
-    // 3. Deterministic split-K sum.
-    if (st.split_k > 1) e = splitk_reduce_launch(st.partial, st.split_k, M, N, st.ldp, C, ldc, s);
+    // 3. Fixed-order sum of the split tiles' K-slices.
+    if (st.split_tiles > 0) e = kTc[st.config_id].reduce(st, a, s);
     if (ev) cudaEventRecord(ev[3], s);
     return e;
 }

@@ -1,0 +1,153 @@
+"""Measure every kernel configuration on the benchmark shapes and regenerate
+csrc/dispatch_table.inc with the fastest one per shape.
+
+The dispatcher reads that table first ("no single kernel is fastest": the
+pages' lesson that libraries pick a variant per shape), and falls back to a
+rule for shapes it does not list.  Run on the target GPU:
+
+    python -m software_pipelined_gb300.tune --json gpurun_out/tune.json \\
+        --inc software_pipelined_gb300/csrc/dispatch_table.inc
+
+Each candidate is planned with forced options, warmed up, and timed as the
+median of three batches of back-to-back runs (CUDA events on one stream).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+
+import software_pipelined_gb300 as g  # noqa: E402
+from software_pipelined_gb300 import inputs  # noqa: E402
+
+SIMT_CFGS = [(128, 128, 2), (128, 128, 3), (128, 128, 1), (64, 64, 2), (64, 64, 3), (64, 64, 1),
+             (32, 32, 2), (32, 32, 1), (128, 64, 2)]
+TC_BN = [64, 128, 256]
+SPLITS = [1, 2, 3, 4, 6, 8, 12, 16]
+
+
+def time_plan(plan, dA, dB, dC, stream, target_ms=5.0, batches=3):
+    import torch
+    run = lambda: plan.run_ptr(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream.cuda_stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        run()
+    e0.record(stream)
+    run()
+    e1.record(stream)
+    e1.synchronize()
+    reps = int(max(1, min(500, target_ms / max(e0.elapsed_time(e1), 1e-3))))
+    res = []
+    for _ in range(batches):
+        e0.record(stream)
+        for _ in range(reps):
+            run()
+        e1.record(stream)
+        e1.synchronize()
+        res.append(e0.elapsed_time(e1) / reps)
+    if plan.check() != g.OK:
+        raise RuntimeError("device status not OK")
+    return statistics.median(res)
+
+
+def candidates(M, N, K):
+    out = []
+    macs = M * N * K
+    if macs <= 2 ** 31:
+        for (bm, bn, st) in SIMT_CFGS:
+            for sp in SPLITS:
+                if sp == 1 or K // sp >= 32:
+                    out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp))
+    if K >= 16:
+        for bn in TC_BN:
+            for sp in [0] + SPLITS:
+                if sp <= 1 or (K + 31) // 32 >= sp:
+                    out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp))
+    return out
+
+
+def main():
+    import torch
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--json", default=None)
+    ap.add_argument("--inc", default=None)
+    ap.add_argument("--workloads", default="tiny_32,small_ragged,tall_skinny,square_1024,large_squares")
+    args = ap.parse_args()
+    g.load()
+    stream = torch.cuda.current_stream()
+    results = []
+    for key in args.workloads.split(","):
+        for (name, M, N, K, dist, sa, sb) in inputs.WORKLOADS[key]:
+            A, B = inputs.make_operands(M, N, K, dist, sa, sb)
+            dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+            dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            rows = []
+            for c in candidates(M, N, K):
+                try:
+                    with g.Plan(M, N, K, **c) as p:
+                        ms = time_plan(p, dA, dB, dC, stream)
+                        rows.append(dict(opts=c, us=round(ms * 1e3, 3), plan=p.describe()))
+                except g.GemmError:
+                    continue
+            rows.sort(key=lambda r: r["us"])
+            with g.Plan(M, N, K) as p:
+                auto_desc = p.describe()
+                auto_us = round(time_plan(p, dA, dB, dC, stream) * 1e3, 3)
+            results.append(dict(shape=name, M=M, N=N, K=K, best=rows[0], top=rows[:8],
+                                auto=dict(plan=auto_desc, us=auto_us), n_candidates=len(rows)))
+            print(f"{name:18s} best {rows[0]['us']:10.3f} us  {rows[0]['plan']}   (auto {auto_us} us)",
+                  flush=True)
+            del dA, dB, dC
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(results, f, indent=1)
+    if args.inc:
+        write_inc(results, args.inc)
+
+
+def write_inc(results, path):
+    lines = [
+        "// Per-shape dispatch table: the fastest configuration measured on GB300 for",
+        "// each benchmark shape (exact match on M, N, K), written by",
+        "// software_pipelined_gb300/tune.py from its timing sweep.  Shapes not listed",
+        "// fall back to the rule in choose().  Fields: variant (1 SIMT, 2 tcgen05),",
+        "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
+        "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices).",
+        "struct TableRow {",
+        "    int64_t M, N, K;",
+        "    DispatchChoice c;",
+        "};",
+        "",
+        "const TableRow kTable[] = {",
+    ]
+    for r in results:
+        o = r["best"]["opts"]
+        lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
+                     f"{o['stages']}, {o['split_k']}}}}},  // {r['best']['us']} us")
+    lines += [
+        "    {0, 0, 0, {0, 0, 0, 0, 0}},  // sentinel",
+        "};",
+        "",
+        "bool table_lookup(int64_t M, int64_t N, int64_t K, DispatchChoice& out)",
+        "{",
+        "    for (const TableRow& r : kTable) {",
+        "        if (r.M == M && r.N == N && r.K == K && r.c.variant != 0) {",
+        "            out = r.c;",
+        "            return true;",
+        "        }",
+        "    }",
+        "    return false;",
+        "}",
+        "",
+    ]
+    with open(path, "w") as f:
+        f.write("\n".join(lines))
+
+
+if __name__ == "__main__":
+    main()

@@ -209,6 +209,22 @@ def test_persistent_many_tiles_per_cta():
     assert canaries and ok, f"{desc}: {err}"
 
 
+@pytest.mark.parametrize("shape,bn", [((128 * 20, 128 * 17, 1024), 128), ((128 * 33, 256 * 9 + 40, 640), 256)],
+                         ids=["bn128", "bn256_ragged"])
+def test_tail_wave_split(shape, bn):
+    # More tiles than SMs with a partial last wave: the dispatcher's automatic
+    # policy computes those tiles in K-slices (dense partial tiles + fixed-order
+    # reduction); the result must meet the bound and be deterministic.
+    M, N, K = shape
+    A = inputs.uniform_pm1(981, M, K)
+    B = inputs.uniform_pm1(982, K, N)
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, variant=g.VARIANT_TCGEN05, tile_n=bn)
+    assert "split=0x" not in desc, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+    assert np.array_equal(outs[0], outs[1]), desc
+
+
 @pytest.mark.parametrize("w", inputs.WORKLOADS["large_squares"], ids=lambda w: w[0])
 def test_large_squares_sampled(w):
     # The launch configuration the bench times (dispatcher's choice), checked on
