@@ -94,7 +94,11 @@ typedef struct {
                                      load of that pipeline fill (1-based), so the MMA
                                      warp's bounded wait runs out and the run reports
                                      GEMM_F32_ERR_TIMEOUT through gemm_f32_check */
-    int32_t reserved[7];
+    int32_t separate_syncs; /* ablation of the pages' barrier coalescing: 1 publishes A and
+                               B through separate synchronisations (SIMT: one barrier after
+                               each operand's copy; TC: separate "full" mbarriers for A and
+                               B); 0 = one synchronisation for both (default) */
+    int32_t reserved[6];
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

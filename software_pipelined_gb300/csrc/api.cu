@@ -96,6 +96,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
         return GEMM_F32_ERR_INVALID_ARG;
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -210,7 +211,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 
         if (c.variant == GEMM_F32_VARIANT_SIMT) {
             p->kind = kSimt;
-            p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages);
+            p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages, o.separate_syncs != 0);
             if (p->simt_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             const int bk = simt_config(p->simt_id).bk;
             int64_t split = c.split_k < 1 ? 1 : c.split_k;
@@ -225,8 +226,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             }
             const SimtConfig& sc = simt_config(p->simt_id);
             snprintf(p->desc, sizeof p->desc,
-                     "simt tile=%dx%dx%d thread=%dx%d stages=%d split_k=%d", sc.bm, sc.bn, sc.bk,
-                     sc.tm, sc.tn, sc.stages, p->split_k);
+                     "simt tile=%dx%dx%d thread=%dx%d stages=%d%s split_k=%d", sc.bm, sc.bn, sc.bk,
+                     sc.tm, sc.tn, sc.stages, sc.sep ? " separate-syncs" : "", p->split_k);
         } else {
             // The two-piece TF32 split keeps 22 of FP32's 24 significand bits, so
             // each product carries an error up to about 3*2^-22*|a||b|; against the
@@ -234,7 +235,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if (K < kTcMinK) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             p->kind = kTc;
             TcPlanState& t = p->tc;
-            t.config_id = tc_find_config(c.tile_n, c.stages);
+            t.config_id = tc_find_config(c.tile_n, c.stages, o.separate_syncs != 0);
             if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             const TcConfig& tcfg = tc_config(t.config_id);
             t.terms = o.tf32_terms ? o.tf32_terms : 3;
@@ -251,8 +252,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 bytes += align256(t.partial_bytes);
             }
             snprintf(p->desc, sizeof p->desc,
-                     "tcgen05 3xtf32 terms=%d tile=%dx%dx%d stages=%d tiles=%d whole=%d split=%dx%d kp=%lld",
-                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m * t.tiles_n, t.dp_tiles,
+                     "tcgen05 3xtf32 terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d kp=%lld",
+                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, tcfg.sep ? " separate-syncs" : "",
+                     t.tiles_m * t.tiles_n, t.dp_tiles,
                      t.split_tiles, t.splits, (long long)t.kp);
         }
     }

@@ -13,11 +13,12 @@ struct SimtConfig {
     int bm, bn, bk;   // CTA tile
     int tm, tn;       // per-thread register tile
     int stages;       // cp.async ring depth (1 = single buffer, 2 = double, ...)
+    bool sep;         // A and B published by separate barriers (ablation)
 };
 // Configurations compiled into the library; `id` indexes this table.
 int simt_num_configs();
 const SimtConfig& simt_config(int id);
-int simt_find_config(int bm, int bn, int stages);  // -1 if none
+int simt_find_config(int bm, int bn, int stages, bool sep = false);  // -1 if none
 
 struct SimtArgs {
     int64_t M, N, K;
@@ -42,10 +43,11 @@ cudaError_t zero_fill_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaSt
 struct TcConfig {
     int bm, bn, bk;  // CTA tile (bm = 128 rows = TMEM lanes; bk = 32 fp32 = 128 B)
     int stages;      // smem ring depth
+    bool sep;        // separate full barriers for A and B (ablation)
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);
-int tc_find_config(int bn, int stages);
+int tc_find_config(int bn, int stages, bool sep = false);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
 // tensor maps that describe it, and the work decomposition.

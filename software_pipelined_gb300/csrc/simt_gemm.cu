@@ -10,6 +10,12 @@
 // single-buffered sibling (load, barrier, compute, barrier) kept for the
 // pipeline-depth ablation.
 //
+// SEP = true is the ablation of the barrier coalescing of "Dependence-aware
+// group synchronization on M1 Max" ("Transformation and safety boundary"): A
+// and B are copied as separate cp.async groups and each gets its own barrier
+// (copy A; barrier; copy B; barrier; compute; ...), where the default form
+// publishes both with one barrier.
+//
 // Layout: A tile As[BM][BK+4] (row-major, as in global memory, so the copy is a
 // straight 16-byte cp.async when rows are 16-byte aligned), B tile
 // Bs[BK][BN+4].  Each thread owns a TM x TN register tile built from 4x4 blocks
@@ -24,7 +30,7 @@
 namespace gemm_f32 {
 namespace {
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
 struct SimtKernel {
     static constexpr int TX = BN / TN;
     static constexpr int TY = BM / TM;
@@ -37,13 +43,14 @@ struct SimtKernel {
     static_assert(TM % 4 == 0 && TN % 4 == 0, "register tile is built from 4x4 blocks");
     static_assert(BK % 4 == 0, "BK multiple of 4");
     static_assert(NT >= 32 && NT <= 1024, "block size");
+    static_assert(!SEP || STAGES <= 2, "separate barriers: 1 or 2 stages");
 };
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
 simt_gemm_kernel(SimtArgs a)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB>;
+    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
     constexpr int NT = KT::NT, TX = KT::TX;
     constexpr int RG = TM / 4, CG = TN / 4;
     extern __shared__ __align__(16) float smem[];
@@ -63,10 +70,9 @@ simt_gemm_kernel(SimtArgs a)
 
     // Issue the cp.async copies of K-tile t into ring slot st.  Out-of-range
     // elements (ragged M, N or K) are zero-filled by the copy itself.
-    auto load_tile = [&](int st, int t) {
+    auto load_a = [&](int st, int t) {
         const int64_t k0 = kbeg + (int64_t)t * BK;
         float* as = As + st * KT::A_STAGE;
-        float* bs = Bs + st * KT::B_STAGE;
         if constexpr (VA) {
             for (int c = tid; c < BM * BK / 4; c += NT) {
                 const int r = c / (BK / 4), kc = (c % (BK / 4)) * 4;
@@ -88,6 +94,10 @@ simt_gemm_kernel(SimtArgs a)
                                 ok ? A + gm * a.lda + gk : A, ok ? 4 : 0);
             }
         }
+    };
+    auto load_b = [&](int st, int t) {
+        const int64_t k0 = kbeg + (int64_t)t * BK;
+        float* bs = Bs + st * KT::B_STAGE;
         if constexpr (VB) {
             for (int c = tid; c < BK * BN / 4; c += NT) {
                 const int r = c / (BN / 4), nc = (c % (BN / 4)) * 4;
@@ -109,6 +119,10 @@ simt_gemm_kernel(SimtArgs a)
                                 ok ? B + gk * a.ldb + gn : B, ok ? 4 : 0);
             }
         }
+    };
+    auto load_tile = [&](int st, int t) {
+        load_a(st, t);
+        load_b(st, t);
     };
 
     float acc[TM][TN];
@@ -149,7 +163,41 @@ simt_gemm_kernel(SimtArgs a)
         }
     };
 
-    if constexpr (STAGES == 1) {
+    if constexpr (SEP && STAGES == 1) {
+        // Single-buffered, separate publication: copy A; barrier; copy B;
+        // barrier; compute; barrier (three per step).
+        for (int t = 0; t < nk; ++t) {
+            load_a(0, t);
+            ptx::cp_async_commit();
+            ptx::cp_async_wait<0>();
+            __syncthreads();
+            load_b(0, t);
+            ptx::cp_async_commit();
+            ptx::cp_async_wait<0>();
+            __syncthreads();
+            compute_tile(0);
+            __syncthreads();
+        }
+    } else if constexpr (SEP) {
+        // Double-buffered, separate publication: A and B of a tile are two
+        // cp.async groups, each published by its own barrier (two per step).
+        load_a(0, 0);
+        ptx::cp_async_commit();
+        load_b(0, 0);
+        ptx::cp_async_commit();
+        for (int t = 0; t < nk; ++t) {
+            ptx::cp_async_wait<1>();   // A of tile t
+            __syncthreads();
+            ptx::cp_async_wait<0>();   // B of tile t
+            __syncthreads();           // also: everyone is done with slot (t+1)%2
+            if (t + 1 < nk) load_a((t + 1) & 1, t + 1);
+            ptx::cp_async_commit();
+            if (t + 1 < nk) load_b((t + 1) & 1, t + 1);
+            ptx::cp_async_commit();
+            compute_tile(t & 1);
+        }
+        ptx::cp_async_wait<0>();
+    } else if constexpr (STAGES == 1) {
         // Single-buffered: load, wait, barrier, compute, barrier (two per step).
         for (int t = 0; t < nk; ++t) {
             load_tile(0, t);
@@ -210,11 +258,11 @@ simt_gemm_kernel(SimtArgs a)
     }
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
 cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB>;
-    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB>;
+    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
+    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
     static bool attr_done = false;  // per-instantiation; benign race (idempotent)
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -227,15 +275,15 @@ cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false>
 cudaError_t launch_cfg(const SimtArgs& a, cudaStream_t s)
 {
     const bool va = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0);
     const bool vb = (a.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0);
-    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true>(a, s);
-    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false>(a, s);
-    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true>(a, s);
-    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false>(a, s);
+    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP>(a, s);
+    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP>(a, s);
+    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP>(a, s);
+    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false, SEP>(a, s);
 }
 
 using LaunchFn = cudaError_t (*)(const SimtArgs&, cudaStream_t);
@@ -245,27 +293,34 @@ struct SimtEntry {
 };
 
 const SimtEntry kSimt[] = {
-    {{128, 128, 16, 8, 8, 2}, launch_cfg<128, 128, 16, 8, 8, 2>},
-    {{128, 128, 16, 8, 8, 3}, launch_cfg<128, 128, 16, 8, 8, 3>},
-    {{128, 128, 16, 8, 8, 1}, launch_cfg<128, 128, 16, 8, 8, 1>},
-    {{64, 64, 16, 4, 4, 2}, launch_cfg<64, 64, 16, 4, 4, 2>},
-    {{64, 64, 16, 4, 4, 3}, launch_cfg<64, 64, 16, 4, 4, 3>},
-    {{64, 64, 16, 4, 4, 1}, launch_cfg<64, 64, 16, 4, 4, 1>},
-    {{64, 64, 32, 4, 4, 2}, launch_cfg<64, 64, 32, 4, 4, 2>},
-    {{32, 32, 32, 4, 4, 2}, launch_cfg<32, 32, 32, 4, 4, 2>},
-    {{32, 32, 32, 4, 4, 1}, launch_cfg<32, 32, 32, 4, 4, 1>},
-    {{128, 64, 16, 8, 4, 2}, launch_cfg<128, 64, 16, 8, 4, 2>},
+    {{128, 128, 16, 8, 8, 2, false}, launch_cfg<128, 128, 16, 8, 8, 2>},
+    {{128, 128, 16, 8, 8, 3, false}, launch_cfg<128, 128, 16, 8, 8, 3>},
+    {{128, 128, 16, 8, 8, 1, false}, launch_cfg<128, 128, 16, 8, 8, 1>},
+    {{64, 64, 16, 4, 4, 2, false}, launch_cfg<64, 64, 16, 4, 4, 2>},
+    {{64, 64, 16, 4, 4, 3, false}, launch_cfg<64, 64, 16, 4, 4, 3>},
+    {{64, 64, 16, 4, 4, 1, false}, launch_cfg<64, 64, 16, 4, 4, 1>},
+    {{64, 64, 32, 4, 4, 2, false}, launch_cfg<64, 64, 32, 4, 4, 2>},
+    {{32, 32, 32, 4, 4, 2, false}, launch_cfg<32, 32, 32, 4, 4, 2>},
+    {{32, 32, 32, 4, 4, 1, false}, launch_cfg<32, 32, 32, 4, 4, 1>},
+    {{128, 64, 16, 8, 4, 2, false}, launch_cfg<128, 64, 16, 8, 4, 2>},
+    // barrier-coalescing ablation: A and B published separately
+    {{128, 128, 16, 8, 8, 2, true}, launch_cfg<128, 128, 16, 8, 8, 2, true>},
+    {{128, 128, 16, 8, 8, 1, true}, launch_cfg<128, 128, 16, 8, 8, 1, true>},
+    {{64, 64, 16, 4, 4, 2, true}, launch_cfg<64, 64, 16, 4, 4, 2, true>},
+    {{64, 64, 16, 4, 4, 1, true}, launch_cfg<64, 64, 16, 4, 4, 1, true>},
+    {{32, 32, 32, 4, 4, 2, true}, launch_cfg<32, 32, 32, 4, 4, 2, true>},
+    {{32, 32, 32, 4, 4, 1, true}, launch_cfg<32, 32, 32, 4, 4, 1, true>},
 };
 
 }  // namespace
 
 int simt_num_configs() { return (int)(sizeof(kSimt) / sizeof(kSimt[0])); }
 const SimtConfig& simt_config(int id) { return kSimt[id].cfg; }
-int simt_find_config(int bm, int bn, int stages)
+int simt_find_config(int bm, int bn, int stages, bool sep)
 {
     for (int i = 0; i < simt_num_configs(); ++i) {
         const SimtConfig& c = kSimt[i].cfg;
-        if (c.bm == bm && c.bn == bn && c.stages == stages) return i;
+        if (c.bm == bm && c.bn == bn && c.stages == stages && c.sep == sep) return i;
     }
     return -1;
 }

@@ -237,8 +237,12 @@ struct TcLayout {
     static constexpr int B_BYTES = BN * kBK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
-    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES;
+    static constexpr int NBARS = 3 * STAGES + 5;    // full, empty, tmem x4, drain, full_b
+    static constexpr int BAR_BYTES = 8 * NBARS + 16;
+    // At least 116 KB, so that two CTAs never share an SM (each holds up to
+    // all 512 TMEM columns for its whole lifetime).
+    static constexpr int SMEM_USED = 1024 + RING_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulator buffers
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512, "TMEM cols");
@@ -278,7 +282,10 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = r / gsz;
 }
 
-template <int BN, int STAGES>
+// SEP = true is the ablation of the pages' barrier coalescing: the A and B
+// tiles of a stage land on two separate "full" barriers (two expect-tx, two
+// waits) instead of one.
+template <int BN, int STAGES, bool SEP>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
                const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
@@ -291,9 +298,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     const uint32_t ring = (raw_addr + 1023u) & ~1023u;
     uint8_t* ring_ptr = smem_raw + (ring - raw_addr);
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + L::RING_BYTES);
-    // bars[0..S-1] full, [S..2S-1] empty, [2S..2S+1] tmem_full, [2S+2..2S+3] tmem_empty,
-    // [2S+4] drain; then the TMEM base address slot and the abort flag.
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    // bars[0..S-1] full (A and B, or A only when SEP), [S..2S-1] empty,
+    // [2S..2S+1] tmem_full, [2S+2..2S+3] tmem_empty, [2S+4] drain,
+    // [2S+5..3S+4] full_b (SEP); then the TMEM base address slot and the abort flag.
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -303,6 +311,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     auto tfull_bar = [&](int b) { return ptx::smem_u32(bars + 2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return ptx::smem_u32(bars + 2 * STAGES + 2 + b); };
     const uint32_t drain_bar = ptx::smem_u32(bars + 2 * STAGES + 4);
+    auto fullb_bar = [&](int s) { return ptx::smem_u32(bars + (SEP ? 2 * STAGES + 5 + s : s)); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -314,6 +323,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             ptx::mbar_init(tempty_bar(b), 4);
         }
         ptx::mbar_init(drain_bar, 1);
+        if (SEP)
+            for (int s = 0; s < STAGES; ++s) ptx::mbar_init(fullb_bar(s), 1);
         *abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -357,12 +368,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
                     ++fills;
                     if (fills != (uint32_t)args.withhold) {
                         const uint32_t sb = ring + stage * L::STAGE_BYTES;
-                        ptx::mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
                         const int kc = kb * kBK;
+                        // One expect-tx covers all four operand tiles (A and B
+                        // publish together); SEP arms A and B separately.
+                        ptx::mbar_arrive_expect_tx(full_bar(stage), SEP ? 2 * L::A_BYTES : L::STAGE_BYTES);
                         ptx::tma_load_2d(sb, &tm_ahi, full_bar(stage), kc, tm * kBM);
                         ptx::tma_load_2d(sb + L::A_BYTES, &tm_alo, full_bar(stage), kc, tm * kBM);
-                        ptx::tma_load_2d(sb + 2 * L::A_BYTES, &tm_bhi, full_bar(stage), kc, tn * BN);
-                        ptx::tma_load_2d(sb + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, full_bar(stage), kc,
+                        if (SEP) ptx::mbar_arrive_expect_tx(fullb_bar(stage), 2 * L::B_BYTES);
+                        ptx::tma_load_2d(sb + 2 * L::A_BYTES, &tm_bhi, fullb_bar(stage), kc, tn * BN);
+                        ptx::tma_load_2d(sb + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, fullb_bar(stage), kc,
                                          tn * BN);
                     }
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -379,6 +393,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
                 const long long t0 = clock64();
                 while (!ptx::mbar_try_wait(full_bar(s), par)) {
                     if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+                }
+                if (SEP) {
+                    const long long t1 = clock64();
+                    while (!ptx::mbar_try_wait(fullb_bar(s), par)) {
+                        if (clock64() - t1 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+                    }
                 }
             }
         }
@@ -400,7 +420,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, limit, abort_flag, args.status)) {
+                    if (!wait_phase(full_bar(stage), phase, limit, abort_flag, args.status) ||
+                        (SEP && !wait_phase(fullb_bar(stage), phase, limit, abort_flag, args.status))) {
                         stop = true;
                         break;
                     }
@@ -605,11 +626,11 @@ int grid_cap(int64_t work, int sms)
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool SEP = false>
 cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
 {
     using L = TcLayout<BN, STAGES>;
-    auto kern = tc_gemm_kernel<BN, STAGES>;
+    auto kern = tc_gemm_kernel<BN, STAGES, SEP>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
@@ -641,23 +662,32 @@ struct TcEntry {
     LaunchFn reduce;
 };
 const TcEntry kTc[] = {
-    {{128, 128, 32, 3}, launch_main<128, 3>, launch_reduce<128>},
-    {{128, 256, 32, 2}, launch_main<256, 2>, launch_reduce<256>},
-    {{128, 64, 32, 4}, launch_main<64, 4>, launch_reduce<64>},
+    // the ring as deep as shared memory allows, per tile width
+    {{128, 128, 32, 3, false}, launch_main<128, 3>, launch_reduce<128>},
+    {{128, 256, 32, 2, false}, launch_main<256, 2>, launch_reduce<256>},
+    {{128, 64, 32, 4, false}, launch_main<64, 4>, launch_reduce<64>},
+    // pipeline-depth ablation: single-buffered (1) and shallower rings
+    {{128, 256, 32, 1, false}, launch_main<256, 1>, launch_reduce<256>},
+    {{128, 128, 32, 1, false}, launch_main<128, 1>, launch_reduce<128>},
+    {{128, 128, 32, 2, false}, launch_main<128, 2>, launch_reduce<128>},
+    {{128, 64, 32, 2, false}, launch_main<64, 2>, launch_reduce<64>},
+    // barrier-coalescing ablation: separate full barriers for A and B
+    {{128, 256, 32, 2, true}, launch_main<256, 2, true>, launch_reduce<256>},
+    {{128, 128, 32, 3, true}, launch_main<128, 3, true>, launch_reduce<128>},
 };
 
 }  // namespace
 
 int tc_num_configs() { return (int)(sizeof(kTc) / sizeof(kTc[0])); }
 const TcConfig& tc_config(int id) { return kTc[id].cfg; }
-int tc_find_config(int bn, int stages)
+int tc_find_config(int bn, int stages, bool sep)
 {
     for (int i = 0; i < tc_num_configs(); ++i)
-        if (kTc[i].cfg.bn == bn && kTc[i].cfg.stages == stages) return i;
-    // Stage count not compiled for this tile width: take the one that is.
+        if (kTc[i].cfg.bn == bn && kTc[i].cfg.stages == stages && kTc[i].cfg.sep == sep) return i;
+    // Stage count 0: the first (deepest) ring compiled for this tile width.
     if (stages == 0)
         for (int i = 0; i < tc_num_configs(); ++i)
-            if (kTc[i].cfg.bn == bn) return i;
+            if (kTc[i].cfg.bn == bn && kTc[i].cfg.sep == sep) return i;
     return -1;
 }
 

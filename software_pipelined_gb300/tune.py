@@ -9,7 +9,8 @@ rule for shapes it does not list.  Run on the target GPU:
         --inc software_pipelined_gb300/csrc/dispatch_table.inc
 
 Each candidate is planned with forced options, warmed up, and timed as the
-median of three batches of back-to-back runs (CUDA events on one stream).
+median of three replays of a CUDA graph holding back-to-back runs (events
+around each replay), so launch overhead on the host does not decide.
 """
 from __future__ import annotations
 
@@ -32,25 +33,36 @@ SPLITS = [1, 2, 3, 4, 6, 8, 12, 16]
 
 
 def time_plan(plan, dA, dB, dC, stream, target_ms=5.0, batches=3):
+    """Median device time per run (ms): runs captured back to back in a CUDA
+    graph, the graph replayed between two events."""
     import torch
-    run = lambda: plan.run_ptr(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream.cuda_stream)
+    s = torch.cuda.Stream()
+    run = lambda: plan.run_ptr(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), s.cuda_stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(3):
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            run()
+        e0.record(s)
         run()
-    e0.record(stream)
-    run()
-    e1.record(stream)
+        e1.record(s)
     e1.synchronize()
-    reps = int(max(1, min(500, target_ms / max(e0.elapsed_time(e1), 1e-3))))
-    res = []
-    for _ in range(batches):
-        e0.record(stream)
+    reps = int(max(1, min(200, target_ms / max(e0.elapsed_time(e1), 1e-3))))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
         for _ in range(reps):
             run()
-        e1.record(stream)
-        e1.synchronize()
-        res.append(e0.elapsed_time(e1) / reps)
-    if plan.check() != g.OK:
+    res = []
+    with torch.cuda.stream(s):  # replay() launches on the current stream
+        graph.replay()
+        s.synchronize()
+        for _ in range(batches):
+            e0.record(s)
+            graph.replay()
+            e1.record(s)
+            e1.synchronize()
+            res.append(e0.elapsed_time(e1) / reps)
+    del graph
+    if plan.check(s.cuda_stream) != g.OK:
         raise RuntimeError("device status not OK")
     return statistics.median(res)
 
@@ -110,6 +122,20 @@ def main():
         write_inc(results, args.inc)
 
 
+def effective_split(desc: str) -> int:
+    """The table's split field for the configuration a plan description shows:
+    SIMT: its split_k; tensor cores: 1 = no split tile, 0 = only the last wave
+    split (automatic), n = every tile in n K-slices."""
+    import re
+    if desc.startswith("simt"):
+        return int(re.search(r"split_k=(\d+)", desc).group(1))
+    whole = int(re.search(r"whole=(\d+)", desc).group(1))
+    tiles, slices = (int(v) for v in re.search(r"split=(\d+)x(\d+)", desc).groups())
+    if tiles == 0:
+        return 1
+    return 0 if whole > 0 else slices
+
+
 def write_inc(results, path):
     lines = [
         "// Per-shape dispatch table: the fastest configuration measured on GB300 for",
@@ -127,8 +153,9 @@ def write_inc(results, path):
     ]
     for r in results:
         o = r["best"]["opts"]
+        split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
-                     f"{o['stages']}, {o['split_k']}}}}},  // {r['best']['us']} us")
+                     f"{o['stages']}, {split}}}}},  // {r['best']['us']} us")
     lines += [
         "    {0, 0, 0, {0, 0, 0, 0, 0}},  // sentinel",
         "};",

@@ -166,34 +166,44 @@ def test_3xtf32_accuracy_matches_fp32_simt():
     assert et <= 3 * es + 1e-3, (et, es)
 
 
-SIMT_CFGS = [(128, 128, 2), (128, 128, 3), (128, 128, 1), (64, 64, 2), (64, 64, 3), (64, 64, 1),
-             (32, 32, 2), (32, 32, 1), (128, 64, 2)]
+SIMT_CFGS = [(128, 128, 2, 0), (128, 128, 3, 0), (128, 128, 1, 0), (64, 64, 2, 0), (64, 64, 3, 0),
+             (64, 64, 1, 0), (32, 32, 2, 0), (32, 32, 1, 0), (128, 64, 2, 0),
+             (128, 128, 2, 1), (128, 128, 1, 1), (64, 64, 2, 1), (64, 64, 1, 1), (32, 32, 2, 1),
+             (32, 32, 1, 1)]
 
 
-@pytest.mark.parametrize("cfg", SIMT_CFGS, ids=[f"{a}x{b}s{c}" for a, b, c in SIMT_CFGS])
-def test_every_simt_config(cfg):
-    bm, bn, st = cfg
+@pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
+@pytest.mark.parametrize("cfg", SIMT_CFGS, ids=[f"{a}x{b}s{c}{'sep' if d else ''}" for a, b, c, d in SIMT_CFGS])
+def test_every_simt_config(cfg, aligned):
+    # last field: separate barriers for A and B (barrier-coalescing ablation)
+    bm, bn, st, sep = cfg
     M, N, K = 3 * bm + 5, 2 * bn + 3, 97
     A = inputs.uniform_pm1(951, M, K)
     B = inputs.uniform_pm1(952, K, N)
-    C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st)
+    kw = {} if aligned else dict(lda=K + 1, ldb=N + 2, a_off=1, b_off=1)
+    C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st,
+                                    separate_syncs=sep, **kw)
+    assert ("separate-syncs" in desc) == bool(sep), desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
 
 
-TC_CFGS = [(128, 3), (256, 2), (64, 4)]
+TC_CFGS = [(128, 3, 0), (256, 2, 0), (64, 4, 0), (256, 1, 0), (128, 1, 0), (128, 2, 0), (64, 2, 0),
+           (256, 2, 1), (128, 3, 1)]
 
 
-@pytest.mark.parametrize("cfg", TC_CFGS, ids=[f"n{a}s{b}" for a, b in TC_CFGS])
+@pytest.mark.parametrize("cfg", TC_CFGS, ids=[f"n{a}s{b}{'sep' if c else ''}" for a, b, c in TC_CFGS])
 @pytest.mark.parametrize("split", [1, 2])
 def test_every_tcgen05_config(cfg, split):
-    bn, st = cfg
+    bn, st, sep = cfg
     # Several M and N tiles plus a ragged edge, and more k-blocks than stages so
     # every ring slot is reused across the loop back-edge.
     M, N, K = 2 * 128 + 17, 3 * bn + 9, 32 * 11 + 7
     A = inputs.uniform_pm1(961, M, K)
     B = inputs.normal(962, K, N)
-    C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_TCGEN05, tile_n=bn, stages=st, split_k=split)
+    C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_TCGEN05, tile_n=bn, stages=st, split_k=split,
+                                    separate_syncs=sep)
+    assert f"stages={st}" in desc and ("separate-syncs" in desc) == bool(sep), desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
 
