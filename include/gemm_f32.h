@@ -98,7 +98,12 @@ typedef struct {
                                B through separate synchronisations (SIMT: one barrier after
                                each operand's copy; TC: separate "full" mbarriers for A and
                                B); 0 = one synchronisation for both (default) */
-    int32_t reserved[6];
+    int32_t operand_split;  /* TC only: where the 3xTF32 split happens.  0 = dispatcher's
+                               choice; 1 = a pre-pass writes hi/lo operands to scratch;
+                               2 = inside the GEMM kernel (needs K >= 32 and lda, ldb
+                               multiples of 4; falls back to 1 at run time for a base
+                               pointer of A or B that is not 16-byte aligned) */
+    int32_t reserved[5];
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

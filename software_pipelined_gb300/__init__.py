@@ -40,7 +40,8 @@ class Opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32), ("tf32_terms", ctypes.c_int32),
                 ("wait_timeout_cycles", ctypes.c_int64), ("debug_withhold_stage", ctypes.c_int32),
-                ("separate_syncs", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
+                ("separate_syncs", ctypes.c_int32), ("operand_split", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 5)]
 
 
 _lock = threading.Lock()
@@ -192,7 +193,7 @@ class Plan:
 
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, *, variant=VARIANT_AUTO, tile_m=0,
                  tile_n=0, stages=0, split_k=0, tf32_terms=0, wait_timeout_cycles=0,
-                 debug_withhold_stage=0, separate_syncs=0):
+                 debug_withhold_stage=0, separate_syncs=0, operand_split=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.lda = int(lda if lda is not None else max(K, 1))
         self.ldb = int(ldb if ldb is not None else max(N, 1))
@@ -202,6 +203,7 @@ class Plan:
         o.tf32_terms, o.wait_timeout_cycles = tf32_terms, wait_timeout_cycles
         o.debug_withhold_stage = debug_withhold_stage
         o.separate_syncs = separate_syncs
+        o.operand_split = operand_split
         s, h = gemm_f32_plan_ex(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, o)
         if s != OK:
             raise GemmError(s, "gemm_f32_plan_ex")

@@ -21,12 +21,16 @@ namespace {
 
 enum PlanKind : int { kNoop = 0, kZeroFill = 1, kSimt = 2, kTc = 3 };
 
-// Smallest K the tensor-core path accepts (accuracy of the 3xTF32 split).
+// Smallest K the tensor-core path accepts (accuracy of the 3xTF32 split):
+// 16 with the round-to-nearest split of the pre-pass, 32 with the truncating
+// split of the in-kernel path (each product's error is then up to 2^-19|a||b|).
 constexpr int64_t kTcMinK = 16;
+constexpr int64_t kTcFusedMinK = 32;
 
 struct DispatchChoice {
     int variant;   // GEMM_F32_VARIANT_SIMT / _TCGEN05
     int tile_m, tile_n, stages, split_k;
+    int fused;     // TC: 1 = operands split inside the kernel
 };
 
 #include "dispatch_table.inc"
@@ -97,6 +101,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.operand_split < 0 || o.operand_split > 2) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -235,8 +240,16 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if (K < kTcMinK) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             p->kind = kTc;
             TcPlanState& t = p->tc;
-            t.config_id = tc_find_config(c.tile_n, c.stages, o.separate_syncs != 0);
+            bool fused = o.operand_split == 2 || (o.operand_split == 0 && c.fused);
+            const bool fused_ok = K >= kTcFusedMinK && lda % 4 == 0 && ldb % 4 == 0 && !o.separate_syncs &&
+                                  tc_find_config(c.tile_n, 0, false, true) >= 0;
+            if (fused && !fused_ok) {
+                if (o.operand_split == 2) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                fused = false;
+            }
+            t.config_id = tc_find_config(c.tile_n, fused ? 0 : c.stages, o.separate_syncs != 0, fused);
             if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            if (fused) t.fallback_config_id = tc_find_config(c.tile_n, 0, false, false);
             const TcConfig& tcfg = tc_config(t.config_id);
             t.terms = o.tf32_terms ? o.tf32_terms : 3;
             t.num_sms = p->num_sms;
@@ -252,8 +265,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 bytes += align256(t.partial_bytes);
             }
             snprintf(p->desc, sizeof p->desc,
-                     "tcgen05 3xtf32 terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d kp=%lld",
-                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, tcfg.sep ? " separate-syncs" : "",
+                     "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d kp=%lld",
+                     tcfg.fused ? " in-kernel-split" : "", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
+                     tcfg.sep ? " separate-syncs" : "",
                      t.tiles_m * t.tiles_n, t.dp_tiles,
                      t.split_tiles, t.splits, (long long)t.kp);
         }

@@ -44,10 +44,11 @@ struct TcConfig {
     int bm, bn, bk;  // CTA tile (bm = 128 rows = TMEM lanes; bk = 32 fp32 = 128 B)
     int stages;      // smem ring depth
     bool sep;        // separate full barriers for A and B (ablation)
+    bool fused;      // operands split inside the kernel (raw A and B by TMA)
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);
-int tc_find_config(int bn, int stages, bool sep = false);
+int tc_find_config(int bn, int stages, bool sep = false, bool fused = false);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
 // tensor maps that describe it, and the work decomposition.
@@ -81,6 +82,14 @@ struct TcPlanState {
     int num_sms = 0;
     int64_t timeout_cycles = 0;
     int withhold_stage = 0;
+    // In-kernel split (fused) plans: the pre-split configuration of the same
+    // tile width, used when a base pointer of A or B is not 16-byte aligned;
+    // tensor maps over the caller's raw A and B, re-encoded when they change.
+    int fallback_config_id = -1;
+    mutable const float* raw_a = nullptr;
+    mutable const float* raw_b = nullptr;
+    alignas(64) mutable unsigned char tmap_a_raw[128];
+    alignas(64) mutable unsigned char tmap_b_raw[128];
 };
 // Work decomposition for config t.config_id: split_request 0 = automatic
 // (split the tiles of a partial last wave), 1 = none, >= 2 = every tile in that

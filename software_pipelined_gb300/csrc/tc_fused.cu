@@ -1,0 +1,340 @@
+// tcgen05 3xTF32 GEMM that splits the operands inside the kernel.
+//
+// Same pipeline as tc_gemm.cu ("Double Buffering" technique page and "Case
+// Study: The Double-Buffered GEMM": the next tile is fetched while the current
+// one is multiplied), but the TMA engine copies the caller's raw FP32 A and B
+// tiles, so no split pre-pass and no split operands in HBM are needed:
+//
+//   * A arrives K-major in the 128-byte swizzled layout the MMA reads.  A
+//     kind::tf32 MMA uses the top 19 bits of each FP32 operand (measured on
+//     GB300: it truncates), so the raw tile itself is hi_A = trunc_tf32(A).
+//     Converter warps add lo_A = RN_tf32(A - hi_A) beside it, element by
+//     element in the same swizzled layout.
+//   * B arrives N-major (B is row-major K x N) as 32 x 32 boxes.  Converter
+//     warps transpose it to the K-major swizzled layout as hi_B (the raw value,
+//     truncated by the MMA) and lo_B = RN_tf32(B - trunc_tf32(B)).
+//
+// With this truncation split each product carries up to about 2^-19*|a||b|
+// of error (hi_A*lo_B + lo_A*hi_B + hi_A*hi_B drops lo_A*lo_B < 2^-20|ab| and
+// rounds each lo to 11 bits), which meets the FP32 bound 2*K*2^-24*sum|a||b|
+// for K >= 32; plans take this kernel only then.
+//
+// Shared memory: SLOTS MMA-facing slots [A_raw | lo_A | hi_B | lo_B] and RAWB
+// staging buffers for raw B.  Barriers per slot: full_a (A landed), conv
+// (converters done: hi/lo of A and B ready), empty (MMAs done); per raw-B
+// buffer: full_b (B landed), free_b (converters done reading it).
+//
+// Roles (320 threads, one CTA per SM, persistent over units of work):
+//   warp 0      TMA producer           warp 1      TMEM allocator + MMA issuer
+//   warps 2..5  epilogue (TMEM lanes 32*(w%4)..)   warps 6..9  converters
+// Every wait is bounded as in tc_gemm.cu (timeout -> status word, abort flag,
+// drain, TMEM freed).
+#include <cstdint>
+
+#include "tc_common.cuh"
+
+namespace gemm_f32 {
+namespace {
+
+using namespace tc;
+constexpr int kFusedThreads = 320;
+constexpr int kConvThreads = 128;
+
+template <int BN, int SLOTS, int RAWB>
+struct FusedLayout {
+    static constexpr int A_BYTES = kBM * kBK * 4;          // 16 KB
+    static constexpr int B_BYTES = BN * kBK * 4;
+    static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int RAWB_BYTES = B_BYTES;              // BN/32 boxes of 32 k x 32 n
+    static constexpr int RING_BYTES = SLOTS * SLOT_BYTES + RAWB * RAWB_BYTES;
+    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 5;  // + tmem full/empty x2, drain
+    static constexpr int BAR_BYTES = 8 * NBARS + 16;
+    static constexpr int SMEM_USED = 1024 + RING_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static_assert(BN % 32 == 0 && BN <= 256, "B arrives in 32-column boxes");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Byte offset of element (row, k) in a K-major 128-byte-swizzled tile (rows of
+// 32 FP32 = 128 B, 8-row atoms of 1024 B, 16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t kmajor_off(int row, int kq)
+{
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((kq ^ (row & 7)) << 4));
+}
+
+template <int BN, int SLOTS, int RAWB>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const TcArgs args)
+{
+    using L = FusedLayout<BN, SLOTS, RAWB>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    const uint32_t ring = (raw_addr + 1023u) & ~1023u;
+    uint8_t* ring_ptr = smem_raw + (ring - raw_addr);
+    const uint32_t rawb0 = ring + SLOTS * L::SLOT_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + L::RING_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto full_a = [&](int s) { return ptx::smem_u32(bars + s); };
+    auto conv = [&](int s) { return ptx::smem_u32(bars + SLOTS + s); };
+    auto empty = [&](int s) { return ptx::smem_u32(bars + 2 * SLOTS + s); };
+    auto full_b = [&](int r) { return ptx::smem_u32(bars + 3 * SLOTS + r); };
+    auto free_b = [&](int r) { return ptx::smem_u32(bars + 3 * SLOTS + RAWB + r); };
+    auto tfull = [&](int b) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + b); };
+    auto tempty = [&](int b) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 2 + b); };
+    const uint32_t drain_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SLOTS; ++s) {
+            ptx::mbar_init(full_a(s), 1);
+            ptx::mbar_init(conv(s), kConvThreads / 32);
+            ptx::mbar_init(empty(s), 1);
+        }
+        for (int r = 0; r < RAWB; ++r) {
+            ptx::mbar_init(full_b(r), 1);
+            ptx::mbar_init(free_b(r), kConvThreads / 32);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull(b), 1);
+            ptx::mbar_init(tempty(b), 4);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tm_a);
+        ptx::tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // the previous kernel on the stream may still be writing A or B
+
+    const int num_work = args.dp_tiles + args.split_tiles * args.splits;
+    const int64_t limit = args.timeout;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            uint32_t fills = 0;
+            bool stop = false;
+            for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
+                const Unit u = decode_unit(w, args);
+                int tm, tn;
+                tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                    const int s = fills % SLOTS, r = fills % RAWB;
+                    const uint32_t ps = (fills / SLOTS) & 1u, pr = (fills / RAWB) & 1u;
+                    if (!wait_phase(empty(s), ps ^ 1u, limit, abort_flag, args.status) ||
+                        !wait_phase(free_b(r), pr ^ 1u, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ++fills;
+                    if (fills == (uint32_t)args.withhold) continue;
+                    const int kc = kb * kBK;
+                    ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES);
+                    ptx::tma_load_2d(ring + s * L::SLOT_BYTES, &tm_a, full_a(s), kc, tm * kBM);
+                    ptx::mbar_arrive_expect_tx(full_b(r), L::RAWB_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j)
+                        ptx::tma_load_2d(rawb0 + r * L::RAWB_BYTES + j * 4096, &tm_b, full_b(r),
+                                         tn * BN + 32 * j, kc);
+                }
+            }
+            // Drain: the last fill of every slot and raw-B buffer must have landed.
+            const uint32_t total = fills;
+            auto drain = [&](uint32_t bar_of_last, uint32_t last, int depth) {
+                if (last + 1 == (uint32_t)args.withhold) return;
+                const uint32_t par = (last / depth) & 1u;
+                const long long t0 = clock64();
+                while (!ptx::mbar_try_wait(bar_of_last, par))
+                    if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+            };
+            for (int s = 0; s < SLOTS && (uint32_t)s < total; ++s)
+                drain(full_a(s), (total - 1 - s) / SLOTS * SLOTS + s, SLOTS);
+            for (int r = 0; r < RAWB && (uint32_t)r < total; ++r)
+                drain(full_b(r), (total - 1 - r) / RAWB * RAWB + r, RAWB);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ----------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_tf32<BN>();
+            uint32_t fills = 0;
+            int iter = 0;
+            bool stop = false;
+            for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x, ++iter) {
+                const Unit u = decode_unit(w, args);
+                const int buf = iter & 1;
+                const uint32_t tphase = (iter >> 1) & 1;
+                if (!wait_phase(tempty(buf), tphase ^ 1u, limit, abort_flag, args.status)) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+                    const int s = fills % SLOTS;
+                    const uint32_t ps = (fills / SLOTS) & 1u;
+                    if (!wait_phase(conv(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_hi = ring + s * L::SLOT_BYTES, a_lo = a_hi + L::A_BYTES;
+                    const uint32_t b_hi = a_hi + 2 * L::A_BYTES, b_lo = b_hi + L::B_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
+                        const uint32_t off = ks * kUmmaK * 4;
+                        const uint32_t acc = (kb > u.kb0 || ks > 0) ? 1u : 0u;
+                        if (args.terms == 3) {
+                            ptx::mma_tf32(d_tmem, sw128_desc(a_lo + off), sw128_desc(b_hi + off), idesc, acc);
+                            ptx::mma_tf32(d_tmem, sw128_desc(a_hi + off), sw128_desc(b_lo + off), idesc, 1u);
+                            ptx::mma_tf32(d_tmem, sw128_desc(a_hi + off), sw128_desc(b_hi + off), idesc, 1u);
+                        } else {
+                            ptx::mma_tf32(d_tmem, sw128_desc(a_hi + off), sw128_desc(b_hi + off), idesc, acc);
+                        }
+                    }
+                    ptx::mma_commit(empty(s));
+                }
+                if (stop) break;
+                ptx::mma_commit(tfull(buf));
+            }
+            ptx::mma_commit(drain_bar);
+            const long long t0 = clock64();
+            while (!ptx::mbar_try_wait(drain_bar, 0))
+                if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------ epilogue ------------------------------
+        const int quad = warp & 3;
+        const int row_in_tile = quad * 32 + lane;
+        int iter = 0;
+        for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++iter) {
+            const Unit u = decode_unit(w, args);
+            int tm, tn;
+            tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+            const int buf = iter & 1;
+            const uint32_t tphase = (iter >> 1) & 1;
+            if (!wait_phase(tfull(buf), tphase, limit, abort_flag, args.status)) break;
+            ptx::tc_fence_after();
+            store_accumulator<BN>(args, u, tm, tn,
+                                  tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN, row_in_tile);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty(buf));
+        }
+    } else {
+        // ------------------------------ converters ----------------------------
+        const int ct = threadIdx.x - 6 * 32;  // 0 .. 127
+        uint32_t fills = 0;
+        bool stop = false;
+        for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
+            const Unit u = decode_unit(w, args);
+            for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+                const int s = fills % SLOTS, r = fills % RAWB;
+                const uint32_t ps = (fills / SLOTS) & 1u, pr = (fills / RAWB) & 1u;
+                if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status) ||
+                    !wait_phase(full_b(r), pr, limit, abort_flag, args.status)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t* slot = ring_ptr + s * L::SLOT_BYTES;
+                const uint8_t* a_raw = slot;
+                uint8_t* a_lo = slot + L::A_BYTES;
+                uint8_t* b_hi = slot + 2 * L::A_BYTES;
+                uint8_t* b_lo = b_hi + L::B_BYTES;
+                const uint8_t* b_raw = ring_ptr + SLOTS * L::SLOT_BYTES + r * L::RAWB_BYTES;
+                // A: lo beside the raw tile, same swizzled position, 16 bytes at a time.
+#pragma unroll 4
+                for (int c = ct; c < L::A_BYTES / 16; c += kConvThreads) {
+                    const float4 x = *reinterpret_cast<const float4*>(a_raw + c * 16);
+                    float4 l;
+                    l.x = tf32_rne(x.x - tf32_trunc(x.x));
+                    l.y = tf32_rne(x.y - tf32_trunc(x.y));
+                    l.z = tf32_rne(x.z - tf32_trunc(x.z));
+                    l.w = tf32_rne(x.w - tf32_trunc(x.w));
+                    *reinterpret_cast<float4*>(a_lo + c * 16) = l;
+                }
+                // B: transpose 32-column boxes (row k = 128 B of n, chunk (n%32/4) ^ (k%8))
+                // into K-major rows n (chunk k/4 ^ (n%8)).  A warp takes 32
+                // consecutive n and one 4-wide k group: conflict-free reads along
+                // a box row, conflict-free 16-byte writes across 8 swizzled rows.
+#pragma unroll 2
+                for (int q = ct; q < BN * 8; q += kConvThreads) {
+                    const int ln = q & 31, grp = q >> 5;
+                    const int kq = grp & 7, nb = grp >> 3;
+                    const int n = nb * 32 + ln;
+                    const uint8_t* box = b_raw + nb * 4096;
+                    float v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int k = kq * 4 + j;
+                        v[j] = *reinterpret_cast<const float*>(box + k * 128 + ((((ln >> 2) ^ (k & 7))) << 4) +
+                                                               (ln & 3) * 4);
+                    }
+                    const uint32_t o = kmajor_off(n, kq);
+                    *reinterpret_cast<float4*>(b_hi + o) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4*>(b_lo + o) =
+                        make_float4(tf32_rne(v[0] - tf32_trunc(v[0])), tf32_rne(v[1] - tf32_trunc(v[1])),
+                                    tf32_rne(v[2] - tf32_trunc(v[2])), tf32_rne(v[3] - tf32_trunc(v[3])));
+                }
+                ptx::fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(free_b(r));
+                    ptx::mbar_arrive(conv(s));
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    pdl_trigger();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int BN, int SLOTS, int RAWB>
+cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
+                         cudaStream_t s)
+{
+    using L = FusedLayout<BN, SLOTS, RAWB>;
+    auto kern = tc_fused_kernel<BN, SLOTS, RAWB>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int work = a.dp_tiles + a.split_tiles * a.splits;
+    const int grid = work < st.num_sms ? work : st.num_sms;
+    return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, ta, tb, a);
+}
+
+}  // namespace
+
+cudaError_t tc_fused_main(int bn, const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
+                          const CUtensorMap& tb, cudaStream_t s)
+{
+    switch (bn) {
+    case 128: return launch_fused<128, 3, 2>(st, a, ta, tb, s);
+    case 256: return launch_fused<256, 2, 1>(st, a, ta, tb, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gemm_f32

@@ -47,82 +47,17 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace gemm_f32 {
 namespace {
 
-constexpr int kBM = 128;      // tile rows = TMEM lanes
-constexpr int kBK = 32;       // fp32 elements per 128-byte swizzle row
-constexpr int kUmmaK = 8;     // K of one kind::tf32 MMA
+using namespace tc;
 constexpr int kThreads = 192;
-constexpr int64_t kDefaultTimeout = int64_t(1) << 32;  // SM clock cycles
-
-struct TcArgs {
-    int64_t M, N;
-    int64_t ldc;
-    float* C;
-    float* partial;      // split units' dense 128 x BN partial tiles
-    int* status;
-    int64_t timeout;
-    int tiles_m, tiles_n;
-    int num_kb;          // k-blocks of 32 in the padded K
-    int dp_tiles;        // tiles computed whole, written to C
-    int split_tiles;     // tiles computed in `splits` K-slices each
-    int splits;
-    int kb_per_split;
-    int terms;           // 3 = 3xTF32, 1 = hi*hi only
-    int withhold;        // test hook: 1-based fill index the producer skips (0 = none)
-};
-
-// One unit of work of the persistent kernel: a whole tile, or one K-slice of a
-// split tile.
-struct Unit {
-    int tile;            // index in tile order
-    int kb0, kb1;        // k-block range
-    int slot;            // -1: write C; else index of the dense partial tile
-};
-
-__device__ __forceinline__ Unit decode_unit(int w, const TcArgs& a)
-{
-    Unit u;
-    if (w < a.dp_tiles) {
-        u.tile = w;
-        u.kb0 = 0;
-        u.kb1 = a.num_kb;
-        u.slot = -1;
-    } else {
-        const int t = w - a.dp_tiles;
-        const int z = t % a.splits;
-        u.tile = a.dp_tiles + t / a.splits;
-        u.kb0 = z * a.kb_per_split;
-        u.kb1 = min(a.num_kb, u.kb0 + a.kb_per_split);
-        u.slot = t;
-    }
-    return u;
-}
-
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Operand split pre-pass.
 // ---------------------------------------------------------------------------
-
-// Round an FP32 value to the nearest TF32 value (10 explicit mantissa bits),
-// ties to even, by integer arithmetic on the bit pattern; the low 13 bits of
-// the result are zero.  Inf stays Inf; NaN stays NaN.
-__device__ __forceinline__ float tf32_rne(float x)
-{
-    uint32_t u = __float_as_uint(x);
-    if ((u & 0x7F800000u) != 0x7F800000u) u += 0x0FFFu + ((u >> 13) & 1u);
-    return __uint_as_float(u & 0xFFFFE000u);
-}
-
-__device__ __forceinline__ void split3(float x, float& hi, float& lo)
-{
-    hi = tf32_rne(x);
-    lo = tf32_rne(x - hi);  // x - hi is exact in FP32
-}
 
 constexpr int kSplitBK = 32;    // k rows per B tile of the split pre-pass
 constexpr int kSplitBN = 128;   // n columns per B tile
@@ -207,30 +142,6 @@ split_operands_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t
 // Main kernel.
 // ---------------------------------------------------------------------------
 
-// Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile
-// in the 128-byte swizzled layout TMA writes: rows of 128 B, 8-row atoms 1024 B
-// apart (stride byte offset), leading byte offset unused for swizzled K-major.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4)
-         | ((uint64_t)1 << 16)                  // leading byte offset (unused)
-         | ((uint64_t)(1024 >> 4) << 32)        // stride byte offset
-         | ((uint64_t)1 << 46)                  // descriptor version (tcgen05)
-         | ((uint64_t)2 << 61);                 // swizzle: 128 B
-}
-
-// Instruction descriptor, kind::tf32: D fp32, A and B tf32, both K-major,
-// M = 128, N = BN.
-template <int BN>
-__host__ __device__ constexpr uint32_t idesc_tf32()
-{
-    return (1u << 4)                 // D format: F32
-         | (2u << 7)                 // A format: TF32
-         | (2u << 10)                // B format: TF32
-         | ((uint32_t)(BN >> 3) << 17)
-         | ((uint32_t)(kBM >> 4) << 24);
-}
-
 template <int BN, int STAGES>
 struct TcLayout {
     static constexpr int A_BYTES = kBM * kBK * 4;   // 16 KB
@@ -248,39 +159,6 @@ struct TcLayout {
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512, "TMEM cols");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
-
-// Bounded wait on phase `parity` of an mbarrier.  Gives up when the limit runs
-// out or another role has raised the abort flag; on a timeout it records the
-// status word and raises the flag.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int64_t limit,
-                                           volatile int* abort_flag, int* status)
-{
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > limit) {
-            atomicExch(status, kStatusTimeout);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-// Tile order: groups of 8 tile-rows, column-major inside a group, so the CTAs
-// running together share A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn)
-{
-    constexpr int G = 8;
-    const int group_size = G * tiles_n;
-    const int gid = tile / group_size;
-    const int first_m = gid * G;
-    const int gsz = min(tiles_m - first_m, G);
-    const int r = tile % group_size;
-    tm = first_m + r % gsz;
-    tn = r / gsz;
-}
 
 // SEP = true is the ablation of the pages' barrier coalescing: the A and B
 // tiles of a stage land on two separate "full" barriers (two expect-tx, two
@@ -468,46 +346,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             const uint32_t tphase = (iter >> 1) & 1;
             if (!wait_phase(tfull_bar(buf), tphase, limit, abort_flag, args.status)) break;
             ptx::tc_fence_after();
-            // Whole tiles go to C (guarded); K-slices to a dense 128 x BN partial
-            // tile, all of it (rows past M hold the zero-filled operands' zeros).
-            float* orow;
-            int64_t col0, ncols;
-            bool vec, row_ok;
-            if (u.slot < 0) {
-                const int64_t grow = (int64_t)tm * kBM + row_in_tile;
-                row_ok = grow < args.M;
-                orow = args.C + (row_ok ? grow : 0) * args.ldc;
-                col0 = (int64_t)tn * BN;
-                ncols = args.N;
-                vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
-            } else {
-                row_ok = true;
-                orow = args.partial + ((int64_t)u.slot * kBM + row_in_tile) * BN;
-                col0 = 0;
-                ncols = BN;
-                vec = true;
-            }
-            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                uint32_t r[16];
-                ptx::tmem_ld_32x32b_x16(taddr + c, r);
-                ptx::tmem_wait_ld();
-                const int64_t gn = col0 + c;
-                if (row_ok) {
-                    if (vec && gn + 15 < ncols) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4*>(orow + gn + j) =
-                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (gn + j < ncols) orow[gn + j] = __uint_as_float(r[j]);
-                    }
-                }
-            }
+            store_accumulator<BN>(args, u, tm, tn,
+                                  tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN, row_in_tile);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
@@ -599,31 +439,44 @@ cudaError_t encode_kmajor(void* out, float* base, int64_t rows, int64_t kp, int 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Launch with programmatic stream serialisation: the kernel may start while
-// the previous kernel on the stream finishes, and waits for it (griddepcontrol)
-// before touching that kernel's output.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args&&... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 int grid_cap(int64_t work, int sms)
 {
     const int64_t blocks = (work + 255) / 256;
     const int64_t cap = (int64_t)sms * 8;
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+// Tensor maps over the caller's raw operands for the in-kernel split: A (M x K,
+// lda) as K-major boxes {32, 128}; B (K x N, ldb) as boxes of 32 columns x 32
+// rows.  Both 128-byte swizzled with zero fill; need 16-byte aligned rows.
+cudaError_t encode_raw_a(void* out, const float* A, int64_t M, int64_t K, int64_t lda)
+{
+    EncodeFn enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(lda * 4)};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                     const_cast<float*>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_raw_b(void* out, const float* B, int64_t K, int64_t N, int64_t ldb)
+{
+    EncodeFn enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldb * 4)};
+    cuuint32_t box[2] = {32, (cuuint32_t)kBK};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                     const_cast<float*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int BN, int STAGES, bool SEP = false>
@@ -658,36 +511,43 @@ cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s
 using LaunchFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
 struct TcEntry {
     TcConfig cfg;
-    LaunchFn main;
+    LaunchFn main;    // NULL for fused configurations (tc_fused_main)
     LaunchFn reduce;
 };
 const TcEntry kTc[] = {
     // the ring as deep as shared memory allows, per tile width
-    {{128, 128, 32, 3, false}, launch_main<128, 3>, launch_reduce<128>},
-    {{128, 256, 32, 2, false}, launch_main<256, 2>, launch_reduce<256>},
-    {{128, 64, 32, 4, false}, launch_main<64, 4>, launch_reduce<64>},
+    {{128, 128, 32, 3, false, false}, launch_main<128, 3>, launch_reduce<128>},
+    {{128, 256, 32, 2, false, false}, launch_main<256, 2>, launch_reduce<256>},
+    {{128, 64, 32, 4, false, false}, launch_main<64, 4>, launch_reduce<64>},
     // pipeline-depth ablation: single-buffered (1) and shallower rings
-    {{128, 256, 32, 1, false}, launch_main<256, 1>, launch_reduce<256>},
-    {{128, 128, 32, 1, false}, launch_main<128, 1>, launch_reduce<128>},
-    {{128, 128, 32, 2, false}, launch_main<128, 2>, launch_reduce<128>},
-    {{128, 64, 32, 2, false}, launch_main<64, 2>, launch_reduce<64>},
+    {{128, 256, 32, 1, false, false}, launch_main<256, 1>, launch_reduce<256>},
+    {{128, 128, 32, 1, false, false}, launch_main<128, 1>, launch_reduce<128>},
+    {{128, 128, 32, 2, false, false}, launch_main<128, 2>, launch_reduce<128>},
+    {{128, 64, 32, 2, false, false}, launch_main<64, 2>, launch_reduce<64>},
     // barrier-coalescing ablation: separate full barriers for A and B
-    {{128, 256, 32, 2, true}, launch_main<256, 2, true>, launch_reduce<256>},
-    {{128, 128, 32, 3, true}, launch_main<128, 3, true>, launch_reduce<128>},
+    {{128, 256, 32, 2, true, false}, launch_main<256, 2, true>, launch_reduce<256>},
+    {{128, 128, 32, 3, true, false}, launch_main<128, 3, true>, launch_reduce<128>},
+    // operands split inside the kernel (stages = MMA-facing slots)
+    {{128, 128, 32, 3, false, true}, nullptr, launch_reduce<128>},
+    {{128, 256, 32, 2, false, true}, nullptr, launch_reduce<256>},
 };
 
 }  // namespace
 
 int tc_num_configs() { return (int)(sizeof(kTc) / sizeof(kTc[0])); }
 const TcConfig& tc_config(int id) { return kTc[id].cfg; }
-int tc_find_config(int bn, int stages, bool sep)
+int tc_find_config(int bn, int stages, bool sep, bool fused)
 {
-    for (int i = 0; i < tc_num_configs(); ++i)
-        if (kTc[i].cfg.bn == bn && kTc[i].cfg.stages == stages && kTc[i].cfg.sep == sep) return i;
+    for (int i = 0; i < tc_num_configs(); ++i) {
+        const TcConfig& c = kTc[i].cfg;
+        if (c.bn == bn && c.stages == stages && c.sep == sep && c.fused == fused) return i;
+    }
     // Stage count 0: the first (deepest) ring compiled for this tile width.
     if (stages == 0)
-        for (int i = 0; i < tc_num_configs(); ++i)
-            if (kTc[i].cfg.bn == bn && kTc[i].cfg.sep == sep) return i;
+        for (int i = 0; i < tc_num_configs(); ++i) {
+            const TcConfig& c = kTc[i].cfg;
+            if (c.bn == bn && c.sep == sep && c.fused == fused) return i;
+        }
     return -1;
 }
 
@@ -752,20 +612,6 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
                       const float* B, int64_t ldb, float* C, int64_t ldc, int* status, cudaStream_t s,
                       cudaEvent_t* ev)
 {
-    if (ev) cudaEventRecord(ev[0], s);
-    // 1. Split both operands (B transposed) into the plan's scratch, one launch.
-    {
-        const int vec_a = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
-        const int vec_b = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
-        const int a_blocks = grid_cap(M * (st.kp / 4), st.num_sms);
-        const int64_t b_blocks = (st.kp / kSplitBK) * ((N + kSplitBN - 1) / kSplitBN);
-        split_operands_kernel<<<(unsigned)(a_blocks + b_blocks), 256, 0, s>>>(
-            A, M, K, lda, vec_a, B, N, ldb, vec_b, st.kp, reinterpret_cast<float4*>(st.a_hi),
-            reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    // 2. The pipelined tensor-core GEMM (and the reduction of split tiles).
     TcArgs a{};
     a.M = M; a.N = N; a.ldc = ldc; a.C = C; a.partial = st.partial;
     a.status = status;
@@ -779,12 +625,44 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
     a.kb_per_split = st.kb_per_split;
     a.terms = st.terms;
     a.withhold = st.withhold_stage;
-    if (ev) cudaEventRecord(ev[1], s);
-    cudaError_t e = kTc[st.config_id].main(st, a, s);
+
+    int id = st.config_id;
+    const TcConfig& c = kTc[id].cfg;
+    const bool aligned = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
+    cudaError_t e = cudaSuccess;
+    if (ev) cudaEventRecord(ev[0], s);
+    if (c.fused && aligned) {
+        // Raw operands straight from the caller's buffers: no pre-pass.
+        if (A != st.raw_a) {
+            if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda)) != cudaSuccess) return e;
+            st.raw_a = A;
+        }
+        if (B != st.raw_b) {
+            if ((e = encode_raw_b(st.tmap_b_raw, B, K, N, ldb)) != cudaSuccess) return e;
+            st.raw_b = B;
+        }
+        if (ev) cudaEventRecord(ev[1], s);
+        e = tc_fused_main(c.bn, st, a, *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
+                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw), s);
+    } else {
+        if (c.fused) id = st.fallback_config_id;
+        // 1. Split both operands (B transposed) into the plan's scratch, one launch.
+        const int vec_a = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
+        const int vec_b = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
+        const int a_blocks = grid_cap(M * (st.kp / 4), st.num_sms);
+        const int64_t b_blocks = (st.kp / kSplitBK) * ((N + kSplitBN - 1) / kSplitBN);
+        split_operands_kernel<<<(unsigned)(a_blocks + b_blocks), 256, 0, s>>>(
+            A, M, K, lda, vec_a, B, N, ldb, vec_b, st.kp, reinterpret_cast<float4*>(st.a_hi),
+            reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // 2. The pipelined tensor-core GEMM.
+        if (ev) cudaEventRecord(ev[1], s);
+        e = kTc[id].main(st, a, s);
+    }
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);
     // 3. Fixed-order sum of the split tiles' K-slices.
-    if (st.split_tiles > 0) e = kTc[st.config_id].reduce(st, a, s);
+    if (st.split_tiles > 0) e = kTc[id].reduce(st, a, s);
     if (ev) cudaEventRecord(ev[3], s);
     return e;
 }

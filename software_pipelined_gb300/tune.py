@@ -77,9 +77,11 @@ def candidates(M, N, K):
                     out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp))
     if K >= 16:
         for bn in TC_BN:
-            for sp in [0] + SPLITS:
-                if sp <= 1 or (K + 31) // 32 >= sp:
-                    out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp))
+            for fused in ((1, 2) if bn in (128, 256) and K >= 32 else (1,)):
+                for sp in [0] + SPLITS:
+                    if sp <= 1 or (K + 31) // 32 >= sp:
+                        out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp,
+                                        operand_split=fused))
     return out
 
 
@@ -143,7 +145,8 @@ def write_inc(results, path):
         "// software_pipelined_gb300/tune.py from its timing sweep.  Shapes not listed",
         "// fall back to the rule in choose().  Fields: variant (1 SIMT, 2 tcgen05),",
         "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
-        "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices).",
+        "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
+        "// fused (tcgen05: 1 = operands split inside the kernel).",
         "struct TableRow {",
         "    int64_t M, N, K;",
         "    DispatchChoice c;",
@@ -155,9 +158,10 @@ def write_inc(results, path):
         o = r["best"]["opts"]
         split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
-                     f"{o['stages']}, {split}}}}},  // {r['best']['us']} us")
+                     f"{o['stages']}, {split}, {1 if 'in-kernel-split' in r['best']['plan'] else 0}}}}},"
+                     f"  // {r['best']['us']} us")
     lines += [
-        "    {0, 0, 0, {0, 0, 0, 0, 0}},  // sentinel",
+        "    {0, 0, 0, {0, 0, 0, 0, 0, 0}},  // sentinel",
         "};",
         "",
         "bool table_lookup(int64_t M, int64_t N, int64_t K, DispatchChoice& out)",
