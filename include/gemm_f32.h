@@ -101,8 +101,10 @@ typedef struct {
     int32_t operand_split;  /* TC only: where the 3xTF32 split happens.  0 = dispatcher's
                                choice; 1 = a pre-pass writes hi/lo operands to scratch;
                                2 = inside the GEMM kernel (needs K >= 32 and lda, ldb
-                               multiples of 4; falls back to 1 at run time for a base
-                               pointer of A or B that is not 16-byte aligned) */
+                               multiples of 4); 3 = A inside the kernel, B by the pre-pass
+                               (needs K >= 32, lda a multiple of 4).  2 and 3 fall back to 1
+                               at run time for a base pointer of A (or, for 2, B) that is
+                               not 16-byte aligned */
     int32_t reserved[5];
 } gemm_f32_opts;
 

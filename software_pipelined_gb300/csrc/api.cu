@@ -30,7 +30,7 @@ constexpr int64_t kTcFusedMinK = 32;
 struct DispatchChoice {
     int variant;   // GEMM_F32_VARIANT_SIMT / _TCGEN05
     int tile_m, tile_n, stages, split_k;
-    int fused;     // TC: 1 = operands split inside the kernel
+    int fused;     // TC: where the split happens (kSplitPrepass / kSplitInKernel / kSplitHybrid)
 };
 
 #include "dispatch_table.inc"
@@ -101,7 +101,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
-    if (o.operand_split < 0 || o.operand_split > 2) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.operand_split < 0 || o.operand_split > 3) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -240,16 +240,20 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if (K < kTcMinK) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             p->kind = kTc;
             TcPlanState& t = p->tc;
-            bool fused = o.operand_split == 2 || (o.operand_split == 0 && c.fused);
-            const bool fused_ok = K >= kTcFusedMinK && lda % 4 == 0 && ldb % 4 == 0 && !o.separate_syncs &&
-                                  tc_find_config(c.tile_n, 0, false, true) >= 0;
-            if (fused && !fused_ok) {
-                if (o.operand_split == 2) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-                fused = false;
+            // operand_split: 1 pre-pass, 2 in the kernel, 3 hybrid (A in the kernel,
+            // B by the pre-pass); 0 = the dispatcher's choice.
+            int where = o.operand_split ? o.operand_split - 1 : c.fused;
+            const bool ok = where == kSplitPrepass ||
+                            (K >= kTcFusedMinK && lda % 4 == 0 && (where == kSplitHybrid || ldb % 4 == 0) &&
+                             !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where) >= 0);
+            if (!ok) {
+                if (o.operand_split) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                where = kSplitPrepass;
             }
-            t.config_id = tc_find_config(c.tile_n, fused ? 0 : c.stages, o.separate_syncs != 0, fused);
+            t.config_id = tc_find_config(c.tile_n, where != kSplitPrepass ? 0 : c.stages, o.separate_syncs != 0,
+                                         where);
             if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-            if (fused) t.fallback_config_id = tc_find_config(c.tile_n, 0, false, false);
+            if (where != kSplitPrepass) t.fallback_config_id = tc_find_config(c.tile_n, 0, false, kSplitPrepass);
             const TcConfig& tcfg = tc_config(t.config_id);
             t.terms = o.tf32_terms ? o.tf32_terms : 3;
             t.num_sms = p->num_sms;
@@ -266,7 +270,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             }
             snprintf(p->desc, sizeof p->desc,
                      "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d kp=%lld",
-                     tcfg.fused ? " in-kernel-split" : "", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
+                     tcfg.split == kSplitInKernel ? " in-kernel-split"
+                     : tcfg.split == kSplitHybrid ? " hybrid-split" : "",
+                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
                      tcfg.sep ? " separate-syncs" : "",
                      t.tiles_m * t.tiles_n, t.dp_tiles,
                      t.split_tiles, t.splits, (long long)t.kp);
@@ -457,7 +463,12 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
     switch (p->kind) {
     case kZeroFill: return 1;
     case kSimt: return p->split_k > 1 ? 2 : 1;
-    case kTc: return 2 + (p->tc.split_tiles > 0 ? 1 : 0);
+    case kTc: {
+        // the pre-pass (unless both operands are split in the kernel), the GEMM,
+        // and the reduction of split tiles
+        const int split = tc_config(p->tc.config_id).split;
+        return (split == kSplitInKernel ? 1 : 2) + (p->tc.split_tiles > 0 ? 1 : 0);
+    }
     default: return 0;
     }
 }

@@ -44,11 +44,16 @@ struct TcConfig {
     int bm, bn, bk;  // CTA tile (bm = 128 rows = TMEM lanes; bk = 32 fp32 = 128 B)
     int stages;      // smem ring depth
     bool sep;        // separate full barriers for A and B (ablation)
-    bool fused;      // operands split inside the kernel (raw A and B by TMA)
+    int split;       // where the 3xTF32 split happens: kSplitPrepass, kSplitInKernel, kSplitHybrid
+};
+enum : int {
+    kSplitPrepass = 0,   // a pre-pass writes hi/lo of A and B to scratch
+    kSplitInKernel = 1,  // raw A and B by TMA, split by converter warps
+    kSplitHybrid = 2     // raw A split in the kernel, B split by the pre-pass
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);
-int tc_find_config(int bn, int stages, bool sep = false, bool fused = false);
+int tc_find_config(int bn, int stages, bool sep = false, int split = 0);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
 // tensor maps that describe it, and the work decomposition.
@@ -82,7 +87,7 @@ struct TcPlanState {
     int num_sms = 0;
     int64_t timeout_cycles = 0;
     int withhold_stage = 0;
-    // In-kernel split (fused) plans: the pre-split configuration of the same
+    // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.
     int fallback_config_id = -1;

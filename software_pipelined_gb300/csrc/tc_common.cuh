@@ -217,8 +217,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 }  // namespace tc
 
-// The in-kernel split kernel for tile width bn (tc_fused.cu).
-cudaError_t tc_fused_main(int bn, const TcPlanState& st, const tc::TcArgs& a, const CUtensorMap& ta,
-                          const CUtensorMap& tb, cudaStream_t s);
+// The in-kernel split kernel for tile width bn (tc_fused.cu); b_presplit: B
+// comes split by the pre-pass (tbhi/tblo) and only A is split in the kernel.
+cudaError_t tc_fused_main(int bn, bool b_presplit, const TcPlanState& st, const tc::TcArgs& a,
+                          const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
+                          const CUtensorMap& tblo, cudaStream_t s);
 
 }  // namespace gemm_f32

@@ -8,25 +8,29 @@
 //   * A arrives K-major in the 128-byte swizzled layout the MMA reads.  A
 //     kind::tf32 MMA uses the top 19 bits of each FP32 operand (measured on
 //     GB300: it truncates), so the raw tile itself is hi_A = trunc_tf32(A).
-//     Converter warps add lo_A = RN_tf32(A - hi_A) beside it, element by
+//     Converter warps add lo_A = A - hi_A rounded to TF32 beside it, element by
 //     element in the same swizzled layout.
 //   * B arrives N-major (B is row-major K x N) as 32 x 32 boxes.  Converter
 //     warps transpose it to the K-major swizzled layout as hi_B (the raw value,
-//     truncated by the MMA) and lo_B = RN_tf32(B - trunc_tf32(B)).
+//     truncated by the MMA) and lo_B = B - trunc_tf32(B) rounded to TF32.
 //
 // With this truncation split each product carries up to about 2^-19*|a||b|
 // of error (hi_A*lo_B + lo_A*hi_B + hi_A*hi_B drops lo_A*lo_B < 2^-20|ab| and
 // rounds each lo to 11 bits), which meets the FP32 bound 2*K*2^-24*sum|a||b|
 // for K >= 32; plans take this kernel only then.
 //
+// A hybrid form takes B already split and transposed by the pre-pass (hi/lo
+// copied straight into the slot) and converts only A in the kernel: half the
+// pre-pass, and a quarter of the converters' shared-memory traffic.
+//
 // Shared memory: SLOTS MMA-facing slots [A_raw | lo_A | hi_B | lo_B] and RAWB
 // staging buffers for raw B.  Barriers per slot: full_a (A landed), conv
 // (converters done: hi/lo of A and B ready), empty (MMAs done); per raw-B
 // buffer: full_b (B landed), free_b (converters done reading it).
 //
-// Roles (320 threads, one CTA per SM, persistent over units of work):
+// Roles (448 threads, one CTA per SM, persistent over units of work):
 //   warp 0      TMA producer           warp 1      TMEM allocator + MMA issuer
-//   warps 2..5  epilogue (TMEM lanes 32*(w%4)..)   warps 6..9  converters
+//   warps 2..5  epilogue (TMEM lanes 32*(w%4)..)   warps 6..13 converters
 // Every wait is bounded as in tc_gemm.cu (timeout -> status word, abort flag,
 // drain, TMEM freed).
 #include <cstdint>
@@ -37,8 +41,9 @@ namespace gemm_f32 {
 namespace {
 
 using namespace tc;
-constexpr int kFusedThreads = 320;
-constexpr int kConvThreads = 128;
+constexpr int kConvWarps = 8;                       // one per 4-wide k group of a 32-k block
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kFusedThreads = 6 * 32 + kConvThreads;
 
 template <int BN, int SLOTS, int RAWB>
 struct FusedLayout {
@@ -56,6 +61,17 @@ struct FusedLayout {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
+// lo = RN(x - trunc_tf32(x)) to 11 significant bits, ties away from zero: the
+// difference is exact in FP32; adding half an ulp of TF32 to the magnitude and
+// clearing the low 13 bits rounds it.  Two integer and one float operation per
+// element (plus the truncation), no special cases: for finite x the result is
+// finite; a non-finite x makes the hi*hi product non-finite anyway.
+__device__ __forceinline__ float lo_part(float x)
+{
+    const float d = x - tf32_trunc(x);
+    return __uint_as_float((__float_as_uint(d) + 0x1000u) & 0xFFFFE000u);
+}
+
 // Byte offset of element (row, k) in a K-major 128-byte-swizzled tile (rows of
 // 32 FP32 = 128 B, 8-row atoms of 1024 B, 16-byte chunk index XOR row % 8).
 __device__ __forceinline__ uint32_t kmajor_off(int row, int kq)
@@ -63,11 +79,16 @@ __device__ __forceinline__ uint32_t kmajor_off(int row, int kq)
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((kq ^ (row & 7)) << 4));
 }
 
+// RAWB == 0 is the hybrid form: B comes already split (hi/lo, K-major) from the
+// pre-pass through tm_bhi/tm_blo, straight into the slot, and the converters
+// only add lo_A.  Otherwise tm_b copies raw B into the RAWB staging buffers.
 template <int BN, int SLOTS, int RAWB>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
                 const TcArgs args)
 {
+    constexpr bool BPRE = RAWB == 0;
     using L = FusedLayout<BN, SLOTS, RAWB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -109,7 +130,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tm_a);
-        ptx::tma_prefetch_desc(&tm_b);
+        if (BPRE) {
+            ptx::tma_prefetch_desc(&tm_bhi);
+            ptx::tma_prefetch_desc(&tm_blo);
+        } else {
+            ptx::tma_prefetch_desc(&tm_b);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
@@ -134,23 +160,38 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 int tm, tn;
                 tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
-                    const int s = fills % SLOTS, r = fills % RAWB;
-                    const uint32_t ps = (fills / SLOTS) & 1u, pr = (fills / RAWB) & 1u;
-                    if (!wait_phase(empty(s), ps ^ 1u, limit, abort_flag, args.status) ||
-                        !wait_phase(free_b(r), pr ^ 1u, limit, abort_flag, args.status)) {
+                    const int s = fills % SLOTS;
+                    const uint32_t ps = (fills / SLOTS) & 1u;
+                    if (!wait_phase(empty(s), ps ^ 1u, limit, abort_flag, args.status)) {
                         stop = true;
                         break;
                     }
-                    ++fills;
-                    if (fills == (uint32_t)args.withhold) continue;
                     const int kc = kb * kBK;
-                    ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES);
-                    ptx::tma_load_2d(ring + s * L::SLOT_BYTES, &tm_a, full_a(s), kc, tm * kBM);
-                    ptx::mbar_arrive_expect_tx(full_b(r), L::RAWB_BYTES);
+                    const uint32_t slot = ring + s * L::SLOT_BYTES;
+                    if constexpr (BPRE) {
+                        ++fills;
+                        if (fills == (uint32_t)args.withhold) continue;
+                        ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + 2 * L::B_BYTES);
+                        ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, tm * kBM);
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES, &tm_bhi, full_a(s), kc, tn * BN);
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, full_a(s), kc, tn * BN);
+                    } else {
+                        const int r = fills % RAWB;
+                        const uint32_t pr = (fills / RAWB) & 1u;
+                        if (!wait_phase(free_b(r), pr ^ 1u, limit, abort_flag, args.status)) {
+                            stop = true;
+                            break;
+                        }
+                        ++fills;
+                        if (fills == (uint32_t)args.withhold) continue;
+                        ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES);
+                        ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, tm * kBM);
+                        ptx::mbar_arrive_expect_tx(full_b(r), L::RAWB_BYTES);
 #pragma unroll
-                    for (int j = 0; j < BN / 32; ++j)
-                        ptx::tma_load_2d(rawb0 + r * L::RAWB_BYTES + j * 4096, &tm_b, full_b(r),
-                                         tn * BN + 32 * j, kc);
+                        for (int j = 0; j < BN / 32; ++j)
+                            ptx::tma_load_2d(rawb0 + r * L::RAWB_BYTES + j * 4096, &tm_b, full_b(r),
+                                             tn * BN + 32 * j, kc);
+                    }
                 }
             }
             // Drain: the last fill of every slot and raw-B buffer must have landed.
@@ -164,8 +205,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             };
             for (int s = 0; s < SLOTS && (uint32_t)s < total; ++s)
                 drain(full_a(s), (total - 1 - s) / SLOTS * SLOTS + s, SLOTS);
-            for (int r = 0; r < RAWB && (uint32_t)r < total; ++r)
-                drain(full_b(r), (total - 1 - r) / RAWB * RAWB + r, RAWB);
+            if constexpr (!BPRE)
+                for (int r = 0; r < RAWB && (uint32_t)r < total; ++r)
+                    drain(full_b(r), (total - 1 - r) / RAWB * RAWB + r, RAWB);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -236,16 +278,27 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         }
     } else {
         // ------------------------------ converters ----------------------------
-        const int ct = threadIdx.x - 6 * 32;  // 0 .. 127
+        const int ct = threadIdx.x - 6 * 32;  // 0 .. kConvThreads-1
+        const int cw = ct >> 5;               // k group of this warp: k = 4*cw .. 4*cw+3
         uint32_t fills = 0;
         bool stop = false;
+        // Offsets inside a raw-B box of the four k rows this lane reads (row k,
+        // chunk (lane/4) ^ (k%8), word lane%4): fixed for the whole kernel.
+        uint32_t box_off[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = cw * 4 + j;
+            box_off[j] = (uint32_t)(k * 128 + (((lane >> 2) ^ (k & 7)) << 4) + (lane & 3) * 4);
+        }
         for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
             const Unit u = decode_unit(w, args);
             for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
-                const int s = fills % SLOTS, r = fills % RAWB;
-                const uint32_t ps = (fills / SLOTS) & 1u, pr = (fills / RAWB) & 1u;
+                const int s = fills % SLOTS;
+                const uint32_t ps = (fills / SLOTS) & 1u;
+                const int r = BPRE ? 0 : fills % (BPRE ? 1 : RAWB);
+                const uint32_t pr = BPRE ? 0u : (fills / (BPRE ? 1 : RAWB)) & 1u;
                 if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status) ||
-                    !wait_phase(full_b(r), pr, limit, abort_flag, args.status)) {
+                    (!BPRE && !wait_phase(full_b(r), pr, limit, abort_flag, args.status))) {
                     stop = true;
                     break;
                 }
@@ -256,43 +309,31 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 uint8_t* b_lo = b_hi + L::B_BYTES;
                 const uint8_t* b_raw = ring_ptr + SLOTS * L::SLOT_BYTES + r * L::RAWB_BYTES;
                 // A: lo beside the raw tile, same swizzled position, 16 bytes at a time.
-#pragma unroll 4
+#pragma unroll
                 for (int c = ct; c < L::A_BYTES / 16; c += kConvThreads) {
                     const float4 x = *reinterpret_cast<const float4*>(a_raw + c * 16);
-                    float4 l;
-                    l.x = tf32_rne(x.x - tf32_trunc(x.x));
-                    l.y = tf32_rne(x.y - tf32_trunc(x.y));
-                    l.z = tf32_rne(x.z - tf32_trunc(x.z));
-                    l.w = tf32_rne(x.w - tf32_trunc(x.w));
-                    *reinterpret_cast<float4*>(a_lo + c * 16) = l;
+                    *reinterpret_cast<float4*>(a_lo + c * 16) =
+                        make_float4(lo_part(x.x), lo_part(x.y), lo_part(x.z), lo_part(x.w));
                 }
-                // B: transpose 32-column boxes (row k = 128 B of n, chunk (n%32/4) ^ (k%8))
-                // into K-major rows n (chunk k/4 ^ (n%8)).  A warp takes 32
-                // consecutive n and one 4-wide k group: conflict-free reads along
-                // a box row, conflict-free 16-byte writes across 8 swizzled rows.
+                // B: transpose 32-column boxes into K-major rows.  This warp owns
+                // k = 4*cw..4*cw+3; lane = n within a box: the reads of a box row
+                // are conflict-free, and the 16-byte writes of 8 consecutive rows
+                // land in 8 different swizzled chunks.
 #pragma unroll 2
-                for (int q = ct; q < BN * 8; q += kConvThreads) {
-                    const int ln = q & 31, grp = q >> 5;
-                    const int kq = grp & 7, nb = grp >> 3;
-                    const int n = nb * 32 + ln;
+                for (int nb = 0; nb < (BPRE ? 0 : BN / 32); ++nb) {
                     const uint8_t* box = b_raw + nb * 4096;
                     float v[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int k = kq * 4 + j;
-                        v[j] = *reinterpret_cast<const float*>(box + k * 128 + ((((ln >> 2) ^ (k & 7))) << 4) +
-                                                               (ln & 3) * 4);
-                    }
-                    const uint32_t o = kmajor_off(n, kq);
+                    for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const float*>(box + box_off[j]);
+                    const uint32_t o = kmajor_off(nb * 32 + lane, cw);
                     *reinterpret_cast<float4*>(b_hi + o) = make_float4(v[0], v[1], v[2], v[3]);
                     *reinterpret_cast<float4*>(b_lo + o) =
-                        make_float4(tf32_rne(v[0] - tf32_trunc(v[0])), tf32_rne(v[1] - tf32_trunc(v[1])),
-                                    tf32_rne(v[2] - tf32_trunc(v[2])), tf32_rne(v[3] - tf32_trunc(v[3])));
+                        make_float4(lo_part(v[0]), lo_part(v[1]), lo_part(v[2]), lo_part(v[3]));
                 }
                 ptx::fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::mbar_arrive(free_b(r));
+                    if (!BPRE) ptx::mbar_arrive(free_b(r));
                     ptx::mbar_arrive(conv(s));
                 }
             }
@@ -310,7 +351,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 
 template <int BN, int SLOTS, int RAWB>
 cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
-                         cudaStream_t s)
+                         const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
 {
     using L = FusedLayout<BN, SLOTS, RAWB>;
     auto kern = tc_fused_kernel<BN, SLOTS, RAWB>;
@@ -322,17 +363,25 @@ cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorM
     }
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
-    return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, ta, tb, a);
+    return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, ta, tb, tbhi, tblo, a);
 }
 
 }  // namespace
 
-cudaError_t tc_fused_main(int bn, const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
-                          const CUtensorMap& tb, cudaStream_t s)
+cudaError_t tc_fused_main(int bn, bool b_presplit, const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
+                          const CUtensorMap& tb, const CUtensorMap& tbhi, const CUtensorMap& tblo,
+                          cudaStream_t s)
 {
+    if (b_presplit) {
+        switch (bn) {
+        case 128: return launch_fused<128, 3, 0>(st, a, ta, tb, tbhi, tblo, s);
+        case 256: return launch_fused<256, 2, 0>(st, a, ta, tb, tbhi, tblo, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (bn) {
-    case 128: return launch_fused<128, 3, 2>(st, a, ta, tb, s);
-    case 256: return launch_fused<256, 2, 1>(st, a, ta, tb, s);
+    case 128: return launch_fused<128, 3, 2>(st, a, ta, tb, tbhi, tblo, s);
+    case 256: return launch_fused<256, 2, 1>(st, a, ta, tb, tbhi, tblo, s);
     default: return cudaErrorInvalidValue;
     }
 }

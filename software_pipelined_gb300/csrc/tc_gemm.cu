@@ -511,42 +511,45 @@ cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s
 using LaunchFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
 struct TcEntry {
     TcConfig cfg;
-    LaunchFn main;    // NULL for fused configurations (tc_fused_main)
+    LaunchFn main;    // NULL where the split happens in the kernel (tc_fused_main)
     LaunchFn reduce;
 };
 const TcEntry kTc[] = {
     // the ring as deep as shared memory allows, per tile width
-    {{128, 128, 32, 3, false, false}, launch_main<128, 3>, launch_reduce<128>},
-    {{128, 256, 32, 2, false, false}, launch_main<256, 2>, launch_reduce<256>},
-    {{128, 64, 32, 4, false, false}, launch_main<64, 4>, launch_reduce<64>},
+    {{128, 128, 32, 3, false, kSplitPrepass}, launch_main<128, 3>, launch_reduce<128>},
+    {{128, 256, 32, 2, false, kSplitPrepass}, launch_main<256, 2>, launch_reduce<256>},
+    {{128, 64, 32, 4, false, kSplitPrepass}, launch_main<64, 4>, launch_reduce<64>},
     // pipeline-depth ablation: single-buffered (1) and shallower rings
-    {{128, 256, 32, 1, false, false}, launch_main<256, 1>, launch_reduce<256>},
-    {{128, 128, 32, 1, false, false}, launch_main<128, 1>, launch_reduce<128>},
-    {{128, 128, 32, 2, false, false}, launch_main<128, 2>, launch_reduce<128>},
-    {{128, 64, 32, 2, false, false}, launch_main<64, 2>, launch_reduce<64>},
+    {{128, 256, 32, 1, false, kSplitPrepass}, launch_main<256, 1>, launch_reduce<256>},
+    {{128, 128, 32, 1, false, kSplitPrepass}, launch_main<128, 1>, launch_reduce<128>},
+    {{128, 128, 32, 2, false, kSplitPrepass}, launch_main<128, 2>, launch_reduce<128>},
+    {{128, 64, 32, 2, false, kSplitPrepass}, launch_main<64, 2>, launch_reduce<64>},
     // barrier-coalescing ablation: separate full barriers for A and B
-    {{128, 256, 32, 2, true, false}, launch_main<256, 2, true>, launch_reduce<256>},
-    {{128, 128, 32, 3, true, false}, launch_main<128, 3, true>, launch_reduce<128>},
+    {{128, 256, 32, 2, true, kSplitPrepass}, launch_main<256, 2, true>, launch_reduce<256>},
+    {{128, 128, 32, 3, true, kSplitPrepass}, launch_main<128, 3, true>, launch_reduce<128>},
     // operands split inside the kernel (stages = MMA-facing slots)
-    {{128, 128, 32, 3, false, true}, nullptr, launch_reduce<128>},
-    {{128, 256, 32, 2, false, true}, nullptr, launch_reduce<256>},
+    {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>},
+    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>},
+    // A split inside the kernel, B by the pre-pass
+    {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>},
+    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>},
 };
 
 }  // namespace
 
 int tc_num_configs() { return (int)(sizeof(kTc) / sizeof(kTc[0])); }
 const TcConfig& tc_config(int id) { return kTc[id].cfg; }
-int tc_find_config(int bn, int stages, bool sep, bool fused)
+int tc_find_config(int bn, int stages, bool sep, int split)
 {
     for (int i = 0; i < tc_num_configs(); ++i) {
         const TcConfig& c = kTc[i].cfg;
-        if (c.bn == bn && c.stages == stages && c.sep == sep && c.fused == fused) return i;
+        if (c.bn == bn && c.stages == stages && c.sep == sep && c.split == split) return i;
     }
     // Stage count 0: the first (deepest) ring compiled for this tile width.
     if (stages == 0)
         for (int i = 0; i < tc_num_configs(); ++i) {
             const TcConfig& c = kTc[i].cfg;
-            if (c.bn == bn && c.sep == sep && c.fused == fused) return i;
+            if (c.bn == bn && c.sep == sep && c.split == split) return i;
         }
     return -1;
 }
@@ -628,40 +631,49 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
 
     int id = st.config_id;
     const TcConfig& c = kTc[id].cfg;
-    const bool aligned = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
+    const bool a_ok = reinterpret_cast<uintptr_t>(A) % 16 == 0;
+    const bool b_ok = reinterpret_cast<uintptr_t>(B) % 16 == 0;
+    const bool in_kernel = (c.split == kSplitInKernel && a_ok && b_ok) || (c.split == kSplitHybrid && a_ok);
     cudaError_t e = cudaSuccess;
     if (ev) cudaEventRecord(ev[0], s);
-    if (c.fused && aligned) {
-        // Raw operands straight from the caller's buffers: no pre-pass.
-        if (A != st.raw_a) {
-            if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda)) != cudaSuccess) return e;
-            st.raw_a = A;
-        }
-        if (B != st.raw_b) {
-            if ((e = encode_raw_b(st.tmap_b_raw, B, K, N, ldb)) != cudaSuccess) return e;
-            st.raw_b = B;
-        }
-        if (ev) cudaEventRecord(ev[1], s);
-        e = tc_fused_main(c.bn, st, a, *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
-                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw), s);
-    } else {
-        if (c.fused) id = st.fallback_config_id;
-        // 1. Split both operands (B transposed) into the plan's scratch, one launch.
-        const int vec_a = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
-        const int vec_b = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
-        const int a_blocks = grid_cap(M * (st.kp / 4), st.num_sms);
+    const int vec_a = (lda % 4 == 0) && a_ok;
+    const int vec_b = (ldb % 4 == 0) && b_ok;
+    if (!in_kernel || c.split == kSplitHybrid) {
+        // 1. The pre-pass: hi/lo of B (transposed) and, unless A is split in
+        // the kernel, of A, into the plan's scratch; one launch.
+        if (!in_kernel && c.split != kSplitPrepass) id = st.fallback_config_id;
+        const int a_blocks = in_kernel ? 0 : grid_cap(M * (st.kp / 4), st.num_sms);
         const int64_t b_blocks = (st.kp / kSplitBK) * ((N + kSplitBN - 1) / kSplitBN);
         split_operands_kernel<<<(unsigned)(a_blocks + b_blocks), 256, 0, s>>>(
             A, M, K, lda, vec_a, B, N, ldb, vec_b, st.kp, reinterpret_cast<float4*>(st.a_hi),
             reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        // 2. The pipelined tensor-core GEMM.
-        if (ev) cudaEventRecord(ev[1], s);
+    }
+    if (ev) cudaEventRecord(ev[1], s);
+    if (in_kernel) {
+        // 2. Raw operands straight from the caller's buffers.
+        if (A != st.raw_a) {
+            if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda)) != cudaSuccess) return e;
+            st.raw_a = A;
+        }
+        if (c.split == kSplitInKernel && B != st.raw_b) {
+            if ((e = encode_raw_b(st.tmap_b_raw, B, K, N, ldb)) != cudaSuccess) return e;
+            st.raw_b = B;
+        }
+        e = tc_fused_main(c.bn, c.split == kSplitHybrid, st, a,
+                          *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
+                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw),
+                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
+                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), s);
+    } else {
+        // 2. The pipelined tensor-core GEMM on the split operands.
         e = kTc[id].main(st, a, s);
     }
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);
-    // 3. Fixed-order sum of the split tiles' K-slices.
+    // 3. Fixed-order sum of the split tiles' K-slices, over all SMs.  (Summing
+    // in the CTA that finishes a tile's last slice was measured slower: one
+    // CTA's four epilogue warps are latency-bound on the slices' L2 reads.)
     if (st.split_tiles > 0) e = kTc[id].reduce(st, a, s);
     if (ev) cudaEventRecord(ev[3], s);
     return e;

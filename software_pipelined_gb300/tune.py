@@ -77,7 +77,7 @@ def candidates(M, N, K):
                     out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp))
     if K >= 16:
         for bn in TC_BN:
-            for fused in ((1, 2) if bn in (128, 256) and K >= 32 else (1,)):
+            for fused in ((1, 2, 3) if bn in (128, 256) and K >= 32 else (1,)):
                 for sp in [0] + SPLITS:
                     if sp <= 1 or (K + 31) // 32 >= sp:
                         out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp,
@@ -138,6 +138,11 @@ def effective_split(desc: str) -> int:
     return 0 if whole > 0 else slices
 
 
+def split_where(desc: str) -> int:
+    """The table's last field: 0 pre-pass, 1 in the kernel, 2 hybrid."""
+    return 1 if "in-kernel-split" in desc else 2 if "hybrid-split" in desc else 0
+
+
 def write_inc(results, path):
     lines = [
         "// Per-shape dispatch table: the fastest configuration measured on GB300 for",
@@ -146,7 +151,7 @@ def write_inc(results, path):
         "// fall back to the rule in choose().  Fields: variant (1 SIMT, 2 tcgen05),",
         "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
-        "// fused (tcgen05: 1 = operands split inside the kernel).",
+        "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass).",
         "struct TableRow {",
         "    int64_t M, N, K;",
         "    DispatchChoice c;",
@@ -158,7 +163,7 @@ def write_inc(results, path):
         o = r["best"]["opts"]
         split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
-                     f"{o['stages']}, {split}, {1 if 'in-kernel-split' in r['best']['plan'] else 0}}}}},"
+                     f"{o['stages']}, {split}, {split_where(r['best']['plan'])}}}}},"
                      f"  // {r['best']['us']} us")
     lines += [
         "    {0, 0, 0, {0, 0, 0, 0, 0, 0}},  // sentinel",

@@ -259,51 +259,61 @@ def test_large_squares_sampled(w):
 # ---------------------------------------------------------------------------
 
 FUSED = {"variant": g.VARIANT_TCGEN05, "operand_split": 2}
+HYBRID = {"variant": g.VARIANT_TCGEN05, "operand_split": 3}
+MODES = [(FUSED, "in-kernel-split"), (HYBRID, "hybrid-split")]
 
 
+@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("split", [1, 2, 0])
-def test_in_kernel_split_configs(bn, split):
+def test_in_kernel_split_configs(bn, split, mode):
     # Ragged M and N (last B box partly outside N), K not a multiple of 32, more
     # k-blocks than slots; split 0 = the dispatcher's split policy.
+    opts, tag = mode
     M, N, K = 2 * 128 + 17, 3 * bn + 9, 32 * 11 + 4
     A = inputs.uniform_pm1(1601, M, K)
     B = inputs.normal(1602, K, N)
     # B's rows must be 16-byte aligned for the TMA copy of raw B: pad ldb
-    C, desc, canaries, outs = run_gemm(A, B, repeat=2, tile_n=bn, split_k=split, ldb=N + (-N % 4), **FUSED)
-    assert "in-kernel-split" in desc, desc
+    ldb = N + (-N % 4) if opts is FUSED else N
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, tile_n=bn, split_k=split, ldb=ldb, **opts)
+    assert tag in desc, desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
     assert np.array_equal(outs[0], outs[1]), desc
 
 
-def test_in_kernel_split_many_tiles_and_tail_wave():
+@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+def test_in_kernel_split_many_tiles_and_tail_wave(mode):
     M, N, K = 128 * 21, 256 * 9 + 68, 512
     A = inputs.uniform_pm1(1603, M, K)
     B = inputs.uniform_pm1(1604, K, N)
-    C, desc, canaries, _ = run_gemm(A, B, tile_n=256, **FUSED)
+    C, desc, canaries, _ = run_gemm(A, B, tile_n=256, **mode[0])
+    assert mode[1] in desc, desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
 
 
-def test_in_kernel_split_padded_and_misaligned_fallback():
-    # lda, ldb multiples of 4 (a fused plan), but base pointers 4 bytes off a
-    # 16-byte boundary: the run falls back to the pre-split kernel.
+@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+def test_in_kernel_split_padded_and_misaligned_fallback(mode):
+    # lda, ldb multiples of 4 (an in-kernel plan), but base pointers 4 bytes off
+    # a 16-byte boundary: the run falls back to the pre-split kernel.
     M, N, K = 300, 260, 96
     A = inputs.uniform_pm1(1605, M, K)
     B = inputs.uniform_pm1(1606, K, N)
-    for kw in (dict(lda=K + 4, ldb=N + 4, ldc=N + 3), dict(a_off=1, b_off=1, c_off=1)):
-        C, desc, canaries, _ = run_gemm(A, B, **FUSED, **kw)
-        assert "in-kernel-split" in desc
+    for kw in (dict(lda=K + 4, ldb=N + 4, ldc=N + 3), dict(a_off=1, b_off=1, c_off=1),
+               dict(b_off=1), dict(a_off=1)):
+        C, desc, canaries, _ = run_gemm(A, B, **mode[0], **kw)
+        assert mode[1] in desc
         err, ok = check_against_oracle(C, A, B)
         assert canaries and ok, f"{kw} {desc}: {err}"
 
 
-def test_in_kernel_split_small_integers_bit_exact():
+@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+def test_in_kernel_split_small_integers_bit_exact(mode):
     M, N, K = 200, 300, 1000
     A = inputs.small_int(1607, M, K)
     B = inputs.small_int(1608, K, N)
-    C, desc, canaries, _ = run_gemm(A, B, **FUSED)
+    C, desc, canaries, _ = run_gemm(A, B, **mode[0])
     Cref, _ = oracle.gemm_f64(A, B)
     assert canaries and np.array_equal(C, Cref), desc
 
@@ -318,14 +328,21 @@ def test_in_kernel_split_refusals():
     with pytest.raises(g.GemmError) as ei:
         g.Plan(64, 64, 64, variant=g.VARIANT_TCGEN05, operand_split=2, tile_n=64)  # no fused 64-wide
     assert ei.value.status == g.ERR_UNSUPPORTED
+    with pytest.raises(g.GemmError) as ei:
+        g.Plan(64, 64, 61, variant=g.VARIANT_TCGEN05, operand_split=3)      # lda = 61
+    assert ei.value.status == g.ERR_UNSUPPORTED
+    # hybrid takes any ldb
+    with g.Plan(64, 61, 64, variant=g.VARIANT_TCGEN05, operand_split=3) as p:
+        assert "hybrid-split" in p.describe()
 
 
-def test_in_kernel_split_negative_control():
+@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+def test_in_kernel_split_negative_control(mode):
     M, N, K = 256, 256, 32
     A = inputs.uniform_pm1(1609, M, K)
     B = inputs.uniform_pm1(1610, K, N)
-    C1, _, _, _ = run_gemm(A, B, tf32_terms=1, **FUSED)
-    C3, _, _, _ = run_gemm(A, B, **FUSED)
+    C1, _, _, _ = run_gemm(A, B, tf32_terms=1, **mode[0])
+    C3, _, _, _ = run_gemm(A, B, **mode[0])
     e1, ok1 = check_against_oracle(C1, A, B)
     e3, ok3 = check_against_oracle(C3, A, B)
     assert not ok1 and e1 > 4, e1
