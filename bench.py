@@ -379,7 +379,8 @@ def run_gpu_arm(args):
     bk = per_kernel[big["name"]]
     achieved = bk["main_tflops"]
     peak = pk["f32_3xtf32_tflops_burst"]
-    kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", "tc_gemm.cu")])
+    kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", f)
+                             for f in ("tc_gemm.cu", "tc_common.cuh", "ptx.cuh")])
     traffic, traffic_src = traffic_for(kern_hash)
     for w in work:
         t = traffic.get(w["name"]) if traffic else None
@@ -444,6 +445,7 @@ def run_gpu_arm(args):
     # ---- per shape: every configuration's shapes ----------------------------
     per_shape = None
     floors = None
+    batched = None
     if rank == 0 and not args.no_per_shape:
         per_shape = []
         from software_pipelined_gb300 import inputs
@@ -472,10 +474,17 @@ def run_gpu_arm(args):
                 t_roof = max(fl / (P * 1e12), byts / (pk["hbm_gbs"] * 1e9))
                 t_roof_simt = max(fl / (pk["f32_simt_tflops_nominal"] * 1e12), byts / (pk["hbm_gbs"] * 1e9))
                 err, how = (None, None) if args.quick else parity(A, B, dC)
+                # comparison column, off the measured path: PyTorch's FP32 matmul
+                # (cuBLAS SGEMM, TF32 disabled) timed the same way
+                torch.backends.cuda.matmul.allow_tf32 = False
+                dC2 = torch.empty_like(dC)
+                cb, _, _, _ = time_graph(lambda st, a=dA, b=dB, c=dC2: torch.mm(a, b, out=c))
+                del dC2
                 per_shape.append({
                     "config": key, "shape": name, "plan": plan.describe(),
                     "us": round(med * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
                     "us_direct_launch": round(s_med * 1e3, 3),
+                    "torch_fp32_matmul_us": round(cb * 1e3, 3),
                     "phases_us_split_main_reduce": ph,
                     "tflops": round(fl / (med * 1e-3) / 1e12, 3),
                     "roofline_frac": round(t_roof / (med * 1e-3), 4),
@@ -500,6 +509,30 @@ def run_gpu_arm(args):
         med, _, _, _ = time_batches(lambda: zp.run_ptr(0, 0, z.data_ptr(), sptr), stream)
         gmed, _, _, _ = time_graph(lambda st: zp.run_ptr(0, 0, z.data_ptr(), st))
         zp.close()
+        batched = []
+        for (bm, bn, bk, nb) in ((32, 32, 32, 1024), (128, 128, 128, 256), (64, 64, 64, 512)):
+            from software_pipelined_gb300 import inputs as _in
+            Ab = torch.from_numpy(_in.uniform_pm1(6001, nb * bm, bk)).cuda()
+            Bb = torch.from_numpy(_in.uniform_pm1(6002, nb * bk, bn)).cuda()
+            Cb = torch.empty((nb * bm, bn), dtype=torch.float32, device="cuda")
+            with g.Plan(bm, bn, bk, bk, bn, bn, batch=nb, stride_a=bm * bk, stride_b=bk * bn,
+                        stride_c=bm * bn) as bp:
+                bmed, _, _, _ = time_graph(lambda st, p=bp: p.run_ptr(Ab.data_ptr(), Bb.data_ptr(),
+                                                                       Cb.data_ptr(), st))
+                bdesc = bp.describe()
+            # spot check of the last product against the oracle
+            import oracle as _or
+            a_last = Ab[(nb - 1) * bm:].cpu().numpy()
+            b_last = Bb[(nb - 1) * bk:].cpu().numpy()
+            cr, sr = _or.gemm_f64(a_last, b_last)
+            berr = _or.normalised_error(Cb[(nb - 1) * bm:].cpu().numpy(), cr, sr, bk)
+            fl = 2.0 * bm * bn * bk * nb
+            batched.append({"products": nb, "shape": f"{bm}x{bn}x{bk}", "plan": bdesc,
+                            "us_per_launch": round(bmed * 1e3, 3),
+                            "us_per_product": round(bmed * 1e3 / nb, 4),
+                            "tflops": round(fl / (bmed * 1e-3) / 1e12, 3),
+                            "max_normalised_error_last_product": round(berr, 4)})
+            del Ab, Bb, Cb
         floors = {"event_pair_us": round(statistics.median(ts) * 1e3, 3),
                   "smallest_kernel_direct_launch_us": round(med * 1e3, 3),
                   "smallest_kernel_graph_us": round(gmed * 1e3, 3),
@@ -528,6 +561,7 @@ def run_gpu_arm(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "headline_parity": headline_parity, "per_shape": per_shape, "floors": floors,
+            "batched": batched,
             "peaks": pk, "device": dev_name,
             "library_sha256_16": source_hash([g.LIB_PATH]),
         }

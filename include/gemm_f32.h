@@ -105,7 +105,9 @@ typedef struct {
                                (needs K >= 32, lda a multiple of 4).  2 and 3 fall back to 1
                                at run time for a base pointer of A (or, for 2, B) that is
                                not 16-byte aligned */
-    int32_t reserved[5];
+    int32_t tile_group;     /* TC only: tile order of the persistent kernel, in tile-rows per
+                               raster group (1..64; 0 = the dispatcher's choice, else 8) */
+    int32_t reserved[4];
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */
@@ -133,6 +135,26 @@ GEMM_F32_API gemm_f32_status gemm_f32_plan_ex(int64_t M, int64_t N, int64_t K,
                                  const gemm_f32_opts* opts, gemm_f32_plan_t* plan);
 
 /*
+ * Plan `batch` independent products of the same shape, run by one launch:
+ * C_z = A_z * B_z for z = 0 .. batch-1, with A_z = A + z*stride_a,
+ * B_z = B + z*stride_b, C_z = C + z*stride_c (strides in elements; 0 for A or
+ * B reuses one operand for every product).  Many small GEMMs in one launch pay
+ * the launch latency once; the pages tie such small, latency-dominated
+ * products to the decode regime ("Case Study: The Double-Buffered GEMM", the
+ * three-regimes paragraph).  Runs on the SIMT kernel (no split-K).  gemm_f32_run
+ * takes the base pointers A, B, C of product 0.
+ *
+ * INVALID_ARG: as gemm_f32_plan; batch < 0 or > 65535; a negative stride; or
+ * stride_c smaller than one C (the outputs would overlap).  batch == 0 is an
+ * empty problem.  opts may be NULL; its variant must be AUTO or SIMT.
+ */
+GEMM_F32_API gemm_f32_status gemm_f32_plan_batched(int64_t M, int64_t N, int64_t K,
+                                                   int64_t lda, int64_t ldb, int64_t ldc,
+                                                   int64_t batch, int64_t stride_a, int64_t stride_b,
+                                                   int64_t stride_c, const gemm_f32_opts* opts,
+                                                   gemm_f32_plan_t* plan);
+
+/*
  * Enqueue C = A*B on `stream`.  A, B, C are device pointers with the plan's
  * shapes and leading dimensions.  Asynchronous: returns after the launches are
  * queued; nothing is synchronised.  INVALID_ARG for a NULL plan or a NULL
@@ -147,7 +169,7 @@ GEMM_F32_API gemm_f32_status gemm_f32_run(gemm_f32_plan_t plan, const float* A, 
  * (allocated on first use), runs, copies C back to host memory and
  * synchronises `stream`.  For pinned host memory the copies are asynchronous
  * DMA; pageable memory works but is slower.  Returns the run's status, or
- * TIMEOUT if a device-side wait ran out.
+ * TIMEOUT if a device-side wait ran out; UNSUPPORTED for a batched plan.
  */
 GEMM_F32_API gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t plan, const float* A_host,
                                   const float* B_host, float* C_host,

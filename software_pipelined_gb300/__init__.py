@@ -26,7 +26,7 @@ EXPORTED = ("gemm_f32_opts_init", "gemm_f32_plan", "gemm_f32_plan_ex", "gemm_f32
             "gemm_f32_run_host", "gemm_f32_check", "gemm_f32_plan_destroy",
             "gemm_f32_plan_describe", "gemm_f32_plan_workspace_bytes", "gemm_f32_status_string",
             "gemm_f32_version", "gemm_f32_plan_kernel_launches", "gemm_f32_trace_enable",
-            "gemm_f32_trace_read", "gemm_f32_run_splitk_noalloc")
+            "gemm_f32_trace_read", "gemm_f32_run_splitk_noalloc", "gemm_f32_plan_batched")
 
 
 class GemmError(RuntimeError):
@@ -41,7 +41,7 @@ class Opts(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32), ("tf32_terms", ctypes.c_int32),
                 ("wait_timeout_cycles", ctypes.c_int64), ("debug_withhold_stage", ctypes.c_int32),
                 ("separate_syncs", ctypes.c_int32), ("operand_split", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("tile_group", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
 
 _lock = threading.Lock()
@@ -91,6 +91,9 @@ def load(path: str | None = None):
         lib.gemm_f32_run_splitk_noalloc.argtypes = [i64, i64, i64, i64, i64, i64, vp, vp, vp,
                                                     ctypes.c_int32, vp]
         lib.gemm_f32_run_splitk_noalloc.restype = st
+        lib.gemm_f32_plan_batched.argtypes = [i64, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                              ctypes.POINTER(Opts), ctypes.POINTER(vp)]
+        lib.gemm_f32_plan_batched.restype = st
         _lib = lib
         return lib
 
@@ -116,6 +119,13 @@ def gemm_f32_plan_ex(M, N, K, lda, ldb, ldc, opts: Opts | None):
     h = ctypes.c_void_p()
     s = load().gemm_f32_plan_ex(M, N, K, lda, ldb, ldc, ctypes.byref(opts) if opts is not None else None,
                                 ctypes.byref(h))
+    return s, h.value
+
+
+def gemm_f32_plan_batched(M, N, K, lda, ldb, ldc, batch, stride_a, stride_b, stride_c, opts: Opts | None):
+    h = ctypes.c_void_p()
+    s = load().gemm_f32_plan_batched(M, N, K, lda, ldb, ldc, batch, stride_a, stride_b, stride_c,
+                                     ctypes.byref(opts) if opts is not None else None, ctypes.byref(h))
     return s, h.value
 
 
@@ -193,7 +203,8 @@ class Plan:
 
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, *, variant=VARIANT_AUTO, tile_m=0,
                  tile_n=0, stages=0, split_k=0, tf32_terms=0, wait_timeout_cycles=0,
-                 debug_withhold_stage=0, separate_syncs=0, operand_split=0):
+                 debug_withhold_stage=0, separate_syncs=0, operand_split=0, tile_group=0, batch=None,
+                 stride_a=0, stride_b=0, stride_c=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.lda = int(lda if lda is not None else max(K, 1))
         self.ldb = int(ldb if ldb is not None else max(N, 1))
@@ -204,9 +215,14 @@ class Plan:
         o.debug_withhold_stage = debug_withhold_stage
         o.separate_syncs = separate_syncs
         o.operand_split = operand_split
-        s, h = gemm_f32_plan_ex(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, o)
+        o.tile_group = tile_group
+        if batch is None:
+            s, h = gemm_f32_plan_ex(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, o)
+        else:
+            s, h = gemm_f32_plan_batched(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, int(batch),
+                                         int(stride_a), int(stride_b), int(stride_c), o)
         if s != OK:
-            raise GemmError(s, "gemm_f32_plan_ex")
+            raise GemmError(s, "gemm_f32_plan_ex" if batch is None else "gemm_f32_plan_batched")
         self.handle = h
 
     def describe(self) -> str:

@@ -31,6 +31,7 @@ struct DispatchChoice {
     int variant;   // GEMM_F32_VARIANT_SIMT / _TCGEN05
     int tile_m, tile_n, stages, split_k;
     int fused;     // TC: where the split happens (kSplitPrepass / kSplitInKernel / kSplitHybrid)
+    int group;     // TC: tile-rows per raster group (0 = default)
 };
 
 #include "dispatch_table.inc"
@@ -43,7 +44,8 @@ struct gemm_f32_plan_s {
     int device = -1;
     int kind = kNoop;
     int num_sms = 0;
-    // SIMT path
+    // SIMT path (batch > 1: strided batch of independent products)
+    int64_t batch = 1, stride_a = 0, stride_b = 0, stride_c = 0;
     int simt_id = -1;
     int split_k = 1;
     int64_t k_chunk = 0;
@@ -102,6 +104,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
     if (o.operand_split < 0 || o.operand_split > 3) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -259,6 +262,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             t.num_sms = p->num_sms;
             t.timeout_cycles = o.wait_timeout_cycles;
             t.withhold_stage = o.debug_withhold_stage;
+            t.tile_group = o.tile_group ? o.tile_group : c.group;
             tc_configure(t, M, N, K, c.split_k);
             ahi_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             alo_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
@@ -340,6 +344,47 @@ gemm_f32_status gemm_f32_plan_ex(int64_t M, int64_t N, int64_t K, int64_t lda, i
     return make_plan(M, N, K, lda, ldb, ldc, opts, plan);
 }
 
+gemm_f32_status gemm_f32_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                      int64_t ldc, int64_t batch, int64_t stride_a, int64_t stride_b,
+                                      int64_t stride_c, const gemm_f32_opts* opts, gemm_f32_plan_t* plan)
+{
+    if (!plan) return GEMM_F32_ERR_INVALID_ARG;
+    *plan = nullptr;
+    if (batch < 0 || batch > 65535 || stride_a < 0 || stride_b < 0 || stride_c < 0)
+        return GEMM_F32_ERR_INVALID_ARG;
+    gemm_f32_status st = validate_dims(M, N, K, lda, ldb, ldc);
+    if (st != GEMM_F32_OK) return st;
+    if (batch > 1 && M > 0 && N > 0 && stride_c < (M - 1) * ldc + N) return GEMM_F32_ERR_INVALID_ARG;
+    gemm_f32_opts o{};
+    if (opts) o = *opts;
+    if (o.variant != GEMM_F32_VARIANT_AUTO && o.variant != GEMM_F32_VARIANT_SIMT) return GEMM_F32_ERR_UNSUPPORTED;
+    if (batch <= 1 || M == 0 || N == 0) {
+        // one product (or none): an ordinary plan
+        if (batch == 0) return make_plan(0, N, K, lda, ldb, ldc, &o, plan);
+        o.variant = o.variant ? o.variant : GEMM_F32_VARIANT_AUTO;
+        return make_plan(M, N, K, lda, ldb, ldc, &o, plan);
+    }
+    // SIMT tile for the per-product shape; no split-K (the batch fills the GPU).
+    o.variant = GEMM_F32_VARIANT_SIMT;
+    if (!o.tile_m || !o.tile_n) {
+        const int64_t d = M > N ? M : N;
+        o.tile_m = o.tile_n = d <= 32 ? 32 : d <= 64 ? 64 : 128;
+        if (!o.stages) o.stages = d <= 32 ? 1 : 2;
+    }
+    if (!o.stages) o.stages = 2;
+    o.split_k = 1;
+    st = make_plan(M, N, K, lda, ldb, ldc, &o, plan);
+    if (st != GEMM_F32_OK) return st;
+    gemm_f32_plan_s* p = *plan;
+    p->batch = batch;
+    p->stride_a = stride_a;
+    p->stride_b = stride_b;
+    p->stride_c = stride_c;
+    const size_t len = strlen(p->desc);
+    snprintf(p->desc + len, sizeof p->desc - len, " batch=%lld", (long long)batch);
+    return GEMM_F32_OK;
+}
+
 gemm_f32_status gemm_f32_run(gemm_f32_plan_t p, const float* A, const float* B, float* C,
                              gemm_f32_stream_t stream)
 {
@@ -354,7 +399,8 @@ gemm_f32_status gemm_f32_run(gemm_f32_plan_t p, const float* A, const float* B, 
     switch (p->kind) {
     case kZeroFill:
         if (ev) { cudaEventRecord(ev[0], s); cudaEventRecord(ev[1], s); }
-        e = zero_fill_launch(C, p->M, p->N, p->ldc, s);
+        for (int64_t z = 0; z < p->batch && e == cudaSuccess; ++z)
+            e = zero_fill_launch(C + z * p->stride_c, p->M, p->N, p->ldc, s);
         if (ev) { cudaEventRecord(ev[2], s); cudaEventRecord(ev[3], s); }
         break;
     case kSimt: {
@@ -362,6 +408,7 @@ gemm_f32_status gemm_f32_run(gemm_f32_plan_t p, const float* A, const float* B, 
         a.M = p->M; a.N = p->N; a.K = p->K;
         a.A = A; a.lda = p->lda; a.B = B; a.ldb = p->ldb; a.C = C; a.ldc = p->ldc;
         a.split_k = p->split_k; a.k_chunk = p->k_chunk; a.partial = p->partial; a.ldp = p->ldp;
+        a.batch = p->batch; a.stride_a = p->stride_a; a.stride_b = p->stride_b; a.stride_c = p->stride_c;
         if (ev) { cudaEventRecord(ev[0], s); cudaEventRecord(ev[1], s); }
         e = simt_launch(p->simt_id, a, s);
         if (ev) cudaEventRecord(ev[2], s);
@@ -385,6 +432,7 @@ gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t p, const float* A_host, const 
     if (!p) return GEMM_F32_ERR_INVALID_ARG;
     if (p->kind == kNoop) return GEMM_F32_OK;
     if (!C_host || (p->K > 0 && (!A_host || !B_host))) return GEMM_F32_ERR_INVALID_ARG;
+    if (p->batch > 1) return GEMM_F32_ERR_UNSUPPORTED;
     if (!current_device_is(p->device)) return GEMM_F32_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t a_bytes = p->K > 0 ? size_t(p->M) * size_t(p->lda) * sizeof(float) : 0;
@@ -461,7 +509,7 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
 {
     if (!p) return -1;
     switch (p->kind) {
-    case kZeroFill: return 1;
+    case kZeroFill: return (int)p->batch;
     case kSimt: return p->split_k > 1 ? 2 : 1;
     case kTc: {
         // the pre-pass (unless both operands are split in the kernel), the GEMM,

@@ -29,6 +29,10 @@ struct SimtArgs {
     int64_t k_chunk;      // K per split (multiple of bk)
     float* partial;       // split_k x M x ldp
     int64_t ldp;
+    // Strided batch (split_k == 1): grid z runs `batch` independent products,
+    // problem z at A + z*stride_a, B + z*stride_b, C + z*stride_c.
+    int64_t batch = 1;
+    int64_t stride_a = 0, stride_b = 0, stride_c = 0;
 };
 cudaError_t simt_launch(int config_id, const SimtArgs& a, cudaStream_t s);
 
@@ -87,6 +91,7 @@ struct TcPlanState {
     int num_sms = 0;
     int64_t timeout_cycles = 0;
     int withhold_stage = 0;
+    int tile_group = 0;        // tile-rows per raster group (0 = default)
     // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.

@@ -61,12 +61,13 @@ simt_gemm_kernel(SimtArgs a)
     const int tx = tid % TX, ty = tid / TX;
     const int64_t m0 = (int64_t)blockIdx.y * BM;
     const int64_t n0 = (int64_t)blockIdx.x * BN;
-    const int64_t kbeg = (int64_t)blockIdx.z * a.k_chunk;
-    const int64_t kend = min(a.K, kbeg + a.k_chunk);
+    const bool batched = a.batch > 1;
+    const int64_t kbeg = batched ? 0 : (int64_t)blockIdx.z * a.k_chunk;
+    const int64_t kend = batched ? a.K : min(a.K, kbeg + a.k_chunk);
     const int nk = kend > kbeg ? (int)((kend - kbeg + BK - 1) / BK) : 0;
     const int64_t M = a.M, N = a.N;
-    const float* __restrict__ A = a.A;
-    const float* __restrict__ B = a.B;
+    const float* __restrict__ A = a.A + (batched ? (int64_t)blockIdx.z * a.stride_a : 0);
+    const float* __restrict__ B = a.B + (batched ? (int64_t)blockIdx.z * a.stride_b : 0);
 
     // Issue the cp.async copies of K-tile t into ring slot st.  Out-of-range
     // elements (ragged M, N or K) are zero-filled by the copy itself.
@@ -234,7 +235,7 @@ simt_gemm_kernel(SimtArgs a)
         ld = a.ldp;
         vec = true;
     } else {
-        out = a.C;
+        out = a.C + (batched ? (int64_t)blockIdx.z * a.stride_c : 0);
         ld = a.ldc;
         vec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
     }
@@ -270,7 +271,8 @@ cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM), (unsigned)a.split_k);
+    dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
+              (unsigned)(a.batch > 1 ? a.batch : a.split_k));
     kern<<<grid, KT::NT, KT::SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
@@ -278,8 +280,10 @@ cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
 template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false>
 cudaError_t launch_cfg(const SimtArgs& a, cudaStream_t s)
 {
-    const bool va = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0);
-    const bool vb = (a.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0);
+    const bool va = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) &&
+                    (a.batch <= 1 || a.stride_a % 4 == 0);
+    const bool vb = (a.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
+                    (a.batch <= 1 || a.stride_b % 4 == 0);
     if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP>(a, s);
     if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP>(a, s);
     if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP>(a, s);

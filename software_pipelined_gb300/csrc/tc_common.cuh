@@ -36,6 +36,7 @@ struct TcArgs {
     int kb_per_split;
     int terms;           // 3 = 3xTF32, 1 = hi*hi only
     int withhold;        // test hook: 1-based fill index the producer skips (0 = none)
+    int group;           // tile-rows per raster group of the tile order
 };
 
 // One unit of work of the persistent kernel: a whole tile, or one K-slice of a
@@ -134,11 +135,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int64_
     }
 }
 
-// Tile order: groups of 8 tile-rows, column-major inside a group, so the CTAs
+// Tile order: groups of G tile-rows, column-major inside a group, so the CTAs
 // running together share A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn)
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int G, int& tm, int& tn)
 {
-    constexpr int G = 8;
     const int group_size = G * tiles_n;
     const int gid = tile / group_size;
     const int first_m = gid * G;

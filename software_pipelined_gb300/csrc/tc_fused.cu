@@ -158,7 +158,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
                 const Unit u = decode_unit(w, args);
                 int tm, tn;
-                tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+                tile_coords(u.tile, args.tiles_m, args.tiles_n, args.group, tm, tn);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     const int s = fills % SLOTS;
                     const uint32_t ps = (fills / SLOTS) & 1u;
@@ -265,7 +265,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++iter) {
             const Unit u = decode_unit(w, args);
             int tm, tn;
-            tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+            tile_coords(u.tile, args.tiles_m, args.tiles_n, args.group, tm, tn);
             const int buf = iter & 1;
             const uint32_t tphase = (iter >> 1) & 1;
             if (!wait_phase(tfull(buf), tphase, limit, abort_flag, args.status)) break;

@@ -237,7 +237,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
                 const Unit u = decode_unit(w, args);
                 int tm, tn;
-                tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+                tile_coords(u.tile, args.tiles_m, args.tiles_n, args.group, tm, tn);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, limit, abort_flag, args.status)) {
                         stop = true;
@@ -341,7 +341,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++iter) {
             const Unit u = decode_unit(w, args);
             int tm, tn;
-            tile_coords(u.tile, args.tiles_m, args.tiles_n, tm, tn);
+            tile_coords(u.tile, args.tiles_m, args.tiles_n, args.group, tm, tn);
             const int buf = iter & 1;
             const uint32_t tphase = (iter >> 1) & 1;
             if (!wait_phase(tfull_bar(buf), tphase, limit, abort_flag, args.status)) break;
@@ -368,7 +368,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
 template <int BN>
 __global__ void __launch_bounds__(256)
 tile_reduce_kernel(const float4* __restrict__ partial, int dp_tiles, int split_tiles, int splits,
-                   int tiles_m, int tiles_n, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
+                   int tiles_m, int tiles_n, int group, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
 {
     pdl_wait();
     constexpr int Q = BN / 4;                 // float4 per partial row
@@ -381,7 +381,7 @@ tile_reduce_kernel(const float4* __restrict__ partial, int dp_tiles, int split_t
         const int rem = (int)(idx % PER_TILE);
         const int r = rem / Q, c = (rem % Q) * 4;
         int tm, tn;
-        tile_coords(dp_tiles + j, tiles_m, tiles_n, tm, tn);
+        tile_coords(dp_tiles + j, tiles_m, tiles_n, group, tm, tn);
         const int64_t grow = (int64_t)tm * kBM + r, gcol = (int64_t)tn * BN + c;
         if (grow >= M || gcol >= N) continue;
         const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
@@ -505,7 +505,7 @@ cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s
     const int64_t total = (int64_t)a.split_tiles * kBM * (BN / 4);
     return launch_pdl(tile_reduce_kernel<BN>, dim3(grid_cap(total, st.num_sms)), dim3(256), 0, s,
                       reinterpret_cast<const float4*>(a.partial), a.dp_tiles, a.split_tiles, a.splits,
-                      a.tiles_m, a.tiles_n, a.M, a.N, a.C, a.ldc);
+                      a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
 }
 
 using LaunchFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
@@ -628,6 +628,7 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
     a.kb_per_split = st.kb_per_split;
     a.terms = st.terms;
     a.withhold = st.withhold_stage;
+    a.group = st.tile_group > 0 ? st.tile_group : 8;
 
     int id = st.config_id;
     const TcConfig& c = kTc[id].cfg;

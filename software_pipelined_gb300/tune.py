@@ -109,6 +109,14 @@ def main():
                 except g.GemmError:
                     continue
             rows.sort(key=lambda r: r["us"])
+            if rows[0]["opts"]["variant"] == g.VARIANT_TCGEN05:
+                # the tile order of the winner: tile-rows per raster group
+                for grp in (4, 8, 12, 16, 24):
+                    c = dict(rows[0]["opts"], tile_group=grp)
+                    with g.Plan(M, N, K, **c) as p:
+                        rows.append(dict(opts=c, us=round(time_plan(p, dA, dB, dC, stream) * 1e3, 3),
+                                         plan=p.describe()))
+                rows.sort(key=lambda r: r["us"])
             with g.Plan(M, N, K) as p:
                 auto_desc = p.describe()
                 auto_us = round(time_plan(p, dA, dB, dC, stream) * 1e3, 3)
@@ -151,7 +159,8 @@ def write_inc(results, path):
         "// fall back to the rule in choose().  Fields: variant (1 SIMT, 2 tcgen05),",
         "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
-        "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass).",
+        "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass),",
+        "// tile_group (tcgen05: tile-rows per raster group, 0 = default).",
         "struct TableRow {",
         "    int64_t M, N, K;",
         "    DispatchChoice c;",
@@ -163,10 +172,10 @@ def write_inc(results, path):
         o = r["best"]["opts"]
         split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
-                     f"{o['stages']}, {split}, {split_where(r['best']['plan'])}}}}},"
+                     f"{o['stages']}, {split}, {split_where(r['best']['plan'])}, {o.get('tile_group', 0)}}}}},"
                      f"  // {r['best']['us']} us")
     lines += [
-        "    {0, 0, 0, {0, 0, 0, 0, 0, 0}},  // sentinel",
+        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0}},  // sentinel",
         "};",
         "",
         "bool table_lookup(int64_t M, int64_t N, int64_t K, DispatchChoice& out)",

@@ -115,3 +115,21 @@ def test_binding_fails_loudly_without_library(tmp_path):
     fresh.loader.exec_module(m)
     with pytest.raises(RuntimeError, match="not built"):
         m.load(str(tmp_path / "missing.so"))
+
+
+@pytest.mark.parametrize("args", [
+    (8, 8, 8, 8, 8, 8, -1, 64, 64, 64),       # negative batch
+    (8, 8, 8, 8, 8, 8, 65536, 64, 64, 64),    # beyond the grid limit
+    (8, 8, 8, 8, 8, 8, 4, -64, 64, 64),       # negative stride
+    (8, 8, 8, 8, 8, 8, 4, 64, 64, 63),        # outputs would overlap
+])
+def test_batched_plan_rejects_bad_args(lib, args):
+    s, h = g.gemm_f32_plan_batched(*args, None)
+    assert s == g.ERR_INVALID_ARG and h is None
+
+
+def test_batched_plan_rejects_tensor_core_variant(lib):
+    o = g.gemm_f32_opts_init()
+    o.variant = g.VARIANT_TCGEN05
+    s, h = g.gemm_f32_plan_batched(8, 8, 8, 8, 8, 8, 4, 64, 64, 64, o)
+    assert s == g.ERR_UNSUPPORTED and h is None
