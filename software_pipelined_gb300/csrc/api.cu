@@ -315,6 +315,19 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
     return GEMM_F32_OK;
 }
 
+// Copy a rows x cols matrix with leading dimension ld (same on both sides):
+// one linear copy when the rows are contiguous, a pitched copy otherwise
+// (so the destination's padding columns are never written).
+cudaError_t copy_rows(float* dst, const float* src, int64_t rows, int64_t cols, int64_t ld,
+                      cudaMemcpyKind kind, cudaStream_t s)
+{
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (ld == cols || rows == 1)
+        return cudaMemcpyAsync(dst, src, size_t(rows) * size_t(cols) * sizeof(float), kind, s);
+    return cudaMemcpy2DAsync(dst, size_t(ld) * sizeof(float), src, size_t(ld) * sizeof(float),
+                             size_t(cols) * sizeof(float), size_t(rows), kind, s);
+}
+
 bool current_device_is(int dev)
 {
     int d = -1;
@@ -445,19 +458,16 @@ gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t p, const float* A_host, const 
         if ((e = cudaMalloc(&p->hC, c_bytes)) != cudaSuccess) goto fail;
     }
     if (p->K > 0) {
-        e = cudaMemcpy2DAsync(p->hA, p->lda * sizeof(float), A_host, p->lda * sizeof(float),
-                              p->K * sizeof(float), p->M, cudaMemcpyHostToDevice, s);
+        e = copy_rows(p->hA, A_host, p->M, p->K, p->lda, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return from_cuda(e);
-        e = cudaMemcpy2DAsync(p->hB, p->ldb * sizeof(float), B_host, p->ldb * sizeof(float),
-                              p->N * sizeof(float), p->K, cudaMemcpyHostToDevice, s);
+        e = copy_rows(p->hB, B_host, p->K, p->N, p->ldb, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return from_cuda(e);
     }
     {
         gemm_f32_status st = gemm_f32_run(p, p->hA, p->hB, p->hC, stream);
         if (st != GEMM_F32_OK) return st;
     }
-    e = cudaMemcpy2DAsync(C_host, p->ldc * sizeof(float), p->hC, p->ldc * sizeof(float),
-                          p->N * sizeof(float), p->M, cudaMemcpyDeviceToHost, s);
+    e = copy_rows(C_host, p->hC, p->M, p->N, p->ldc, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return from_cuda(e);
     return gemm_f32_check(p, stream);
 fail:

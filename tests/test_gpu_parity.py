@@ -347,3 +347,52 @@ def test_in_kernel_split_negative_control(mode):
     e3, ok3 = check_against_oracle(C3, A, B)
     assert not ok1 and e1 > 4, e1
     assert ok3, e3
+
+
+# ---------------------------------------------------------------------------
+# Host-buffer entry point: copies in, product, copy out, synchronised.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pad", [False, True], ids=["contiguous", "padded"])
+@pytest.mark.parametrize("shape", [(300, 200, 96), (1024, 512, 640)], ids=["small", "tensor_core"])
+def test_run_host_buffers(shape, pad):
+    M, N, K = shape
+    lda, ldb, ldc = (K + 3, N + 5, N + 7) if pad else (K, N, N)
+    A = inputs.uniform_pm1(1701, M, K, ld=lda if pad else None)
+    B = inputs.uniform_pm1(1702, K, N, ld=ldb if pad else None)
+    Abuf = np.lib.stride_tricks.as_strided(A, shape=(M, lda), strides=(4 * lda, 4)) if pad else A
+    Bbuf = np.lib.stride_tricks.as_strided(B, shape=(K, ldb), strides=(4 * ldb, 4)) if pad else B
+    Cbuf = np.full((M, ldc), 321.0, dtype=np.float32)
+    with g.Plan(M, N, K, lda, ldb, ldc) as p:
+        for _ in range(2):
+            s = p.run_host(Abuf.ctypes.data, Bbuf.ctypes.data, Cbuf.ctypes.data, 0)
+            assert s == g.OK, g.gemm_f32_status_string(s)
+    Cref, S = oracle.gemm_f64(np.ascontiguousarray(A), np.ascontiguousarray(B))
+    assert oracle.within_bound(Cbuf[:, :N], Cref, S, K)
+    if pad:
+        assert (Cbuf[:, N:] == 321.0).all()
+
+
+# ---------------------------------------------------------------------------
+# Extreme aspect ratios: a very long K (many k-blocks per tile, long
+# accumulation) and a very tall, thin product.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [AUTO, SIMT, TC, FUSED], ids=["auto", "simt", "tcgen05", "in_kernel"])
+def test_long_k(variant):
+    M, N, K = 128, 96, 262144
+    A = inputs.uniform_pm1(1801, M, K)
+    B = inputs.uniform_pm1(1802, K, N)
+    C, desc, canaries, _ = run_gemm(A, B, **variant)
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+
+
+@pytest.mark.parametrize("variant", [AUTO, SIMT, TC], ids=["auto", "simt", "tcgen05"])
+def test_very_tall(variant):
+    M, N, K = 1 << 18, 24, 40
+    A = inputs.normal(1803, M, K)
+    B = inputs.normal(1804, K, N)
+    C, desc, canaries, _ = run_gemm(A, B, **variant)
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
