@@ -107,7 +107,9 @@ typedef struct {
                                not 16-byte aligned */
     int32_t tile_group;     /* TC only: tile order of the persistent kernel, in tile-rows per
                                raster group (1..64; 0 = the dispatcher's choice, else 8) */
-    int32_t reserved[4];
+    int32_t tile_k;         /* SIMT only: K-tile depth (16/32/64; 0 = the compiled default
+                               for the tile and stage count) */
+    int32_t reserved[3];
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

@@ -32,6 +32,7 @@ struct DispatchChoice {
     int tile_m, tile_n, stages, split_k;
     int fused;     // TC: where the split happens (kSplitPrepass / kSplitInKernel / kSplitHybrid)
     int group;     // TC: tile-rows per raster group (0 = default)
+    int tile_k;    // SIMT: K-tile depth (0 = compiled default)
 };
 
 #include "dispatch_table.inc"
@@ -105,6 +106,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
     if (o.operand_split < 0 || o.operand_split > 3) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -219,7 +221,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 
         if (c.variant == GEMM_F32_VARIANT_SIMT) {
             p->kind = kSimt;
-            p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages, o.separate_syncs != 0);
+            p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages, o.separate_syncs != 0,
+                                          o.tile_k ? o.tile_k : c.tile_k);
             if (p->simt_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             const int bk = simt_config(p->simt_id).bk;
             int64_t split = c.split_k < 1 ? 1 : c.split_k;

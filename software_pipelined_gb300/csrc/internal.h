@@ -18,7 +18,8 @@ struct SimtConfig {
 // Configurations compiled into the library; `id` indexes this table.
 int simt_num_configs();
 const SimtConfig& simt_config(int id);
-int simt_find_config(int bm, int bn, int stages, bool sep = false);  // -1 if none
+// bk = 0: the first compiled K-tile depth for that tile and ring.  -1 if none.
+int simt_find_config(int bm, int bn, int stages, bool sep = false, int bk = 0);
 
 struct SimtArgs {
     int64_t M, N, K;

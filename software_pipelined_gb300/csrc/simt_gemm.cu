@@ -1,338 +1,57 @@
-// SIMT FFMA GEMM with a cp.async multi-stage shared-memory ring.
-//
-// This is the pages' software-pipelined K-loop ("Double Buffering" technique
-// page; "Case Study: The Double-Buffered GEMM") on GB300's per-thread async
-// copy: every thread issues the cp.async prefetch of tile l+S-1 and then
-// computes on tile l, so the copy engine and the FFMA pipe overlap.  With S=2
-// it is exactly the double-buffered loop: one __syncthreads per iteration does
-// the pages' "double duty" (tile l has landed for every thread, and every thread
-// has finished reading the buffer about to be refilled).  S=1 is the
-// single-buffered sibling (load, barrier, compute, barrier) kept for the
-// pipeline-depth ablation.
-//
-// SEP = true is the ablation of the barrier coalescing of "Dependence-aware
-// group synchronization on M1 Max" ("Transformation and safety boundary"): A
-// and B are copied as separate cp.async groups and each gets its own barrier
-// (copy A; barrier; copy B; barrier; compute; ...), where the default form
-// publishes both with one barrier.
-//
-// Layout: A tile As[BM][BK+4] (row-major, as in global memory, so the copy is a
-// straight 16-byte cp.async when rows are 16-byte aligned), B tile
-// Bs[BK][BN+4].  Each thread owns a TM x TN register tile built from 4x4 blocks
-// spread BM/(TM/4) rows and BN/(TN/4) columns apart, so that a warp's 16-byte
-// fragment loads hit distinct banks.  A fragments are read as float4 along k
-// (4 k-steps per load), B fragments as float4 along n.
+// SIMT FFMA GEMM: the table of compiled configurations and its lookup.  The
+// kernel is simt_kernel.cuh; its instantiations are in simt_configs_*.cu.
 #include <cstdint>
 
-#include "internal.h"
-#include "ptx.cuh"
+#include "simt_kernel.cuh"
 
 namespace gemm_f32 {
+namespace simt_detail {
+extern const SimtEntry kSimtPartA[];
+extern const int kSimtPartACount;
+extern const SimtEntry kSimtPartB[];
+extern const int kSimtPartBCount;
+extern const SimtEntry kSimtPartC[];
+extern const int kSimtPartCCount;
+}  // namespace simt_detail
+
 namespace {
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
-struct SimtKernel {
-    static constexpr int TX = BN / TN;
-    static constexpr int TY = BM / TM;
-    static constexpr int NT = TX * TY;
-    static constexpr int LDA_S = BK + 4;   // floats per As row
-    static constexpr int LDB_S = BN + 4;   // floats per Bs row
-    static constexpr int A_STAGE = BM * LDA_S;
-    static constexpr int B_STAGE = BK * LDB_S;
-    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
-    static_assert(TM % 4 == 0 && TN % 4 == 0, "register tile is built from 4x4 blocks");
-    static_assert(BK % 4 == 0, "BK multiple of 4");
-    static_assert(NT >= 32 && NT <= 1024, "block size");
-    static_assert(!SEP || STAGES <= 2, "separate barriers: 1 or 2 stages");
-};
+using simt_detail::SimtEntry;
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
-__global__ void __launch_bounds__((BM / TM) * (BN / TN))
-simt_gemm_kernel(SimtArgs a)
+const SimtEntry& entry(int id)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
-    constexpr int NT = KT::NT, TX = KT::TX;
-    constexpr int RG = TM / 4, CG = TN / 4;
-    extern __shared__ __align__(16) float smem[];
-    float* As = smem;
-    float* Bs = smem + STAGES * KT::A_STAGE;
-
-    const int tid = threadIdx.x;
-    const int tx = tid % TX, ty = tid / TX;
-    const int64_t m0 = (int64_t)blockIdx.y * BM;
-    const int64_t n0 = (int64_t)blockIdx.x * BN;
-    const bool batched = a.batch > 1;
-    const int64_t kbeg = batched ? 0 : (int64_t)blockIdx.z * a.k_chunk;
-    const int64_t kend = batched ? a.K : min(a.K, kbeg + a.k_chunk);
-    const int nk = kend > kbeg ? (int)((kend - kbeg + BK - 1) / BK) : 0;
-    const int64_t M = a.M, N = a.N;
-    const float* __restrict__ A = a.A + (batched ? (int64_t)blockIdx.z * a.stride_a : 0);
-    const float* __restrict__ B = a.B + (batched ? (int64_t)blockIdx.z * a.stride_b : 0);
-
-    // Issue the cp.async copies of K-tile t into ring slot st.  Out-of-range
-    // elements (ragged M, N or K) are zero-filled by the copy itself.
-    auto load_a = [&](int st, int t) {
-        const int64_t k0 = kbeg + (int64_t)t * BK;
-        float* as = As + st * KT::A_STAGE;
-        if constexpr (VA) {
-            for (int c = tid; c < BM * BK / 4; c += NT) {
-                const int r = c / (BK / 4), kc = (c % (BK / 4)) * 4;
-                const int64_t gm = m0 + r, gk = k0 + kc;
-                int bytes = 0;
-                const float* src = A;
-                if (gm < M && gk < kend) {
-                    bytes = 4 * (int)(kend - gk < 4 ? kend - gk : 4);
-                    src = A + gm * a.lda + gk;
-                }
-                ptx::cp_async_16(ptx::smem_u32(as + r * KT::LDA_S + kc), src, bytes);
-            }
-        } else {
-            for (int e = tid; e < BM * BK; e += NT) {
-                const int r = e / BK, kk = e % BK;
-                const int64_t gm = m0 + r, gk = k0 + kk;
-                const bool ok = gm < M && gk < kend;
-                ptx::cp_async_4(ptx::smem_u32(as + r * KT::LDA_S + kk),
-                                ok ? A + gm * a.lda + gk : A, ok ? 4 : 0);
-            }
-        }
-    };
-    auto load_b = [&](int st, int t) {
-        const int64_t k0 = kbeg + (int64_t)t * BK;
-        float* bs = Bs + st * KT::B_STAGE;
-        if constexpr (VB) {
-            for (int c = tid; c < BK * BN / 4; c += NT) {
-                const int r = c / (BN / 4), nc = (c % (BN / 4)) * 4;
-                const int64_t gk = k0 + r, gn = n0 + nc;
-                int bytes = 0;
-                const float* src = B;
-                if (gk < kend && gn < N) {
-                    bytes = 4 * (int)(N - gn < 4 ? N - gn : 4);
-                    src = B + gk * a.ldb + gn;
-                }
-                ptx::cp_async_16(ptx::smem_u32(bs + r * KT::LDB_S + nc), src, bytes);
-            }
-        } else {
-            for (int e = tid; e < BK * BN; e += NT) {
-                const int r = e / BN, nn = e % BN;
-                const int64_t gk = k0 + r, gn = n0 + nn;
-                const bool ok = gk < kend && gn < N;
-                ptx::cp_async_4(ptx::smem_u32(bs + r * KT::LDB_S + nn),
-                                ok ? B + gk * a.ldb + gn : B, ok ? 4 : 0);
-            }
-        }
-    };
-    auto load_tile = [&](int st, int t) {
-        load_a(st, t);
-        load_b(st, t);
-    };
-
-    float acc[TM][TN];
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-    auto compute_tile = [&](int st) {
-        const float* as = As + st * KT::A_STAGE;
-        const float* bs = Bs + st * KT::B_STAGE;
-#pragma unroll
-        for (int kk = 0; kk < BK; kk += 4) {
-            float4 av[TM];
-#pragma unroll
-            for (int g = 0; g < RG; ++g)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    av[g * 4 + i] = *reinterpret_cast<const float4*>(
-                        as + (g * (BM / RG) + ty * 4 + i) * KT::LDA_S + kk);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float bv[TN];
-#pragma unroll
-                for (int h = 0; h < CG; ++h) {
-                    const float4 t = *reinterpret_cast<const float4*>(
-                        bs + (kk + q) * KT::LDB_S + h * (BN / CG) + tx * 4);
-                    bv[h * 4 + 0] = t.x; bv[h * 4 + 1] = t.y;
-                    bv[h * 4 + 2] = t.z; bv[h * 4 + 3] = t.w;
-                }
-#pragma unroll
-                for (int i = 0; i < TM; ++i) {
-                    const float av_q = q == 0 ? av[i].x : q == 1 ? av[i].y : q == 2 ? av[i].z : av[i].w;
-#pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av_q, bv[j], acc[i][j]);
-                }
-            }
-        }
-    };
-
-    if constexpr (SEP && STAGES == 1) {
-        // Single-buffered, separate publication: copy A; barrier; copy B;
-        // barrier; compute; barrier (three per step).
-        for (int t = 0; t < nk; ++t) {
-            load_a(0, t);
-            ptx::cp_async_commit();
-            ptx::cp_async_wait<0>();
-            __syncthreads();
-            load_b(0, t);
-            ptx::cp_async_commit();
-            ptx::cp_async_wait<0>();
-            __syncthreads();
-            compute_tile(0);
-            __syncthreads();
-        }
-    } else if constexpr (SEP) {
-        // Double-buffered, separate publication: A and B of a tile are two
-        // cp.async groups, each published by its own barrier (two per step).
-        load_a(0, 0);
-        ptx::cp_async_commit();
-        load_b(0, 0);
-        ptx::cp_async_commit();
-        for (int t = 0; t < nk; ++t) {
-            ptx::cp_async_wait<1>();   // A of tile t
-            __syncthreads();
-            ptx::cp_async_wait<0>();   // B of tile t
-            __syncthreads();           // also: everyone is done with slot (t+1)%2
-            if (t + 1 < nk) load_a((t + 1) & 1, t + 1);
-            ptx::cp_async_commit();
-            if (t + 1 < nk) load_b((t + 1) & 1, t + 1);
-            ptx::cp_async_commit();
-            compute_tile(t & 1);
-        }
-        ptx::cp_async_wait<0>();
-    } else if constexpr (STAGES == 1) {
-        // Single-buffered: load, wait, barrier, compute, barrier (two per step).
-        for (int t = 0; t < nk; ++t) {
-            load_tile(0, t);
-            ptx::cp_async_commit();
-            ptx::cp_async_wait<0>();
-            __syncthreads();
-            compute_tile(0);
-            __syncthreads();
-        }
-    } else {
-        // Prologue: tiles 0 .. S-2 in flight.
-#pragma unroll
-        for (int s = 0; s < STAGES - 1; ++s) {
-            if (s < nk) load_tile(s, s);
-            ptx::cp_async_commit();
-        }
-        for (int t = 0; t < nk; ++t) {
-            ptx::cp_async_wait<STAGES - 2>();  // my copies of tile t have landed
-            __syncthreads();                   // everyone's have, and slot (t-1)%S is free
-            const int nt = t + STAGES - 1;
-            if (nt < nk) load_tile(nt % STAGES, nt);
-            ptx::cp_async_commit();
-            compute_tile(t % STAGES);
-        }
-        ptx::cp_async_wait<0>();
-    }
-
-    // Epilogue: guarded stores of the register tile (16-byte when aligned).
-    float* out;
-    int64_t ld;
-    bool vec;
-    if (a.split_k > 1) {
-        out = a.partial + (int64_t)blockIdx.z * M * a.ldp;
-        ld = a.ldp;
-        vec = true;
-    } else {
-        out = a.C + (batched ? (int64_t)blockIdx.z * a.stride_c : 0);
-        ld = a.ldc;
-        vec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    }
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int64_t gm = m0 + (i / 4) * (BM / RG) + ty * 4 + (i % 4);
-        if (gm >= M) continue;
-        float* row = out + gm * ld;
-#pragma unroll
-        for (int h = 0; h < CG; ++h) {
-            const int64_t gn = n0 + h * (BN / CG) + tx * 4;
-            if (vec && gn + 3 < N) {
-                *reinterpret_cast<float4*>(row + gn) =
-                    make_float4(acc[i][h * 4 + 0], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (gn + j < N) row[gn + j] = acc[i][h * 4 + j];
-            }
-        }
-    }
+    using namespace simt_detail;
+    if (id < kSimtPartACount) return kSimtPartA[id];
+    id -= kSimtPartACount;
+    if (id < kSimtPartBCount) return kSimtPartB[id];
+    return kSimtPartC[id - kSimtPartBCount];
 }
-
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
-cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
-{
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
-    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
-    static bool attr_done = false;  // per-instantiation; benign race (idempotent)
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             KT::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
-    dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
-              (unsigned)(a.batch > 1 ? a.batch : a.split_k));
-    kern<<<grid, KT::NT, KT::SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false>
-cudaError_t launch_cfg(const SimtArgs& a, cudaStream_t s)
-{
-    const bool va = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) &&
-                    (a.batch <= 1 || a.stride_a % 4 == 0);
-    const bool vb = (a.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
-                    (a.batch <= 1 || a.stride_b % 4 == 0);
-    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP>(a, s);
-    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP>(a, s);
-    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP>(a, s);
-    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false, SEP>(a, s);
-}
-
-using LaunchFn = cudaError_t (*)(const SimtArgs&, cudaStream_t);
-struct SimtEntry {
-    SimtConfig cfg;
-    LaunchFn fn;
-};
-
-const SimtEntry kSimt[] = {
-    {{128, 128, 16, 8, 8, 2, false}, launch_cfg<128, 128, 16, 8, 8, 2>},
-    {{128, 128, 16, 8, 8, 3, false}, launch_cfg<128, 128, 16, 8, 8, 3>},
-    {{128, 128, 16, 8, 8, 1, false}, launch_cfg<128, 128, 16, 8, 8, 1>},
-    {{64, 64, 16, 4, 4, 2, false}, launch_cfg<64, 64, 16, 4, 4, 2>},
-    {{64, 64, 16, 4, 4, 3, false}, launch_cfg<64, 64, 16, 4, 4, 3>},
-    {{64, 64, 16, 4, 4, 1, false}, launch_cfg<64, 64, 16, 4, 4, 1>},
-    {{64, 64, 32, 4, 4, 2, false}, launch_cfg<64, 64, 32, 4, 4, 2>},
-    {{32, 32, 32, 4, 4, 2, false}, launch_cfg<32, 32, 32, 4, 4, 2>},
-    {{32, 32, 32, 4, 4, 1, false}, launch_cfg<32, 32, 32, 4, 4, 1>},
-    {{128, 64, 16, 8, 4, 2, false}, launch_cfg<128, 64, 16, 8, 4, 2>},
-    // barrier-coalescing ablation: A and B published separately
-    {{128, 128, 16, 8, 8, 2, true}, launch_cfg<128, 128, 16, 8, 8, 2, true>},
-    {{128, 128, 16, 8, 8, 1, true}, launch_cfg<128, 128, 16, 8, 8, 1, true>},
-    {{64, 64, 16, 4, 4, 2, true}, launch_cfg<64, 64, 16, 4, 4, 2, true>},
-    {{64, 64, 16, 4, 4, 1, true}, launch_cfg<64, 64, 16, 4, 4, 1, true>},
-    {{32, 32, 32, 4, 4, 2, true}, launch_cfg<32, 32, 32, 4, 4, 2, true>},
-    {{32, 32, 32, 4, 4, 1, true}, launch_cfg<32, 32, 32, 4, 4, 1, true>},
-};
 
 }  // namespace
 
-int simt_num_configs() { return (int)(sizeof(kSimt) / sizeof(kSimt[0])); }
-const SimtConfig& simt_config(int id) { return kSimt[id].cfg; }
-int simt_find_config(int bm, int bn, int stages, bool sep)
+int simt_num_configs()
 {
+    using namespace simt_detail;
+    return kSimtPartACount + kSimtPartBCount + kSimtPartCCount;
+}
+const SimtConfig& simt_config(int id) { return entry(id).cfg; }
+int simt_find_config(int bm, int bn, int stages, bool sep, int bk)
+{
+    // bk == 0: the shallowest K-tile compiled for this tile and ring
+    int best = -1;
     for (int i = 0; i < simt_num_configs(); ++i) {
-        const SimtConfig& c = kSimt[i].cfg;
-        if (c.bm == bm && c.bn == bn && c.stages == stages && c.sep == sep) return i;
+        const SimtConfig& c = entry(i).cfg;
+        if (c.bm != bm || c.bn != bn || c.stages != stages || c.sep != sep) continue;
+        if (bk != 0 && c.bk != bk) continue;
+        if (best < 0 || c.bk < entry(best).cfg.bk) best = i;
     }
-    return -1;
+    return best;
 }
 
 cudaError_t simt_launch(int config_id, const SimtArgs& a, cudaStream_t s)
 {
     if (config_id < 0 || config_id >= simt_num_configs()) return cudaErrorInvalidValue;
-    return kSimt[config_id].fn(a, s);
+    return entry(config_id).fn(a, s);
 }
 
 }  // namespace gemm_f32

@@ -26,8 +26,10 @@ sys.path.insert(0, os.path.dirname(HERE))
 import software_pipelined_gb300 as g  # noqa: E402
 from software_pipelined_gb300 import inputs  # noqa: E402
 
-SIMT_CFGS = [(128, 128, 2), (128, 128, 3), (128, 128, 1), (64, 64, 2), (64, 64, 3), (64, 64, 1),
-             (32, 32, 2), (32, 32, 1), (128, 64, 2)]
+# (tile_m, tile_n, stages, tile_k)
+SIMT_CFGS = [(128, 128, 2, 16), (128, 128, 3, 16), (128, 128, 1, 16), (64, 64, 2, 16), (64, 64, 3, 16),
+             (64, 64, 1, 16), (64, 64, 2, 32), (32, 32, 2, 32), (32, 32, 1, 32), (128, 64, 2, 16),
+             (32, 32, 3, 32), (32, 32, 1, 64), (32, 32, 2, 64), (32, 64, 2, 32), (64, 32, 2, 32)]
 TC_BN = [64, 128, 256]
 SPLITS = [1, 2, 3, 4, 6, 8, 12, 16]
 
@@ -71,10 +73,11 @@ def candidates(M, N, K):
     out = []
     macs = M * N * K
     if macs <= 2 ** 31:
-        for (bm, bn, st) in SIMT_CFGS:
+        for (bm, bn, st, bk) in SIMT_CFGS:
             for sp in SPLITS:
                 if sp == 1 or K // sp >= 32:
-                    out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp))
+                    out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp,
+                                    tile_k=bk))
     if K >= 16:
         for bn in TC_BN:
             for fused in ((1, 2, 3) if bn in (128, 256) and K >= 32 else (1,)):
@@ -160,7 +163,7 @@ def write_inc(results, path):
         "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
         "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass),",
-        "// tile_group (tcgen05: tile-rows per raster group, 0 = default).",
+        "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k (SIMT).",
         "struct TableRow {",
         "    int64_t M, N, K;",
         "    DispatchChoice c;",
@@ -172,10 +175,11 @@ def write_inc(results, path):
         o = r["best"]["opts"]
         split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
-                     f"{o['stages']}, {split}, {split_where(r['best']['plan'])}, {o.get('tile_group', 0)}}}}},"
+                     f"{o['stages']}, {split}, {split_where(r['best']['plan'])}, {o.get('tile_group', 0)}, "
+                     f"{o.get('tile_k', 0)}}}}},"
                      f"  // {r['best']['us']} us")
     lines += [
-        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0}},  // sentinel",
+        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel",
         "};",
         "",
         "bool table_lookup(int64_t M, int64_t N, int64_t K, DispatchChoice& out)",
