@@ -84,6 +84,23 @@ def algorithmic_bytes(M, N, K):
     return 4 * (M * K + K * N + M * N)
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of the ranks' values (every rank gets it); the value itself
+    without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(flops_per_rank_step, world, seconds_per_step):
+    """Whole-job throughput in TFLOP/s: every rank runs one replica of the
+    step, and the job's step time is the slowest rank's."""
+    return world * flops_per_rank_step / seconds_per_step / 1e12
+
+
 # ---------------------------------------------------------------------------
 # Clocks sampled during the timed region.
 # ---------------------------------------------------------------------------
@@ -345,13 +362,9 @@ def run_gpu_arm(args):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dist, "cuda")
     ms_step = ms_total / args.steps
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_rate(flops_step, world, ms_step * 1e-3)
     for w in work:
         s = w["plan"].check()
         if s != g.OK:
@@ -430,12 +443,8 @@ def run_gpu_arm(args):
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             e2e_step()
-        dt = (time.perf_counter() - t0) / n_e2e
-        if dist:
-            t = torch.tensor([dt], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": round(world * flops_step / dt / 1e12, 3), "unit": "TFLOP/s",
+        dt = max_over_ranks((time.perf_counter() - t0) / n_e2e, dist, "cuda")
+        e2e = {"value": round(whole_job_rate(flops_step, world, dt), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(sum(4 * (w["M"] * w["K"] + w["K"] * w["N"]) for w in work)),
                "d2h_bytes_per_step": int(sum(4 * w["M"] * w["N"] for w in work)),
                "ms_per_step": round(dt * 1e3, 3), "steps": n_e2e,

@@ -166,24 +166,29 @@ def test_3xtf32_accuracy_matches_fp32_simt():
     assert et <= 3 * es + 1e-3, (et, es)
 
 
-SIMT_CFGS = [(128, 128, 2, 0), (128, 128, 3, 0), (128, 128, 1, 0), (64, 64, 2, 0), (64, 64, 3, 0),
-             (64, 64, 1, 0), (32, 32, 2, 0), (32, 32, 1, 0), (128, 64, 2, 0),
-             (128, 128, 2, 1), (128, 128, 1, 1), (64, 64, 2, 1), (64, 64, 1, 1), (32, 32, 2, 1),
-             (32, 32, 1, 1)]
+# (tile_m, tile_n, stages, separate barriers, tile_k); 0 = the default K-tile
+SIMT_CFGS = [(128, 128, 2, 0, 0), (128, 128, 3, 0, 0), (128, 128, 1, 0, 0), (64, 64, 2, 0, 0),
+             (64, 64, 3, 0, 0), (64, 64, 1, 0, 0), (64, 64, 2, 0, 32), (32, 32, 2, 0, 0), (32, 32, 1, 0, 0),
+             (128, 64, 2, 0, 0), (32, 32, 3, 0, 0), (32, 32, 1, 0, 64), (32, 32, 2, 0, 64), (32, 64, 2, 0, 0),
+             (64, 32, 2, 0, 0),
+             (128, 128, 2, 1, 0), (128, 128, 1, 1, 0), (64, 64, 2, 1, 0), (64, 64, 1, 1, 0), (32, 32, 2, 1, 0),
+             (32, 32, 1, 1, 0)]
 
 
 @pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
-@pytest.mark.parametrize("cfg", SIMT_CFGS, ids=[f"{a}x{b}s{c}{'sep' if d else ''}" for a, b, c, d in SIMT_CFGS])
+@pytest.mark.parametrize("cfg", SIMT_CFGS,
+                         ids=[f"{a}x{b}s{c}{'sep' if d else ''}k{e}" for a, b, c, d, e in SIMT_CFGS])
 def test_every_simt_config(cfg, aligned):
-    # last field: separate barriers for A and B (barrier-coalescing ablation)
-    bm, bn, st, sep = cfg
+    # separate barriers for A and B: the barrier-coalescing ablation
+    bm, bn, st, sep, bk = cfg
     M, N, K = 3 * bm + 5, 2 * bn + 3, 97
     A = inputs.uniform_pm1(951, M, K)
     B = inputs.uniform_pm1(952, K, N)
     kw = {} if aligned else dict(lda=K + 1, ldb=N + 2, a_off=1, b_off=1)
     C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st,
-                                    separate_syncs=sep, **kw)
+                                    separate_syncs=sep, tile_k=bk, **kw)
     assert ("separate-syncs" in desc) == bool(sep), desc
+    assert f"tile={bm}x{bn}x" in desc and (bk == 0 or f"x{bk} " in desc), desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
 
