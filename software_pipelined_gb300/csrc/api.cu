@@ -214,6 +214,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 c.split_k = tiles >= p->num_sms / 2 ? 0 : auto_split(tiles, K, 256, p->num_sms);
             }
         }
+        // A forced tile or ring replaces the choice, so the table's K-tile depth
+        // and tile order (tuned for its own tile) no longer apply.
+        if (o.tile_m || o.tile_n || o.stages) c.tile_k = c.group = 0;
         if (o.tile_m) c.tile_m = o.tile_m;
         if (o.tile_n) c.tile_n = o.tile_n;
         if (o.stages) c.stages = o.stages;

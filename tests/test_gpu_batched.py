@@ -52,7 +52,7 @@ def _run_batched(M, N, K, batch, lda, ldb, ldc, sa, sb, sc, seed, **kw):
 
 
 @pytest.mark.parametrize("shape,batch", [((32, 32, 32), 256), ((33, 47, 29), 7), ((64, 64, 64), 40),
-                                         ((128, 96, 200), 9)])
+                                         ((128, 96, 200), 9), ((128, 128, 128), 6), ((127, 193, 61), 3)])
 def test_batched_matches_oracle(shape, batch):
     M, N, K = shape
     lda, ldb, ldc = K, N, N

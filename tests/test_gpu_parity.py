@@ -54,6 +54,19 @@ def test_benchmark_shapes_full_output(w, variant):
     assert ok, f"{name} {desc}: max normalised error {err}"
 
 
+@pytest.mark.parametrize("w", BENCH_SHAPES, ids=[w[0] for w in BENCH_SHAPES])
+def test_forced_tiles_on_table_shapes(w):
+    # A shape the dispatch table lists, with forced tile/stage options: the
+    # table's own K-tile depth and tile order must not leak into the override.
+    name, M, N, K, dist, sa, sb = w
+    A, B = _operands(M, N, K, dist, sa, sb)
+    for kw in (dict(variant=g.VARIANT_SIMT, tile_m=128, tile_n=128, stages=2),
+               dict(variant=g.VARIANT_SIMT, tile_m=64, tile_n=64, stages=3)):
+        C, desc, canaries, _ = run_gemm(A, B, **kw)
+        err, ok = check_against_oracle(C, A, B)
+        assert canaries and ok, f"{name} {desc}: {err}"
+
+
 EDGE = [
     (1, 1, 1), (1, 37, 19), (41, 1, 23), (17, 29, 1), (33, 65, 5), (130, 260, 33),
     (257, 129, 257), (64, 64, 64), (128, 256, 96), (255, 513, 100), (300, 200, 1000),
