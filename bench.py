@@ -328,7 +328,8 @@ def run_gpu_arm(args):
     work = []
     for (name, M, N, K, dist_name, sa, sb) in shapes_of(args.workload, args.shape):
         A, B, dA, dB, dC = make_device_operands(M, N, K, dist_name, sa, sb)
-        plan = g.Plan(M, N, K)
+        variant = {"auto": g.VARIANT_AUTO, "simt": g.VARIANT_SIMT, "tcgen05": g.VARIANT_TCGEN05}[args.variant]
+        plan = g.Plan(M, N, K, variant=variant)
         plan.trace_enable(args.steps)
         work.append(dict(name=name, M=M, N=N, K=K, A=A, B=B, dA=dA, dB=dB, dC=dC, plan=plan,
                          run=(lambda p=plan, a=dA, b=dB, c=dC: p.run_ptr(a.data_ptr(), b.data_ptr(),
@@ -391,7 +392,8 @@ def run_gpu_arm(args):
     big = max(work, key=lambda w: w["M"] * w["N"] * w["K"])
     bk = per_kernel[big["name"]]
     achieved = bk["main_tflops"]
-    peak = pk["f32_3xtf32_tflops_burst"]
+    simt_main = big["plan"].describe().startswith("simt")
+    peak = pk["f32_simt_tflops_nominal"] if simt_main else pk["f32_3xtf32_tflops_burst"]
     kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", f)
                              for f in ("tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "dispatch_table.inc")])
     traffic, traffic_src = traffic_for(kern_hash)
@@ -399,10 +401,13 @@ def run_gpu_arm(args):
         t = traffic.get(w["name"]) if traffic else None
         per_kernel[w["name"]]["dram_bytes_per_launch"] = t
         per_kernel[w["name"]]["frac"] = round(per_kernel[w["name"]]["main_tflops"] / peak, 4)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": round(peak, 2), "unit": "TFLOP/s",
+    roofline = {"bound": "alu" if simt_main else "tensor", "achieved": achieved, "peak": round(peak, 2),
+                "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": per_kernel[big["name"]]["dram_bytes_per_launch"],
-                "kernel": f"tc_gemm_kernel (tcgen05 3xTF32 main GEMM), {big['name']} launches",
-                "peak_basis": f"of {pk['source']}: burst bf16 x {TF32_OVER_BF16:.4f} (nominal tf32/bf16) / 3",
+                "kernel": (f"simt_gemm_kernel (FFMA), {big['name']} launches" if simt_main else
+                           f"tc_gemm_kernel (tcgen05 3xTF32 main GEMM), {big['name']} launches"),
+                "peak_basis": ("nominal FP32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz" if simt_main else
+                               f"of {pk['source']}: burst bf16 x {TF32_OVER_BF16:.4f} (nominal tf32/bf16) / 3"),
                 "frac_of_sustained_peak": round(achieved / pk["f32_3xtf32_tflops_sustained"], 4),
                 "algorithmic_flops_per_launch": 2.0 * big["M"] * big["N"] * big["K"],
                 "algorithmic_bytes_per_launch": algorithmic_bytes(big["M"], big["N"], big["K"]),
@@ -633,6 +638,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--shape", default=None, help="time one MxNxK shape instead of the workload")
+    ap.add_argument("--variant", choices=["auto", "simt", "tcgen05"], default="auto",
+                    help="kernel for the timed shapes (default: the dispatcher's choice)")
     ap.add_argument("--no-per-shape", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -102,9 +102,10 @@ typedef struct {
                                choice; 1 = a pre-pass writes hi/lo operands to scratch;
                                2 = inside the GEMM kernel (needs K >= 32 and lda, ldb
                                multiples of 4); 3 = A inside the kernel, B by the pre-pass
-                               (needs K >= 32, lda a multiple of 4).  2 and 3 fall back to 1
-                               at run time for a base pointer of A (or, for 2, B) that is
-                               not 16-byte aligned */
+                               (needs K >= 32, lda a multiple of 4); 4 = hi of A read from
+                               A itself, lo of A and B by the pre-pass (same needs).  2, 3 and
+                               4 fall back to 1 at run time for a base pointer of A (or, for
+                               2, B) that is not 16-byte aligned */
     int32_t tile_group;     /* TC only: tile order of the persistent kernel, in tile-rows per
                                raster group (1..64; 0 = the dispatcher's choice, else 8) */
     int32_t tile_k;         /* SIMT only: K-tile depth (16/32/64; 0 = the compiled default

@@ -62,6 +62,9 @@ struct gemm_f32_plan_s {
     float* hA = nullptr;
     float* hB = nullptr;
     float* hC = nullptr;
+    // two internal streams so the copies of gemm_f32_run_host use two copy engines
+    cudaStream_t xs[2] = {nullptr, nullptr};
+    cudaEvent_t xev[3] = {nullptr, nullptr, nullptr};
     char desc[256] = {0};
     // tracing: 4 events per recorded run
     std::vector<cudaEvent_t> trace_ev;
@@ -104,7 +107,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
-    if (o.operand_split < 0 || o.operand_split > 3) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.operand_split < 0 || o.operand_split > 4) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
@@ -250,10 +253,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             p->kind = kTc;
             TcPlanState& t = p->tc;
             // operand_split: 1 pre-pass, 2 in the kernel, 3 hybrid (A in the kernel,
-            // B by the pre-pass); 0 = the dispatcher's choice.
+            // B by the pre-pass), 4 hi of A read from A; 0 = the dispatcher's choice.
             int where = o.operand_split ? o.operand_split - 1 : c.fused;
             const bool ok = where == kSplitPrepass ||
-                            (K >= kTcFusedMinK && lda % 4 == 0 && (where == kSplitHybrid || ldb % 4 == 0) &&
+                            (K >= kTcFusedMinK && lda % 4 == 0 && (where != kSplitInKernel || ldb % 4 == 0) &&
                              !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where) >= 0);
             if (!ok) {
                 if (o.operand_split) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
@@ -281,7 +284,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             snprintf(p->desc, sizeof p->desc,
                      "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d kp=%lld",
                      tcfg.split == kSplitInKernel ? " in-kernel-split"
-                     : tcfg.split == kSplitHybrid ? " hybrid-split" : "",
+                     : tcfg.split == kSplitHybrid ? " hybrid-split"
+                     : tcfg.split == kSplitRawA ? " raw-a-split" : "",
                      t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
                      tcfg.sep ? " separate-syncs" : "",
                      t.tiles_m * t.tiles_n, t.dp_tiles,
@@ -463,18 +467,49 @@ gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t p, const float* A_host, const 
         if (b_bytes && (e = cudaMalloc(&p->hB, b_bytes)) != cudaSuccess) goto fail;
         if ((e = cudaMalloc(&p->hC, c_bytes)) != cudaSuccess) goto fail;
     }
-    if (p->K > 0) {
-        e = copy_rows(p->hA, A_host, p->M, p->K, p->lda, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return from_cuda(e);
-        e = copy_rows(p->hB, B_host, p->K, p->N, p->ldb, cudaMemcpyHostToDevice, s);
+    if (!p->xs[0]) {
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&p->xs[i], cudaStreamNonBlocking);
+        for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&p->xev[i], cudaEventDisableTiming);
         if (e != cudaSuccess) return from_cuda(e);
     }
     {
+        // Each matrix is copied as two row halves on the two internal streams
+        // (two copy engines at once); the caller's stream waits for both.
+        auto fork = [&]() -> cudaError_t {
+            cudaError_t r = cudaEventRecord(p->xev[0], s);
+            for (int i = 0; i < 2 && r == cudaSuccess; ++i) r = cudaStreamWaitEvent(p->xs[i], p->xev[0], 0);
+            return r;
+        };
+        auto join = [&]() -> cudaError_t {
+            cudaError_t r = cudaSuccess;
+            for (int i = 0; i < 2 && r == cudaSuccess; ++i) {
+                r = cudaEventRecord(p->xev[1 + i], p->xs[i]);
+                if (r == cudaSuccess) r = cudaStreamWaitEvent(s, p->xev[1 + i], 0);
+            }
+            return r;
+        };
+        auto halves = [&](float* dst, const float* src, int64_t rows, int64_t cols, int64_t ld,
+                          cudaMemcpyKind kind) -> cudaError_t {
+            const int64_t top = rows / 2;
+            cudaError_t r = copy_rows(dst, src, top, cols, ld, kind, p->xs[0]);
+            if (r == cudaSuccess)
+                r = copy_rows(dst + top * ld, src + top * ld, rows - top, cols, ld, kind, p->xs[1]);
+            return r;
+        };
+        if (p->K > 0) {
+            if ((e = fork()) != cudaSuccess) return from_cuda(e);
+            if ((e = halves(p->hA, A_host, p->M, p->K, p->lda, cudaMemcpyHostToDevice)) != cudaSuccess ||
+                (e = halves(p->hB, B_host, p->K, p->N, p->ldb, cudaMemcpyHostToDevice)) != cudaSuccess ||
+                (e = join()) != cudaSuccess)
+                return from_cuda(e);
+        }
         gemm_f32_status st = gemm_f32_run(p, p->hA, p->hB, p->hC, stream);
         if (st != GEMM_F32_OK) return st;
+        if ((e = fork()) != cudaSuccess ||
+            (e = halves(C_host, p->hC, p->M, p->N, p->ldc, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+            (e = join()) != cudaSuccess)
+            return from_cuda(e);
     }
-    e = copy_rows(C_host, p->hC, p->M, p->N, p->ldc, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return from_cuda(e);
     return gemm_f32_check(p, stream);
 fail:
     cudaGetLastError();
@@ -509,6 +544,10 @@ void gemm_f32_plan_destroy(gemm_f32_plan_t p)
     if (p->hA) cudaFree(p->hA);
     if (p->hB) cudaFree(p->hB);
     if (p->hC) cudaFree(p->hC);
+    for (cudaStream_t x : p->xs)
+        if (x) cudaStreamDestroy(x);
+    for (cudaEvent_t x : p->xev)
+        if (x) cudaEventDestroy(x);
     delete p;
 }
 

@@ -1,5 +1,6 @@
 // Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -7,6 +8,22 @@
 #include "../../include/gemm_f32.h"
 
 namespace gemm_f32 {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute belongs to the device's context).
+// `done` is one bit per device ordinal (< 64), kept by the caller per kernel.
+template <typename Kernel>
+inline cudaError_t smem_limit_once(Kernel kern, int bytes, std::atomic<uint64_t>& done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // ---- SIMT FFMA kernel (simt_gemm.cu) --------------------------------------
 struct SimtConfig {
@@ -54,7 +71,8 @@ struct TcConfig {
 enum : int {
     kSplitPrepass = 0,   // a pre-pass writes hi/lo of A and B to scratch
     kSplitInKernel = 1,  // raw A and B by TMA, split by converter warps
-    kSplitHybrid = 2     // raw A split in the kernel, B split by the pre-pass
+    kSplitHybrid = 2,    // raw A split in the kernel, B split by the pre-pass
+    kSplitRawA = 3       // hi of A read from A (truncated by the MMA); the pre-pass writes lo of A, hi/lo of B
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);

@@ -265,13 +265,8 @@ cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
 {
     using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
     auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
-    static bool attr_done = false;  // per-instantiation; benign race (idempotent)
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             KT::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = smem_limit_once(kern, KT::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
               (unsigned)(a.batch > 1 ? a.batch : a.split_k));
     kern<<<grid, KT::NT, KT::SMEM_BYTES, s>>>(a);

@@ -92,6 +92,17 @@ __device__ __forceinline__ float tf32_trunc(float x)
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
+// lo = RN(x - trunc_tf32(x)) to 11 significant bits, ties away from zero: the
+// difference is exact in FP32; adding half an ulp of TF32 to the magnitude and
+// clearing the low 13 bits rounds it.  Two integer and one float operation per
+// element (plus the truncation), no special cases: for finite x the result is
+// finite; a non-finite x makes the hi*hi product non-finite anyway.
+__device__ __forceinline__ float lo_part(float x)
+{
+    const float d = x - tf32_trunc(x);
+    return __uint_as_float((__float_as_uint(d) + 0x1000u) & 0xFFFFE000u);
+}
+
 // Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile
 // in the 128-byte swizzled layout TMA writes: rows of 128 B, 8-row atoms 1024 B
 // apart (stride byte offset), leading byte offset unused for swizzled K-major.

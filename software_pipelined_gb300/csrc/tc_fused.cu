@@ -61,17 +61,6 @@ struct FusedLayout {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// lo = RN(x - trunc_tf32(x)) to 11 significant bits, ties away from zero: the
-// difference is exact in FP32; adding half an ulp of TF32 to the magnitude and
-// clearing the low 13 bits rounds it.  Two integer and one float operation per
-// element (plus the truncation), no special cases: for finite x the result is
-// finite; a non-finite x makes the hi*hi product non-finite anyway.
-__device__ __forceinline__ float lo_part(float x)
-{
-    const float d = x - tf32_trunc(x);
-    return __uint_as_float((__float_as_uint(d) + 0x1000u) & 0xFFFFE000u);
-}
-
 // Byte offset of element (row, k) in a K-major 128-byte-swizzled tile (rows of
 // 32 FP32 = 128 B, 8-row atoms of 1024 B, 16-byte chunk index XOR row % 8).
 __device__ __forceinline__ uint32_t kmajor_off(int row, int kq)
@@ -355,12 +344,8 @@ cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorM
 {
     using L = FusedLayout<BN, SLOTS, RAWB>;
     auto kern = tc_fused_kernel<BN, SLOTS, RAWB>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
     return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, ta, tb, tbhi, tblo, a);

@@ -64,7 +64,8 @@ constexpr int kSplitBN = 128;   // n columns per B tile
 
 // One launch splits both operands.  Blocks [0, a_blocks) stream A (M x K, lda)
 // into a_hi, a_lo (M x kp, K-major, zero for k >= K), 16 bytes at a time where
-// the rows allow.  The remaining blocks each take a 32 (k) x 128 (n) tile of B
+// the rows allow; with a_lo_only they write only lo = A - trunc_tf32(A) rounded
+// (the GEMM then reads hi straight from A, truncated by the MMA).  The remaining blocks each take a 32 (k) x 128 (n) tile of B
 // (K x N, ldb), stage it in shared memory and write it transposed to b_hi,
 // b_lo (N x kp): reads are coalesced along n, writes along k.  The last thing
 // each block does is allow the dependent GEMM launch to start its prologue.
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(256)
 split_operands_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t lda, int vec_a,
                       const float* __restrict__ B, int64_t N, int64_t ldb, int vec_b, int64_t kp,
                       float4* __restrict__ a_hi, float4* __restrict__ a_lo,
-                      float* __restrict__ b_hi, float* __restrict__ b_lo, int a_blocks)
+                      float* __restrict__ b_hi, float* __restrict__ b_lo, int a_blocks, int a_lo_only)
 {
     if ((int)blockIdx.x < a_blocks) {
         const int64_t kp4 = kp / 4;
@@ -88,6 +89,11 @@ split_operands_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] = (k + j < K) ? __ldg(row + k + j) : 0.f;
+            }
+            if (a_lo_only) {
+                // hi_A is the caller's A itself (the MMA truncates it): only lo
+                a_lo[idx] = make_float4(lo_part(v[0]), lo_part(v[1]), lo_part(v[2]), lo_part(v[3]));
+                continue;
             }
             float h[4], l[4];
 #pragma unroll
@@ -480,20 +486,16 @@ cudaError_t encode_raw_b(void* out, const float* B, int64_t K, int64_t N, int64_
 }
 
 template <int BN, int STAGES, bool SEP = false>
-cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
+cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, const void* tmap_a_hi, cudaStream_t s)
 {
     using L = TcLayout<BN, STAGES>;
     auto kern = tc_gemm_kernel<BN, STAGES, SEP>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), L::SMEM_BYTES, s,
-                      *reinterpret_cast<const CUtensorMap*>(st.tmap_a_hi),
+                      *reinterpret_cast<const CUtensorMap*>(tmap_a_hi),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_a_lo),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), a);
@@ -508,10 +510,11 @@ cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s
                       a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
 }
 
+using MainFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, const void*, cudaStream_t);
 using LaunchFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
 struct TcEntry {
     TcConfig cfg;
-    LaunchFn main;    // NULL where the split happens in the kernel (tc_fused_main)
+    MainFn main;      // NULL where the split happens in the kernel (tc_fused_main)
     LaunchFn reduce;
 };
 const TcEntry kTc[] = {
@@ -533,6 +536,9 @@ const TcEntry kTc[] = {
     // A split inside the kernel, B by the pre-pass
     {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>},
     {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>},
+    // hi of A read from the caller's A, lo of A and both pieces of B by the pre-pass
+    {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>},
+    {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>},
 };
 
 }  // namespace
@@ -635,25 +641,31 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
     const bool a_ok = reinterpret_cast<uintptr_t>(A) % 16 == 0;
     const bool b_ok = reinterpret_cast<uintptr_t>(B) % 16 == 0;
     const bool in_kernel = (c.split == kSplitInKernel && a_ok && b_ok) || (c.split == kSplitHybrid && a_ok);
+    const bool raw_a = c.split == kSplitRawA && a_ok;
     cudaError_t e = cudaSuccess;
     if (ev) cudaEventRecord(ev[0], s);
     const int vec_a = (lda % 4 == 0) && a_ok;
     const int vec_b = (ldb % 4 == 0) && b_ok;
+    if ((raw_a || (c.split == kSplitInKernel && in_kernel)) && A != st.raw_a) {
+        if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda)) != cudaSuccess) return e;
+        st.raw_a = A;
+    }
     if (!in_kernel || c.split == kSplitHybrid) {
         // 1. The pre-pass: hi/lo of B (transposed) and, unless A is split in
-        // the kernel, of A, into the plan's scratch; one launch.
-        if (!in_kernel && c.split != kSplitPrepass) id = st.fallback_config_id;
+        // the kernel, of A (only lo when hi is read from A), into the plan's
+        // scratch; one launch.
+        if (!in_kernel && !raw_a && c.split != kSplitPrepass) id = st.fallback_config_id;
         const int a_blocks = in_kernel ? 0 : grid_cap(M * (st.kp / 4), st.num_sms);
         const int64_t b_blocks = (st.kp / kSplitBK) * ((N + kSplitBN - 1) / kSplitBN);
         split_operands_kernel<<<(unsigned)(a_blocks + b_blocks), 256, 0, s>>>(
             A, M, K, lda, vec_a, B, N, ldb, vec_b, st.kp, reinterpret_cast<float4*>(st.a_hi),
-            reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks);
+            reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks, raw_a ? 1 : 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (ev) cudaEventRecord(ev[1], s);
     if (in_kernel) {
         // 2. Raw operands straight from the caller's buffers.
-        if (A != st.raw_a) {
+        if (c.split == kSplitHybrid && A != st.raw_a) {
             if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda)) != cudaSuccess) return e;
             st.raw_a = A;
         }
@@ -668,7 +680,7 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), s);
     } else {
         // 2. The pipelined tensor-core GEMM on the split operands.
-        e = kTc[id].main(st, a, s);
+        e = kTc[id].main(st, a, raw_a ? st.tmap_a_raw : st.tmap_a_hi, s);
     }
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);

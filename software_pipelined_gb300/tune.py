@@ -80,7 +80,7 @@ def candidates(M, N, K):
                                     tile_k=bk))
     if K >= 16:
         for bn in TC_BN:
-            for fused in ((1, 2, 3) if bn in (128, 256) and K >= 32 else (1,)):
+            for fused in ((1, 2, 3, 4) if bn in (128, 256) and K >= 32 else (1,)):
                 for sp in [0] + SPLITS:
                     if sp <= 1 or (K + 31) // 32 >= sp:
                         out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp,
@@ -150,8 +150,9 @@ def effective_split(desc: str) -> int:
 
 
 def split_where(desc: str) -> int:
-    """The table's last field: 0 pre-pass, 1 in the kernel, 2 hybrid."""
-    return 1 if "in-kernel-split" in desc else 2 if "hybrid-split" in desc else 0
+    """The table's split field: 0 pre-pass, 1 in the kernel, 2 hybrid, 3 raw A."""
+    return (1 if "in-kernel-split" in desc else 2 if "hybrid-split" in desc
+            else 3 if "raw-a-split" in desc else 0)
 
 
 def write_inc(results, path):
@@ -162,7 +163,8 @@ def write_inc(results, path):
         "// fall back to the rule in choose().  Fields: variant (1 SIMT, 2 tcgen05),",
         "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
-        "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass),",
+        "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass,",
+        "// 3 hi of A read from A),",
         "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k (SIMT).",
         "struct TableRow {",
         "    int64_t M, N, K;",

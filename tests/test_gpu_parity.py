@@ -278,10 +278,12 @@ def test_large_squares_sampled(w):
 
 FUSED = {"variant": g.VARIANT_TCGEN05, "operand_split": 2}
 HYBRID = {"variant": g.VARIANT_TCGEN05, "operand_split": 3}
-MODES = [(FUSED, "in-kernel-split"), (HYBRID, "hybrid-split")]
+RAWA = {"variant": g.VARIANT_TCGEN05, "operand_split": 4}
+MODES = [(FUSED, "in-kernel-split"), (HYBRID, "hybrid-split"), (RAWA, "raw-a-split")]
+MODE_IDS = ["in_kernel", "hybrid", "raw_a"]
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("split", [1, 2, 0])
 def test_in_kernel_split_configs(bn, split, mode):
@@ -300,7 +302,7 @@ def test_in_kernel_split_configs(bn, split, mode):
     assert np.array_equal(outs[0], outs[1]), desc
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
 def test_in_kernel_split_many_tiles_and_tail_wave(mode):
     M, N, K = 128 * 21, 256 * 9 + 68, 512
     A = inputs.uniform_pm1(1603, M, K)
@@ -311,7 +313,7 @@ def test_in_kernel_split_many_tiles_and_tail_wave(mode):
     assert canaries and ok, f"{desc}: {err}"
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
 def test_in_kernel_split_padded_and_misaligned_fallback(mode):
     # lda, ldb multiples of 4 (an in-kernel plan), but base pointers 4 bytes off
     # a 16-byte boundary: the run falls back to the pre-split kernel.
@@ -326,7 +328,7 @@ def test_in_kernel_split_padded_and_misaligned_fallback(mode):
         assert canaries and ok, f"{kw} {desc}: {err}"
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
 def test_in_kernel_split_small_integers_bit_exact(mode):
     M, N, K = 200, 300, 1000
     A = inputs.small_int(1607, M, K)
@@ -346,15 +348,18 @@ def test_in_kernel_split_refusals():
     with pytest.raises(g.GemmError) as ei:
         g.Plan(64, 64, 64, variant=g.VARIANT_TCGEN05, operand_split=2, tile_n=64)  # no fused 64-wide
     assert ei.value.status == g.ERR_UNSUPPORTED
-    with pytest.raises(g.GemmError) as ei:
-        g.Plan(64, 64, 61, variant=g.VARIANT_TCGEN05, operand_split=3)      # lda = 61
-    assert ei.value.status == g.ERR_UNSUPPORTED
+    for mode in (3, 4):
+        with pytest.raises(g.GemmError) as ei:
+            g.Plan(64, 64, 61, variant=g.VARIANT_TCGEN05, operand_split=mode)   # lda = 61
+        assert ei.value.status == g.ERR_UNSUPPORTED
+    with g.Plan(64, 61, 64, variant=g.VARIANT_TCGEN05, operand_split=4) as p:   # any ldb
+        assert "raw-a-split" in p.describe()
     # hybrid takes any ldb
     with g.Plan(64, 61, 64, variant=g.VARIANT_TCGEN05, operand_split=3) as p:
         assert "hybrid-split" in p.describe()
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
 def test_in_kernel_split_negative_control(mode):
     M, N, K = 256, 256, 32
     A = inputs.uniform_pm1(1609, M, K)
