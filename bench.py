@@ -395,7 +395,7 @@ def run_gpu_arm(args):
     simt_main = big["plan"].describe().startswith("simt")
     peak = pk["f32_simt_tflops_nominal"] if simt_main else pk["f32_3xtf32_tflops_burst"]
     kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", f)
-                             for f in ("tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "dispatch_table.inc")])
+                             for f in ("tc_kernels.cuh", "tc_common.cuh", "ptx.cuh", "dispatch_table.inc")])
     traffic, traffic_src = traffic_for(kern_hash)
     for w in work:
         t = traffic.get(w["name"]) if traffic else None

@@ -110,7 +110,11 @@ typedef struct {
                                raster group (1..64; 0 = the dispatcher's choice, else 8) */
     int32_t tile_k;         /* SIMT only: K-tile depth (16/32/64; 0 = the compiled default
                                for the tile and stage count) */
-    int32_t reserved[3];
+    int32_t host_panels;    /* TC only, gemm_f32_run_host: row panels the host-buffer run is
+                               pipelined over (A panel copies, panel GEMMs and C panel
+                               copies overlap); 0 = the dispatcher's choice, 1 = none,
+                               n = n panels of whole 128-row tiles (at most 64) */
+    int32_t reserved[2];
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */
@@ -171,8 +175,12 @@ GEMM_F32_API gemm_f32_status gemm_f32_run(gemm_f32_plan_t plan, const float* A, 
  * C = A*B with HOST operands: copies A and B to device buffers the plan owns
  * (allocated on first use), runs, copies C back to host memory and
  * synchronises `stream`.  For pinned host memory the copies are asynchronous
- * DMA; pageable memory works but is slower.  Returns the run's status, or
- * TIMEOUT if a device-side wait ran out; UNSUPPORTED for a batched plan.
+ * DMA; pageable memory works but is slower.  Tensor-core plans with enough
+ * tiles run as a pipeline over row panels of A and C: B is copied and split
+ * once, then each panel's GEMM overlaps the next panel's A copy and the
+ * previous panel's C copy (two internal streams, ordered by events after
+ * `stream`'s earlier work).  Returns the run's status, or TIMEOUT if a
+ * device-side wait ran out; UNSUPPORTED for a batched plan.
  */
 GEMM_F32_API gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t plan, const float* A_host,
                                   const float* B_host, float* C_host,

@@ -41,7 +41,8 @@ class Opts(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32), ("tf32_terms", ctypes.c_int32),
                 ("wait_timeout_cycles", ctypes.c_int64), ("debug_withhold_stage", ctypes.c_int32),
                 ("separate_syncs", ctypes.c_int32), ("operand_split", ctypes.c_int32),
-                ("tile_group", ctypes.c_int32), ("tile_k", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("tile_group", ctypes.c_int32), ("tile_k", ctypes.c_int32), ("host_panels", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lock = threading.Lock()
@@ -203,7 +204,8 @@ class Plan:
 
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, *, variant=VARIANT_AUTO, tile_m=0,
                  tile_n=0, stages=0, split_k=0, tf32_terms=0, wait_timeout_cycles=0,
-                 debug_withhold_stage=0, separate_syncs=0, operand_split=0, tile_group=0, tile_k=0, batch=None,
+                 debug_withhold_stage=0, separate_syncs=0, operand_split=0, tile_group=0, tile_k=0, host_panels=0,
+                 batch=None,
                  stride_a=0, stride_b=0, stride_c=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.lda = int(lda if lda is not None else max(K, 1))
@@ -217,6 +219,7 @@ class Plan:
         o.operand_split = operand_split
         o.tile_group = tile_group
         o.tile_k = tile_k
+        o.host_panels = host_panels
         if batch is None:
             s, h = gemm_f32_plan_ex(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, o)
         else:

@@ -65,6 +65,14 @@ struct gemm_f32_plan_s {
     // two internal streams so the copies of gemm_f32_run_host use two copy engines
     cudaStream_t xs[2] = {nullptr, nullptr};
     cudaEvent_t xev[3] = {nullptr, nullptr, nullptr};
+    // row panels of the pipelined gemm_f32_run_host (tensor-core plans): each
+    // panel's state and first row, their partial-tile scratch, and one event
+    // per landed operand (B, then every A panel) and per finished C panel
+    std::vector<TcPlanState> panels;
+    std::vector<int64_t> panel_r0;
+    float* panel_partial = nullptr;
+    int panel_count = 0;
+    std::vector<cudaEvent_t> pev;
     char desc[256] = {0};
     // tracing: 4 events per recorded run
     std::vector<cudaEvent_t> trace_ev;
@@ -110,6 +118,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.operand_split < 0 || o.operand_split > 4) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -125,22 +134,25 @@ int auto_split(int64_t tiles, int64_t K, int64_t min_k_per_split, int sms)
     return s < 1 ? 1 : (int)s;
 }
 
-DispatchChoice choose(int64_t M, int64_t N, int64_t K, int sms)
+// The rule for tensor-core plans outside the table: 128x256 tiles for big
+// products, 128x128 below; a K-split only when the tiles fill under half the SMs.
+DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int sms)
 {
     DispatchChoice c{};
-    if (table_lookup(M, N, K, c)) return c;
-    // Shapes outside the measured table: tensor cores once the product is big
-    // enough to amortise the operand split; SIMT below that.
-    const double macs = double(M) * double(N) * double(K);
-    if (macs >= 6.0e7 && K >= 32) {  // K >= kTcMinK with margin
-        c.variant = GEMM_F32_VARIANT_TCGEN05;
-        c.tile_m = 128;
-        c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
-        c.stages = 0;  // the depth compiled for that tile width
-        const int64_t tiles = ((M + 127) / 128) * ((N + c.tile_n - 1) / c.tile_n);
-        c.split_k = tiles >= sms / 2 ? 0 : auto_split(tiles, K, 256, sms);
-        return c;
-    }
+    c.variant = GEMM_F32_VARIANT_TCGEN05;
+    c.tile_m = 128;
+    c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
+    c.stages = 0;  // the depth compiled for that tile width
+    const int64_t tiles = ((M + 127) / 128) * ((N + c.tile_n - 1) / c.tile_n);
+    c.split_k = tiles >= sms / 2 ? 0 : auto_split(tiles, K, 256, sms);
+    return c;
+}
+
+// The rule for SIMT plans outside the table: the largest square tile that
+// still gives every SM work, two stages, K-split to fill the SMs.
+DispatchChoice choose_simt(int64_t M, int64_t N, int64_t K, int sms)
+{
+    DispatchChoice c{};
     c.variant = GEMM_F32_VARIANT_SIMT;
     c.stages = 2;
     const int64_t t128 = ((M + 127) / 128) * ((N + 127) / 128);
@@ -151,6 +163,17 @@ DispatchChoice choose(int64_t M, int64_t N, int64_t K, int sms)
     const int64_t tiles = ((M + c.tile_m - 1) / c.tile_m) * ((N + c.tile_n - 1) / c.tile_n);
     c.split_k = auto_split(tiles, K, 64, sms);
     return c;
+}
+
+DispatchChoice choose(int64_t M, int64_t N, int64_t K, int sms)
+{
+    DispatchChoice c{};
+    if (table_lookup(M, N, K, c)) return c;
+    // Shapes outside the measured table: tensor cores once the product is big
+    // enough to amortise the operand split; SIMT below that.
+    const double macs = double(M) * double(N) * double(K);
+    if (macs >= 6.0e7 && K >= 32) return choose_tc(M, N, K, sms);  // K >= kTcMinK with margin
+    return choose_simt(M, N, K, sms);
 }
 
 gemm_f32_status device_check(int* dev, int* sms)
@@ -208,14 +231,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         DispatchChoice c = choose(M, N, K, p->num_sms);
         if (o.variant != GEMM_F32_VARIANT_AUTO && o.variant != c.variant) {
             // A forced variant starts from that variant's own rule.
-            c.variant = o.variant;
-            if (c.variant == GEMM_F32_VARIANT_SIMT) {
-                c.tile_m = c.tile_n = 64; c.stages = 2; c.split_k = 1;
-            } else {
-                c.tile_m = 128; c.tile_n = 128; c.stages = 0;
-                const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
-                c.split_k = tiles >= p->num_sms / 2 ? 0 : auto_split(tiles, K, 256, p->num_sms);
-            }
+            c = o.variant == GEMM_F32_VARIANT_SIMT ? choose_simt(M, N, K, p->num_sms)
+                                                   : choose_tc(M, N, K, p->num_sms);
         }
         // A forced tile or ring replaces the choice, so the table's K-tile depth
         // and tile order (tuned for its own tile) no longer apply.
@@ -342,6 +359,123 @@ bool current_device_is(int dev)
 {
     int d = -1;
     return cudaGetDevice(&d) == cudaSuccess && d == dev;
+}
+
+// Row panels of the pipelined host-buffer run: the option's count, else a
+// count from the waves of output tiles (measured on GB300 with pinned host
+// memory at about 200 GB/s each way: 8192^3, 13 waves, is fastest with 6
+// panels; 4096^3, 3.4 waves, with 3); never more panels than tile-rows.
+// 1 = the plain copy-run-copy sequence.
+int host_panel_count(const gemm_f32_plan_s* p)
+{
+    if (p->kind != kTc || p->K == 0) return 1;
+    int n = p->opts.host_panels;
+    if (n == 0) {
+        const int64_t waves = int64_t(p->tc.tiles_m) * p->tc.tiles_n / (p->num_sms > 0 ? p->num_sms : 1);
+        n = waves >= 8 ? 6 : waves >= 2 ? 3 : waves >= 1 ? 2 : 1;
+    }
+    if (n > p->tc.tiles_m) n = p->tc.tiles_m;
+    return n < 1 ? 1 : n;
+}
+
+void drop_panels(gemm_f32_plan_s* p)
+{
+    p->panels.clear();
+    p->panel_r0.clear();
+    p->panel_count = 0;
+    if (p->panel_partial) cudaFree(p->panel_partial);
+    p->panel_partial = nullptr;
+}
+
+// Panel states for `count` panels of whole 128-row tiles over the staging
+// buffers, their partial-tile scratch and events; kept until the count changes.
+cudaError_t make_panels(gemm_f32_plan_s* p, int count)
+{
+    if (!p->panels.empty() && p->panel_count == count) return cudaSuccess;
+    drop_panels(p);
+    const int64_t rows = round_up((p->M + count - 1) / count, 128);
+    size_t need = 0;
+    cudaError_t e = cudaSuccess;
+    for (int64_t r0 = 0; r0 < p->M; r0 += rows) {
+        const int64_t mp = p->M - r0 < rows ? p->M - r0 : rows;
+        TcPlanState ps;
+        if ((e = tc_panel_prepare(p->tc, r0, mp, p->N, p->K, p->hA, p->lda, p->hB, p->ldb, ps)) != cudaSuccess) {
+            drop_panels(p);
+            return e;
+        }
+        if (ps.partial_bytes > need) need = ps.partial_bytes;
+        p->panels.push_back(ps);
+        p->panel_r0.push_back(r0);
+    }
+    if (need && (e = cudaMalloc(&p->panel_partial, need)) != cudaSuccess) {
+        p->panel_partial = nullptr;
+        drop_panels(p);
+        return e;
+    }
+    for (TcPlanState& ps : p->panels) ps.partial = p->panel_partial;
+    while (e == cudaSuccess && p->pev.size() < 1 + 2 * p->panels.size()) {
+        cudaEvent_t x = nullptr;
+        e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+        if (e == cudaSuccess) p->pev.push_back(x);
+    }
+    if (e != cudaSuccess) drop_panels(p);
+    else p->panel_count = count;
+    return e;
+}
+
+// The panel pipeline.  Stream xs[0] copies B, then every A panel, each
+// followed by an event; the caller's stream splits B once and runs each
+// panel's pre-pass, GEMM and reduction after its A panel has landed; stream
+// xs[1] copies each C panel back once it is done.  So panel i's GEMM overlaps
+// the copy of A panel i+1 and of C panel i-1.
+cudaError_t run_host_panels(gemm_f32_plan_s* p, const float* A_host, const float* B_host, float* C_host,
+                            cudaStream_t s)
+{
+    const size_t np = p->panels.size();
+    cudaEvent_t ev_b = p->pev[0];
+    const cudaEvent_t* ev_a = &p->pev[1];
+    const cudaEvent_t* ev_c = &p->pev[1 + np];
+    cudaError_t e;
+    // both copy streams start after the caller's earlier work
+    if ((e = cudaEventRecord(p->xev[0], s)) != cudaSuccess) return e;
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaStreamWaitEvent(p->xs[i], p->xev[0], 0)) != cudaSuccess) return e;
+    // host -> device: B, then the A panels
+    if ((e = copy_rows(p->hB, B_host, p->K, p->N, p->ldb, cudaMemcpyHostToDevice, p->xs[0])) != cudaSuccess ||
+        (e = cudaEventRecord(ev_b, p->xs[0])) != cudaSuccess)
+        return e;
+    for (size_t i = 0; i < np; ++i) {
+        const int64_t r0 = p->panel_r0[i];
+        const int64_t mp = (i + 1 < np ? p->panel_r0[i + 1] : p->M) - r0;
+        if ((e = copy_rows(p->hA + r0 * p->lda, A_host + r0 * p->lda, mp, p->K, p->lda, cudaMemcpyHostToDevice,
+                           p->xs[0])) != cudaSuccess ||
+            (e = cudaEventRecord(ev_a[i], p->xs[0])) != cudaSuccess)
+            return e;
+    }
+    // compute: B's split once, then panel by panel
+    if ((e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess ||
+        (e = tc_split_b(p->tc, p->N, p->K, p->hA, p->hB, p->ldb, s)) != cudaSuccess)
+        return e;
+    for (size_t i = 0; i < np; ++i) {
+        const int64_t r0 = p->panel_r0[i];
+        const int64_t mp = (i + 1 < np ? p->panel_r0[i + 1] : p->M) - r0;
+        if ((e = cudaStreamWaitEvent(s, ev_a[i], 0)) != cudaSuccess ||
+            (e = tc_panel_run(p->panels[i], mp, p->N, p->K, p->hA + r0 * p->lda, p->lda, p->hB, p->ldb,
+                              p->hC + r0 * p->ldc, p->ldc, p->d_status, s)) != cudaSuccess ||
+            (e = cudaEventRecord(ev_c[i], s)) != cudaSuccess)
+            return e;
+    }
+    // device -> host: each C panel when it is done; the caller's stream joins
+    for (size_t i = 0; i < np; ++i) {
+        const int64_t r0 = p->panel_r0[i];
+        const int64_t mp = (i + 1 < np ? p->panel_r0[i + 1] : p->M) - r0;
+        if ((e = cudaStreamWaitEvent(p->xs[1], ev_c[i], 0)) != cudaSuccess ||
+            (e = copy_rows(C_host + r0 * p->ldc, p->hC + r0 * p->ldc, mp, p->N, p->ldc, cudaMemcpyDeviceToHost,
+                           p->xs[1])) != cudaSuccess)
+            return e;
+    }
+    if ((e = cudaEventRecord(p->xev[2], p->xs[1])) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(s, p->xev[2], 0);
 }
 
 }  // namespace
@@ -472,6 +606,11 @@ gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t p, const float* A_host, const 
         for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&p->xev[i], cudaEventDisableTiming);
         if (e != cudaSuccess) return from_cuda(e);
     }
+    if (const int panels = host_panel_count(p); panels > 1) {
+        if ((e = make_panels(p, panels)) != cudaSuccess || (e = run_host_panels(p, A_host, B_host, C_host, s)) != cudaSuccess)
+            return from_cuda(e);
+        return gemm_f32_check(p, stream);
+    }
     {
         // Each matrix is copied as two row halves on the two internal streams
         // (two copy engines at once); the caller's stream waits for both.
@@ -515,6 +654,7 @@ fail:
     cudaGetLastError();
     cudaFree(p->hA); cudaFree(p->hB); cudaFree(p->hC);
     p->hA = p->hB = p->hC = nullptr;
+    drop_panels(p);
     return from_cuda(e);
 }
 
@@ -548,6 +688,8 @@ void gemm_f32_plan_destroy(gemm_f32_plan_t p)
         if (x) cudaStreamDestroy(x);
     for (cudaEvent_t x : p->xev)
         if (x) cudaEventDestroy(x);
+    drop_panels(p);
+    for (cudaEvent_t x : p->pev) cudaEventDestroy(x);
     delete p;
 }
 

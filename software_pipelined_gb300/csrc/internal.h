@@ -111,6 +111,7 @@ struct TcPlanState {
     int64_t timeout_cycles = 0;
     int withhold_stage = 0;
     int tile_group = 0;        // tile-rows per raster group (0 = default)
+    int split_request = 0;     // the split policy tc_configure was given
     // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.
@@ -126,6 +127,19 @@ struct TcPlanState {
 void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_request);
 // Allocates nothing: encodes tensor maps over already-allocated split buffers.
 cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K);
+// Row panels of a plan, for the pipelined host-buffer path: `out` becomes the
+// plan's state re-configured for rows [r0, r0 + mp) of A and C (A, B: the
+// device buffers the panels read); its partial-tile buffer is left NULL for
+// the caller to provide (out.partial_bytes long).
+cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, int64_t N, int64_t K,
+                             const float* A, int64_t lda, const float* B, int64_t ldb, TcPlanState& out);
+// The B part of the pre-pass for the whole plan (when its route needs it).
+cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const float* A, const float* B,
+                       int64_t ldb, cudaStream_t s);
+// One panel: its A rows' pre-pass (when needed), the GEMM, the reduction.
+cudaError_t tc_panel_run(const TcPlanState& panel, int64_t mp, int64_t N, int64_t K, const float* A_panel,
+                         int64_t lda, const float* B, int64_t ldb, float* C_panel, int64_t ldc, int* status,
+                         cudaStream_t s);
 // ev: NULL, or four events recorded before the split, before the main kernel,
 // after the main kernel and after the split-K reduction.
 cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K,

@@ -397,6 +397,76 @@ def test_run_host_buffers(shape, pad):
 
 
 # ---------------------------------------------------------------------------
+# The pipelined host-buffer run: row panels of whole 128-row tiles, B copied
+# and split once, each panel's A copy / GEMM / C copy overlapped on three
+# streams.  Every operand mode, ragged panels, padded leading dimensions,
+# pinned host memory, repeated runs (the panel states are kept).
+# ---------------------------------------------------------------------------
+
+def _pinned(host, ld):
+    import torch
+    rows, cols = host.shape
+    t = torch.full((rows, ld), 321.0, dtype=torch.float32).pin_memory()
+    t[:, :cols] = torch.from_numpy(host)
+    return t
+
+
+@pytest.mark.parametrize("panels", [2, 3, 7])
+@pytest.mark.parametrize("mode", [1, 2, 3, 4], ids=["pre_pass", "in_kernel", "hybrid", "raw_a"])
+def test_run_host_panels(mode, panels):
+    M, N, K = 1000, 520, 264
+    lda, ldb, ldc = K + 4, N + 8, N + 3
+    A = inputs.uniform_pm1(1711, M, K)
+    B = inputs.uniform_pm1(1712, K, N)
+    hA, hB = _pinned(A, lda), _pinned(B, ldb)
+    hC = _pinned(np.full((M, N), np.nan, dtype=np.float32), ldc)
+    with g.Plan(M, N, K, lda, ldb, ldc, variant=g.VARIANT_TCGEN05, operand_split=mode,
+                host_panels=panels) as p:
+        for _ in range(2):
+            hC[:, :N] = float("nan")
+            s = p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0)
+            assert s == g.OK, g.gemm_f32_status_string(s)
+            C = hC.numpy()
+            Cref, S = oracle.gemm_f64(A, B)
+            assert oracle.within_bound(C[:, :N], Cref, S, K), p.describe()
+            assert (C[:, N:] == 321.0).all()
+
+
+@pytest.mark.parametrize("mode", [1, 4], ids=["pre_pass", "raw_a"])
+def test_run_host_panels_bit_identical_to_device_run(mode):
+    # With no K-split every output tile is summed in the same order whichever
+    # panel it falls in, so the panel pipeline must reproduce the one-launch
+    # device run bit for bit (a wrong panel offset cannot hide in the bound).
+    import torch
+    M, N, K = 1536, 640, 192
+    A = inputs.normal(1713, M, K)
+    B = inputs.normal(1714, K, N)
+    hA, hB = _pinned(A, K), _pinned(B, N)
+    hC = _pinned(np.zeros((M, N), dtype=np.float32), N)
+    opts = dict(variant=g.VARIANT_TCGEN05, operand_split=mode, split_k=1)
+    with g.Plan(M, N, K, host_panels=4, **opts) as p:
+        assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
+    C, desc, canaries, _ = run_gemm(A, B, host_panels=1, **opts)
+    assert canaries
+    assert np.array_equal(hC.numpy().astype(np.float64), C), desc
+
+
+def test_run_host_panel_option_validation():
+    for bad in (-1, 65):
+        with pytest.raises(g.GemmError):
+            g.Plan(256, 256, 256, variant=g.VARIANT_TCGEN05, host_panels=bad)
+    # more panels than tile-rows: clamped to one panel per tile-row
+    M, N, K = 200, 64, 64
+    A = inputs.uniform_pm1(1715, M, K)
+    B = inputs.uniform_pm1(1716, K, N)
+    C = np.full((M, N), np.nan, dtype=np.float32)
+    with g.Plan(M, N, K, variant=g.VARIANT_TCGEN05, host_panels=64) as p:
+        assert p.run_host(A.ctypes.data, B.ctypes.data, C.ctypes.data, 0) == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(C, Cref, S, K)
+
+
+# ---------------------------------------------------------------------------
 # Extreme aspect ratios: a very long K (many k-blocks per tile, long
 # accumulation) and a very tall, thin product.
 # ---------------------------------------------------------------------------
