@@ -114,7 +114,14 @@ typedef struct {
                                pipelined over (A panel copies, panel GEMMs and C panel
                                copies overlap); 0 = the dispatcher's choice, 1 = none,
                                n = n panels of whole 128-row tiles (at most 64) */
-    int32_t reserved[2];
+    int32_t split_reduce;   /* TC only: how the K-slices of split tiles are summed.  0 = the
+                               dispatcher's choice (the reduction kernel: measured faster);
+                               1 = a reduction kernel over partial tiles in scratch; 2 = the
+                               slices of a tile run as one cluster of 2, 4 or 8 CTAs and sum
+                               in distributed shared memory (needs every tile split, all
+                               slices resident at once, a ring of depth >= 2; else
+                               UNSUPPORTED) */
+    int32_t reserved[1];
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

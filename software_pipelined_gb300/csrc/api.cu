@@ -119,6 +119,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.split_reduce < 0 || o.split_reduce > 2) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -289,7 +290,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             t.timeout_cycles = o.wait_timeout_cycles;
             t.withhold_stage = o.debug_withhold_stage;
             t.tile_group = o.tile_group ? o.tile_group : c.group;
+            t.cluster_mode = o.split_reduce;
             tc_configure(t, M, N, K, c.split_k);
+            if (o.split_reduce == 2 && t.cluster == 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             ahi_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             alo_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             bhi_off = bytes; bytes += align256(size_t(N) * size_t(t.kp) * sizeof(float));
@@ -299,14 +302,14 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 bytes += align256(t.partial_bytes);
             }
             snprintf(p->desc, sizeof p->desc,
-                     "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d kp=%lld",
+                     "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d%s kp=%lld",
                      tcfg.split == kSplitInKernel ? " in-kernel-split"
                      : tcfg.split == kSplitHybrid ? " hybrid-split"
                      : tcfg.split == kSplitRawA ? " raw-a-split" : "",
                      t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
                      tcfg.sep ? " separate-syncs" : "",
                      t.tiles_m * t.tiles_n, t.dp_tiles,
-                     t.split_tiles, t.splits, (long long)t.kp);
+                     t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", (long long)t.kp);
         }
     }
 
@@ -412,7 +415,12 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
         drop_panels(p);
         return e;
     }
-    for (TcPlanState& ps : p->panels) ps.partial = p->panel_partial;
+    for (TcPlanState& ps : p->panels)
+        if (e == cudaSuccess) e = tc_set_partial(ps, p->panel_partial);
+    if (e != cudaSuccess) {
+        drop_panels(p);
+        return e;
+    }
     while (e == cudaSuccess && p->pev.size() < 1 + 2 * p->panels.size()) {
         cudaEvent_t x = nullptr;
         e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
@@ -712,7 +720,7 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
         // the pre-pass (unless both operands are split in the kernel), the GEMM,
         // and the reduction of split tiles
         const int split = tc_config(p->tc.config_id).split;
-        return (split == kSplitInKernel ? 1 : 2) + (p->tc.split_tiles > 0 ? 1 : 0);
+        return (split == kSplitInKernel ? 1 : 2) + (p->tc.split_tiles > 0 && !p->tc.cluster ? 1 : 0);
     }
     default: return 0;
     }

@@ -112,6 +112,8 @@ struct TcPlanState {
     int withhold_stage = 0;
     int tile_group = 0;        // tile-rows per raster group (0 = default)
     int split_request = 0;     // the split policy tc_configure was given
+    int cluster_mode = 0;      // K-slice sums: 2 = in a cluster where possible, else the reduction kernel
+    int cluster = 0;           // > 1: slices per tile, summed in a thread-block cluster
     // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.
@@ -120,13 +122,24 @@ struct TcPlanState {
     mutable const float* raw_b = nullptr;
     alignas(64) mutable unsigned char tmap_a_raw[128];
     alignas(64) mutable unsigned char tmap_b_raw[128];
+    // TMA-store maps: the partial-tile buffer (set with tc_set_partial) and the
+    // caller's C (re-encoded when C moves; c_tma = 0 when C cannot take TMA
+    // stores: base not 16-byte aligned, or ldc or N not a multiple of 4)
+    alignas(64) unsigned char tmap_p[128];
+    alignas(64) mutable unsigned char tmap_c[128];
+    mutable float* c_ptr = nullptr;
+    mutable int c_tma = 0;
 };
 // Work decomposition for config t.config_id: split_request 0 = automatic
 // (split the tiles of a partial last wave), 1 = none, >= 2 = every tile in that
 // many K-slices.  Sets kp, tiles, dp/split tiles, splits and partial_bytes.
 void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_request);
-// Allocates nothing: encodes tensor maps over already-allocated split buffers.
+// Allocates nothing: encodes tensor maps over already-allocated split buffers
+// (and over st.partial when set).
 cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K);
+// Point the state's split units at `partial` (partial_bytes long) and encode
+// the TMA-store map over it.
+cudaError_t tc_set_partial(TcPlanState& st, float* partial);
 // Row panels of a plan, for the pipelined host-buffer path: `out` becomes the
 // plan's state re-configured for rows [r0, r0 + mp) of A and C (A, B: the
 // device buffers the panels read); its partial-tile buffer is left NULL for

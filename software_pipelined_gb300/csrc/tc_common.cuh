@@ -37,6 +37,10 @@ struct TcArgs {
     int terms;           // 3 = 3xTF32, 1 = hi*hi only
     int withhold;        // test hook: 1-based fill index the producer skips (0 = none)
     int group;           // tile-rows per raster group of the tile order
+    int c_tma;           // 1: the C tensor map is valid (C 16-byte aligned, ldc % 4 == 0)
+    int cluster;         // > 1: every tile split in `cluster` K-slices, one CTA each, the
+                         // slices of a tile one thread-block cluster that sums them
+                         // through distributed shared memory (no partial tiles)
 };
 
 // One unit of work of the persistent kernel: a whole tile, or one K-slice of a
@@ -146,6 +150,24 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int64_
     }
 }
 
+// The same bounded wait on a barrier that other CTAs of the cluster arrive on
+// (acquire at cluster scope).
+__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, int64_t limit,
+                                                   volatile int* abort_flag, int* status)
+{
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            atomicExch(status, kStatusTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // Tile order: groups of G tile-rows, column-major inside a group, so the CTAs
 // running together share A and B panels in L2.
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int G, int& tm, int& tn)
@@ -206,11 +228,123 @@ __device__ __forceinline__ void store_accumulator(const TcArgs& args, const Unit
     }
 }
 
+// Epilogue through TMA stores, for a CTA's last unit (its operand ring is then
+// idle and serves as staging).  The calling warp owns TMEM lanes = tile rows
+// y0 .. y0+31 of the destination (C, or the partial-tile buffer) and the 8 KB
+// of staging at `stage` (two 4 KB boxes of 32 rows x 32 FP32 in the 128-byte
+// swizzled layout: 16-byte chunk q of row r at chunk q ^ (r % 8), so the 8
+// lanes of each store phase hit 8 different chunks).  Per 32 columns: two
+// TMEM loads, 8 conflict-free 16-byte shared stores per lane, one TMA store
+// of the box (clipped at the tensor's edge; boxes wholly past it are skipped).
+template <int BN>
+__device__ __forceinline__ void store_accumulator_tma(const CUtensorMap* map, int64_t x0, int64_t y0,
+                                                      int64_t xlim, int64_t ylim, uint32_t taddr, int lane,
+                                                      uint32_t stage, uint8_t* stage_ptr)
+{
+    // Only boxes that are stored are staged, so every staged box is one
+    // committed group and "at most one group still reading" below means the
+    // store of the box two back (the same buffer) is done with it.
+    const int cols = y0 < ylim ? (int)(xlim - x0 < BN ? xlim - x0 : BN) : 0;
+#pragma unroll 1
+    for (int c = 0; c < cols; c += 32) {
+        const int b = (c >> 5) & 1;
+        if (c >= 64) {
+            // box b was stored two boxes ago: its store must be done reading
+            if (lane == 0) ptx::bulk_wait_read<1>();
+            __syncwarp();
+        }
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r));
+        ptx::tmem_ld_32x32b_x16(taddr + c + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        ptx::tmem_wait_ld();
+        uint8_t* row = stage_ptr + b * 4096 + lane * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        ptx::fence_proxy_async_shared();  // generic-proxy writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+            ptx::tma_store_2d(map, stage + b * 4096, (int32_t)(x0 + c), (int32_t)y0);
+            ptx::bulk_commit();
+        }
+    }
+    if (lane == 0) ptx::bulk_wait_all();  // complete before the staging is reused or freed
+    __syncwarp();
+}
+
+// Epilogue of a K-sliced tile whose S = args.cluster slices are the S CTAs of
+// one cluster (rank z = slice z).  Rows are owned in blocks: rank r sums rows
+// r*128/S .. (r+1)*128/S - 1 of the tile.  Called by the 128 epilogue threads
+// (thread = TMEM lane = tile row) once this CTA's accumulator is complete.
+//   1. This CTA's MMAs are done, so its operand ring is idle: one thread
+//      arrives on every rank's `ready` barrier.
+//   2. Wait until all S rings are idle (`ready` complete: S arrivals).
+//   3. Each thread sends its row (BN FP32, from TMEM) into slice z's row of
+//      the owner's receive buffer, laid over the owner's idle ring
+//      ([S][128/S][BN + 4] FP32; the 4-float pad spreads the rows of a warp
+//      over the banks), then arrives on the owner's `recv` barrier.
+//   4. Wait for the 128 rows this CTA owns (`recv` complete: 128 arrivals),
+//      sum the S slices in slice order (the order of the reduction kernel, so
+//      the result is the same bit for bit) and store them to C.
+// Every wait is bounded; false means a wait gave up (status already set).  No
+// CTA leaves the kernel before the cluster barrier at its end, so no remote
+// access ever targets a CTA that has exited.
+template <int BN>
+__device__ bool cluster_reduce_store(const TcArgs& args, int tm, int tn, uint32_t taddr, int row,
+                                     uint32_t recv_addr, const float* recv_ptr, uint32_t ready_bar,
+                                     uint32_t recv_bar, int64_t limit, volatile int* abort_flag)
+{
+    constexpr int LD = BN + 4;
+    const int S = args.cluster;
+    const int rows_per = kBM / S;
+    const uint32_t z = ptx::cluster_ctarank();
+    if (row == 0)
+        for (int r = 0; r < S; ++r) ptx::mbar_arrive_cluster(ptx::mapa(ready_bar, (uint32_t)r));
+    // warp-uniform outcome: the TMEM loads below are warp-collective
+    if (!__all_sync(0xffffffffu, wait_phase_cluster(ready_bar, 0, limit, abort_flag, args.status))) return false;
+    const uint32_t owner = (uint32_t)(row / rows_per);
+    const uint32_t dst = ptx::mapa(recv_addr, owner) +
+                         (uint32_t)(((int)z * rows_per + row % rows_per) * LD) * 4u;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld_32x32b_x16(taddr + c, r);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+            ptx::st_cluster_v4(dst + (uint32_t)(c + j) * 4u, r[j], r[j + 1], r[j + 2], r[j + 3]);
+    }
+    ptx::mbar_arrive_cluster(ptx::mapa(recv_bar, owner));
+    if (!__all_sync(0xffffffffu, wait_phase_cluster(recv_bar, 0, limit, abort_flag, args.status))) return false;
+    const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
+    const int row0 = tm * kBM + (int)z * rows_per;
+    for (int idx = row; idx < rows_per * (BN / 4); idx += kBM) {
+        const int r = idx / (BN / 4), c4 = idx % (BN / 4);
+        float4 acc = *reinterpret_cast<const float4*>(recv_ptr + r * LD + 4 * c4);
+        for (int s = 1; s < S; ++s) {
+            const float4 t = *reinterpret_cast<const float4*>(recv_ptr + (s * rows_per + r) * LD + 4 * c4);
+            acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+        }
+        const int64_t grow = (int64_t)row0 + r, gcol = (int64_t)tn * BN + 4 * c4;
+        if (grow >= args.M) continue;
+        float* dst_c = args.C + grow * args.ldc + gcol;
+        if (vec && gcol + 3 < args.N) {
+            *reinterpret_cast<float4*>(dst_c) = acc;
+        } else {
+            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int q = 0; q < 4 && gcol + q < args.N; ++q) dst_c[q] = v[q];
+        }
+    }
+    return true;
+}
+
 // Launch with programmatic stream serialisation: the kernel may start while
 // the previous kernel on the stream finishes, and waits for it (griddepcontrol)
-// before touching that kernel's output.
+// before touching that kernel's output.  cluster > 1: thread-block clusters of
+// that many consecutive CTAs (the grid is a multiple of it).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
                        Args&&... args)
 {
     cudaLaunchConfig_t cfg = {};
@@ -218,11 +352,19 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {
+        if (grid.x % (unsigned)cluster != 0) return cudaErrorInvalidValue;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

@@ -52,7 +52,9 @@ struct FusedLayout {
     static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RAWB_BYTES = B_BYTES;              // BN/32 boxes of 32 k x 32 n
     static constexpr int RING_BYTES = SLOTS * SLOT_BYTES + RAWB * RAWB_BYTES;
-    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 5;  // + tmem full/empty x2, drain
+    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 7;  // + tmem full/empty x2, drain, ready, recv
+    // cluster K-slice reduction: the receive buffer laid over the idle ring
+    static constexpr bool CLUSTER_OK = kBM * (BN + 4) * 4 <= RING_BYTES;
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     static constexpr int SMEM_USED = 1024 + RING_BYTES + BAR_BYTES;
     static constexpr int SMEM_BYTES = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
@@ -60,6 +62,9 @@ struct FusedLayout {
     static_assert(BN % 32 == 0 && BN <= 256, "B arrives in 32-column boxes");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+
+template <int BN, int SLOTS, int RAWB>
+constexpr bool L_STAGING_FITS = FusedLayout<BN, SLOTS, RAWB>::RING_BYTES >= 4 * 8192;
 
 // Byte offset of element (row, k) in a K-major 128-byte-swizzled tile (rows of
 // 32 FP32 = 128 B, 8-row atoms of 1024 B, 16-byte chunk index XOR row % 8).
@@ -75,6 +80,7 @@ template <int BN, int SLOTS, int RAWB>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
+                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
                 const TcArgs args)
 {
     constexpr bool BPRE = RAWB == 0;
@@ -98,6 +104,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     auto tfull = [&](int b) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + b); };
     auto tempty = [&](int b) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 2 + b); };
     const uint32_t drain_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 4);
+    const uint32_t ready_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 5);
+    const uint32_t recv_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 6);
+    const bool clustered = L::CLUSTER_OK && args.cluster > 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
@@ -114,6 +123,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             ptx::mbar_init(tempty(b), 4);
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(ready_bar, clustered ? args.cluster : 1);
+        ptx::mbar_init(recv_bar, kBM);
         *abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -132,6 +143,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // the peers' barriers are initialised before any remote arrival
+    if (clustered) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     pdl_wait();  // the previous kernel on the stream may still be writing A or B
@@ -259,8 +272,23 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             const uint32_t tphase = (iter >> 1) & 1;
             if (!wait_phase(tfull(buf), tphase, limit, abort_flag, args.status)) break;
             ptx::tc_fence_after();
-            store_accumulator<BN>(args, u, tm, tn,
-                                  tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN, row_in_tile);
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
+            if (clustered) {
+                if (!cluster_reduce_store<BN>(args, tm, tn, taddr, row_in_tile, ring,
+                                              reinterpret_cast<const float*>(ring_ptr), ready_bar, recv_bar,
+                                              limit, abort_flag))
+                    break;
+            } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
+                // this CTA's last unit: the ring is idle, stage and store by TMA
+                if (u.slot < 0)
+                    store_accumulator_tma<BN>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
+                                              args.M, taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+                else
+                    store_accumulator_tma<BN>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
+                                              taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+            } else {
+                store_accumulator<BN>(args, u, tm, tn, taddr, row_in_tile);
+            }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty(buf));
@@ -331,6 +359,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 
     ptx::tc_fence_before();
     __syncthreads();
+    // no CTA of the cluster leaves while a peer may still reach its shared memory
+    if (clustered) ptx::cluster_sync();
     pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();
@@ -342,13 +372,17 @@ template <int BN, int SLOTS, int RAWB>
 cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
 {
+    static_assert(L_STAGING_FITS<BN, SLOTS, RAWB>, "the ring holds the TMA-store staging");
     using L = FusedLayout<BN, SLOTS, RAWB>;
     auto kern = tc_fused_kernel<BN, SLOTS, RAWB>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
-    return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, ta, tb, tbhi, tblo, a);
+    if (a.cluster > 1 && !L::CLUSTER_OK) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, a.cluster, ta, tb, tbhi, tblo,
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
 }
 
 }  // namespace

@@ -55,6 +55,22 @@ cudaError_t encode_kmajor(void* out, float* base, int64_t rows, int64_t kp, int 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Row-major FP32 matrix (rows x cols, leading dimension ld) as the target of
+// TMA stores of 32 x 32 boxes in the 128-byte swizzled layout.
+cudaError_t encode_store_map(void* out, float* base, int64_t rows, int64_t cols, int64_t ld)
+{
+    EncodeFn enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int grid_cap(int64_t work, int sms)
 {
     const int64_t blocks = (work + 255) / 256;
@@ -104,18 +120,22 @@ cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, const void* tmap
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::SMEM_BYTES, s,
+    static_assert(L::RING_BYTES >= 4 * 8192, "the ring holds the TMA-store staging");
+    if (a.cluster > 1 && !L::CLUSTER_OK) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::SMEM_BYTES, s, a.cluster,
                       *reinterpret_cast<const CUtensorMap*>(tmap_a_hi),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_a_lo),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
-                      *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), a);
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
 }
 
 template <int BN>
 cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
 {
     const int64_t total = (int64_t)a.split_tiles * kBM * (BN / 4);
-    return launch_pdl(tile_reduce_kernel<BN>, dim3(grid_cap(total, st.num_sms)), dim3(256), 0, s,
+    return launch_pdl(tile_reduce_kernel<BN>, dim3(grid_cap(total, st.num_sms)), dim3(256), 0, s, 1,
                       reinterpret_cast<const float4*>(a.partial), a.dp_tiles, a.split_tiles, a.splits,
                       a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
 }
@@ -126,29 +146,33 @@ struct TcEntry {
     TcConfig cfg;
     MainFn main;      // NULL where the split happens in the kernel (tc_fused_main)
     LaunchFn reduce;
+    bool cluster_ok;  // the ring can hold the cluster reduction's receive buffer
 };
+template <int BN, int STAGES>
+constexpr bool kClusterOk = TcLayout<BN, STAGES>::CLUSTER_OK;
 const TcEntry kTc[] = {
     // the ring as deep as shared memory allows, per tile width
-    {{128, 128, 32, 3, false, kSplitPrepass}, launch_main<128, 3>, launch_reduce<128>},
-    {{128, 256, 32, 2, false, kSplitPrepass}, launch_main<256, 2>, launch_reduce<256>},
-    {{128, 64, 32, 4, false, kSplitPrepass}, launch_main<64, 4>, launch_reduce<64>},
+    {{128, 128, 32, 3, false, kSplitPrepass}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>},
+    {{128, 256, 32, 2, false, kSplitPrepass}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>},
+    {{128, 64, 32, 4, false, kSplitPrepass}, launch_main<64, 4>, launch_reduce<64>, kClusterOk<64, 4>},
     // pipeline-depth ablation: single-buffered (1) and shallower rings
-    {{128, 256, 32, 1, false, kSplitPrepass}, launch_main<256, 1>, launch_reduce<256>},
-    {{128, 128, 32, 1, false, kSplitPrepass}, launch_main<128, 1>, launch_reduce<128>},
-    {{128, 128, 32, 2, false, kSplitPrepass}, launch_main<128, 2>, launch_reduce<128>},
-    {{128, 64, 32, 2, false, kSplitPrepass}, launch_main<64, 2>, launch_reduce<64>},
+    {{128, 256, 32, 1, false, kSplitPrepass}, launch_main<256, 1>, launch_reduce<256>, kClusterOk<256, 1>},
+    {{128, 128, 32, 1, false, kSplitPrepass}, launch_main<128, 1>, launch_reduce<128>, kClusterOk<128, 1>},
+    {{128, 128, 32, 2, false, kSplitPrepass}, launch_main<128, 2>, launch_reduce<128>, kClusterOk<128, 2>},
+    {{128, 64, 32, 2, false, kSplitPrepass}, launch_main<64, 2>, launch_reduce<64>, kClusterOk<64, 2>},
     // barrier-coalescing ablation: separate full barriers for A and B
-    {{128, 256, 32, 2, true, kSplitPrepass}, launch_main<256, 2, true>, launch_reduce<256>},
-    {{128, 128, 32, 3, true, kSplitPrepass}, launch_main<128, 3, true>, launch_reduce<128>},
-    // operands split inside the kernel (stages = MMA-facing slots)
-    {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>},
-    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>},
+    {{128, 256, 32, 2, true, kSplitPrepass}, launch_main<256, 2, true>, launch_reduce<256>, kClusterOk<256, 2>},
+    {{128, 128, 32, 3, true, kSplitPrepass}, launch_main<128, 3, true>, launch_reduce<128>, kClusterOk<128, 3>},
+    // operands split inside the kernel (stages = MMA-facing slots; the fused
+    // kernel's rings of 3 x 64 KB and 2 x 96 KB hold the receive buffer)
+    {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>, true},
+    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>, true},
     // A split inside the kernel, B by the pre-pass
-    {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>},
-    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>},
+    {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>, true},
+    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>, true},
     // hi of A read from the caller's A, lo of A and both pieces of B by the pre-pass
-    {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>},
-    {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>},
+    {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>},
+    {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>},
 };
 
 }  // namespace
@@ -213,7 +237,24 @@ void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_req
         }
     }
     if (t.split_tiles == 0) t.kb_per_split = num_kb;
-    t.partial_bytes = t.split_tiles ? size_t(t.split_tiles) * t.splits * kBM * c.bn * sizeof(float) : 0;
+    // Every tile in 2, 4 or 8 slices, one CTA per slice, all at once: the
+    // slices of a tile can run as one thread-block cluster that sums them in
+    // distributed shared memory (no partial tiles, no reduction launch).
+    t.cluster = 0;
+    const bool cluster_fits = kTc[t.config_id].cluster_ok && t.dp_tiles == 0 && t.split_tiles > 0 &&
+                              (t.splits == 2 || t.splits == 4 || t.splits == 8) &&
+                              t.split_tiles * t.splits <= sms;
+    if (cluster_fits && t.cluster_mode == 2) t.cluster = t.splits;
+    t.partial_bytes = t.split_tiles && !t.cluster ? size_t(t.split_tiles) * t.splits * kBM * c.bn * sizeof(float)
+                                                  : 0;
+}
+
+cudaError_t tc_set_partial(TcPlanState& st, float* partial)
+{
+    st.partial = partial;
+    if (!partial || st.partial_bytes == 0) return cudaSuccess;
+    const int64_t bn = kTc[st.config_id].cfg.bn;
+    return encode_store_map(st.tmap_p, partial, (int64_t)(st.partial_bytes / (bn * sizeof(float))), bn, bn);
 }
 
 cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K)
@@ -221,6 +262,7 @@ cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K)
     (void)K;
     const TcConfig& c = kTc[st.config_id].cfg;
     cudaError_t e;
+    if ((e = tc_set_partial(st, st.partial)) != cudaSuccess) return e;
     if ((e = encode_kmajor(st.tmap_a_hi, st.a_hi, M, st.kp, kBM)) != cudaSuccess) return e;
     if ((e = encode_kmajor(st.tmap_a_lo, st.a_lo, M, st.kp, kBM)) != cudaSuccess) return e;
     if ((e = encode_kmajor(st.tmap_b_hi, st.b_hi, N, st.kp, c.bn)) != cudaSuccess) return e;
@@ -255,6 +297,22 @@ Route route(const TcPlanState& st, const float* A, const float* B)
     return r;
 }
 
+// The TMA-store map over C, re-encoded when C moves; C's base must be 16-byte
+// aligned and ldc and N multiples of 4, else the kernels store C directly.
+// (N: a store clipped at the right edge of C was measured to write the whole
+// 16-byte chunk holding the last column, i.e. into ldc's padding.)
+void prepare_c_map(const TcPlanState& st, float* C, int64_t M, int64_t N, int64_t ldc)
+{
+    if (reinterpret_cast<uintptr_t>(C) % 16 != 0 || ldc % 4 != 0 || N % 4 != 0) {
+        st.c_tma = 0;
+        return;
+    }
+    if (C != st.c_ptr || !st.c_tma) {
+        st.c_tma = encode_store_map(st.tmap_c, C, M, N, ldc) == cudaSuccess ? 1 : 0;
+        st.c_ptr = C;
+    }
+}
+
 TcArgs make_args(const TcPlanState& st, int64_t M, int64_t N, float* C, int64_t ldc, int* status)
 {
     TcArgs a{};
@@ -271,6 +329,9 @@ TcArgs make_args(const TcPlanState& st, int64_t M, int64_t N, float* C, int64_t 
     a.terms = st.terms;
     a.withhold = st.withhold_stage;
     a.group = st.tile_group > 0 ? st.tile_group : 8;
+    a.cluster = st.cluster;
+    prepare_c_map(st, C, M, N, ldc);
+    a.c_tma = st.c_tma;
     return a;
 }
 
@@ -298,6 +359,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
                             cudaStream_t s)
 {
     const TcConfig& c = kTc[st.config_id].cfg;
+    if (a.cluster > 1 && !kTc[r.id].cluster_ok) return cudaErrorInvalidValue;
     cudaError_t e;
     if (r.in_kernel) {
         e = tc_fused_main(c.bn, c.split == kSplitHybrid, st, a,
@@ -310,7 +372,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     }
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);
-    if (st.split_tiles > 0) e = kTc[r.id].reduce(st, a, s);
+    if (st.split_tiles > 0 && a.cluster <= 1) e = kTc[r.id].reduce(st, a, s);
     if (ev) cudaEventRecord(ev[3], s);
     return e;
 }
@@ -348,6 +410,8 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     out = full;
     tc_configure(out, mp, N, K, full.split_request);
     out.partial = nullptr;
+    out.c_ptr = nullptr;
+    out.c_tma = 0;
     out.a_hi = full.a_hi + r0 * full.kp;
     out.a_lo = full.a_lo + r0 * full.kp;
     cudaError_t e;

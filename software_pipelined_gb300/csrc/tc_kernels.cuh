@@ -154,7 +154,9 @@ struct TcLayout {
     static constexpr int B_BYTES = BN * kBK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int NBARS = 3 * STAGES + 5;    // full, empty, tmem x4, drain, full_b
+    // cluster K-slice reduction: the receive buffer laid over the idle ring
+    static constexpr bool CLUSTER_OK = kBM * (BN + 4) * 4 <= RING_BYTES;
+    static constexpr int NBARS = 3 * STAGES + 7;    // full, empty, tmem x4, drain, full_b, ready, recv
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     // At least 116 KB, so that two CTAs never share an SM (each holds up to
     // all 512 TMEM columns for its whole lifetime).
@@ -173,6 +175,7 @@ template <int BN, int STAGES, bool SEP>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
                const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
+               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
                const TcArgs args)
 {
     using L = TcLayout<BN, STAGES>;
@@ -184,7 +187,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + L::RING_BYTES);
     // bars[0..S-1] full (A and B, or A only when SEP), [S..2S-1] empty,
     // [2S..2S+1] tmem_full, [2S+2..2S+3] tmem_empty, [2S+4] drain,
-    // [2S+5..3S+4] full_b (SEP); then the TMEM base address slot and the abort flag.
+    // [2S+5..3S+4] full_b (SEP), [3S+5] ready, [3S+6] recv (cluster reduction);
+    // then the TMEM base address slot and the abort flag.
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -196,6 +200,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     auto tempty_bar = [&](int b) { return ptx::smem_u32(bars + 2 * STAGES + 2 + b); };
     const uint32_t drain_bar = ptx::smem_u32(bars + 2 * STAGES + 4);
     auto fullb_bar = [&](int s) { return ptx::smem_u32(bars + (SEP ? 2 * STAGES + 5 + s : s)); };
+    const uint32_t ready_bar = ptx::smem_u32(bars + 3 * STAGES + 5);
+    const uint32_t recv_bar = ptx::smem_u32(bars + 3 * STAGES + 6);
+    const bool clustered = L::CLUSTER_OK && args.cluster > 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -209,6 +216,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
         ptx::mbar_init(drain_bar, 1);
         if (SEP)
             for (int s = 0; s < STAGES; ++s) ptx::mbar_init(fullb_bar(s), 1);
+        ptx::mbar_init(ready_bar, clustered ? args.cluster : 1);
+        ptx::mbar_init(recv_bar, kBM);
         *abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -224,6 +233,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // the peers' barriers are initialised before any remote arrival
+    if (clustered) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // Everything above overlaps the split pre-pass; its outputs are read only
@@ -352,8 +363,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             const uint32_t tphase = (iter >> 1) & 1;
             if (!wait_phase(tfull_bar(buf), tphase, limit, abort_flag, args.status)) break;
             ptx::tc_fence_after();
-            store_accumulator<BN>(args, u, tm, tn,
-                                  tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN, row_in_tile);
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
+            if (clustered) {
+                if (!cluster_reduce_store<BN>(args, tm, tn, taddr, row_in_tile, ring,
+                                              reinterpret_cast<const float*>(ring_ptr), ready_bar, recv_bar,
+                                              limit, abort_flag))
+                    break;
+            } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
+                // this CTA's last unit: the ring is idle, stage and store by TMA
+                if (u.slot < 0)
+                    store_accumulator_tma<BN>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
+                                              args.M, taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+                else
+                    store_accumulator_tma<BN>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
+                                              taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+            } else {
+                store_accumulator<BN>(args, u, tm, tn, taddr, row_in_tile);
+            }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
@@ -362,6 +388,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
 
     ptx::tc_fence_before();
     __syncthreads();
+    // no CTA of the cluster leaves while a peer may still reach its shared memory
+    if (clustered) ptx::cluster_sync();
     pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();

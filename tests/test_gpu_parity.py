@@ -397,6 +397,93 @@ def test_run_host_buffers(shape, pad):
 
 
 # ---------------------------------------------------------------------------
+# The TMA-store epilogue of a CTA's last tile: 32-column boxes staged in two
+# alternating buffers; tiles wider than the rest of C store only some boxes
+# (one to seven of eight), the last one clipped.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("N", [8, 33, 64, 96, 100, 200])
+def test_tma_store_epilogue_partial_boxes(N, bn):
+    M, K = 200, 64
+    A = inputs.uniform_pm1(1731, M, K)
+    B = inputs.uniform_pm1(1732, K, N)
+    C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_TCGEN05, tile_n=bn, split_k=1, ldc=N + 4 - N % 4)
+    assert canaries, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert ok, f"{desc}: {err}"
+
+
+# ---------------------------------------------------------------------------
+# K-slices summed inside a thread-block cluster (distributed shared memory)
+# instead of by the reduction kernel: the same slice order, so the same bits.
+# ---------------------------------------------------------------------------
+
+CLUSTER_CASES = [
+    # M, N, K, tile_n, split_k, operand_split
+    (1024, 1024, 1024, 128, 2, 2),   # in-kernel split, the 1024^3 plan
+    (512, 512, 512, 128, 8, 2),      # 8 slices, clusters of 8
+    (1000, 520, 264, 128, 2, 1),     # ragged; slices of 5 and 4 k-blocks; pre-pass
+    (500, 520, 256, 128, 4, 4),      # raw A, 4 slices
+    (600, 700, 1024, 256, 2, 3),     # hybrid, 128x256 tiles
+    (384, 300, 640, 64, 4, 1),       # 128x64 tiles
+    (256, 256, 160, 128, 2, 1),      # slices of 3 and 2 k-blocks
+]
+
+
+@pytest.mark.parametrize("case", CLUSTER_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}_bn{c[3]}_s{c[4]}_m{c[5]}"
+                                                     for c in CLUSTER_CASES])
+def test_cluster_sum_matches_reduction_kernel(case):
+    M, N, K, bn, split, mode = case
+    A = inputs.uniform_pm1(1721, M, K)
+    B = inputs.uniform_pm1(1722, K, N)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=bn, split_k=split, operand_split=mode)
+    Cc, dc, okc, _ = run_gemm(A, B, split_reduce=2, **opts)
+    Ck, dk, okk, _ = run_gemm(A, B, split_reduce=1, **opts)
+    assert "cluster-sum" in dc and "cluster-sum" not in dk
+    assert okc and okk
+    assert np.array_equal(Cc, Ck), dc
+    err, ok = check_against_oracle(Cc, A, B)
+    assert ok, f"{dc}: {err}"
+
+
+def test_cluster_sum_misaligned_fallback_and_padding():
+    # A misaligned base pointer sends an in-kernel plan to the pre-pass kernel,
+    # which sums its slices in a cluster too; padded C stays untouched.
+    M, N, K = 512, 512, 512
+    A = inputs.uniform_pm1(1723, M, K)
+    B = inputs.uniform_pm1(1724, K, N)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=8, operand_split=2, split_reduce=2)
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, ldc=N + 5, a_off=1, c_off=3, **opts)
+    assert canaries and "cluster-sum" in desc
+    err, ok = check_against_oracle(C, A, B)
+    assert ok, f"{desc}: {err}"
+
+
+def test_cluster_sum_launch_count():
+    with g.Plan(1024, 1024, 1024, split_reduce=2) as p:
+        assert "cluster-sum" in p.describe()
+        assert p.kernel_launches == 1
+    with g.Plan(1024, 1024, 1024, split_reduce=1) as p:
+        assert "cluster-sum" not in p.describe()
+        assert p.kernel_launches == 2
+
+
+@pytest.mark.parametrize("opts", [
+    dict(tile_n=128, split_k=3),                 # 3 slices: not a cluster size used
+    dict(tile_n=128, stages=1, split_k=2),       # a single-stage ring cannot hold the sums
+    dict(tile_n=128, split_k=0),                 # tail-wave split: whole tiles too
+], ids=["three_slices", "one_stage", "tail_split"])
+def test_cluster_sum_refusals(opts):
+    with pytest.raises(g.GemmError) as e:
+        g.Plan(2048, 1024, 1024, variant=g.VARIANT_TCGEN05, split_reduce=2, **opts)
+    assert e.value.status == g.ERR_UNSUPPORTED
+    # more slices than fit at once
+    with pytest.raises(g.GemmError):
+        g.Plan(2048, 2048, 1024, variant=g.VARIANT_TCGEN05, tile_n=128, split_k=2, split_reduce=2)
+
+
+# ---------------------------------------------------------------------------
 # The pipelined host-buffer run: row panels of whole 128-row tiles, B copied
 # and split once, each panel's A copy / GEMM / C copy overlapped on three
 # streams.  Every operand mode, ragged panels, padded leading dimensions,

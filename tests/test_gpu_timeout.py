@@ -67,3 +67,30 @@ def test_short_timeout_does_not_fire_on_a_normal_run():
         assert p.check() == g.OK
     Cref, S = oracle.gemm_f64(A, B)
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["pre_pass", "in_kernel"])
+def test_withheld_stage_in_a_cluster(mode):
+    # Two K-slices of 3 and 2 k-blocks per tile, summed in a cluster of two.
+    # Withholding fill 3 stops only the 3-block slice: its partner finishes,
+    # offers its ring, waits for the other CTA's offer, and must give up after
+    # the limit without sending anything.  Both CTAs then meet at the cluster's
+    # closing barrier; the host sees TIMEOUT and the next run is right.
+    import torch
+    M, N, K = 256, 256, 160
+    A = inputs.uniform_pm1(1505, M, K)
+    B = inputs.uniform_pm1(1506, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=2, operand_split=mode, split_reduce=2)
+    with g.Plan(M, N, K, wait_timeout_cycles=1 << 22, debug_withhold_stage=3, **opts) as p:
+        assert "cluster-sum" in p.describe()
+        p.run(dA, dB, dC)
+        assert p.check() == g.ERR_TIMEOUT
+    torch.cuda.synchronize()
+    dC.fill_(float("nan"))
+    with g.Plan(M, N, K, **opts) as p:
+        p.run(dA, dB, dC)
+        assert p.check() == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
