@@ -117,10 +117,10 @@ typedef struct {
     int32_t split_reduce;   /* TC only: how the K-slices of split tiles are summed.  0 = the
                                dispatcher's choice (the reduction kernel: measured faster);
                                1 = a reduction kernel over partial tiles in scratch; 2 = the
-                               slices of a tile run as one cluster of 2, 4 or 8 CTAs and sum
-                               in distributed shared memory (needs every tile split, all
-                               slices resident at once, a ring of depth >= 2; else
-                               UNSUPPORTED) */
+                               slices of a tile run as one cluster of 2 or 4 CTAs and sum in
+                               distributed shared memory (needs every tile split in 2 or 4,
+                               all slices resident at once, tiles at most 128 wide and a ring
+                               of 128 KB or more; else UNSUPPORTED) */
     int32_t reserved[1];
 } gemm_f32_opts;
 

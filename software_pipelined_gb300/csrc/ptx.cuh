@@ -163,6 +163,14 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t a, uint32_t x, uint32_t y
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};\n"
                  :: "r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to a
+// CTA of the cluster (dst and its mbarrier as shared::cluster addresses); the
+// destination mbarrier's transaction count drops by the bytes as they land.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t remote_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+                 :: "r"(dst), "r"(src), "r"(bytes), "r"(remote_bar) : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster (shared::cluster
 // address), releasing this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {

@@ -228,112 +228,180 @@ __device__ __forceinline__ void store_accumulator(const TcArgs& args, const Unit
     }
 }
 
+// Write 32 FP32 of one row (this lane) into a 32 x 32 box of the 128-byte
+// swizzled layout (16-byte chunk q of row r at chunk q ^ (r % 8)): the 8 lanes
+// of each store phase hit 8 different chunks, so no bank conflicts.
+__device__ __forceinline__ void stage_row(uint8_t* box, int lane, const uint32_t* r)
+{
+    uint8_t* row = box + lane * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+}
+
 // Epilogue through TMA stores, for a CTA's last unit (its operand ring is then
 // idle and serves as staging).  The calling warp owns TMEM lanes = tile rows
-// y0 .. y0+31 of the destination (C, or the partial-tile buffer) and the 8 KB
-// of staging at `stage` (two 4 KB boxes of 32 rows x 32 FP32 in the 128-byte
-// swizzled layout: 16-byte chunk q of row r at chunk q ^ (r % 8), so the 8
-// lanes of each store phase hit 8 different chunks).  Per 32 columns: two
-// TMEM loads, 8 conflict-free 16-byte shared stores per lane, one TMA store
-// of the box (clipped at the tensor's edge; boxes wholly past it are skipped).
-template <int BN>
+// y0 .. y0+31 of the destination (C, or the partial-tile buffer) and NBUF
+// staging boxes of 32 rows x 32 FP32 (4 KB each) from `stage`.  Boxes go in
+// pairs: four TMEM loads (64 columns) and one wait, two staged boxes, two TMA
+// stores (clipped at the tensor's edge; boxes wholly past it are neither
+// staged nor stored, so every staged box is one committed group).  A box
+// buffer is reused only once the store that read it is done.
+template <int BN, int NBUF>
 __device__ __forceinline__ void store_accumulator_tma(const CUtensorMap* map, int64_t x0, int64_t y0,
                                                       int64_t xlim, int64_t ylim, uint32_t taddr, int lane,
                                                       uint32_t stage, uint8_t* stage_ptr)
 {
-    // Only boxes that are stored are staged, so every staged box is one
-    // committed group and "at most one group still reading" below means the
-    // store of the box two back (the same buffer) is done with it.
+    static_assert(NBUF >= 2 && BN % 64 == 0, "box pairs");
     const int cols = y0 < ylim ? (int)(xlim - x0 < BN ? xlim - x0 : BN) : 0;
+    const int nbox = (cols + 31) >> 5;
 #pragma unroll 1
-    for (int c = 0; c < cols; c += 32) {
-        const int b = (c >> 5) & 1;
-        if (c >= 64) {
-            // box b was stored two boxes ago: its store must be done reading
-            if (lane == 0) ptx::bulk_wait_read<1>();
+    for (int j = 0; j < nbox; j += 2) {
+        if (j + 1 >= NBUF) {
+            // boxes up to j + 1 - NBUF (the previous users of these buffers) are read
+            if (lane == 0) ptx::bulk_wait_read<NBUF - 2>();
             __syncwarp();
         }
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r));
-        ptx::tmem_ld_32x32b_x16(taddr + c + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        ptx::tmem_wait_ld();
-        uint8_t* row = stage_ptr + b * 4096 + lane * 128;
+        uint32_t r[64];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) =
-                make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        for (int h = 0; h < 4; ++h)
+            ptx::tmem_ld_32x32b_x16(taddr + j * 32 + h * 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * h));
+        ptx::tmem_wait_ld();
+        stage_row(stage_ptr + (j % NBUF) * 4096, lane, r);
+        if (j + 1 < nbox) stage_row(stage_ptr + ((j + 1) % NBUF) * 4096, lane, r + 32);
         ptx::fence_proxy_async_shared();  // generic-proxy writes -> the TMA engine's reads
         __syncwarp();
         if (lane == 0) {
-            ptx::tma_store_2d(map, stage + b * 4096, (int32_t)(x0 + c), (int32_t)y0);
+            ptx::tma_store_2d(map, stage + (j % NBUF) * 4096, (int32_t)(x0 + j * 32), (int32_t)y0);
             ptx::bulk_commit();
+            if (j + 1 < nbox) {
+                ptx::tma_store_2d(map, stage + ((j + 1) % NBUF) * 4096, (int32_t)(x0 + j * 32 + 32), (int32_t)y0);
+                ptx::bulk_commit();
+            }
         }
     }
     if (lane == 0) ptx::bulk_wait_all();  // complete before the staging is reused or freed
     __syncwarp();
 }
 
-// Epilogue of a K-sliced tile whose S = args.cluster slices are the S CTAs of
-// one cluster (rank z = slice z).  Rows are owned in blocks: rank r sums rows
-// r*128/S .. (r+1)*128/S - 1 of the tile.  Called by the 128 epilogue threads
-// (thread = TMEM lane = tile row) once this CTA's accumulator is complete.
-//   1. This CTA's MMAs are done, so its operand ring is idle: one thread
-//      arrives on every rank's `ready` barrier.
-//   2. Wait until all S rings are idle (`ready` complete: S arrivals).
-//   3. Each thread sends its row (BN FP32, from TMEM) into slice z's row of
-//      the owner's receive buffer, laid over the owner's idle ring
-//      ([S][128/S][BN + 4] FP32; the 4-float pad spreads the rows of a warp
-//      over the banks), then arrives on the owner's `recv` barrier.
-//   4. Wait for the 128 rows this CTA owns (`recv` complete: 128 arrivals),
-//      sum the S slices in slice order (the order of the reduction kernel, so
-//      the result is the same bit for bit) and store them to C.
-// Every wait is bounded; false means a wait gave up (status already set).  No
-// CTA leaves the kernel before the cluster barrier at its end, so no remote
-// access ever targets a CTA that has exited.
+// Shared-memory plan of the cluster K-slice sum, laid over the idle ring:
+// STG holds this CTA's whole accumulator as 32 x 32 swizzled boxes, quadrant
+// (32 rows) by quadrant; RECV holds the peers' slices of the rows this CTA
+// owns, one slot per slice.  Rank r owns quadrants r*4/S .. (r+1)*4/S - 1, a
+// contiguous block of STG, so each slice travels as one bulk copy.
 template <int BN>
-__device__ bool cluster_reduce_store(const TcArgs& args, int tm, int tn, uint32_t taddr, int row,
-                                     uint32_t recv_addr, const float* recv_ptr, uint32_t ready_bar,
-                                     uint32_t recv_bar, int64_t limit, volatile int* abort_flag)
+struct ClusterSum {
+    static constexpr int QUAD_BYTES = 32 * BN * 4;
+    static constexpr int STG_BYTES = 4 * QUAD_BYTES;
+    static constexpr int BYTES = 2 * STG_BYTES;     // STG + RECV (S slots of a block)
+    static __device__ __forceinline__ int block_bytes(int S) { return (4 / S) * QUAD_BYTES; }
+};
+
+// Epilogue of a K-sliced tile whose S = args.cluster (2 or 4) slices are the
+// S CTAs of one cluster (rank z = slice z).  Called by the 128 epilogue
+// threads (e = TMEM lane = tile row) once this CTA's accumulator is complete.
+//   1. The ring is idle: one thread arrives on every rank's `ready` barrier.
+//   2. Each warp stages its quadrant into STG; `stg` (4 arrivals) marks it.
+//   3. One thread waits for `stg` and for `ready` (S arrivals: every ring is
+//      free), then pushes the block of each owner p != z from STG into slot z
+//      of p's RECV with one bulk copy that completes on p's `recv` barrier
+//      (armed at start for the S-1 incoming blocks).
+//   4. Everyone waits for `recv` (the S-1 blocks landed) and `stg`, sums the
+//      S slices of the owned block in slice order (the reduction kernel's
+//      order: the same bits) into STG, and marks it on `sumd` (4 arrivals).
+//   5. The owned boxes go to C by TMA stores (or by direct stores when C
+//      cannot take them).
+// Every wait is bounded; false means one gave up (status set).  No CTA
+// leaves before the cluster barrier at the kernel's end, so no remote access
+// targets an exited CTA.
+template <int BN>
+__device__ bool cluster_reduce_store(const TcArgs& args, const CUtensorMap* tm_c, int tm, int tn,
+                                     uint32_t taddr, int quad, int lane, uint32_t ring, uint8_t* ring_ptr,
+                                     uint32_t ready_bar, uint32_t recv_bar, uint32_t stg_bar, uint32_t sum_bar,
+                                     int64_t limit, volatile int* abort_flag)
 {
-    constexpr int LD = BN + 4;
+    using CS = ClusterSum<BN>;
+    constexpr int NB = BN / 32;  // boxes per quadrant row
     const int S = args.cluster;
-    const int rows_per = kBM / S;
+    const int e = quad * 32 + lane;
     const uint32_t z = ptx::cluster_ctarank();
-    if (row == 0)
+    const int block = CS::block_bytes(S);
+    const uint32_t stg = ring, recv = ring + CS::STG_BYTES;
+    uint8_t* stg_ptr = ring_ptr;
+    const uint8_t* recv_ptr = ring_ptr + CS::STG_BYTES;
+    // 1.
+    if (e == 0)
         for (int r = 0; r < S; ++r) ptx::mbar_arrive_cluster(ptx::mapa(ready_bar, (uint32_t)r));
-    // warp-uniform outcome: the TMEM loads below are warp-collective
-    if (!__all_sync(0xffffffffu, wait_phase_cluster(ready_bar, 0, limit, abort_flag, args.status))) return false;
-    const uint32_t owner = (uint32_t)(row / rows_per);
-    const uint32_t dst = ptx::mapa(recv_addr, owner) +
-                         (uint32_t)(((int)z * rows_per + row % rows_per) * LD) * 4u;
+    // 2.
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-        uint32_t r[16];
-        ptx::tmem_ld_32x32b_x16(taddr + c, r);
+    for (int bx = 0; bx < NB; ++bx) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x16(taddr + bx * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+        ptx::tmem_ld_32x32b_x16(taddr + bx * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
         ptx::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-            ptx::st_cluster_v4(dst + (uint32_t)(c + j) * 4u, r[j], r[j + 1], r[j + 2], r[j + 3]);
+        stage_row(stg_ptr + (quad * NB + bx) * 4096, lane, r);
     }
-    ptx::mbar_arrive_cluster(ptx::mapa(recv_bar, owner));
-    if (!__all_sync(0xffffffffu, wait_phase_cluster(recv_bar, 0, limit, abort_flag, args.status))) return false;
-    const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
-    const int row0 = tm * kBM + (int)z * rows_per;
-    for (int idx = row; idx < rows_per * (BN / 4); idx += kBM) {
-        const int r = idx / (BN / 4), c4 = idx % (BN / 4);
-        float4 acc = *reinterpret_cast<const float4*>(recv_ptr + r * LD + 4 * c4);
+    ptx::fence_proxy_async_shared();  // visible to the bulk copies that read STG
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(stg_bar);
+    // 3.
+    if (e == 0) {
+        bool ok = wait_phase(stg_bar, 0, limit, abort_flag, args.status) &&
+                  wait_phase_cluster(ready_bar, 0, limit, abort_flag, args.status);
+        if (ok)
+            for (int p = 0; p < S; ++p)
+                if (p != (int)z)
+                    ptx::bulk_copy_to_cluster(ptx::mapa(recv + z * block, (uint32_t)p), stg + p * block,
+                                              (uint32_t)block, ptx::mapa(recv_bar, (uint32_t)p));
+    }
+    // 4.
+    const bool ok = wait_phase_cluster(recv_bar, 0, limit, abort_flag, args.status) &&
+                    wait_phase(stg_bar, 0, limit, abort_flag, args.status);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    uint8_t* own = stg_ptr + z * block;
+    for (int o = e * 16; o < block; o += 128 * 16) {
+        float4 acc = z == 0 ? *reinterpret_cast<const float4*>(own + o)
+                            : *reinterpret_cast<const float4*>(recv_ptr + o);
         for (int s = 1; s < S; ++s) {
-            const float4 t = *reinterpret_cast<const float4*>(recv_ptr + (s * rows_per + r) * LD + 4 * c4);
+            const float4 t = s == (int)z ? *reinterpret_cast<const float4*>(own + o)
+                                         : *reinterpret_cast<const float4*>(recv_ptr + s * block + o);
             acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
         }
-        const int64_t grow = (int64_t)row0 + r, gcol = (int64_t)tn * BN + 4 * c4;
-        if (grow >= args.M) continue;
-        float* dst_c = args.C + grow * args.ldc + gcol;
-        if (vec && gcol + 3 < args.N) {
-            *reinterpret_cast<float4*>(dst_c) = acc;
-        } else {
-            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-            for (int q = 0; q < 4 && gcol + q < args.N; ++q) dst_c[q] = v[q];
+        *reinterpret_cast<float4*>(own + o) = acc;
+    }
+    ptx::fence_proxy_async_shared();  // visible to the TMA stores
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sum_bar);
+    if (!__all_sync(0xffffffffu, wait_phase(sum_bar, 0, limit, abort_flag, args.status))) return false;
+    // 5.
+    const int quads = 4 / S, q0 = (int)z * quads;
+    if (args.c_tma) {
+        if (e < quads * NB) {
+            const int qd = q0 + e / NB, bx = e % NB;
+            const int64_t y = (int64_t)tm * kBM + qd * 32, x = (int64_t)tn * BN + bx * 32;
+            if (y < args.M && x < args.N) {
+                ptx::tma_store_2d(tm_c, stg + (qd * NB + bx) * 4096, (int32_t)x, (int32_t)y);
+                ptx::bulk_commit();
+                ptx::bulk_wait_all();
+            }
+        }
+    } else {
+        const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
+        for (int idx = e; idx < quads * 32 * (BN / 4); idx += 128) {
+            const int rb = idx / (BN / 4), c4 = idx % (BN / 4);
+            const int qd = q0 + rb / 32, rr = rb % 32, bx = c4 / 8, q = c4 % 8;
+            const float4 v = *reinterpret_cast<const float4*>(stg_ptr + (qd * NB + bx) * 4096 + rr * 128 +
+                                                              ((q ^ (rr & 7)) << 4));
+            const int64_t grow = (int64_t)tm * kBM + qd * 32 + rr, gcol = (int64_t)tn * BN + 4 * c4;
+            if (grow >= args.M) continue;
+            float* dst = args.C + grow * args.ldc + gcol;
+            if (vec && gcol + 3 < args.N) {
+                *reinterpret_cast<float4*>(dst) = v;
+            } else {
+                const float w[4] = {v.x, v.y, v.z, v.w};
+                for (int k = 0; k < 4 && gcol + k < args.N; ++k) dst[k] = w[k];
+            }
         }
     }
     return true;

@@ -52,9 +52,9 @@ struct FusedLayout {
     static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RAWB_BYTES = B_BYTES;              // BN/32 boxes of 32 k x 32 n
     static constexpr int RING_BYTES = SLOTS * SLOT_BYTES + RAWB * RAWB_BYTES;
-    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 7;  // + tmem full/empty x2, drain, ready, recv
-    // cluster K-slice reduction: the receive buffer laid over the idle ring
-    static constexpr bool CLUSTER_OK = kBM * (BN + 4) * 4 <= RING_BYTES;
+    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 9;  // + tmem full/empty x2, drain, ready, recv, stg, sumd
+    // cluster K-slice sum: its staging and receive buffers laid over the idle ring
+    static constexpr bool CLUSTER_OK = ClusterSum<BN>::BYTES <= RING_BYTES;
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     static constexpr int SMEM_USED = 1024 + RING_BYTES + BAR_BYTES;
     static constexpr int SMEM_BYTES = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
@@ -106,6 +106,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     const uint32_t drain_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 4);
     const uint32_t ready_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 5);
     const uint32_t recv_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 6);
+    const uint32_t stg_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 7);
+    const uint32_t sum_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 8);
     const bool clustered = L::CLUSTER_OK && args.cluster > 1;
 
     if (threadIdx.x == 0) {
@@ -124,7 +126,13 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(ready_bar, clustered ? args.cluster : 1);
-        ptx::mbar_init(recv_bar, kBM);
+        ptx::mbar_init(recv_bar, 1);
+        ptx::mbar_init(stg_bar, 4);
+        ptx::mbar_init(sum_bar, 4);
+        // the S-1 incoming slices of this CTA's rows complete the one phase
+        if (clustered)
+            ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((args.cluster - 1) *
+                                                            ClusterSum<BN>::block_bytes(args.cluster)));
         *abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -147,7 +155,10 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     if (clustered) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();  // the previous kernel on the stream may still be writing A or B
+    // Programmatic launch: only the producer reads global memory first, so only
+    // it waits for the previous kernel on the stream (below); the next kernel
+    // may start its own prologue now.
+    pdl_trigger();
 
     const int num_work = args.dp_tiles + args.split_tiles * args.splits;
     const int64_t limit = args.timeout;
@@ -155,6 +166,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
+            pdl_wait();  // the previous kernel's writes (A, B, C) are done
             uint32_t fills = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
@@ -274,18 +286,20 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
             if (clustered) {
-                if (!cluster_reduce_store<BN>(args, tm, tn, taddr, row_in_tile, ring,
-                                              reinterpret_cast<const float*>(ring_ptr), ready_bar, recv_bar,
-                                              limit, abort_flag))
+                if (!cluster_reduce_store<BN>(args, &tm_c, tm, tn, taddr, quad, lane, ring, ring_ptr, ready_bar,
+                                              recv_bar, stg_bar, sum_bar, limit, abort_flag))
                     break;
             } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
                 // this CTA's last unit: the ring is idle, stage and store by TMA
+                // staging: a box per 32 columns where the ring holds them, per warp
+                constexpr int NBUF = L::RING_BYTES / (4 * 4096) < BN / 32 ? L::RING_BYTES / (4 * 4096) : BN / 32;
+                const uint32_t stg = (uint32_t)(quad * NBUF * 4096);
                 if (u.slot < 0)
-                    store_accumulator_tma<BN>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
-                                              args.M, taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+                    store_accumulator_tma<BN, NBUF>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
+                                                    args.M, taddr, lane, ring + stg, ring_ptr + stg);
                 else
-                    store_accumulator_tma<BN>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
-                                              taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+                    store_accumulator_tma<BN, NBUF>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
+                                                    taddr, lane, ring + stg, ring_ptr + stg);
             } else {
                 store_accumulator<BN>(args, u, tm, tn, taddr, row_in_tile);
             }
@@ -361,7 +375,6 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     __syncthreads();
     // no CTA of the cluster leaves while a peer may still reach its shared memory
     if (clustered) ptx::cluster_sync();
-    pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);

@@ -164,12 +164,13 @@ const TcEntry kTc[] = {
     {{128, 256, 32, 2, true, kSplitPrepass}, launch_main<256, 2, true>, launch_reduce<256>, kClusterOk<256, 2>},
     {{128, 128, 32, 3, true, kSplitPrepass}, launch_main<128, 3, true>, launch_reduce<128>, kClusterOk<128, 3>},
     // operands split inside the kernel (stages = MMA-facing slots; the fused
-    // kernel's rings of 3 x 64 KB and 2 x 96 KB hold the receive buffer)
+    // kernel's 3 x 64 KB ring holds the cluster sum's 128 KB, its 2 x 96 KB
+    // ring of 128 x 256 tiles not the 256 KB those would need)
     {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>, true},
-    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>, true},
+    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>, false},
     // A split inside the kernel, B by the pre-pass
     {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>, true},
-    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>, true},
+    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>, false},
     // hi of A read from the caller's A, lo of A and both pieces of B by the pre-pass
     {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>},
     {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>},
@@ -237,13 +238,12 @@ void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_req
         }
     }
     if (t.split_tiles == 0) t.kb_per_split = num_kb;
-    // Every tile in 2, 4 or 8 slices, one CTA per slice, all at once: the
-    // slices of a tile can run as one thread-block cluster that sums them in
+    // Every tile in 2 or 4 slices, one CTA per slice, all at once: the slices
+    // of a tile can run as one thread-block cluster that sums them in
     // distributed shared memory (no partial tiles, no reduction launch).
     t.cluster = 0;
     const bool cluster_fits = kTc[t.config_id].cluster_ok && t.dp_tiles == 0 && t.split_tiles > 0 &&
-                              (t.splits == 2 || t.splits == 4 || t.splits == 8) &&
-                              t.split_tiles * t.splits <= sms;
+                              (t.splits == 2 || t.splits == 4) && t.split_tiles * t.splits <= sms;
     if (cluster_fits && t.cluster_mode == 2) t.cluster = t.splits;
     t.partial_bytes = t.split_tiles && !t.cluster ? size_t(t.split_tiles) * t.splits * kBM * c.bn * sizeof(float)
                                                   : 0;

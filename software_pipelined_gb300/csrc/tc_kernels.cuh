@@ -155,8 +155,8 @@ struct TcLayout {
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     // cluster K-slice reduction: the receive buffer laid over the idle ring
-    static constexpr bool CLUSTER_OK = kBM * (BN + 4) * 4 <= RING_BYTES;
-    static constexpr int NBARS = 3 * STAGES + 7;    // full, empty, tmem x4, drain, full_b, ready, recv
+    static constexpr bool CLUSTER_OK = ClusterSum<BN>::BYTES <= RING_BYTES;
+    static constexpr int NBARS = 3 * STAGES + 9;    // full, empty, tmem x4, drain, full_b, ready, recv, stg, sumd
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     // At least 116 KB, so that two CTAs never share an SM (each holds up to
     // all 512 TMEM columns for its whole lifetime).
@@ -202,6 +202,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     auto fullb_bar = [&](int s) { return ptx::smem_u32(bars + (SEP ? 2 * STAGES + 5 + s : s)); };
     const uint32_t ready_bar = ptx::smem_u32(bars + 3 * STAGES + 5);
     const uint32_t recv_bar = ptx::smem_u32(bars + 3 * STAGES + 6);
+    const uint32_t stg_bar = ptx::smem_u32(bars + 3 * STAGES + 7);
+    const uint32_t sum_bar = ptx::smem_u32(bars + 3 * STAGES + 8);
     const bool clustered = L::CLUSTER_OK && args.cluster > 1;
 
     if (threadIdx.x == 0) {
@@ -217,7 +219,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
         if (SEP)
             for (int s = 0; s < STAGES; ++s) ptx::mbar_init(fullb_bar(s), 1);
         ptx::mbar_init(ready_bar, clustered ? args.cluster : 1);
-        ptx::mbar_init(recv_bar, kBM);
+        ptx::mbar_init(recv_bar, 1);
+        ptx::mbar_init(stg_bar, 4);
+        ptx::mbar_init(sum_bar, 4);
+        // the S-1 incoming slices of this CTA's rows complete the one phase
+        if (clustered)
+            ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((args.cluster - 1) *
+                                                            ClusterSum<BN>::block_bytes(args.cluster)));
         *abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -237,9 +245,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     if (clustered) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // Everything above overlaps the split pre-pass; its outputs are read only
-    // after this point.
-    pdl_wait();
+    // Programmatic launch: this grid may start while the previous kernel on the
+    // stream (the split pre-pass, or the last GEMM) still runs.  Only the
+    // producer reads global memory first, so only it waits for that kernel
+    // (below); every other global access comes after its loads through the
+    // mbarrier chain.  The next kernel may start its own prologue now.
+    pdl_trigger();
 
     const int num_work = args.dp_tiles + args.split_tiles * args.splits;
     const int64_t limit = args.timeout;
@@ -247,6 +258,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
+            pdl_wait();  // the previous kernel's writes (split operands, C) are done
             int stage = 0;
             uint32_t phase = 0;
             uint32_t fills = 0;
@@ -365,18 +377,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
             if (clustered) {
-                if (!cluster_reduce_store<BN>(args, tm, tn, taddr, row_in_tile, ring,
-                                              reinterpret_cast<const float*>(ring_ptr), ready_bar, recv_bar,
-                                              limit, abort_flag))
+                if (!cluster_reduce_store<BN>(args, &tm_c, tm, tn, taddr, quad, lane, ring, ring_ptr, ready_bar,
+                                              recv_bar, stg_bar, sum_bar, limit, abort_flag))
                     break;
             } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
                 // this CTA's last unit: the ring is idle, stage and store by TMA
+                // staging: a box per 32 columns where the ring holds them, per warp
+                constexpr int NBUF = L::RING_BYTES / (4 * 4096) < BN / 32 ? L::RING_BYTES / (4 * 4096) : BN / 32;
+                const uint32_t stg = (uint32_t)(quad * NBUF * 4096);
                 if (u.slot < 0)
-                    store_accumulator_tma<BN>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
-                                              args.M, taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+                    store_accumulator_tma<BN, NBUF>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
+                                                    args.M, taddr, lane, ring + stg, ring_ptr + stg);
                 else
-                    store_accumulator_tma<BN>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
-                                              taddr, lane, ring + quad * 8192, ring_ptr + quad * 8192);
+                    store_accumulator_tma<BN, NBUF>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
+                                                    taddr, lane, ring + stg, ring_ptr + stg);
             } else {
                 store_accumulator<BN>(args, u, tm, tn, taddr, row_in_tile);
             }
@@ -390,7 +404,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     __syncthreads();
     // no CTA of the cluster leaves while a peer may still reach its shared memory
     if (clustered) ptx::cluster_sync();
-    pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
@@ -404,6 +417,7 @@ __global__ void __launch_bounds__(256)
 tile_reduce_kernel(const float4* __restrict__ partial, int dp_tiles, int split_tiles, int splits,
                    int tiles_m, int tiles_n, int group, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
 {
+    pdl_trigger();  // the next kernel may start its prologue; it waits for this one itself
     pdl_wait();
     constexpr int Q = BN / 4;                 // float4 per partial row
     constexpr int PER_TILE = kBM * Q;

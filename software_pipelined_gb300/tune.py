@@ -123,7 +123,7 @@ def main():
             with g.Plan(M, N, K) as p:
                 auto_desc = p.describe()
                 auto_us = round(time_plan(p, dA, dB, dC, stream) * 1e3, 3)
-            results.append(dict(shape=name, M=M, N=N, K=K, best=rows[0], top=rows[:8],
+            results.append(dict(shape=name, M=M, N=N, K=K, best=rows[0], top=rows[:40],
                                 auto=dict(plan=auto_desc, us=auto_us), n_candidates=len(rows)))
             print(f"{name:18s} best {rows[0]['us']:10.3f} us  {rows[0]['plan']}   (auto {auto_us} us)",
                   flush=True)

@@ -422,10 +422,10 @@ def test_tma_store_epilogue_partial_boxes(N, bn):
 CLUSTER_CASES = [
     # M, N, K, tile_n, split_k, operand_split
     (1024, 1024, 1024, 128, 2, 2),   # in-kernel split, the 1024^3 plan
-    (512, 512, 512, 128, 8, 2),      # 8 slices, clusters of 8
+    (512, 512, 512, 128, 4, 2),      # 4 slices, clusters of 4
     (1000, 520, 264, 128, 2, 1),     # ragged; slices of 5 and 4 k-blocks; pre-pass
     (500, 520, 256, 128, 4, 4),      # raw A, 4 slices
-    (600, 700, 1024, 256, 2, 3),     # hybrid, 128x256 tiles
+    (600, 700, 1024, 128, 2, 3),     # hybrid
     (384, 300, 640, 64, 4, 1),       # 128x64 tiles
     (256, 256, 160, 128, 2, 1),      # slices of 3 and 2 k-blocks
 ]
@@ -453,7 +453,7 @@ def test_cluster_sum_misaligned_fallback_and_padding():
     M, N, K = 512, 512, 512
     A = inputs.uniform_pm1(1723, M, K)
     B = inputs.uniform_pm1(1724, K, N)
-    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=8, operand_split=2, split_reduce=2)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=4, operand_split=2, split_reduce=2)
     C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, ldc=N + 5, a_off=1, c_off=3, **opts)
     assert canaries and "cluster-sum" in desc
     err, ok = check_against_oracle(C, A, B)
@@ -469,18 +469,18 @@ def test_cluster_sum_launch_count():
         assert p.kernel_launches == 2
 
 
-@pytest.mark.parametrize("opts", [
-    dict(tile_n=128, split_k=3),                 # 3 slices: not a cluster size used
-    dict(tile_n=128, stages=1, split_k=2),       # a single-stage ring cannot hold the sums
-    dict(tile_n=128, split_k=0),                 # tail-wave split: whole tiles too
-], ids=["three_slices", "one_stage", "tail_split"])
-def test_cluster_sum_refusals(opts):
+@pytest.mark.parametrize("shape,opts", [
+    ((512, 512, 512), dict(tile_n=128, split_k=3)),           # 3 slices: rows do not split in 3
+    ((512, 512, 512), dict(tile_n=128, split_k=8)),           # 8 slices: a quadrant is not a block
+    ((512, 512, 512), dict(tile_n=256, split_k=2)),           # 128 x 256 tiles: ring too small
+    ((512, 512, 512), dict(tile_n=128, stages=1, split_k=2, operand_split=1)),  # 1-stage ring too small
+    ((2048, 1024, 1024), dict(tile_n=128, split_k=0)),        # no split at all
+    ((2048, 2048, 1024), dict(tile_n=128, split_k=2)),        # more slices than fit at once
+], ids=["three_slices", "eight_slices", "wide_tiles", "one_stage", "no_split", "too_many"])
+def test_cluster_sum_refusals(shape, opts):
     with pytest.raises(g.GemmError) as e:
-        g.Plan(2048, 1024, 1024, variant=g.VARIANT_TCGEN05, split_reduce=2, **opts)
+        g.Plan(*shape, variant=g.VARIANT_TCGEN05, split_reduce=2, **opts)
     assert e.value.status == g.ERR_UNSUPPORTED
-    # more slices than fit at once
-    with pytest.raises(g.GemmError):
-        g.Plan(2048, 2048, 1024, variant=g.VARIANT_TCGEN05, tile_n=128, split_k=2, split_reduce=2)
 
 
 # ---------------------------------------------------------------------------
