@@ -461,10 +461,11 @@ def test_cluster_sum_misaligned_fallback_and_padding():
 
 
 def test_cluster_sum_launch_count():
-    with g.Plan(1024, 1024, 1024, split_reduce=2) as p:
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=2, operand_split=2)
+    with g.Plan(1024, 1024, 1024, split_reduce=2, **opts) as p:
         assert "cluster-sum" in p.describe()
         assert p.kernel_launches == 1
-    with g.Plan(1024, 1024, 1024, split_reduce=1) as p:
+    with g.Plan(1024, 1024, 1024, split_reduce=1, **opts) as p:
         assert "cluster-sum" not in p.describe()
         assert p.kernel_launches == 2
 
