@@ -115,8 +115,13 @@ typedef struct {
                                copies overlap); 0 = the dispatcher's choice, 1 = none,
                                n = n panels of whole 128-row tiles (at most 64) */
     int32_t split_reduce;   /* TC only: how the K-slices of split tiles are summed.  0 = the
-                               dispatcher's choice (the reduction kernel: measured faster);
-                               1 = a reduction kernel over partial tiles in scratch; 2 = the
+                               dispatcher's choice (1: measured fastest); 1 = a
+                               reduction kernel over partial tiles in scratch; 3 = no extra
+                               launch: every slice stores its partial tile, and the last slice
+                               of each tile to arrive (an atomic count per 32-row quadrant) sums
+                               them in slice order and writes C (needs at most 8 slices, at most
+                               one wave of split units and a ring of 144 KB or more; else
+                               UNSUPPORTED); 2 = the
                                slices of a tile run as one cluster of 2 or 4 CTAs and sum in
                                distributed shared memory (needs every tile split in 2 or 4,
                                all slices resident at once, tiles at most 128 wide and a ring

@@ -71,6 +71,8 @@ struct gemm_f32_plan_s {
     std::vector<TcPlanState> panels;
     std::vector<int64_t> panel_r0;
     float* panel_partial = nullptr;
+    int* panel_sem = nullptr;
+    size_t panel_sem_bytes = 0;
     int panel_count = 0;
     std::vector<cudaEvent_t> pev;
     char desc[256] = {0};
@@ -119,7 +121,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
-    if (o.split_reduce < 0 || o.split_reduce > 2) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.split_reduce < 0 || o.split_reduce > 3) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -221,7 +223,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         return st;
     }
 
-    size_t status_off = 0, part_off = 0, ahi_off = 0, alo_off = 0, bhi_off = 0, blo_off = 0;
+    size_t status_off = 0, part_off = 0, ahi_off = 0, alo_off = 0, bhi_off = 0, blo_off = 0, sem_off = 0;
     size_t bytes = align256(sizeof(int));
     status_off = 0;
 
@@ -292,7 +294,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             t.tile_group = o.tile_group ? o.tile_group : c.group;
             t.cluster_mode = o.split_reduce;
             tc_configure(t, M, N, K, c.split_k);
-            if (o.split_reduce == 2 && t.cluster == 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            if ((o.split_reduce == 2 && t.cluster == 0) || (o.split_reduce == 3 && t.fixup == 0)) {
+                delete p;
+                return GEMM_F32_ERR_UNSUPPORTED;
+            }
             ahi_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             alo_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             bhi_off = bytes; bytes += align256(size_t(N) * size_t(t.kp) * sizeof(float));
@@ -300,6 +305,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if (t.partial_bytes) {
                 part_off = bytes;
                 bytes += align256(t.partial_bytes);
+            }
+            if (t.sem_bytes) {
+                sem_off = bytes;
+                bytes += align256(t.sem_bytes);
             }
             snprintf(p->desc, sizeof p->desc,
                      "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d%s kp=%lld",
@@ -309,7 +318,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                      t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
                      tcfg.sep ? " separate-syncs" : "",
                      t.tiles_m * t.tiles_n, t.dp_tiles,
-                     t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", (long long)t.kp);
+                     t.split_tiles, t.splits, t.cluster ? " cluster-sum" : t.fixup ? " last-arriver-sum" : "",
+                     (long long)t.kp);
         }
     }
 
@@ -331,6 +341,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         t.b_hi = reinterpret_cast<float*>(base + bhi_off);
         t.b_lo = reinterpret_cast<float*>(base + blo_off);
         if (t.partial_bytes) t.partial = reinterpret_cast<float*>(base + part_off);
+        if (t.sem_bytes) {
+            t.sem = reinterpret_cast<int*>(base + sem_off);
+            if (e == cudaSuccess) e = cudaMemset(t.sem, 0, t.sem_bytes);
+        }
         if (e == cudaSuccess) e = tc_prepare(t, M, N, K);
     }
     if (e != cudaSuccess) {
@@ -388,6 +402,9 @@ void drop_panels(gemm_f32_plan_s* p)
     p->panel_count = 0;
     if (p->panel_partial) cudaFree(p->panel_partial);
     p->panel_partial = nullptr;
+    if (p->panel_sem) cudaFree(p->panel_sem);
+    p->panel_sem = nullptr;
+    p->panel_sem_bytes = 0;
 }
 
 // Panel states for `count` panels of whole 128-row tiles over the staging
@@ -407,6 +424,7 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
             return e;
         }
         if (ps.partial_bytes > need) need = ps.partial_bytes;
+        if (ps.sem_bytes > p->panel_sem_bytes) p->panel_sem_bytes = ps.sem_bytes;
         p->panels.push_back(ps);
         p->panel_r0.push_back(r0);
     }
@@ -415,8 +433,20 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
         drop_panels(p);
         return e;
     }
-    for (TcPlanState& ps : p->panels)
+    // the panels run one after another and leave their counters at zero, so
+    // they share one zeroed counter buffer
+    if (p->panel_sem_bytes) {
+        e = cudaMalloc(&p->panel_sem, p->panel_sem_bytes);
+        if (e == cudaSuccess) e = cudaMemset(p->panel_sem, 0, p->panel_sem_bytes);
+        if (e != cudaSuccess) {
+            drop_panels(p);
+            return e;
+        }
+    }
+    for (TcPlanState& ps : p->panels) {
         if (e == cudaSuccess) e = tc_set_partial(ps, p->panel_partial);
+        ps.sem = ps.sem_bytes ? p->panel_sem : nullptr;
+    }
     if (e != cudaSuccess) {
         drop_panels(p);
         return e;
@@ -678,6 +708,9 @@ gemm_f32_status gemm_f32_check(gemm_f32_plan_t p, gemm_f32_stream_t stream)
     if (e != cudaSuccess) return from_cuda(e);
     if (h != kStatusOk) {
         e = cudaMemset(p->d_status, 0, sizeof(int));
+        // a run that gave up may have left split-tile arrival counts behind
+        if (e == cudaSuccess && p->kind == kTc && p->tc.sem_bytes) e = cudaMemset(p->tc.sem, 0, p->tc.sem_bytes);
+        if (e == cudaSuccess && p->panel_sem) e = cudaMemset(p->panel_sem, 0, p->panel_sem_bytes);
         if (e != cudaSuccess) return from_cuda(e);
         return GEMM_F32_ERR_TIMEOUT;
     }
@@ -720,7 +753,7 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
         // the pre-pass (unless both operands are split in the kernel), the GEMM,
         // and the reduction of split tiles
         const int split = tc_config(p->tc.config_id).split;
-        return (split == kSplitInKernel ? 1 : 2) + (p->tc.split_tiles > 0 && !p->tc.cluster ? 1 : 0);
+        return (split == kSplitInKernel ? 1 : 2) + (p->tc.split_tiles > 0 && !p->tc.cluster && !p->tc.fixup ? 1 : 0);
     }
     default: return 0;
     }

@@ -112,8 +112,14 @@ struct TcPlanState {
     int withhold_stage = 0;
     int tile_group = 0;        // tile-rows per raster group (0 = default)
     int split_request = 0;     // the split policy tc_configure was given
-    int cluster_mode = 0;      // K-slice sums: 2 = in a cluster where possible, else the reduction kernel
+    // K-slice sums (the plan's split_reduce option): 0 and 1 = the reduction
+    // kernel; 2 = in a thread-block cluster where possible; 3 = the last slice
+    // to arrive sums the tile where possible
+    int cluster_mode = 0;
     int cluster = 0;           // > 1: slices per tile, summed in a thread-block cluster
+    int fixup = 0;             // 1: the last slice to arrive sums the tile
+    int* sem = nullptr;        // fixup arrival counters (zero between runs), sem_bytes long
+    size_t sem_bytes = 0;
     // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.

@@ -141,6 +141,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
+// Order this thread's async-proxy (TMA) global accesses against its generic
+// ones, both ways.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+
 // ---- thread-block clusters (distributed shared memory) ----------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -38,6 +38,8 @@ struct TcArgs {
     int withhold;        // test hook: 1-based fill index the producer skips (0 = none)
     int group;           // tile-rows per raster group of the tile order
     int c_tma;           // 1: the C tensor map is valid (C 16-byte aligned, ldc % 4 == 0)
+    int* sem;            // fixup: one arrival counter per (split tile, 32-row quadrant), or NULL
+    int fixup;           // 1: split units sum their tile's slices themselves (last arriver)
     int cluster;         // > 1: every tile split in `cluster` K-slices, one CTA each, the
                          // slices of a tile one thread-block cluster that sums them
                          // through distributed shared memory (no partial tiles)
@@ -283,6 +285,131 @@ __device__ __forceinline__ void store_accumulator_tma(const CUtensorMap* map, in
     }
     if (lane == 0) ptx::bulk_wait_all();  // complete before the staging is reused or freed
     __syncwarp();
+}
+
+// Last-arriver sum of a split tile's K-slices, for split units that are their
+// CTA's last unit (the ring is idle and gives each epilogue warp kFixWarpBytes
+// of staging).  Per warp, i.e. per 32-row quadrant of the tile:
+//   1. this slice's rows of the partial tile go out by TMA and complete;
+//   2. the warp counts its arrival on the (tile, quadrant) counter (proxy
+//      fence and release before, so the rows are visible to whoever reads);
+//   3. the warp that arrives S-th reads the other S-1 slices' rows box by box
+//      (TMA loads), adds them to its own rows (TMEM) in slice order - the
+//      reduction kernel's order, so the same bits - stores the sums to C and
+//      resets the counter for the next run.
+// No warp ever waits for another CTA; every wait is bounded.  false = a wait
+// gave up (status set).
+constexpr int kFixLoadBoxes = 7;                            // other slices: S <= 8
+constexpr int kFixWarpBytes = (kFixLoadBoxes + 2) * 4096;   // + two output boxes
+constexpr int kFixRingBytes = 4 * kFixWarpBytes;            // 144 KB of ring
+
+template <int BN>
+__device__ bool fixup_store(const TcArgs& args, const CUtensorMap* tm_p, const CUtensorMap* tm_c, const Unit& u,
+                            int tm, int tn, uint32_t taddr, int quad, int lane, uint32_t stage, uint8_t* stage_ptr,
+                            uint32_t ld_bar, int64_t limit, volatile int* abort_flag)
+{
+    constexpr int NB = BN / 32;
+    constexpr int NSTORE = NB < kFixLoadBoxes + 2 ? NB : kFixLoadBoxes + 2;
+    const int S = args.splits;
+    const int j = u.slot / S, mine = u.slot % S;
+    // 1.
+    store_accumulator_tma<BN, NSTORE>(tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX, taddr, lane,
+                                      stage, stage_ptr);
+    // 2.
+    int* counter = args.sem + j * 4 + quad;
+    int old = 0;
+    if (lane == 0) {
+        ptx::fence_proxy_async_global();
+        __threadfence();
+        old = atomicAdd(counter, 1);
+    }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != S - 1) return true;
+    // 3. the last arriver
+    if (lane == 0) {
+        __threadfence();
+        ptx::fence_proxy_async_global();
+        *reinterpret_cast<volatile int*>(counter) = 0;
+    }
+    __syncwarp();
+    const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
+    const int64_t y = (int64_t)tm * kBM + quad * 32;
+    // only the boxes that reach into C: each one is stored (one bulk group)
+    const int64_t ncols = args.N - (int64_t)tn * BN;
+    const int nb = y < args.M ? (int)((ncols < BN ? ncols : BN) + 31) / 32 : 0;
+#pragma unroll 1
+    for (int b = 0; b < nb; ++b) {
+        const int64_t x = (int64_t)tn * BN + b * 32;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(ld_bar, (uint32_t)((S - 1) * 4096));
+            for (int z = 0, i = 0; z < S; ++z)
+                if (z != mine)
+                    ptx::tma_load_2d(stage + (i++) * 4096, tm_p, ld_bar, b * 32, (j * S + z) * kBM + quad * 32);
+        }
+        uint32_t own[32];
+        ptx::tmem_ld_32x32b_x16(taddr + b * 32, *reinterpret_cast<uint32_t(*)[16]>(own));
+        ptx::tmem_ld_32x32b_x16(taddr + b * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(own + 16));
+        ptx::tmem_wait_ld();
+        if (!__all_sync(0xffffffffu, wait_phase(ld_bar, (uint32_t)(b & 1), limit, abort_flag, args.status)))
+            return false;
+        uint32_t sum[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int off = lane * 128 + ((q ^ (lane & 7)) << 4);
+            float4 acc;
+            for (int z = 0, i = 0; z < S; ++z) {
+                float4 v;
+                if (z == mine) {
+                    v = make_float4(__uint_as_float(own[4 * q]), __uint_as_float(own[4 * q + 1]),
+                                    __uint_as_float(own[4 * q + 2]), __uint_as_float(own[4 * q + 3]));
+                } else {
+                    v = *reinterpret_cast<const float4*>(stage_ptr + (i++) * 4096 + off);
+                }
+                if (z == 0) {
+                    acc = v;
+                } else {
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+            }
+            sum[4 * q] = __float_as_uint(acc.x); sum[4 * q + 1] = __float_as_uint(acc.y);
+            sum[4 * q + 2] = __float_as_uint(acc.z); sum[4 * q + 3] = __float_as_uint(acc.w);
+        }
+        ptx::fence_proxy_async_shared();  // these generic reads before the next box's TMA writes
+        if (args.c_tma) {
+            const int ob = kFixLoadBoxes + (b & 1);
+            if (b >= 2) {
+                if (lane == 0) ptx::bulk_wait_read<1>();  // output box ob stored two boxes ago
+                __syncwarp();
+            }
+            stage_row(stage_ptr + ob * 4096, lane, sum);
+            ptx::fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(tm_c, stage + ob * 4096, (int32_t)x, (int32_t)y);
+                ptx::bulk_commit();
+            }
+        } else {
+            __syncwarp();
+            const int64_t grow = y + lane;
+            if (grow < args.M) {
+                float* row = args.C + grow * args.ldc;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const int64_t gcol = x + c;
+                    if (vec && gcol + 3 < args.N) {
+                        *reinterpret_cast<float4*>(row + gcol) =
+                            make_float4(__uint_as_float(sum[c]), __uint_as_float(sum[c + 1]),
+                                        __uint_as_float(sum[c + 2]), __uint_as_float(sum[c + 3]));
+                    } else {
+                        for (int k = 0; k < 4 && gcol + k < args.N; ++k) row[gcol + k] = __uint_as_float(sum[c + k]);
+                    }
+                }
+            }
+        }
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
+    return true;
 }
 
 // Shared-memory plan of the cluster K-slice sum, laid over the idle ring:

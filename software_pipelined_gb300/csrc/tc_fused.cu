@@ -52,7 +52,9 @@ struct FusedLayout {
     static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RAWB_BYTES = B_BYTES;              // BN/32 boxes of 32 k x 32 n
     static constexpr int RING_BYTES = SLOTS * SLOT_BYTES + RAWB * RAWB_BYTES;
-    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 9;  // + tmem full/empty x2, drain, ready, recv, stg, sumd
+    // + tmem full/empty x2, drain, ready, recv, stg, sumd, fixup loads x4
+    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 13;
+    static constexpr bool FIXUP_OK = kFixRingBytes <= RING_BYTES;
     // cluster K-slice sum: its staging and receive buffers laid over the idle ring
     static constexpr bool CLUSTER_OK = ClusterSum<BN>::BYTES <= RING_BYTES;
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
@@ -108,7 +110,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     const uint32_t recv_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 6);
     const uint32_t stg_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 7);
     const uint32_t sum_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 8);
+    auto fix_bar = [&](int q) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 9 + q); };
     const bool clustered = L::CLUSTER_OK && args.cluster > 1;
+    const bool fixup = L::FIXUP_OK && args.fixup && !clustered;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
@@ -129,6 +133,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         ptx::mbar_init(recv_bar, 1);
         ptx::mbar_init(stg_bar, 4);
         ptx::mbar_init(sum_bar, 4);
+        for (int q = 0; q < 4; ++q) ptx::mbar_init(fix_bar(q), 1);
         // the S-1 incoming slices of this CTA's rows complete the one phase
         if (clustered)
             ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((args.cluster - 1) *
@@ -289,6 +294,11 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 if (!cluster_reduce_store<BN>(args, &tm_c, tm, tn, taddr, quad, lane, ring, ring_ptr, ready_bar,
                                               recv_bar, stg_bar, sum_bar, limit, abort_flag))
                     break;
+            } else if (fixup && u.slot >= 0 && w + (int)gridDim.x >= num_work) {
+                // a split unit (always its CTA's last): sum the tile's slices if last to arrive
+                if (!fixup_store<BN>(args, &tm_p, &tm_c, u, tm, tn, taddr, quad, lane, ring + quad * kFixWarpBytes,
+                                     ring_ptr + quad * kFixWarpBytes, fix_bar(quad), limit, abort_flag))
+                    break;
             } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
                 // this CTA's last unit: the ring is idle, stage and store by TMA
                 // staging: a box per 32 columns where the ring holds them, per warp
@@ -392,7 +402,7 @@ cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorM
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
-    if (a.cluster > 1 && !L::CLUSTER_OK) return cudaErrorInvalidValue;
+    if ((a.cluster > 1 && !L::CLUSTER_OK) || (a.fixup && !L::FIXUP_OK)) return cudaErrorInvalidValue;
     return launch_pdl(kern, dim3(grid), dim3(kFusedThreads), L::SMEM_BYTES, s, a.cluster, ta, tb, tbhi, tblo,
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);

@@ -121,7 +121,7 @@ cudaError_t launch_main(const TcPlanState& st, const TcArgs& a, const void* tmap
     const int work = a.dp_tiles + a.split_tiles * a.splits;
     const int grid = work < st.num_sms ? work : st.num_sms;
     static_assert(L::RING_BYTES >= 4 * 8192, "the ring holds the TMA-store staging");
-    if (a.cluster > 1 && !L::CLUSTER_OK) return cudaErrorInvalidValue;
+    if ((a.cluster > 1 && !L::CLUSTER_OK) || (a.fixup && !L::FIXUP_OK)) return cudaErrorInvalidValue;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), L::SMEM_BYTES, s, a.cluster,
                       *reinterpret_cast<const CUtensorMap*>(tmap_a_hi),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_a_lo),
@@ -147,33 +147,36 @@ struct TcEntry {
     MainFn main;      // NULL where the split happens in the kernel (tc_fused_main)
     LaunchFn reduce;
     bool cluster_ok;  // the ring can hold the cluster reduction's receive buffer
+    bool fixup_ok;    // the ring can hold the last-arriver sum's staging
 };
 template <int BN, int STAGES>
 constexpr bool kClusterOk = TcLayout<BN, STAGES>::CLUSTER_OK;
+template <int BN, int STAGES>
+constexpr bool kFixupOk = TcLayout<BN, STAGES>::FIXUP_OK;
 const TcEntry kTc[] = {
     // the ring as deep as shared memory allows, per tile width
-    {{128, 128, 32, 3, false, kSplitPrepass}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>},
-    {{128, 256, 32, 2, false, kSplitPrepass}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>},
-    {{128, 64, 32, 4, false, kSplitPrepass}, launch_main<64, 4>, launch_reduce<64>, kClusterOk<64, 4>},
+    {{128, 128, 32, 3, false, kSplitPrepass}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>, kFixupOk<128, 3>},
+    {{128, 256, 32, 2, false, kSplitPrepass}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>, kFixupOk<256, 2>},
+    {{128, 64, 32, 4, false, kSplitPrepass}, launch_main<64, 4>, launch_reduce<64>, kClusterOk<64, 4>, kFixupOk<64, 4>},
     // pipeline-depth ablation: single-buffered (1) and shallower rings
-    {{128, 256, 32, 1, false, kSplitPrepass}, launch_main<256, 1>, launch_reduce<256>, kClusterOk<256, 1>},
-    {{128, 128, 32, 1, false, kSplitPrepass}, launch_main<128, 1>, launch_reduce<128>, kClusterOk<128, 1>},
-    {{128, 128, 32, 2, false, kSplitPrepass}, launch_main<128, 2>, launch_reduce<128>, kClusterOk<128, 2>},
-    {{128, 64, 32, 2, false, kSplitPrepass}, launch_main<64, 2>, launch_reduce<64>, kClusterOk<64, 2>},
+    {{128, 256, 32, 1, false, kSplitPrepass}, launch_main<256, 1>, launch_reduce<256>, kClusterOk<256, 1>, kFixupOk<256, 1>},
+    {{128, 128, 32, 1, false, kSplitPrepass}, launch_main<128, 1>, launch_reduce<128>, kClusterOk<128, 1>, kFixupOk<128, 1>},
+    {{128, 128, 32, 2, false, kSplitPrepass}, launch_main<128, 2>, launch_reduce<128>, kClusterOk<128, 2>, kFixupOk<128, 2>},
+    {{128, 64, 32, 2, false, kSplitPrepass}, launch_main<64, 2>, launch_reduce<64>, kClusterOk<64, 2>, kFixupOk<64, 2>},
     // barrier-coalescing ablation: separate full barriers for A and B
-    {{128, 256, 32, 2, true, kSplitPrepass}, launch_main<256, 2, true>, launch_reduce<256>, kClusterOk<256, 2>},
-    {{128, 128, 32, 3, true, kSplitPrepass}, launch_main<128, 3, true>, launch_reduce<128>, kClusterOk<128, 3>},
+    {{128, 256, 32, 2, true, kSplitPrepass}, launch_main<256, 2, true>, launch_reduce<256>, kClusterOk<256, 2>, kFixupOk<256, 2>},
+    {{128, 128, 32, 3, true, kSplitPrepass}, launch_main<128, 3, true>, launch_reduce<128>, kClusterOk<128, 3>, kFixupOk<128, 3>},
     // operands split inside the kernel (stages = MMA-facing slots; the fused
     // kernel's 3 x 64 KB ring holds the cluster sum's 128 KB, its 2 x 96 KB
     // ring of 128 x 256 tiles not the 256 KB those would need)
-    {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>, true},
-    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>, false},
+    {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>, true, true},
+    {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>, false, true},
     // A split inside the kernel, B by the pre-pass
-    {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>, true},
-    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>, false},
+    {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>, true, true},
+    {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>, false, true},
     // hi of A read from the caller's A, lo of A and both pieces of B by the pre-pass
-    {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>},
-    {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>},
+    {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>, kFixupOk<128, 3>},
+    {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>, kFixupOk<256, 2>},
 };
 
 }  // namespace
@@ -245,6 +248,13 @@ void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_req
     const bool cluster_fits = kTc[t.config_id].cluster_ok && t.dp_tiles == 0 && t.split_tiles > 0 &&
                               (t.splits == 2 || t.splits == 4) && t.split_tiles * t.splits <= sms;
     if (cluster_fits && t.cluster_mode == 2) t.cluster = t.splits;
+    // Split units that are all their CTA's last unit (at most one wave of
+    // them) and at most 8 slices: the last slice to arrive sums the tile.
+    t.fixup = 0;
+    const bool fixup_fits = kTc[t.config_id].fixup_ok && t.split_tiles > 0 && t.splits <= 8 &&
+                            t.split_tiles * t.splits <= sms && !t.cluster;
+    if (fixup_fits && t.cluster_mode == 3) t.fixup = 1;
+    t.sem_bytes = t.fixup ? size_t(t.split_tiles) * 4 * sizeof(int) : 0;
     t.partial_bytes = t.split_tiles && !t.cluster ? size_t(t.split_tiles) * t.splits * kBM * c.bn * sizeof(float)
                                                   : 0;
 }
@@ -330,6 +340,8 @@ TcArgs make_args(const TcPlanState& st, int64_t M, int64_t N, float* C, int64_t 
     a.withhold = st.withhold_stage;
     a.group = st.tile_group > 0 ? st.tile_group : 8;
     a.cluster = st.cluster;
+    a.fixup = st.fixup;
+    a.sem = st.sem;
     prepare_c_map(st, C, M, N, ldc);
     a.c_tma = st.c_tma;
     return a;
@@ -360,6 +372,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
 {
     const TcConfig& c = kTc[st.config_id].cfg;
     if (a.cluster > 1 && !kTc[r.id].cluster_ok) return cudaErrorInvalidValue;
+    if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
     if (r.in_kernel) {
         e = tc_fused_main(c.bn, c.split == kSplitHybrid, st, a,
@@ -372,7 +385,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     }
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);
-    if (st.split_tiles > 0 && a.cluster <= 1) e = kTc[r.id].reduce(st, a, s);
+    if (st.split_tiles > 0 && a.cluster <= 1 && !a.fixup) e = kTc[r.id].reduce(st, a, s);
     if (ev) cudaEventRecord(ev[3], s);
     return e;
 }
@@ -410,6 +423,7 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     out = full;
     tc_configure(out, mp, N, K, full.split_request);
     out.partial = nullptr;
+    out.sem = nullptr;
     out.c_ptr = nullptr;
     out.c_tma = 0;
     out.a_hi = full.a_hi + r0 * full.kp;

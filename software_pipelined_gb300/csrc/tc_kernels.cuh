@@ -156,7 +156,9 @@ struct TcLayout {
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     // cluster K-slice reduction: the receive buffer laid over the idle ring
     static constexpr bool CLUSTER_OK = ClusterSum<BN>::BYTES <= RING_BYTES;
-    static constexpr int NBARS = 3 * STAGES + 9;    // full, empty, tmem x4, drain, full_b, ready, recv, stg, sumd
+    static constexpr bool FIXUP_OK = kFixRingBytes <= RING_BYTES;
+    // full, empty, tmem x4, drain, full_b, ready, recv, stg, sumd, fixup loads x4
+    static constexpr int NBARS = 3 * STAGES + 13;
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     // At least 116 KB, so that two CTAs never share an SM (each holds up to
     // all 512 TMEM columns for its whole lifetime).
@@ -204,7 +206,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     const uint32_t recv_bar = ptx::smem_u32(bars + 3 * STAGES + 6);
     const uint32_t stg_bar = ptx::smem_u32(bars + 3 * STAGES + 7);
     const uint32_t sum_bar = ptx::smem_u32(bars + 3 * STAGES + 8);
+    auto fix_bar = [&](int q) { return ptx::smem_u32(bars + 3 * STAGES + 9 + q); };
     const bool clustered = L::CLUSTER_OK && args.cluster > 1;
+    const bool fixup = L::FIXUP_OK && args.fixup && !clustered;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -222,6 +226,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
         ptx::mbar_init(recv_bar, 1);
         ptx::mbar_init(stg_bar, 4);
         ptx::mbar_init(sum_bar, 4);
+        for (int q = 0; q < 4; ++q) ptx::mbar_init(fix_bar(q), 1);
         // the S-1 incoming slices of this CTA's rows complete the one phase
         if (clustered)
             ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((args.cluster - 1) *
@@ -379,6 +384,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             if (clustered) {
                 if (!cluster_reduce_store<BN>(args, &tm_c, tm, tn, taddr, quad, lane, ring, ring_ptr, ready_bar,
                                               recv_bar, stg_bar, sum_bar, limit, abort_flag))
+                    break;
+            } else if (fixup && u.slot >= 0 && w + (int)gridDim.x >= num_work) {
+                // a split unit (always its CTA's last): sum the tile's slices if last to arrive
+                if (!fixup_store<BN>(args, &tm_p, &tm_c, u, tm, tn, taddr, quad, lane, ring + quad * kFixWarpBytes,
+                                     ring_ptr + quad * kFixWarpBytes, fix_bar(quad), limit, abort_flag))
                     break;
             } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
                 // this CTA's last unit: the ring is idle, stage and store by TMA

@@ -485,6 +485,71 @@ def test_cluster_sum_refusals(shape, opts):
 
 
 # ---------------------------------------------------------------------------
+# K-slices summed by the last slice to arrive (per 32-row quadrant, an atomic
+# count) instead of the reduction kernel: the same slice order, the same bits.
+# ---------------------------------------------------------------------------
+
+FIXUP_CASES = [
+    # M, N, K, tile_n, split_k, operand_split
+    (1024, 1024, 1024, 256, 4, 2),   # the 1024^3 plan
+    (1024, 1024, 1024, 128, 2, 2),
+    (512, 512, 512, 128, 8, 2),      # 8 slices
+    (1000, 520, 264, 128, 2, 1),     # ragged; slices of 5 and 4 k-blocks
+    (500, 520, 256, 128, 4, 4),      # raw A
+    (600, 700, 1024, 256, 2, 3),     # hybrid, 128x256 tiles
+    (384, 300, 640, 64, 4, 1),       # 128x64 tiles
+    (200, 61, 160, 128, 2, 1),       # N not a multiple of 4: C by direct stores
+    (130, 33, 96, 64, 3, 1),         # quadrants past M, three slices
+]
+
+
+@pytest.mark.parametrize("case", FIXUP_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}_bn{c[3]}_s{c[4]}_m{c[5]}"
+                                                   for c in FIXUP_CASES])
+def test_last_arriver_sum_matches_reduction_kernel(case):
+    M, N, K, bn, split, mode = case
+    A = inputs.uniform_pm1(1741, M, K)
+    B = inputs.uniform_pm1(1742, K, N)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=bn, split_k=split, operand_split=mode)
+    Cf, df, okf, runs = run_gemm(A, B, split_reduce=3, repeat=3, **opts)
+    Ck, dk, okk, _ = run_gemm(A, B, split_reduce=1, **opts)
+    assert "last-arriver-sum" in df and "last-arriver-sum" not in dk
+    assert okf and okk
+    assert all(np.array_equal(r, Cf) for r in runs), "repeat runs differ (counters not reset?)"
+    assert np.array_equal(Cf, Ck), df
+    err, ok = check_against_oracle(Cf, A, B)
+    assert ok, f"{df}: {err}"
+
+
+def test_last_arriver_sum_tail_wave():
+    # 2560^2 with 128x256 tiles: 200 tiles, the last 48 split in 3 (144 units)
+    M = N = 2560
+    K = 1024
+    A = inputs.uniform_pm1(1743, M, K)
+    B = inputs.uniform_pm1(1744, K, N)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=256, operand_split=4)
+    Cf, df, okf, _ = run_gemm(A, B, split_reduce=3, **opts)
+    Ck, dk, okk, _ = run_gemm(A, B, split_reduce=1, **opts)
+    assert "last-arriver-sum" in df and "whole=152" in df, df
+    assert okf and okk and np.array_equal(Cf, Ck)
+    rows = np.repeat(np.array([0, 1, 1279, 2047, 2431, 2559]), N)
+    cols = np.tile(np.arange(N), 6)
+    Cref, S = oracle.gemm_f64_entries(A, B, rows, cols)
+    assert oracle.within_bound(Cf[rows, cols], Cref, S, K)
+
+
+@pytest.mark.parametrize("shape,opts", [
+    ((512, 512, 2048), dict(tile_n=128, split_k=16)),                            # 16 slices
+    ((512, 512, 512), dict(tile_n=128, stages=1, split_k=2, operand_split=1)),   # ring too small
+    ((2048, 2048, 1024), dict(tile_n=128, split_k=2)),                           # two waves of split units
+    ((2048, 1024, 1024), dict(tile_n=128, split_k=1)),                           # nothing split
+], ids=["sixteen_slices", "one_stage", "two_waves", "no_split"])
+def test_last_arriver_sum_refusals(shape, opts):
+    with pytest.raises(g.GemmError) as e:
+        g.Plan(*shape, variant=g.VARIANT_TCGEN05, split_reduce=3, **opts)
+    assert e.value.status == g.ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
 # The pipelined host-buffer run: row panels of whole 128-row tiles, B copied
 # and split once, each panel's A copy / GEMM / C copy overlapped on three
 # streams.  Every operand mode, ragged panels, padded leading dimensions,

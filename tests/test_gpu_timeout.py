@@ -94,3 +94,30 @@ def test_withheld_stage_in_a_cluster(mode):
         assert p.check() == g.OK
     Cref, S = oracle.gemm_f64(A, B)
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
+def test_withheld_stage_with_last_arriver_sum():
+    # Slices of 3 and 2 k-blocks; the 3-block slice never arrives.  Its
+    # partner counts its own arrival (not the last) and finishes; nobody sums
+    # the tile.  The host sees TIMEOUT; the check clears the arrival counters,
+    # and a normal plan afterwards is right.
+    import torch
+    M, N, K = 256, 256, 160
+    A = inputs.uniform_pm1(1507, M, K)
+    B = inputs.uniform_pm1(1508, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=2, operand_split=1, split_reduce=3)
+    with g.Plan(M, N, K, wait_timeout_cycles=1 << 22, debug_withhold_stage=3, **opts) as p:
+        assert "last-arriver-sum" in p.describe()
+        p.run(dA, dB, dC)
+        assert p.check() == g.ERR_TIMEOUT
+        assert p.check() == g.OK
+    torch.cuda.synchronize()
+    dC.fill_(float("nan"))
+    with g.Plan(M, N, K, **opts) as p:
+        for _ in range(2):
+            p.run(dA, dB, dC)
+        assert p.check() == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
