@@ -126,7 +126,10 @@ typedef struct {
                                distributed shared memory (needs every tile split in 2 or 4,
                                all slices resident at once, tiles at most 128 wide and a ring
                                of 128 KB or more; else UNSUPPORTED) */
-    int32_t reserved[1];
+    int32_t k_slices;       /* SIMT only: thread groups of a CTA that split each K-tile between
+                               them and add their register tiles at the end (1, 2 or 4; 0 = the
+                               dispatcher's choice): more warps per SM for small grids without a
+                               second launch */
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

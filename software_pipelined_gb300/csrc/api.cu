@@ -33,6 +33,7 @@ struct DispatchChoice {
     int fused;     // TC: where the split happens (kSplitPrepass / kSplitInKernel / kSplitHybrid)
     int group;     // TC: tile-rows per raster group (0 = default)
     int tile_k;    // SIMT: K-tile depth (0 = compiled default)
+    int k_slices;  // SIMT: K-slice groups inside the CTA (0 = 1)
 };
 
 #include "dispatch_table.inc"
@@ -122,6 +123,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.split_reduce < 0 || o.split_reduce > 3) return GEMM_F32_ERR_INVALID_ARG;
+    if (!(o.k_slices == 0 || o.k_slices == 1 || o.k_slices == 2 || o.k_slices == 4)) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -239,7 +241,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         }
         // A forced tile or ring replaces the choice, so the table's K-tile depth
         // and tile order (tuned for its own tile) no longer apply.
-        if (o.tile_m || o.tile_n || o.stages) c.tile_k = c.group = 0;
+        if (o.tile_m || o.tile_n || o.stages) c.tile_k = c.group = c.k_slices = 0;
         if (o.tile_m) c.tile_m = o.tile_m;
         if (o.tile_n) c.tile_n = o.tile_n;
         if (o.stages) c.stages = o.stages;
@@ -247,8 +249,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 
         if (c.variant == GEMM_F32_VARIANT_SIMT) {
             p->kind = kSimt;
+            const int ksl = o.k_slices ? o.k_slices : c.k_slices ? c.k_slices : 1;
             p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages, o.separate_syncs != 0,
-                                          o.tile_k ? o.tile_k : c.tile_k);
+                                          o.tile_k ? o.tile_k : c.tile_k, ksl);
             if (p->simt_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             const int bk = simt_config(p->simt_id).bk;
             int64_t split = c.split_k < 1 ? 1 : c.split_k;
@@ -262,9 +265,11 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 bytes += align256(size_t(split) * size_t(M) * size_t(p->ldp) * sizeof(float));
             }
             const SimtConfig& sc = simt_config(p->simt_id);
+            char ks[24] = "";
+            if (sc.ksl > 1) snprintf(ks, sizeof ks, " k_slices=%d", sc.ksl);
             snprintf(p->desc, sizeof p->desc,
-                     "simt tile=%dx%dx%d thread=%dx%d stages=%d%s split_k=%d", sc.bm, sc.bn, sc.bk,
-                     sc.tm, sc.tn, sc.stages, sc.sep ? " separate-syncs" : "", p->split_k);
+                     "simt tile=%dx%dx%d thread=%dx%d stages=%d%s%s split_k=%d", sc.bm, sc.bn, sc.bk,
+                     sc.tm, sc.tn, sc.stages, sc.sep ? " separate-syncs" : "", ks, p->split_k);
         } else {
             // The two-piece TF32 split keeps 22 of FP32's 24 significand bits, so
             // each product carries an error up to about 3*2^-22*|a||b|; against the

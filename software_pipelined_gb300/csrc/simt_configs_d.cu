@@ -1,0 +1,23 @@
+// Instantiations of the SIMT kernel, part d of 4: K split inside the CTA
+// (sliced K) for the small and skinny shapes, whose grids hold too few warps.
+#include "simt_kernel.cuh"
+
+namespace gemm_f32 {
+namespace simt_detail {
+
+extern const SimtEntry kSimtPartD[] = {
+    {{64, 64, 16, 4, 4, 3, false, 2}, launch_cfg<64, 64, 16, 4, 4, 3, false, 2>},
+    {{64, 64, 16, 4, 4, 2, false, 2}, launch_cfg<64, 64, 16, 4, 4, 2, false, 2>},
+    {{64, 64, 32, 4, 4, 2, false, 2}, launch_cfg<64, 64, 32, 4, 4, 2, false, 2>},
+    {{64, 64, 32, 4, 4, 2, false, 4}, launch_cfg<64, 64, 32, 4, 4, 2, false, 4>},
+    {{32, 32, 64, 4, 4, 1, false, 4}, launch_cfg<32, 32, 64, 4, 4, 1, false, 4>},
+    {{32, 32, 64, 4, 4, 2, false, 4}, launch_cfg<32, 32, 64, 4, 4, 2, false, 4>},
+    {{32, 32, 32, 4, 4, 2, false, 2}, launch_cfg<32, 32, 32, 4, 4, 2, false, 2>},
+    {{32, 32, 32, 4, 4, 2, false, 4}, launch_cfg<32, 32, 32, 4, 4, 2, false, 4>},
+    {{32, 64, 32, 4, 4, 2, false, 2}, launch_cfg<32, 64, 32, 4, 4, 2, false, 2>},
+    {{64, 32, 32, 4, 4, 2, false, 2}, launch_cfg<64, 32, 32, 4, 4, 2, false, 2>},
+};
+extern const int kSimtPartDCount = (int)(sizeof(kSimtPartD) / sizeof(kSimtPartD[0]));
+
+}  // namespace simt_detail
+}  // namespace gemm_f32

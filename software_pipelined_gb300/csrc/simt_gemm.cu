@@ -12,6 +12,8 @@ extern const SimtEntry kSimtPartB[];
 extern const int kSimtPartBCount;
 extern const SimtEntry kSimtPartC[];
 extern const int kSimtPartCCount;
+extern const SimtEntry kSimtPartD[];
+extern const int kSimtPartDCount;
 }  // namespace simt_detail
 
 namespace {
@@ -24,7 +26,9 @@ const SimtEntry& entry(int id)
     if (id < kSimtPartACount) return kSimtPartA[id];
     id -= kSimtPartACount;
     if (id < kSimtPartBCount) return kSimtPartB[id];
-    return kSimtPartC[id - kSimtPartBCount];
+    id -= kSimtPartBCount;
+    if (id < kSimtPartCCount) return kSimtPartC[id];
+    return kSimtPartD[id - kSimtPartCCount];
 }
 
 }  // namespace
@@ -32,16 +36,16 @@ const SimtEntry& entry(int id)
 int simt_num_configs()
 {
     using namespace simt_detail;
-    return kSimtPartACount + kSimtPartBCount + kSimtPartCCount;
+    return kSimtPartACount + kSimtPartBCount + kSimtPartCCount + kSimtPartDCount;
 }
 const SimtConfig& simt_config(int id) { return entry(id).cfg; }
-int simt_find_config(int bm, int bn, int stages, bool sep, int bk)
+int simt_find_config(int bm, int bn, int stages, bool sep, int bk, int ksl)
 {
-    // bk == 0: the shallowest K-tile compiled for this tile and ring
+    // bk == 0: the shallowest K-tile compiled for this tile, ring and slicing
     int best = -1;
     for (int i = 0; i < simt_num_configs(); ++i) {
         const SimtConfig& c = entry(i).cfg;
-        if (c.bm != bm || c.bn != bn || c.stages != stages || c.sep != sep) continue;
+        if (c.bm != bm || c.bn != bn || c.stages != stages || c.sep != sep || c.ksl != ksl) continue;
         if (bk != 0 && c.bk != bk) continue;
         if (best < 0 || c.bk < entry(best).cfg.bk) best = i;
     }

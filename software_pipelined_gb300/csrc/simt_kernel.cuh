@@ -16,6 +16,13 @@
 // (copy A; barrier; copy B; barrier; compute; ...), where the default form
 // publishes both with one barrier.
 //
+// KSL > 1 splits K inside the CTA ("sliced K"): KSL groups of threads share
+// the staged tiles, group g taking k = g*BK/KSL .. (g+1)*BK/KSL-1 of every
+// K-tile with its own register tile; at the end groups 1..KSL-1 hand their
+// tiles to group 0 through shared memory, which adds them in group order and
+// stores.  For small grids (tens of CTAs) it multiplies the warps an SM can
+// switch between without a second (reduction) launch.
+//
 // Layout: A tile As[BM][BK+4] (row-major, as in global memory, so the copy is a
 // straight 16-byte cp.async when rows are 16-byte aligned), B tile
 // Bs[BK][BN+4].  Each thread owns a TM x TN register tile built from 4x4 blocks
@@ -31,35 +38,41 @@
 namespace gemm_f32 {
 namespace simt_detail {
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL>
 struct SimtKernel {
     static constexpr int TX = BN / TN;
     static constexpr int TY = BM / TM;
-    static constexpr int NT = TX * TY;
+    static constexpr int NT = TX * TY;       // threads of one K-slice group
+    static constexpr int NTT = NT * KSL;     // threads of the CTA
     static constexpr int LDA_S = BK + 4;   // floats per As row
     static constexpr int LDB_S = BN + 4;   // floats per Bs row
     static constexpr int A_STAGE = BM * LDA_S;
     static constexpr int B_STAGE = BK * LDB_S;
-    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr int RING_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr int RED_BYTES = (KSL - 1) * NT * TM * TN * 4;  // the groups' hand-over
+    static constexpr int SMEM_BYTES = RING_BYTES > RED_BYTES ? RING_BYTES : RED_BYTES;
     static_assert(TM % 4 == 0 && TN % 4 == 0, "register tile is built from 4x4 blocks");
-    static_assert(BK % 4 == 0, "BK multiple of 4");
-    static_assert(NT >= 32 && NT <= 1024, "block size");
+    static_assert(BK % (4 * KSL) == 0, "each K-slice group takes whole float4 columns of A");
+    static_assert(NT >= 32 && NTT <= 1024, "block size");
     static_assert(!SEP || STAGES <= 2, "separate barriers: 1 or 2 stages");
+    static_assert(!SEP || KSL == 1, "the barrier ablation runs unsliced");
 };
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
-__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN) * KSL)
 simt_gemm_kernel(SimtArgs a)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
-    constexpr int NT = KT::NT, TX = KT::TX;
+    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
+    constexpr int NT = KT::NT, NTT = KT::NTT, TX = KT::TX;
     constexpr int RG = TM / 4, CG = TN / 4;
     extern __shared__ __align__(16) float smem[];
     float* As = smem;
     float* Bs = smem + STAGES * KT::A_STAGE;
 
-    const int tid = threadIdx.x;
-    const int tx = tid % TX, ty = tid / TX;
+    const int tid = threadIdx.x;              // copies: all NTT threads
+    const int slice = tid / NT;               // K-slice group
+    const int tt = tid % NT;                  // thread within the group
+    const int tx = tt % TX, ty = tt / TX;
     const int64_t m0 = (int64_t)blockIdx.y * BM;
     const int64_t n0 = (int64_t)blockIdx.x * BN;
     const bool batched = a.batch > 1;
@@ -76,7 +89,7 @@ simt_gemm_kernel(SimtArgs a)
         const int64_t k0 = kbeg + (int64_t)t * BK;
         float* as = As + st * KT::A_STAGE;
         if constexpr (VA) {
-            for (int c = tid; c < BM * BK / 4; c += NT) {
+            for (int c = tid; c < BM * BK / 4; c += NTT) {
                 const int r = c / (BK / 4), kc = (c % (BK / 4)) * 4;
                 const int64_t gm = m0 + r, gk = k0 + kc;
                 int bytes = 0;
@@ -88,7 +101,7 @@ simt_gemm_kernel(SimtArgs a)
                 ptx::cp_async_16(ptx::smem_u32(as + r * KT::LDA_S + kc), src, bytes);
             }
         } else {
-            for (int e = tid; e < BM * BK; e += NT) {
+            for (int e = tid; e < BM * BK; e += NTT) {
                 const int r = e / BK, kk = e % BK;
                 const int64_t gm = m0 + r, gk = k0 + kk;
                 const bool ok = gm < M && gk < kend;
@@ -101,7 +114,7 @@ simt_gemm_kernel(SimtArgs a)
         const int64_t k0 = kbeg + (int64_t)t * BK;
         float* bs = Bs + st * KT::B_STAGE;
         if constexpr (VB) {
-            for (int c = tid; c < BK * BN / 4; c += NT) {
+            for (int c = tid; c < BK * BN / 4; c += NTT) {
                 const int r = c / (BN / 4), nc = (c % (BN / 4)) * 4;
                 const int64_t gk = k0 + r, gn = n0 + nc;
                 int bytes = 0;
@@ -113,7 +126,7 @@ simt_gemm_kernel(SimtArgs a)
                 ptx::cp_async_16(ptx::smem_u32(bs + r * KT::LDB_S + nc), src, bytes);
             }
         } else {
-            for (int e = tid; e < BK * BN; e += NT) {
+            for (int e = tid; e < BK * BN; e += NTT) {
                 const int r = e / BN, nn = e % BN;
                 const int64_t gk = k0 + r, gn = n0 + nn;
                 const bool ok = gk < kend && gn < N;
@@ -137,7 +150,8 @@ simt_gemm_kernel(SimtArgs a)
         const float* as = As + st * KT::A_STAGE;
         const float* bs = Bs + st * KT::B_STAGE;
 #pragma unroll
-        for (int kk = 0; kk < BK; kk += 4) {
+        for (int k4 = 0; k4 < BK / KSL; k4 += 4) {
+            const int kk = slice * (BK / KSL) + k4;
             float4 av[TM];
 #pragma unroll
             for (int g = 0; g < RG; ++g)
@@ -227,6 +241,26 @@ simt_gemm_kernel(SimtArgs a)
         ptx::cp_async_wait<0>();
     }
 
+    if constexpr (KSL > 1) {
+        // Hand the register tiles of groups 1..KSL-1 to group 0 (lane-major:
+        // consecutive threads, consecutive words), which adds them in order.
+        __syncthreads();  // every group is done reading the ring
+        float* red = smem;
+        if (slice > 0) {
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) red[((slice - 1) * TM * TN + i * TN + j) * NT + tt] = acc[i][j];
+        }
+        __syncthreads();
+        if (slice > 0) return;
+        for (int g = 1; g < KSL; ++g)
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] += red[((g - 1) * TM * TN + i * TN + j) * NT + tt];
+    }
+
     // Epilogue: guarded stores of the register tile (16-byte when aligned).
     float* out;
     int64_t ld;
@@ -260,30 +294,30 @@ simt_gemm_kernel(SimtArgs a)
     }
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL>
 cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
-    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP>;
+    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
+    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, KT::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
               (unsigned)(a.batch > 1 ? a.batch : a.split_k));
-    kern<<<grid, KT::NT, KT::SMEM_BYTES, s>>>(a);
+    kern<<<grid, KT::NTT, KT::SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false, int KSL = 1>
 cudaError_t launch_cfg(const SimtArgs& a, cudaStream_t s)
 {
     const bool va = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) &&
                     (a.batch <= 1 || a.stride_a % 4 == 0);
     const bool vb = (a.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
                     (a.batch <= 1 || a.stride_b % 4 == 0);
-    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP>(a, s);
-    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP>(a, s);
-    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP>(a, s);
-    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false, SEP>(a, s);
+    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP, KSL>(a, s);
+    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP, KSL>(a, s);
+    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP, KSL>(a, s);
+    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false, SEP, KSL>(a, s);
 }
 
 using LaunchFn = cudaError_t (*)(const SimtArgs&, cudaStream_t);

@@ -74,10 +74,11 @@ def candidates(M, N, K):
     macs = M * N * K
     if macs <= 2 ** 31:
         for (bm, bn, st, bk) in SIMT_CFGS:
-            for sp in SPLITS:
-                if sp == 1 or K // sp >= 32:
-                    out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp,
-                                    tile_k=bk))
+            for ksl in (1, 2, 4):
+                for sp in SPLITS:
+                    if sp == 1 or K // sp >= 32:
+                        out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp,
+                                        tile_k=bk, k_slices=ksl))
     if K >= 16:
         for bn in TC_BN:
             for fused in ((1, 2, 3, 4) if bn in (128, 256) and K >= 32 else (1,)):
@@ -165,7 +166,8 @@ def write_inc(results, path):
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
         "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass,",
         "// 3 hi of A read from A),",
-        "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k (SIMT).",
+        "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k and",
+        "// k_slices (SIMT: K-tile depth, K-slice groups inside the CTA).",
         "struct TableRow {",
         "    int64_t M, N, K;",
         "    DispatchChoice c;",
@@ -178,10 +180,10 @@ def write_inc(results, path):
         split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
                      f"{o['stages']}, {split}, {split_where(r['best']['plan'])}, {o.get('tile_group', 0)}, "
-                     f"{o.get('tile_k', 0)}}}}},"
+                     f"{o.get('tile_k', 0)}, {o.get('k_slices', 0)}}}}},"
                      f"  // {r['best']['us']} us")
     lines += [
-        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel",
+        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel",
         "};",
         "",
         "bool table_lookup(int64_t M, int64_t N, int64_t K, DispatchChoice& out)",

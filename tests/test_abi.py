@@ -46,7 +46,7 @@ def test_status_strings_and_version(lib):
 
 
 def test_opts_layout_matches_header(lib):
-    # int32 x6, int64, int32, int32[7] -> 6*4 + 8 + 4 + 28 = 64 bytes
+    # int32 x6, int64, int32 x8 -> 6*4 + 8 + 8*4 = 64 bytes
     assert ctypes.sizeof(g.Opts) == 64
     o = g.gemm_f32_opts_init()
     assert o.variant == 0 and o.split_k == 0 and o.wait_timeout_cycles == 0
@@ -70,7 +70,7 @@ def test_plan_rejects_bad_dims(lib, dims):
 def test_plan_rejects_bad_options(lib):
     for field, value in [("variant", 7), ("split_k", 65), ("tf32_terms", 2), ("stages", -1),
                          ("wait_timeout_cycles", -5), ("operand_split", 5), ("tile_group", 65),
-                         ("host_panels", 65), ("host_panels", -1), ("split_reduce", 4), ("split_reduce", -1)]:
+                         ("host_panels", 65), ("host_panels", -1), ("split_reduce", 4), ("split_reduce", -1), ("k_slices", 3), ("k_slices", 8)]:
         o = g.gemm_f32_opts_init()
         setattr(o, field, value)
         s, h = g.gemm_f32_plan_ex(64, 64, 64, 64, 64, 64, o)

@@ -206,6 +206,46 @@ def test_every_simt_config(cfg, aligned):
     assert canaries and ok, f"{desc}: {err}"
 
 
+# K split inside the CTA: (tile_m, tile_n, stages, tile_k, k_slices)
+SIMT_KSL_CFGS = [(64, 64, 3, 16, 2), (64, 64, 2, 16, 2), (64, 64, 2, 32, 2), (64, 64, 2, 32, 4),
+                 (32, 32, 1, 64, 4), (32, 32, 2, 64, 4), (32, 32, 2, 32, 2), (32, 32, 2, 32, 4),
+                 (32, 64, 2, 32, 2), (64, 32, 2, 32, 2)]
+
+
+@pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
+@pytest.mark.parametrize("cfg", SIMT_KSL_CFGS, ids=[f"{a}x{b}x{d}s{c}ksl{e}" for a, b, c, d, e in SIMT_KSL_CFGS])
+def test_every_sliced_k_simt_config(cfg, aligned):
+    bm, bn, st, bk, ksl = cfg
+    # ragged in M, N and K (K not a multiple of the tile, so the last tile's
+    # slices are partly or wholly zero-filled), with and without split-K
+    M, N, K = 2 * bm + 5, 3 * bn + 3, 3 * bk + 7
+    A = inputs.uniform_pm1(953, M, K)
+    B = inputs.uniform_pm1(954, K, N)
+    kw = {} if aligned else dict(lda=K + 1, ldb=N + 2, a_off=1, b_off=1)
+    for split in (1, 2):
+        C, desc, canaries, runs = run_gemm(A, B, variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st,
+                                           tile_k=bk, k_slices=ksl, split_k=split, repeat=2, **kw)
+        assert f"k_slices={ksl}" in desc and f"tile={bm}x{bn}x{bk}" in desc, desc
+        assert np.array_equal(runs[0], runs[1]), "not deterministic"
+        err, ok = check_against_oracle(C, A, B)
+        assert canaries and ok, f"{desc}: {err}"
+
+
+def test_sliced_k_small_integers_bit_exact():
+    M, N, K = 70, 90, 200
+    A = inputs.small_int(955, M, K)
+    B = inputs.small_int(956, K, N)
+    C, desc, canaries, _ = run_gemm(A, B, variant=g.VARIANT_SIMT, tile_m=32, tile_n=32, stages=2, tile_k=64,
+                                    k_slices=4)
+    assert canaries and np.array_equal(C, A.astype(np.float64) @ B.astype(np.float64)), desc
+
+
+def test_sliced_k_refusals():
+    for opts in (dict(k_slices=3), dict(tile_m=128, tile_n=128, stages=2, k_slices=2)):
+        with pytest.raises(g.GemmError):
+            g.Plan(256, 256, 256, variant=g.VARIANT_SIMT, **opts)
+
+
 TC_CFGS = [(128, 3, 0), (256, 2, 0), (64, 4, 0), (256, 1, 0), (128, 1, 0), (128, 2, 0), (64, 2, 0),
            (256, 2, 1), (128, 3, 1)]
 
