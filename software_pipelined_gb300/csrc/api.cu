@@ -279,7 +279,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             TcPlanState& t = p->tc;
             // operand_split: 1 pre-pass, 2 in the kernel, 3 hybrid (A in the kernel,
             // B by the pre-pass), 4 hi of A read from A; 0 = the dispatcher's choice.
-            int where = o.operand_split ? o.operand_split - 1 : c.fused;
+            // A forced ring depth exists only in the pre-pass form (the other
+            // forms have one depth per tile width), so it selects that form.
+            int where = o.operand_split ? o.operand_split - 1 : o.stages ? kSplitPrepass : c.fused;
             const bool ok = where == kSplitPrepass ||
                             (K >= kTcFusedMinK && lda % 4 == 0 && (where != kSplitInKernel || ldb % 4 == 0) &&
                              !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where) >= 0);

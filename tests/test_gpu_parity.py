@@ -212,6 +212,17 @@ SIMT_KSL_CFGS = [(64, 64, 3, 16, 2), (64, 64, 2, 16, 2), (64, 64, 2, 32, 2), (64
                  (32, 64, 2, 32, 2), (64, 32, 2, 32, 2)]
 
 
+@pytest.mark.parametrize("shape", [(512, 512, 512), (1024, 1024, 1024), (4096, 4096, 4096)])
+@pytest.mark.parametrize("stages", [1, 2])
+def test_forced_stages_select_the_pre_pass_form(shape, stages):
+    # the table picks in-kernel or raw-A splits (fixed depth) for these shapes;
+    # a forced depth must give that depth, in the pre-pass form
+    bn = 256 if stages == 1 else 128
+    with g.Plan(*shape, variant=g.VARIANT_TCGEN05, tile_n=bn, stages=stages) as p:
+        d = p.describe()
+    assert f"stages={stages}" in d and "in-kernel" not in d and "raw-a" not in d and "hybrid" not in d, d
+
+
 @pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
 @pytest.mark.parametrize("cfg", SIMT_KSL_CFGS, ids=[f"{a}x{b}x{d}s{c}ksl{e}" for a, b, c, d, e in SIMT_KSL_CFGS])
 def test_every_sliced_k_simt_config(cfg, aligned):
