@@ -605,8 +605,8 @@ def run_reference_arm(args):
     name, M, N, K, dist_name, sa, sb = big
     A, B = inputs.make_operands(M, N, K, dist_name, sa, sb)
     threads = oracle.get_threads()
-    # size one step so that warmup + steps take about two minutes in all
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    # size one step so that warmup + steps take about --ref-seconds in all
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     _, rows, _, _ = oracle_sample(A, B, budget)
     for _ in range(args.warmup):
         oracle_rows_rate(A, B, rows)
@@ -645,6 +645,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the parity checks inside the bench")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle work for warm-up + timed steps")
     ap.add_argument("--json-out", default=None)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
