@@ -4,15 +4,21 @@
  * The operation is the tiled dense FP32 GEMM whose K-loop stages tiles of A
  * and B through on-chip memory with a double-buffered / multi-stage prefetch
  * ("Double Buffering" technique page; "Case Study: The Double-Buffered GEMM",
- * the sync_copy_db listing and the paragraph on the single barrier's double
- * duty).  Three kernels sit behind this interface:
+ * its kernel listing and the paragraph on the single barrier's double duty).
+ * Behind this interface:
  *
- *   - a tcgen05 tensor-core kernel: a TMA producer warp fills an N-stage
+ *   - tcgen05 tensor-core kernels: a TMA producer warp fills an N-stage
  *     mbarrier ring in shared memory, an MMA warp accumulates into TMEM with an
- *     error-compensated 3xTF32 split, an epilogue warpgroup drains TMEM;
- *   - a SIMT FFMA kernel with cp.async double/multi-stage buffering, for tiny,
- *     latency-bound shapes;
- *   - a deterministic split-K reduction.
+ *     error-compensated 3xTF32 split, an epilogue warpgroup drains TMEM
+ *     (TMA stores for each CTA's last tile); persistent over tiles, the last
+ *     wave's tiles split into K-slices.  The operands are split into TF32
+ *     pieces by a pre-pass kernel, or inside the GEMM kernel by converter
+ *     warps, or half and half (see gemm_f32_opts.operand_split);
+ *   - a SIMT FFMA kernel with cp.async double/multi-stage buffering (and an
+ *     optional K split across the thread groups of a CTA), for small,
+ *     latency-bound shapes and strided batches;
+ *   - deterministic split-K reductions (a reduction kernel; optionally inside
+ *     a thread-block cluster or by the last K-slice to arrive).
  *
  * A per-shape dispatcher chooses kernel, tile, stage count and split-K
  * ("Double Buffering" page, last paragraph, and the case study's first
