@@ -257,21 +257,42 @@ def make_device_operands(M, N, K, dist, sa, sb):
     return A, B, dA, dB, dC
 
 
-def parity(A, B, Cd, full_limit=2 ** 31):
-    """Max normalised error of the GPU result against the oracle: the full
-    output for moderate sizes, sampled outputs beyond."""
-    import oracle
+def capture_for_check(A, B, Cd, full_limit=2 ** 31):
+    """What the oracle comparison needs of a GPU result (no oracle here): the
+    whole output for moderate sizes, 1028 sampled entries beyond."""
     M, K = A.shape
     N = B.shape[1]
-    C = Cd.cpu().numpy()
     if M * N * K <= full_limit:
-        Cr, S = oracle.gemm_f64(A, B)
-        return oracle.normalised_error(C, Cr, S, K), "full"
+        return {"A": A, "B": B, "kind": "full", "C": Cd.cpu().numpy()}
     rng = np.random.default_rng(12345)
     rows = np.concatenate([[0, M - 1, 0, M - 1], rng.integers(0, M, 1024)])
     cols = np.concatenate([[0, 0, N - 1, N - 1], rng.integers(0, N, 1024)])
-    c, s = oracle.gemm_f64_entries(A, B, rows, cols)
-    return oracle.normalised_error(C[rows, cols], c, s, K), "sampled-1028"
+    import torch
+    vals = Cd[torch.from_numpy(rows).to(Cd.device), torch.from_numpy(cols).to(Cd.device)].cpu().numpy()
+    return {"A": A, "B": B, "kind": "sampled-1028", "rows": rows, "cols": cols, "vals": vals}
+
+
+def compare_with_oracle(chk):
+    """Max normalised error of a captured GPU result against the oracle."""
+    import oracle
+    A, B = chk["A"], chk["B"]
+    K = A.shape[1]
+    if chk["kind"] == "full":
+        Cr, S = oracle.gemm_f64(A, B)
+        return round(oracle.normalised_error(chk["C"], Cr, S, K), 4), "full"
+    c, s = oracle.gemm_f64_entries(A, B, chk["rows"], chk["cols"])
+    return round(oracle.normalised_error(chk["vals"], c, s, K), 4), chk["kind"]
+
+
+def time_oracle(A, B, n):
+    """Median host wall time (s) of n full oracle products."""
+    import oracle
+    ts = []
+    for _ in range(n):
+        t0 = time.perf_counter()
+        oracle.gemm_f64(A, B, with_scale=False)
+        ts.append(time.perf_counter() - t0)
+    return statistics.median(ts)
 
 
 def source_hash(paths):
@@ -417,12 +438,14 @@ def run_gpu_arm(args):
                 "per_shape": per_kernel}
     launches = args.steps * sum(w["plan"].kernel_launches for w in work)
 
-    # headline parity (sampled against the oracle)
+    # headline results kept for the comparison with the oracle (below, in the
+    # CPU-baseline leg; nothing here runs the oracle)
     headline_parity = {}
+    checks = []  # (where to record, captured result)
     if rank == 0 and not args.quick:
         for w in work:
-            err, how = parity(w["A"], w["B"], w["dC"], full_limit=0)
-            headline_parity[w["name"]] = {"max_normalised_error": round(err, 4), "checked": how}
+            headline_parity[w["name"]] = {}
+            checks.append((headline_parity[w["name"]], capture_for_check(w["A"], w["B"], w["dC"], full_limit=0)))
 
     # ---- e2e: through the C-ABI host-buffer call ------------------------------
     e2e = None
@@ -463,53 +486,95 @@ def run_gpu_arm(args):
     if rank == 0 and not args.no_per_shape:
         per_shape = []
         from software_pipelined_gb300 import inputs
+        # every shape's operands and plan, kept for all rounds
+        cases = []
         for key in ("tiny_32", "small_ragged", "tall_skinny", "square_1024", "large_squares"):
             for (name, M, N, K, dist_name, sa, sb) in inputs.WORKLOADS[key]:
                 if key == args.workload and not args.shape:
                     w = next(x for x in work if x["name"] == name)
                     A, B, dA, dB, dC, plan = w["A"], w["B"], w["dA"], w["dB"], w["dC"], w["plan"]
+                    own = False
                 else:
                     A, B, dA, dB, dC = make_device_operands(M, N, K, dist_name, sa, sb)
                     plan = g.Plan(M, N, K)
-                run = (lambda p=plan, a=dA, b=dB, c=dC: p.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), sptr))
-                run_on = (lambda st, p=plan, a=dA, b=dB, c=dC: p.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), st))
-                s_med, _, _, _ = time_batches(run, stream)
+                    own = True
+                cases.append(dict(key=key, name=name, M=M, N=N, K=K, A=A, B=B, dA=dA, dB=dB, dC=dC, plan=plan,
+                                  own=own, rounds=[], lo=float("inf"), hi=0.0, reps=0))
+        # rounds in rotated shape order (timing protocol of the comparison on
+        # the pages: a shape's place in the sequence must not favour it);
+        # each round: the median of 5 graph-replayed batches per shape
+        ROUNDS = 3
+        for r in range(ROUNDS):
+            for i in range(len(cases)):
+                c = cases[(i + r) % len(cases)]
+                run_on = (lambda st, p=c["plan"], a=c["dA"], b=c["dB"], cc=c["dC"]:
+                          p.run_ptr(a.data_ptr(), b.data_ptr(), cc.data_ptr(), st))
                 med, lo, hi, reps = time_graph(run_on)
-                # phase breakdown of a few more runs (library-recorded events)
-                plan.trace_enable(8)
-                for _ in range(8):
+                c["rounds"].append(med)
+                c["lo"], c["hi"], c["reps"] = min(c["lo"], lo), max(c["hi"], hi), reps
+        flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > L2
+        for c in cases:
+            key, name, M, N, K = c["key"], c["name"], c["M"], c["N"], c["K"]
+            A, B, dA, dB, dC, plan = c["A"], c["B"], c["dA"], c["dB"], c["dC"], c["plan"]
+            run = (lambda p=plan, a=dA, b=dB, cc=dC: p.run_ptr(a.data_ptr(), b.data_ptr(), cc.data_ptr(), sptr))
+            med = statistics.median(c["rounds"])
+            s_med, _, _, _ = time_batches(run, stream)
+            # phase breakdown of a few more runs (library-recorded events)
+            plan.trace_enable(8)
+            for _ in range(8):
+                run()
+            phases = plan.trace_read(8)
+            plan.trace_enable(0)
+            ph = [round(sum(r[i] for r in phases) / len(phases) * 1e3, 3) for i in range(3)]
+            # cold L2 for the 1024^3 square: a 256 MB write between runs, outside the events
+            cold = None
+            if name == "1024x1024x1024":
+                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ts = []
+                for _ in range(9):
+                    flush.fill_(1.0)
+                    ev0.record(stream)
                     run()
-                phases = plan.trace_read(8)
-                plan.trace_enable(0)
-                ph = [round(sum(r[i] for r in phases) / len(phases) * 1e3, 3) for i in range(3)]
-                fl = 2.0 * M * N * K
-                byts = algorithmic_bytes(M, N, K)
-                P = pk["f32_3xtf32_tflops_burst"]
-                t_roof = max(fl / (P * 1e12), byts / (pk["hbm_gbs"] * 1e9))
-                t_roof_simt = max(fl / (pk["f32_simt_tflops_nominal"] * 1e12), byts / (pk["hbm_gbs"] * 1e9))
-                err, how = (None, None) if args.quick else parity(A, B, dC)
-                # comparison column, off the measured path: PyTorch's FP32 matmul
-                # (cuBLAS SGEMM, TF32 disabled) timed the same way
-                torch.backends.cuda.matmul.allow_tf32 = False
-                dC2 = torch.empty_like(dC)
-                cb, _, _, _ = time_graph(lambda st, a=dA, b=dB, c=dC2: torch.mm(a, b, out=c))
-                del dC2
-                per_shape.append({
-                    "config": key, "shape": name, "plan": plan.describe(),
-                    "us": round(med * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
-                    "us_direct_launch": round(s_med * 1e3, 3),
-                    "torch_fp32_matmul_us": round(cb * 1e3, 3),
-                    "phases_us_split_main_reduce": ph,
-                    "tflops": round(fl / (med * 1e-3) / 1e12, 3),
-                    "roofline_frac": round(t_roof / (med * 1e-3), 4),
-                    "roofline_frac_vs_simt_peak": round(t_roof_simt / (med * 1e-3), 4),
-                    "max_normalised_error": None if err is None else round(err, 4), "checked": how,
-                    "l2": "warm (back-to-back)" if byts < 100e6 else "inputs larger than L2",
-                    "timing": "CUDA graph of back-to-back runs, events around each replay",
-                    "runs_per_batch": reps})
-                if key != args.workload or args.shape:
-                    plan.close()
-                    del dA, dB, dC
+                    ev1.record(stream)
+                    ev1.synchronize()
+                    ts.append(ev0.elapsed_time(ev1))
+                cold = round(statistics.median(ts) * 1e3, 3)
+            fl = 2.0 * M * N * K
+            byts = algorithmic_bytes(M, N, K)
+            P = pk["f32_3xtf32_tflops_burst"]
+            t_roof = max(fl / (P * 1e12), byts / (pk["hbm_gbs"] * 1e9))
+            t_roof_simt = max(fl / (pk["f32_simt_tflops_nominal"] * 1e12), byts / (pk["hbm_gbs"] * 1e9))
+            # comparison column, off the measured path: PyTorch's FP32 matmul
+            # (cuBLAS SGEMM, TF32 disabled) timed the same way
+            torch.backends.cuda.matmul.allow_tf32 = False
+            dC2 = torch.empty_like(dC)
+            cb, _, _, _ = time_graph(lambda st, a=dA, b=dB, cc=dC2: torch.mm(a, b, out=cc))
+            del dC2
+            entry = {
+                "config": key, "shape": name, "plan": plan.describe(),
+                "us": round(med * 1e3, 3), "us_min": round(c["lo"] * 1e3, 3), "us_max": round(c["hi"] * 1e3, 3),
+                "us_rounds": [round(x * 1e3, 3) for x in c["rounds"]],
+                "us_direct_launch": round(s_med * 1e3, 3),
+                "torch_fp32_matmul_us": round(cb * 1e3, 3),
+                "phases_us_split_main_reduce": ph,
+                "tflops": round(fl / (med * 1e-3) / 1e12, 3),
+                "roofline_frac": round(t_roof / (med * 1e-3), 4),
+                "roofline_frac_vs_simt_peak": round(t_roof_simt / (med * 1e-3), 4),
+                "max_normalised_error": None, "checked": None,  # filled by the CPU-baseline leg
+                "l2": "warm (back-to-back)" if byts < 100e6 else "inputs larger than L2",
+                "timing": (f"median of {ROUNDS} rounds (rotated shape order) of the median of 5 CUDA-graph "
+                           "replays of back-to-back runs, events around each replay"),
+                "runs_per_batch": c["reps"]}
+            if cold is not None:
+                entry["us_cold_l2"] = cold
+            per_shape.append(entry)
+            if not args.quick:
+                checks.append((entry, capture_for_check(A, B, dC)))
+        del flush
+        for c in cases:
+            if c["own"]:
+                c["plan"].close()
+        del cases
         # launch/event floors on this stream
         ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ts = []
@@ -534,32 +599,53 @@ def run_gpu_arm(args):
                 bmed, _, _, _ = time_graph(lambda st, p=bp: p.run_ptr(Ab.data_ptr(), Bb.data_ptr(),
                                                                        Cb.data_ptr(), st))
                 bdesc = bp.describe()
-            # spot check of the last product against the oracle
-            import oracle as _or
-            a_last = Ab[(nb - 1) * bm:].cpu().numpy()
-            b_last = Bb[(nb - 1) * bk:].cpu().numpy()
-            cr, sr = _or.gemm_f64(a_last, b_last)
-            berr = _or.normalised_error(Cb[(nb - 1) * bm:].cpu().numpy(), cr, sr, bk)
+            # the last product, kept for the comparison with the oracle
+            last = {"A": Ab[(nb - 1) * bm:].cpu().numpy(), "B": Bb[(nb - 1) * bk:].cpu().numpy(),
+                    "kind": "full", "C": Cb[(nb - 1) * bm:].cpu().numpy()}
             fl = 2.0 * bm * bn * bk * nb
             batched.append({"products": nb, "shape": f"{bm}x{bn}x{bk}", "plan": bdesc,
                             "us_per_launch": round(bmed * 1e3, 3),
                             "us_per_product": round(bmed * 1e3 / nb, 4),
-                            "tflops": round(fl / (bmed * 1e-3) / 1e12, 3),
-                            "max_normalised_error_last_product": round(berr, 4)})
+                            "tflops": round(fl / (bmed * 1e-3) / 1e12, 3)})
+            if not args.quick:
+                checks.append((batched[-1], dict(last, field="max_normalised_error_last_product")))
             del Ab, Bb, Cb
         floors = {"event_pair_us": round(statistics.median(ts) * 1e3, 3),
                   "smallest_kernel_direct_launch_us": round(med * 1e3, 3),
                   "smallest_kernel_graph_us": round(gmed * 1e3, 3),
                   "note": "smallest kernel = this library's 1x1 zero-fill, back to back"}
 
-    # ---- CPU baseline: the oracle on a bounded sample ------------------------
+    # ---- CPU-baseline leg: the oracle, on this host's cores ------------------
+    # The only part of the GPU arm that runs the oracle: its throughput on a
+    # bounded sample of the headline workload, its time beside each small
+    # shape, and the comparison of every result kept above against it.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
         big = max(work, key=lambda w: w["M"] * w["N"] * w["K"])
         tf, rows, dt, threads = oracle_sample(big["A"], big["B"], args.cpu_seconds)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"first {rows} rows of {big['name']} ({rows}x{big['N']}x{big['K']}), "
                          f"FP64 i-k-j triple loop, {dt:.1f} s"}
+        for where, chk in checks:
+            err, how = compare_with_oracle(chk)
+            if "field" in chk:
+                where[chk["field"]] = err
+            else:
+                where["max_normalised_error"], where["checked"] = err, how
+            A, B = chk["A"], chk["B"]
+            macs = A.shape[0] * B.shape[1] * A.shape[1]
+            if "shape" in where and macs <= 1024 ** 3:
+                # the oracle timed beside the GPU: median of 3, all cores; one core up to 512^3
+                orc = {"ms_all_cores": round(time_oracle(A, B, 3) * 1e3, 3), "cores": threads}
+                if macs <= 512 ** 3:
+                    oracle.set_threads(1)
+                    try:
+                        orc["ms_one_core"] = round(time_oracle(A, B, 3) * 1e3, 3)
+                    finally:
+                        oracle.set_threads(threads)
+                where["oracle"] = orc
+    del checks
 
     if rank == 0:
         line = {
