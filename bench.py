@@ -295,6 +295,33 @@ def time_oracle(A, B, n):
     return statistics.median(ts)
 
 
+def run_environment(device):
+    """Where the numbers were taken: device, SM count, driver and CUDA versions,
+    host cores, and the sources (git revision where .git exists, else a hash
+    of the CUDA sources, the header and the dispatch table)."""
+    import subprocess
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    env = {"device": props.name, "sm_count": props.multi_processor_count,
+           "memory_gib": round(props.total_memory / 2 ** 30, 1),
+           "cuda_runtime": torch.version.cuda, "torch": torch.__version__, "host_cores": os.cpu_count()}
+    try:
+        env["driver"] = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                                        "-i", str(device)], capture_output=True, text=True,
+                                       timeout=20).stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        env["driver"] = None
+    try:
+        env["git_revision"] = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                                             text=True, timeout=20).stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        env["git_revision"] = None
+    csrc = os.path.join(ROOT, "software_pipelined_gb300", "csrc")
+    env["sources_sha256_16"] = source_hash(sorted(os.path.join(csrc, f) for f in os.listdir(csrc)) +
+                                           [os.path.join(ROOT, "include", "gemm_f32.h")])
+    return env
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -663,6 +690,7 @@ def run_gpu_arm(args):
             "clocks": clk, "headline_parity": headline_parity, "per_shape": per_shape, "floors": floors,
             "batched": batched,
             "peaks": pk, "device": dev_name,
+            "environment": run_environment(local),
             "library_sha256_16": source_hash([g.LIB_PATH]),
         }
         print(json.dumps(line), flush=True)
