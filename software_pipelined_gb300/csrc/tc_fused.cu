@@ -23,10 +23,14 @@
 // copied straight into the slot) and converts only A in the kernel: half the
 // pre-pass, and a quarter of the converters' shared-memory traffic.
 //
-// Shared memory: SLOTS MMA-facing slots [A_raw | lo_A | hi_B | lo_B] and RAWB
-// staging buffers for raw B.  Barriers per slot: full_a (A landed), conv
-// (converters done: hi/lo of A and B ready), empty (MMAs done); per raw-B
-// buffer: full_b (B landed), free_b (converters done reading it).
+// Shared memory: SLOTS MMA-facing slots [A_raw | lo_A | hi_B | lo_B].  Raw B
+// (32 x 32 boxes, N-major) lands in the lo_B part of its own slot: the
+// converters read it into registers, write hi_B beside it, agree that every
+// warp has read (the slot's `rd` barrier), then write lo_B over it.  So B's
+// copy recycles with the slot, as deep as the ring, instead of through
+// separate staging buffers.  Barriers per slot: full (A and raw B landed), rd
+// (every converter warp holds its raw B), conv (converters done: hi/lo of A
+// and B ready), empty (MMAs done).
 //
 // Roles (448 threads, one CTA per SM, persistent over units of work):
 //   warp 0      TMA producer           warp 1      TMEM allocator + MMA issuer
@@ -45,15 +49,15 @@ constexpr int kConvWarps = 8;                       // one per 4-wide k group of
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kFusedThreads = 6 * 32 + kConvThreads;
 
-template <int BN, int SLOTS, int RAWB>
+template <int BN, int SLOTS, bool BPRE>
 struct FusedLayout {
     static constexpr int A_BYTES = kBM * kBK * 4;          // 16 KB
-    static constexpr int B_BYTES = BN * kBK * 4;
+    static constexpr int B_BYTES = BN * kBK * 4;           // also raw B: BN/32 boxes of 32 k x 32 n
     static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-    static constexpr int RAWB_BYTES = B_BYTES;              // BN/32 boxes of 32 k x 32 n
-    static constexpr int RING_BYTES = SLOTS * SLOT_BYTES + RAWB * RAWB_BYTES;
-    // + tmem full/empty x2, drain, ready, recv, stg, sumd, fixup loads x4
-    static constexpr int NBARS = 3 * SLOTS + 2 * RAWB + 13;
+    static constexpr int RING_BYTES = SLOTS * SLOT_BYTES;
+    // full, rd, conv, empty per slot + tmem full/empty x2, drain, ready, recv,
+    // stg, sumd, fixup loads x4
+    static constexpr int NBARS = 4 * SLOTS + 13;
     static constexpr bool FIXUP_OK = kFixRingBytes <= RING_BYTES;
     // cluster K-slice sum: its staging and receive buffers laid over the idle ring
     static constexpr bool CLUSTER_OK = ClusterSum<BN>::BYTES <= RING_BYTES;
@@ -65,8 +69,8 @@ struct FusedLayout {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-template <int BN, int SLOTS, int RAWB>
-constexpr bool L_STAGING_FITS = FusedLayout<BN, SLOTS, RAWB>::RING_BYTES >= 4 * 8192;
+template <int BN, int SLOTS, bool BPRE>
+constexpr bool L_STAGING_FITS = FusedLayout<BN, SLOTS, BPRE>::RING_BYTES >= 4 * 8192;
 
 // Byte offset of element (row, k) in a K-major 128-byte-swizzled tile (rows of
 // 32 FP32 = 128 B, 8-row atoms of 1024 B, 16-byte chunk index XOR row % 8).
@@ -75,23 +79,21 @@ __device__ __forceinline__ uint32_t kmajor_off(int row, int kq)
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((kq ^ (row & 7)) << 4));
 }
 
-// RAWB == 0 is the hybrid form: B comes already split (hi/lo, K-major) from the
+// BPRE is the hybrid form: B comes already split (hi/lo, K-major) from the
 // pre-pass through tm_bhi/tm_blo, straight into the slot, and the converters
-// only add lo_A.  Otherwise tm_b copies raw B into the RAWB staging buffers.
-template <int BN, int SLOTS, int RAWB>
+// only add lo_A.  Otherwise tm_b copies raw B into the slot's lo_B part.
+template <int BN, int SLOTS, bool BPRE>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
                 const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
                 const TcArgs args)
 {
-    constexpr bool BPRE = RAWB == 0;
-    using L = FusedLayout<BN, SLOTS, RAWB>;
+    using L = FusedLayout<BN, SLOTS, BPRE>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t ring = (raw_addr + 1023u) & ~1023u;
     uint8_t* ring_ptr = smem_raw + (ring - raw_addr);
-    const uint32_t rawb0 = ring + SLOTS * L::SLOT_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + L::RING_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -101,16 +103,15 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     auto full_a = [&](int s) { return ptx::smem_u32(bars + s); };
     auto conv = [&](int s) { return ptx::smem_u32(bars + SLOTS + s); };
     auto empty = [&](int s) { return ptx::smem_u32(bars + 2 * SLOTS + s); };
-    auto full_b = [&](int r) { return ptx::smem_u32(bars + 3 * SLOTS + r); };
-    auto free_b = [&](int r) { return ptx::smem_u32(bars + 3 * SLOTS + RAWB + r); };
-    auto tfull = [&](int b) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + b); };
-    auto tempty = [&](int b) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 2 + b); };
-    const uint32_t drain_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 4);
-    const uint32_t ready_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 5);
-    const uint32_t recv_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 6);
-    const uint32_t stg_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 7);
-    const uint32_t sum_bar = ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 8);
-    auto fix_bar = [&](int q) { return ptx::smem_u32(bars + 3 * SLOTS + 2 * RAWB + 9 + q); };
+    auto rd = [&](int s) { return ptx::smem_u32(bars + 3 * SLOTS + s); };
+    auto tfull = [&](int b) { return ptx::smem_u32(bars + 4 * SLOTS + b); };
+    auto tempty = [&](int b) { return ptx::smem_u32(bars + 4 * SLOTS + 2 + b); };
+    const uint32_t drain_bar = ptx::smem_u32(bars + 4 * SLOTS + 4);
+    const uint32_t ready_bar = ptx::smem_u32(bars + 4 * SLOTS + 5);
+    const uint32_t recv_bar = ptx::smem_u32(bars + 4 * SLOTS + 6);
+    const uint32_t stg_bar = ptx::smem_u32(bars + 4 * SLOTS + 7);
+    const uint32_t sum_bar = ptx::smem_u32(bars + 4 * SLOTS + 8);
+    auto fix_bar = [&](int q) { return ptx::smem_u32(bars + 4 * SLOTS + 9 + q); };
     const bool clustered = L::CLUSTER_OK && args.cluster > 1;
     const bool fixup = L::FIXUP_OK && args.fixup && !clustered;
 
@@ -119,10 +120,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             ptx::mbar_init(full_a(s), 1);
             ptx::mbar_init(conv(s), kConvThreads / 32);
             ptx::mbar_init(empty(s), 1);
-        }
-        for (int r = 0; r < RAWB; ++r) {
-            ptx::mbar_init(full_b(r), 1);
-            ptx::mbar_init(free_b(r), kConvThreads / 32);
+            ptx::mbar_init(rd(s), kConvThreads / 32);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull(b), 1);
@@ -195,25 +193,19 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                         ptx::tma_load_2d(slot + 2 * L::A_BYTES, &tm_bhi, full_a(s), kc, tn * BN);
                         ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, full_a(s), kc, tn * BN);
                     } else {
-                        const int r = fills % RAWB;
-                        const uint32_t pr = (fills / RAWB) & 1u;
-                        if (!wait_phase(free_b(r), pr ^ 1u, limit, abort_flag, args.status)) {
-                            stop = true;
-                            break;
-                        }
                         ++fills;
                         if (fills == (uint32_t)args.withhold) continue;
-                        ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES);
+                        // raw A into the A part, raw B boxes into the lo_B part
+                        ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + L::B_BYTES);
                         ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, tm * kBM);
-                        ptx::mbar_arrive_expect_tx(full_b(r), L::RAWB_BYTES);
 #pragma unroll
                         for (int j = 0; j < BN / 32; ++j)
-                            ptx::tma_load_2d(rawb0 + r * L::RAWB_BYTES + j * 4096, &tm_b, full_b(r),
+                            ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES + j * 4096, &tm_b, full_a(s),
                                              tn * BN + 32 * j, kc);
                     }
                 }
             }
-            // Drain: the last fill of every slot and raw-B buffer must have landed.
+            // Drain: the last fill of every slot must have landed.
             const uint32_t total = fills;
             auto drain = [&](uint32_t bar_of_last, uint32_t last, int depth) {
                 if (last + 1 == (uint32_t)args.withhold) return;
@@ -224,9 +216,6 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             };
             for (int s = 0; s < SLOTS && (uint32_t)s < total; ++s)
                 drain(full_a(s), (total - 1 - s) / SLOTS * SLOTS + s, SLOTS);
-            if constexpr (!BPRE)
-                for (int r = 0; r < RAWB && (uint32_t)r < total; ++r)
-                    drain(full_b(r), (total - 1 - r) / RAWB * RAWB + r, RAWB);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -336,10 +325,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
                 const int s = fills % SLOTS;
                 const uint32_t ps = (fills / SLOTS) & 1u;
-                const int r = BPRE ? 0 : fills % (BPRE ? 1 : RAWB);
-                const uint32_t pr = BPRE ? 0u : (fills / (BPRE ? 1 : RAWB)) & 1u;
-                if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status) ||
-                    (!BPRE && !wait_phase(full_b(r), pr, limit, abort_flag, args.status))) {
+                if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
                     stop = true;
                     break;
                 }
@@ -347,8 +333,24 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 const uint8_t* a_raw = slot;
                 uint8_t* a_lo = slot + L::A_BYTES;
                 uint8_t* b_hi = slot + 2 * L::A_BYTES;
-                uint8_t* b_lo = b_hi + L::B_BYTES;
-                const uint8_t* b_raw = ring_ptr + SLOTS * L::SLOT_BYTES + r * L::RAWB_BYTES;
+                uint8_t* b_lo = b_hi + L::B_BYTES;  // holds raw B until every warp has read it
+                // B: this warp's raw values (k = 4*cw..4*cw+3, n = lane of every
+                // 32-column box) into registers; hi_B written at once.  The reads
+                // of a box row are conflict-free, and the 16-byte writes of 8
+                // consecutive rows land in 8 different swizzled chunks.
+                float v[BPRE ? 1 : BN / 32][4];
+                if constexpr (!BPRE) {
+#pragma unroll
+                    for (int nb = 0; nb < BN / 32; ++nb) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            v[nb][j] = *reinterpret_cast<const float*>(b_lo + nb * 4096 + box_off[j]);
+                        *reinterpret_cast<float4*>(b_hi + kmajor_off(nb * 32 + lane, cw)) =
+                            make_float4(v[nb][0], v[nb][1], v[nb][2], v[nb][3]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(rd(s));
+                }
                 // A: lo beside the raw tile, same swizzled position, 16 bytes at a time.
 #pragma unroll
                 for (int c = ct; c < L::A_BYTES / 16; c += kConvThreads) {
@@ -356,27 +358,21 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                     *reinterpret_cast<float4*>(a_lo + c * 16) =
                         make_float4(lo_part(x.x), lo_part(x.y), lo_part(x.z), lo_part(x.w));
                 }
-                // B: transpose 32-column boxes into K-major rows.  This warp owns
-                // k = 4*cw..4*cw+3; lane = n within a box: the reads of a box row
-                // are conflict-free, and the 16-byte writes of 8 consecutive rows
-                // land in 8 different swizzled chunks.
-#pragma unroll 2
-                for (int nb = 0; nb < (BPRE ? 0 : BN / 32); ++nb) {
-                    const uint8_t* box = b_raw + nb * 4096;
-                    float v[4];
+                if constexpr (!BPRE) {
+                    // every warp holds its raw B: lo_B may overwrite it
+                    if (!wait_phase(rd(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const float*>(box + box_off[j]);
-                    const uint32_t o = kmajor_off(nb * 32 + lane, cw);
-                    *reinterpret_cast<float4*>(b_hi + o) = make_float4(v[0], v[1], v[2], v[3]);
-                    *reinterpret_cast<float4*>(b_lo + o) =
-                        make_float4(lo_part(v[0]), lo_part(v[1]), lo_part(v[2]), lo_part(v[3]));
+                    for (int nb = 0; nb < BN / 32; ++nb)
+                        *reinterpret_cast<float4*>(b_lo + kmajor_off(nb * 32 + lane, cw)) =
+                            make_float4(lo_part(v[nb][0]), lo_part(v[nb][1]), lo_part(v[nb][2]),
+                                        lo_part(v[nb][3]));
                 }
                 ptx::fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
                 __syncwarp();
-                if (lane == 0) {
-                    if (!BPRE) ptx::mbar_arrive(free_b(r));
-                    ptx::mbar_arrive(conv(s));
-                }
+                if (lane == 0) ptx::mbar_arrive(conv(s));
             }
         }
     }
@@ -391,13 +387,13 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
 }
 
-template <int BN, int SLOTS, int RAWB>
+template <int BN, int SLOTS, bool BPRE>
 cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
 {
-    static_assert(L_STAGING_FITS<BN, SLOTS, RAWB>, "the ring holds the TMA-store staging");
-    using L = FusedLayout<BN, SLOTS, RAWB>;
-    auto kern = tc_fused_kernel<BN, SLOTS, RAWB>;
+    static_assert(L_STAGING_FITS<BN, SLOTS, BPRE>, "the ring holds the TMA-store staging");
+    using L = FusedLayout<BN, SLOTS, BPRE>;
+    auto kern = tc_fused_kernel<BN, SLOTS, BPRE>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
@@ -416,14 +412,14 @@ cudaError_t tc_fused_main(int bn, bool b_presplit, const TcPlanState& st, const 
 {
     if (b_presplit) {
         switch (bn) {
-        case 128: return launch_fused<128, 3, 0>(st, a, ta, tb, tbhi, tblo, s);
-        case 256: return launch_fused<256, 2, 0>(st, a, ta, tb, tbhi, tblo, s);
+        case 128: return launch_fused<128, 3, true>(st, a, ta, tb, tbhi, tblo, s);
+        case 256: return launch_fused<256, 2, true>(st, a, ta, tb, tbhi, tblo, s);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (bn) {
-    case 128: return launch_fused<128, 3, 2>(st, a, ta, tb, tbhi, tblo, s);
-    case 256: return launch_fused<256, 2, 1>(st, a, ta, tb, tbhi, tblo, s);
+    case 128: return launch_fused<128, 3, false>(st, a, ta, tb, tbhi, tblo, s);
+    case 256: return launch_fused<256, 2, false>(st, a, ta, tb, tbhi, tblo, s);
     default: return cudaErrorInvalidValue;
     }
 }
