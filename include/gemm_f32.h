@@ -114,8 +114,10 @@ typedef struct {
                                2, B) that is not 16-byte aligned */
     int32_t tile_group;     /* TC only: tile order of the persistent kernel, in tile-rows per
                                raster group (1..64; 0 = the dispatcher's choice, else 8) */
-    int32_t tile_k;         /* SIMT only: K-tile depth (16/32/64; 0 = the compiled default
-                               for the tile and stage count) */
+    int32_t tile_k;         /* K-tile depth.  SIMT: 16/32/64 (0 = the compiled default for the
+                               tile and stage count).  tcgen05: 32, or 16 for half-size,
+                               twice-as-deep stages of the in-kernel split (selects that
+                               form); 0 = the dispatcher's choice */
     int32_t host_panels;    /* TC only, gemm_f32_run_host: row panels the host-buffer run is
                                pipelined over (A panel copies, panel GEMMs and C panel
                                copies overlap); 0 = the dispatcher's choice, 1 = none,

@@ -281,16 +281,23 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // B by the pre-pass), 4 hi of A read from A; 0 = the dispatcher's choice.
             // A forced ring depth exists only in the pre-pass form (the other
             // forms have one depth per tile width), so it selects that form.
-            int where = o.operand_split ? o.operand_split - 1 : o.stages ? kSplitPrepass : c.fused;
+            // Half-size (16-k) stages exist only in the in-kernel form, so a
+            // forced tile_k of 16 selects that form.
+            int where = o.operand_split ? o.operand_split - 1
+                        : o.stages      ? kSplitPrepass
+                        : o.tile_k == 16 ? kSplitInKernel
+                                         : c.fused;
+            const int tc_bk = where == kSplitInKernel ? (o.tile_k ? o.tile_k : c.tile_k) : 0;
             const bool ok = where == kSplitPrepass ||
                             (K >= kTcFusedMinK && lda % 4 == 0 && (where != kSplitInKernel || ldb % 4 == 0) &&
-                             !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where) >= 0);
+                             !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where, tc_bk) >= 0);
             if (!ok) {
-                if (o.operand_split) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                if (o.operand_split || o.tile_k == 16) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
                 where = kSplitPrepass;
             }
+            if (o.tile_k && where != kSplitInKernel && o.tile_k != 32) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             t.config_id = tc_find_config(c.tile_n, where != kSplitPrepass ? 0 : c.stages, o.separate_syncs != 0,
-                                         where);
+                                         where, where == kSplitInKernel ? tc_bk : 0);
             if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             if (where != kSplitPrepass) t.fallback_config_id = tc_find_config(c.tile_n, 0, false, kSplitPrepass);
             const TcConfig& tcfg = tc_config(t.config_id);

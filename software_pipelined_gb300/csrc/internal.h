@@ -77,7 +77,7 @@ enum : int {
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);
-int tc_find_config(int bn, int stages, bool sep = false, int split = 0);
+int tc_find_config(int bn, int stages, bool sep, int split, int bk = 0);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
 // tensor maps that describe it, and the work decomposition.

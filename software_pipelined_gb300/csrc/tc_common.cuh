@@ -565,9 +565,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 }  // namespace tc
 
-// The in-kernel split kernel for tile width bn (tc_fused.cu); b_presplit: B
-// comes split by the pre-pass (tbhi/tblo) and only A is split in the kernel.
-cudaError_t tc_fused_main(int bn, bool b_presplit, const TcPlanState& st, const tc::TcArgs& a,
+// The in-kernel split kernel for tile width bn and stage depth bk (32 or 16;
+// tc_fused.cu); b_presplit: B comes split by the pre-pass (tbhi/tblo) and
+// only A is split in the kernel.
+cudaError_t tc_fused_main(int bn, int bk, bool b_presplit, const TcPlanState& st, const tc::TcArgs& a,
                           const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
                           const CUtensorMap& tblo, cudaStream_t s);
 

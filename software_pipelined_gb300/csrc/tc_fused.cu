@@ -49,10 +49,17 @@ constexpr int kConvWarps = 8;                       // one per 4-wide k group of
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kFusedThreads = 6 * 32 + kConvThreads;
 
-template <int BN, int SLOTS, bool BPRE>
+// KB: k per pipeline stage.  32 = one 128-byte swizzled row of FP32 per operand
+// row (the same layout as the pre-split operands); 16 = half-size stages in
+// the 64-byte swizzled layout, twice as many of them in the same shared memory.
+template <int BN, int SLOTS, bool BPRE, int KB>
 struct FusedLayout {
-    static constexpr int A_BYTES = kBM * kBK * 4;          // 16 KB
-    static constexpr int B_BYTES = BN * kBK * 4;           // also raw B: BN/32 boxes of 32 k x 32 n
+    static constexpr int A_BYTES = kBM * KB * 4;           // 16 KB (KB 32), 8 KB (KB 16)
+    static constexpr int B_BYTES = BN * KB * 4;            // also raw B: BN/32 boxes of KB k x 32 n
+    static constexpr int BOX_BYTES = 32 * KB * 4;          // one raw-B box
+    static_assert(KB == 32 || KB == 16, "stage depth");
+    static_assert(B_BYTES == BN / 32 * BOX_BYTES, "raw B fills the lo_B part exactly");
+    static_assert(!BPRE || KB == 32, "pre-split B comes in 32-k rows");
     static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RING_BYTES = SLOTS * SLOT_BYTES;
     // full, rd, conv, empty per slot + tmem full/empty x2, drain, ready, recv,
@@ -69,27 +76,49 @@ struct FusedLayout {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-template <int BN, int SLOTS, bool BPRE>
-constexpr bool L_STAGING_FITS = FusedLayout<BN, SLOTS, BPRE>::RING_BYTES >= 4 * 8192;
+template <int BN, int SLOTS, bool BPRE, int KB>
+constexpr bool L_STAGING_FITS = FusedLayout<BN, SLOTS, BPRE, KB>::RING_BYTES >= 4 * 8192;
 
-// Byte offset of element (row, k) in a K-major 128-byte-swizzled tile (rows of
-// 32 FP32 = 128 B, 8-row atoms of 1024 B, 16-byte chunk index XOR row % 8).
+// Byte offset of the 16-byte chunk kq of row `row` in a K-major swizzled tile:
+// KB 32: rows of 128 B in 8-row atoms of 1024 B, chunk index XOR row % 8;
+// KB 16: rows of 64 B in 8-row atoms of 512 B, chunk index XOR (row / 2) % 4
+// (the 64-byte swizzle: byte-address bits 4-5 XOR bits 7-8).
+template <int KB>
 __device__ __forceinline__ uint32_t kmajor_off(int row, int kq)
 {
-    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((kq ^ (row & 7)) << 4));
+    if constexpr (KB == 32)
+        return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((kq ^ (row & 7)) << 4));
+    else
+        return (uint32_t)((row >> 3) * 512 + (row & 7) * 64 + ((kq ^ ((row >> 1) & 3)) << 4));
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the layout above.
+template <int KB>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr)
+{
+    if constexpr (KB == 32) {
+        return sw128_desc(saddr);
+    } else {
+        return (uint64_t)((saddr & 0x3FFFFu) >> 4)
+             | ((uint64_t)1 << 16)                  // leading byte offset (unused)
+             | ((uint64_t)(512 >> 4) << 32)         // stride byte offset: 8 rows of 64 B
+             | ((uint64_t)1 << 46)                  // descriptor version (tcgen05)
+             | ((uint64_t)4 << 61);                 // swizzle: 64 B
+    }
 }
 
 // BPRE is the hybrid form: B comes already split (hi/lo, K-major) from the
 // pre-pass through tm_bhi/tm_blo, straight into the slot, and the converters
 // only add lo_A.  Otherwise tm_b copies raw B into the slot's lo_B part.
-template <int BN, int SLOTS, bool BPRE>
+template <int BN, int SLOTS, bool BPRE, int KB>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
                 const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
                 const TcArgs args)
 {
-    using L = FusedLayout<BN, SLOTS, BPRE>;
+    using L = FusedLayout<BN, SLOTS, BPRE, KB>;
+    constexpr int HALVES = kBK / KB;  // stages per 32-k block of the work decomposition
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t ring = (raw_addr + 1023u) & ~1023u;
@@ -176,14 +205,14 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 const Unit u = decode_unit(w, args);
                 int tm, tn;
                 tile_coords(u.tile, args.tiles_m, args.tiles_n, args.group, tm, tn);
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh) {
                     const int s = fills % SLOTS;
                     const uint32_t ps = (fills / SLOTS) & 1u;
                     if (!wait_phase(empty(s), ps ^ 1u, limit, abort_flag, args.status)) {
                         stop = true;
                         break;
                     }
-                    const int kc = kb * kBK;
+                    const int kc = kh * KB;
                     const uint32_t slot = ring + s * L::SLOT_BYTES;
                     if constexpr (BPRE) {
                         ++fills;
@@ -200,8 +229,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                         ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, tm * kBM);
 #pragma unroll
                         for (int j = 0; j < BN / 32; ++j)
-                            ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES + j * 4096, &tm_b, full_a(s),
-                                             tn * BN + 32 * j, kc);
+                            ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES + j * L::BOX_BYTES, &tm_b,
+                                             full_a(s), tn * BN + 32 * j, kc);
                     }
                 }
             }
@@ -232,7 +261,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 if (!wait_phase(tempty(buf), tphase ^ 1u, limit, abort_flag, args.status)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+                for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
                     const int s = fills % SLOTS;
                     const uint32_t ps = (fills / SLOTS) & 1u;
                     if (!wait_phase(conv(s), ps, limit, abort_flag, args.status)) {
@@ -243,15 +272,15 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                     const uint32_t a_hi = ring + s * L::SLOT_BYTES, a_lo = a_hi + L::A_BYTES;
                     const uint32_t b_hi = a_hi + 2 * L::A_BYTES, b_lo = b_hi + L::B_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
+                    for (int ks = 0; ks < KB / kUmmaK; ++ks) {
                         const uint32_t off = ks * kUmmaK * 4;
-                        const uint32_t acc = (kb > u.kb0 || ks > 0) ? 1u : 0u;
+                        const uint32_t acc = (kh > u.kb0 * HALVES || ks > 0) ? 1u : 0u;
                         if (args.terms == 3) {
-                            ptx::mma_tf32(d_tmem, sw128_desc(a_lo + off), sw128_desc(b_hi + off), idesc, acc);
-                            ptx::mma_tf32(d_tmem, sw128_desc(a_hi + off), sw128_desc(b_lo + off), idesc, 1u);
-                            ptx::mma_tf32(d_tmem, sw128_desc(a_hi + off), sw128_desc(b_hi + off), idesc, 1u);
+                            ptx::mma_tf32(d_tmem, kmajor_desc<KB>(a_lo + off), kmajor_desc<KB>(b_hi + off), idesc, acc);
+                            ptx::mma_tf32(d_tmem, kmajor_desc<KB>(a_hi + off), kmajor_desc<KB>(b_lo + off), idesc, 1u);
+                            ptx::mma_tf32(d_tmem, kmajor_desc<KB>(a_hi + off), kmajor_desc<KB>(b_hi + off), idesc, 1u);
                         } else {
-                            ptx::mma_tf32(d_tmem, sw128_desc(a_hi + off), sw128_desc(b_hi + off), idesc, acc);
+                            ptx::mma_tf32(d_tmem, kmajor_desc<KB>(a_hi + off), kmajor_desc<KB>(b_hi + off), idesc, acc);
                         }
                     }
                     ptx::mma_commit(empty(s));
@@ -309,11 +338,14 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     } else {
         // ------------------------------ converters ----------------------------
         const int ct = threadIdx.x - 6 * 32;  // 0 .. kConvThreads-1
-        const int cw = ct >> 5;               // k group of this warp: k = 4*cw .. 4*cw+3
+        constexpr int KG = KB / 4;            // 4-wide k groups per stage
+        constexpr int PARTS = kConvWarps / KG;  // warps per k group: they share the boxes
+        const int cw = (ct >> 5) % KG;        // k group of this warp: k = 4*cw .. 4*cw+3
+        const int part = (ct >> 5) / KG;      // boxes part, part + PARTS, ...
         uint32_t fills = 0;
         bool stop = false;
-        // Offsets inside a raw-B box of the four k rows this lane reads (row k,
-        // chunk (lane/4) ^ (k%8), word lane%4): fixed for the whole kernel.
+        // Offsets inside a raw-B box (rows of 32 n, 128-byte swizzled) of the four
+        // k rows this lane reads (row k, chunk (lane/4) ^ (k%8), word lane%4).
         uint32_t box_off[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -322,7 +354,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         }
         for (int w = blockIdx.x; w < num_work && !stop; w += gridDim.x) {
             const Unit u = decode_unit(w, args);
-            for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+            for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
                 const int s = fills % SLOTS;
                 const uint32_t ps = (fills / SLOTS) & 1u;
                 if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
@@ -334,19 +366,21 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 uint8_t* a_lo = slot + L::A_BYTES;
                 uint8_t* b_hi = slot + 2 * L::A_BYTES;
                 uint8_t* b_lo = b_hi + L::B_BYTES;  // holds raw B until every warp has read it
-                // B: this warp's raw values (k = 4*cw..4*cw+3, n = lane of every
-                // 32-column box) into registers; hi_B written at once.  The reads
-                // of a box row are conflict-free, and the 16-byte writes of 8
-                // consecutive rows land in 8 different swizzled chunks.
-                float v[BPRE ? 1 : BN / 32][4];
+                // B: this warp's raw values (k = 4*cw..4*cw+3, n = lane of its
+                // 32-column boxes) into registers; hi_B written at once.  The
+                // reads of a box row are conflict-free, and the 16-byte writes of
+                // 8 consecutive rows land in 8 different swizzled chunks.
+                constexpr int NBW = BPRE ? 1 : BN / 32 / PARTS;  // boxes per warp
+                float v[NBW][4];
                 if constexpr (!BPRE) {
 #pragma unroll
-                    for (int nb = 0; nb < BN / 32; ++nb) {
+                    for (int i = 0; i < NBW; ++i) {
+                        const int nb = part + i * PARTS;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            v[nb][j] = *reinterpret_cast<const float*>(b_lo + nb * 4096 + box_off[j]);
-                        *reinterpret_cast<float4*>(b_hi + kmajor_off(nb * 32 + lane, cw)) =
-                            make_float4(v[nb][0], v[nb][1], v[nb][2], v[nb][3]);
+                            v[i][j] = *reinterpret_cast<const float*>(b_lo + nb * L::BOX_BYTES + box_off[j]);
+                        *reinterpret_cast<float4*>(b_hi + kmajor_off<KB>(nb * 32 + lane, cw)) =
+                            make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
                     }
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(rd(s));
@@ -365,10 +399,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                         break;
                     }
 #pragma unroll
-                    for (int nb = 0; nb < BN / 32; ++nb)
-                        *reinterpret_cast<float4*>(b_lo + kmajor_off(nb * 32 + lane, cw)) =
-                            make_float4(lo_part(v[nb][0]), lo_part(v[nb][1]), lo_part(v[nb][2]),
-                                        lo_part(v[nb][3]));
+                    for (int i = 0; i < NBW; ++i)
+                        *reinterpret_cast<float4*>(b_lo + kmajor_off<KB>((part + i * PARTS) * 32 + lane, cw)) =
+                            make_float4(lo_part(v[i][0]), lo_part(v[i][1]), lo_part(v[i][2]), lo_part(v[i][3]));
                 }
                 ptx::fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
                 __syncwarp();
@@ -387,13 +420,13 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
 }
 
-template <int BN, int SLOTS, bool BPRE>
+template <int BN, int SLOTS, bool BPRE, int KB>
 cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
 {
-    static_assert(L_STAGING_FITS<BN, SLOTS, BPRE>, "the ring holds the TMA-store staging");
-    using L = FusedLayout<BN, SLOTS, BPRE>;
-    auto kern = tc_fused_kernel<BN, SLOTS, BPRE>;
+    static_assert(L_STAGING_FITS<BN, SLOTS, BPRE, KB>, "the ring holds the TMA-store staging");
+    using L = FusedLayout<BN, SLOTS, BPRE, KB>;
+    auto kern = tc_fused_kernel<BN, SLOTS, BPRE, KB>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
@@ -406,20 +439,27 @@ cudaError_t launch_fused(const TcPlanState& st, const TcArgs& a, const CUtensorM
 
 }  // namespace
 
-cudaError_t tc_fused_main(int bn, bool b_presplit, const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
-                          const CUtensorMap& tb, const CUtensorMap& tbhi, const CUtensorMap& tblo,
-                          cudaStream_t s)
+cudaError_t tc_fused_main(int bn, int bk, bool b_presplit, const TcPlanState& st, const TcArgs& a,
+                          const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
+                          const CUtensorMap& tblo, cudaStream_t s)
 {
     if (b_presplit) {
         switch (bn) {
-        case 128: return launch_fused<128, 3, true>(st, a, ta, tb, tbhi, tblo, s);
-        case 256: return launch_fused<256, 2, true>(st, a, ta, tb, tbhi, tblo, s);
+        case 128: return launch_fused<128, 3, true, 32>(st, a, ta, tb, tbhi, tblo, s);
+        case 256: return launch_fused<256, 2, true, 32>(st, a, ta, tb, tbhi, tblo, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    if (bk == 16) {
+        switch (bn) {
+        case 128: return launch_fused<128, 6, false, 16>(st, a, ta, tb, tbhi, tblo, s);
+        case 256: return launch_fused<256, 4, false, 16>(st, a, ta, tb, tbhi, tblo, s);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (bn) {
-    case 128: return launch_fused<128, 3, false>(st, a, ta, tb, tbhi, tblo, s);
-    case 256: return launch_fused<256, 2, false>(st, a, ta, tb, tbhi, tblo, s);
+    case 128: return launch_fused<128, 3, false, 32>(st, a, ta, tb, tbhi, tblo, s);
+    case 256: return launch_fused<256, 2, false, 32>(st, a, ta, tb, tbhi, tblo, s);
     default: return cudaErrorInvalidValue;
     }
 }

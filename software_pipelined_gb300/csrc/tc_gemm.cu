@@ -81,28 +81,29 @@ int grid_cap(int64_t work, int sms)
 // Tensor maps over the caller's raw operands for the in-kernel split: A (M x K,
 // lda) as K-major boxes {32, 128}; B (K x N, ldb) as boxes of 32 columns x 32
 // rows.  Both 128-byte swizzled with zero fill; need 16-byte aligned rows.
-cudaError_t encode_raw_a(void* out, const float* A, int64_t M, int64_t K, int64_t lda)
+cudaError_t encode_raw_a(void* out, const float* A, int64_t M, int64_t K, int64_t lda, int box_k)
 {
     EncodeFn enc = get_encode();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)(lda * 4)};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)kBM};
     cuuint32_t estr[2] = {1, 1};
+    // rows of 32 FP32 in the 128-byte swizzle, of 16 in the 64-byte one
     CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                      const_cast<float*>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     box_k == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t encode_raw_b(void* out, const float* B, int64_t K, int64_t N, int64_t ldb)
+cudaError_t encode_raw_b(void* out, const float* B, int64_t K, int64_t N, int64_t ldb, int box_k)
 {
     EncodeFn enc = get_encode();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
     cuuint64_t strides[1] = {(cuuint64_t)(ldb * 4)};
-    cuuint32_t box[2] = {32, (cuuint32_t)kBK};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_k};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                      const_cast<float*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -171,6 +172,9 @@ const TcEntry kTc[] = {
     // ring of 128 x 256 tiles not the 256 KB those would need)
     {{128, 128, 32, 3, false, kSplitInKernel}, nullptr, launch_reduce<128>, true, true},
     {{128, 256, 32, 2, false, kSplitInKernel}, nullptr, launch_reduce<256>, false, true},
+    // the same with half-size (16-k) stages, twice as deep: 6 x 32 KB, 4 x 48 KB
+    {{128, 128, 16, 6, false, kSplitInKernel}, nullptr, launch_reduce<128>, true, true},
+    {{128, 256, 16, 4, false, kSplitInKernel}, nullptr, launch_reduce<256>, false, true},
     // A split inside the kernel, B by the pre-pass
     {{128, 128, 32, 3, false, kSplitHybrid}, nullptr, launch_reduce<128>, true, true},
     {{128, 256, 32, 2, false, kSplitHybrid}, nullptr, launch_reduce<256>, false, true},
@@ -183,18 +187,14 @@ const TcEntry kTc[] = {
 
 int tc_num_configs() { return (int)(sizeof(kTc) / sizeof(kTc[0])); }
 const TcConfig& tc_config(int id) { return kTc[id].cfg; }
-int tc_find_config(int bn, int stages, bool sep, int split)
+int tc_find_config(int bn, int stages, bool sep, int split, int bk)
 {
     for (int i = 0; i < tc_num_configs(); ++i) {
         const TcConfig& c = kTc[i].cfg;
-        if (c.bn == bn && c.stages == stages && c.sep == sep && c.split == split) return i;
+        if (c.bn == bn && (stages == 0 || c.stages == stages) && c.sep == sep && c.split == split &&
+            (bk == 0 || c.bk == bk))
+            return i;
     }
-    // Stage count 0: the first (deepest) ring compiled for this tile width.
-    if (stages == 0)
-        for (int i = 0; i < tc_num_configs(); ++i) {
-            const TcConfig& c = kTc[i].cfg;
-            if (c.bn == bn && c.sep == sep && c.split == split) return i;
-        }
     return -1;
 }
 
@@ -375,7 +375,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
     if (r.in_kernel) {
-        e = tc_fused_main(c.bn, c.split == kSplitHybrid, st, a,
+        e = tc_fused_main(c.bn, c.bk, c.split == kSplitHybrid, st, a,
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw),
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
@@ -402,11 +402,11 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
     if (ev) cudaEventRecord(ev[0], s);
     // Tensor maps over the caller's raw operands, re-encoded when they move.
     if ((r.raw_a || r.in_kernel) && A != st.raw_a) {
-        if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda)) != cudaSuccess) return e;
+        if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda, c.bk)) != cudaSuccess) return e;
         st.raw_a = A;
     }
     if (r.in_kernel && c.split == kSplitInKernel && B != st.raw_b) {
-        if ((e = encode_raw_b(st.tmap_b_raw, B, K, N, ldb)) != cudaSuccess) return e;
+        if ((e = encode_raw_b(st.tmap_b_raw, B, K, N, ldb, c.bk)) != cudaSuccess) return e;
         st.raw_b = B;
     }
     // 1. The pre-pass into the plan's scratch (what the route needs of it).
@@ -433,11 +433,11 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     if ((e = encode_kmajor(out.tmap_a_lo, out.a_lo, mp, out.kp, kBM)) != cudaSuccess) return e;
     const Route r = route(out, A + r0 * lda, B);
     if (r.raw_a || r.in_kernel) {
-        if ((e = encode_raw_a(out.tmap_a_raw, A + r0 * lda, mp, K, lda)) != cudaSuccess) return e;
+        if ((e = encode_raw_a(out.tmap_a_raw, A + r0 * lda, mp, K, lda, c.bk)) != cudaSuccess) return e;
         out.raw_a = A + r0 * lda;
     }
     if (r.in_kernel && c.split == kSplitInKernel) {
-        if ((e = encode_raw_b(out.tmap_b_raw, B, K, N, ldb)) != cudaSuccess) return e;
+        if ((e = encode_raw_b(out.tmap_b_raw, B, K, N, ldb, c.bk)) != cudaSuccess) return e;
         out.raw_b = B;
     }
     return cudaSuccess;

@@ -82,10 +82,11 @@ def candidates(M, N, K):
     if K >= 16:
         for bn in TC_BN:
             for fused in ((1, 2, 3, 4) if bn in (128, 256) and K >= 32 else (1,)):
-                for sp in [0] + SPLITS:
-                    if sp <= 1 or (K + 31) // 32 >= sp:
-                        out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp,
-                                        operand_split=fused))
+                for tk in ((0, 16) if fused == 2 else (0,)):
+                    for sp in [0] + SPLITS:
+                        if sp <= 1 or (K + 31) // 32 >= sp:
+                            out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, stages=0, split_k=sp,
+                                            operand_split=fused, tile_k=tk))
     return out
 
 

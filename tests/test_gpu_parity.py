@@ -328,10 +328,12 @@ def test_large_squares_sampled(w):
 # ---------------------------------------------------------------------------
 
 FUSED = {"variant": g.VARIANT_TCGEN05, "operand_split": 2}
+FUSED16 = {"variant": g.VARIANT_TCGEN05, "operand_split": 2, "tile_k": 16}
 HYBRID = {"variant": g.VARIANT_TCGEN05, "operand_split": 3}
 RAWA = {"variant": g.VARIANT_TCGEN05, "operand_split": 4}
-MODES = [(FUSED, "in-kernel-split"), (HYBRID, "hybrid-split"), (RAWA, "raw-a-split")]
-MODE_IDS = ["in_kernel", "hybrid", "raw_a"]
+MODES = [(FUSED, "in-kernel-split"), (FUSED16, "in-kernel-split"), (HYBRID, "hybrid-split"),
+         (RAWA, "raw-a-split")]
+MODE_IDS = ["in_kernel", "in_kernel_k16", "hybrid", "raw_a"]
 
 
 @pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
@@ -345,9 +347,10 @@ def test_in_kernel_split_configs(bn, split, mode):
     A = inputs.uniform_pm1(1601, M, K)
     B = inputs.normal(1602, K, N)
     # B's rows must be 16-byte aligned for the TMA copy of raw B: pad ldb
-    ldb = N + (-N % 4) if opts is FUSED else N
+    ldb = N + (-N % 4) if opts in (FUSED, FUSED16) else N
     C, desc, canaries, outs = run_gemm(A, B, repeat=2, tile_n=bn, split_k=split, ldb=ldb, **opts)
     assert tag in desc, desc
+    assert (f"tile=128x{bn}x16" in desc) == (opts is FUSED16), desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
     assert np.array_equal(outs[0], outs[1]), desc
