@@ -674,6 +674,43 @@ def test_run_host_panel_option_validation():
 
 
 # ---------------------------------------------------------------------------
+# Non-finite inputs: an Inf in A makes its row of C non-finite, a NaN in B its
+# column (the 3xTF32 split turns Inf into NaN, so only non-finiteness is
+# asserted); every other element stays finite and within the bound - nothing
+# leaks across tiles, K-slices or the operand split.
+# ---------------------------------------------------------------------------
+
+NONFINITE_VARIANTS = [SIMT, TC, {"variant": g.VARIANT_TCGEN05, "operand_split": 2},
+                      {"variant": g.VARIANT_TCGEN05, "operand_split": 2, "tile_k": 16},
+                      {"variant": g.VARIANT_TCGEN05, "operand_split": 3},
+                      {"variant": g.VARIANT_TCGEN05, "operand_split": 4},
+                      {"variant": g.VARIANT_TCGEN05, "split_k": 4}]
+
+
+@pytest.mark.parametrize("variant", NONFINITE_VARIANTS,
+                         ids=["simt", "tcgen05", "in_kernel", "in_kernel_k16", "hybrid", "raw_a", "split4"])
+def test_non_finite_inputs(variant):
+    M, N, K = 300, 260, 100
+    A = inputs.uniform_pm1(1751, M, K)
+    B = inputs.uniform_pm1(1752, K, N)
+    A[5, 17] = np.inf
+    B[33, 200] = np.nan
+    C, desc, canaries, _ = run_gemm(A, B, **variant)
+    assert canaries, desc
+    assert not np.isfinite(C[5, :]).any(), desc
+    assert not np.isfinite(C[:, 200]).any(), desc
+    rest = np.ones((M, N), dtype=bool)
+    rest[5, :] = False
+    rest[:, 200] = False
+    assert np.isfinite(C[rest]).all(), desc
+    A0, B0 = A.copy(), B.copy()
+    A0[5, 17] = 0.0
+    B0[33, 200] = 0.0
+    Cref, S = oracle.gemm_f64(A0, B0)
+    assert oracle.within_bound(C[rest], Cref[rest], S[rest], K), desc
+
+
+# ---------------------------------------------------------------------------
 # Extreme aspect ratios: a very long K (many k-blocks per tile, long
 # accumulation) and a very tall, thin product.
 # ---------------------------------------------------------------------------
