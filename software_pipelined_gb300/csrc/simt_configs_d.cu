@@ -16,6 +16,13 @@ extern const SimtEntry kSimtPartD[] = {
     {{32, 32, 32, 4, 4, 2, false, 4}, launch_cfg<32, 32, 32, 4, 4, 2, false, 4>},
     {{32, 64, 32, 4, 4, 2, false, 2}, launch_cfg<32, 64, 32, 4, 4, 2, false, 2>},
     {{64, 32, 32, 4, 4, 2, false, 2}, launch_cfg<64, 32, 32, 4, 4, 2, false, 2>},
+    // deeper rings: a small tile's FFMAs per K-tile are too few to cover a copy
+    {{32, 32, 32, 4, 4, 3, false, 4}, launch_cfg<32, 32, 32, 4, 4, 3, false, 4>},
+    {{32, 32, 32, 4, 4, 4, false, 4}, launch_cfg<32, 32, 32, 4, 4, 4, false, 4>},
+    {{32, 32, 64, 4, 4, 3, false, 4}, launch_cfg<32, 32, 64, 4, 4, 3, false, 4>},
+    {{64, 64, 16, 4, 4, 4, false, 2}, launch_cfg<64, 64, 16, 4, 4, 4, false, 2>},
+    {{32, 64, 32, 4, 4, 3, false, 2}, launch_cfg<32, 64, 32, 4, 4, 3, false, 2>},
+    {{64, 32, 32, 4, 4, 3, false, 2}, launch_cfg<64, 32, 32, 4, 4, 3, false, 2>},
 };
 extern const int kSimtPartDCount = (int)(sizeof(kSimtPartD) / sizeof(kSimtPartD[0]));
 

@@ -209,7 +209,8 @@ def test_every_simt_config(cfg, aligned):
 # K split inside the CTA: (tile_m, tile_n, stages, tile_k, k_slices)
 SIMT_KSL_CFGS = [(64, 64, 3, 16, 2), (64, 64, 2, 16, 2), (64, 64, 2, 32, 2), (64, 64, 2, 32, 4),
                  (32, 32, 1, 64, 4), (32, 32, 2, 64, 4), (32, 32, 2, 32, 2), (32, 32, 2, 32, 4),
-                 (32, 64, 2, 32, 2), (64, 32, 2, 32, 2)]
+                 (32, 64, 2, 32, 2), (64, 32, 2, 32, 2), (32, 32, 3, 32, 4), (32, 32, 4, 32, 4),
+                 (32, 32, 3, 64, 4), (64, 64, 4, 16, 2), (32, 64, 3, 32, 2), (64, 32, 3, 32, 2)]
 
 
 @pytest.mark.parametrize("shape", [(512, 512, 512), (1024, 1024, 1024), (4096, 4096, 4096)])
