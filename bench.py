@@ -330,9 +330,11 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel_src_hash):
+def traffic_for(kernel_src_hash, plans):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, only if it was taken on the current kernel source."""
+    summary, for each shape whose plan (its description: tile, operand split,
+    stages, K-slices, tile order) and kernel sources are those the capture was
+    taken on; plans: {shape name: plan description}."""
     path = os.path.join(ROOT, "profiles", "tcgen05_main_dram_traffic.txt")
     try:
         with open(path) as f:
@@ -342,11 +344,14 @@ def traffic_for(kernel_src_hash):
     kv = dict(l.split("=", 1) for l in lines if "=" in l)
     if kv.get("kernel_source_sha256_16") != kernel_src_hash:
         return None, "kernel changed since the ncu capture"
-    try:
-        return {k[len("bytes_per_launch_"):]: float(v) for k, v in kv.items()
-                if k.startswith("bytes_per_launch_")}, "ncu"
-    except ValueError:
-        return None, "unreadable ncu summary"
+    out = {}
+    for name, desc in plans.items():
+        if kv.get("plan_" + name) == desc and "bytes_per_launch_" + name in kv:
+            try:
+                out[name] = float(kv["bytes_per_launch_" + name])
+            except ValueError:
+                return None, "unreadable ncu summary"
+    return (out, "ncu") if out else (None, "plan changed since the ncu capture")
 
 
 def run_gpu_arm(args):
@@ -443,8 +448,8 @@ def run_gpu_arm(args):
     simt_main = big["plan"].describe().startswith("simt")
     peak = pk["f32_simt_tflops_nominal"] if simt_main else pk["f32_3xtf32_tflops_burst"]
     kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", f)
-                             for f in ("tc_kernels.cuh", "tc_common.cuh", "ptx.cuh", "dispatch_table.inc")])
-    traffic, traffic_src = traffic_for(kern_hash)
+                             for f in ("tc_kernels.cuh", "tc_common.cuh", "ptx.cuh")])
+    traffic, traffic_src = traffic_for(kern_hash, {w["name"]: w["plan"].describe() for w in work})
     for w in work:
         t = traffic.get(w["name"]) if traffic else None
         per_kernel[w["name"]]["dram_bytes_per_launch"] = t

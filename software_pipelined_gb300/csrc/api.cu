@@ -325,7 +325,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 bytes += align256(t.sem_bytes);
             }
             snprintf(p->desc, sizeof p->desc,
-                     "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d%s kp=%lld",
+                     "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d%s group=%d "
+                     "kp=%lld",
                      tcfg.split == kSplitInKernel ? " in-kernel-split"
                      : tcfg.split == kSplitHybrid ? " hybrid-split"
                      : tcfg.split == kSplitRawA ? " raw-a-split" : "",
@@ -333,7 +334,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                      tcfg.sep ? " separate-syncs" : "",
                      t.tiles_m * t.tiles_n, t.dp_tiles,
                      t.split_tiles, t.splits, t.cluster ? " cluster-sum" : t.fixup ? " last-arriver-sum" : "",
-                     (long long)t.kp);
+                     t.tile_group > 0 ? t.tile_group : 8, (long long)t.kp);
         }
     }
 
