@@ -534,7 +534,46 @@ __device__ bool cluster_reduce_store(const TcArgs& args, const CUtensorMap* tm_c
     return true;
 }
 
-// Launch with programmatic stream serialisation: the kernel may start while
+// The epilogue barriers of one warp: the cluster sum's (ready, recv, stg,
+// sumd) and this warp's last-arriver load barrier.
+struct EpilogueBars {
+    uint32_t ready, recv, stg, sumd, fix;
+};
+
+// Drain one accumulator buffer of TMEM (this warp's quadrant of the tile) by
+// the unit's way out: the cluster K-slice sum, the last-arriver sum of a split
+// unit, TMA stores through the idle ring for a CTA's last unit (RING bytes of
+// it; a box per 32 columns per warp where they fit), or direct stores.
+// false = a bounded wait gave up.
+template <int BN, int RING>
+__device__ __forceinline__ bool drain_unit(const TcArgs& args, const CUtensorMap* tm_c, const CUtensorMap* tm_p,
+                                           const Unit& u, int tm, int tn, uint32_t taddr, int quad, int lane,
+                                           bool last_unit, bool clustered, bool fixup, uint32_t ring,
+                                           uint8_t* ring_ptr, const EpilogueBars& eb, int64_t limit,
+                                           volatile int* abort_flag)
+{
+    if (clustered)
+        return cluster_reduce_store<BN>(args, tm_c, tm, tn, taddr, quad, lane, ring, ring_ptr, eb.ready, eb.recv,
+                                        eb.stg, eb.sumd, limit, abort_flag);
+    if (fixup && u.slot >= 0 && last_unit)
+        return fixup_store<BN>(args, tm_p, tm_c, u, tm, tn, taddr, quad, lane, ring + quad * kFixWarpBytes,
+                               ring_ptr + quad * kFixWarpBytes, eb.fix, limit, abort_flag);
+    if (last_unit && (u.slot >= 0 || args.c_tma)) {
+        constexpr int NBUF = RING / (4 * 4096) < BN / 32 ? RING / (4 * 4096) : BN / 32;
+        const uint32_t stg = (uint32_t)(quad * NBUF * 4096);
+        if (u.slot < 0)
+            store_accumulator_tma<BN, NBUF>(tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N, args.M,
+                                            taddr, lane, ring + stg, ring_ptr + stg);
+        else
+            store_accumulator_tma<BN, NBUF>(tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX, taddr, lane,
+                                            ring + stg, ring_ptr + stg);
+        return true;
+    }
+    store_accumulator<BN>(args, u, tm, tn, taddr, quad * 32 + lane);
+    return true;
+}
+
+// Launch with programmatic stream serialisation// Launch with programmatic stream serialisation: the kernel may start while
 // the previous kernel on the stream finishes, and waits for it (griddepcontrol)
 // before touching that kernel's output.  cluster > 1: thread-block clusters of
 // that many consecutive CTAs (the grid is a multiple of it).

@@ -370,7 +370,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
     } else {
         // ------------------------------ epilogue ------------------------------
         const int quad = warp & 3;              // TMEM lane quadrant this warp may access
-        const int row_in_tile = quad * 32 + lane;
         int iter = 0;
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++iter) {
             const Unit u = decode_unit(w, args);
@@ -381,29 +380,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
             if (!wait_phase(tfull_bar(buf), tphase, limit, abort_flag, args.status)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
-            if (clustered) {
-                if (!cluster_reduce_store<BN>(args, &tm_c, tm, tn, taddr, quad, lane, ring, ring_ptr, ready_bar,
-                                              recv_bar, stg_bar, sum_bar, limit, abort_flag))
-                    break;
-            } else if (fixup && u.slot >= 0 && w + (int)gridDim.x >= num_work) {
-                // a split unit (always its CTA's last): sum the tile's slices if last to arrive
-                if (!fixup_store<BN>(args, &tm_p, &tm_c, u, tm, tn, taddr, quad, lane, ring + quad * kFixWarpBytes,
-                                     ring_ptr + quad * kFixWarpBytes, fix_bar(quad), limit, abort_flag))
-                    break;
-            } else if (w + (int)gridDim.x >= num_work && (u.slot >= 0 || args.c_tma)) {
-                // this CTA's last unit: the ring is idle, stage and store by TMA
-                // staging: a box per 32 columns where the ring holds them, per warp
-                constexpr int NBUF = L::RING_BYTES / (4 * 4096) < BN / 32 ? L::RING_BYTES / (4 * 4096) : BN / 32;
-                const uint32_t stg = (uint32_t)(quad * NBUF * 4096);
-                if (u.slot < 0)
-                    store_accumulator_tma<BN, NBUF>(&tm_c, (int64_t)tn * BN, (int64_t)tm * kBM + quad * 32, args.N,
-                                                    args.M, taddr, lane, ring + stg, ring_ptr + stg);
-                else
-                    store_accumulator_tma<BN, NBUF>(&tm_p, 0, (int64_t)u.slot * kBM + quad * 32, BN, INT64_MAX,
-                                                    taddr, lane, ring + stg, ring_ptr + stg);
-            } else {
-                store_accumulator<BN>(args, u, tm, tn, taddr, row_in_tile);
-            }
+            const EpilogueBars eb{ready_bar, recv_bar, stg_bar, sum_bar, fix_bar(quad)};
+            if (!drain_unit<BN, L::RING_BYTES>(args, &tm_c, &tm_p, u, tm, tn, taddr, quad, lane,
+                                               w + (int)gridDim.x >= num_work, clustered, fixup, ring, ring_ptr, eb,
+                                               limit, abort_flag))
+                break;
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
