@@ -713,6 +713,13 @@ def run_gpu_arm(args):
 # Reference arm: the CPU oracle on the same workload.
 # ---------------------------------------------------------------------------
 
+def workload_label(workload):
+    """What a workload is, with its sizes."""
+    shapes = " + ".join(w[0] for w in shapes_of(workload))
+    return ("large squares: " if workload == HEADLINE else workload.replace("_", " ") + ": ") + \
+        f"{shapes} FP32 GEMM, row-major"
+
+
 def run_reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -741,8 +748,7 @@ def run_reference_arm(args):
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64, uniform[-1,1))",
-            "config": {"workload": "large squares: 4096x4096x4096 + 8192x8192x8192 FP32 GEMM, row-major",
-                       "sample": sample},
+            "config": {"workload": workload_label(args.workload), "sample": sample},
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -283,23 +283,40 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // forms have one depth per tile width), so it selects that form.
             // Half-size (16-k) stages exist only in the in-kernel form, so a
             // forced tile_k of 16 selects that form.
-            int where = o.operand_split ? o.operand_split - 1
-                        : o.stages      ? kSplitPrepass
-                        : o.tile_k == 16 ? kSplitInKernel
-                                         : c.fused;
-            const int tc_bk = where == kSplitInKernel ? (o.tile_k ? o.tile_k : c.tile_k) : 0;
-            const bool ok = where == kSplitPrepass ||
-                            (K >= kTcFusedMinK && lda % 4 == 0 && (where != kSplitInKernel || ldb % 4 == 0) &&
-                             !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where, tc_bk) >= 0);
-            if (!ok) {
-                if (o.operand_split || o.tile_k == 16) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-                where = kSplitPrepass;
+            // tile_m 256: a pair of CTAs per 256-row tile (one tcgen05.mma
+            // across both), operands split in the kernel only.
+            const bool pair = c.tile_m == 256;
+            if (pair) {
+                if ((o.operand_split && o.operand_split != 2) || o.stages || o.separate_syncs ||
+                    o.split_reduce >= 2 || K < kTcFusedMinK || lda % 4 != 0 || ldb % 4 != 0) {
+                    delete p;
+                    return GEMM_F32_ERR_UNSUPPORTED;
+                }
+                const int pbk = o.tile_k ? o.tile_k : c.tile_k;
+                t.config_id = tc_find_pair_config(c.tile_n, pbk);
+                if (t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                t.pair_slots = tc_pair_slots(c.tile_n, tc_config(t.config_id).bk, p->num_sms);
+                if (t.pair_slots < 1) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                t.fallback_config_id = tc_find_config(c.tile_n, 0, false, kSplitPrepass);
+            } else {
+                int where = o.operand_split ? o.operand_split - 1
+                            : o.stages      ? kSplitPrepass
+                            : o.tile_k == 16 ? kSplitInKernel
+                                             : c.fused;
+                const int tc_bk = where == kSplitInKernel ? (o.tile_k ? o.tile_k : c.tile_k) : 0;
+                const bool ok = where == kSplitPrepass ||
+                                (K >= kTcFusedMinK && lda % 4 == 0 && (where != kSplitInKernel || ldb % 4 == 0) &&
+                                 !o.separate_syncs && tc_find_config(c.tile_n, 0, false, where, tc_bk) >= 0);
+                if (!ok) {
+                    if (o.operand_split || o.tile_k == 16) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                    where = kSplitPrepass;
+                }
+                if (o.tile_k && where != kSplitInKernel && o.tile_k != 32) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                t.config_id = tc_find_config(c.tile_n, where != kSplitPrepass ? 0 : c.stages, o.separate_syncs != 0,
+                                             where, where == kSplitInKernel ? tc_bk : 0);
+                if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                if (where != kSplitPrepass) t.fallback_config_id = tc_find_config(c.tile_n, 0, false, kSplitPrepass);
             }
-            if (o.tile_k && where != kSplitInKernel && o.tile_k != 32) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-            t.config_id = tc_find_config(c.tile_n, where != kSplitPrepass ? 0 : c.stages, o.separate_syncs != 0,
-                                         where, where == kSplitInKernel ? tc_bk : 0);
-            if (c.tile_m != 128 || t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-            if (where != kSplitPrepass) t.fallback_config_id = tc_find_config(c.tile_n, 0, false, kSplitPrepass);
             const TcConfig& tcfg = tc_config(t.config_id);
             t.terms = o.tf32_terms ? o.tf32_terms : 3;
             t.num_sms = p->num_sms;
@@ -311,6 +328,14 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if ((o.split_reduce == 2 && t.cluster == 0) || (o.split_reduce == 3 && t.fixup == 0)) {
                 delete p;
                 return GEMM_F32_ERR_UNSUPPORTED;
+            }
+            if (pair) {
+                // a run with operands the TMA cannot take falls back to the
+                // one-CTA pre-pass form: the partial buffer holds either's slices
+                TcPlanState fb = t;
+                fb.config_id = t.fallback_config_id;
+                tc_configure(fb, M, N, K, c.split_k);
+                if (fb.partial_bytes > t.partial_bytes) t.partial_bytes = fb.partial_bytes;
             }
             ahi_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
             alo_off = bytes; bytes += align256(size_t(M) * size_t(t.kp) * sizeof(float));
@@ -324,17 +349,25 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 sem_off = bytes;
                 bytes += align256(t.sem_bytes);
             }
-            snprintf(p->desc, sizeof p->desc,
-                     "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d%s group=%d "
-                     "kp=%lld",
-                     tcfg.split == kSplitInKernel ? " in-kernel-split"
-                     : tcfg.split == kSplitHybrid ? " hybrid-split"
-                     : tcfg.split == kSplitRawA ? " raw-a-split" : "",
-                     t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
-                     tcfg.sep ? " separate-syncs" : "",
-                     t.tiles_m * t.tiles_n, t.dp_tiles,
-                     t.split_tiles, t.splits, t.cluster ? " cluster-sum" : t.fixup ? " last-arriver-sum" : "",
-                     t.tile_group > 0 ? t.tile_group : 8, (long long)t.kp);
+            if (pair)
+                snprintf(p->desc, sizeof p->desc,
+                         "tcgen05 3xtf32 in-kernel-split cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
+                         "whole=%d split=%dx%d resident=%d group=%d kp=%lld",
+                         t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
+                         t.split_tiles, t.splits, t.pair_slots, t.tile_group > 0 ? t.tile_group : 8,
+                         (long long)t.kp);
+            else
+                snprintf(p->desc, sizeof p->desc,
+                         "tcgen05 3xtf32%s terms=%d tile=%dx%dx%d stages=%d%s tiles=%d whole=%d split=%dx%d%s "
+                         "group=%d kp=%lld",
+                         tcfg.split == kSplitInKernel ? " in-kernel-split"
+                         : tcfg.split == kSplitHybrid ? " hybrid-split"
+                         : tcfg.split == kSplitRawA ? " raw-a-split" : "",
+                         t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages,
+                         tcfg.sep ? " separate-syncs" : "",
+                         t.tiles_m * t.tiles_n, t.dp_tiles,
+                         t.split_tiles, t.splits, t.cluster ? " cluster-sum" : t.fixup ? " last-arriver-sum" : "",
+                         t.tile_group > 0 ? t.tile_group : 8, (long long)t.kp);
         }
     }
 
@@ -400,7 +433,7 @@ bool current_device_is(int dev)
 // 1 = the plain copy-run-copy sequence.
 int host_panel_count(const gemm_f32_plan_s* p)
 {
-    if (p->kind != kTc || p->K == 0) return 1;
+    if (p->kind != kTc || p->K == 0 || tc_config(p->tc.config_id).bm != 128) return 1;
     int n = p->opts.host_panels;
     if (n == 0) {
         const int64_t waves = int64_t(p->tc.tiles_m) * p->tc.tiles_n / (p->num_sms > 0 ? p->num_sms : 1);

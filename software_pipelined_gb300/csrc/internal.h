@@ -64,7 +64,7 @@ cudaError_t zero_fill_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaSt
 
 // ---- tcgen05 3xTF32 kernel (tc_gemm.cu) -----------------------------------
 struct TcConfig {
-    int bm, bn, bk;  // CTA tile (bm = 128 rows = TMEM lanes; bk = 32 fp32 = 128 B)
+    int bm, bn, bk;  // tile (bm = 128 rows = TMEM lanes, or 256 for a CTA pair; bk = 32 fp32 = 128 B)
     int stages;      // smem ring depth
     bool sep;        // separate full barriers for A and B (ablation)
     int split;       // where the 3xTF32 split happens: kSplitPrepass, kSplitInKernel, kSplitHybrid
@@ -78,6 +78,12 @@ enum : int {
 int tc_num_configs();
 const TcConfig& tc_config(int id);
 int tc_find_config(int bn, int stages, bool sep, int split, int bk = 0);
+// The CTA-pair configuration (256-row tiles, operands split in the kernel) of
+// tile width bn and stage depth bk (0 = 32), or -1.
+int tc_find_pair_config(int bn, int bk);
+// How many pairs of that configuration run at once on this device (0 when the
+// occupancy query fails).
+int tc_pair_slots(int bn, int bk, int sms);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
 // tensor maps that describe it, and the work decomposition.
@@ -125,6 +131,7 @@ struct TcPlanState {
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.
     int fallback_config_id = -1;
+    int pair_slots = 0;        // CTA-pair plans: pairs of CTAs resident at once
     mutable const float* raw_a = nullptr;
     mutable const float* raw_b = nullptr;
     alignas(64) mutable unsigned char tmap_a_raw[128];

@@ -193,5 +193,40 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// ---- tcgen05 across a CTA pair (cta_group::2) -------------------------------
+// One warp of each CTA of the pair performs the pair's allocation together;
+// every tcgen05 instruction of a kernel that uses these has cta_group::2.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+// D (128 TMEM lanes in each CTA of the pair) (+)= A (M = 256: 128 rows from
+// each CTA's shared memory at the descriptor's address) * B (N columns: the
+// first half from this CTA, the second from the peer), kind::tf32.  Issued by
+// one thread of the pair's even CTA.
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` of every CTA in `cta_mask` when
+// every pair MMA issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;\n" :: "r"(bar), "h"(cta_mask) : "memory");
+}
+// Store a 32-bit value to shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;\n" :: "r"(a), "r"(v) : "memory");
+}
+
 }  // namespace ptx
 }  // namespace gemm_f32

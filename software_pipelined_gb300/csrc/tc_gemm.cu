@@ -3,6 +3,7 @@
 // the tensor maps, and the launch sequence of one run (operand pre-pass, main
 // kernel, split-tile reduction), whole or by row panels.  The kernels are in
 // tc_kernels.cuh.
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <utility>
@@ -141,6 +142,12 @@ cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s
                       a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
 }
 
+template <int BN>
+cudaError_t launch_pair_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
+{
+    return tc_pair_reduce(BN, st, a, s);
+}
+
 using MainFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, const void*, cudaStream_t);
 using LaunchFn = cudaError_t (*)(const TcPlanState&, const TcArgs&, cudaStream_t);
 struct TcEntry {
@@ -181,6 +188,12 @@ const TcEntry kTc[] = {
     // hi of A read from the caller's A, lo of A and both pieces of B by the pre-pass
     {{128, 128, 32, 3, false, kSplitRawA}, launch_main<128, 3>, launch_reduce<128>, kClusterOk<128, 3>, kFixupOk<128, 3>},
     {{128, 256, 32, 2, false, kSplitRawA}, launch_main<256, 2>, launch_reduce<256>, kClusterOk<256, 2>, kFixupOk<256, 2>},
+    // CTA pairs (tc_pair.cu): 256 x BN tiles, operands split in the kernel,
+    // each CTA holding its 128 rows of A and half of B; rings of 192 KB
+    {{256, 256, 32, 3, false, kSplitInKernel}, nullptr, launch_pair_reduce<256>, false, false},
+    {{256, 256, 16, 6, false, kSplitInKernel}, nullptr, launch_pair_reduce<256>, false, false},
+    {{256, 128, 32, 4, false, kSplitInKernel}, nullptr, launch_pair_reduce<128>, false, false},
+    {{256, 128, 16, 8, false, kSplitInKernel}, nullptr, launch_pair_reduce<128>, false, false},
 };
 
 }  // namespace
@@ -191,17 +204,83 @@ int tc_find_config(int bn, int stages, bool sep, int split, int bk)
 {
     for (int i = 0; i < tc_num_configs(); ++i) {
         const TcConfig& c = kTc[i].cfg;
-        if (c.bn == bn && (stages == 0 || c.stages == stages) && c.sep == sep && c.split == split &&
+        if (c.bm == kBM && c.bn == bn && (stages == 0 || c.stages == stages) && c.sep == sep && c.split == split &&
             (bk == 0 || c.bk == bk))
             return i;
     }
     return -1;
 }
 
+int tc_find_pair_config(int bn, int bk)
+{
+    for (int i = 0; i < tc_num_configs(); ++i) {
+        const TcConfig& c = kTc[i].cfg;
+        if (c.bm == 2 * kBM && c.bn == bn && c.bk == (bk ? bk : kBK)) return i;
+    }
+    return -1;
+}
+
+namespace {
+
+// The work of a CTA-pair plan, in pair tiles (two tile rows of one tile
+// column): the same policy as below with a pair tile for a tile and the pairs
+// resident at once for the SMs.  tiles_m counts 128-row tiles, rounded up to
+// whole pairs (the second tile of the last pair may lie past M: its rows are
+// computed from TMA's zero fill and never stored).
+void pair_configure(TcPlanState& t, int64_t M, int64_t N, int split_request)
+{
+    const TcConfig& c = kTc[t.config_id].cfg;
+    const int num_kb = (int)(t.kp / kBK);
+    t.tiles_m = 2 * (int)((M + 2 * kBM - 1) / (2 * kBM));
+    t.tiles_n = (int)((N + c.bn - 1) / c.bn);
+    const int ptiles = t.tiles_m / 2 * t.tiles_n;
+    const int wave = t.pair_slots > 0 ? t.pair_slots : (t.num_sms > 1 ? t.num_sms / 2 : 1);
+    t.dp_tiles = ptiles;
+    t.split_tiles = 0;
+    t.splits = 1;
+    int want = 1;
+    if (split_request >= 2) {
+        want = split_request;
+        t.dp_tiles = 0;
+        t.split_tiles = ptiles;
+    } else if (split_request == 0 && ptiles > wave && ptiles % wave != 0) {
+        const int rem = ptiles % wave;
+        want = std::min(std::min(wave / rem, 8), num_kb / 4);
+        if (want >= 2) {
+            t.dp_tiles = ptiles - rem;
+            t.split_tiles = rem;
+        }
+    }
+    if (t.split_tiles > 0) {
+        if (want > num_kb) want = num_kb;
+        const int kb_per = (num_kb + want - 1) / want;
+        const int splits = (num_kb + kb_per - 1) / kb_per;
+        if (splits < 2) {
+            t.dp_tiles = ptiles;
+            t.split_tiles = 0;
+        } else {
+            t.splits = splits;
+            t.kb_per_split = kb_per;
+        }
+    }
+    if (t.split_tiles == 0) t.kb_per_split = num_kb;
+    t.cluster = 0;
+    t.fixup = 0;
+    t.sem_bytes = 0;
+    t.partial_bytes = t.split_tiles ? size_t(2) * t.split_tiles * t.splits * kBM * c.bn * sizeof(float) : 0;
+}
+
+}  // namespace
+
 void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_request)
 {
     const TcConfig& c = kTc[t.config_id].cfg;
     t.split_request = split_request;
+    if (c.bm == 2 * kBM) {
+        t.kp = (K + kBK - 1) / kBK * kBK;
+        pair_configure(t, M, N, split_request);
+        return;
+    }
     t.kp = (K + kBK - 1) / kBK * kBK;
     const int num_kb = (int)(t.kp / kBK);
     t.tiles_m = (int)((M + kBM - 1) / kBM);
@@ -374,7 +453,10 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     if (a.cluster > 1 && !kTc[r.id].cluster_ok) return cudaErrorInvalidValue;
     if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
-    if (r.in_kernel) {
+    if (c.bm == 2 * kBM) {
+        e = tc_pair_main(c.bn, c.bk, st, a, *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw), s);
+    } else if (r.in_kernel) {
         e = tc_fused_main(c.bn, c.bk, c.split == kSplitHybrid, st, a,
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw),
@@ -398,6 +480,15 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
 {
     const TcConfig& c = kTc[st.config_id].cfg;
     const Route r = route(st, A, B);
+    if (c.bm == 2 * kBM && !r.in_kernel) {
+        // A CTA-pair plan with a base pointer the TMA cannot take: the one-CTA
+        // pre-pass form of the same tile width, its own work decomposition,
+        // the same scratch (the partial buffer holds either).
+        TcPlanState fb = st;
+        fb.config_id = st.fallback_config_id;
+        tc_configure(fb, M, N, K, st.split_request);
+        return tc_launch(fb, M, N, K, A, lda, B, ldb, C, ldc, status, s, ev);
+    }
     cudaError_t e = cudaSuccess;
     if (ev) cudaEventRecord(ev[0], s);
     // Tensor maps over the caller's raw operands, re-encoded when they move.

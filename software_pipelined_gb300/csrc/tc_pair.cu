@@ -1,0 +1,526 @@
+// tcgen05 3xTF32 GEMM on CTA pairs: one 256 x BN output tile per pair of CTAs
+// (a thread-block cluster of two), one tcgen05.mma.cta_group::2 for the pair.
+//
+// The same software pipeline as tc_fused.cu ("Double Buffering" technique page
+// and "Case Study: The Double-Buffered GEMM": the next K-tile is fetched while
+// the current one is multiplied), with the operand split inside the kernel,
+// but the pair shares the work of staging the operands:
+//
+//   * each CTA holds its own 128 rows of A (raw by TMA, lo_A by its converter
+//     warps) and HALF of the tile's B columns (raw 32 x 32 boxes by TMA,
+//     transposed to hi_B / lo_B by its converters);
+//   * the even CTA's MMA thread issues M = 256, N = BN MMAs that read A rows
+//     0..127 and B columns 0..BN/2-1 from its own shared memory and the rest
+//     from its peer's, at the same addresses, and accumulate the even CTA's
+//     128 rows in its TMEM and the odd CTA's 128 rows in the odd CTA's TMEM.
+//
+// Per CTA and k-block this halves the B tile a CTA copies, converts and feeds
+// to the tensor core, against a 128 x BN tile of the one-CTA kernel with the
+// same MMA work per SM, so the ring holds more stages.
+//
+// Synchronisation (every wait bounded; a CTA that gives up raises its own and
+// its peer's abort flag):
+//   full_a[s]  TMA of the CTA's raw A and B landed (local)
+//   rd[s]      every converter warp of the CTA holds its raw B (local)
+//   conv[s]    (even CTA) both CTAs' converters are done: counts 2 x 8 warps,
+//              the odd CTA's arriving remotely with release at cluster scope
+//   empty[s]   the pair's MMAs of slot s completed: one commit, multicast to
+//              both CTAs
+//   tfull      accumulator complete: commit multicast to both CTAs
+//   tempty     (even CTA) both CTAs' epilogues drained the accumulator: 8 warps
+// Both CTAs take the same units in the same order.  Before they read any
+// peer state they pass a cluster barrier, and before either exits (or frees
+// TMEM) a second one, so no CTA leaves while its shared memory may still be
+// read by the pair's MMAs or written by its peer.
+#include <cstdint>
+
+#include "tc_common.cuh"
+
+namespace gemm_f32 {
+namespace {
+
+using namespace tc;
+constexpr int kPairConvWarps = 8;
+constexpr int kPairConvThreads = kPairConvWarps * 32;
+constexpr int kPairThreads = 6 * 32 + kPairConvThreads;
+
+// BN: the pair's tile width (each CTA holds BN/2 columns of B); KB: k per stage.
+template <int BN, int SLOTS, int KB>
+struct PairLayout {
+    static constexpr int BH = BN / 2;                    // B columns per CTA
+    static constexpr int A_BYTES = kBM * KB * 4;
+    static constexpr int B_BYTES = BH * KB * 4;          // also raw B: BH/32 boxes
+    static constexpr int BOX_BYTES = 32 * KB * 4;
+    static_assert(KB == 32 || KB == 16, "stage depth");
+    static_assert(BH % 32 == 0 && B_BYTES == BH / 32 * BOX_BYTES, "raw B fills the lo_B part exactly");
+    static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int RING_BYTES = SLOTS * SLOT_BYTES;
+    // full, rd, conv, empty per slot + tfull/tempty x2, drain, spare
+    static constexpr int NBARS = 4 * SLOTS + 6;
+    static constexpr int BAR_BYTES = 8 * NBARS + 16;
+    // B_BYTES of slack after the barriers: every MMA operand read of the pair
+    // stays inside this CTA's allocation even if one ran BH rows past a slot
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + B_BYTES;
+    // At most 256 TMEM columns per CTA: two accumulators of BN columns when they
+    // fit, else one (the MMA of a CTA's next unit then waits for the epilogue).
+    static constexpr int TBUFS = 2 * BN <= 256 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = TBUFS * BN;
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 256 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM cols");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(RING_BYTES >= 4 * 8192, "the ring holds the TMA-store staging");
+};
+
+template <int KB>
+__device__ __forceinline__ uint32_t pair_kmajor_off(int row, int kq)
+{
+    if constexpr (KB == 32)
+        return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((kq ^ (row & 7)) << 4));
+    else
+        return (uint32_t)((row >> 3) * 512 + (row & 7) * 64 + ((kq ^ ((row >> 1) & 3)) << 4));
+}
+
+template <int KB>
+__device__ __forceinline__ uint64_t pair_kmajor_desc(uint32_t saddr)
+{
+    if constexpr (KB == 32) {
+        return sw128_desc(saddr);
+    } else {
+        return (uint64_t)((saddr & 0x3FFFFu) >> 4)
+             | ((uint64_t)1 << 16)                  // leading byte offset (unused)
+             | ((uint64_t)(512 >> 4) << 32)         // stride byte offset: 8 rows of 64 B
+             | ((uint64_t)1 << 46)                  // descriptor version (tcgen05)
+             | ((uint64_t)4 << 61);                 // swizzle: 64 B
+    }
+}
+
+// Instruction descriptor, kind::tf32, M = 256 (a CTA pair), N = BN.
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_tf32_pair()
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+// The unit of a pair in pair tiles (dp_tiles, split_tiles in pair tiles), and
+// this CTA's 128-row tile and partial slot in it.  Pair tile P covers tile
+// rows 2*ptm and 2*ptm + 1 of tile column tn, (ptm, tn) in the grouped order
+// over pair rows; a split pair tile q's slice z goes to slots
+// (2q + rank) * splits + z, so that tile j = 2q + rank of the split tiles
+// owns slots j * splits .. j * splits + splits - 1.
+struct PairUnit {
+    Unit u;      // this CTA's share: tile = 2P + rank, kb range, slot (-1: C)
+    int tm, tn;  // this CTA's 128-row tile
+};
+
+__device__ __forceinline__ PairUnit pair_unit(int w, const TcArgs& a, int rank)
+{
+    const Unit pu = decode_unit(w, a);
+    PairUnit r;
+    int ptm, tn;
+    tile_coords(pu.tile, a.tiles_m / 2, a.tiles_n, a.group, ptm, tn);
+    r.tm = 2 * ptm + rank;
+    r.tn = tn;
+    r.u.tile = 2 * pu.tile + rank;
+    r.u.kb0 = pu.kb0;
+    r.u.kb1 = pu.kb1;
+    if (pu.slot < 0) {
+        r.u.slot = -1;
+    } else {
+        const int q = pu.slot / a.splits, z = pu.slot % a.splits;
+        r.u.slot = (2 * q + rank) * a.splits + z;
+    }
+    return r;
+}
+
+template <int BN, int SLOTS, int KB>
+__global__ void __launch_bounds__(kPairThreads, 1)
+tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
+               const TcArgs args)
+{
+    using L = PairLayout<BN, SLOTS, KB>;
+    constexpr int HALVES = kBK / KB;  // stages per 32-k block of the work decomposition
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    const uint32_t ring = (raw_addr + 1023u) & ~1023u;
+    uint8_t* ring_ptr = smem_raw + (ring - raw_addr);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + L::RING_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the pair's MMAs
+    auto full_a = [&](int s) { return ptx::smem_u32(bars + s); };
+    auto conv = [&](int s) { return ptx::smem_u32(bars + SLOTS + s); };
+    auto empty = [&](int s) { return ptx::smem_u32(bars + 2 * SLOTS + s); };
+    auto rd = [&](int s) { return ptx::smem_u32(bars + 3 * SLOTS + s); };
+    auto tfull = [&](int b) { return ptx::smem_u32(bars + 4 * SLOTS + b); };
+    auto tempty = [&](int b) { return ptx::smem_u32(bars + 4 * SLOTS + 2 + b); };
+    const uint32_t drain_bar = ptx::smem_u32(bars + 4 * SLOTS + 4);
+    // the abort flag of the peer CTA (shared::cluster address)
+    const uint32_t peer_abort = ptx::mapa(ptx::smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        ptx::st_cluster_u32(peer_abort, 1u);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SLOTS; ++s) {
+            ptx::mbar_init(full_a(s), 1);
+            ptx::mbar_init(conv(s), 2 * kPairConvWarps);
+            ptx::mbar_init(empty(s), 1);
+            ptx::mbar_init(rd(s), kPairConvWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull(b), 1);
+            ptx::mbar_init(tempty(b), 8);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tm_a);
+        ptx::tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers initialised, TMEM allocated, abort flags cleared
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int num_work = args.dp_tiles + args.split_tiles * args.splits;
+    const int64_t limit = args.timeout;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            pdl_wait();  // the previous kernel's writes (A, B, C) are done
+            uint32_t fills = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs) {
+                const PairUnit pu = pair_unit(w, args, (int)rank);
+                for (int kh = pu.u.kb0 * HALVES; kh < pu.u.kb1 * HALVES; ++kh) {
+                    const int s = fills % SLOTS;
+                    const uint32_t ps = (fills / SLOTS) & 1u;
+                    if (!wait_phase(empty(s), ps ^ 1u, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ++fills;
+                    if (fills == (uint32_t)args.withhold) continue;
+                    const int kc = kh * KB;
+                    const uint32_t slot = ring + s * L::SLOT_BYTES;
+                    // raw A (this CTA's 128 rows) into the A part, raw B boxes
+                    // (this CTA's half of the columns) into the lo_B part
+                    ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + L::B_BYTES);
+                    ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
+#pragma unroll
+                    for (int j = 0; j < L::BH / 32; ++j)
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES + j * L::BOX_BYTES, &tm_b, full_a(s),
+                                         pu.tn * BN + (int)rank * L::BH + 32 * j, kc);
+                }
+            }
+            if (stop) give_up();
+            // Drain: the last fill of every slot must have landed.
+            const uint32_t total = fills;
+            for (int s = 0; s < SLOTS && (uint32_t)s < total; ++s) {
+                const uint32_t last = (total - 1 - s) / SLOTS * SLOTS + s;
+                if (last + 1 == (uint32_t)args.withhold) continue;
+                const uint32_t par = (last / SLOTS) & 1u;
+                const long long t0 = clock64();
+                while (!ptx::mbar_try_wait(full_a(s), par))
+                    if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ----------------------------
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_tf32_pair<BN>();
+            uint32_t fills = 0;
+            int iter = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs, ++iter) {
+                const Unit u = decode_unit(w, args);
+                const int buf = L::TBUFS == 2 ? (iter & 1) : 0;
+                const uint32_t tphase = (uint32_t)(iter / L::TBUFS) & 1u;
+                if (!wait_phase_cluster(tempty(buf), tphase ^ 1u, limit, abort_flag, args.status)) {
+                    stop = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
+                    const int s = fills % SLOTS;
+                    const uint32_t ps = (fills / SLOTS) & 1u;
+                    if (!wait_phase_cluster(conv(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_hi = ring + s * L::SLOT_BYTES, a_lo = a_hi + L::A_BYTES;
+                    const uint32_t b_hi = a_hi + 2 * L::A_BYTES, b_lo = b_hi + L::B_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < KB / kUmmaK; ++ks) {
+                        const uint32_t off = ks * kUmmaK * 4;
+                        const uint32_t acc = (kh > u.kb0 * HALVES || ks > 0) ? 1u : 0u;
+                        if (args.terms == 3) {
+                            ptx::mma_tf32_pair(d_tmem, pair_kmajor_desc<KB>(a_lo + off),
+                                               pair_kmajor_desc<KB>(b_hi + off), idesc, acc);
+                            ptx::mma_tf32_pair(d_tmem, pair_kmajor_desc<KB>(a_hi + off),
+                                               pair_kmajor_desc<KB>(b_lo + off), idesc, 1u);
+                            ptx::mma_tf32_pair(d_tmem, pair_kmajor_desc<KB>(a_hi + off),
+                                               pair_kmajor_desc<KB>(b_hi + off), idesc, 1u);
+                        } else {
+                            ptx::mma_tf32_pair(d_tmem, pair_kmajor_desc<KB>(a_hi + off),
+                                               pair_kmajor_desc<KB>(b_hi + off), idesc, acc);
+                        }
+                    }
+                    ptx::mma_commit_pair(empty(s), 0x3);  // both CTAs' slot s free once these finish
+                }
+                if (stop) break;
+                ptx::mma_commit_pair(tfull(buf), 0x3);  // both CTAs' accumulators complete
+            }
+            if (stop) give_up();
+            ptx::mma_commit_pair(drain_bar, 0x1);
+            const long long t0 = clock64();
+            while (!ptx::mbar_try_wait(drain_bar, 0))
+                if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------ epilogue ------------------------------
+        const int quad = warp & 3;
+        const uint32_t lead_tempty0 = ptx::mapa(tempty(0), 0), lead_tempty1 = ptx::mapa(tempty(1), 0);
+        int iter = 0;
+        bool stop = false;
+        for (int w = pair; w < num_work; w += npairs, ++iter) {
+            const PairUnit pu = pair_unit(w, args, (int)rank);
+            const int buf = L::TBUFS == 2 ? (iter & 1) : 0;
+            const uint32_t tphase = (uint32_t)(iter / L::TBUFS) & 1u;
+            if (!wait_phase(tfull(buf), tphase, limit, abort_flag, args.status)) {
+                stop = true;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
+            const EpilogueBars eb{drain_bar, drain_bar, drain_bar, drain_bar, drain_bar};  // unused: no cluster sum
+            drain_unit<BN, L::RING_BYTES>(args, &tm_c, &tm_p, pu.u, pu.tm, pu.tn, taddr, quad, lane,
+                                          w + npairs >= num_work, false, false, ring, ring_ptr, eb, limit,
+                                          abort_flag);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(buf ? lead_tempty1 : lead_tempty0);
+        }
+        if (stop && lane == 0) give_up();
+    } else {
+        // ------------------------------ converters ----------------------------
+        const int ct = threadIdx.x - 6 * 32;    // 0 .. kPairConvThreads-1
+        constexpr int KG = KB / 4;              // 4-wide k groups per stage
+        constexpr int PARTS = kPairConvWarps / KG;  // warps per k group: they share the boxes
+        const int cw = (ct >> 5) % KG;
+        const int part = (ct >> 5) / KG;
+        uint32_t fills = 0;
+        bool stop = false;
+        uint32_t box_off[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = cw * 4 + j;
+            box_off[j] = (uint32_t)(k * 128 + (((lane >> 2) ^ (k & 7)) << 4) + (lane & 3) * 4);
+        }
+        for (int w = pair; w < num_work && !stop; w += npairs) {
+            const Unit u = decode_unit(w, args);
+            for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
+                const int s = fills % SLOTS;
+                const uint32_t ps = (fills / SLOTS) & 1u;
+                if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t* slot = ring_ptr + s * L::SLOT_BYTES;
+                const uint8_t* a_raw = slot;
+                uint8_t* a_lo = slot + L::A_BYTES;
+                uint8_t* b_hi = slot + 2 * L::A_BYTES;
+                uint8_t* b_lo = b_hi + L::B_BYTES;  // holds raw B until every warp has read it
+                constexpr int NBW = L::BH / 32 / PARTS;  // boxes per warp
+                static_assert(NBW >= 1 && NBW * PARTS == L::BH / 32, "boxes per converter warp");
+                float v[NBW][4];
+#pragma unroll
+                for (int i = 0; i < NBW; ++i) {
+                    const int nb = part + i * PARTS;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        v[i][j] = *reinterpret_cast<const float*>(b_lo + nb * L::BOX_BYTES + box_off[j]);
+                    *reinterpret_cast<float4*>(b_hi + pair_kmajor_off<KB>(nb * 32 + lane, cw)) =
+                        make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(rd(s));
+#pragma unroll
+                for (int c = ct; c < L::A_BYTES / 16; c += kPairConvThreads) {
+                    const float4 x = *reinterpret_cast<const float4*>(a_raw + c * 16);
+                    *reinterpret_cast<float4*>(a_lo + c * 16) =
+                        make_float4(lo_part(x.x), lo_part(x.y), lo_part(x.z), lo_part(x.w));
+                }
+                if (!wait_phase(rd(s), ps, limit, abort_flag, args.status)) {
+                    stop = true;
+                    break;
+                }
+#pragma unroll
+                for (int i = 0; i < NBW; ++i)
+                    *reinterpret_cast<float4*>(b_lo + pair_kmajor_off<KB>((part + i * PARTS) * 32 + lane, cw)) =
+                        make_float4(lo_part(v[i][0]), lo_part(v[i][1]), lo_part(v[i][2]), lo_part(v[i][3]));
+                ptx::fence_proxy_async_shared();  // generic-proxy writes -> the pair's tensor-core reads
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(conv(s), 0));
+            }
+        }
+        if (stop && lane == 0) give_up();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    // no CTA leaves (or frees TMEM) while the pair's MMAs may still read its
+    // shared memory or its peer may still arrive on its barriers
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// Sum the K-slices of every split pair tile (its two 128-row tiles) in slice
+// order and write C (guarded).  Grid-stride over 2 x split_tiles (pairs) x 128
+// x BN/4 float4 positions; tile j = 2q + r of the split tiles is row half r of
+// split pair tile q.
+template <int BN>
+__global__ void __launch_bounds__(256)
+pair_reduce_kernel(const float4* __restrict__ partial, int dp_pairs, int split_pairs, int splits, int tiles_m,
+                   int tiles_n, int group, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
+{
+    pdl_trigger();
+    pdl_wait();
+    constexpr int Q = BN / 4;
+    constexpr int PER_TILE = kBM * Q;
+    const bool vec = ((ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    const int64_t total = (int64_t)2 * split_pairs * PER_TILE;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(idx / PER_TILE);
+        const int rem = (int)(idx % PER_TILE);
+        const int r = rem / Q, c = (rem % Q) * 4;
+        int ptm, tn;
+        tile_coords(dp_pairs + j / 2, tiles_m / 2, tiles_n, group, ptm, tn);
+        const int64_t grow = ((int64_t)2 * ptm + (j & 1)) * kBM + r, gcol = (int64_t)tn * BN + c;
+        if (grow >= M || gcol >= N) continue;
+        const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
+        float4 acc = __ldg(p);
+        for (int z = 1; z < splits; ++z) {
+            const float4 t = __ldg(p + (int64_t)z * PER_TILE);
+            acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+        }
+        float* dst = C + grow * ldc + gcol;
+        if (vec && gcol + 3 < N) {
+            *reinterpret_cast<float4*>(dst) = acc;
+        } else {
+            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int q = 0; q < 4 && gcol + q < N; ++q) dst[q] = v[q];
+        }
+    }
+}
+
+int reduce_grid(int64_t work, int sms)
+{
+    const int64_t blocks = (work + 255) / 256;
+    const int64_t cap = (int64_t)sms * 8;
+    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+template <int BN, int SLOTS, int KB>
+cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
+                        cudaStream_t s)
+{
+    using L = PairLayout<BN, SLOTS, KB>;
+    auto kern = tc_pair_kernel<BN, SLOTS, KB>;
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
+    const int work = a.dp_tiles + a.split_tiles * a.splits;
+    const int pairs = work < st.pair_slots ? work : st.pair_slots;
+    if (pairs < 1) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s, 2, ta, tb,
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
+}
+
+template <int BN, int SLOTS, int KB>
+int pair_slots_for(int sms)
+{
+    using L = PairLayout<BN, SLOTS, KB>;
+    auto kern = tc_pair_kernel<BN, SLOTS, KB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1));
+    cfg.blockDim = dim3(kPairThreads);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace
+
+cudaError_t tc_pair_main(int bn, int bk, const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
+                         const CUtensorMap& tb, cudaStream_t s)
+{
+    if (bn == 256 && bk == 32) return launch_pair<256, 3, 32>(st, a, ta, tb, s);
+    if (bn == 256 && bk == 16) return launch_pair<256, 6, 16>(st, a, ta, tb, s);
+    if (bn == 128 && bk == 32) return launch_pair<128, 4, 32>(st, a, ta, tb, s);
+    if (bn == 128 && bk == 16) return launch_pair<128, 8, 16>(st, a, ta, tb, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const TcArgs& a, cudaStream_t s)
+{
+    const int64_t total = (int64_t)2 * a.split_tiles * kBM * (bn / 4);
+    const dim3 grid(reduce_grid(total, st.num_sms));
+    const float4* p = reinterpret_cast<const float4*>(a.partial);
+    if (bn == 256)
+        return launch_pdl(pair_reduce_kernel<256>, grid, dim3(256), 0, s, 1, p, a.dp_tiles, a.split_tiles, a.splits,
+                          a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
+    if (bn == 128)
+        return launch_pdl(pair_reduce_kernel<128>, grid, dim3(256), 0, s, 1, p, a.dp_tiles, a.split_tiles, a.splits,
+                          a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
+    return cudaErrorInvalidValue;
+}
+
+int tc_pair_slots(int bn, int bk, int sms)
+{
+    if (bn == 256 && bk == 32) return pair_slots_for<256, 3, 32>(sms);
+    if (bn == 256 && bk == 16) return pair_slots_for<256, 6, 16>(sms);
+    if (bn == 128 && bk == 32) return pair_slots_for<128, 4, 32>(sms);
+    if (bn == 128 && bk == 16) return pair_slots_for<128, 8, 16>(sms);
+    return 0;
+}
+
+}  // namespace gemm_f32

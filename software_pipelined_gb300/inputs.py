@@ -27,20 +27,39 @@ GOLDEN_GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-_CHUNK = 1 << 22
+_CHUNK = 1 << 20
+
+
+def _chunks(seed: int, n: int, start: int = 0):
+    """Yield (offset, x) over outputs start .. start+n-1 of the stream, x a
+    buffer of at most _CHUNK uint64 that is reused between chunks (every step
+    in place, so long streams cost no allocation per chunk)."""
+    s = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
+    z = np.empty(min(n, _CHUNK), dtype=np.uint64)
+    t = np.empty_like(z)
+    with np.errstate(over="ignore"):
+        for lo in range(0, n, _CHUNK):
+            m = min(n, lo + _CHUNK) - lo
+            x, y = z[:m], t[:m]
+            x[:] = np.arange(start + lo + 1, start + lo + m + 1, dtype=np.uint64)
+            np.multiply(x, GOLDEN_GAMMA, out=x)
+            np.add(x, s, out=x)
+            np.right_shift(x, np.uint64(30), out=y)
+            np.bitwise_xor(x, y, out=x)
+            np.multiply(x, _M1, out=x)
+            np.right_shift(x, np.uint64(27), out=y)
+            np.bitwise_xor(x, y, out=x)
+            np.multiply(x, _M2, out=x)
+            np.right_shift(x, np.uint64(31), out=y)
+            np.bitwise_xor(x, y, out=x)
+            yield lo, x
 
 
 def splitmix64(seed: int, n: int, start: int = 0) -> np.ndarray:
     """Outputs start .. start+n-1 of the SplitMix64 stream seeded with ``seed``."""
     out = np.empty(n, dtype=np.uint64)
-    s = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
-    with np.errstate(over="ignore"):
-        for lo in range(0, n, _CHUNK):
-            hi = min(n, lo + _CHUNK)
-            z = np.arange(start + lo + 1, start + hi + 1, dtype=np.uint64) * GOLDEN_GAMMA + s
-            z = (z ^ (z >> np.uint64(30))) * _M1
-            z = (z ^ (z >> np.uint64(27))) * _M2
-            out[lo:hi] = z ^ (z >> np.uint64(31))
+    for lo, x in _chunks(seed, n, start):
+        out[lo:lo + len(x)] = x
     return out
 
 
@@ -50,8 +69,16 @@ def uniform_pm1(seed: int, rows: int, cols: int, ld: int | None = None) -> np.nd
     With ``ld`` > cols the result is a row-padded view of a rows x ld buffer
     whose padding holds NaN (so a reader that touches it is caught).
     """
-    x = splitmix64(seed, rows * cols)
-    v = ((x >> np.uint64(40)).astype(np.float64) * 2.0 ** -23 - 1.0).astype(np.float32)
+    n = rows * cols
+    v = np.empty(n, dtype=np.float32)
+    f = np.empty(min(n, _CHUNK), dtype=np.float64)
+    for lo, x in _chunks(seed, n):
+        g = f[:len(x)]
+        np.right_shift(x, np.uint64(40), out=x)
+        g[:] = x
+        np.multiply(g, 2.0 ** -23, out=g)
+        np.subtract(g, 1.0, out=g)
+        v[lo:lo + len(x)] = g
     return _place(v.reshape(rows, cols), ld)
 
 
@@ -59,24 +86,26 @@ def normal(seed: int, rows: int, cols: int, ld: int | None = None) -> np.ndarray
     """rows x cols float32 matrix, i.i.d. N(0, 1) by FP64 Box-Muller."""
     n = rows * cols
     pairs = (n + 1) // 2
-    x = splitmix64(seed, 2 * pairs)
-    u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
-    u2 = (x[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
-    r = np.sqrt(-2.0 * np.log(u1))
-    t = 2.0 * np.pi * u2
-    z = np.empty(2 * pairs, dtype=np.float64)
-    z[0::2] = r * np.cos(t)
-    z[1::2] = r * np.sin(t)
-    return _place(z[:n].astype(np.float32).reshape(rows, cols), ld)
+    z = np.empty(2 * pairs, dtype=np.float32)
+    for lo, x in _chunks(seed, 2 * pairs):  # _CHUNK is even: chunks hold whole pairs
+        u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+        u2 = (x[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        r = np.sqrt(-2.0 * np.log(u1))
+        t = 2.0 * np.pi * u2
+        z[lo:lo + len(x):2] = r * np.cos(t)
+        z[lo + 1:lo + len(x):2] = r * np.sin(t)
+    return _place(z[:n].reshape(rows, cols), ld)
 
 
 def small_int(seed: int, rows: int, cols: int, lo: int = -8, hi: int = 8,
               ld: int | None = None) -> np.ndarray:
     """Integers uniform on [lo, hi] stored as float32 (exact in TF32 and FP32)."""
-    x = splitmix64(seed, rows * cols)
+    n = rows * cols
     span = np.uint64(hi - lo + 1)
-    v = ((x >> np.uint64(32)) % span).astype(np.int64) + lo
-    return _place(v.astype(np.float32).reshape(rows, cols), ld)
+    v = np.empty(n, dtype=np.float32)
+    for c0, x in _chunks(seed, n):
+        v[c0:c0 + len(x)] = ((x >> np.uint64(32)) % span).astype(np.int64) + lo
+    return _place(v.reshape(rows, cols), ld)
 
 
 def _place(M: np.ndarray, ld: int | None) -> np.ndarray:

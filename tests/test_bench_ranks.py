@@ -60,14 +60,17 @@ def test_reference_arm_other_ranks_exit_quietly():
 
 def test_reference_arm_json_line():
     # The reference arm (the CPU oracle on this host's cores) prints one JSON
-    # line with the contract's keys; a few seconds of work here.
+    # line with the contract's keys; a few seconds of work here (on the 1024^3
+    # workload: the large squares' operands alone take minutes to page in on
+    # some hosts).
     import json
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
     r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
-                        "--warmup", "3", "--ref-seconds", "3"], env=env, capture_output=True, text=True,
+                        "--warmup", "3", "--ref-seconds", "3", "--workload", "square_1024"], env=env,
+                       capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
@@ -79,4 +82,4 @@ def test_reference_arm_json_line():
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["unit"] == d["unit"]
-    assert "workload" in d["config"]
+    assert d["config"]["workload"].startswith("square 1024: 1024x1024x1024")

@@ -1,0 +1,142 @@
+"""CTA pairs (tile_m = 256): one tcgen05.mma.cta_group::2 per 256 x BN tile.
+
+Each CTA of the pair stages its own 128 rows of A and half of the tile's B
+columns, converts them (3xTF32 split inside the kernel), and the even CTA's
+MMA thread multiplies the pair's operands out of both CTAs' shared memory
+into both CTAs' TMEM.  Checked against the FP64 oracle with the FP32 bound,
+on ragged shapes (a pair's second tile row past M, partial B boxes past N, K
+not a multiple of the stage depth), whole tiles and K-slices, several units
+per pair, both stage depths and tile widths; exact on small integers;
+deterministic; a withheld stage must time out on both CTAs and leave the
+context usable.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import software_pipelined_gb300 as g
+from software_pipelined_gb300 import inputs
+
+from gpu_util import check_against_oracle, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+PAIR = dict(variant=g.VARIANT_TCGEN05, tile_m=256)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from software_pipelined_gb300 import build
+    build.build()
+    g.load()
+
+
+def _ldb(N):
+    return N + (-N % 4)  # raw B rows by TMA: 16-byte aligned
+
+
+CASES = [
+    # M, N, K, tile_n, tile_k, split_k
+    (512, 512, 256, 256, 32, 2),
+    (512, 512, 256, 128, 32, 1),
+    (300, 520, 264, 256, 32, 2),     # second tile row of the last pair past M; N and K ragged
+    (300, 520, 264, 128, 16, 3),
+    (1024, 1024, 1024, 256, 16, 4),  # the 1024^3 shape, 64 pairs
+    (1024, 1024, 1024, 256, 32, 4),
+    (1024, 1024, 1024, 128, 32, 2),
+    (2048, 2048, 256, 128, 32, 1),   # 128 pair tiles: several units per pair, two accumulators
+    (2048, 2048, 256, 256, 32, 1),   # 64 pair tiles of 256: one accumulator, the MMA waits for the epilogue
+    (2304, 4096, 320, 256, 32, 0),   # 144 pair tiles: a partial last wave split automatically
+    (130, 33, 96, 128, 32, 2),       # one pair, most of it past M and N
+]
+IDS = [f"{m}x{n}x{k}_bn{bn}_k{bk}_s{s}" for m, n, k, bn, bk, s in CASES]
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_pair_matches_the_oracle(case):
+    M, N, K, bn, bk, split = case
+    A = inputs.uniform_pm1(2101, M, K)
+    B = inputs.normal(2102, K, N)
+    C, desc, canaries, outs = run_gemm(A, B, ldb=_ldb(N), repeat=2, tile_n=bn, tile_k=bk, split_k=split, **PAIR)
+    assert "cta-pair" in desc and f"tile=256x{bn}x{bk}" in desc, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+    assert np.array_equal(outs[0], outs[1]), desc
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[4]], ids=[IDS[0], IDS[3], IDS[4]])
+def test_pair_small_integers_bit_exact(case):
+    M, N, K, bn, bk, split = case
+    A = inputs.small_int(2103, M, K, -4, 4)
+    B = inputs.small_int(2104, K, N, -4, 4)
+    C, desc, canaries, _ = run_gemm(A, B, ldb=_ldb(N), tile_n=bn, tile_k=bk, split_k=split, **PAIR)
+    assert canaries
+    assert np.array_equal(C, A.astype(np.float64) @ B.astype(np.float64)), desc
+
+
+def test_pair_padded_leading_dimensions_and_misaligned_fallback():
+    M, N, K = 520, 300, 200
+    A = inputs.uniform_pm1(2105, M, K)
+    B = inputs.uniform_pm1(2106, K, N)
+    # padded rows (multiples of 4): the pair kernel itself
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 8, ldb=N + 4, ldc=N + 3, tile_n=128, split_k=2, **PAIR)
+    err, ok = check_against_oracle(C, A, B)
+    assert "cta-pair" in desc and canaries and ok, f"{desc}: {err}"
+    # A's base 4 bytes off a 16-byte boundary: the one-CTA pre-pass form runs instead
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 8, ldb=N + 4, a_off=1, tile_n=128, split_k=2, **PAIR)
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+
+
+@pytest.mark.parametrize("opts", [
+    dict(operand_split=1), dict(operand_split=3), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=2),
+    dict(tile_n=64), dict(tile_k=64),
+], ids=["pre_pass", "hybrid", "stages", "separate_syncs", "cluster_sum", "bn64", "tile_k64"])
+def test_pair_refusals(opts):
+    with pytest.raises(g.GemmError) as e:
+        g.Plan(512, 512, 512, **dict(PAIR, **opts))
+    assert e.value.status in (g.ERR_UNSUPPORTED, g.ERR_INVALID_ARG)
+
+
+def test_pair_refuses_unaligned_leading_dimensions():
+    for lda, ldb in ((257, 512), (256, 514)):
+        with pytest.raises(g.GemmError):
+            g.Plan(512, 512, 256, lda, ldb, 512, **PAIR)
+
+
+def test_pair_withheld_stage_times_out_and_context_survives():
+    import torch
+    M, N, K = 512, 512, 512
+    A = inputs.uniform_pm1(2107, M, K)
+    B = inputs.uniform_pm1(2108, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    for withhold in (1, 3):
+        with g.Plan(M, N, K, tile_n=256, split_k=2, wait_timeout_cycles=1 << 22, debug_withhold_stage=withhold,
+                    **PAIR) as p:
+            p.run(dA, dB, dC)
+            assert p.check() == g.ERR_TIMEOUT
+    torch.cuda.synchronize()
+    dC.fill_(float("nan"))
+    with g.Plan(M, N, K, tile_n=256, split_k=2, **PAIR) as p:
+        p.run(dA, dB, dC)
+        assert p.check() == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
+def test_pair_launch_count_and_host_run():
+    import torch
+    M, N, K = 1024, 1024, 1024
+    A = inputs.uniform_pm1(2109, M, K)
+    B = inputs.uniform_pm1(2110, K, N)
+    with g.Plan(M, N, K, tile_n=256, split_k=4, **PAIR) as p:
+        assert g.gemm_f32_plan_kernel_launches(p.handle) == 2  # the pair kernel and the reduction
+        hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+        hC = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+        assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
+    err, ok = check_against_oracle(hC.numpy().astype(np.float64), A, B)
+    assert ok, err
