@@ -88,7 +88,12 @@ typedef enum {
  * field; gemm_f32_opts_init fills the defaults. */
 typedef struct {
     int32_t variant;        /* gemm_f32_variant */
-    int32_t tile_m;         /* output tile rows (SIMT: 32/64/128; TC: 128) */
+    int32_t tile_m;         /* output tile rows (SIMT: 32/64/128; TC: 128, or 256 = one tile per pair
+                               of CTAs, a thread-block cluster of two sharing each tcgen05.mma
+                               (cta_group::2): operands split in the kernel only, tile_n 128 or
+                               256, tile_k 32 or 16; needs K >= 32 and lda, ldb multiples of 4,
+                               else UNSUPPORTED; a base pointer of A or B that is not 16-byte
+                               aligned runs the one-CTA pre-pass form instead) */
     int32_t tile_n;         /* output tile cols (SIMT: 32/64/128; TC: 64/128/256) */
     int32_t stages;         /* pipeline depth (SIMT: 1..4; TC: 2..8) */
     int32_t split_k;        /* K splits, 1 = none (max 64) */

@@ -145,6 +145,18 @@ DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int sms)
 {
     DispatchChoice c{};
     c.variant = GEMM_F32_VARIANT_TCGEN05;
+    if (M >= 768 && N >= 768 && K >= 256 && M <= 3072 && N <= 3072) {
+        // Mid sizes: 256 x 256 tiles on CTA pairs, operands split in the kernel
+        // (measured on GB300: 1024^3 18.3 vs 19.0 us, 2048^3 72 vs 81 us for the
+        // best one-CTA plans); K-split to give each pair of SMs work.
+        c.tile_m = 256;
+        c.tile_n = 256;
+        c.tile_k = 32;
+        c.fused = kSplitInKernel;
+        const int64_t ptiles = ((M + 255) / 256) * ((N + 255) / 256);
+        c.split_k = ptiles >= sms / 4 ? 0 : auto_split(ptiles, K, 256, sms / 2);
+        return c;
+    }
     c.tile_m = 128;
     c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
     c.stages = 0;  // the depth compiled for that tile width
@@ -285,13 +297,17 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // forced tile_k of 16 selects that form.
             // tile_m 256: a pair of CTAs per 256-row tile (one tcgen05.mma
             // across both), operands split in the kernel only.
-            const bool pair = c.tile_m == 256;
+            bool pair = c.tile_m == 256;
+            if (pair && ((o.operand_split && o.operand_split != 2) || o.stages || o.separate_syncs ||
+                         o.split_reduce >= 2 || K < kTcFusedMinK || lda % 4 != 0 || ldb % 4 != 0)) {
+                // forced: refused; the dispatcher's choice: the one-CTA kernel
+                if (o.tile_m == 256) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                pair = false;
+                c.tile_m = 128;
+                c.fused = kSplitPrepass;
+                c.tile_k = 0;
+            }
             if (pair) {
-                if ((o.operand_split && o.operand_split != 2) || o.stages || o.separate_syncs ||
-                    o.split_reduce >= 2 || K < kTcFusedMinK || lda % 4 != 0 || ldb % 4 != 0) {
-                    delete p;
-                    return GEMM_F32_ERR_UNSUPPORTED;
-                }
                 const int pbk = o.tile_k ? o.tile_k : c.tile_k;
                 t.config_id = tc_find_pair_config(c.tile_n, pbk);
                 if (t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }

@@ -21,9 +21,11 @@
 // Synchronisation (every wait bounded; a CTA that gives up raises its own and
 // its peer's abort flag):
 //   full_a[s]  TMA of the CTA's raw A and B landed (local)
-//   rd[s]      every converter warp of the CTA holds its raw B (local)
-//   conv[s]    (even CTA) both CTAs' converters are done: counts 2 x 8 warps,
-//              the odd CTA's arriving remotely with release at cluster scope
+//   rd[s]      every converter warp (of the group on that stage) holds its
+//              raw B (local)
+//   conv[s]    (even CTA) both CTAs' converters are done: counts 2 x 4 warps
+//              (one group of each CTA), the odd CTA's arriving remotely with
+//              release at cluster scope
 //   empty[s]   the pair's MMAs of slot s completed: one commit, multicast to
 //              both CTAs
 //   tfull      accumulator complete: commit multicast to both CTAs
@@ -41,6 +43,7 @@ namespace {
 
 using namespace tc;
 constexpr int kPairConvWarps = 8;
+constexpr int kConvGroups = 2;                      // converter groups, on alternate stages
 constexpr int kPairConvThreads = kPairConvWarps * 32;
 constexpr int kPairThreads = 6 * 32 + kPairConvThreads;
 
@@ -61,11 +64,11 @@ struct PairLayout {
     // B_BYTES of slack after the barriers: every MMA operand read of the pair
     // stays inside this CTA's allocation even if one ran BH rows past a slot
     static constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + B_BYTES;
-    // At most 256 TMEM columns per CTA: two accumulators of BN columns when they
-    // fit, else one (the MMA of a CTA's next unit then waits for the epilogue).
-    static constexpr int TBUFS = 2 * BN <= 256 ? 2 : 1;
+    // Two accumulators of BN columns: a unit's epilogue drains one while the
+    // next unit's MMAs fill the other.
+    static constexpr int TBUFS = 2;
     static constexpr uint32_t TMEM_COLS = TBUFS * BN;
-    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 256 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM cols");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM cols");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(RING_BYTES >= 4 * 8192, "the ring holds the TMA-store staging");
 };
@@ -167,9 +170,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
             ptx::mbar_init(full_a(s), 1);
-            ptx::mbar_init(conv(s), 2 * kPairConvWarps);
+            ptx::mbar_init(conv(s), 2 * kPairConvWarps / kConvGroups);  // one group of each CTA
             ptx::mbar_init(empty(s), 1);
-            ptx::mbar_init(rd(s), kPairConvWarps);
+            ptx::mbar_init(rd(s), kPairConvWarps / kConvGroups);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull(b), 1);
@@ -323,24 +326,32 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if (stop && lane == 0) give_up();
     } else {
         // ------------------------------ converters ----------------------------
-        const int ct = threadIdx.x - 6 * 32;    // 0 .. kPairConvThreads-1
-        constexpr int KG = KB / 4;              // 4-wide k groups per stage
-        constexpr int PARTS = kPairConvWarps / KG;  // warps per k group: they share the boxes
-        const int cw = (ct >> 5) % KG;
-        const int part = (ct >> 5) / KG;
+        // Two groups of warps take alternate stages, so that one group's
+        // per-stage synchronisation (the raw-B hand-over, the proxy fence, the
+        // release to the even CTA) overlaps the other group's conversion.
+        constexpr int GW = kPairConvWarps / kConvGroups;  // warps per group
+        constexpr int KG = KB / 4;                         // 4-wide k groups per stage
+        constexpr int NBOX = L::BH / 32;                   // raw-B boxes per stage
+        constexpr int PER = KG * NBOX / GW;                // (k group, box) pairs per warp
+        static_assert(PER >= 1 && PER * GW == KG * NBOX, "converter work split");
+        const int ct = threadIdx.x - 6 * 32;  // 0 .. kPairConvThreads-1
+        const int grp = (ct >> 5) / GW, gw = (ct >> 5) % GW;
+        const int gt = ct - grp * GW * 32;    // thread index in the group
         uint32_t fills = 0;
         bool stop = false;
-        uint32_t box_off[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int k = cw * 4 + j;
-            box_off[j] = (uint32_t)(k * 128 + (((lane >> 2) ^ (k & 7)) << 4) + (lane & 3) * 4);
-        }
         for (int w = pair; w < num_work && !stop; w += npairs) {
             const Unit u = decode_unit(w, args);
             for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
+                if ((int)(fills % kConvGroups) != grp) continue;  // the other group's stage
                 const int s = fills % SLOTS;
                 const uint32_t ps = (fills / SLOTS) & 1u;
+                // The slot's previous use may belong to the other group, and its
+                // copy may land after this group's last one: wait until the MMAs
+                // released it, so that the parity wait below is for this use.
+                if (fills >= (uint32_t)SLOTS && !wait_phase(empty(s), ps ^ 1u, limit, abort_flag, args.status)) {
+                    stop = true;
+                    break;
+                }
                 if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
                     stop = true;
                     break;
@@ -349,23 +360,26 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 const uint8_t* a_raw = slot;
                 uint8_t* a_lo = slot + L::A_BYTES;
                 uint8_t* b_hi = slot + 2 * L::A_BYTES;
-                uint8_t* b_lo = b_hi + L::B_BYTES;  // holds raw B until every warp has read it
-                constexpr int NBW = L::BH / 32 / PARTS;  // boxes per warp
-                static_assert(NBW >= 1 && NBW * PARTS == L::BH / 32, "boxes per converter warp");
-                float v[NBW][4];
+                uint8_t* b_lo = b_hi + L::B_BYTES;  // holds raw B until every warp of the group has read it
+                // B: this warp's (k group, box) pairs into registers (row k of a
+                // box: chunk (lane/4) ^ (k%8), word lane%4), hi_B written at once.
+                float v[PER][4];
 #pragma unroll
-                for (int i = 0; i < NBW; ++i) {
-                    const int nb = part + i * PARTS;
+                for (int i = 0; i < PER; ++i) {
+                    const int pr = gw + i * GW, cw = pr % KG, nb = pr / KG;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        v[i][j] = *reinterpret_cast<const float*>(b_lo + nb * L::BOX_BYTES + box_off[j]);
+                    for (int j = 0; j < 4; ++j) {
+                        const int k = cw * 4 + j;
+                        v[i][j] = *reinterpret_cast<const float*>(
+                            b_lo + nb * L::BOX_BYTES + k * 128 + (((lane >> 2) ^ (k & 7)) << 4) + (lane & 3) * 4);
+                    }
                     *reinterpret_cast<float4*>(b_hi + pair_kmajor_off<KB>(nb * 32 + lane, cw)) =
                         make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(rd(s));
 #pragma unroll
-                for (int c = ct; c < L::A_BYTES / 16; c += kPairConvThreads) {
+                for (int c = gt; c < L::A_BYTES / 16; c += GW * 32) {
                     const float4 x = *reinterpret_cast<const float4*>(a_raw + c * 16);
                     *reinterpret_cast<float4*>(a_lo + c * 16) =
                         make_float4(lo_part(x.x), lo_part(x.y), lo_part(x.z), lo_part(x.w));
@@ -375,9 +389,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     break;
                 }
 #pragma unroll
-                for (int i = 0; i < NBW; ++i)
-                    *reinterpret_cast<float4*>(b_lo + pair_kmajor_off<KB>((part + i * PARTS) * 32 + lane, cw)) =
+                for (int i = 0; i < PER; ++i) {
+                    const int pr = gw + i * GW, cw = pr % KG, nb = pr / KG;
+                    *reinterpret_cast<float4*>(b_lo + pair_kmajor_off<KB>(nb * 32 + lane, cw)) =
                         make_float4(lo_part(v[i][0]), lo_part(v[i][1]), lo_part(v[i][2]), lo_part(v[i][3]));
+                }
                 ptx::fence_proxy_async_shared();  // generic-proxy writes -> the pair's tensor-core reads
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(conv(s), 0));

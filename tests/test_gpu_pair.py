@@ -48,7 +48,7 @@ CASES = [
     (1024, 1024, 1024, 256, 32, 4),
     (1024, 1024, 1024, 128, 32, 2),
     (2048, 2048, 256, 128, 32, 1),   # 128 pair tiles: several units per pair, two accumulators
-    (2048, 2048, 256, 256, 32, 1),   # 64 pair tiles of 256: one accumulator, the MMA waits for the epilogue
+    (2048, 4096, 256, 256, 32, 1),   # 128 pair tiles of 256: both accumulators of 256 columns in turn
     (2304, 4096, 320, 256, 32, 0),   # 144 pair tiles: a partial last wave split automatically
     (130, 33, 96, 128, 32, 2),       # one pair, most of it past M and N
 ]

@@ -298,7 +298,7 @@ def test_tail_wave_split(shape, bn):
     M, N, K = shape
     A = inputs.uniform_pm1(981, M, K)
     B = inputs.uniform_pm1(982, K, N)
-    C, desc, canaries, outs = run_gemm(A, B, repeat=2, variant=g.VARIANT_TCGEN05, tile_n=bn)
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn)
     assert "split=0x" not in desc, desc
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
@@ -492,7 +492,7 @@ def test_cluster_sum_matches_reduction_kernel(case):
     M, N, K, bn, split, mode = case
     A = inputs.uniform_pm1(1721, M, K)
     B = inputs.uniform_pm1(1722, K, N)
-    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=bn, split_k=split, operand_split=mode)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, split_k=split, operand_split=mode)
     Cc, dc, okc, _ = run_gemm(A, B, split_reduce=2, **opts)
     Ck, dk, okk, _ = run_gemm(A, B, split_reduce=1, **opts)
     assert "cluster-sum" in dc and "cluster-sum" not in dk
@@ -508,7 +508,7 @@ def test_cluster_sum_misaligned_fallback_and_padding():
     M, N, K = 512, 512, 512
     A = inputs.uniform_pm1(1723, M, K)
     B = inputs.uniform_pm1(1724, K, N)
-    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=4, operand_split=2, split_reduce=2)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=128, split_k=4, operand_split=2, split_reduce=2)
     C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, ldc=N + 5, a_off=1, c_off=3, **opts)
     assert canaries and "cluster-sum" in desc
     err, ok = check_against_oracle(C, A, B)
@@ -516,7 +516,7 @@ def test_cluster_sum_misaligned_fallback_and_padding():
 
 
 def test_cluster_sum_launch_count():
-    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=128, split_k=2, operand_split=2)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=128, split_k=2, operand_split=2)
     with g.Plan(1024, 1024, 1024, split_reduce=2, **opts) as p:
         assert "cluster-sum" in p.describe()
         assert p.kernel_launches == 1
@@ -564,7 +564,7 @@ def test_last_arriver_sum_matches_reduction_kernel(case):
     M, N, K, bn, split, mode = case
     A = inputs.uniform_pm1(1741, M, K)
     B = inputs.uniform_pm1(1742, K, N)
-    opts = dict(variant=g.VARIANT_TCGEN05, tile_n=bn, split_k=split, operand_split=mode)
+    opts = dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=bn, split_k=split, operand_split=mode)
     Cf, df, okf, runs = run_gemm(A, B, split_reduce=3, repeat=3, **opts)
     Ck, dk, okk, _ = run_gemm(A, B, split_reduce=1, **opts)
     assert "last-arriver-sum" in df and "last-arriver-sum" not in dk
