@@ -5,6 +5,7 @@
 // Double-Buffered GEMM", first paragraph): it picks the kernel, its tile, the
 // stage count and split-K per problem shape, from a table of timings measured on
 // GB300 (dispatch_table.inc) with a rule for shapes the table does not cover.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -34,6 +35,7 @@ struct DispatchChoice {
     int group;     // TC: tile-rows per raster group (0 = default)
     int tile_k;    // SIMT: K-tile depth (0 = compiled default)
     int k_slices;  // SIMT: K-slice groups inside the CTA (0 = 1)
+    int reduce;    // TC: how split tiles' K-slices are summed (the split_reduce option; 0 = kernel)
 };
 
 #include "dispatch_table.inc"
@@ -146,15 +148,25 @@ DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int sms)
     DispatchChoice c{};
     c.variant = GEMM_F32_VARIANT_TCGEN05;
     if (M >= 768 && N >= 768 && K >= 256 && M <= 3072 && N <= 3072) {
-        // Mid sizes: 256 x 256 tiles on CTA pairs, operands split in the kernel
-        // (measured on GB300: 1024^3 18.3 vs 19.0 us, 2048^3 72 vs 81 us for the
-        // best one-CTA plans); K-split to give each pair of SMs work.
+        // Mid sizes: 256-row tiles on CTA pairs, operands split in the kernel
+        // (measured on GB300 against the best one-CTA plans: 768^3 13.2 vs 18.0
+        // us, 1024^3 18.3 vs 19.0, 2048^3 72 vs 81); K-split so that the pairs
+        // fill the machine, with the tile width (256, or 128 on ties lost) that
+        // keeps the most pairs busy.
         c.tile_m = 256;
-        c.tile_n = 256;
         c.tile_k = 32;
         c.fused = kSplitInKernel;
-        const int64_t ptiles = ((M + 255) / 256) * ((N + 255) / 256);
-        c.split_k = ptiles >= sms / 4 ? 0 : auto_split(ptiles, K, 256, sms / 2);
+        int64_t best = -1;
+        for (const int bn : {256, 128}) {
+            const int64_t ptiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+            const int split = ptiles >= sms / 4 ? 1 : auto_split(ptiles, K, 256, sms / 2);
+            const int64_t busy = std::min<int64_t>(ptiles * split, sms / 2);
+            if (busy > best) {
+                best = busy;
+                c.tile_n = bn;
+                c.split_k = split == 1 ? 0 : split;
+            }
+        }
         return c;
     }
     c.tile_m = 128;
@@ -299,7 +311,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // across both), operands split in the kernel only.
             bool pair = c.tile_m == 256;
             if (pair && ((o.operand_split && o.operand_split != 2) || o.stages || o.separate_syncs ||
-                         o.split_reduce >= 2 || K < kTcFusedMinK || lda % 4 != 0 || ldb % 4 != 0)) {
+                         o.split_reduce == 3 || K < kTcFusedMinK || lda % 4 != 0 || ldb % 4 != 0)) {
                 // forced: refused; the dispatcher's choice: the one-CTA kernel
                 if (o.tile_m == 256) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
                 pair = false;
@@ -339,7 +351,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             t.timeout_cycles = o.wait_timeout_cycles;
             t.withhold_stage = o.debug_withhold_stage;
             t.tile_group = o.tile_group ? o.tile_group : c.group;
-            t.cluster_mode = o.split_reduce;
+            // the table's K-slice sum goes with its own split
+            t.cluster_mode = o.split_reduce ? o.split_reduce : o.split_k ? 0 : c.reduce;
             tc_configure(t, M, N, K, c.split_k);
             if ((o.split_reduce == 2 && t.cluster == 0) || (o.split_reduce == 3 && t.fixup == 0)) {
                 delete p;
@@ -368,9 +381,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             if (pair)
                 snprintf(p->desc, sizeof p->desc,
                          "tcgen05 3xtf32 in-kernel-split cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
-                         "whole=%d split=%dx%d resident=%d group=%d kp=%lld",
+                         "whole=%d split=%dx%d%s resident=%d group=%d kp=%lld",
                          t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
-                         t.split_tiles, t.splits, t.pair_slots, t.tile_group > 0 ? t.tile_group : 8,
+                         t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", t.pair_slots,
+                         t.tile_group > 0 ? t.tile_group : 8,
                          (long long)t.kp);
             else
                 snprintf(p->desc, sizeof p->desc,

@@ -264,10 +264,15 @@ void pair_configure(TcPlanState& t, int64_t M, int64_t N, int split_request)
         }
     }
     if (t.split_tiles == 0) t.kb_per_split = num_kb;
-    t.cluster = 0;
+    // Every tile in 2 or 4 K-slices: with the cluster sum asked for, the S
+    // pairs of a tile run as one cluster and sum the slices in distributed
+    // shared memory (no partial tiles, no reduction launch).
+    t.cluster = t.cluster_mode == 2 && t.dp_tiles == 0 && t.split_tiles > 0 && (t.splits == 2 || t.splits == 4)
+                    ? t.splits : 0;
     t.fixup = 0;
     t.sem_bytes = 0;
-    t.partial_bytes = t.split_tiles ? size_t(2) * t.split_tiles * t.splits * kBM * c.bn * sizeof(float) : 0;
+    t.partial_bytes = t.split_tiles && !t.cluster ? size_t(2) * t.split_tiles * t.splits * kBM * c.bn * sizeof(float)
+                                                 : 0;
 }
 
 }  // namespace
@@ -450,7 +455,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
                             cudaStream_t s)
 {
     const TcConfig& c = kTc[st.config_id].cfg;
-    if (a.cluster > 1 && !kTc[r.id].cluster_ok) return cudaErrorInvalidValue;
+    if (a.cluster > 1 && !kTc[r.id].cluster_ok && c.bm != 2 * kBM) return cudaErrorInvalidValue;
     if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
     if (c.bm == 2 * kBM) {

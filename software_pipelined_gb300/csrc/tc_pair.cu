@@ -58,8 +58,8 @@ struct PairLayout {
     static_assert(BH % 32 == 0 && B_BYTES == BH / 32 * BOX_BYTES, "raw B fills the lo_B part exactly");
     static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int RING_BYTES = SLOTS * SLOT_BYTES;
-    // full, rd, conv, empty per slot + tfull/tempty x2, drain, spare
-    static constexpr int NBARS = 4 * SLOTS + 6;
+    // full, rd, conv, empty per slot + tfull/tempty x2, drain, ready, recv, spare
+    static constexpr int NBARS = 4 * SLOTS + 8;
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     // B_BYTES of slack after the barriers: every MMA operand read of the pair
     // stays inside this CTA's allocation even if one ran BH rows past a slot
@@ -134,6 +134,115 @@ __device__ __forceinline__ PairUnit pair_unit(int w, const TcArgs& a, int rank)
     return r;
 }
 
+// The K-slice sum of a tile inside a cluster of S pairs (S = 2 or 4; the pairs
+// are the tile's S K-slices, slice z = cluster rank / 2).  The S CTAs holding
+// the same 128-row half h of the tile form a group; in it, slice z owns
+// quadrants (32-row blocks) z*4/S .. (z+1)*4/S - 1 and sums them.  Per
+// epilogue warp (quadrant q of this CTA's accumulator), once the accumulator
+// is complete (the ring is idle):
+//   * one thread tells every group member that this ring is free (`ready`,
+//     S arrivals);
+//   * a warp whose quadrant another slice owns stages it in the ring (32 x 32
+//     swizzled boxes) and, once every group member is ready, pushes it with
+//     one bulk copy into the owner's receive slot for this slice, completing
+//     on the owner's `recv` barrier (armed at start for all incoming bytes);
+//   * a warp of an owned quadrant waits for `recv`, adds the S slices in slice
+//     order (this slice's from TMEM; the order of the reduction kernel, so the
+//     same bits) and stores C.
+// Ring layout: the 4 - 4/S quadrants staged out, then (S-1) x 4/S received
+// blocks.  Every wait bounded; false means this warp gave up.
+template <int BN>
+struct PairSum {
+    static constexpr int QUAD_BYTES = 32 * BN * 4;
+    static constexpr __host__ __device__ int ring_bytes(int S) { return (4 - 4 / S + (S - 1) * (4 / S)) * QUAD_BYTES; }
+};
+
+template <int BN>
+__device__ bool pair_cluster_sum(const TcArgs& args, const CUtensorMap* tm_c, int tm, int tn, uint32_t taddr,
+                                 int quad, int lane, int z, int h, uint32_t ring, uint8_t* ring_ptr,
+                                 uint32_t ready_bar, uint32_t recv_bar, int64_t limit, volatile int* abort_flag)
+{
+    constexpr int QB = PairSum<BN>::QUAD_BYTES, NB = BN / 32;
+    const int S = args.cluster, qpo = 4 / S, own0 = z * qpo;
+    const int owner = quad / qpo;
+    const uint32_t recv = ring + (4 - qpo) * QB;
+    uint8_t* recv_ptr = ring_ptr + (4 - qpo) * QB;
+    if (quad == 0 && lane == 0)
+        for (int g = 0; g < S; ++g) ptx::mbar_arrive_cluster(ptx::mapa(ready_bar, (uint32_t)(2 * g + h)));
+    if (owner != z) {
+        const int slot = quad < own0 ? quad : quad - qpo;  // staging slot of this quadrant
+        uint8_t* stg_ptr = ring_ptr + slot * QB;
+#pragma unroll 1
+        for (int bx = 0; bx < NB; ++bx) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x16(taddr + bx * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+            ptx::tmem_ld_32x32b_x16(taddr + bx * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            ptx::tmem_wait_ld();
+            stage_row(stg_ptr + bx * 4096, lane, r);
+        }
+        ptx::fence_proxy_async_shared();  // generic-proxy writes -> the bulk copy's reads
+        __syncwarp();
+        int ok = 1;
+        if (lane == 0) {
+            ok = wait_phase_cluster(ready_bar, 0, limit, abort_flag, args.status);
+            if (ok) {
+                const int rs = (z < owner ? z : z - 1) * qpo + (quad - owner * qpo);  // owner's receive slot
+                const uint32_t dst = (uint32_t)(2 * owner + h);
+                ptx::bulk_copy_to_cluster(ptx::mapa(recv + rs * QB, dst), ring + slot * QB, (uint32_t)QB,
+                                          ptx::mapa(recv_bar, dst));
+            }
+        }
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+    if (!__all_sync(0xffffffffu, wait_phase_cluster(recv_bar, 0, limit, abort_flag, args.status))) return false;
+    const int i = quad - own0;
+    const int64_t grow = (int64_t)tm * kBM + quad * 32 + lane;
+    const bool vec = ((args.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(args.C) & 15) == 0);
+#pragma unroll 1
+    for (int bx = 0; bx < NB; ++bx) {
+        float acc[32];
+#pragma unroll 1
+        for (int sl = 0; sl < S; ++sl) {
+            if (sl == z) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[16];
+                    ptx::tmem_ld_32x32b_x16(taddr + bx * 32 + hh * 16, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        acc[hh * 16 + c] = sl == 0 ? __uint_as_float(r[c]) : acc[hh * 16 + c] + __uint_as_float(r[c]);
+                }
+            } else {
+                const uint8_t* row = recv_ptr + ((sl < z ? sl : sl - 1) * qpo + i) * QB + bx * 4096 + lane * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 t = *reinterpret_cast<const float4*>(row + ((q ^ (lane & 7)) << 4));
+                    if (sl == 0) {
+                        acc[4 * q] = t.x; acc[4 * q + 1] = t.y; acc[4 * q + 2] = t.z; acc[4 * q + 3] = t.w;
+                    } else {
+                        acc[4 * q] += t.x; acc[4 * q + 1] += t.y; acc[4 * q + 2] += t.z; acc[4 * q + 3] += t.w;
+                    }
+                }
+            }
+        }
+        const int64_t gcol = (int64_t)tn * BN + bx * 32;
+        if (grow < args.M && gcol < args.N) {
+            float* dst = args.C + grow * args.ldc + gcol;
+            if (vec && gcol + 31 < args.N) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4*>(dst + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (gcol + c < args.N) dst[c] = acc[c];
+            }
+        }
+    }
+    return true;
+}
+
 template <int BN, int SLOTS, int KB>
 __global__ void __launch_bounds__(kPairThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -152,7 +261,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the pair's MMAs
+    // The cluster is one pair, or (the K-slice sum in distributed shared
+    // memory) the S pairs of a tile's S K-slices: cluster rank = 2 x slice + rank
+    // in the pair.  The pair's even CTA issues its MMAs.
+    const uint32_t crank = ptx::cluster_ctarank();
+    const uint32_t rank = crank & 1u, lead = crank & ~1u;
+    const uint16_t pair_mask = (uint16_t)(3u << lead);
+    const bool clustered = args.cluster > 1;
     auto full_a = [&](int s) { return ptx::smem_u32(bars + s); };
     auto conv = [&](int s) { return ptx::smem_u32(bars + SLOTS + s); };
     auto empty = [&](int s) { return ptx::smem_u32(bars + 2 * SLOTS + s); };
@@ -160,8 +275,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     auto tfull = [&](int b) { return ptx::smem_u32(bars + 4 * SLOTS + b); };
     auto tempty = [&](int b) { return ptx::smem_u32(bars + 4 * SLOTS + 2 + b); };
     const uint32_t drain_bar = ptx::smem_u32(bars + 4 * SLOTS + 4);
+    const uint32_t ready_bar = ptx::smem_u32(bars + 4 * SLOTS + 5);  // cluster sum: the group's rings are idle
+    const uint32_t recv_bar = ptx::smem_u32(bars + 4 * SLOTS + 6);   // cluster sum: the owned blocks landed
     // the abort flag of the peer CTA (shared::cluster address)
-    const uint32_t peer_abort = ptx::mapa(ptx::smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+    const uint32_t peer_abort = ptx::mapa(ptx::smem_u32(const_cast<int*>(abort_flag)), crank ^ 1u);
     auto give_up = [&]() {
         *abort_flag = 1;
         ptx::st_cluster_u32(peer_abort, 1u);
@@ -179,6 +296,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             ptx::mbar_init(tempty(b), 8);
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(ready_bar, clustered ? args.cluster : 1);
+        ptx::mbar_init(recv_bar, 1);
+        // the S-1 other slices' blocks of this CTA's owned quadrants complete the one phase
+        if (clustered)
+            ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((args.cluster - 1) * PairSum<BN>::QUAD_BYTES * 4 /
+                                                            args.cluster));
         *abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -287,13 +410,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                                                pair_kmajor_desc<KB>(b_hi + off), idesc, acc);
                         }
                     }
-                    ptx::mma_commit_pair(empty(s), 0x3);  // both CTAs' slot s free once these finish
+                    ptx::mma_commit_pair(empty(s), pair_mask);  // both CTAs' slot s free once these finish
                 }
                 if (stop) break;
-                ptx::mma_commit_pair(tfull(buf), 0x3);  // both CTAs' accumulators complete
+                ptx::mma_commit_pair(tfull(buf), pair_mask);  // both CTAs' accumulators complete
             }
             if (stop) give_up();
-            ptx::mma_commit_pair(drain_bar, 0x1);
+            ptx::mma_commit_pair(drain_bar, (uint16_t)(1u << lead));
             const long long t0 = clock64();
             while (!ptx::mbar_try_wait(drain_bar, 0))
                 if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
@@ -302,7 +425,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     } else if (warp < 6) {
         // ------------------------------ epilogue ------------------------------
         const int quad = warp & 3;
-        const uint32_t lead_tempty0 = ptx::mapa(tempty(0), 0), lead_tempty1 = ptx::mapa(tempty(1), 0);
+        const uint32_t lead_tempty0 = ptx::mapa(tempty(0), lead), lead_tempty1 = ptx::mapa(tempty(1), lead);
         int iter = 0;
         bool stop = false;
         for (int w = pair; w < num_work; w += npairs, ++iter) {
@@ -315,10 +438,18 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             }
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + buf * BN;
-            const EpilogueBars eb{drain_bar, drain_bar, drain_bar, drain_bar, drain_bar};  // unused: no cluster sum
-            drain_unit<BN, L::RING_BYTES>(args, &tm_c, &tm_p, pu.u, pu.tm, pu.tn, taddr, quad, lane,
-                                          w + npairs >= num_work, false, false, ring, ring_ptr, eb, limit,
-                                          abort_flag);
+            if (clustered) {
+                if (!pair_cluster_sum<BN>(args, &tm_c, pu.tm, pu.tn, taddr, quad, lane, (int)(crank >> 1),
+                                          (int)rank, ring, ring_ptr, ready_bar, recv_bar, limit, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+            } else {
+                const EpilogueBars eb{drain_bar, drain_bar, drain_bar, drain_bar, drain_bar};  // unused
+                drain_unit<BN, L::RING_BYTES>(args, &tm_c, &tm_p, pu.u, pu.tm, pu.tn, taddr, quad, lane,
+                                              w + npairs >= num_work, false, false, ring, ring_ptr, eb, limit,
+                                              abort_flag);
+            }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(buf ? lead_tempty1 : lead_tempty0);
@@ -396,7 +527,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
                 ptx::fence_proxy_async_shared();  // generic-proxy writes -> the pair's tensor-core reads
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(conv(s), 0));
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(conv(s), lead));
             }
         }
         if (stop && lane == 0) give_up();
@@ -469,9 +600,14 @@ cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMa
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
-    const int pairs = work < st.pair_slots ? work : st.pair_slots;
+    // cluster sum: every pair its one unit, the S pairs of a tile one cluster
+    const int pairs = a.cluster > 1 ? work : (work < st.pair_slots ? work : st.pair_slots);
     if (pairs < 1) return cudaErrorInvalidValue;
-    return launch_pdl(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s, 2, ta, tb,
+    if (a.cluster > 1 && (a.dp_tiles != 0 || a.splits != a.cluster ||
+                          PairSum<BN>::ring_bytes(a.cluster) > L::RING_BYTES))
+        return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s, a.cluster > 1 ? 2 * a.cluster : 2,
+                      ta, tb,
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
 }

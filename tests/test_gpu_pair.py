@@ -92,9 +92,9 @@ def test_pair_padded_leading_dimensions_and_misaligned_fallback():
 
 
 @pytest.mark.parametrize("opts", [
-    dict(operand_split=1), dict(operand_split=3), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=2),
+    dict(operand_split=1), dict(operand_split=3), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=3),
     dict(tile_n=64), dict(tile_k=64),
-], ids=["pre_pass", "hybrid", "stages", "separate_syncs", "cluster_sum", "bn64", "tile_k64"])
+], ids=["pre_pass", "hybrid", "stages", "separate_syncs", "last_arriver", "bn64", "tile_k64"])
 def test_pair_refusals(opts):
     with pytest.raises(g.GemmError) as e:
         g.Plan(512, 512, 512, **dict(PAIR, **opts))
@@ -140,3 +140,62 @@ def test_pair_launch_count_and_host_run():
         assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
     err, ok = check_against_oracle(hC.numpy().astype(np.float64), A, B)
     assert ok, err
+
+
+# ---------------------------------------------------------------------------
+# K-slices of a pair tile summed inside a cluster of S pairs (split_reduce 2):
+# the slices' order of the reduction kernel, so the same bits.
+# ---------------------------------------------------------------------------
+
+CLUSTER_CASES = [
+    # M, N, K, tile_n, tile_k, split_k
+    (1024, 1024, 1024, 256, 32, 4),  # the 1024^3 plan: 16 clusters of 8 CTAs
+    (1024, 1024, 1024, 256, 16, 4),
+    (512, 512, 512, 128, 32, 2),     # clusters of 4
+    (300, 520, 264, 256, 32, 2),     # ragged: quadrants past M, a tile column past N
+    (520, 300, 200, 128, 16, 4),
+]
+CLUSTER_IDS = [f"{m}x{n}x{k}_bn{bn}_k{bk}_s{s}" for m, n, k, bn, bk, s in CLUSTER_CASES]
+
+
+@pytest.mark.parametrize("case", CLUSTER_CASES, ids=CLUSTER_IDS)
+def test_pair_cluster_sum_matches_reduction_kernel(case):
+    M, N, K, bn, bk, split = case
+    A = inputs.uniform_pm1(2111, M, K)
+    B = inputs.normal(2112, K, N)
+    opts = dict(PAIR, tile_n=bn, tile_k=bk, split_k=split)
+    Cc, dc, okc, runs = run_gemm(A, B, ldb=_ldb(N), repeat=2, split_reduce=2, **opts)
+    Ck, dk, okk, _ = run_gemm(A, B, ldb=_ldb(N), split_reduce=1, **opts)
+    assert "cluster-sum" in dc and "cluster-sum" not in dk, dc
+    assert okc and okk
+    assert np.array_equal(runs[0], runs[1]), dc
+    assert np.array_equal(Cc, Ck), dc
+    err, ok = check_against_oracle(Cc, A, B)
+    assert ok, f"{dc}: {err}"
+
+
+def test_pair_cluster_sum_launch_count_and_refusals():
+    with g.Plan(1024, 1024, 1024, tile_n=256, split_k=4, split_reduce=2, **PAIR) as p:
+        assert g.gemm_f32_plan_kernel_launches(p.handle) == 1  # no reduction kernel
+    for kw in (dict(split_k=3), dict(split_k=1), dict(split_k=0)):
+        with pytest.raises(g.GemmError):
+            g.Plan(2048, 2048, 1024, tile_n=256, split_reduce=2, **dict(PAIR, **kw))
+
+
+def test_pair_cluster_sum_withheld_stage_times_out():
+    import torch
+    M, N, K = 512, 512, 512
+    A = inputs.uniform_pm1(2113, M, K)
+    B = inputs.uniform_pm1(2114, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    with g.Plan(M, N, K, tile_n=256, split_k=2, split_reduce=2, wait_timeout_cycles=1 << 22,
+                debug_withhold_stage=2, **PAIR) as p:
+        p.run(dA, dB, dC)
+        assert p.check() == g.ERR_TIMEOUT
+    torch.cuda.synchronize()
+    with g.Plan(M, N, K, tile_n=256, split_k=2, split_reduce=2, **PAIR) as p:
+        p.run(dA, dB, dC)
+        assert p.check() == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
