@@ -147,26 +147,18 @@ DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int sms)
 {
     DispatchChoice c{};
     c.variant = GEMM_F32_VARIANT_TCGEN05;
-    if (M >= 768 && N >= 768 && K >= 256 && M <= 3072 && N <= 3072) {
-        // Mid sizes: 256-row tiles on CTA pairs, operands split in the kernel
-        // (measured on GB300 against the best one-CTA plans: 768^3 13.2 vs 18.0
-        // us, 1024^3 18.3 vs 19.0, 2048^3 72 vs 81); K-split so that the pairs
-        // fill the machine, with the tile width (256, or 128 on ties lost) that
-        // keeps the most pairs busy.
+    if (M >= 1024 && N >= 1024 && K >= 256 && M <= 3072 && N <= 3072) {
+        // Mid sizes: 256 x 256 tiles on CTA pairs, operands split in the kernel
+        // (measured on GB300 against the best one-CTA plans: 1024^3 18.4 vs 19.2
+        // us, 1280^3 26.1 vs 29.1, 1536^3 36.6 vs 41.3, 2048^3 73 vs 81-101,
+        // 2048x3072x4096 216 vs 253; below 1024 the one-CTA kernel wins); K-split
+        // so that the pairs fill the machine.
         c.tile_m = 256;
+        c.tile_n = 256;
         c.tile_k = 32;
         c.fused = kSplitInKernel;
-        int64_t best = -1;
-        for (const int bn : {256, 128}) {
-            const int64_t ptiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
-            const int split = ptiles >= sms / 4 ? 1 : auto_split(ptiles, K, 256, sms / 2);
-            const int64_t busy = std::min<int64_t>(ptiles * split, sms / 2);
-            if (busy > best) {
-                best = busy;
-                c.tile_n = bn;
-                c.split_k = split == 1 ? 0 : split;
-            }
-        }
+        const int64_t ptiles = ((M + 255) / 256) * ((N + 255) / 256);
+        c.split_k = ptiles >= sms / 4 ? 0 : auto_split(ptiles, K, 256, sms / 2);
         return c;
     }
     c.tile_m = 128;

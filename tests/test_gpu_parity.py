@@ -535,7 +535,7 @@ def test_cluster_sum_launch_count():
 ], ids=["three_slices", "eight_slices", "wide_tiles", "one_stage", "no_split", "too_many"])
 def test_cluster_sum_refusals(shape, opts):
     with pytest.raises(g.GemmError) as e:
-        g.Plan(*shape, variant=g.VARIANT_TCGEN05, split_reduce=2, **opts)
+        g.Plan(*shape, variant=g.VARIANT_TCGEN05, tile_m=128, split_reduce=2, **opts)
     assert e.value.status == g.ERR_UNSUPPORTED
 
 
