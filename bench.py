@@ -448,7 +448,11 @@ def run_gpu_arm(args):
     simt_main = big["plan"].describe().startswith("simt")
     peak = pk["f32_simt_tflops_nominal"] if simt_main else pk["f32_3xtf32_tflops_burst"]
     kern_hash = source_hash([os.path.join(ROOT, "software_pipelined_gb300", "csrc", f)
-                             for f in ("tc_kernels.cuh", "tc_common.cuh", "ptx.cuh")])
+                             for f in ("tc_kernels.cuh", "tc_pair.cu", "tc_common.cuh", "ptx.cuh")])
+    big_desc = big["plan"].describe()
+    kname = ("simt_gemm_kernel (FFMA)" if simt_main else
+             "tc_pair_kernel (tcgen05 3xTF32 main GEMM on CTA pairs)" if "cta-pair" in big_desc else
+             "tc_gemm_kernel (tcgen05 3xTF32 main GEMM)")
     traffic, traffic_src = traffic_for(kern_hash, {w["name"]: w["plan"].describe() for w in work})
     for w in work:
         t = traffic.get(w["name"]) if traffic else None
@@ -457,8 +461,7 @@ def run_gpu_arm(args):
     roofline = {"bound": "alu" if simt_main else "tensor", "achieved": achieved, "peak": round(peak, 2),
                 "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": per_kernel[big["name"]]["dram_bytes_per_launch"],
-                "kernel": (f"simt_gemm_kernel (FFMA), {big['name']} launches" if simt_main else
-                           f"tc_gemm_kernel (tcgen05 3xTF32 main GEMM), {big['name']} launches"),
+                "kernel": f"{kname}, {big['name']} launches",
                 "peak_basis": ("nominal FP32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz" if simt_main else
                                f"of {pk['source']}: burst bf16 x {TF32_OVER_BF16:.4f} (nominal tf32/bf16) / 3"),
                 "frac_of_sustained_peak": round(achieved / pk["f32_3xtf32_tflops_sustained"], 4),

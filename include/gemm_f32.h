@@ -126,7 +126,8 @@ typedef struct {
     int32_t host_panels;    /* TC only, gemm_f32_run_host: row panels the host-buffer run is
                                pipelined over (A panel copies, panel GEMMs and C panel
                                copies overlap); 0 = the dispatcher's choice, 1 = none,
-                               n = n panels of whole 128-row tiles (at most 64) */
+                               n = n panels of whole tiles (128 rows; 256 for CTA-pair plans;
+                               at most 64) */
     int32_t split_reduce;   /* TC only: how the K-slices of split tiles are summed.  0 = the
                                dispatcher's choice (1: measured fastest); 1 = a
                                reduction kernel over partial tiles in scratch; 3 = no extra

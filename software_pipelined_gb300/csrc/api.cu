@@ -301,9 +301,14 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // forced tile_k of 16 selects that form.
             // tile_m 256: a pair of CTAs per 256-row tile (one tcgen05.mma
             // across both), operands split in the kernel only.
+            // operand_split 3 (B by the pre-pass) asks for the pairs' hybrid form
             bool pair = c.tile_m == 256;
-            if (pair && ((o.operand_split && o.operand_split != 2) || o.stages || o.separate_syncs ||
-                         o.split_reduce == 3 || K < kTcFusedMinK || lda % 4 != 0 || ldb % 4 != 0)) {
+            const int pair_split = o.operand_split == 3 ? kSplitHybrid
+                                   : o.operand_split ? kSplitInKernel
+                                                     : (c.fused == kSplitHybrid ? kSplitHybrid : kSplitInKernel);
+            if (pair && ((o.operand_split && o.operand_split != 2 && o.operand_split != 3) || o.stages ||
+                         o.separate_syncs || o.split_reduce == 3 || K < kTcFusedMinK || lda % 4 != 0 ||
+                         (pair_split == kSplitInKernel && ldb % 4 != 0))) {
                 // forced: refused; the dispatcher's choice: the one-CTA kernel
                 if (o.tile_m == 256) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
                 pair = false;
@@ -313,7 +318,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             }
             if (pair) {
                 const int pbk = o.tile_k ? o.tile_k : c.tile_k;
-                t.config_id = tc_find_pair_config(c.tile_n, pbk);
+                t.config_id = tc_find_pair_config(c.tile_n, pbk, pair_split);
                 if (t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
                 t.pair_slots = tc_pair_slots(c.tile_n, tc_config(t.config_id).bk, p->num_sms);
                 if (t.pair_slots < 1) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
@@ -372,9 +377,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             }
             if (pair)
                 snprintf(p->desc, sizeof p->desc,
-                         "tcgen05 3xtf32 in-kernel-split cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
+                         "tcgen05 3xtf32 %s cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
                          "whole=%d split=%dx%d%s resident=%d group=%d kp=%lld",
-                         t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
+                         tcfg.split == kSplitHybrid ? "hybrid-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
                          t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", t.pair_slots,
                          t.tile_group > 0 ? t.tile_group : 8,
                          (long long)t.kp);
@@ -455,13 +460,15 @@ bool current_device_is(int dev)
 // 1 = the plain copy-run-copy sequence.
 int host_panel_count(const gemm_f32_plan_s* p)
 {
-    if (p->kind != kTc || p->K == 0 || tc_config(p->tc.config_id).bm != 128) return 1;
+    if (p->kind != kTc || p->K == 0) return 1;
     int n = p->opts.host_panels;
     if (n == 0) {
         const int64_t waves = int64_t(p->tc.tiles_m) * p->tc.tiles_n / (p->num_sms > 0 ? p->num_sms : 1);
         n = waves >= 8 ? 6 : waves >= 2 ? 3 : waves >= 1 ? 2 : 1;
     }
-    if (n > p->tc.tiles_m) n = p->tc.tiles_m;
+    // whole tile rows per panel (two 128-row tiles for a CTA-pair plan)
+    const int tile_rows = p->tc.tiles_m / (tc_config(p->tc.config_id).bm / 128);
+    if (n > tile_rows) n = tile_rows;
     return n < 1 ? 1 : n;
 }
 
@@ -483,7 +490,7 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
 {
     if (!p->panels.empty() && p->panel_count == count) return cudaSuccess;
     drop_panels(p);
-    const int64_t rows = round_up((p->M + count - 1) / count, 128);
+    const int64_t rows = round_up((p->M + count - 1) / count, tc_config(p->tc.config_id).bm);
     size_t need = 0;
     cudaError_t e = cudaSuccess;
     for (int64_t r0 = 0; r0 < p->M; r0 += rows) {

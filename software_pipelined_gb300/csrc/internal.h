@@ -78,9 +78,10 @@ enum : int {
 int tc_num_configs();
 const TcConfig& tc_config(int id);
 int tc_find_config(int bn, int stages, bool sep, int split, int bk = 0);
-// The CTA-pair configuration (256-row tiles, operands split in the kernel) of
-// tile width bn and stage depth bk (0 = 32), or -1.
-int tc_find_pair_config(int bn, int bk);
+// The CTA-pair configuration (256-row tiles) of tile width bn, stage depth bk
+// (0 = 32) and split mode (kSplitInKernel, or kSplitHybrid: B by the
+// pre-pass), or -1.
+int tc_find_pair_config(int bn, int bk, int split = kSplitInKernel);
 // How many pairs of that configuration run at once on this device (0 when the
 // occupancy query fails).
 int tc_pair_slots(int bn, int bk, int sms);

@@ -614,8 +614,9 @@ cudaError_t tc_fused_main(int bn, int bk, bool b_presplit, const TcPlanState& st
 // The CTA-pair kernel (tc_pair.cu): 256 x bn tiles, operands split in the
 // kernel, stage depth bk; the work in a's dp_tiles / split_tiles counts pair
 // tiles.  And the sum of its split pair tiles' K-slices.
-cudaError_t tc_pair_main(int bn, int bk, const TcPlanState& st, const tc::TcArgs& a, const CUtensorMap& ta,
-                         const CUtensorMap& tb, cudaStream_t s);
+cudaError_t tc_pair_main(int bn, int bk, bool b_presplit, const TcPlanState& st, const tc::TcArgs& a,
+                         const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
+                         const CUtensorMap& tblo, cudaStream_t s);
 cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const tc::TcArgs& a, cudaStream_t s);
 
 }  // namespace gemm_f32

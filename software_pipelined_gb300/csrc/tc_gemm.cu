@@ -194,6 +194,10 @@ const TcEntry kTc[] = {
     {{256, 256, 16, 6, false, kSplitInKernel}, nullptr, launch_pair_reduce<256>, false, false},
     {{256, 128, 32, 4, false, kSplitInKernel}, nullptr, launch_pair_reduce<128>, false, false},
     {{256, 128, 16, 8, false, kSplitInKernel}, nullptr, launch_pair_reduce<128>, false, false},
+    // CTA pairs with B split by the pre-pass (each CTA loads its half of hi_B
+    // and lo_B), only lo_A computed in the kernel
+    {{256, 256, 32, 3, false, kSplitHybrid}, nullptr, launch_pair_reduce<256>, false, false},
+    {{256, 128, 32, 4, false, kSplitHybrid}, nullptr, launch_pair_reduce<128>, false, false},
 };
 
 }  // namespace
@@ -211,11 +215,11 @@ int tc_find_config(int bn, int stages, bool sep, int split, int bk)
     return -1;
 }
 
-int tc_find_pair_config(int bn, int bk)
+int tc_find_pair_config(int bn, int bk, int split)
 {
     for (int i = 0; i < tc_num_configs(); ++i) {
         const TcConfig& c = kTc[i].cfg;
-        if (c.bm == 2 * kBM && c.bn == bn && c.bk == (bk ? bk : kBK)) return i;
+        if (c.bm == 2 * kBM && c.bn == bn && c.bk == (bk ? bk : kBK) && c.split == split) return i;
     }
     return -1;
 }
@@ -359,8 +363,10 @@ cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K)
     if ((e = tc_set_partial(st, st.partial)) != cudaSuccess) return e;
     if ((e = encode_kmajor(st.tmap_a_hi, st.a_hi, M, st.kp, kBM)) != cudaSuccess) return e;
     if ((e = encode_kmajor(st.tmap_a_lo, st.a_lo, M, st.kp, kBM)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(st.tmap_b_hi, st.b_hi, N, st.kp, c.bn)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(st.tmap_b_lo, st.b_lo, N, st.kp, c.bn)) != cudaSuccess) return e;
+    // a CTA of a pair loads half of the tile's columns of the split B
+    const int64_t b_rows = c.bm == 2 * kBM ? c.bn / 2 : c.bn;
+    if ((e = encode_kmajor(st.tmap_b_hi, st.b_hi, N, st.kp, b_rows)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(st.tmap_b_lo, st.b_lo, N, st.kp, b_rows)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
@@ -459,8 +465,11 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
     if (c.bm == 2 * kBM) {
-        e = tc_pair_main(c.bn, c.bk, st, a, *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
-                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw), s);
+        e = tc_pair_main(c.bn, c.bk, c.split == kSplitHybrid, st, a,
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw),
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), s);
     } else if (r.in_kernel) {
         e = tc_fused_main(c.bn, c.bk, c.split == kSplitHybrid, st, a,
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
@@ -492,6 +501,11 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
         TcPlanState fb = st;
         fb.config_id = st.fallback_config_id;
         tc_configure(fb, M, N, K, st.split_request);
+        // the split B's maps with the one-CTA tile's rows
+        const int64_t bn = kTc[fb.config_id].cfg.bn;
+        cudaError_t e;
+        if ((e = encode_kmajor(fb.tmap_b_hi, fb.b_hi, N, fb.kp, bn)) != cudaSuccess) return e;
+        if ((e = encode_kmajor(fb.tmap_b_lo, fb.b_lo, N, fb.kp, bn)) != cudaSuccess) return e;
         return tc_launch(fb, M, N, K, A, lda, B, ldb, C, ldc, status, s, ev);
     }
     cudaError_t e = cudaSuccess;
@@ -551,6 +565,8 @@ cudaError_t tc_panel_run(const TcPlanState& panel, int64_t mp, int64_t N, int64_
                          cudaStream_t s)
 {
     const Route r = route(panel, A_panel, B);
+    // the panels' operands are the plan's own device buffers, 16-byte aligned
+    if (kTc[panel.config_id].cfg.bm == 2 * kBM && !r.in_kernel) return cudaErrorInvalidValue;
     cudaError_t e = prepass(panel, mp, N, K, A_panel, lda, B, ldb, r.pre_a, r.raw_a, false, s);
     if (e != cudaSuccess) return e;
     return main_and_reduce(panel, r, make_args(panel, mp, N, C_panel, ldc, status), nullptr, s);

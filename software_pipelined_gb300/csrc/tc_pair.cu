@@ -243,12 +243,18 @@ __device__ bool pair_cluster_sum(const TcArgs& args, const CUtensorMap* tm_c, in
     return true;
 }
 
-template <int BN, int SLOTS, int KB>
+// BPRE: B comes split and transposed by the pre-pass (hi and lo, K-major, by
+// TMA through tm_bhi / tm_blo: this CTA's half of the tile's columns) and the
+// converters only add lo_A; otherwise tm_b copies raw B boxes and the
+// converters split both operands.
+template <int BN, int SLOTS, int KB, bool BPRE>
 __global__ void __launch_bounds__(kPairThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
                const TcArgs args)
 {
+    static_assert(!BPRE || KB == 32, "pre-split B comes in 32-k rows");
     using L = PairLayout<BN, SLOTS, KB>;
     constexpr int HALVES = kBK / KB;  // stages per 32-k block of the work decomposition
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -307,7 +313,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tm_a);
-        ptx::tma_prefetch_desc(&tm_b);
+        if (BPRE) {
+            ptx::tma_prefetch_desc(&tm_bhi);
+            ptx::tma_prefetch_desc(&tm_blo);
+        } else {
+            ptx::tma_prefetch_desc(&tm_b);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
@@ -344,14 +355,23 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     if (fills == (uint32_t)args.withhold) continue;
                     const int kc = kh * KB;
                     const uint32_t slot = ring + s * L::SLOT_BYTES;
-                    // raw A (this CTA's 128 rows) into the A part, raw B boxes
-                    // (this CTA's half of the columns) into the lo_B part
-                    ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + L::B_BYTES);
-                    ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
+                    if constexpr (BPRE) {
+                        // raw A into the A part, this CTA's half of hi_B and lo_B
+                        ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + 2 * L::B_BYTES);
+                        ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
+                        const int n0 = pu.tn * BN + (int)rank * L::BH;
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES, &tm_bhi, full_a(s), kc, n0);
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, full_a(s), kc, n0);
+                    } else {
+                        // raw A (this CTA's 128 rows) into the A part, raw B boxes
+                        // (this CTA's half of the columns) into the lo_B part
+                        ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + L::B_BYTES);
+                        ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
 #pragma unroll
-                    for (int j = 0; j < L::BH / 32; ++j)
-                        ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES + j * L::BOX_BYTES, &tm_b, full_a(s),
-                                         pu.tn * BN + (int)rank * L::BH + 32 * j, kc);
+                        for (int j = 0; j < L::BH / 32; ++j)
+                            ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES + j * L::BOX_BYTES, &tm_b,
+                                             full_a(s), pu.tn * BN + (int)rank * L::BH + 32 * j, kc);
+                    }
                 }
             }
             if (stop) give_up();
@@ -495,6 +515,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 // B: this warp's (k group, box) pairs into registers (row k of a
                 // box: chunk (lane/4) ^ (k%8), word lane%4), hi_B written at once.
                 float v[PER][4];
+                if constexpr (!BPRE) {
 #pragma unroll
                 for (int i = 0; i < PER; ++i) {
                     const int pr = gw + i * GW, cw = pr % KG, nb = pr / KG;
@@ -509,21 +530,24 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(rd(s));
+                }
 #pragma unroll
                 for (int c = gt; c < L::A_BYTES / 16; c += GW * 32) {
                     const float4 x = *reinterpret_cast<const float4*>(a_raw + c * 16);
                     *reinterpret_cast<float4*>(a_lo + c * 16) =
                         make_float4(lo_part(x.x), lo_part(x.y), lo_part(x.z), lo_part(x.w));
                 }
-                if (!wait_phase(rd(s), ps, limit, abort_flag, args.status)) {
-                    stop = true;
-                    break;
-                }
+                if constexpr (!BPRE) {
+                    if (!wait_phase(rd(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
 #pragma unroll
-                for (int i = 0; i < PER; ++i) {
-                    const int pr = gw + i * GW, cw = pr % KG, nb = pr / KG;
-                    *reinterpret_cast<float4*>(b_lo + pair_kmajor_off<KB>(nb * 32 + lane, cw)) =
-                        make_float4(lo_part(v[i][0]), lo_part(v[i][1]), lo_part(v[i][2]), lo_part(v[i][3]));
+                    for (int i = 0; i < PER; ++i) {
+                        const int pr = gw + i * GW, cw = pr % KG, nb = pr / KG;
+                        *reinterpret_cast<float4*>(b_lo + pair_kmajor_off<KB>(nb * 32 + lane, cw)) =
+                            make_float4(lo_part(v[i][0]), lo_part(v[i][1]), lo_part(v[i][2]), lo_part(v[i][3]));
+                    }
                 }
                 ptx::fence_proxy_async_shared();  // generic-proxy writes -> the pair's tensor-core reads
                 __syncwarp();
@@ -591,12 +615,12 @@ int reduce_grid(int64_t work, int sms)
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
-template <int BN, int SLOTS, int KB>
+template <int BN, int SLOTS, int KB, bool BPRE>
 cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
-                        cudaStream_t s)
+                        const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
 {
     using L = PairLayout<BN, SLOTS, KB>;
-    auto kern = tc_pair_kernel<BN, SLOTS, KB>;
+    auto kern = tc_pair_kernel<BN, SLOTS, KB, BPRE>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
@@ -607,16 +631,16 @@ cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMa
                           PairSum<BN>::ring_bytes(a.cluster) > L::RING_BYTES))
         return cudaErrorInvalidValue;
     return launch_pdl(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s, a.cluster > 1 ? 2 * a.cluster : 2,
-                      ta, tb,
+                      ta, tb, tbhi, tblo,
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
 }
 
-template <int BN, int SLOTS, int KB>
+template <int BN, int SLOTS, int KB, bool BPRE>
 int pair_slots_for(int sms)
 {
     using L = PairLayout<BN, SLOTS, KB>;
-    auto kern = tc_pair_kernel<BN, SLOTS, KB>;
+    auto kern = tc_pair_kernel<BN, SLOTS, KB, BPRE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -642,13 +666,19 @@ int pair_slots_for(int sms)
 
 }  // namespace
 
-cudaError_t tc_pair_main(int bn, int bk, const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
-                         const CUtensorMap& tb, cudaStream_t s)
+cudaError_t tc_pair_main(int bn, int bk, bool b_presplit, const TcPlanState& st, const TcArgs& a,
+                         const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
+                         const CUtensorMap& tblo, cudaStream_t s)
 {
-    if (bn == 256 && bk == 32) return launch_pair<256, 3, 32>(st, a, ta, tb, s);
-    if (bn == 256 && bk == 16) return launch_pair<256, 6, 16>(st, a, ta, tb, s);
-    if (bn == 128 && bk == 32) return launch_pair<128, 4, 32>(st, a, ta, tb, s);
-    if (bn == 128 && bk == 16) return launch_pair<128, 8, 16>(st, a, ta, tb, s);
+    if (b_presplit) {
+        if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, true>(st, a, ta, tb, tbhi, tblo, s);
+        if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, true>(st, a, ta, tb, tbhi, tblo, s);
+        return cudaErrorInvalidValue;
+    }
+    if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, false>(st, a, ta, tb, tbhi, tblo, s);
+    if (bn == 256 && bk == 16) return launch_pair<256, 6, 16, false>(st, a, ta, tb, tbhi, tblo, s);
+    if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, false>(st, a, ta, tb, tbhi, tblo, s);
+    if (bn == 128 && bk == 16) return launch_pair<128, 8, 16, false>(st, a, ta, tb, tbhi, tblo, s);
     return cudaErrorInvalidValue;
 }
 
@@ -668,10 +698,11 @@ cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const TcArgs& a, cudaS
 
 int tc_pair_slots(int bn, int bk, int sms)
 {
-    if (bn == 256 && bk == 32) return pair_slots_for<256, 3, 32>(sms);
-    if (bn == 256 && bk == 16) return pair_slots_for<256, 6, 16>(sms);
-    if (bn == 128 && bk == 32) return pair_slots_for<128, 4, 32>(sms);
-    if (bn == 128 && bk == 16) return pair_slots_for<128, 8, 16>(sms);
+    // the same shared memory and threads for both forms of B
+    if (bn == 256 && bk == 32) return pair_slots_for<256, 3, 32, false>(sms);
+    if (bn == 256 && bk == 16) return pair_slots_for<256, 6, 16, false>(sms);
+    if (bn == 128 && bk == 32) return pair_slots_for<128, 4, 32, false>(sms);
+    if (bn == 128 && bk == 16) return pair_slots_for<128, 8, 16, false>(sms);
     return 0;
 }
 

@@ -80,6 +80,15 @@ def candidates(M, N, K):
                     if sp == 1 or K // sp >= 32:
                         out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp,
                                         tile_k=bk, k_slices=ksl))
+    if K >= 32 and macs >= 2 ** 27:
+        # CTA pairs (256-row tiles): operands split in the kernel, or B by the pre-pass
+        for bn in (256, 128):
+            for fused in (2, 3):
+                for tk in ((32, 16) if fused == 2 else (32,)):
+                    for sp in [0] + SPLITS:
+                        if sp <= 1 or (K + 31) // 32 >= sp:
+                            out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=256, tile_n=bn, stages=0,
+                                            split_k=sp, operand_split=fused, tile_k=tk))
     if K >= 16:
         for bn in TC_BN:
             for fused in ((1, 2, 3, 4) if bn in (128, 256) and K >= 32 else (1,)):
@@ -164,7 +173,7 @@ def write_inc(results, path):
         "// each benchmark shape (exact match on M, N, K), written by",
         "// software_pipelined_gb300/tune.py from its timing sweep.  Shapes not listed",
         "// fall back to the rule in choose().  Fields: variant (1 SIMT, 2 tcgen05),",
-        "// tile_m, tile_n, stages (0 = compiled default), split_k (0 = automatic",
+        "// tile_m (tcgen05: 256 = CTA pairs), tile_n, stages (0 = compiled default), split_k (0 = automatic",
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
         "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass,",
         "// 3 hi of A read from A),",

@@ -67,6 +67,40 @@ def test_pair_matches_the_oracle(case):
     assert np.array_equal(outs[0], outs[1]), desc
 
 
+HYBRID_CASES = [
+    # M, N, K, tile_n, split_k: B split by the pre-pass, only lo_A in the kernel
+    (512, 512, 256, 256, 2),
+    (300, 521, 264, 256, 2),      # ldb = 521: B needs no 16-byte rows here
+    (1024, 1024, 1024, 256, 4),
+    (2048, 2048, 256, 128, 1),    # several units per pair
+    (2304, 4096, 320, 256, 0),    # partial last wave split automatically
+]
+
+
+@pytest.mark.parametrize("case", HYBRID_CASES, ids=[f"{m}x{n}x{k}_bn{bn}_s{s}" for m, n, k, bn, s in HYBRID_CASES])
+def test_pair_hybrid_matches_the_oracle(case):
+    M, N, K, bn, split = case
+    A = inputs.uniform_pm1(2115, M, K)
+    B = inputs.normal(2116, K, N)
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, tile_n=bn, split_k=split, operand_split=3, **PAIR)
+    assert "hybrid-split cta-pair" in desc, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+    assert np.array_equal(outs[0], outs[1]), desc
+
+
+def test_pair_hybrid_small_integers_and_misaligned_fallback():
+    M, N, K = 520, 300, 200
+    A = inputs.small_int(2117, M, K, -4, 4)
+    B = inputs.small_int(2118, K, N, -4, 4)
+    exact = A.astype(np.float64) @ B.astype(np.float64)
+    C, desc, canaries, _ = run_gemm(A, B, tile_n=256, split_k=2, operand_split=3, **PAIR)
+    assert "hybrid-split cta-pair" in desc and canaries and np.array_equal(C, exact), desc
+    # A's base off a 16-byte boundary: the one-CTA pre-pass form (its own B maps)
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, a_off=1, tile_n=256, split_k=2, operand_split=3, **PAIR)
+    assert canaries and np.array_equal(C, exact), desc
+
+
 @pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[4]], ids=[IDS[0], IDS[3], IDS[4]])
 def test_pair_small_integers_bit_exact(case):
     M, N, K, bn, bk, split = case
@@ -92,9 +126,9 @@ def test_pair_padded_leading_dimensions_and_misaligned_fallback():
 
 
 @pytest.mark.parametrize("opts", [
-    dict(operand_split=1), dict(operand_split=3), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=3),
-    dict(tile_n=64), dict(tile_k=64),
-], ids=["pre_pass", "hybrid", "stages", "separate_syncs", "last_arriver", "bn64", "tile_k64"])
+    dict(operand_split=1), dict(operand_split=4), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=3),
+    dict(tile_n=64), dict(tile_k=64), dict(operand_split=3, tile_k=16),
+], ids=["pre_pass", "raw_a", "stages", "separate_syncs", "last_arriver", "bn64", "tile_k64", "hybrid_k16"])
 def test_pair_refusals(opts):
     with pytest.raises(g.GemmError) as e:
         g.Plan(512, 512, 512, **dict(PAIR, **opts))
@@ -199,3 +233,23 @@ def test_pair_cluster_sum_withheld_stage_times_out():
         assert p.check() == g.OK
     Cref, S = oracle.gemm_f64(A, B)
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
+@pytest.mark.parametrize("mode", [2, 3], ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("panels", [2, 3])
+def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels):
+    # Without a K-split every tile is summed in the same order whichever 256-row
+    # panel it falls in: the panel pipeline must reproduce the device run bit
+    # for bit (a wrong panel offset cannot hide in the bound).
+    import torch
+    M, N, K = 1536, 768, 320
+    A = inputs.normal(2119, M, K)
+    B = inputs.normal(2120, K, N)
+    hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+    hC = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    opts = dict(PAIR, tile_n=256, split_k=1, operand_split=mode)
+    with g.Plan(M, N, K, host_panels=panels, **opts) as p:
+        assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
+    C, desc, canaries, _ = run_gemm(A, B, host_panels=1, **opts)
+    assert canaries
+    assert np.array_equal(hC.numpy().astype(np.float64), C), desc
