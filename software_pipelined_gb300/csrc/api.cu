@@ -5,7 +5,6 @@
 // Double-Buffered GEMM", first paragraph): it picks the kernel, its tile, the
 // stage count and split-K per problem shape, from a table of timings measured on
 // GB300 (dispatch_table.inc) with a rule for shapes the table does not cover.
-#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
