@@ -573,7 +573,47 @@ __device__ __forceinline__ bool drain_unit(const TcArgs& args, const CUtensorMap
     return true;
 }
 
-// Launch with programmatic stream serialisation// Launch with programmatic stream serialisation: the kernel may start while
+// The K-slices of one float4 of a split tile, summed in slice order (so every
+// way of summing them gives the same bits), with the loads of up to four
+// slices in flight at once (the first, then three at a time).  p: slice 0;
+// STRIDE: float4 from one slice to the next.
+template <int STRIDE>
+__device__ __forceinline__ float4 sum_slices(const float4* __restrict__ p, int splits)
+{
+    float4 acc = __ldg(p);
+    for (int z = 1; z < splits; z += 3) {
+        float4 t[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (z + i < splits) t[i] = __ldg(p + (int64_t)(z + i) * STRIDE);
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (z + i < splits) {
+                acc.x += t[i].x; acc.y += t[i].y; acc.z += t[i].z; acc.w += t[i].w;
+            }
+    }
+    return acc;
+}
+
+// Reduction kernels: 192 threads of at most 42 registers (8 blocks per SM),
+// so one block (at most 8064 registers) fits beside a running 448-thread GEMM
+// CTA of 128 registers a thread.  Under programmatic serialisation the
+// reduction is then resident before the GEMM ends, and the next GEMM's CTAs
+// start their setup beside the reduction's last blocks.
+constexpr int kReduceThreads = 192;
+constexpr int kReduceBlocksPerSm = 8;
+
+// Blocks of a grid-stride reduction over `work` float4: a thread per float4
+// (its slices' loads all in flight at once), up to eight full residencies of
+// every SM; beyond that the threads loop.
+inline int reduce_blocks(int64_t work, int sms)
+{
+    const int64_t blocks = (work + kReduceThreads - 1) / kReduceThreads;
+    const int64_t cap = (int64_t)sms * kReduceBlocksPerSm * 8;
+    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while
 // the previous kernel on the stream finishes, and waits for it (griddepcontrol)
 // before touching that kernel's output.  cluster > 1: thread-block clusters of
 // that many consecutive CTAs (the grid is a multiple of it).

@@ -137,7 +137,7 @@ template <int BN>
 cudaError_t launch_reduce(const TcPlanState& st, const TcArgs& a, cudaStream_t s)
 {
     const int64_t total = (int64_t)a.split_tiles * kBM * (BN / 4);
-    return launch_pdl(tile_reduce_kernel<BN>, dim3(grid_cap(total, st.num_sms)), dim3(256), 0, s, 1,
+    return launch_pdl(tile_reduce_kernel<BN>, dim3(reduce_blocks(total, st.num_sms)), dim3(kReduceThreads), 0, s, 1,
                       reinterpret_cast<const float4*>(a.partial), a.dp_tiles, a.split_tiles, a.splits,
                       a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
 }

@@ -404,7 +404,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant
 // Sum the K-slices of every split tile in slice order and write the tile to C
 // (guarded).  Grid-stride over split_tiles x 128 x BN/4 float4 positions.
 template <int BN>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kReduceThreads, kReduceBlocksPerSm)
 tile_reduce_kernel(const float4* __restrict__ partial, int dp_tiles, int split_tiles, int splits,
                    int tiles_m, int tiles_n, int group, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
 {
@@ -424,11 +424,7 @@ tile_reduce_kernel(const float4* __restrict__ partial, int dp_tiles, int split_t
         const int64_t grow = (int64_t)tm * kBM + r, gcol = (int64_t)tn * BN + c;
         if (grow >= M || gcol >= N) continue;
         const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
-        float4 acc = __ldg(p);
-        for (int z = 1; z < splits; ++z) {
-            const float4 t = __ldg(p + (int64_t)z * PER_TILE);
-            acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
-        }
+        const float4 acc = sum_slices<PER_TILE>(p, splits);
         float* dst = C + grow * ldc + gcol;
         if (vec && gcol + 3 < N) {
             *reinterpret_cast<float4*>(dst) = acc;

@@ -573,7 +573,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 // x BN/4 float4 positions; tile j = 2q + r of the split tiles is row half r of
 // split pair tile q.
 template <int BN>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kReduceThreads, kReduceBlocksPerSm)
 pair_reduce_kernel(const float4* __restrict__ partial, int dp_pairs, int split_pairs, int splits, int tiles_m,
                    int tiles_n, int group, int64_t M, int64_t N, float* __restrict__ C, int64_t ldc)
 {
@@ -593,11 +593,7 @@ pair_reduce_kernel(const float4* __restrict__ partial, int dp_pairs, int split_p
         const int64_t grow = ((int64_t)2 * ptm + (j & 1)) * kBM + r, gcol = (int64_t)tn * BN + c;
         if (grow >= M || gcol >= N) continue;
         const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
-        float4 acc = __ldg(p);
-        for (int z = 1; z < splits; ++z) {
-            const float4 t = __ldg(p + (int64_t)z * PER_TILE);
-            acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
-        }
+        const float4 acc = sum_slices<PER_TILE>(p, splits);
         float* dst = C + grow * ldc + gcol;
         if (vec && gcol + 3 < N) {
             *reinterpret_cast<float4*>(dst) = acc;
@@ -606,13 +602,6 @@ pair_reduce_kernel(const float4* __restrict__ partial, int dp_pairs, int split_p
             for (int q = 0; q < 4 && gcol + q < N; ++q) dst[q] = v[q];
         }
     }
-}
-
-int reduce_grid(int64_t work, int sms)
-{
-    const int64_t blocks = (work + 255) / 256;
-    const int64_t cap = (int64_t)sms * 8;
-    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
 template <int BN, int SLOTS, int KB, bool BPRE>
@@ -685,13 +674,13 @@ cudaError_t tc_pair_main(int bn, int bk, bool b_presplit, const TcPlanState& st,
 cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const TcArgs& a, cudaStream_t s)
 {
     const int64_t total = (int64_t)2 * a.split_tiles * kBM * (bn / 4);
-    const dim3 grid(reduce_grid(total, st.num_sms));
+    const dim3 grid(reduce_blocks(total, st.num_sms));
     const float4* p = reinterpret_cast<const float4*>(a.partial);
     if (bn == 256)
-        return launch_pdl(pair_reduce_kernel<256>, grid, dim3(256), 0, s, 1, p, a.dp_tiles, a.split_tiles, a.splits,
+        return launch_pdl(pair_reduce_kernel<256>, grid, dim3(kReduceThreads), 0, s, 1, p, a.dp_tiles, a.split_tiles, a.splits,
                           a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
     if (bn == 128)
-        return launch_pdl(pair_reduce_kernel<128>, grid, dim3(256), 0, s, 1, p, a.dp_tiles, a.split_tiles, a.splits,
+        return launch_pdl(pair_reduce_kernel<128>, grid, dim3(kReduceThreads), 0, s, 1, p, a.dp_tiles, a.split_tiles, a.splits,
                           a.tiles_m, a.tiles_n, a.group, a.M, a.N, a.C, a.ldc);
     return cudaErrorInvalidValue;
 }
