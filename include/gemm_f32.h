@@ -144,6 +144,13 @@ typedef struct {
                                them and add their register tiles at the end (1, 2 or 4; 0 = the
                                dispatcher's choice): more warps per SM for small grids without a
                                second launch */
+    int32_t host_col_blocks; /* TC only, gemm_f32_run_host with two or more row panels: the
+                               first row panel runs as this many column blocks of whole tiles,
+                               B copied block by block, each block's GEMM starting as soon as
+                               its columns of B have landed (the GEMM starts after a fraction
+                               of B instead of all of it).  0 = the dispatcher's choice, 1 =
+                               none, at most 16; only for plans that split A inside the GEMM
+                               kernel (operand_split 2 or 3), otherwise as 1 */
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

@@ -72,6 +72,11 @@ struct gemm_f32_plan_s {
     // per landed operand (B, then every A panel) and per finished C panel
     std::vector<TcPlanState> panels;
     std::vector<int64_t> panel_r0;
+    // column blocks of the first row panel (host_col_blocks): state, first
+    // column; one event per landed B block and per finished C block
+    std::vector<TcPlanState> blocks;
+    std::vector<int64_t> block_c0;
+    int64_t block_width = 0;
     float* panel_partial = nullptr;
     int* panel_sem = nullptr;
     size_t panel_sem_bytes = 0;
@@ -125,6 +130,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.split_reduce < 0 || o.split_reduce > 3) return GEMM_F32_ERR_INVALID_ARG;
     if (!(o.k_slices == 0 || o.k_slices == 1 || o.k_slices == 2 || o.k_slices == 4)) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.host_col_blocks < 0 || o.host_col_blocks > 16) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -452,18 +458,34 @@ bool current_device_is(int dev)
     return cudaGetDevice(&d) == cudaSuccess && d == dev;
 }
 
+// Column blocks of the first row panel asked for (before rounding to whole
+// tiles): the option's count, else 3 from N = 6144 and 2 from N = 2048
+// (measured on GB300, pinned host memory at about 200 GB/s each way: 8192^3
+// 5.18 ms with 5 panels and 3 blocks against 6.04 ms with 6 panels and none;
+// 4096^3 1.08 ms with 3 panels and 2 blocks against 1.12 ms with none, 1.27
+// with 4).  Only for plans that split A inside the GEMM kernel (the first
+// panel's blocks would otherwise each repeat that panel's pre-pass of A).
+int host_col_request(const gemm_f32_plan_s* p)
+{
+    const TcConfig& c = tc_config(p->tc.config_id);
+    if (c.split != kSplitInKernel && c.split != kSplitHybrid) return 1;
+    const int q = p->opts.host_col_blocks;
+    return q != 0 ? q : p->N >= 6144 ? 3 : p->N >= 2048 ? 2 : 1;
+}
+
 // Row panels of the pipelined host-buffer run: the option's count, else a
 // count from the waves of output tiles (measured on GB300 with pinned host
 // memory at about 200 GB/s each way: 8192^3, 13 waves, is fastest with 6
-// panels; 4096^3, 3.4 waves, with 3); never more panels than tile-rows.
-// 1 = the plain copy-run-copy sequence.
+// panels, or 5 when the first panel runs in column blocks; 4096^3, 3.4
+// waves, with 3); never more panels than tile-rows.  1 = the plain
+// copy-run-copy sequence.
 int host_panel_count(const gemm_f32_plan_s* p)
 {
     if (p->kind != kTc || p->K == 0) return 1;
     int n = p->opts.host_panels;
     if (n == 0) {
         const int64_t waves = int64_t(p->tc.tiles_m) * p->tc.tiles_n / (p->num_sms > 0 ? p->num_sms : 1);
-        n = waves >= 8 ? 6 : waves >= 2 ? 3 : waves >= 1 ? 2 : 1;
+        n = waves >= 8 ? (host_col_request(p) > 1 ? 5 : 6) : waves >= 2 ? 3 : waves >= 1 ? 2 : 1;
     }
     // whole tile rows per panel (two 128-row tiles for a CTA-pair plan)
     const int tile_rows = p->tc.tiles_m / (tc_config(p->tc.config_id).bm / 128);
@@ -471,10 +493,24 @@ int host_panel_count(const gemm_f32_plan_s* p)
     return n < 1 ? 1 : n;
 }
 
+// Width of the first row panel's column blocks (whole tiles), 0 = no blocks
+// (fewer than two row panels, or one block).  Without blocks the copy of B,
+// 1.3 ms at 8192 x 8192, comes whole before the first GEMM.
+int64_t host_col_width(const gemm_f32_plan_s* p, int panels)
+{
+    const int q = host_col_request(p);
+    if (panels < 2 || q <= 1) return 0;
+    const int64_t w = round_up((p->N + q - 1) / q, tc_config(p->tc.config_id).bn);
+    return w < p->N ? w : 0;
+}
+
 void drop_panels(gemm_f32_plan_s* p)
 {
     p->panels.clear();
     p->panel_r0.clear();
+    p->blocks.clear();
+    p->block_c0.clear();
+    p->block_width = 0;
     p->panel_count = 0;
     if (p->panel_partial) cudaFree(p->panel_partial);
     p->panel_partial = nullptr;
@@ -484,10 +520,11 @@ void drop_panels(gemm_f32_plan_s* p)
 }
 
 // Panel states for `count` panels of whole 128-row tiles over the staging
-// buffers, their partial-tile scratch and events; kept until the count changes.
-cudaError_t make_panels(gemm_f32_plan_s* p, int count)
+// buffers (and the first panel's column blocks of `width` columns, 0 = none),
+// their partial-tile scratch and events; kept until the counts change.
+cudaError_t make_panels(gemm_f32_plan_s* p, int count, int64_t width)
 {
-    if (!p->panels.empty() && p->panel_count == count) return cudaSuccess;
+    if (!p->panels.empty() && p->panel_count == count && p->block_width == width) return cudaSuccess;
     drop_panels(p);
     const int64_t rows = round_up((p->M + count - 1) / count, tc_config(p->tc.config_id).bm);
     size_t need = 0;
@@ -504,6 +541,19 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
         p->panels.push_back(ps);
         p->panel_r0.push_back(r0);
     }
+    const int64_t mp0 = p->panels.size() > 1 ? p->panel_r0[1] : p->M;
+    for (int64_t c0 = 0; width > 0 && c0 < p->N; c0 += width) {
+        TcPlanState bs;
+        const int64_t nq = p->N - c0 < width ? p->N - c0 : width;
+        if ((e = tc_block_prepare(p->tc, 0, mp0, c0, nq, p->K, p->hA, p->lda, p->hB, p->ldb, bs)) != cudaSuccess) {
+            drop_panels(p);
+            return e;
+        }
+        if (bs.partial_bytes > need) need = bs.partial_bytes;
+        if (bs.sem_bytes > p->panel_sem_bytes) p->panel_sem_bytes = bs.sem_bytes;
+        p->blocks.push_back(bs);
+        p->block_c0.push_back(c0);
+    }
     if (need && (e = cudaMalloc(&p->panel_partial, need)) != cudaSuccess) {
         p->panel_partial = nullptr;
         drop_panels(p);
@@ -519,21 +569,26 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
             return e;
         }
     }
-    for (TcPlanState& ps : p->panels) {
-        if (e == cudaSuccess) e = tc_set_partial(ps, p->panel_partial);
-        ps.sem = ps.sem_bytes ? p->panel_sem : nullptr;
-    }
+    for (std::vector<TcPlanState>* v : {&p->panels, &p->blocks})
+        for (TcPlanState& ps : *v) {
+            if (e == cudaSuccess) e = tc_set_partial(ps, p->panel_partial);
+            ps.sem = ps.sem_bytes ? p->panel_sem : nullptr;
+        }
     if (e != cudaSuccess) {
         drop_panels(p);
         return e;
     }
-    while (e == cudaSuccess && p->pev.size() < 1 + 2 * p->panels.size()) {
+    while (e == cudaSuccess && p->pev.size() < 1 + 2 * p->panels.size() + 2 * p->blocks.size()) {
         cudaEvent_t x = nullptr;
         e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
         if (e == cudaSuccess) p->pev.push_back(x);
     }
-    if (e != cudaSuccess) drop_panels(p);
-    else p->panel_count = count;
+    if (e != cudaSuccess) {
+        drop_panels(p);
+    } else {
+        p->panel_count = count;
+        p->block_width = width;
+    }
     return e;
 }
 
@@ -542,50 +597,98 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count)
 // panel's pre-pass, GEMM and reduction after its A panel has landed; stream
 // xs[1] copies each C panel back once it is done.  So panel i's GEMM overlaps
 // the copy of A panel i+1 and of C panel i-1.
+//
+// With column blocks, the first panel is the blocks instead: xs[0] copies B
+// block 0, A panel 0, then the other B blocks (each a pitched copy of its
+// columns), then A panels 1..; the caller's stream splits each B block as it
+// lands and runs its block of the first panel (rows of panel 0, the block's
+// columns), then panels 1.. over the whole of B; xs[1] copies each C block
+// and then each C panel back.  The first GEMM waits for one block of B and
+// one panel of A instead of all of B.
 cudaError_t run_host_panels(gemm_f32_plan_s* p, const float* A_host, const float* B_host, float* C_host,
                             cudaStream_t s)
 {
-    const size_t np = p->panels.size();
+    const size_t np = p->panels.size(), nb = p->blocks.size();
     cudaEvent_t ev_b = p->pev[0];
     const cudaEvent_t* ev_a = &p->pev[1];
     const cudaEvent_t* ev_c = &p->pev[1 + np];
+    const cudaEvent_t* ev_bb = &p->pev[1 + 2 * np];
+    const cudaEvent_t* ev_cb = &p->pev[1 + 2 * np + nb];
+    auto panel_rows = [&](size_t i) { return (i + 1 < np ? p->panel_r0[i + 1] : p->M) - p->panel_r0[i]; };
+    auto block_cols = [&](size_t j) { return (j + 1 < nb ? p->block_c0[j + 1] : p->N) - p->block_c0[j]; };
+    // a rows x cols block at column c0 of a matrix with leading dimension ld
+    auto copy_block = [](float* dst, const float* src, int64_t rows, int64_t cols, int64_t ld, cudaMemcpyKind kind,
+                         cudaStream_t st) -> cudaError_t {
+        if (rows <= 0 || cols <= 0) return cudaSuccess;
+        return cudaMemcpy2DAsync(dst, size_t(ld) * sizeof(float), src, size_t(ld) * sizeof(float),
+                                 size_t(cols) * sizeof(float), size_t(rows), kind, st);
+    };
     cudaError_t e;
     // both copy streams start after the caller's earlier work
     if ((e = cudaEventRecord(p->xev[0], s)) != cudaSuccess) return e;
     for (int i = 0; i < 2; ++i)
         if ((e = cudaStreamWaitEvent(p->xs[i], p->xev[0], 0)) != cudaSuccess) return e;
-    // host -> device: B, then the A panels
-    if ((e = copy_rows(p->hB, B_host, p->K, p->N, p->ldb, cudaMemcpyHostToDevice, p->xs[0])) != cudaSuccess ||
-        (e = cudaEventRecord(ev_b, p->xs[0])) != cudaSuccess)
-        return e;
-    for (size_t i = 0; i < np; ++i) {
+    // host -> device: B (whole, or block 0 with the other blocks after A panel 0), then the A panels
+    auto copy_a = [&](size_t i) -> cudaError_t {
         const int64_t r0 = p->panel_r0[i];
-        const int64_t mp = (i + 1 < np ? p->panel_r0[i + 1] : p->M) - r0;
-        if ((e = copy_rows(p->hA + r0 * p->lda, A_host + r0 * p->lda, mp, p->K, p->lda, cudaMemcpyHostToDevice,
-                           p->xs[0])) != cudaSuccess ||
-            (e = cudaEventRecord(ev_a[i], p->xs[0])) != cudaSuccess)
+        cudaError_t r = copy_rows(p->hA + r0 * p->lda, A_host + r0 * p->lda, panel_rows(i), p->K, p->lda,
+                                  cudaMemcpyHostToDevice, p->xs[0]);
+        return r == cudaSuccess ? cudaEventRecord(ev_a[i], p->xs[0]) : r;
+    };
+    if (nb == 0) {
+        if ((e = copy_rows(p->hB, B_host, p->K, p->N, p->ldb, cudaMemcpyHostToDevice, p->xs[0])) != cudaSuccess ||
+            (e = cudaEventRecord(ev_b, p->xs[0])) != cudaSuccess || (e = copy_a(0)) != cudaSuccess)
             return e;
+    } else {
+        for (size_t j = 0; j < nb; ++j) {
+            const int64_t c0 = p->block_c0[j];
+            if ((e = copy_block(p->hB + c0, B_host + c0, p->K, block_cols(j), p->ldb, cudaMemcpyHostToDevice,
+                                p->xs[0])) != cudaSuccess ||
+                (e = cudaEventRecord(ev_bb[j], p->xs[0])) != cudaSuccess)
+                return e;
+            if (j == 0 && (e = copy_a(0)) != cudaSuccess) return e;
+        }
     }
-    // compute: B's split once, then panel by panel
-    if ((e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess ||
-        (e = tc_split_b(p->tc, p->N, p->K, p->hA, p->hB, p->ldb, s)) != cudaSuccess)
-        return e;
-    for (size_t i = 0; i < np; ++i) {
+    for (size_t i = 1; i < np; ++i)
+        if ((e = copy_a(i)) != cudaSuccess) return e;
+    // compute: the first panel (whole, after B's split, or block by block), then the others
+    if (nb == 0) {
+        if ((e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess ||
+            (e = tc_split_b(p->tc, p->N, p->K, p->hA, p->hB, p->ldb, s)) != cudaSuccess)
+            return e;
+    } else {
+        for (size_t j = 0; j < nb; ++j) {
+            const int64_t c0 = p->block_c0[j];
+            if ((e = cudaStreamWaitEvent(s, ev_bb[j], 0)) != cudaSuccess ||
+                (e = tc_split_b(p->blocks[j], block_cols(j), p->K, p->hA, p->hB + c0, p->ldb, s)) != cudaSuccess ||
+                (j == 0 && (e = cudaStreamWaitEvent(s, ev_a[0], 0)) != cudaSuccess) ||
+                (e = tc_panel_run(p->blocks[j], panel_rows(0), block_cols(j), p->K, p->hA, p->lda, p->hB + c0,
+                                  p->ldb, p->hC + c0, p->ldc, p->d_status, s)) != cudaSuccess ||
+                (e = cudaEventRecord(ev_cb[j], s)) != cudaSuccess)
+                return e;
+        }
+    }
+    for (size_t i = nb == 0 ? 0 : 1; i < np; ++i) {
         const int64_t r0 = p->panel_r0[i];
-        const int64_t mp = (i + 1 < np ? p->panel_r0[i + 1] : p->M) - r0;
         if ((e = cudaStreamWaitEvent(s, ev_a[i], 0)) != cudaSuccess ||
-            (e = tc_panel_run(p->panels[i], mp, p->N, p->K, p->hA + r0 * p->lda, p->lda, p->hB, p->ldb,
+            (e = tc_panel_run(p->panels[i], panel_rows(i), p->N, p->K, p->hA + r0 * p->lda, p->lda, p->hB, p->ldb,
                               p->hC + r0 * p->ldc, p->ldc, p->d_status, s)) != cudaSuccess ||
             (e = cudaEventRecord(ev_c[i], s)) != cudaSuccess)
             return e;
     }
-    // device -> host: each C panel when it is done; the caller's stream joins
-    for (size_t i = 0; i < np; ++i) {
+    // device -> host: each C block and C panel when it is done; the caller's stream joins
+    for (size_t j = 0; j < nb; ++j) {
+        const int64_t c0 = p->block_c0[j];
+        if ((e = cudaStreamWaitEvent(p->xs[1], ev_cb[j], 0)) != cudaSuccess ||
+            (e = copy_block(C_host + c0, p->hC + c0, panel_rows(0), block_cols(j), p->ldc, cudaMemcpyDeviceToHost,
+                            p->xs[1])) != cudaSuccess)
+            return e;
+    }
+    for (size_t i = nb == 0 ? 0 : 1; i < np; ++i) {
         const int64_t r0 = p->panel_r0[i];
-        const int64_t mp = (i + 1 < np ? p->panel_r0[i + 1] : p->M) - r0;
         if ((e = cudaStreamWaitEvent(p->xs[1], ev_c[i], 0)) != cudaSuccess ||
-            (e = copy_rows(C_host + r0 * p->ldc, p->hC + r0 * p->ldc, mp, p->N, p->ldc, cudaMemcpyDeviceToHost,
-                           p->xs[1])) != cudaSuccess)
+            (e = copy_rows(C_host + r0 * p->ldc, p->hC + r0 * p->ldc, panel_rows(i), p->N, p->ldc,
+                           cudaMemcpyDeviceToHost, p->xs[1])) != cudaSuccess)
             return e;
     }
     if ((e = cudaEventRecord(p->xev[2], p->xs[1])) != cudaSuccess) return e;
@@ -721,7 +824,8 @@ gemm_f32_status gemm_f32_run_host(gemm_f32_plan_t p, const float* A_host, const 
         if (e != cudaSuccess) return from_cuda(e);
     }
     if (const int panels = host_panel_count(p); panels > 1) {
-        if ((e = make_panels(p, panels)) != cudaSuccess || (e = run_host_panels(p, A_host, B_host, C_host, s)) != cudaSuccess)
+        if ((e = make_panels(p, panels, host_col_width(p, panels))) != cudaSuccess ||
+            (e = run_host_panels(p, A_host, B_host, C_host, s)) != cudaSuccess)
             return from_cuda(e);
         return gemm_f32_check(p, stream);
     }
@@ -889,6 +993,6 @@ const char* gemm_f32_status_string(gemm_f32_status s)
     return "GEMM_F32_ERR_UNKNOWN";
 }
 
-int gemm_f32_version(void) { return 100; }
+int gemm_f32_version(void) { return 101; }
 
 }  // extern "C"

@@ -161,6 +161,12 @@ cudaError_t tc_set_partial(TcPlanState& st, float* partial);
 // the caller to provide (out.partial_bytes long).
 cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, int64_t N, int64_t K,
                              const float* A, int64_t lda, const float* B, int64_t ldb, TcPlanState& out);
+// A block of rows r0..r0+mp and columns c0..c0+nq of the product (c0 and nq
+// whole tiles): the panel state over those rows, with the block's rows of the
+// split B and the block's columns of the raw B.  The block's split B is
+// written by tc_split_b on this state with B + c0 and N = nq.
+cudaError_t tc_block_prepare(const TcPlanState& full, int64_t r0, int64_t mp, int64_t c0, int64_t nq, int64_t K,
+                             const float* A, int64_t lda, const float* B, int64_t ldb, TcPlanState& out);
 // The B part of the pre-pass for the whole plan (when its route needs it).
 cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const float* A, const float* B,
                        int64_t ldb, cudaStream_t s);

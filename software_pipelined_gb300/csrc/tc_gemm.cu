@@ -553,6 +553,20 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     return cudaSuccess;
 }
 
+cudaError_t tc_block_prepare(const TcPlanState& full, int64_t r0, int64_t mp, int64_t c0, int64_t nq, int64_t K,
+                             const float* A, int64_t lda, const float* B, int64_t ldb, TcPlanState& out)
+{
+    cudaError_t e = tc_panel_prepare(full, r0, mp, nq, K, A, lda, B + c0, ldb, out);
+    if (e != cudaSuccess) return e;
+    // the block's rows of the split B (B transposed: one row per column of B)
+    const TcConfig& c = kTc[full.config_id].cfg;
+    out.b_hi = full.b_hi + c0 * full.kp;
+    out.b_lo = full.b_lo + c0 * full.kp;
+    const int64_t b_rows = c.bm == 2 * kBM ? c.bn / 2 : c.bn;
+    if ((e = encode_kmajor(out.tmap_b_hi, out.b_hi, nq, out.kp, b_rows)) != cudaSuccess) return e;
+    return encode_kmajor(out.tmap_b_lo, out.b_lo, nq, out.kp, b_rows);
+}
+
 cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const float* A, const float* B,
                        int64_t ldb, cudaStream_t s)
 {

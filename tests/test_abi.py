@@ -42,12 +42,12 @@ def test_status_strings_and_version(lib):
     assert g.gemm_f32_status_string(0) == "GEMM_F32_OK"
     assert g.gemm_f32_status_string(4) == "GEMM_F32_ERR_TIMEOUT"
     assert g.gemm_f32_status_string(99) == "GEMM_F32_ERR_UNKNOWN"
-    assert g.gemm_f32_version() >= 100
+    assert g.gemm_f32_version() >= 101
 
 
 def test_opts_layout_matches_header(lib):
-    # int32 x6, int64, int32 x8 -> 6*4 + 8 + 8*4 = 64 bytes
-    assert ctypes.sizeof(g.Opts) == 64
+    # int32 x6, int64, int32 x9 -> 6*4 + 8 + 9*4 = 68 bytes, padded to the int64's 8: 72
+    assert ctypes.sizeof(g.Opts) == 72
     o = g.gemm_f32_opts_init()
     assert o.variant == 0 and o.split_k == 0 and o.wait_timeout_cycles == 0
 
@@ -70,7 +70,8 @@ def test_plan_rejects_bad_dims(lib, dims):
 def test_plan_rejects_bad_options(lib):
     for field, value in [("variant", 7), ("split_k", 65), ("tf32_terms", 2), ("stages", -1),
                          ("wait_timeout_cycles", -5), ("operand_split", 5), ("tile_group", 65),
-                         ("host_panels", 65), ("host_panels", -1), ("split_reduce", 4), ("split_reduce", -1), ("k_slices", 3), ("k_slices", 8)]:
+                         ("host_panels", 65), ("host_panels", -1), ("split_reduce", 4), ("split_reduce", -1), ("k_slices", 3), ("k_slices", 8),
+                         ("host_col_blocks", -1), ("host_col_blocks", 17)]:
         o = g.gemm_f32_opts_init()
         setattr(o, field, value)
         s, h = g.gemm_f32_plan_ex(64, 64, 64, 64, 64, 64, o)

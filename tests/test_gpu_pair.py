@@ -236,11 +236,12 @@ def test_pair_cluster_sum_withheld_stage_times_out():
 
 
 @pytest.mark.parametrize("mode", [2, 3], ids=["in_kernel", "hybrid"])
-@pytest.mark.parametrize("panels", [2, 3])
-def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels):
+@pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (3, 2), (2, 3)])
+def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels, cols):
     # Without a K-split every tile is summed in the same order whichever 256-row
-    # panel it falls in: the panel pipeline must reproduce the device run bit
-    # for bit (a wrong panel offset cannot hide in the bound).
+    # panel (or column block of the first panel) it falls in: the panel
+    # pipeline must reproduce the device run bit for bit (a wrong panel or
+    # block offset cannot hide in the bound).
     import torch
     M, N, K = 1536, 768, 320
     A = inputs.normal(2119, M, K)
@@ -248,7 +249,7 @@ def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels):
     hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
     hC = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
     opts = dict(PAIR, tile_n=256, split_k=1, operand_split=mode)
-    with g.Plan(M, N, K, host_panels=panels, **opts) as p:
+    with g.Plan(M, N, K, host_panels=panels, host_col_blocks=cols, **opts) as p:
         assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
     C, desc, canaries, _ = run_gemm(A, B, host_panels=1, **opts)
     assert canaries

@@ -619,9 +619,12 @@ def _pinned(host, ld):
     return t
 
 
-@pytest.mark.parametrize("panels", [2, 3, 7])
+@pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (7, 1), (3, 3), (2, 2)])
 @pytest.mark.parametrize("mode", [1, 2, 3, 4], ids=["pre_pass", "in_kernel", "hybrid", "raw_a"])
-def test_run_host_panels(mode, panels):
+def test_run_host_panels(mode, panels, cols):
+    # cols > 1: the first panel in column blocks (in-kernel and hybrid splits;
+    # the pre-pass forms ignore it); N = 520 leaves a ragged last block, and
+    # ldc = N + 3 keeps C from the TMA-store epilogue
     M, N, K = 1000, 520, 264
     lda, ldb, ldc = K + 4, N + 8, N + 3
     A = inputs.uniform_pm1(1711, M, K)
@@ -629,7 +632,7 @@ def test_run_host_panels(mode, panels):
     hA, hB = _pinned(A, lda), _pinned(B, ldb)
     hC = _pinned(np.full((M, N), np.nan, dtype=np.float32), ldc)
     with g.Plan(M, N, K, lda, ldb, ldc, variant=g.VARIANT_TCGEN05, operand_split=mode,
-                host_panels=panels) as p:
+                host_panels=panels, host_col_blocks=cols) as p:
         for _ in range(2):
             hC[:, :N] = float("nan")
             s = p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0)
@@ -640,19 +643,21 @@ def test_run_host_panels(mode, panels):
             assert (C[:, N:] == 321.0).all()
 
 
-@pytest.mark.parametrize("mode", [1, 4], ids=["pre_pass", "raw_a"])
-def test_run_host_panels_bit_identical_to_device_run(mode):
+@pytest.mark.parametrize("mode,cols", [(1, 0), (4, 0), (2, 3), (3, 2)],
+                         ids=["pre_pass", "raw_a", "in_kernel_blocks", "hybrid_blocks"])
+def test_run_host_panels_bit_identical_to_device_run(mode, cols):
     # With no K-split every output tile is summed in the same order whichever
-    # panel it falls in, so the panel pipeline must reproduce the one-launch
-    # device run bit for bit (a wrong panel offset cannot hide in the bound).
+    # panel (or column block of the first panel) it falls in, so the panel
+    # pipeline must reproduce the one-launch device run bit for bit (a wrong
+    # panel or block offset cannot hide in the bound).
     import torch
     M, N, K = 1536, 640, 192
     A = inputs.normal(1713, M, K)
     B = inputs.normal(1714, K, N)
     hA, hB = _pinned(A, K), _pinned(B, N)
     hC = _pinned(np.zeros((M, N), dtype=np.float32), N)
-    opts = dict(variant=g.VARIANT_TCGEN05, operand_split=mode, split_k=1)
-    with g.Plan(M, N, K, host_panels=4, **opts) as p:
+    opts = dict(variant=g.VARIANT_TCGEN05, operand_split=mode, split_k=1, tile_m=128)
+    with g.Plan(M, N, K, host_panels=4, host_col_blocks=cols, **opts) as p:
         assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
     C, desc, canaries, _ = run_gemm(A, B, host_panels=1, **opts)
     assert canaries
