@@ -13,7 +13,7 @@ For every benchmark shape each variant is planned with forced options and
 timed as CUDA-graph replays of back-to-back runs (device time, no host
 launch overhead).  Prints a JSON document (and a markdown table with --md):
 
-    python -m software_pipelined_gb300.ablation --json gpurun_out/ablation.json --md
+    python -m software_pipelined_gb300.ablation --json ablation.json --md
 """
 from __future__ import annotations
 

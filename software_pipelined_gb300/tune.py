@@ -5,7 +5,7 @@ The dispatcher reads that table first ("no single kernel is fastest": the
 pages' lesson that libraries pick a variant per shape), and falls back to a
 rule for shapes it does not list.  Run on the target GPU:
 
-    python -m software_pipelined_gb300.tune --json gpurun_out/tune.json \\
+    python -m software_pipelined_gb300.tune --json tune.json \\
         --inc software_pipelined_gb300/csrc/dispatch_table.inc
 
 Each candidate is planned with forced options, warmed up, and timed as the
