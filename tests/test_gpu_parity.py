@@ -289,6 +289,23 @@ def test_persistent_many_tiles_per_cta():
     assert canaries and ok, f"{desc}: {err}"
 
 
+@pytest.mark.parametrize("opts", [dict(tile_m=128, tile_n=128), dict(tile_m=256, tile_n=256)],
+                         ids=["one_cta_128", "pair_256"])
+def test_reduction_larger_than_one_grid(opts):
+    # Every tile split: more float4 of partial tiles to sum (4096 x 2048 x 2
+    # slices, about 2.1 M per slice set) than the reduction's grid has threads
+    # (152 SMs x 64 blocks x 192), so its threads take several float4 each.
+    M, N, K = 4096, 2048 + 40, 256
+    A = inputs.uniform_pm1(983, M, K)
+    B = inputs.uniform_pm1(984, K, N)
+    C, desc, canaries, outs = run_gemm(A, B, ldb=N + (-N % 4), repeat=2, variant=g.VARIANT_TCGEN05, split_k=2,
+                                       **opts)
+    assert "whole=0" in desc, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+    assert np.array_equal(outs[0], outs[1]), desc
+
+
 @pytest.mark.parametrize("shape,bn", [((128 * 20, 128 * 17, 1024), 128), ((128 * 33, 256 * 9 + 40, 640), 256)],
                          ids=["bn128", "bn256_ragged"])
 def test_tail_wave_split(shape, bn):
