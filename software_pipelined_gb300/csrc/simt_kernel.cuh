@@ -82,6 +82,9 @@ simt_gemm_kernel(SimtArgs a)
     const int64_t M = a.M, N = a.N;
     const float* __restrict__ A = a.A + (batched ? (int64_t)blockIdx.z * a.stride_a : 0);
     const float* __restrict__ B = a.B + (batched ? (int64_t)blockIdx.z * a.stride_b : 0);
+    // Programmatic serialisation: wait for the previous kernel's writes before
+    // the first copy (a no-op when launched without the attribute).
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // Issue the cp.async copies of K-tile t into ring slot st.  Out-of-range
     // elements (ragged M, N or K) are zero-filled by the copy itself.
@@ -240,6 +243,11 @@ simt_gemm_kernel(SimtArgs a)
         }
         ptx::cp_async_wait<0>();
     }
+    // The next kernel on the stream may launch its CTAs now, during this
+    // epilogue.  Not earlier: waiting CTAs of the next launches (each would
+    // release its own successor) would fill the SMs' slots and shared memory
+    // while this grid still runs.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     if constexpr (KSL > 1) {
         // Hand the register tiles of groups 1..KSL-1 to group 0 (lane-major:
@@ -301,10 +309,18 @@ cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
     auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, KT::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
-              (unsigned)(a.batch > 1 ? a.batch : a.split_k));
-    kern<<<grid, KT::NTT, KT::SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
+                       (unsigned)(a.batch > 1 ? a.batch : a.split_k));
+    cfg.blockDim = dim3(KT::NTT);
+    cfg.dynamicSmemBytes = KT::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false, int KSL = 1>

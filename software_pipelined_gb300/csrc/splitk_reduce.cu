@@ -13,10 +13,35 @@
 namespace gemm_f32 {
 namespace {
 
+// Programmatic serialisation: this kernel may be launched while the split-K
+// GEMM before it finishes, and waits for it before reading its partials.  It
+// releases its own successor only by completing: a successor's CTAs waiting
+// early would take the slots these blocks need.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 __global__ void __launch_bounds__(256)
 splitk_reduce_vec4(const float4* __restrict__ P, int splits, int64_t M, int64_t n4,
                    int64_t ldp4, int64_t slice4, float4* __restrict__ C, int64_t ldc4)
 {
+    pdl_enter();
     const int64_t total = M * n4;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -35,6 +60,7 @@ __global__ void __launch_bounds__(256)
 splitk_reduce_scalar(const float* __restrict__ P, int splits, int64_t M, int64_t N,
                      int64_t ldp, int64_t slice, float* __restrict__ C, int64_t ldc)
 {
+    pdl_enter();
     const int64_t total = M * N;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -81,13 +107,10 @@ cudaError_t splitk_reduce_launch(const float* P, int splits, int64_t M, int64_t 
                      (reinterpret_cast<uintptr_t>(P) % 16 == 0);
     if (vec) {
         const int64_t n4 = N / 4;
-        splitk_reduce_vec4<<<grid_for(M * n4), 256, 0, s>>>(
-            reinterpret_cast<const float4*>(P), splits, M, n4, ldp / 4, slice / 4,
-            reinterpret_cast<float4*>(C), ldc / 4);
-    } else {
-        splitk_reduce_scalar<<<grid_for(M * N), 256, 0, s>>>(P, splits, M, N, ldp, slice, C, ldc);
+        return launch_pdl(splitk_reduce_vec4, grid_for(M * n4), s, reinterpret_cast<const float4*>(P), splits,
+                          M, n4, ldp / 4, slice / 4, reinterpret_cast<float4*>(C), ldc / 4);
     }
-    return cudaGetLastError();
+    return launch_pdl(splitk_reduce_scalar, grid_for(M * N), s, P, splits, M, N, ldp, slice, C, ldc);
 }
 
 cudaError_t zero_fill_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t s)
