@@ -676,7 +676,10 @@ cudaError_t run_host_panels(gemm_f32_plan_s* p, const float* A_host, const float
             (e = cudaEventRecord(ev_c[i], s)) != cudaSuccess)
             return e;
     }
-    // device -> host: each C block and C panel when it is done; the caller's stream joins
+    // device -> host: each C block and C panel when it is done; the caller's stream joins.
+    // The C blocks wait for the last B block too: until then the host link's
+    // other direction carries B, which the GEMMs are waiting for.
+    if (nb > 0 && (e = cudaStreamWaitEvent(p->xs[1], ev_bb[nb - 1], 0)) != cudaSuccess) return e;
     for (size_t j = 0; j < nb; ++j) {
         const int64_t c0 = p->block_c0[j];
         if ((e = cudaStreamWaitEvent(p->xs[1], ev_cb[j], 0)) != cudaSuccess ||
