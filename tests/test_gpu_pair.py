@@ -236,6 +236,28 @@ def test_pair_cluster_sum_withheld_stage_times_out():
 
 
 @pytest.mark.parametrize("mode", [2, 3], ids=["in_kernel", "hybrid"])
+def test_pair_run_host_blocks_ragged_with_splits(mode):
+    # Ragged M and N (the last panel's second tile row and the last block's
+    # columns past the edge), K-slices in every panel's last wave, padded C:
+    # the bound, and the padding untouched.
+    import torch
+    M, N, K, ldc = 1300, 1100, 300, 1107
+    A = inputs.uniform_pm1(2131, M, K)
+    B = inputs.uniform_pm1(2132, K, N)
+    hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+    hC = torch.full((M, ldc), 321.0, dtype=torch.float32).pin_memory()
+    with g.Plan(M, N, K, K, N, ldc, host_panels=3, host_col_blocks=3, tile_n=256, operand_split=mode,
+                **PAIR) as p:
+        for _ in range(2):
+            hC[:, :N] = float("nan")
+            assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
+            C = hC.numpy()
+            err, ok = check_against_oracle(C[:, :N].astype(np.float64), A, B)
+            assert ok, f"{p.describe()}: {err}"
+            assert (C[:, N:] == 321.0).all()
+
+
+@pytest.mark.parametrize("mode", [2, 3], ids=["in_kernel", "hybrid"])
 @pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (3, 2), (2, 3)])
 def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels, cols):
     # Without a K-split every tile is summed in the same order whichever 256-row
