@@ -247,6 +247,94 @@ def time_graph(run_on, target_ms=20.0, batches=5):
     return statistics.median(res), min(res), max(res), reps
 
 
+class CublasCompare:
+    """cuBLAS through ctypes, for the comparison columns only (never on the
+    measured path): FP32 emulated with BF16 pieces (compute type
+    CUBLAS_COMPUTE_32F_EMULATED_16BFX9, emulation strategy EAGER so that it is
+    used at every size) and single TF32 (CUBLAS_COMPUTE_32F_FAST_TF32, not
+    FP32-accurate: the tensor pipe's own rate).  Row-major C = A B is computed
+    as the column-major C^T = B^T A^T.  Unavailable (None times) when the
+    library or a call is missing."""
+
+    COMPUTE = {"bf16x9": 78, "tf32": 77, "sgemm": 68}
+
+    def __init__(self):
+        import ctypes
+        import glob
+        import torch
+        self.ok = False
+        self.why = None
+        torch.mm(torch.zeros(8, 8, device="cuda"), torch.zeros(8, 8, device="cuda"))  # torch's cuBLAS loaded
+        cands = ["libcublas.so.13"]
+        for p in sys.path:
+            cands += sorted(glob.glob(os.path.join(p, "nvidia", "cu13", "lib", "libcublas.so.*")))
+            cands += sorted(glob.glob(os.path.join(p, "nvidia", "cublas", "lib", "libcublas.so.*")))
+        cands.append("/usr/local/cuda/lib64/libcublas.so")
+        self.lib = None
+        for c in cands:
+            try:
+                self.lib = ctypes.CDLL(c)
+                break
+            except OSError:
+                continue
+        if self.lib is None:
+            self.why = "libcublas not found"
+            return
+        self.c = ctypes
+        self.h = ctypes.c_void_p()
+        if self.lib.cublasCreate_v2(ctypes.byref(self.h)) != 0:
+            self.why = "cublasCreate failed"
+            return
+        ver = ctypes.c_int()
+        self.lib.cublasGetVersion_v2(self.h, ctypes.byref(ver))
+        self.version = ver.value
+        self.ws = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        if self.lib.cublasSetWorkspace_v2(self.h, ctypes.c_void_p(self.ws.data_ptr()),
+                                          ctypes.c_size_t(self.ws.numel())) != 0:
+            self.why = "cublasSetWorkspace failed"
+            return
+        try:
+            emu = self.lib.cublasSetEmulationStrategy(self.h, 2)
+        except AttributeError:
+            emu = -1
+        self.emulation = emu == 0
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        self.lib.cublasGemmEx.argtypes = [vp, i, i, i, i, i, vp, vp, i, i, vp, i, i, vp, vp, i, i, i, i]
+        self.lib.cublasSetStream_v2.argtypes = [vp, vp]
+        self.one, self.zero = ctypes.c_float(1.0), ctypes.c_float(0.0)
+        self.ok = True
+
+    def gemm(self, kind, st, dA, dB, dC, M, N, K):
+        c = self.c
+        self.lib.cublasSetStream_v2(self.h, c.c_void_p(st))
+        return self.lib.cublasGemmEx(self.h, 0, 0, N, M, K, c.byref(self.one), dB.data_ptr(), 0, N,
+                                     dA.data_ptr(), 0, K, c.byref(self.zero), dC.data_ptr(), 0, N,
+                                     self.COMPUTE[kind], -1)
+
+    def time(self, kind, dA, dB, dC, M, N, K):
+        """Graph-replayed per-call time (ms) of one compute type, or None."""
+        import torch
+        if not self.ok or (kind == "bf16x9" and not self.emulation):
+            return None
+        if self.gemm(kind, torch.cuda.current_stream().cuda_stream, dA, dB, dC, M, N, K) != 0:
+            return None
+        torch.cuda.synchronize()
+        try:
+            med, _, _, _ = time_graph(lambda st: self.gemm(kind, st, dA, dB, dC, M, N, K))
+        except RuntimeError:
+            return None
+        finally:
+            self.lib.cublasSetStream_v2(self.h, self.c.c_void_p(torch.cuda.current_stream().cuda_stream))
+        return med
+
+    def close(self):
+        if self.ok:
+            import torch
+            torch.cuda.synchronize()
+            self.lib.cublasDestroy_v2(self.h)
+            self.ok = False
+
+
 def make_device_operands(M, N, K, dist, sa, sb):
     import torch
     from software_pipelined_gb300 import inputs
@@ -259,10 +347,11 @@ def make_device_operands(M, N, K, dist, sa, sb):
 
 def capture_for_check(A, B, Cd, full_limit=2 ** 31):
     """What the oracle comparison needs of a GPU result (no oracle here): the
-    whole output for moderate sizes, 1028 sampled entries beyond."""
+    whole output for moderate sizes (always, with full_limit None), 1028
+    sampled entries beyond."""
     M, K = A.shape
     N = B.shape[1]
-    if M * N * K <= full_limit:
+    if full_limit is None or M * N * K <= full_limit:
         return {"A": A, "B": B, "kind": "full", "C": Cd.cpu().numpy()}
     rng = np.random.default_rng(12345)
     rows = np.concatenate([[0, M - 1, 0, M - 1], rng.integers(0, M, 1024)])
@@ -272,13 +361,21 @@ def capture_for_check(A, B, Cd, full_limit=2 ** 31):
     return {"A": A, "B": B, "kind": "sampled-1028", "rows": rows, "cols": cols, "vals": vals}
 
 
-def compare_with_oracle(chk):
-    """Max normalised error of a captured GPU result against the oracle."""
+def compare_with_oracle(chk, cache=None):
+    """Max normalised error of a captured GPU result against the oracle.  With
+    a cache (a dict), the oracle's product of the same A and B objects is
+    computed once."""
     import oracle
     A, B = chk["A"], chk["B"]
     K = A.shape[1]
     if chk["kind"] == "full":
-        Cr, S = oracle.gemm_f64(A, B)
+        key = (id(A), id(B))
+        if cache is not None and key in cache:
+            Cr, S = cache[key]
+        else:
+            Cr, S = oracle.gemm_f64(A, B)
+            if cache is not None:
+                cache[key] = (Cr, S)
         return round(oracle.normalised_error(chk["C"], Cr, S, K), 4), "full"
     c, s = oracle.gemm_f64_entries(A, B, chk["rows"], chk["cols"])
     return round(oracle.normalised_error(chk["vals"], c, s, K), 4), chk["kind"]
@@ -471,6 +568,17 @@ def run_gpu_arm(args):
                 "main_kernel_share_of_step": round(main_ms / ms_step, 4),
                 "split_pass_share_of_step": round(split_ms / ms_step, 4),
                 "per_shape": per_kernel}
+    # The same fraction per clock: against the tensor pipe's dense TF32 rate at
+    # the SM clock sampled in the timed region (2048 TF32 multiply-adds per SM
+    # per clock, half of BF16's 4096, as the nominal dense peaks are; three
+    # TF32 products per FP32 product).
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    if not simt_main and clk.get("sm_mhz"):
+        per_clock = sms * 2 * 2048 / 3.0 * clk["sm_mhz"] * 1e6 / 1e12
+        roofline["peak_per_clock"] = round(per_clock, 2)
+        roofline["frac_per_clock"] = round(achieved / per_clock, 4)
+        roofline["peak_per_clock_basis"] = (f"{sms} SMs x 2048 TF32 FMA/clk x 2 / 3 at the median SM clock "
+                                            f"{clk['sm_mhz']:.0f} MHz of the timed region")
     launches = args.steps * sum(w["plan"].kernel_launches for w in work)
 
     # headline results kept for the comparison with the oracle (below, in the
@@ -480,7 +588,7 @@ def run_gpu_arm(args):
     if rank == 0 and not args.quick:
         for w in work:
             headline_parity[w["name"]] = {}
-            checks.append((headline_parity[w["name"]], capture_for_check(w["A"], w["B"], w["dC"], full_limit=0)))
+            checks.append((headline_parity[w["name"]], capture_for_check(w["A"], w["B"], w["dC"], full_limit=None)))
 
     # ---- e2e: through the C-ABI host-buffer call ------------------------------
     e2e = None
@@ -500,17 +608,21 @@ def run_gpu_arm(args):
         for w in work:
             w["plan"].trace_enable(0)
         e2e_step()
-        n_e2e = max(3, args.steps // 10)
+        n_e2e = max(10, args.steps // 5)
         if dist:
             dist.barrier()
-        t0 = time.perf_counter()
+        calls = []
         for _ in range(n_e2e):
-            e2e_step()
-        dt = max_over_ranks((time.perf_counter() - t0) / n_e2e, dist, "cuda")
+            t0 = time.perf_counter()
+            e2e_step()  # synchronous: the call copies C back and synchronises
+            calls.append(time.perf_counter() - t0)
+        dt = max_over_ranks(sum(calls) / n_e2e, dist, "cuda")
         e2e = {"value": round(whole_job_rate(flops_step, world, dt), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(sum(4 * (w["M"] * w["K"] + w["K"] * w["N"]) for w in work)),
                "d2h_bytes_per_step": int(sum(4 * w["M"] * w["N"] for w in work)),
                "ms_per_step": round(dt * 1e3, 3), "steps": n_e2e,
+               "ms_min": round(min(calls) * 1e3, 3), "ms_median": round(statistics.median(calls) * 1e3, 3),
+               "ms_max": round(max(calls) * 1e3, 3),
                "call": "gemm_f32_run_host (pinned host A, B, C; copies and sync inside the call)"}
         del hbufs
 
@@ -520,6 +632,17 @@ def run_gpu_arm(args):
     batched = None
     if rank == 0 and not args.no_per_shape:
         per_shape = []
+        cublas = None
+        try:
+            cublas = CublasCompare()
+        except (OSError, AttributeError, RuntimeError) as ex:
+            cublas_note = f"cuBLAS comparison unavailable: {ex}"
+        else:
+            cublas_note = (f"cuBLAS {cublas.version}, FP32 emulation (BF16x9, strategy EAGER) "
+                           f"{'available' if cublas.emulation else 'not exposed'}" if cublas.ok else
+                           f"cuBLAS comparison unavailable: {cublas.why}")
+            if not cublas.ok:
+                cublas = None
         from software_pipelined_gb300 import inputs
         # every shape's operands and plan, kept for all rounds
         cases = []
@@ -584,6 +707,12 @@ def run_gpu_arm(args):
             torch.backends.cuda.matmul.allow_tf32 = False
             dC2 = torch.empty_like(dC)
             cb, _, _, _ = time_graph(lambda st, a=dA, b=dB, cc=dC2: torch.mm(a, b, out=cc))
+            # cuBLAS FP32 emulated with BF16 pieces and single TF32, same protocol
+            emu = cublas.time("bf16x9", dA, dB, dC2, M, N, K) if cublas else None
+            emu_chk = None
+            if emu is not None and not args.quick and M * N * K <= 2 ** 31:
+                emu_chk = capture_for_check(A, B, dC2)
+            tf1 = cublas.time("tf32", dA, dB, dC2, M, N, K) if cublas else None
             del dC2
             entry = {
                 "config": key, "shape": name, "plan": plan.describe(),
@@ -591,6 +720,8 @@ def run_gpu_arm(args):
                 "us_rounds": [round(x * 1e3, 3) for x in c["rounds"]],
                 "us_direct_launch": round(s_med * 1e3, 3),
                 "torch_fp32_matmul_us": round(cb * 1e3, 3),
+                "cublas_fp32_emulated_bf16x9_us": round(emu * 1e3, 3) if emu is not None else None,
+                "cublas_tf32_us": round(tf1 * 1e3, 3) if tf1 is not None else None,
                 "phases_us_split_main_reduce": ph,
                 "tflops": round(fl / (med * 1e-3) / 1e12, 3),
                 "roofline_frac": round(t_roof / (med * 1e-3), 4),
@@ -603,9 +734,15 @@ def run_gpu_arm(args):
             if cold is not None:
                 entry["us_cold_l2"] = cold
             per_shape.append(entry)
+            if emu_chk is not None:
+                checks.append((entry, dict(emu_chk, field="cublas_bf16x9_max_normalised_error")))
             if not args.quick:
-                checks.append((entry, capture_for_check(A, B, dC)))
+                # the headline shapes: the whole output (their oracle product is shared
+                # with the headline check); the others up to 2^31 multiply-adds
+                checks.append((entry, capture_for_check(A, B, dC, full_limit=None if not c["own"] else 2 ** 31)))
         del flush
+        if cublas:
+            cublas.close()
         for c in cases:
             if c["own"]:
                 c["plan"].close()
@@ -648,7 +785,8 @@ def run_gpu_arm(args):
         floors = {"event_pair_us": round(statistics.median(ts) * 1e3, 3),
                   "smallest_kernel_direct_launch_us": round(med * 1e3, 3),
                   "smallest_kernel_graph_us": round(gmed * 1e3, 3),
-                  "note": "smallest kernel = this library's 1x1 zero-fill, back to back"}
+                  "note": "smallest kernel = this library's 1x1 zero-fill, back to back",
+                  "comparison_columns": cublas_note}
 
     # ---- CPU-baseline leg: the oracle, on this host's cores ------------------
     # The only part of the GPU arm that runs the oracle: its throughput on a
@@ -662,8 +800,9 @@ def run_gpu_arm(args):
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"first {rows} rows of {big['name']} ({rows}x{big['N']}x{big['K']}), "
                          f"FP64 i-k-j triple loop, {dt:.1f} s"}
+        products = {}
         for where, chk in checks:
-            err, how = compare_with_oracle(chk)
+            err, how = compare_with_oracle(chk, products)
             if "field" in chk:
                 where[chk["field"]] = err
             else:
@@ -680,6 +819,7 @@ def run_gpu_arm(args):
                     finally:
                         oracle.set_threads(threads)
                 where["oracle"] = orc
+        del products
     del checks
 
     if rank == 0:
@@ -701,6 +841,12 @@ def run_gpu_arm(args):
             "environment": run_environment(local),
             "library_sha256_16": source_hash([g.LIB_PATH]),
         }
+        # last key, so that it survives in a tail of the output: per shape
+        # [us, TFLOP/s, roofline fraction, max normalised error, plan]
+        if per_shape:
+            line["per_shape_summary"] = {e["shape"]: [e["us"], e["tflops"], e["roofline_frac"],
+                                                      e["max_normalised_error"], plan_tag(e["plan"])]
+                                         for e in per_shape}
         print(json.dumps(line), flush=True)
         if args.json_out:
             with open(args.json_out, "w") as f:
@@ -715,6 +861,13 @@ def run_gpu_arm(args):
 # ---------------------------------------------------------------------------
 # Reference arm: the CPU oracle on the same workload.
 # ---------------------------------------------------------------------------
+
+def plan_tag(desc):
+    """A short form of a plan description: kernel, split form, tile, stages,
+    split-K and tile order (drops sizes that follow from the shape)."""
+    drop = ("terms=", "ws=", "kp=", "resident=", "whole=", "pairs=", "tiles=", "thread=")
+    return " ".join(t for t in desc.split() if not t.startswith(drop) and t != "3xtf32")
+
 
 def workload_label(workload):
     """What a workload is, with its sizes."""

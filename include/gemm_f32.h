@@ -34,13 +34,24 @@
  *   - A and B must not overlap C.  This is not checked.
  *   - Any base-pointer alignment and any leading dimension is accepted; the
  *     dispatcher routes around what a kernel cannot take.
- *   - Accuracy: every element satisfies |C - C_exact| <= 2*K*2^-24*sum_k|A_ik||B_kj|
- *     for finite inputs.  The tensor-core path splits each operand into two
- *     TF32 pieces (22 significand bits), whose per-product error of about
- *     3*2^-22*|a||b| meets that bound only for K of about 10 and up, so it
- *     takes K >= 16 only; smaller K always runs on the SIMT kernel.  With non-finite inputs the affected outputs are
- *     non-finite, but not necessarily the IEEE value (the 3xTF32 split turns
- *     +-Inf into NaN).
+ *   - Accuracy: for finite A and B with every S_ij = sum_k |A_ik||B_kj| below
+ *     2^127, every element satisfies
+ *         |C_ij - C_exact,ij| <= 2*K*2^-24*S_ij + K*2^-149 + t_ij.
+ *     The first term is the usual bound of a K-term FP32 dot product.  The
+ *     second is gradual underflow: each FP32 operation whose result falls
+ *     below 2^-126 can be off by 2^-150, so it matters only for results or
+ *     partial sums in the subnormal range.  t_ij = 0 for SIMT plans; for
+ *     tensor-core plans t_ij = 2^-136 * sum_k (|B_kj| [0 < |A_ik| < 2^-113] +
+ *     |A_ik| [0 < |B_kj| < 2^-113]): each operand is split into two TF32
+ *     pieces, which resolve nothing finer than 2^-136 (TF32's smallest
+ *     subnormal), so an element below 2^-113 is carried to within 2^-137.
+ *     Subnormal operands are not flushed, and finite operands up to FLT_MAX
+ *     stay finite through the split.  The two pieces carry 22 significand
+ *     bits, whose per-product error of about 3*2^-22*|a||b| meets the first
+ *     term only for K of about 10 and up, so the tensor-core path takes
+ *     K >= 16 only; smaller K always runs on the SIMT kernel.  With
+ *     non-finite inputs the affected outputs are non-finite, but not
+ *     necessarily the IEEE value (the 3xTF32 split turns +-Inf into NaN).
  *   - Errors are returned as status codes; nothing calls exit or abort.
  *   - A plan is bound to the CUDA device that was current when it was made and
  *     must run with that device current.  One plan may be used from one stream

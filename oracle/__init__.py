@@ -15,6 +15,22 @@ ctypes, plus the accuracy criterion the GPU result must meet:
 
 reported as the normalised error  |C_gpu - C| / (K * 2^-24 * S)  (pass iff <= 2;
 where S == 0 the GPU value must be exactly 0).
+
+That bound is the usual one for a K-term FP32 dot product and assumes that no
+result or intermediate falls below FP32's normal range.  For inputs where one
+can, ``bound_ratio`` adds the two absolute terms that hold without that
+assumption:
+
+    |C_gpu - C| <= 2 K 2^-24 S + K 2^-149 + 2^-136 T
+
+K 2^-149: gradual underflow (an FP32 operation whose result is subnormal is
+off by up to 2^-150, half the subnormal step), K of them per element with a
+factor of 2 as in the first term.  2^-136 T, T = ``tf32_grid_term(A, B)``: a
+product split into TF32 pieces cannot resolve anything finer than 2^-136
+(TF32's smallest subnormal), so an element below 2^-113 in magnitude (whose
+remainder after the first piece lies below that step) is carried to within
+2^-137; T is the sum of the magnitudes such an element multiplies.  Only the
+tensor-core plans have that term (T = None for the SIMT plans).
 """
 from __future__ import annotations
 
@@ -134,6 +150,36 @@ def normalised_error(C_gpu, C_ref, S_ref, K: int):
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.where(scale > 0, diff / np.where(scale > 0, scale, 1.0),
                      np.where(diff == 0, 0.0, np.inf))
+    r = np.where(np.isfinite(Cg), r, np.inf)
+    return float(r.max()) if r.size else 0.0
+
+
+TF32_FINEST = 2.0 ** -136   # TF32's smallest subnormal (10 stored mantissa bits below 2^-126)
+TF32_FULL = 2.0 ** -113     # smallest magnitude whose TF32 pieces carry it to full FP32 accuracy
+UNDERFLOW_STEP = 2.0 ** -149  # FP32's smallest subnormal
+
+
+def tf32_grid_term(A: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """T[i][j] = sum_k |B_kj| [0 < |A_ik| < 2^-113] + |A_ik| [0 < |B_kj| < 2^-113],
+    in FP64 (a matrix product of the masks with the magnitudes)."""
+    a = np.abs(np.asarray(A, dtype=np.float64))
+    b = np.abs(np.asarray(B, dtype=np.float64))
+    ma = ((a > 0) & (a < TF32_FULL)).astype(np.float64)
+    mb = ((b > 0) & (b < TF32_FULL)).astype(np.float64)
+    return ma @ b + a @ mb
+
+
+def bound_ratio(C_gpu, C_ref, S_ref, K: int, T=None) -> float:
+    """max over elements of |C_gpu - C_ref| / (2 K 2^-24 S + K 2^-149 + 2^-136 T)
+    (pass iff <= 1).  T None: no TF32 term.  A non-finite GPU value counts +inf;
+    a zero tolerance (K == 0) demands an exact match."""
+    Cg = np.asarray(C_gpu, dtype=np.float64)
+    diff = np.abs(Cg - C_ref)
+    tol = 2.0 * max(K, 1) * EPS_F32 * S_ref + K * UNDERFLOW_STEP
+    if T is not None:
+        tol = tol + TF32_FINEST * T
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(tol > 0, diff / np.where(tol > 0, tol, 1.0), np.where(diff == 0, 0.0, np.inf))
     r = np.where(np.isfinite(Cg), r, np.inf)
     return float(r.max()) if r.size else 0.0
 

@@ -77,11 +77,19 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 // Round an FP32 value to the nearest TF32 value (10 explicit mantissa bits),
 // ties to even, by integer arithmetic on the bit pattern; the low 13 bits of
-// the result are zero.  Inf stays Inf; NaN stays NaN.
+// the result are zero.  Inf stays Inf; NaN stays NaN.  A finite x whose
+// rounding would carry into the Inf exponent (|x| >= 0x7F7FF000, the top 4096
+// FP32 values) is truncated instead: there |x| is within 2^-11 of 2^128, so
+// one TF32 ulp (2^117) is at most 2^-11 |x| and x - hi stays as small,
+// relative to x, as a rounded remainder anywhere else.  So no finite x gives
+// a non-finite piece.
 __device__ __forceinline__ float tf32_rne(float x)
 {
     uint32_t u = __float_as_uint(x);
-    if ((u & 0x7F800000u) != 0x7F800000u) u += 0x0FFFu + ((u >> 13) & 1u);
+    if ((u & 0x7F800000u) != 0x7F800000u) {
+        const uint32_t r = u + 0x0FFFu + ((u >> 13) & 1u);
+        if ((r & 0x7F800000u) != 0x7F800000u) u = r;
+    }
     return __uint_as_float(u & 0xFFFFE000u);
 }
 

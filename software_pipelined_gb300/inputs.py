@@ -108,6 +108,46 @@ def small_int(seed: int, rows: int, cols: int, lo: int = -8, hi: int = 8,
     return _place(v.reshape(rows, cols), ld)
 
 
+def _bit_patterns(seed: int, rows: int, cols: int, lo: int, hi: int) -> np.ndarray:
+    """float32 values whose magnitude bit pattern is uniform on [lo, hi)
+    (integers), with a random sign (bit 0 of the same draw)."""
+    n = rows * cols
+    v = np.empty(n, dtype=np.uint32)
+    span = np.uint64(hi - lo)
+    for c0, x in _chunks(seed, n):
+        mag = ((x >> np.uint64(32)) % span + np.uint64(lo)).astype(np.uint32)
+        v[c0:c0 + len(x)] = mag | ((x & np.uint64(1)).astype(np.uint32) << np.uint32(31))
+    return v.view(np.float32).reshape(rows, cols)
+
+
+def top_of_range(seed: int, rows: int, cols: int) -> np.ndarray:
+    """Finite values from the top 8192 FP32 magnitudes (bit patterns
+    0x7F7FE000 .. 0x7F7FFFFF, about 3.4027e38 to FLT_MAX), random signs.  Half
+    of them are at least 0x7F7FF000, where rounding to 10 mantissa bits
+    would carry into the Inf exponent."""
+    return _bit_patterns(seed, rows, cols, 0x7F7FE000, 0x7F800000)
+
+
+def subnormal(seed: int, rows: int, cols: int) -> np.ndarray:
+    """Nonzero FP32 subnormals (bit patterns 1 .. 0x7FFFFF: 2^-149 up to just
+    below 2^-126), random signs."""
+    return _bit_patterns(seed, rows, cols, 1, 0x00800000)
+
+
+def scaled_exponents(seed: int, rows: int, cols: int, e_lo: int, e_hi: int) -> np.ndarray:
+    """u * 2^e per element: u uniform on [-1, 1) (24-bit grid), e an integer
+    uniform on [e_lo, e_hi] from the next draws of the same stream (so
+    magnitudes span about 2^e_lo .. 2^e_hi).  Exact in FP32 as long as
+    2^(e_lo - 23) is not below 2^-149."""
+    u = uniform_pm1(seed, rows, cols).astype(np.float64)
+    n = rows * cols
+    span = np.uint64(e_hi - e_lo + 1)
+    e = np.empty(n, dtype=np.float64)
+    for c0, x in _chunks(seed, n, start=n):
+        e[c0:c0 + len(x)] = ((x >> np.uint64(32)) % span).astype(np.int64) + e_lo
+    return (u * np.exp2(e.reshape(rows, cols))).astype(np.float32)
+
+
 def _place(M: np.ndarray, ld: int | None) -> np.ndarray:
     rows, cols = M.shape
     if ld is None or ld == cols:

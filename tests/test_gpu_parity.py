@@ -323,21 +323,18 @@ def test_tail_wave_split(shape, bn):
 
 
 @pytest.mark.parametrize("w", inputs.WORKLOADS["large_squares"], ids=lambda w: w[0])
-def test_large_squares_sampled(w):
-    # The launch configuration the bench times (dispatcher's choice), checked on
-    # sampled outputs (all four corners, the last row and column, random points).
+def test_large_squares_full_output(w):
+    # The launch configuration the bench times (the dispatcher's plan), every
+    # element of C against the oracle (at 8192^3 about 15 s of oracle on 16
+    # host cores and 1 GB of FP64 C and S).
     name, M, N, K, dist, sa, sb = w
     A, B = _operands(M, N, K, dist, sa, sb)
     C, desc, canaries, _ = run_gemm(A, B)
-    rng = np.random.default_rng(M)
-    rows = np.concatenate([[0, 0, M - 1, M - 1], np.full(64, M - 1), rng.integers(0, M, 1500),
-                           np.arange(0, M, max(M // 64, 1))])
-    cols = np.concatenate([[0, N - 1, 0, N - 1], rng.integers(0, N, 64), rng.integers(0, N, 1500),
-                           np.full(len(range(0, M, max(M // 64, 1))), N - 1)])
-    c_ref, s_ref = oracle.gemm_f64_entries(A, B, rows, cols)
-    err = oracle.normalised_error(C[rows, cols], c_ref, s_ref, K)
     assert canaries
     assert np.isfinite(C).all(), desc
+    Cref, S = oracle.gemm_f64(A, B)
+    del A, B
+    err = oracle.normalised_error(C, Cref, S, K)
     assert err <= 2.0, f"{name} {desc}: {err}"
 
 

@@ -58,3 +58,31 @@ def test_small_int_range():
     I = inputs.small_int(3, 50, 50)
     assert I.min() >= -8 and I.max() <= 8
     assert np.array_equal(I, np.round(I))
+
+
+def test_top_of_range_values():
+    T = inputs.top_of_range(41, 64, 64)
+    bits = np.abs(T).view(np.uint32)
+    assert np.isfinite(T).all()
+    assert bits.min() >= 0x7F7FE000 and bits.max() <= 0x7F7FFFFF
+    # about half would round up into the Inf exponent at 10 mantissa bits
+    assert 0.4 < float((bits >= 0x7F7FF000).mean()) < 0.6
+    assert 0.4 < float((T < 0).mean()) < 0.6
+
+
+def test_subnormal_values():
+    S = inputs.subnormal(42, 64, 64)
+    a = np.abs(S).astype(np.float64)
+    assert (a > 0).all() and (a < 2.0 ** -126).all()
+    assert a.min() >= 2.0 ** -149
+    assert 0.4 < float((S < 0).mean()) < 0.6
+
+
+def test_scaled_exponents_span_and_exactness():
+    X = inputs.scaled_exponents(43, 128, 128, -100, 100)
+    u = inputs.uniform_pm1(43, 128, 128).astype(np.float64)
+    r = X.astype(np.float64) / np.where(u == 0, 1.0, u)
+    e = np.log2(np.abs(r[u != 0]))
+    assert np.array_equal(e, np.round(e))       # an exact power of two per element
+    assert e.min() == -100 and e.max() == 100
+    assert np.array_equal(X, inputs.scaled_exponents(43, 128, 128, -100, 100))

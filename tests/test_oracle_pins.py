@@ -280,3 +280,118 @@ def test_threads_setting_does_not_change_result():
     C2, S2 = oracle.gemm_f64(A, B)
     oracle.set_threads(n0)
     assert np.array_equal(C1, C2) and np.array_equal(S1, S2)
+
+
+# ---------------------------------------------------------------------------
+# The underflow terms of the bound (tensor-core plans on tiny inputs; results
+# below FP32's normal range).  Pinned by closed forms, the threshold's two
+# sides, a symmetry, and planted mistakes.
+# ---------------------------------------------------------------------------
+
+def _grid_term_closed_forms(term):
+    K = 37
+    ok = True
+    # normal-range data has no TF32 term at all
+    A = inputs.uniform_pm1(61, 9, K)
+    B = inputs.uniform_pm1(62, K, 11)
+    ok &= bool(np.array_equal(term(A, B), np.zeros((9, 11))))
+    # A all tiny (c < 2^-113), B = 1 * v^T (normal): T_ij = K |v_j|
+    c = np.float32(2.0 ** -120)
+    v = inputs.uniform_pm1(63, 1, 11)[0] + np.float32(2.0)
+    T = term(np.full((9, K), c, np.float32), np.tile(v, (K, 1)))
+    ok &= bool(np.array_equal(T, np.tile(K * np.abs(v.astype(np.float64)), (9, 1))))
+    # B all tiny, A = u * 1^T (normal): T_ij = K |u_i|
+    u = inputs.uniform_pm1(64, 9, 1)[:, 0] - np.float32(2.0)
+    T = term(np.tile(u[:, None], (1, K)), np.full((K, 11), -c, np.float32))
+    ok &= bool(np.array_equal(T, np.tile(K * np.abs(u.astype(np.float64))[:, None], (1, 11))))
+    # both tiny: each k counts both ways, |b| + |a| = 2c per k
+    T = term(np.full((2, K), c, np.float32), np.full((K, 3), c, np.float32))
+    ok &= bool(np.array_equal(T, np.full((2, 3), 2.0 * K * float(c))))
+    return ok
+
+
+def _grid_term_threshold(term):
+    # exactly 2^-113 is carried in full; the next float below is not; zero never counts;
+    # a value between 2^-126 and 2^-113 (normal FP32, but below full resolution) does
+    vals = np.array([2.0 ** -113, np.nextafter(np.float32(2.0 ** -113), np.float32(0)), 0.0, 2.0 ** -120],
+                    dtype=np.float32)
+    A = vals[:, None]                      # 4 x 1
+    B = np.array([[3.0]], dtype=np.float32)
+    T = term(A, B)[:, 0]
+    return bool(np.array_equal(T, np.array([0.0, 3.0, 0.0, 3.0])))
+
+
+def _grid_term_symmetry(term):
+    A = inputs.scaled_exponents(65, 7, 13, -130, -100)
+    B = inputs.scaled_exponents(66, 13, 5, -130, -100)
+    return bool(np.allclose(term(A, B), term(B.T, A.T).T, rtol=1e-15, atol=0))
+
+
+GRID_PINS = [_grid_term_closed_forms, _grid_term_threshold, _grid_term_symmetry]
+
+
+@pytest.mark.parametrize("pin", GRID_PINS, ids=lambda p: p.__name__)
+def test_tf32_grid_term_pin(pin):
+    assert pin(oracle.tf32_grid_term)
+
+
+def _grid_mutants():
+    def only_a(A, B):  # dropped second term
+        a, b = np.abs(A.astype(np.float64)), np.abs(B.astype(np.float64))
+        return ((a > 0) & (a < 2.0 ** -113)).astype(np.float64) @ b
+
+    def low_threshold(A, B):  # FP32's normal boundary instead of TF32's full-resolution one
+        a, b = np.abs(A.astype(np.float64)), np.abs(B.astype(np.float64))
+        ma = ((a > 0) & (a < 2.0 ** -126)).astype(np.float64)
+        mb = ((b > 0) & (b < 2.0 ** -126)).astype(np.float64)
+        return ma @ b + a @ mb
+
+    def counts_zero(A, B):  # zero entries counted as tiny
+        a, b = np.abs(A.astype(np.float64)), np.abs(B.astype(np.float64))
+        return (a < 2.0 ** -113).astype(np.float64) @ b + a @ (b < 2.0 ** -113).astype(np.float64)
+
+    def transposed_mask(A, B):  # mask of B applied on the A side
+        a, b = np.abs(A.astype(np.float64)), np.abs(B.astype(np.float64))
+        ma = ((a > 0) & (a < 2.0 ** -113)).astype(np.float64)
+        return ma @ b + ma @ b
+    return [only_a, low_threshold, counts_zero, transposed_mask]
+
+
+@pytest.mark.parametrize("mutant", _grid_mutants(), ids=lambda m: m.__name__)
+def test_grid_pins_reject_planted_mistake(mutant):
+    assert not all(p(mutant) for p in GRID_PINS)
+
+
+def test_bound_ratio_terms():
+    K = 64
+    C = inputs.uniform_pm1(67, 5, 6).astype(np.float64)
+    S = np.abs(C) + 1.0
+    T = np.full((5, 6), 2.0 ** 118)  # a TF32 term as large as the relative one
+    tol = 2 * K * 2.0 ** -24 * S + K * 2.0 ** -149 + 2.0 ** -136 * T
+    assert oracle.bound_ratio(C + tol, C, S, K, T) == pytest.approx(1.0, rel=1e-12)
+    assert oracle.bound_ratio(C + 0.5 * tol, C, S, K, T) == pytest.approx(0.5, rel=1e-12)
+    # without T the same error exceeds the bound
+    assert oracle.bound_ratio(C + tol, C, S, K) > 1.0
+    # the underflow term alone: S = 0, an error of K 2^-149 passes, twice that fails
+    Z = np.zeros((5, 6))
+    assert oracle.bound_ratio(Z + K * 2.0 ** -149, Z, Z, K) == pytest.approx(1.0)
+    assert oracle.bound_ratio(Z + 2 * K * 2.0 ** -149, Z, Z, K) == pytest.approx(2.0)
+    # non-finite GPU values never pass; the relative bound is the underflow-free special case
+    bad = C.copy()
+    bad[1, 2] = np.nan
+    assert oracle.bound_ratio(bad, C, S, K) == np.inf
+    err = oracle.normalised_error(C + tol, C, S, K)
+    assert err > 2.0
+
+
+def test_subnormal_products_of_the_oracle_are_exact():
+    # FP64 holds every product of two FP32 values exactly, subnormals included
+    # (2^-149 * 2^-149 = 2^-298 is above FP64's 2^-1074): the oracle's C of
+    # subnormal operands is the exact rational sum.
+    A = inputs.subnormal(68, 3, 4)
+    B = inputs.subnormal(69, 4, 2)
+    C, _ = oracle.gemm_f64(A, B)
+    for i in range(3):
+        for j in range(2):
+            exact = sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(4))
+            assert abs(Fraction(C[i, j]) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
