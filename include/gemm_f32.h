@@ -101,10 +101,12 @@ typedef struct {
     int32_t variant;        /* gemm_f32_variant */
     int32_t tile_m;         /* output tile rows (SIMT: 32/64/128; TC: 128, or 256 = one tile per pair
                                of CTAs, a thread-block cluster of two sharing each tcgen05.mma
-                               (cta_group::2): operands split in the kernel only, tile_n 128 or
-                               256, tile_k 32 or 16; needs K >= 32 and lda, ldb multiples of 4,
-                               else UNSUPPORTED; a base pointer of A or B that is not 16-byte
-                               aligned runs the one-CTA pre-pass form instead) */
+                               (cta_group::2): operand_split 2, 3 or 4 (not the full pre-pass),
+                               tile_n 128 or 256, tile_k 32 or 16 (16: in the kernel, or with
+                               operand_split 4 at tile_n 256); needs K >= 32 and lda a multiple
+                               of 4 (ldb too when B is split in the kernel), else UNSUPPORTED;
+                               a base pointer the TMA cannot take runs the one-CTA pre-pass form
+                               instead) */
     int32_t tile_n;         /* output tile cols (SIMT: 32/64/128; TC: 64/128/256) */
     int32_t stages;         /* pipeline depth (SIMT: 1..4; TC: 2..8) */
     int32_t split_k;        /* K splits, 1 = none (max 64) */
@@ -125,15 +127,17 @@ typedef struct {
                                2 = inside the GEMM kernel (needs K >= 32 and lda, ldb
                                multiples of 4); 3 = A inside the kernel, B by the pre-pass
                                (needs K >= 32, lda a multiple of 4); 4 = hi of A read from
-                               A itself, lo of A and B by the pre-pass (same needs).  2, 3 and
-                               4 fall back to 1 at run time for a base pointer of A (or, for
-                               2, B) that is not 16-byte aligned */
+                               A itself, lo of A and B by the pre-pass (same needs; on CTA
+                               pairs this form has no conversion inside the kernel).  2, 3
+                               and 4 fall back to 1 at run time for a base pointer of A (or,
+                               for 2, B) that is not 16-byte aligned */
     int32_t tile_group;     /* TC only: tile order of the persistent kernel, in tile-rows per
                                raster group (1..64; 0 = the dispatcher's choice, else 8) */
     int32_t tile_k;         /* K-tile depth.  SIMT: 16/32/64 (0 = the compiled default for the
                                tile and stage count).  tcgen05: 32, or 16 for half-size,
                                twice-as-deep stages of the in-kernel split (selects that
-                               form); 0 = the dispatcher's choice */
+                               form) or of the CTA-pair form with operand_split 4; 0 = the
+                               dispatcher's choice */
     int32_t host_panels;    /* TC only, gemm_f32_run_host: row panels the host-buffer run is
                                pipelined over (A panel copies, panel GEMMs and C panel
                                copies overlap); 0 = the dispatcher's choice, 1 = none,
@@ -161,7 +165,8 @@ typedef struct {
                                its columns of B have landed (the GEMM starts after a fraction
                                of B instead of all of it).  0 = the dispatcher's choice, 1 =
                                none, at most 16; only for plans that split A inside the GEMM
-                               kernel (operand_split 2 or 3), otherwise as 1 */
+                               kernel or read hi of A from A (operand_split 2, 3 or 4),
+                               otherwise as 1 */
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */

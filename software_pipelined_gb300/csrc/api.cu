@@ -306,12 +306,15 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // forced tile_k of 16 selects that form.
             // tile_m 256: a pair of CTAs per 256-row tile (one tcgen05.mma
             // across both), operands split in the kernel only.
-            // operand_split 3 (B by the pre-pass) asks for the pairs' hybrid form
+            // operand_split 3 (B by the pre-pass) asks for the pairs' hybrid form,
+            // 4 (lo of A and B by the pre-pass) for their form without converters
             bool pair = c.tile_m == 256;
-            const int pair_split = o.operand_split == 3 ? kSplitHybrid
-                                   : o.operand_split ? kSplitInKernel
-                                                     : (c.fused == kSplitHybrid ? kSplitHybrid : kSplitInKernel);
-            if (pair && ((o.operand_split && o.operand_split != 2 && o.operand_split != 3) || o.stages ||
+            const int pair_split = o.operand_split == 4   ? kSplitRawA
+                                   : o.operand_split == 3 ? kSplitHybrid
+                                   : o.operand_split      ? kSplitInKernel
+                                   : (c.fused == kSplitHybrid || c.fused == kSplitRawA) ? c.fused
+                                                                                         : kSplitInKernel;
+            if (pair && (o.operand_split == 1 || o.stages ||
                          o.separate_syncs || o.split_reduce == 3 || K < kTcFusedMinK || lda % 4 != 0 ||
                          (pair_split == kSplitInKernel && ldb % 4 != 0))) {
                 // forced: refused; the dispatcher's choice: the one-CTA kernel
@@ -384,7 +387,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 snprintf(p->desc, sizeof p->desc,
                          "tcgen05 3xtf32 %s cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
                          "whole=%d split=%dx%d%s resident=%d group=%d kp=%lld",
-                         tcfg.split == kSplitHybrid ? "hybrid-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
+                         tcfg.split == kSplitHybrid ? "hybrid-split"
+                         : tcfg.split == kSplitRawA ? "raw-a-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
                          t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", t.pair_slots,
                          t.tile_group > 0 ? t.tile_group : 8,
                          (long long)t.kp);
@@ -463,12 +467,13 @@ bool current_device_is(int dev)
 // (measured on GB300, pinned host memory at about 200 GB/s each way: 8192^3
 // 5.18 ms with 5 panels and 3 blocks against 6.04 ms with 6 panels and none;
 // 4096^3 1.08 ms with 3 panels and 2 blocks against 1.12 ms with none, 1.27
-// with 4).  Only for plans that split A inside the GEMM kernel (the first
-// panel's blocks would otherwise each repeat that panel's pre-pass of A).
+// with 4).  For plans whose A is split in the GEMM kernel or reads hi of A
+// from A (the blocks share the first panel's pre-split lo of A, made once by
+// the first block); the full pre-pass form keeps whole panels.
 int host_col_request(const gemm_f32_plan_s* p)
 {
     const TcConfig& c = tc_config(p->tc.config_id);
-    if (c.split != kSplitInKernel && c.split != kSplitHybrid) return 1;
+    if (c.split == kSplitPrepass) return 1;
     const int q = p->opts.host_col_blocks;
     return q != 0 ? q : p->N >= 6144 ? 3 : p->N >= 2048 ? 2 : 1;
 }
@@ -663,7 +668,7 @@ cudaError_t run_host_panels(gemm_f32_plan_s* p, const float* A_host, const float
                 (e = tc_split_b(p->blocks[j], block_cols(j), p->K, p->hA, p->hB + c0, p->ldb, s)) != cudaSuccess ||
                 (j == 0 && (e = cudaStreamWaitEvent(s, ev_a[0], 0)) != cudaSuccess) ||
                 (e = tc_panel_run(p->blocks[j], panel_rows(0), block_cols(j), p->K, p->hA, p->lda, p->hB + c0,
-                                  p->ldb, p->hC + c0, p->ldc, p->d_status, s)) != cudaSuccess ||
+                                  p->ldb, p->hC + c0, p->ldc, p->d_status, s, j == 0)) != cudaSuccess ||
                 (e = cudaEventRecord(ev_cb[j], s)) != cudaSuccess)
                 return e;
         }

@@ -67,7 +67,7 @@ struct TcConfig {
     int bm, bn, bk;  // tile (bm = 128 rows = TMEM lanes, or 256 for a CTA pair; bk = 32 fp32 = 128 B)
     int stages;      // smem ring depth
     bool sep;        // separate full barriers for A and B (ablation)
-    int split;       // where the 3xTF32 split happens: kSplitPrepass, kSplitInKernel, kSplitHybrid
+    int split;       // where the 3xTF32 split happens: kSplitPrepass, kSplitInKernel, kSplitHybrid, kSplitRawA
 };
 enum : int {
     kSplitPrepass = 0,   // a pre-pass writes hi/lo of A and B to scratch
@@ -79,8 +79,8 @@ int tc_num_configs();
 const TcConfig& tc_config(int id);
 int tc_find_config(int bn, int stages, bool sep, int split, int bk = 0);
 // The CTA-pair configuration (256-row tiles) of tile width bn, stage depth bk
-// (0 = 32) and split mode (kSplitInKernel, or kSplitHybrid: B by the
-// pre-pass), or -1.
+// (0 = 32) and split mode (kSplitInKernel; kSplitHybrid: B by the pre-pass;
+// kSplitRawA: lo of A and B by the pre-pass), or -1.
 int tc_find_pair_config(int bn, int bk, int split = kSplitInKernel);
 // How many pairs of that configuration run at once on this device (0 when the
 // occupancy query fails).
@@ -170,10 +170,12 @@ cudaError_t tc_block_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
 // The B part of the pre-pass for the whole plan (when its route needs it).
 cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const float* A, const float* B,
                        int64_t ldb, cudaStream_t s);
-// One panel: its A rows' pre-pass (when needed), the GEMM, the reduction.
+// One panel: its A rows' pre-pass (when the route needs one and pre_a is set;
+// the column blocks of one panel share their rows' split A, so only the first
+// block runs it), the GEMM, the reduction.
 cudaError_t tc_panel_run(const TcPlanState& panel, int64_t mp, int64_t N, int64_t K, const float* A_panel,
                          int64_t lda, const float* B, int64_t ldb, float* C_panel, int64_t ldc, int* status,
-                         cudaStream_t s);
+                         cudaStream_t s, bool pre_a = true);
 // ev: NULL, or four events recorded before the split, before the main kernel,
 // after the main kernel and after the split-K reduction.
 cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K,

@@ -659,12 +659,14 @@ cudaError_t tc_fused_main(int bn, int bk, bool b_presplit, const TcPlanState& st
                           const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
                           const CUtensorMap& tblo, cudaStream_t s);
 
-// The CTA-pair kernel (tc_pair.cu): 256 x bn tiles, operands split in the
-// kernel, stage depth bk; the work in a's dp_tiles / split_tiles counts pair
-// tiles.  And the sum of its split pair tiles' K-slices.
-cudaError_t tc_pair_main(int bn, int bk, bool b_presplit, const TcPlanState& st, const tc::TcArgs& a,
+// The CTA-pair kernel (tc_pair.cu): 256 x bn tiles, stage depth bk; split
+// (kSplitInKernel, kSplitHybrid or kSplitRawA) says which operand pieces come
+// from the pre-pass (tbhi, tblo: B; talo: lo of A) and which the kernel's
+// converters make; the work in a's dp_tiles / split_tiles counts pair tiles.
+// And the sum of its split pair tiles' K-slices.
+cudaError_t tc_pair_main(int bn, int bk, int split, const TcPlanState& st, const tc::TcArgs& a,
                          const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
-                         const CUtensorMap& tblo, cudaStream_t s);
+                         const CUtensorMap& tblo, const CUtensorMap& talo, cudaStream_t s);
 cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const tc::TcArgs& a, cudaStream_t s);
 
 }  // namespace gemm_f32

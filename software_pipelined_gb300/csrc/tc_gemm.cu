@@ -40,18 +40,20 @@ EncodeFn get_encode()
     return fn;
 }
 
-// 2-D tensor map over a rows x kp K-major FP32 buffer, box {32, box_rows},
-// 128-byte swizzle, zero fill outside.
-cudaError_t encode_kmajor(void* out, float* base, int64_t rows, int64_t kp, int box_rows)
+// 2-D tensor map over a rows x kp K-major FP32 buffer, box {box_k, box_rows}:
+// rows of 32 FP32 in the 128-byte swizzle, of 16 in the 64-byte one; zero fill
+// outside.
+cudaError_t encode_kmajor(void* out, float* base, int64_t rows, int64_t kp, int box_rows, int box_k = kBK)
 {
     EncodeFn enc = get_encode();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)kp, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(kp * 4)};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     box_k == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -198,6 +200,11 @@ const TcEntry kTc[] = {
     // and lo_B), only lo_A computed in the kernel
     {{256, 256, 32, 3, false, kSplitHybrid}, nullptr, launch_pair_reduce<256>, false, false},
     {{256, 128, 32, 4, false, kSplitHybrid}, nullptr, launch_pair_reduce<128>, false, false},
+    // CTA pairs with lo of A and both pieces of B by the pre-pass, hi of A read
+    // from A: no conversion between a stage's copy and its MMAs
+    {{256, 256, 32, 3, false, kSplitRawA}, nullptr, launch_pair_reduce<256>, false, false},
+    {{256, 256, 16, 6, false, kSplitRawA}, nullptr, launch_pair_reduce<256>, false, false},
+    {{256, 128, 32, 4, false, kSplitRawA}, nullptr, launch_pair_reduce<128>, false, false},
 };
 
 }  // namespace
@@ -355,18 +362,23 @@ cudaError_t tc_set_partial(TcPlanState& st, float* partial)
     return encode_store_map(st.tmap_p, partial, (int64_t)(st.partial_bytes / (bn * sizeof(float))), bn, bn);
 }
 
+// k per box of the pre-split operands' tensor maps: a pair plan loads them in
+// its own stage depth, the one-CTA kernels in 32-k blocks.
+static int split_box_k(const TcConfig& c) { return c.bm == 2 * kBM ? c.bk : kBK; }
+
 cudaError_t tc_prepare(TcPlanState& st, int64_t M, int64_t N, int64_t K)
 {
     (void)K;
     const TcConfig& c = kTc[st.config_id].cfg;
+    const int bk = split_box_k(c);
     cudaError_t e;
     if ((e = tc_set_partial(st, st.partial)) != cudaSuccess) return e;
     if ((e = encode_kmajor(st.tmap_a_hi, st.a_hi, M, st.kp, kBM)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(st.tmap_a_lo, st.a_lo, M, st.kp, kBM)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(st.tmap_a_lo, st.a_lo, M, st.kp, kBM, bk)) != cudaSuccess) return e;
     // a CTA of a pair loads half of the tile's columns of the split B
     const int64_t b_rows = c.bm == 2 * kBM ? c.bn / 2 : c.bn;
-    if ((e = encode_kmajor(st.tmap_b_hi, st.b_hi, N, st.kp, b_rows)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(st.tmap_b_lo, st.b_lo, N, st.kp, b_rows)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(st.tmap_b_hi, st.b_hi, N, st.kp, b_rows, bk)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(st.tmap_b_lo, st.b_lo, N, st.kp, b_rows, bk)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
@@ -379,6 +391,7 @@ struct Route {
     bool raw_a;      // hi of A read from A
     bool pre_a;      // the pre-pass splits A (only lo with raw_a)
     bool pre_b;      // the pre-pass splits B
+    bool pair;       // a CTA-pair plan whose kernel can take these operands
 };
 
 Route route(const TcPlanState& st, const float* A, const float* B)
@@ -394,6 +407,7 @@ Route route(const TcPlanState& st, const float* A, const float* B)
     r.pre_b = !r.in_kernel || c.split == kSplitHybrid;
     // a misaligned base pointer: the pre-pass form of the same tile width
     if (!r.in_kernel && !r.raw_a && c.split != kSplitPrepass) r.id = st.fallback_config_id;
+    r.pair = c.bm == 2 * kBM && (r.in_kernel || r.raw_a);
     return r;
 }
 
@@ -465,11 +479,12 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
     if (c.bm == 2 * kBM) {
-        e = tc_pair_main(c.bn, c.bk, c.split == kSplitHybrid, st, a,
+        e = tc_pair_main(c.bn, c.bk, c.split, st, a,
                          *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw),
                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
-                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), s);
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo),
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_a_lo), s);
     } else if (r.in_kernel) {
         e = tc_fused_main(c.bn, c.bk, c.split == kSplitHybrid, st, a,
                           *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
@@ -494,16 +509,17 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
 {
     const TcConfig& c = kTc[st.config_id].cfg;
     const Route r = route(st, A, B);
-    if (c.bm == 2 * kBM && !r.in_kernel) {
+    if (c.bm == 2 * kBM && !r.pair) {
         // A CTA-pair plan with a base pointer the TMA cannot take: the one-CTA
         // pre-pass form of the same tile width, its own work decomposition,
         // the same scratch (the partial buffer holds either).
         TcPlanState fb = st;
         fb.config_id = st.fallback_config_id;
         tc_configure(fb, M, N, K, st.split_request);
-        // the split B's maps with the one-CTA tile's rows
+        // the split operands' maps with the one-CTA tile's rows and 32-k boxes
         const int64_t bn = kTc[fb.config_id].cfg.bn;
         cudaError_t e;
+        if ((e = encode_kmajor(fb.tmap_a_lo, fb.a_lo, M, fb.kp, kBM)) != cudaSuccess) return e;
         if ((e = encode_kmajor(fb.tmap_b_hi, fb.b_hi, N, fb.kp, bn)) != cudaSuccess) return e;
         if ((e = encode_kmajor(fb.tmap_b_lo, fb.b_lo, N, fb.kp, bn)) != cudaSuccess) return e;
         return tc_launch(fb, M, N, K, A, lda, B, ldb, C, ldc, status, s, ev);
@@ -540,7 +556,7 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     out.a_lo = full.a_lo + r0 * full.kp;
     cudaError_t e;
     if ((e = encode_kmajor(out.tmap_a_hi, out.a_hi, mp, out.kp, kBM)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(out.tmap_a_lo, out.a_lo, mp, out.kp, kBM)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(out.tmap_a_lo, out.a_lo, mp, out.kp, kBM, split_box_k(c))) != cudaSuccess) return e;
     const Route r = route(out, A + r0 * lda, B);
     if (r.raw_a || r.in_kernel) {
         if ((e = encode_raw_a(out.tmap_a_raw, A + r0 * lda, mp, K, lda, c.bk)) != cudaSuccess) return e;
@@ -563,8 +579,8 @@ cudaError_t tc_block_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     out.b_hi = full.b_hi + c0 * full.kp;
     out.b_lo = full.b_lo + c0 * full.kp;
     const int64_t b_rows = c.bm == 2 * kBM ? c.bn / 2 : c.bn;
-    if ((e = encode_kmajor(out.tmap_b_hi, out.b_hi, nq, out.kp, b_rows)) != cudaSuccess) return e;
-    return encode_kmajor(out.tmap_b_lo, out.b_lo, nq, out.kp, b_rows);
+    if ((e = encode_kmajor(out.tmap_b_hi, out.b_hi, nq, out.kp, b_rows, split_box_k(c))) != cudaSuccess) return e;
+    return encode_kmajor(out.tmap_b_lo, out.b_lo, nq, out.kp, b_rows, split_box_k(c));
 }
 
 cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const float* A, const float* B,
@@ -576,12 +592,12 @@ cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const floa
 
 cudaError_t tc_panel_run(const TcPlanState& panel, int64_t mp, int64_t N, int64_t K, const float* A_panel,
                          int64_t lda, const float* B, int64_t ldb, float* C_panel, int64_t ldc, int* status,
-                         cudaStream_t s)
+                         cudaStream_t s, bool pre_a)
 {
     const Route r = route(panel, A_panel, B);
     // the panels' operands are the plan's own device buffers, 16-byte aligned
-    if (kTc[panel.config_id].cfg.bm == 2 * kBM && !r.in_kernel) return cudaErrorInvalidValue;
-    cudaError_t e = prepass(panel, mp, N, K, A_panel, lda, B, ldb, r.pre_a, r.raw_a, false, s);
+    if (kTc[panel.config_id].cfg.bm == 2 * kBM && !r.pair) return cudaErrorInvalidValue;
+    cudaError_t e = prepass(panel, mp, N, K, A_panel, lda, B, ldb, r.pre_a && pre_a, r.raw_a, false, s);
     if (e != cudaSuccess) return e;
     return main_and_reduce(panel, r, make_args(panel, mp, N, C_panel, ldc, status), nullptr, s);
 }

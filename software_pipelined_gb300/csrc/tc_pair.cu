@@ -9,6 +9,11 @@
 //   * each CTA holds its own 128 rows of A (raw by TMA, lo_A by its converter
 //     warps) and HALF of the tile's B columns (raw 32 x 32 boxes by TMA,
 //     transposed to hi_B / lo_B by its converters);
+//   * or, in two lighter forms, B arrives split and transposed by the operand
+//     pre-pass (hi_B and lo_B by TMA), and in the second of them lo_A too (hi
+//     of A is the raw A, which the MMA truncates): then the converter warps
+//     only hand each landed stage to the even CTA, and no conversion sits
+//     between a stage's copy and its MMAs;
 //   * the even CTA's MMA thread issues M = 256, N = BN MMAs that read A rows
 //     0..127 and B columns 0..BN/2-1 from its own shared memory and the rest
 //     from its peer's, at the same addresses, and accumulate the even CTA's
@@ -25,7 +30,8 @@
 //              raw B (local)
 //   conv[s]    (even CTA) both CTAs' converters are done: counts 2 x 4 warps
 //              (one group of each CTA), the odd CTA's arriving remotely with
-//              release at cluster scope
+//              release at cluster scope; in the form with nothing to convert,
+//              one forwarding thread of each CTA (2 arrivals)
 //   empty[s]   the pair's MMAs of slot s completed: one commit, multicast to
 //              both CTAs
 //   tfull      accumulator complete: commit multicast to both CTAs
@@ -46,6 +52,13 @@ constexpr int kPairConvWarps = 8;
 constexpr int kConvGroups = 2;                      // converter groups, on alternate stages
 constexpr int kPairConvThreads = kPairConvWarps * 32;
 constexpr int kPairThreads = 6 * 32 + kPairConvThreads;
+
+// Where the pair kernel's operands are split.
+enum : int {
+    kPairSplitBoth = 0,  // raw A and raw B by TMA, both split by the converters
+    kPairPreB = 1,       // hi_B, lo_B from the pre-pass; lo_A by the converters
+    kPairPreAB = 2       // lo_A, hi_B, lo_B from the pre-pass; hi_A = raw A
+};
 
 // BN: the pair's tile width (each CTA holds BN/2 columns of B); KB: k per stage.
 template <int BN, int SLOTS, int KB>
@@ -243,18 +256,22 @@ __device__ bool pair_cluster_sum(const TcArgs& args, const CUtensorMap* tm_c, in
     return true;
 }
 
-// BPRE: B comes split and transposed by the pre-pass (hi and lo, K-major, by
-// TMA through tm_bhi / tm_blo: this CTA's half of the tile's columns) and the
-// converters only add lo_A; otherwise tm_b copies raw B boxes and the
-// converters split both operands.
-template <int BN, int SLOTS, int KB, bool BPRE>
+// MODE kPairPreB: B comes split and transposed by the pre-pass (hi and lo,
+// K-major, by TMA through tm_bhi / tm_blo: this CTA's half of the tile's
+// columns) and the converters only add lo_A; kPairPreAB: lo_A comes from the
+// pre-pass as well (tm_alo) and the converters convert nothing;
+// kPairSplitBoth: tm_b copies raw B boxes and the converters split both
+// operands.  The pre-split operands' tensor maps have boxes of KB k.
+template <int BN, int SLOTS, int KB, int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
-               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_p,
-               const TcArgs args)
+               const __grid_constant__ CUtensorMap tm_alo, const __grid_constant__ CUtensorMap tm_c,
+               const __grid_constant__ CUtensorMap tm_p, const TcArgs args)
 {
-    static_assert(!BPRE || KB == 32, "pre-split B comes in 32-k rows");
+    constexpr bool BPRE = MODE != kPairSplitBoth;
+    constexpr bool APRE = MODE == kPairPreAB;
+    static_assert(MODE != kPairPreB || KB == 32, "the hybrid form runs 32-k stages");
     using L = PairLayout<BN, SLOTS, KB>;
     constexpr int HALVES = kBK / KB;  // stages per 32-k block of the work decomposition
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -293,7 +310,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
             ptx::mbar_init(full_a(s), 1);
-            ptx::mbar_init(conv(s), 2 * kPairConvWarps / kConvGroups);  // one group of each CTA
+            // one group of each CTA's converters, or (nothing to convert) one
+            // forwarding thread of each CTA
+            ptx::mbar_init(conv(s), APRE ? 2 : 2 * kPairConvWarps / kConvGroups);
             ptx::mbar_init(empty(s), 1);
             ptx::mbar_init(rd(s), kPairConvWarps / kConvGroups);
         }
@@ -313,6 +332,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tm_a);
+        if (APRE) ptx::tma_prefetch_desc(&tm_alo);
         if (BPRE) {
             ptx::tma_prefetch_desc(&tm_bhi);
             ptx::tma_prefetch_desc(&tm_blo);
@@ -355,7 +375,15 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     if (fills == (uint32_t)args.withhold) continue;
                     const int kc = kh * KB;
                     const uint32_t slot = ring + s * L::SLOT_BYTES;
-                    if constexpr (BPRE) {
+                    if constexpr (APRE) {
+                        // raw A (= hi_A) and lo_A, this CTA's half of hi_B and lo_B
+                        ptx::mbar_arrive_expect_tx(full_a(s), 2 * L::A_BYTES + 2 * L::B_BYTES);
+                        ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
+                        ptx::tma_load_2d(slot + L::A_BYTES, &tm_alo, full_a(s), kc, pu.tm * kBM);
+                        const int n0 = pu.tn * BN + (int)rank * L::BH;
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES, &tm_bhi, full_a(s), kc, n0);
+                        ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, full_a(s), kc, n0);
+                    } else if constexpr (BPRE) {
                         // raw A into the A part, this CTA's half of hi_B and lo_B
                         ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + 2 * L::B_BYTES);
                         ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
@@ -475,6 +503,30 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             if (lane == 0) ptx::mbar_arrive_cluster(buf ? lead_tempty1 : lead_tempty0);
         }
         if (stop && lane == 0) give_up();
+    } else if constexpr (APRE) {
+        // ------------------------------ forwarder -----------------------------
+        // Every piece of the stage comes by TMA: one thread of each CTA hands
+        // each landed stage to the even CTA's MMA thread (release at cluster
+        // scope after its own acquire of the copies).  It takes the stages in
+        // order, and a slot is refilled only after the MMAs that needed this
+        // hand-off, so its parity wait is never a phase behind or ahead.
+        if (threadIdx.x == 6 * 32) {
+            uint32_t fills = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs) {
+                const Unit u = decode_unit(w, args);
+                for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
+                    const int s = fills % SLOTS;
+                    const uint32_t ps = (fills / SLOTS) & 1u;
+                    if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::mbar_arrive_cluster(ptx::mapa(conv(s), lead));
+                }
+            }
+            if (stop) give_up();
+        }
     } else {
         // ------------------------------ converters ----------------------------
         // Two groups of warps take alternate stages, so that one group's
@@ -604,12 +656,12 @@ pair_reduce_kernel(const float4* __restrict__ partial, int dp_pairs, int split_p
     }
 }
 
-template <int BN, int SLOTS, int KB, bool BPRE>
+template <int BN, int SLOTS, int KB, int MODE>
 cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta, const CUtensorMap& tb,
-                        const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
+                        const CUtensorMap& tbhi, const CUtensorMap& tblo, const CUtensorMap& talo, cudaStream_t s)
 {
     using L = PairLayout<BN, SLOTS, KB>;
-    auto kern = tc_pair_kernel<BN, SLOTS, KB, BPRE>;
+    auto kern = tc_pair_kernel<BN, SLOTS, KB, MODE>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     const int work = a.dp_tiles + a.split_tiles * a.splits;
@@ -620,16 +672,16 @@ cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMa
                           PairSum<BN>::ring_bytes(a.cluster) > L::RING_BYTES))
         return cudaErrorInvalidValue;
     return launch_pdl(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s, a.cluster > 1 ? 2 * a.cluster : 2,
-                      ta, tb, tbhi, tblo,
+                      ta, tb, tbhi, tblo, talo,
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
                       *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
 }
 
-template <int BN, int SLOTS, int KB, bool BPRE>
+template <int BN, int SLOTS, int KB>
 int pair_slots_for(int sms)
 {
     using L = PairLayout<BN, SLOTS, KB>;
-    auto kern = tc_pair_kernel<BN, SLOTS, KB, BPRE>;
+    auto kern = tc_pair_kernel<BN, SLOTS, KB, kPairSplitBoth>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -655,19 +707,26 @@ int pair_slots_for(int sms)
 
 }  // namespace
 
-cudaError_t tc_pair_main(int bn, int bk, bool b_presplit, const TcPlanState& st, const TcArgs& a,
+cudaError_t tc_pair_main(int bn, int bk, int split, const TcPlanState& st, const TcArgs& a,
                          const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
-                         const CUtensorMap& tblo, cudaStream_t s)
+                         const CUtensorMap& tblo, const CUtensorMap& talo, cudaStream_t s)
 {
-    if (b_presplit) {
-        if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, true>(st, a, ta, tb, tbhi, tblo, s);
-        if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, true>(st, a, ta, tb, tbhi, tblo, s);
+    if (split == kSplitRawA) {
+        if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, kPairPreAB>(st, a, ta, tb, tbhi, tblo, talo, s);
+        if (bn == 256 && bk == 16) return launch_pair<256, 6, 16, kPairPreAB>(st, a, ta, tb, tbhi, tblo, talo, s);
+        if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, kPairPreAB>(st, a, ta, tb, tbhi, tblo, talo, s);
         return cudaErrorInvalidValue;
     }
-    if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, false>(st, a, ta, tb, tbhi, tblo, s);
-    if (bn == 256 && bk == 16) return launch_pair<256, 6, 16, false>(st, a, ta, tb, tbhi, tblo, s);
-    if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, false>(st, a, ta, tb, tbhi, tblo, s);
-    if (bn == 128 && bk == 16) return launch_pair<128, 8, 16, false>(st, a, ta, tb, tbhi, tblo, s);
+    if (split == kSplitHybrid) {
+        if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, kPairPreB>(st, a, ta, tb, tbhi, tblo, talo, s);
+        if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, kPairPreB>(st, a, ta, tb, tbhi, tblo, talo, s);
+        return cudaErrorInvalidValue;
+    }
+    if (split != kSplitInKernel) return cudaErrorInvalidValue;
+    if (bn == 256 && bk == 32) return launch_pair<256, 3, 32, kPairSplitBoth>(st, a, ta, tb, tbhi, tblo, talo, s);
+    if (bn == 256 && bk == 16) return launch_pair<256, 6, 16, kPairSplitBoth>(st, a, ta, tb, tbhi, tblo, talo, s);
+    if (bn == 128 && bk == 32) return launch_pair<128, 4, 32, kPairSplitBoth>(st, a, ta, tb, tbhi, tblo, talo, s);
+    if (bn == 128 && bk == 16) return launch_pair<128, 8, 16, kPairSplitBoth>(st, a, ta, tb, tbhi, tblo, talo, s);
     return cudaErrorInvalidValue;
 }
 
@@ -687,11 +746,11 @@ cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const TcArgs& a, cudaS
 
 int tc_pair_slots(int bn, int bk, int sms)
 {
-    // the same shared memory and threads for both forms of B
-    if (bn == 256 && bk == 32) return pair_slots_for<256, 3, 32, false>(sms);
-    if (bn == 256 && bk == 16) return pair_slots_for<256, 6, 16, false>(sms);
-    if (bn == 128 && bk == 32) return pair_slots_for<128, 4, 32, false>(sms);
-    if (bn == 128 && bk == 16) return pair_slots_for<128, 8, 16, false>(sms);
+    // the same shared memory and threads for every form of the operands
+    if (bn == 256 && bk == 32) return pair_slots_for<256, 3, 32>(sms);
+    if (bn == 256 && bk == 16) return pair_slots_for<256, 6, 16>(sms);
+    if (bn == 128 && bk == 32) return pair_slots_for<128, 4, 32>(sms);
+    if (bn == 128 && bk == 16) return pair_slots_for<128, 8, 16>(sms);
     return 0;
 }
 

@@ -81,10 +81,11 @@ def candidates(M, N, K):
                         out.append(dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, split_k=sp,
                                         tile_k=bk, k_slices=ksl))
     if K >= 32 and macs >= 2 ** 27:
-        # CTA pairs (256-row tiles): operands split in the kernel, or B by the pre-pass
+        # CTA pairs (256-row tiles): operands split in the kernel, B by the
+        # pre-pass, or lo of A and B by the pre-pass (no conversion in the kernel)
         for bn in (256, 128):
-            for fused in (2, 3):
-                for tk in ((32, 16) if fused == 2 else (32,)):
+            for fused in (2, 3, 4):
+                for tk in ((32, 16) if fused == 2 or (fused == 4 and bn == 256) else (32,)):
                     for sp in [0] + SPLITS:
                         if sp <= 1 or (K + 31) // 32 >= sp:
                             out.append(dict(variant=g.VARIANT_TCGEN05, tile_m=256, tile_n=bn, stages=0,

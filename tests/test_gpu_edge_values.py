@@ -37,6 +37,8 @@ FORMS = {
     "hybrid": dict(variant=TC, operand_split=3),
     "pair_in_kernel": dict(variant=TC, tile_m=256, operand_split=2),
     "pair_hybrid": dict(variant=TC, tile_m=256, operand_split=3),
+    "pair_raw_a": dict(variant=TC, tile_m=256, operand_split=4),
+    "pair_raw_a_k16": dict(variant=TC, tile_m=256, tile_n=256, operand_split=4, tile_k=16),
     "split_k4": dict(variant=TC, split_k=4),
 }
 M, N, K = 300, 520, 264

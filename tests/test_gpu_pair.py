@@ -89,6 +89,52 @@ def test_pair_hybrid_matches_the_oracle(case):
     assert np.array_equal(outs[0], outs[1]), desc
 
 
+RAWA_CASES = [
+    # M, N, K, tile_n, tile_k, split_k: lo of A and both pieces of B by the
+    # pre-pass, hi of A the raw A; no conversion inside the kernel
+    (512, 512, 256, 256, 32, 2),
+    (300, 521, 264, 256, 32, 2),      # ldb = 521: B needs no 16-byte rows here
+    (300, 520, 264, 256, 16, 3),      # half-size stages: 64-byte swizzled boxes of every piece
+    (1024, 1024, 1024, 256, 16, 4),
+    (1024, 1024, 1024, 256, 32, 4),
+    (2048, 2048, 256, 128, 32, 1),    # several units per pair
+    (2304, 4096, 320, 256, 32, 0),    # partial last wave split automatically
+    (2304, 4096, 320, 256, 16, 0),
+    (130, 33, 96, 128, 32, 2),        # one pair, most of it past M and N
+]
+RAWA_IDS = [f"{m}x{n}x{k}_bn{bn}_k{bk}_s{s}" for m, n, k, bn, bk, s in RAWA_CASES]
+
+
+@pytest.mark.parametrize("case", RAWA_CASES, ids=RAWA_IDS)
+def test_pair_raw_a_matches_the_oracle(case):
+    M, N, K, bn, bk, split = case
+    A = inputs.uniform_pm1(2121, M, K)
+    B = inputs.normal(2122, K, N)
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, tile_n=bn, tile_k=bk, split_k=split, operand_split=4,
+                                       **PAIR)
+    assert "raw-a-split cta-pair" in desc and f"tile=256x{bn}x{bk}" in desc, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+    assert np.array_equal(outs[0], outs[1]), desc
+
+
+@pytest.mark.parametrize("bk", [32, 16])
+def test_pair_raw_a_small_integers_padding_and_misaligned_fallback(bk):
+    M, N, K = 520, 300, 200
+    A = inputs.small_int(2123, M, K, -4, 4)
+    B = inputs.small_int(2124, K, N, -4, 4)
+    exact = A.astype(np.float64) @ B.astype(np.float64)
+    opts = dict(PAIR, tile_n=256, tile_k=bk, split_k=2, operand_split=4)
+    C, desc, canaries, _ = run_gemm(A, B, **opts)
+    assert "raw-a-split cta-pair" in desc and canaries and np.array_equal(C, exact), desc
+    # padded rows of A (a multiple of 4), of B (any) and of C
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 8, ldb=N + 3, ldc=N + 5, **opts)
+    assert canaries and np.array_equal(C, exact), desc
+    # A's base off a 16-byte boundary: the one-CTA pre-pass form (its own maps)
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, a_off=1, **opts)
+    assert canaries and np.array_equal(C, exact), desc
+
+
 def test_pair_hybrid_small_integers_and_misaligned_fallback():
     M, N, K = 520, 300, 200
     A = inputs.small_int(2117, M, K, -4, 4)
@@ -126,9 +172,9 @@ def test_pair_padded_leading_dimensions_and_misaligned_fallback():
 
 
 @pytest.mark.parametrize("opts", [
-    dict(operand_split=1), dict(operand_split=4), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=3),
-    dict(tile_n=64), dict(tile_k=64), dict(operand_split=3, tile_k=16),
-], ids=["pre_pass", "raw_a", "stages", "separate_syncs", "last_arriver", "bn64", "tile_k64", "hybrid_k16"])
+    dict(operand_split=1), dict(stages=2), dict(separate_syncs=1), dict(split_reduce=3),
+    dict(tile_n=64), dict(tile_k=64), dict(operand_split=3, tile_k=16), dict(operand_split=4, tile_n=128, tile_k=16),
+], ids=["pre_pass", "stages", "separate_syncs", "last_arriver", "bn64", "tile_k64", "hybrid_k16", "raw_a_bn128_k16"])
 def test_pair_refusals(opts):
     with pytest.raises(g.GemmError) as e:
         g.Plan(512, 512, 512, **dict(PAIR, **opts))
@@ -235,7 +281,7 @@ def test_pair_cluster_sum_withheld_stage_times_out():
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
 
 
-@pytest.mark.parametrize("mode", [2, 3], ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", [2, 3, 4], ids=["in_kernel", "hybrid", "raw_a"])
 def test_pair_run_host_blocks_ragged_with_splits(mode):
     # Ragged M and N (the last panel's second tile row and the last block's
     # columns past the edge), K-slices in every panel's last wave, padded C:
@@ -257,7 +303,7 @@ def test_pair_run_host_blocks_ragged_with_splits(mode):
             assert (C[:, N:] == 321.0).all()
 
 
-@pytest.mark.parametrize("mode", [2, 3], ids=["in_kernel", "hybrid"])
+@pytest.mark.parametrize("mode", [2, 3, 4], ids=["in_kernel", "hybrid", "raw_a"])
 @pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (3, 2), (2, 3)])
 def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels, cols):
     # Without a K-split every tile is summed in the same order whichever 256-row
