@@ -167,6 +167,12 @@ typedef struct {
                                none, at most 16; only for plans that split A inside the GEMM
                                kernel or read hi of A from A (operand_split 2, 3 or 4),
                                otherwise as 1 */
+    int32_t simt_fragments;  /* SIMT only: how each thread's register fragments come from the
+                               staged tiles.  0 = 16-byte shared-memory loads that lanes
+                               needing the same values share (broadcast; default); 1 = each
+                               distinct value read once per warp and handed to the lanes by
+                               warp shuffles (an ablation, compiled for a few tiles only;
+                               UNSUPPORTED elsewhere) */
 } gemm_f32_opts;
 
 /* Fill *opts with the defaults (all zero). INVALID_ARG if opts is NULL. */
@@ -174,7 +180,11 @@ GEMM_F32_API gemm_f32_status gemm_f32_opts_init(gemm_f32_opts* opts);
 
 /*
  * Make a plan for C[M x N] = A[M x K] * B[K x N] with the given leading
- * dimensions.  Chooses the kernel and its configuration, allocates the plan's
+ * dimensions: the product the pages' tiled kernel computes ("Case Study: The
+ * Double-Buffered GEMM", its kernel listing: each output tile is the sum, over
+ * the K-tiles staged in on-chip memory, of the products of A's row panel and
+ * B's column panel).  The plan fixes what that kernel takes besides the
+ * matrices: the sizes, and here the leading dimensions.  Chooses the kernel and its configuration, allocates the plan's
  * scratch memory on the current device (cudaMalloc) and prepares the tensor
  * maps of that scratch.  Pointers to A, B and C are given only at run time.
  *
@@ -214,8 +224,12 @@ GEMM_F32_API gemm_f32_status gemm_f32_plan_batched(int64_t M, int64_t N, int64_t
                                                    gemm_f32_plan_t* plan);
 
 /*
- * Enqueue C = A*B on `stream`.  A, B, C are device pointers with the plan's
- * shapes and leading dimensions.  Asynchronous: returns after the launches are
+ * Enqueue C = A*B on `stream`: one pass of the pipelined K-loop over every
+ * output tile ("Double Buffering" technique page: the next K-tile is fetched
+ * while the current one is multiplied, one synchronisation per K-tile
+ * publishing the copy and freeing the buffer it will overwrite; "Case Study:
+ * The Double-Buffered GEMM", kernel listing).  A, B, C are device pointers
+ * with the plan's shapes and leading dimensions.  Asynchronous: returns after the launches are
  * queued; nothing is synchronised.  INVALID_ARG for a NULL plan or a NULL
  * pointer with non-empty work; CUDA if a launch fails.  A device-side timeout
  * is reported later by gemm_f32_check.
@@ -287,23 +301,28 @@ GEMM_F32_API gemm_f32_status gemm_f32_trace_read(gemm_f32_plan_t plan, float* ms
  * latency-critical path that must not take the allocator's locks.
  * gemm_f32_plan allocates its scratch with cudaMalloc; this call does not.
  *
- * It runs the SIMT FFMA kernel with K split into `split_k` slices (2..64; the
- * slices are rounded to whole K-tiles, so fewer may run) followed by the
- * deterministic split-K reduction.  The partial products live in one fixed
+ * It runs the SIMT FFMA kernel with K split into `split_k` slices (2..64),
+ * followed by the deterministic split-K reduction.  The slices hold whole
+ * 16-deep K-tiles, so s = ceil(K / (16 * ceil(ceil(K / split_k) / 16))) of
+ * them run (s <= split_k; s = 1 for K <= 16, which writes C directly and
+ * uses no scratch).  The partial products of s > 1 slices live in one fixed
  * 8 MiB array inside the library image, which every GPU that loads the
- * library holds until the process exits; the call needs
- * split_k * M * round_up(N, 4) floats of it and returns INVALID_ARG when that
- * exceeds 2^21 floats (8 MiB).  Nothing in the call runs cudaMalloc, cudaFree
- * or any other allocating routine.
+ * library holds until the process exits; the call needs s * M * round_up(N, 4)
+ * floats of it and returns INVALID_ARG when that exceeds 2^21 floats (8 MiB).
+ * Nothing in the call runs cudaMalloc, cudaFree or any other allocating
+ * routine.
  *
  * A, B, C are device pointers with the layout of the conventions above; the
- * call is asynchronous on `stream`.  The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  All calls share the one
- * array and each overwrites what the last one left; every partial is written
- * in full before it is read, so nothing has to start at zero.  Calls whose
- * executions overlap on the GPU (different streams, or several host threads)
- * race on the array and give wrong results: serialise them.
+ * call is asynchronous on `stream`.  Each call that uses the array looks up
+ * its device address in the current context (cudaGetSymbolAddress, which
+ * allocates nothing), so the address stays right even if the device's
+ * context is destroyed and created again.  The first such call on a device
+ * also makes the library's device code resident there: make it before any
+ * stream capture.  All calls share the one array and each overwrites what
+ * the last one left; every partial is written in full before it is read, so
+ * nothing has to start at zero.  Calls whose executions overlap on the GPU
+ * (different streams, or several host threads) race on the array and give
+ * wrong results: serialise them.
  *
  * INVALID_ARG: bad sizes or leading dimensions, split_k outside 2..64, NULL
  * pointers with non-empty work, or partials larger than the array.

@@ -43,7 +43,7 @@ class Opts(ctypes.Structure):
                 ("separate_syncs", ctypes.c_int32), ("operand_split", ctypes.c_int32),
                 ("tile_group", ctypes.c_int32), ("tile_k", ctypes.c_int32), ("host_panels", ctypes.c_int32),
                 ("split_reduce", ctypes.c_int32), ("k_slices", ctypes.c_int32),
-                ("host_col_blocks", ctypes.c_int32)]
+                ("host_col_blocks", ctypes.c_int32), ("simt_fragments", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -206,7 +206,7 @@ class Plan:
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, *, variant=VARIANT_AUTO, tile_m=0,
                  tile_n=0, stages=0, split_k=0, tf32_terms=0, wait_timeout_cycles=0,
                  debug_withhold_stage=0, separate_syncs=0, operand_split=0, tile_group=0, tile_k=0, host_panels=0,
-                 split_reduce=0, k_slices=0, host_col_blocks=0, batch=None,
+                 split_reduce=0, k_slices=0, host_col_blocks=0, simt_fragments=0, batch=None,
                  stride_a=0, stride_b=0, stride_c=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.lda = int(lda if lda is not None else max(K, 1))
@@ -224,6 +224,7 @@ class Plan:
         o.split_reduce = split_reduce
         o.k_slices = k_slices
         o.host_col_blocks = host_col_blocks
+        o.simt_fragments = simt_fragments
         if batch is None:
             s, h = gemm_f32_plan_ex(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, o)
         else:

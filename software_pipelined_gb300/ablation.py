@@ -8,12 +8,18 @@
    "Transformation and safety boundary" and "Controlled implementation
    comparison"): publishing A and B with one synchronisation instead of one
    each, with the dynamic barrier counts beside the time.
+3. Fragment loads of the SIMT kernel ("Case Study: The Double-Buffered GEMM",
+   kernel listing: fragments of the staged tiles feed the multiply-adds):
+   16-byte shared-memory loads that lanes needing the same values share
+   (broadcast) against one read per distinct value and warp shuffles, on the
+   small shapes and at 2048^3.
 
 For every benchmark shape each variant is planned with forced options and
 timed as CUDA-graph replays of back-to-back runs (device time, no host
 launch overhead).  Prints a JSON document (and a markdown table with --md):
 
     python -m software_pipelined_gb300.ablation --json ablation.json --md
+    python -m software_pipelined_gb300.ablation --only fragments --md
 """
 from __future__ import annotations
 
@@ -57,6 +63,18 @@ COALESCE = [
 ]
 
 
+FRAGMENTS = [
+    ("simt 128x128x16 S=2", dict(variant=1, tile_m=128, tile_n=128, stages=2, tile_k=16, split_k=1)),
+    ("simt 64x64x16 S=2", dict(variant=1, tile_m=64, tile_n=64, stages=2, tile_k=16, split_k=1)),
+    ("simt 64x64x16 S=4 2 K-groups", dict(variant=1, tile_m=64, tile_n=64, stages=4, tile_k=16, k_slices=2,
+                                          split_k=1)),
+    ("simt 32x32x32 S=3 4 K-groups", dict(variant=1, tile_m=32, tile_n=32, stages=3, tile_k=32, k_slices=4,
+                                          split_k=1)),
+]
+FRAGMENT_SHAPES = [w for key in ("tiny_32", "small_ragged", "tall_skinny", "square_1024")
+                   for w in inputs.WORKLOADS[key]] + [("2048x2048x2048", 2048, 2048, 2048, "uniform", 7001, 7002)]
+
+
 def barrier_count(opts, sep, K, bk):
     """Dynamic barriers one CTA executes over L = ceil(K/bk) K-tiles.
     SIMT: block-wide __syncthreads; tensor cores: mbarrier waits of the MMA
@@ -83,11 +101,24 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--json", default=None)
     ap.add_argument("--md", action="store_true")
+    ap.add_argument("--only", choices=["depth", "fragments"], default=None,
+                    help="depth: the depth and coalescing tables only; fragments: the fragment-load table only")
     args = ap.parse_args()
     g.load()
     stream = torch.cuda.current_stream()
-    out = {"depth": [], "coalesce": []}
-    for (name, M, N, K, dist, sa, sb) in SHAPES:
+    out = {"depth": [], "coalesce": [], "fragments": []}
+    for (name, M, N, K, dist, sa, sb) in (FRAGMENT_SHAPES if args.only != "depth" else []):
+        A, B = inputs.make_operands(M, N, K, dist, sa, sb)
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        for label, o in FRAGMENTS:
+            tb, db = measure(M, N, K, dict(o, simt_fragments=0), dA, dB, dC, stream)
+            ts, ds = measure(M, N, K, dict(o, simt_fragments=1), dA, dB, dC, stream)
+            out["fragments"].append({"shape": name, "variant": label, "broadcast_us": tb, "shuffle_us": ts,
+                                     "shuffle_over_broadcast": round(ts / tb, 4) if tb and ts else None})
+            print(json.dumps(out["fragments"][-1]), flush=True)
+        del dA, dB, dC
+    for (name, M, N, K, dist, sa, sb) in (SHAPES if args.only != "fragments" else []):
         A, B = inputs.make_operands(M, N, K, dist, sa, sb)
         dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
         dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
@@ -114,7 +145,14 @@ def main():
     if args.json:
         with open(args.json, "w") as f:
             json.dump(out, f, indent=1)
-    if args.md:
+    if args.md and out["fragments"]:
+        print("| shape | variant | broadcast loads (us) | warp shuffles (us) | shuffles/broadcast |")
+        print("|---|---|---:|---:|---:|")
+        for r in out["fragments"]:
+            print(f"| {r['shape']} | {r['variant']} | {r['broadcast_us']} | {r['shuffle_us']} | "
+                  f"{r['shuffle_over_broadcast']} |")
+        print()
+    if args.md and out["depth"]:
         labels = [l for l, _ in DEPTH]
         print("| shape | " + " | ".join(labels) + " |")
         print("|---|" + "---:|" * len(labels))

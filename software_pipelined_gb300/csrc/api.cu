@@ -116,6 +116,10 @@ gemm_f32_status validate_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int6
     return GEMM_F32_OK;
 }
 
+// The options struct as the header lays it out (a binding that mirrors it,
+// such as the package's ctypes one, depends on this size).
+static_assert(sizeof(gemm_f32_opts) == 72, "gemm_f32_opts layout");
+
 gemm_f32_status validate_opts(const gemm_f32_opts& o)
 {
     if (o.variant < 0 || o.variant > GEMM_F32_VARIANT_TCGEN05) return GEMM_F32_ERR_INVALID_ARG;
@@ -131,6 +135,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.split_reduce < 0 || o.split_reduce > 3) return GEMM_F32_ERR_INVALID_ARG;
     if (!(o.k_slices == 0 || o.k_slices == 1 || o.k_slices == 2 || o.k_slices == 4)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_col_blocks < 0 || o.host_col_blocks > 16) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.simt_fragments != 0 && o.simt_fragments != 1) return GEMM_F32_ERR_INVALID_ARG;
     return GEMM_F32_OK;
 }
 
@@ -272,7 +277,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             p->kind = kSimt;
             const int ksl = o.k_slices ? o.k_slices : c.k_slices ? c.k_slices : 1;
             p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages, o.separate_syncs != 0,
-                                          o.tile_k ? o.tile_k : c.tile_k, ksl);
+                                          o.tile_k ? o.tile_k : c.tile_k, ksl, o.simt_fragments != 0);
             if (p->simt_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             const int bk = simt_config(p->simt_id).bk;
             int64_t split = c.split_k < 1 ? 1 : c.split_k;
@@ -289,8 +294,9 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             char ks[24] = "";
             if (sc.ksl > 1) snprintf(ks, sizeof ks, " k_slices=%d", sc.ksl);
             snprintf(p->desc, sizeof p->desc,
-                     "simt tile=%dx%dx%d thread=%dx%d stages=%d%s%s split_k=%d", sc.bm, sc.bn, sc.bk,
-                     sc.tm, sc.tn, sc.stages, sc.sep ? " separate-syncs" : "", ks, p->split_k);
+                     "simt tile=%dx%dx%d thread=%dx%d stages=%d%s%s%s split_k=%d", sc.bm, sc.bn, sc.bk,
+                     sc.tm, sc.tn, sc.stages, sc.sep ? " separate-syncs" : "", ks,
+                     sc.shfl ? " shuffle-fragments" : "", p->split_k);
         } else {
             // The two-piece TF32 split keeps 22 of FP32's 24 significand bits, so
             // each product carries an error up to about 3*2^-22*|a||b|; against the
@@ -1001,6 +1007,6 @@ const char* gemm_f32_status_string(gemm_f32_status s)
     return "GEMM_F32_ERR_UNKNOWN";
 }
 
-int gemm_f32_version(void) { return 101; }
+int gemm_f32_version(void) { return 200; }
 
 }  // extern "C"

@@ -32,12 +32,13 @@ struct SimtConfig {
     int stages;       // cp.async ring depth (1 = single buffer, 2 = double, ...)
     bool sep;         // A and B published by separate barriers (ablation)
     int ksl = 1;      // K-slice groups inside the CTA (sliced K)
+    bool shfl = false; // fragments handed out by warp shuffles (ablation), not broadcast loads
 };
 // Configurations compiled into the library; `id` indexes this table.
 int simt_num_configs();
 const SimtConfig& simt_config(int id);
 // bk = 0: the first compiled K-tile depth for that tile and ring.  -1 if none.
-int simt_find_config(int bm, int bn, int stages, bool sep = false, int bk = 0, int ksl = 1);
+int simt_find_config(int bm, int bn, int stages, bool sep = false, int bk = 0, int ksl = 1, bool shfl = false);
 
 struct SimtArgs {
     int64_t M, N, K;

@@ -10,10 +10,9 @@
 // This entry point runs the SIMT FFMA kernel in split-K mode and keeps the
 // per-split partial products in one fixed array that is part of the library
 // image (a file-scope __device__ array).  Every GPU that loads the library
-// holds that array, kNoAllocScratchBytes of it, until the process exits.
+// holds that array, 8 MiB of it, until the process exits.
 // Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <cstdint>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -22,31 +21,23 @@
 namespace gemm_f32 {
 namespace {
 
-// 8 MiB of partial sums: split_k * M * round_up(N, 4) floats must fit.
+// 8 MiB of partial sums: (K-slices that run) * M * round_up(N, 4) floats must fit.
 constexpr int64_t kNoAllocScratchFloats = int64_t(2) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
-std::mutex g_setup_mutex;
-float* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (the host-side symbol is only a stand-in, never a device address).
-cudaError_t scratch_for_current_device(float** out)
+// Device address of the scratch array in the current context.  In host code
+// the array's name is only a stand-in, never a device address, so every call
+// looks the address up (a table lookup that allocates nothing).  Looking it up
+// each time, rather than caching it per device, keeps it right when the
+// device's primary context is destroyed and created again in this process
+// (the array may then sit at another address).
+cudaError_t scratch_for_current_context(float** out)
 {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<float*>(p);
-    }
-    *out = g_scratch_addr[dev];
+    *out = static_cast<float*>(p);
     return cudaSuccess;
 }
 
@@ -84,10 +75,13 @@ extern "C" gemm_f32_status gemm_f32_run_splitk_noalloc(int64_t M, int64_t N, int
     int64_t chunk = ((K + split_k - 1) / split_k + bk - 1) / bk * bk;
     const int64_t splits = (K + chunk - 1) / chunk;  // no empty K-slice
     const int64_t ldp = (N + 3) / 4 * 4;
-    if (splits * M * ldp > kNoAllocScratchFloats) return GEMM_F32_ERR_INVALID_ARG;
-
+    // A single K-slice writes C directly and needs no scratch.  M * ldp < 2^62,
+    // so the comparison cannot overflow.
     float* scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != cudaSuccess) return GEMM_F32_ERR_CUDA;
+    if (splits > 1) {
+        if (M * ldp > kNoAllocScratchFloats / splits) return GEMM_F32_ERR_INVALID_ARG;
+        if (scratch_for_current_context(&scratch) != cudaSuccess) return GEMM_F32_ERR_CUDA;
+    }
 
     SimtArgs a{};
     a.M = M; a.N = N; a.K = K;

@@ -1,4 +1,4 @@
-// Instantiations of the SIMT kernel, part c of 4 (split only to compile in
+// Instantiations of the SIMT kernel, part c of 5 (split only to compile in
 // parallel).
 #include "simt_kernel.cuh"
 

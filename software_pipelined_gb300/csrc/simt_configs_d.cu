@@ -1,4 +1,4 @@
-// Instantiations of the SIMT kernel, part d of 4: K split inside the CTA
+// Instantiations of the SIMT kernel, part d of 5: K split inside the CTA
 // (sliced K) for the small and skinny shapes, whose grids hold too few warps.
 #include "simt_kernel.cuh"
 

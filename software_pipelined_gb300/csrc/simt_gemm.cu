@@ -14,6 +14,8 @@ extern const SimtEntry kSimtPartC[];
 extern const int kSimtPartCCount;
 extern const SimtEntry kSimtPartD[];
 extern const int kSimtPartDCount;
+extern const SimtEntry kSimtPartE[];
+extern const int kSimtPartECount;
 }  // namespace simt_detail
 
 namespace {
@@ -28,7 +30,9 @@ const SimtEntry& entry(int id)
     if (id < kSimtPartBCount) return kSimtPartB[id];
     id -= kSimtPartBCount;
     if (id < kSimtPartCCount) return kSimtPartC[id];
-    return kSimtPartD[id - kSimtPartCCount];
+    id -= kSimtPartCCount;
+    if (id < kSimtPartDCount) return kSimtPartD[id];
+    return kSimtPartE[id - kSimtPartDCount];
 }
 
 }  // namespace
@@ -36,16 +40,17 @@ const SimtEntry& entry(int id)
 int simt_num_configs()
 {
     using namespace simt_detail;
-    return kSimtPartACount + kSimtPartBCount + kSimtPartCCount + kSimtPartDCount;
+    return kSimtPartACount + kSimtPartBCount + kSimtPartCCount + kSimtPartDCount + kSimtPartECount;
 }
 const SimtConfig& simt_config(int id) { return entry(id).cfg; }
-int simt_find_config(int bm, int bn, int stages, bool sep, int bk, int ksl)
+int simt_find_config(int bm, int bn, int stages, bool sep, int bk, int ksl, bool shfl)
 {
     // bk == 0: the shallowest K-tile compiled for this tile, ring and slicing
     int best = -1;
     for (int i = 0; i < simt_num_configs(); ++i) {
         const SimtConfig& c = entry(i).cfg;
-        if (c.bm != bm || c.bn != bn || c.stages != stages || c.sep != sep || c.ksl != ksl) continue;
+        if (c.bm != bm || c.bn != bn || c.stages != stages || c.sep != sep || c.ksl != ksl || c.shfl != shfl)
+            continue;
         if (bk != 0 && c.bk != bk) continue;
         if (best < 0 || c.bk < entry(best).cfg.bk) best = i;
     }

@@ -25,10 +25,22 @@
 //
 // Layout: A tile As[BM][BK+4] (row-major, as in global memory, so the copy is a
 // straight 16-byte cp.async when rows are 16-byte aligned), B tile
-// Bs[BK][BN+4].  Each thread owns a TM x TN register tile built from 4x4 blocks
+// Bs[BK][BN+4].  An operand whose rows are not 16-byte aligned (VA / VB false:
+// a leading dimension that is not a multiple of 4, or a base off a 16-byte
+// boundary) is staged through registers in the steady state: each thread loads 4
+// consecutive floats of a row (four 4-byte loads, consecutive threads on
+// consecutive chunks) and writes them with one 16-byte shared store.  In the
+// multi-stage loop those loads of tile t+S-1 are issued before tile t's FFMAs
+// and their shared stores follow them, so the copy still overlaps the math;
+// the prologue's tiles go by 4-byte cp.async, all in flight at once.
+// Each thread owns a TM x TN register tile built from 4x4 blocks
 // spread BM/(TM/4) rows and BN/(TN/4) columns apart, so that a warp's 16-byte
 // fragment loads hit distinct banks.  A fragments are read as float4 along k
-// (4 k-steps per load), B fragments as float4 along n.
+// (4 k-steps per load), B fragments as float4 along n: lanes that need the
+// same float4 read the same address, which shared memory broadcasts.  SHF is
+// the alternative of the task statement's "warp-shuffle fragment loads" (an
+// ablation): each distinct float4 a warp needs is read by one lane and handed
+// to the others with shuffles.
 #pragma once
 #include <cstdint>
 
@@ -38,7 +50,7 @@
 namespace gemm_f32 {
 namespace simt_detail {
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL, bool SHF>
 struct SimtKernel {
     static constexpr int TX = BN / TN;
     static constexpr int TY = BM / TM;
@@ -56,13 +68,20 @@ struct SimtKernel {
     static_assert(NT >= 32 && NTT <= 1024, "block size");
     static_assert(!SEP || STAGES <= 2, "separate barriers: 1 or 2 stages");
     static_assert(!SEP || KSL == 1, "the barrier ablation runs unsliced");
+    static_assert(!SHF || (32 % TX == 0 && (32 / TX) * TM <= 32 && BN / 4 <= 32 && NT % 32 == 0),
+                  "shuffle fragments: a warp's distinct float4 fit its lanes");
+    // chunks of 4 floats per tile, and per thread when staged through registers
+    static constexpr int A_CH = BM * BK / 4;
+    static constexpr int B_CH = BK * BN / 4;
+    static constexpr int RA = VA ? 1 : (A_CH + NTT - 1) / NTT;
+    static constexpr int RB = VB ? 1 : (B_CH + NTT - 1) / NTT;
 };
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL, bool SHF>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN) * KSL)
 simt_gemm_kernel(SimtArgs a)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
+    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL, SHF>;
     constexpr int NT = KT::NT, NTT = KT::NTT, TX = KT::TX;
     constexpr int RG = TM / 4, CG = TN / 4;
     extern __shared__ __align__(16) float smem[];
@@ -86,8 +105,73 @@ simt_gemm_kernel(SimtArgs a)
     // the first copy (a no-op when launched without the attribute).
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
-    // Issue the cp.async copies of K-tile t into ring slot st.  Out-of-range
-    // elements (ragged M, N or K) are zero-filled by the copy itself.
+    // Register staging of the operands whose rows are not 16-byte aligned:
+    // chunk c of a tile is 4 consecutive floats of one row; out-of-range
+    // elements (ragged M, N or K) are zeros.
+    float4 ra[KT::RA], rb[KT::RB];
+    auto gather_a = [&](int t) {
+        const int64_t k0 = kbeg + (int64_t)t * BK;
+#pragma unroll
+        for (int i = 0; i < KT::RA; ++i) {
+            const int c = tid + i * NTT;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (c < KT::A_CH) {
+                const int r = c / (BK / 4), kc = (c % (BK / 4)) * 4;
+                const int64_t gm = m0 + r, gk = k0 + kc;
+                if (gm < M) {
+                    const float* p = A + gm * a.lda + gk;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gk + j < kend) v[j] = __ldg(p + j);
+                }
+            }
+            ra[i] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    };
+    auto put_a = [&](int st) {
+        float* as = As + st * KT::A_STAGE;
+#pragma unroll
+        for (int i = 0; i < KT::RA; ++i) {
+            const int c = tid + i * NTT;
+            if (c < KT::A_CH)
+                *reinterpret_cast<float4*>(as + (c / (BK / 4)) * KT::LDA_S + (c % (BK / 4)) * 4) = ra[i];
+        }
+    };
+    auto gather_b = [&](int t) {
+        const int64_t k0 = kbeg + (int64_t)t * BK;
+#pragma unroll
+        for (int i = 0; i < KT::RB; ++i) {
+            const int c = tid + i * NTT;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (c < KT::B_CH) {
+                const int r = c / (BN / 4), nc = (c % (BN / 4)) * 4;
+                const int64_t gk = k0 + r, gn = n0 + nc;
+                if (gk < kend) {
+                    const float* p = B + gk * a.ldb + gn;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gn + j < N) v[j] = __ldg(p + j);
+                }
+            }
+            rb[i] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    };
+    auto put_b = [&](int st) {
+        float* bs = Bs + st * KT::B_STAGE;
+#pragma unroll
+        for (int i = 0; i < KT::RB; ++i) {
+            const int c = tid + i * NTT;
+            if (c < KT::B_CH)
+                *reinterpret_cast<float4*>(bs + (c / (BN / 4)) * KT::LDB_S + (c % (BN / 4)) * 4) = rb[i];
+        }
+    };
+
+    // Copies of K-tile t into ring slot st, all by cp.async (out-of-range
+    // elements zero-filled by the copy itself): 16 bytes at a time for 16-byte
+    // aligned rows, else four 4-byte copies per chunk of 4 floats.  These serve
+    // the prologue (every tile of it in flight at once) and the single-stage
+    // and barrier-ablation loops; the multi-stage loop stages unaligned rows
+    // through registers instead (gather / put), which measured faster there.
     auto load_a = [&](int st, int t) {
         const int64_t k0 = kbeg + (int64_t)t * BK;
         float* as = As + st * KT::A_STAGE;
@@ -104,12 +188,16 @@ simt_gemm_kernel(SimtArgs a)
                 ptx::cp_async_16(ptx::smem_u32(as + r * KT::LDA_S + kc), src, bytes);
             }
         } else {
-            for (int e = tid; e < BM * BK; e += NTT) {
-                const int r = e / BK, kk = e % BK;
-                const int64_t gm = m0 + r, gk = k0 + kk;
-                const bool ok = gm < M && gk < kend;
-                ptx::cp_async_4(ptx::smem_u32(as + r * KT::LDA_S + kk),
-                                ok ? A + gm * a.lda + gk : A, ok ? 4 : 0);
+            for (int c = tid; c < KT::A_CH; c += NTT) {
+                const int r = c / (BK / 4), kc = (c % (BK / 4)) * 4;
+                const int64_t gm = m0 + r, gk = k0 + kc;
+                const uint32_t d = ptx::smem_u32(as + r * KT::LDA_S + kc);
+                const float* p = A + (gm < M ? gm : 0) * a.lda + gk;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool ok = gm < M && gk + j < kend;
+                    ptx::cp_async_4(d + 4 * j, ok ? p + j : A, ok ? 4 : 0);
+                }
             }
         }
     };
@@ -129,12 +217,16 @@ simt_gemm_kernel(SimtArgs a)
                 ptx::cp_async_16(ptx::smem_u32(bs + r * KT::LDB_S + nc), src, bytes);
             }
         } else {
-            for (int e = tid; e < BK * BN; e += NTT) {
-                const int r = e / BN, nn = e % BN;
-                const int64_t gk = k0 + r, gn = n0 + nn;
-                const bool ok = gk < kend && gn < N;
-                ptx::cp_async_4(ptx::smem_u32(bs + r * KT::LDB_S + nn),
-                                ok ? B + gk * a.ldb + gn : B, ok ? 4 : 0);
+            for (int c = tid; c < KT::B_CH; c += NTT) {
+                const int r = c / (BN / 4), nc = (c % (BN / 4)) * 4;
+                const int64_t gk = k0 + r, gn = n0 + nc;
+                const uint32_t d = ptx::smem_u32(bs + r * KT::LDB_S + nc);
+                const float* p = B + (gk < kend ? gk : 0) * a.ldb + gn;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool ok = gk < kend && gn + j < N;
+                    ptx::cp_async_4(d + 4 * j, ok ? p + j : B, ok ? 4 : 0);
+                }
             }
         }
     };
@@ -149,6 +241,19 @@ simt_gemm_kernel(SimtArgs a)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
+    // Shuffle fragments: this warp's first thread-grid row, and the float4
+    // each lane reads for the warp (A: row w*TM + i of the warp's WR x TM rows;
+    // B: column chunk h*TX + x of the BN/4 chunks).
+    constexpr int WR = SHF ? 32 / TX : 1;
+    const int lane = tt & 31;
+    const int ty0 = (tt & ~31) / TX;
+    auto shfl4 = [](const float4& v, int src) {
+        return make_float4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                           __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
+    };
+    const int a_row_of_lane = ((lane % TM) / 4) * (BM / RG) + (ty0 + lane / TM) * 4 + (lane % 4);
+    const int b_col_of_lane = (lane / TX) * (BN / CG) + (lane % TX) * 4;
+
     auto compute_tile = [&](int st) {
         const float* as = As + st * KT::A_STAGE;
         const float* bs = Bs + st * KT::B_STAGE;
@@ -156,21 +261,39 @@ simt_gemm_kernel(SimtArgs a)
         for (int k4 = 0; k4 < BK / KSL; k4 += 4) {
             const int kk = slice * (BK / KSL) + k4;
             float4 av[TM];
+            if constexpr (SHF) {
+                float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (lane < WR * TM) mine = *reinterpret_cast<const float4*>(as + a_row_of_lane * KT::LDA_S + kk);
 #pragma unroll
-            for (int g = 0; g < RG; ++g)
+                for (int i = 0; i < TM; ++i) av[i] = shfl4(mine, (ty - ty0) * TM + i);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    av[g * 4 + i] = *reinterpret_cast<const float4*>(
-                        as + (g * (BM / RG) + ty * 4 + i) * KT::LDA_S + kk);
+                for (int g = 0; g < RG; ++g)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        av[g * 4 + i] = *reinterpret_cast<const float4*>(
+                            as + (g * (BM / RG) + ty * 4 + i) * KT::LDA_S + kk);
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float bv[TN];
+                if constexpr (SHF) {
+                    float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (lane < BN / 4) mine = *reinterpret_cast<const float4*>(bs + (kk + q) * KT::LDB_S + b_col_of_lane);
 #pragma unroll
-                for (int h = 0; h < CG; ++h) {
-                    const float4 t = *reinterpret_cast<const float4*>(
-                        bs + (kk + q) * KT::LDB_S + h * (BN / CG) + tx * 4);
-                    bv[h * 4 + 0] = t.x; bv[h * 4 + 1] = t.y;
-                    bv[h * 4 + 2] = t.z; bv[h * 4 + 3] = t.w;
+                    for (int h = 0; h < CG; ++h) {
+                        const float4 t = shfl4(mine, h * TX + tx);
+                        bv[h * 4 + 0] = t.x; bv[h * 4 + 1] = t.y;
+                        bv[h * 4 + 2] = t.z; bv[h * 4 + 3] = t.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < CG; ++h) {
+                        const float4 t = *reinterpret_cast<const float4*>(
+                            bs + (kk + q) * KT::LDB_S + h * (BN / CG) + tx * 4);
+                        bv[h * 4 + 0] = t.x; bv[h * 4 + 1] = t.y;
+                        bv[h * 4 + 2] = t.z; bv[h * 4 + 3] = t.w;
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < TM; ++i) {
@@ -237,9 +360,19 @@ simt_gemm_kernel(SimtArgs a)
             ptx::cp_async_wait<STAGES - 2>();  // my copies of tile t have landed
             __syncthreads();                   // everyone's have, and slot (t-1)%S is free
             const int nt = t + STAGES - 1;
-            if (nt < nk) load_tile(nt % STAGES, nt);
+            if (nt < nk) {
+                // aligned operands: cp.async into the free slot; the others:
+                // their loads now, their shared stores after this tile's FFMAs
+                // (into the same free slot, published by the next barrier)
+                if constexpr (VA) load_a(nt % STAGES, nt); else gather_a(nt);
+                if constexpr (VB) load_b(nt % STAGES, nt); else gather_b(nt);
+            }
             ptx::cp_async_commit();
             compute_tile(t % STAGES);
+            if (nt < nk) {
+                if constexpr (!VA) put_a(nt % STAGES);
+                if constexpr (!VB) put_b(nt % STAGES);
+            }
         }
         ptx::cp_async_wait<0>();
     }
@@ -302,11 +435,11 @@ simt_gemm_kernel(SimtArgs a)
     }
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VA, bool VB, bool SEP, int KSL, bool SHF>
 cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
 {
-    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
-    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL>;
+    using KT = SimtKernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL, SHF>;
+    auto kern = simt_gemm_kernel<BM, BN, BK, TM, TN, STAGES, VA, VB, SEP, KSL, SHF>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = smem_limit_once(kern, KT::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -323,17 +456,17 @@ cudaError_t launch_one(const SimtArgs& a, cudaStream_t s)
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false, int KSL = 1>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool SEP = false, int KSL = 1, bool SHF = false>
 cudaError_t launch_cfg(const SimtArgs& a, cudaStream_t s)
 {
     const bool va = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) &&
                     (a.batch <= 1 || a.stride_a % 4 == 0);
     const bool vb = (a.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
                     (a.batch <= 1 || a.stride_b % 4 == 0);
-    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP, KSL>(a, s);
-    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP, KSL>(a, s);
-    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP, KSL>(a, s);
-    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false, SEP, KSL>(a, s);
+    if (va && vb) return launch_one<BM, BN, BK, TM, TN, STAGES, true, true, SEP, KSL, SHF>(a, s);
+    if (va) return launch_one<BM, BN, BK, TM, TN, STAGES, true, false, SEP, KSL, SHF>(a, s);
+    if (vb) return launch_one<BM, BN, BK, TM, TN, STAGES, false, true, SEP, KSL, SHF>(a, s);
+    return launch_one<BM, BN, BK, TM, TN, STAGES, false, false, SEP, KSL, SHF>(a, s);
 }
 
 using LaunchFn = cudaError_t (*)(const SimtArgs&, cudaStream_t);

@@ -46,7 +46,7 @@ def test_status_strings_and_version(lib):
 
 
 def test_opts_layout_matches_header(lib):
-    # int32 x6, int64, int32 x9 -> 6*4 + 8 + 9*4 = 68 bytes, padded to the int64's 8: 72
+    # int32 x6, int64, int32 x10 -> 6*4 + 8 + 10*4 = 72 bytes
     assert ctypes.sizeof(g.Opts) == 72
     o = g.gemm_f32_opts_init()
     assert o.variant == 0 and o.split_k == 0 and o.wait_timeout_cycles == 0

@@ -258,6 +258,39 @@ def test_sliced_k_refusals():
             g.Plan(256, 256, 256, variant=g.VARIANT_SIMT, **opts)
 
 
+# Fragments handed out by warp shuffles (the fragment-load ablation): the same
+# FFMAs in the same order as the broadcast loads, so the same bits.
+# (tile_m, tile_n, stages, tile_k, k_slices)
+SHFL_CFGS = [(128, 128, 2, 16, 1), (64, 64, 2, 16, 1), (64, 64, 4, 16, 2), (32, 32, 3, 32, 4), (32, 32, 3, 64, 4)]
+
+
+@pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "unaligned"])
+@pytest.mark.parametrize("cfg", SHFL_CFGS, ids=[f"{a}x{b}x{d}s{c}ksl{e}" for a, b, c, d, e in SHFL_CFGS])
+def test_shuffle_fragments_bit_identical_to_broadcast(cfg, aligned):
+    bm, bn, st, bk, ksl = cfg
+    M, N, K = 2 * bm + 5, 3 * bn + 3, 3 * bk + 7
+    A = inputs.uniform_pm1(957, M, K)
+    B = inputs.uniform_pm1(958, K, N)
+    kw = {} if aligned else dict(lda=K + 1, ldb=N + 2, a_off=1, b_off=1)
+    opts = dict(variant=g.VARIANT_SIMT, tile_m=bm, tile_n=bn, stages=st, tile_k=bk, k_slices=ksl, **kw)
+    Cs, ds, oks, _ = run_gemm(A, B, simt_fragments=1, **opts)
+    Cb, db, okb, _ = run_gemm(A, B, **opts)
+    assert "shuffle-fragments" in ds and "shuffle-fragments" not in db, ds
+    assert oks and okb
+    assert np.array_equal(Cs, Cb), ds
+    err, ok = check_against_oracle(Cs, A, B)
+    assert ok, f"{ds}: {err}"
+
+
+def test_shuffle_fragments_refused_where_not_compiled():
+    with pytest.raises(g.GemmError) as e:
+        g.Plan(256, 256, 256, variant=g.VARIANT_SIMT, tile_m=64, tile_n=32, stages=2, simt_fragments=1)
+    assert e.value.status == g.ERR_UNSUPPORTED
+    with pytest.raises(g.GemmError) as e:
+        g.Plan(256, 256, 256, variant=g.VARIANT_SIMT, simt_fragments=2)
+    assert e.value.status == g.ERR_INVALID_ARG
+
+
 TC_CFGS = [(128, 3, 0), (256, 2, 0), (64, 4, 0), (256, 1, 0), (128, 1, 0), (128, 2, 0), (64, 2, 0),
            (256, 2, 1), (128, 3, 1)]
 

@@ -37,15 +37,19 @@ def _planned(A, dA, dB, M, N, K, split):
     return C.cpu().numpy().astype(np.float64)
 
 
-def _noalloc(dA, dB, M, N, K, split, lda=None, ldb=None, ldc=None):
+def _noalloc(dA, dB, M, N, K, split, lda=None, ldb=None, ldc=None, pad=None):
     import torch
     ldc = ldc or N
     Cbuf = torch.full((M, ldc), float("nan"), dtype=torch.float32, device="cuda")
+    if pad is not None and ldc > N:
+        Cbuf[:, N:] = pad
     stream = torch.cuda.current_stream()
     s = g.gemm_f32_run_splitk_noalloc(M, N, K, lda or K, ldb or N, ldc, dA.data_ptr(), dB.data_ptr(),
                                       Cbuf.data_ptr(), split, stream.cuda_stream)
     assert s == g.OK, g.gemm_f32_status_string(s)
     stream.synchronize()
+    if pad is not None and ldc > N:
+        assert (Cbuf[:, N:].cpu().numpy() == pad).all(), "a store landed in C's padding"
     return Cbuf[:, :N].cpu().numpy().astype(np.float64)
 
 
@@ -91,3 +95,63 @@ def test_noalloc_rejects_sizes_beyond_the_array():
     assert g.gemm_f32_run_splitk_noalloc(16, 16, 16, 16, 16, 16, p, p, p, 1, 0) == g.ERR_INVALID_ARG
     assert g.gemm_f32_run_splitk_noalloc(16, 16, 16, 16, 16, 16, p, p, p, 65, 0) == g.ERR_INVALID_ARG
     assert g.gemm_f32_run_splitk_noalloc(0, 16, 16, 16, 16, 16, 0, 0, 0, 2, 0) == g.OK
+
+
+def test_noalloc_padded_leading_dimensions():
+    # Operands inside wider rows whose padding holds NaN (a read of it would
+    # poison the result) and a C whose padding holds a sentinel (a store to it
+    # is caught): the same result as the planned entry point on tight copies.
+    import torch
+    M, N, K, split = 200, 150, 500, 4
+    lda, ldb, ldc = K + 7, N + 5, N + 9
+    A = inputs.uniform_pm1(1501, M, K, ld=lda)
+    B = inputs.uniform_pm1(1502, K, N, ld=ldb)
+    dAp = torch.from_numpy(np.lib.stride_tricks.as_strided(A, shape=(M, lda), strides=(4 * lda, 4)).copy()).cuda()
+    dBp = torch.from_numpy(np.lib.stride_tricks.as_strided(B, shape=(K, ldb), strides=(4 * ldb, 4)).copy()).cuda()
+    assert torch.isnan(dAp[:, K:]).all() and torch.isnan(dBp[:, N:]).all()
+    At, Bt = np.ascontiguousarray(A), np.ascontiguousarray(B)
+    Cp = _planned(At, torch.from_numpy(At).cuda(), torch.from_numpy(Bt).cuda(), M, N, K, split)
+    Cref, S = oracle.gemm_f64(At, Bt)
+    for _ in range(2):
+        Cn = _noalloc(dAp, dBp, M, N, K, split, lda=lda, ldb=ldb, ldc=ldc, pad=12345.0)
+        assert np.isfinite(Cn).all()
+        assert np.all(np.abs(Cn - Cp) <= 2.0 * K * 2.0 ** -24 * S)
+        assert oracle.within_bound(Cn, Cref, S, K)
+
+
+def test_noalloc_single_slice_writes_c_directly():
+    # K no deeper than one 16-deep K-tile: split_k 2 leaves one slice, which
+    # writes C itself (no scratch).  Its size would not fit the array as two
+    # slices (2 x 4096 x 1024 floats > 2^21), so only the one-slice path runs it.
+    import torch
+    M, N, K = 4096, 1024, 16
+    A = inputs.uniform_pm1(1503, M, K)
+    B = inputs.uniform_pm1(1504, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    Cp = _planned(A, dA, dB, M, N, K, 1)
+    Cref, S = oracle.gemm_f64(A, B)
+    for _ in range(2):
+        Cn = _noalloc(dA, dB, M, N, K, 2)
+        assert np.all(np.abs(Cn - Cp) <= 2.0 * K * 2.0 ** -24 * S)
+        assert oracle.within_bound(Cn, Cref, S, K)
+
+
+def test_noalloc_allocates_nothing():
+    # After a warm-up call, a call leaves the device's free memory (what the
+    # driver reports, so any cudaMalloc in the process would show) and torch's
+    # allocator untouched.
+    import torch
+    M, N, K, split = 256, 384, 1024, 4
+    dA = torch.from_numpy(inputs.uniform_pm1(1505, M, K)).cuda()
+    dB = torch.from_numpy(inputs.uniform_pm1(1506, K, N)).cuda()
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    args = (M, N, K, K, N, N, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), split, stream.cuda_stream)
+    assert g.gemm_f32_run_splitk_noalloc(*args) == g.OK
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for _ in range(3):
+        assert g.gemm_f32_run_splitk_noalloc(*args) == g.OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
