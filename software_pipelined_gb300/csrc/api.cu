@@ -151,59 +151,85 @@ int auto_split(int64_t tiles, int64_t K, int64_t min_k_per_split, int sms)
     return s < 1 ? 1 : (int)s;
 }
 
-// The rule for tensor-core plans outside the table: 128x256 tiles for big
-// products, 128x128 below; a K-split only when the tiles fill under half the SMs.
-DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int sms)
+// The rule for tensor-core plans outside the table (checked against the best
+// forced plan on 31 shapes the table does not list: squares 768-6144,
+// rectangles, skinny and ragged shapes, leading dimensions that are not
+// multiples of 4; the sweep is tune.py --rule-sweep):
+//   * A's rows not 16-byte aligned (lda not a multiple of 4) or K < 32: only
+//     the full pre-pass form can run: 128x256 tiles for big products, 128x128
+//     below, a K-split when the tiles fill under half the SMs.
+//   * both M and N at least 1000: 256x256 tiles on CTA pairs (one
+//     tcgen05.mma across two SMs halves each CTA's B traffic).  Products of
+//     2^34 multiply-adds and more with both sides at least 2048 read lo of A
+//     and B pre-split (no conversion inside the kernel; 3072^3 229 vs 233 us,
+//     6144^3 1646 vs 1802 us for the one-CTA pre-pass form the rule took
+//     before; with a side of 1024 the pre-pass costs more than it saves:
+//     1024x4096x4096 176 vs 157 us); the others split both operands in the
+//     kernel (B by the pre-pass when its rows are not 16-byte aligned); a
+//     K-split so that the pairs fill the machine.
+//   * otherwise (skinny, or under 1000 on a side): 128x128 tiles on one CTA,
+//     operands split in the kernel (B by the pre-pass when its rows are not
+//     aligned), K-split to fill the SMs (8192x256x1024 28 vs 40 us,
+//     128x4096x4096 30 vs 73 us, 768^3 11.4 vs 15.8 us against the pre-pass
+//     form).
+DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms)
 {
     DispatchChoice c{};
     c.variant = GEMM_F32_VARIANT_TCGEN05;
-    if (M >= 1024 && N >= 1024 && K >= 256 && M <= 3072 && N <= 3072) {
-        // Mid sizes: 256 x 256 tiles on CTA pairs, operands split in the kernel
-        // (measured on GB300 against the best one-CTA plans: 1024^3 18.4 vs 19.2
-        // us, 1280^3 26.1 vs 29.1, 1536^3 36.6 vs 41.3, 2048^3 73 vs 81-101,
-        // 2048x3072x4096 216 vs 253; below 1024 the one-CTA kernel wins); K-split
-        // so that the pairs fill the machine.
+    const double macs = double(M) * double(N) * double(K);
+    if (lda % 4 != 0 || K < kTcFusedMinK) {
+        c.tile_m = 128;
+        c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
+        c.fused = kSplitPrepass;
+        const int64_t tiles = ((M + 127) / 128) * ((N + c.tile_n - 1) / c.tile_n);
+        c.split_k = tiles >= sms / 2 ? 0 : auto_split(tiles, K, 256, sms);
+        return c;
+    }
+    const int b_split = ldb % 4 == 0 ? kSplitInKernel : kSplitHybrid;
+    if (M >= 1000 && N >= 1000) {
         c.tile_m = 256;
         c.tile_n = 256;
         c.tile_k = 32;
-        c.fused = kSplitInKernel;
+        c.fused = macs >= 17179869184.0 && M >= 2048 && N >= 2048 ? kSplitRawA : b_split;
         const int64_t ptiles = ((M + 255) / 256) * ((N + 255) / 256);
-        c.split_k = ptiles >= sms / 4 ? 0 : auto_split(ptiles, K, 256, sms / 2);
+        c.split_k = ptiles >= sms / 4 ? 0 : auto_split(ptiles, K, 192, sms / 2);
         return c;
     }
     c.tile_m = 128;
-    c.tile_n = (N >= 2048 && M >= 2048) ? 256 : 128;
-    c.stages = 0;  // the depth compiled for that tile width
-    const int64_t tiles = ((M + 127) / 128) * ((N + c.tile_n - 1) / c.tile_n);
-    c.split_k = tiles >= sms / 2 ? 0 : auto_split(tiles, K, 256, sms);
+    c.tile_n = 128;
+    c.fused = b_split;
+    const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    c.split_k = tiles >= sms / 2 ? 0 : auto_split(tiles, K, 192, sms);
     return c;
 }
 
-// The rule for SIMT plans outside the table: the largest square tile that
-// still gives every SM work, two stages, K-split to fill the SMs.
+// The rule for SIMT plans outside the table: 32x32 tiles of 32-deep K-tiles,
+// a 3-stage ring, K split across 4 thread groups of the CTA (more warps per
+// SM without a second launch), and a K-split across CTAs only when the tiles
+// fill under half the SMs and every slice keeps 128 of K (measured against
+// the best forced plan: 64^3 2.04 vs 2.81 us, 200x300x100 2.98 vs 5.78 us,
+// 33x65x129 3.5 vs 5.3 us for the rule's earlier 32x32 two-stage plans).
 DispatchChoice choose_simt(int64_t M, int64_t N, int64_t K, int sms)
 {
     DispatchChoice c{};
     c.variant = GEMM_F32_VARIANT_SIMT;
-    c.stages = 2;
-    const int64_t t128 = ((M + 127) / 128) * ((N + 127) / 128);
-    const int64_t t64 = ((M + 63) / 64) * ((N + 63) / 64);
-    if (t128 >= sms) { c.tile_m = c.tile_n = 128; }
-    else if (t64 >= sms / 4 || M * N > 64 * 64 * 4) { c.tile_m = c.tile_n = 64; }
-    else { c.tile_m = c.tile_n = 32; }
-    const int64_t tiles = ((M + c.tile_m - 1) / c.tile_m) * ((N + c.tile_n - 1) / c.tile_n);
-    c.split_k = auto_split(tiles, K, 64, sms);
+    c.tile_m = c.tile_n = 32;
+    c.stages = 3;
+    c.tile_k = 32;
+    c.k_slices = 4;
+    const int64_t tiles = ((M + 31) / 32) * ((N + 31) / 32);
+    c.split_k = tiles >= sms / 2 ? 1 : auto_split(tiles, K, 128, sms);
     return c;
 }
 
-DispatchChoice choose(int64_t M, int64_t N, int64_t K, int sms)
+DispatchChoice choose(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int sms)
 {
     DispatchChoice c{};
     if (table_lookup(M, N, K, c)) return c;
     // Shapes outside the measured table: tensor cores once the product is big
     // enough to amortise the operand split; SIMT below that.
     const double macs = double(M) * double(N) * double(K);
-    if (macs >= 6.0e7 && K >= 32) return choose_tc(M, N, K, sms);  // K >= kTcMinK with margin
+    if (macs >= 6.0e7 && K >= 32) return choose_tc(M, N, K, lda, ldb, sms);  // K >= kTcMinK with margin
     return choose_simt(M, N, K, sms);
 }
 
@@ -259,11 +285,11 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         p->kind = kZeroFill;
         snprintf(p->desc, sizeof p->desc, "zero-fill M=%lld N=%lld K=0", (long long)M, (long long)N);
     } else {
-        DispatchChoice c = choose(M, N, K, p->num_sms);
+        DispatchChoice c = choose(M, N, K, lda, ldb, p->num_sms);
         if (o.variant != GEMM_F32_VARIANT_AUTO && o.variant != c.variant) {
             // A forced variant starts from that variant's own rule.
             c = o.variant == GEMM_F32_VARIANT_SIMT ? choose_simt(M, N, K, p->num_sms)
-                                                   : choose_tc(M, N, K, p->num_sms);
+                                                   : choose_tc(M, N, K, lda, ldb, p->num_sms);
         }
         // A forced tile or ring replaces the choice, so the table's K-tile depth
         // and tile order (tuned for its own tile) no longer apply.

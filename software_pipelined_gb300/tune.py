@@ -8,6 +8,13 @@ rule for shapes it does not list.  Run on the target GPU:
     python -m software_pipelined_gb300.tune --json tune.json \\
         --inc software_pipelined_gb300/csrc/dispatch_table.inc
 
+With --rule-sweep it checks the rule instead: for shapes the table does not
+list (squares, rectangles, skinny and ragged shapes, leading dimensions that
+are not multiples of 4) it times the dispatcher's own plan against the best
+forced candidate and prints both with their ratio:
+
+    python -m software_pipelined_gb300.tune --rule-sweep --json rule.json --md
+
 Each candidate is planned with forced options, warmed up, and timed as the
 median of three replays of a CUDA graph holding back-to-back runs (events
 around each replay), so launch overhead on the host does not decide.
@@ -101,14 +108,83 @@ def candidates(M, N, K):
     return out
 
 
+# Shapes outside the table: (M, N, K, lda, ldb); lda/ldb None = tight.
+RULE_SHAPES = [
+    (768, 768, 768, None, None), (1280, 1280, 1280, None, None), (1536, 1536, 1536, None, None),
+    (2048, 2048, 2048, None, None), (2560, 2560, 2560, None, None), (3072, 3072, 3072, None, None),
+    (6144, 6144, 6144, None, None), (1000, 1000, 1000, None, None), (4100, 4100, 4100, None, None),
+    (2048, 8192, 1024, None, None), (8192, 2048, 1024, None, None), (4096, 1024, 4096, None, None),
+    (1024, 4096, 4096, None, None), (4096, 4096, 1024, None, None), (3000, 5000, 2000, None, None),
+    (777, 1234, 555, None, None), (8192, 256, 1024, None, None), (256, 8192, 1024, None, None),
+    (16384, 64, 256, None, None), (64, 16384, 512, None, None), (4096, 128, 4096, None, None),
+    (128, 4096, 4096, None, None), (64, 64, 64, None, None), (200, 300, 100, None, None),
+    (96, 96, 1024, None, None), (33, 65, 129, None, None), (300, 40, 700, None, None),
+    (1023, 1025, 1027, None, None), (2049, 2047, 2051, None, None), (1024, 1024, 1024, 1027, 1029),
+    (4096, 4096, 4096, 4097, 4099),
+]
+
+
+def rule_sweep(args):
+    """The dispatcher's plan against the best forced candidate on RULE_SHAPES."""
+    import torch
+    stream = torch.cuda.current_stream()
+    results = []
+    for (M, N, K, lda, ldb) in RULE_SHAPES:
+        lda, ldb = lda or K, ldb or N
+        A = inputs.uniform_pm1(8001, M, K, ld=lda if lda != K else None)
+        B = inputs.uniform_pm1(8002, K, N, ld=ldb if ldb != N else None)
+        dA = torch.full((M * lda,), float("nan"), device="cuda")
+        dA.view(M, lda)[:, :K] = torch.from_numpy(inputs.uniform_pm1(8001, M, K)).cuda()
+        dB = torch.full((K * ldb,), float("nan"), device="cuda")
+        dB.view(K, ldb)[:, :N] = torch.from_numpy(inputs.uniform_pm1(8002, K, N)).cuda()
+        del A, B
+        dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        with g.Plan(M, N, K, lda, ldb, N) as p:
+            auto_desc = p.describe()
+            auto_us = round(time_plan(p, dA, dB, dC, stream) * 1e3, 3)
+        best = (auto_us, auto_desc)
+        cands = candidates(M, N, K)
+        if M * N * K > 2 ** 34:  # big products: every tile sliced in K is never the answer
+            cands = [c for c in cands if c.get("split_k", 0) <= 2]
+        for c in cands:
+            try:
+                with g.Plan(M, N, K, lda, ldb, N, **c) as p:
+                    us = round(time_plan(p, dA, dB, dC, stream) * 1e3, 3)
+                    if us < best[0]:
+                        best = (us, p.describe())
+            except g.GemmError:
+                continue
+        shape = f"{M}x{N}x{K}" + (f" lda={lda} ldb={ldb}" if (lda, ldb) != (K, N) else "")
+        r = dict(shape=shape, rule_us=auto_us, rule_plan=auto_desc, best_us=best[0], best_plan=best[1],
+                 rule_over_best=round(auto_us / best[0], 4))
+        results.append(r)
+        print(json.dumps(r), flush=True)
+        del dA, dB, dC
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(results, f, indent=1)
+    if args.md:
+        short = lambda d: " ".join(t for t in d.split() if not t.startswith(("terms=", "ws=", "kp=", "resident=",
+                                                                             "whole=", "pairs=", "tiles=", "thread=")))
+        print("| shape | rule's plan | us | best forced plan | us | rule / best |")
+        print("|---|---|---:|---|---:|---:|")
+        for r in results:
+            print(f"| {r['shape']} | {short(r['rule_plan'])} | {r['rule_us']} | {short(r['best_plan'])} | "
+                  f"{r['best_us']} | {r['rule_over_best']} |")
+
+
 def main():
     import torch
     ap = argparse.ArgumentParser()
     ap.add_argument("--json", default=None)
     ap.add_argument("--inc", default=None)
     ap.add_argument("--workloads", default="tiny_32,small_ragged,tall_skinny,square_1024,large_squares")
+    ap.add_argument("--rule-sweep", action="store_true")
+    ap.add_argument("--md", action="store_true")
     args = ap.parse_args()
     g.load()
+    if args.rule_sweep:
+        return rule_sweep(args)
     stream = torch.cuda.current_stream()
     results = []
     for key in args.workloads.split(","):

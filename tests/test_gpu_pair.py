@@ -182,9 +182,14 @@ def test_pair_refusals(opts):
 
 
 def test_pair_refuses_unaligned_leading_dimensions():
-    for lda, ldb in ((257, 512), (256, 514)):
-        with pytest.raises(g.GemmError):
-            g.Plan(512, 512, 256, lda, ldb, 512, **PAIR)
+    # raw A by TMA needs 16-byte rows of A in every pair form; raw B by TMA (the
+    # in-kernel split of B) needs them of B, the forms that pre-split B do not
+    with pytest.raises(g.GemmError):
+        g.Plan(512, 512, 256, 257, 512, 512, **PAIR)
+    with pytest.raises(g.GemmError):
+        g.Plan(512, 512, 256, 256, 514, 512, operand_split=2, **PAIR)
+    with g.Plan(512, 512, 256, 256, 514, 512, **PAIR) as p:
+        assert "hybrid-split cta-pair" in p.describe()
 
 
 def test_pair_withheld_stage_times_out_and_context_survives():
