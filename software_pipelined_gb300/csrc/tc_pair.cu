@@ -31,7 +31,8 @@
 //   conv[s]    (even CTA) both CTAs' converters are done: counts 2 x 4 warps
 //              (one group of each CTA), the odd CTA's arriving remotely with
 //              release at cluster scope; in the form with nothing to convert,
-//              one forwarding thread of each CTA (2 arrivals)
+//              the odd CTA's forwarding thread (1 arrival), the MMA thread
+//              waiting on its own CTA's full_a[s] as well
 //   empty[s]   the pair's MMAs of slot s completed: one commit, multicast to
 //              both CTAs
 //   tfull      accumulator complete: commit multicast to both CTAs
@@ -310,9 +311,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
             ptx::mbar_init(full_a(s), 1);
-            // one group of each CTA's converters, or (nothing to convert) one
-            // forwarding thread of each CTA
-            ptx::mbar_init(conv(s), APRE ? 2 : 2 * kPairConvWarps / kConvGroups);
+            // one group of each CTA's converters, or (nothing to convert) the
+            // odd CTA's forwarding thread (the even CTA's MMA thread waits for
+            // its own copies on full_a itself)
+            ptx::mbar_init(conv(s), APRE ? 1 : 2 * kPairConvWarps / kConvGroups);
             ptx::mbar_init(empty(s), 1);
             ptx::mbar_init(rd(s), kPairConvWarps / kConvGroups);
         }
@@ -435,6 +437,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
                     const int s = fills % SLOTS;
                     const uint32_t ps = (fills / SLOTS) & 1u;
+                    if (APRE && !wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
                     if (!wait_phase_cluster(conv(s), ps, limit, abort_flag, args.status)) {
                         stop = true;
                         break;
@@ -505,12 +511,14 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if (stop && lane == 0) give_up();
     } else if constexpr (APRE) {
         // ------------------------------ forwarder -----------------------------
-        // Every piece of the stage comes by TMA: one thread of each CTA hands
-        // each landed stage to the even CTA's MMA thread (release at cluster
-        // scope after its own acquire of the copies).  It takes the stages in
-        // order, and a slot is refilled only after the MMAs that needed this
-        // hand-off, so its parity wait is never a phase behind or ahead.
-        if (threadIdx.x == 6 * 32) {
+        // Every piece of the stage comes by TMA: one thread of the odd CTA
+        // hands each landed stage to the even CTA's MMA thread (release at
+        // cluster scope after its own acquire of the copies); the MMA thread
+        // waits for the even CTA's copies itself.  The forwarder takes the
+        // stages in order, and a slot is refilled only after the MMAs that
+        // needed this hand-off, so its parity wait is never a phase behind or
+        // ahead.
+        if (threadIdx.x == 6 * 32 && rank == 1) {
             uint32_t fills = 0;
             bool stop = false;
             for (int w = pair; w < num_work && !stop; w += npairs) {
