@@ -101,7 +101,7 @@ typedef struct {
     int32_t variant;        /* gemm_f32_variant */
     int32_t tile_m;         /* output tile rows (SIMT: 32/64/128; TC: 128, or 256 = one tile per pair
                                of CTAs, a thread-block cluster of two sharing each tcgen05.mma
-                               (cta_group::2): operand_split 2, 3 or 4 (not the full pre-pass),
+                               (cta_group::2): operand_split 2 to 5 (not the full pre-pass),
                                tile_n 128 or 256, tile_k 32 or 16 (16: in the kernel, or with
                                operand_split 4 at tile_n 256); needs K >= 32 and lda a multiple
                                of 4 (ldb too when B is split in the kernel), else UNSUPPORTED;
@@ -128,9 +128,13 @@ typedef struct {
                                multiples of 4); 3 = A inside the kernel, B by the pre-pass
                                (needs K >= 32, lda a multiple of 4); 4 = hi of A read from
                                A itself, lo of A and B by the pre-pass (same needs; on CTA
-                               pairs this form has no conversion inside the kernel).  2, 3
-                               and 4 fall back to 1 at run time for a base pointer of A (or,
-                               for 2, B) that is not 16-byte aligned */
+                               pairs this form has no conversion inside the kernel); 5 = CTA
+                               pairs only (tile 256x256, tile_k 32): raw A staged by TMA in a
+                               short ring, split by the kernel's loader warps into tensor
+                               memory, B by the pre-pass (same needs; measured slower than
+                               4, never the dispatcher's choice).  2 to 5
+                               fall back to 1 at run time for a base pointer of A (or, for 2,
+                               B) that is not 16-byte aligned */
     int32_t tile_group;     /* TC only: tile order of the persistent kernel, in tile-rows per
                                raster group (1..64; 0 = the dispatcher's choice, else 8) */
     int32_t tile_k;         /* K-tile depth.  SIMT: 16/32/64 (0 = the compiled default for the

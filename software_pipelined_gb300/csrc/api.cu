@@ -128,7 +128,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
-    if (o.operand_split < 0 || o.operand_split > 4) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.operand_split < 0 || o.operand_split > 5) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
@@ -331,7 +331,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             p->kind = kTc;
             TcPlanState& t = p->tc;
             // operand_split: 1 pre-pass, 2 in the kernel, 3 hybrid (A in the kernel,
-            // B by the pre-pass), 4 hi of A read from A; 0 = the dispatcher's choice.
+            // B by the pre-pass), 4 hi of A read from A, 5 A split by the pairs'
+            // loader warps into tensor memory; 0 = the dispatcher's choice.
             // A forced ring depth exists only in the pre-pass form (the other
             // forms have one depth per tile width), so it selects that form.
             // Half-size (16-k) stages exist only in the in-kernel form, so a
@@ -339,13 +340,16 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // tile_m 256: a pair of CTAs per 256-row tile (one tcgen05.mma
             // across both), operands split in the kernel only.
             // operand_split 3 (B by the pre-pass) asks for the pairs' hybrid form,
-            // 4 (lo of A and B by the pre-pass) for their form without converters
+            // 4 (lo of A and B by the pre-pass) for their form without converters,
+            // 5 for their form with A in tensor memory
             bool pair = c.tile_m == 256;
-            const int pair_split = o.operand_split == 4   ? kSplitRawA
+            const int pair_split = o.operand_split == 5   ? kSplitTmemA
+                                   : o.operand_split == 4 ? kSplitRawA
                                    : o.operand_split == 3 ? kSplitHybrid
                                    : o.operand_split      ? kSplitInKernel
-                                   : (c.fused == kSplitHybrid || c.fused == kSplitRawA) ? c.fused
-                                                                                         : kSplitInKernel;
+                                   : (c.fused == kSplitHybrid || c.fused == kSplitRawA || c.fused == kSplitTmemA)
+                                         ? c.fused
+                                         : kSplitInKernel;
             if (pair && (o.operand_split == 1 || o.stages ||
                          o.separate_syncs || o.split_reduce == 3 || K < kTcFusedMinK || lda % 4 != 0 ||
                          (pair_split == kSplitInKernel && ldb % 4 != 0))) {
@@ -360,7 +364,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 const int pbk = o.tile_k ? o.tile_k : c.tile_k;
                 t.config_id = tc_find_pair_config(c.tile_n, pbk, pair_split);
                 if (t.config_id < 0) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-                t.pair_slots = tc_pair_slots(c.tile_n, tc_config(t.config_id).bk, p->num_sms);
+                t.pair_slots = tc_pair_slots(c.tile_n, tc_config(t.config_id).bk, p->num_sms, pair_split);
                 if (t.pair_slots < 1) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
                 t.fallback_config_id = tc_find_config(c.tile_n, 0, false, kSplitPrepass);
             } else {
@@ -420,7 +424,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                          "tcgen05 3xtf32 %s cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
                          "whole=%d split=%dx%d%s resident=%d group=%d kp=%lld",
                          tcfg.split == kSplitHybrid ? "hybrid-split"
-                         : tcfg.split == kSplitRawA ? "raw-a-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
+                         : tcfg.split == kSplitRawA ? "raw-a-split"
+                         : tcfg.split == kSplitTmemA ? "tmem-a-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
                          t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", t.pair_slots,
                          t.tile_group > 0 ? t.tile_group : 8,
                          (long long)t.kp);

@@ -74,18 +74,20 @@ enum : int {
     kSplitPrepass = 0,   // a pre-pass writes hi/lo of A and B to scratch
     kSplitInKernel = 1,  // raw A and B by TMA, split by converter warps
     kSplitHybrid = 2,    // raw A split in the kernel, B split by the pre-pass
-    kSplitRawA = 3       // hi of A read from A (truncated by the MMA); the pre-pass writes lo of A, hi/lo of B
+    kSplitRawA = 3,      // hi of A read from A (truncated by the MMA); the pre-pass writes lo of A, hi/lo of B
+    kSplitTmemA = 4      // CTA pairs only: A split by the kernel's loader warps into tensor memory, B by the pre-pass
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);
 int tc_find_config(int bn, int stages, bool sep, int split, int bk = 0);
 // The CTA-pair configuration (256-row tiles) of tile width bn, stage depth bk
 // (0 = 32) and split mode (kSplitInKernel; kSplitHybrid: B by the pre-pass;
-// kSplitRawA: lo of A and B by the pre-pass), or -1.
+// kSplitRawA: lo of A and B by the pre-pass; kSplitTmemA: A into tensor
+// memory by the kernel, B by the pre-pass), or -1.
 int tc_find_pair_config(int bn, int bk, int split = kSplitInKernel);
 // How many pairs of that configuration run at once on this device (0 when the
 // occupancy query fails).
-int tc_pair_slots(int bn, int bk, int sms);
+int tc_pair_slots(int bn, int bk, int sms, int split = kSplitInKernel);
 
 // Plan-time state of the tensor-core path: split-operand scratch and the
 // tensor maps that describe it, and the work decomposition.

@@ -668,5 +668,10 @@ cudaError_t tc_pair_main(int bn, int bk, int split, const TcPlanState& st, const
                          const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbhi,
                          const CUtensorMap& tblo, const CUtensorMap& talo, cudaStream_t s);
 cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const tc::TcArgs& a, cudaStream_t s);
+// The CTA-pair kernel with A in tensor memory (256 x 256 tiles, 32-k stages):
+// A read from the caller's A by TMA (ta: 16-byte aligned rows) and split by
+// the kernel's loader warps, hi and lo of B by the pre-pass (tbhi, tblo).
+cudaError_t tc_pair_tmem_main(const TcPlanState& st, const tc::TcArgs& a, const CUtensorMap& ta,
+                              const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s);
 
 }  // namespace gemm_f32

@@ -205,6 +205,9 @@ const TcEntry kTc[] = {
     {{256, 256, 32, 3, false, kSplitRawA}, nullptr, launch_pair_reduce<256>, false, false},
     {{256, 256, 16, 6, false, kSplitRawA}, nullptr, launch_pair_reduce<256>, false, false},
     {{256, 128, 32, 4, false, kSplitRawA}, nullptr, launch_pair_reduce<128>, false, false},
+    // CTA pairs with A split by the kernel's loader warps into tensor memory
+    // and hi/lo of B by the pre-pass: 5 B stages, raw A staged 3 deep
+    {{256, 256, 32, 5, false, kSplitTmemA}, nullptr, launch_pair_reduce<256>, false, false},
 };
 
 }  // namespace
@@ -391,6 +394,7 @@ struct Route {
     bool raw_a;      // hi of A read from A
     bool pre_a;      // the pre-pass splits A (only lo with raw_a)
     bool pre_b;      // the pre-pass splits B
+    bool tmem_a;     // A read from A by the kernel's loader warps into tensor memory
     bool pair;       // a CTA-pair plan whose kernel can take these operands
 };
 
@@ -403,11 +407,12 @@ Route route(const TcPlanState& st, const float* A, const float* B)
     r.id = st.config_id;
     r.in_kernel = (c.split == kSplitInKernel && a_ok && b_ok) || (c.split == kSplitHybrid && a_ok);
     r.raw_a = c.split == kSplitRawA && a_ok;
-    r.pre_a = !r.in_kernel;
+    r.tmem_a = c.split == kSplitTmemA && a_ok;
+    r.pre_a = !r.in_kernel && !r.tmem_a;
     r.pre_b = !r.in_kernel || c.split == kSplitHybrid;
     // a misaligned base pointer: the pre-pass form of the same tile width
-    if (!r.in_kernel && !r.raw_a && c.split != kSplitPrepass) r.id = st.fallback_config_id;
-    r.pair = c.bm == 2 * kBM && (r.in_kernel || r.raw_a);
+    if (!r.in_kernel && !r.raw_a && !r.tmem_a && c.split != kSplitPrepass) r.id = st.fallback_config_id;
+    r.pair = c.bm == 2 * kBM && (r.in_kernel || r.raw_a || r.tmem_a);
     return r;
 }
 
@@ -478,7 +483,11 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     if (a.cluster > 1 && !kTc[r.id].cluster_ok && c.bm != 2 * kBM) return cudaErrorInvalidValue;
     if (a.fixup && !kTc[r.id].fixup_ok) return cudaErrorInvalidValue;
     cudaError_t e;
-    if (c.bm == 2 * kBM) {
+    if (c.bm == 2 * kBM && r.tmem_a) {
+        e = tc_pair_tmem_main(st, a, *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
+                              *reinterpret_cast<const CUtensorMap*>(st.tmap_b_hi),
+                              *reinterpret_cast<const CUtensorMap*>(st.tmap_b_lo), s);
+    } else if (c.bm == 2 * kBM) {
         e = tc_pair_main(c.bn, c.bk, c.split, st, a,
                          *reinterpret_cast<const CUtensorMap*>(st.tmap_a_raw),
                          *reinterpret_cast<const CUtensorMap*>(st.tmap_b_raw),
@@ -527,7 +536,7 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
     cudaError_t e = cudaSuccess;
     if (ev) cudaEventRecord(ev[0], s);
     // Tensor maps over the caller's raw operands, re-encoded when they move.
-    if ((r.raw_a || r.in_kernel) && A != st.raw_a) {
+    if ((r.raw_a || r.tmem_a || r.in_kernel) && A != st.raw_a) {
         if ((e = encode_raw_a(st.tmap_a_raw, A, M, K, lda, c.bk)) != cudaSuccess) return e;
         st.raw_a = A;
     }
@@ -558,7 +567,7 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     if ((e = encode_kmajor(out.tmap_a_hi, out.a_hi, mp, out.kp, kBM)) != cudaSuccess) return e;
     if ((e = encode_kmajor(out.tmap_a_lo, out.a_lo, mp, out.kp, kBM, split_box_k(c))) != cudaSuccess) return e;
     const Route r = route(out, A + r0 * lda, B);
-    if (r.raw_a || r.in_kernel) {
+    if (r.raw_a || r.tmem_a || r.in_kernel) {
         if ((e = encode_raw_a(out.tmap_a_raw, A + r0 * lda, mp, K, lda, c.bk)) != cudaSuccess) return e;
         out.raw_a = A + r0 * lda;
     }

@@ -628,6 +628,416 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------------------
+// CTA pairs with A in tensor memory.
+//
+// The pair tile is 256 x 256 as above, but A's pieces never sit in shared
+// memory while the MMAs run: raw A comes by TMA into a small staging ring
+// (16 KB a stage), four loader warps of each CTA (one thread per row of the
+// CTA's 128 rows) read their rows from it, split them in registers (hi = the
+// value truncated to TF32, lo = the remainder rounded to TF32), free the
+// staging slot, and write both pieces into a ring of A slots in tensor memory
+// with tcgen05.st; the MMAs take A from there (the tcgen05.mma form whose A
+// operand is in tensor memory, each CTA of the pair providing its 128 rows).
+// Shared memory then holds this CTA's half of hi_B and lo_B (split and
+// transposed by the pre-pass) 5 stages deep and raw A 3 stages deep, where
+// the 64 KB stages of the forms above fit 3 in all, and no pre-pass writes or
+// reads lo of A.  Tensor memory (512 columns): one 256-column accumulator (a
+// unit's epilogue drains it before the next unit's MMAs start) and 4 A slots
+// of 64 columns (hi in the first 32, lo in the next).
+//
+// Barriers (every wait bounded; a CTA that gives up raises both abort flags):
+//   s_full[j]   raw A of staging slot j landed (TMA, local)
+//   s_empty[j]  this CTA's 4 loader warps have read staging slot j (local)
+//   b_full[s]   this CTA's hi_B / lo_B halves of stage s landed (TMA, local)
+//   b_conv[s]   (even CTA) the odd CTA's stage s landed: its forwarding thread
+//   b_empty[s]  the pair's MMAs of B slot s completed (commit, multicast)
+//   a_full[t]   (even CTA) both CTAs' loader warps wrote A slot t: 8 arrivals
+//   a_empty[t]  the pair's MMAs of A slot t completed (commit, multicast)
+//   tfull       the accumulator is complete (commit, multicast)
+//   tempty      (even CTA) both CTAs' epilogues drained it: 8 arrivals
+template <int NB_SLOTS, int NA_STAGE>
+struct TmemALayout {
+    static constexpr int BN = 256, BH = 128, KB = 32;
+    static constexpr int A_SLOTS = 4;
+    static constexpr int B_BYTES = BH * KB * 4;     // one piece of this CTA's half of B
+    static constexpr int SLOT_BYTES = 2 * B_BYTES;  // hi_B, lo_B
+    static constexpr int RING_BYTES = NB_SLOTS * SLOT_BYTES;
+    static constexpr int STAGE_A_BYTES = kBM * KB * 4;  // raw A of one stage: 128 rows x 32
+    static constexpr int NBARS = 3 * NB_SLOTS + 2 * A_SLOTS + 2 * NA_STAGE + 3;
+    static constexpr int BAR_BYTES = 8 * NBARS + 16;
+    // B_BYTES of slack after the barriers, as in PairLayout
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + NA_STAGE * STAGE_A_BYTES + BAR_BYTES + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t A_COL0 = 256;         // A slot t: columns A_COL0 + 64 t (hi), + 32 (lo)
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(RING_BYTES >= 4 * 8 * 4096, "the ring holds the last unit's TMA-store staging");
+};
+// B producer, MMA, 4 epilogue, 4 loader warps, B forwarder, A producer
+constexpr int kTmemAThreads = 12 * 32;
+
+template <int NB_SLOTS, int NA_STAGE>
+__global__ void __launch_bounds__(kTmemAThreads, 1)
+tc_pair_tmem_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_bhi,
+                    const __grid_constant__ CUtensorMap tm_blo, const __grid_constant__ CUtensorMap tm_c,
+                    const __grid_constant__ CUtensorMap tm_p, const TcArgs args)
+{
+    using L = TmemALayout<NB_SLOTS, NA_STAGE>;
+    constexpr int BN = L::BN, SA = L::A_SLOTS, SB = NB_SLOTS, SS = NA_STAGE;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    const uint32_t ring = (raw_addr + 1023u) & ~1023u;
+    uint8_t* ring_ptr = smem_raw + (ring - raw_addr);
+    const uint32_t astage = ring + L::RING_BYTES;  // raw A staging, after the B ring
+    const uint8_t* astage_ptr = ring_ptr + L::RING_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + L::RING_BYTES + SS * L::STAGE_A_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t crank = ptx::cluster_ctarank();
+    const uint32_t rank = crank & 1u, lead = crank & ~1u;
+    const uint16_t pair_mask = (uint16_t)(3u << lead);
+    auto b_full = [&](int s) { return ptx::smem_u32(bars + s); };
+    auto b_conv = [&](int s) { return ptx::smem_u32(bars + SB + s); };
+    auto b_empty = [&](int s) { return ptx::smem_u32(bars + 2 * SB + s); };
+    auto a_full = [&](int t) { return ptx::smem_u32(bars + 3 * SB + t); };
+    auto a_empty = [&](int t) { return ptx::smem_u32(bars + 3 * SB + SA + t); };
+    const uint32_t tfull = ptx::smem_u32(bars + 3 * SB + 2 * SA);
+    const uint32_t tempty = ptx::smem_u32(bars + 3 * SB + 2 * SA + 1);
+    const uint32_t drain_bar = ptx::smem_u32(bars + 3 * SB + 2 * SA + 2);
+    auto s_full = [&](int j) { return ptx::smem_u32(bars + 3 * SB + 2 * SA + 3 + j); };
+    auto s_empty = [&](int j) { return ptx::smem_u32(bars + 3 * SB + 2 * SA + 3 + SS + j); };
+    const uint32_t peer_abort = ptx::mapa(ptx::smem_u32(const_cast<int*>(abort_flag)), crank ^ 1u);
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        ptx::st_cluster_u32(peer_abort, 1u);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SB; ++s) {
+            ptx::mbar_init(b_full(s), 1);
+            ptx::mbar_init(b_conv(s), 1);
+            ptx::mbar_init(b_empty(s), 1);
+        }
+        for (int t = 0; t < SA; ++t) {
+            ptx::mbar_init(a_full(t), 8);
+            ptx::mbar_init(a_empty(t), 1);
+        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 8);
+        ptx::mbar_init(drain_bar, 1);
+        for (int j = 0; j < SS; ++j) {
+            ptx::mbar_init(s_full(j), 1);
+            ptx::mbar_init(s_empty(j), 4);
+        }
+        *abort_flag = 0;
+        ptx::mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tm_a);
+        ptx::tma_prefetch_desc(&tm_bhi);
+        ptx::tma_prefetch_desc(&tm_blo);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers initialised, TMEM allocated, abort flags cleared
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int num_work = args.dp_tiles + args.split_tiles * args.splits;
+    const int64_t limit = args.timeout;
+
+    if (warp == 0) {
+        // ----------------------------- B producer -----------------------------
+        if (lane == 0) {
+            pdl_wait();  // the previous kernel's writes (split B, C) are done
+            uint32_t fills = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs) {
+                const PairUnit pu = pair_unit(w, args, (int)rank);
+                for (int kb = pu.u.kb0; kb < pu.u.kb1; ++kb) {
+                    const int s = fills % SB;
+                    const uint32_t ps = (fills / SB) & 1u;
+                    if (!wait_phase(b_empty(s), ps ^ 1u, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ++fills;
+                    if (fills == (uint32_t)args.withhold) continue;
+                    const uint32_t slot = ring + s * L::SLOT_BYTES;
+                    const int n0 = pu.tn * BN + (int)rank * L::BH;
+                    ptx::mbar_arrive_expect_tx(b_full(s), L::SLOT_BYTES);
+                    ptx::tma_load_2d(slot, &tm_bhi, b_full(s), kb * L::KB, n0);
+                    ptx::tma_load_2d(slot + L::B_BYTES, &tm_blo, b_full(s), kb * L::KB, n0);
+                }
+            }
+            if (stop) give_up();
+            // Drain: the last fill of every slot must have landed.
+            const uint32_t total = fills;
+            for (int s = 0; s < SB && (uint32_t)s < total; ++s) {
+                const uint32_t last = (total - 1 - s) / SB * SB + s;
+                if (last + 1 == (uint32_t)args.withhold) continue;
+                const uint32_t par = (last / SB) & 1u;
+                const long long t0 = clock64();
+                while (!ptx::mbar_try_wait(b_full(s), par))
+                    if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ----------------------------
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_tf32_pair<BN>();
+            uint32_t fills = 0;
+            int iter = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs, ++iter) {
+                const Unit u = decode_unit(w, args);
+                // the single accumulator: the last unit's epilogues drained it
+                if (!wait_phase_cluster(tempty, ((uint32_t)iter & 1u) ^ 1u, limit, abort_flag, args.status)) {
+                    stop = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+                    const int s = fills % SB, t = fills % SA;
+                    const uint32_t ps = (fills / SB) & 1u, pt = (fills / SA) & 1u;
+                    if (!wait_phase(b_full(s), ps, limit, abort_flag, args.status) ||
+                        !wait_phase_cluster(b_conv(s), ps, limit, abort_flag, args.status) ||
+                        !wait_phase_cluster(a_full(t), pt, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t b_hi = ring + s * L::SLOT_BYTES, b_lo = b_hi + L::B_BYTES;
+                    const uint32_t a_hi = tmem_base + L::A_COL0 + (uint32_t)t * 64u, a_lo = a_hi + 32u;
+#pragma unroll
+                    for (int ks = 0; ks < L::KB / kUmmaK; ++ks) {
+                        const uint32_t boff = ks * kUmmaK * 4, acol = ks * kUmmaK;
+                        const uint32_t acc = (kb > u.kb0 || ks > 0) ? 1u : 0u;
+                        if (args.terms == 3) {
+                            ptx::mma_tf32_pair_ts(tmem_base, a_lo + acol, sw128_desc(b_hi + boff), idesc, acc);
+                            ptx::mma_tf32_pair_ts(tmem_base, a_hi + acol, sw128_desc(b_lo + boff), idesc, 1u);
+                            ptx::mma_tf32_pair_ts(tmem_base, a_hi + acol, sw128_desc(b_hi + boff), idesc, 1u);
+                        } else {
+                            ptx::mma_tf32_pair_ts(tmem_base, a_hi + acol, sw128_desc(b_hi + boff), idesc, acc);
+                        }
+                    }
+                    // both CTAs' B slot s and A slot t are free once these finish
+                    ptx::mma_commit_pair(b_empty(s), pair_mask);
+                    ptx::mma_commit_pair(a_empty(t), pair_mask);
+                }
+                if (stop) break;
+                ptx::mma_commit_pair(tfull, pair_mask);  // both CTAs' accumulators complete
+            }
+            if (stop) give_up();
+            ptx::mma_commit_pair(drain_bar, (uint16_t)(1u << lead));
+            const long long t0 = clock64();
+            while (!ptx::mbar_try_wait(drain_bar, 0))
+                if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------ epilogue ------------------------------
+        const int quad = warp & 3;
+        const uint32_t lead_tempty = ptx::mapa(tempty, lead);
+        int iter = 0;
+        bool stop = false;
+        for (int w = pair; w < num_work; w += npairs, ++iter) {
+            const PairUnit pu = pair_unit(w, args, (int)rank);
+            if (!wait_phase(tfull, (uint32_t)iter & 1u, limit, abort_flag, args.status)) {
+                stop = true;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
+            const EpilogueBars eb{drain_bar, drain_bar, drain_bar, drain_bar, drain_bar};  // unused
+            drain_unit<BN, L::RING_BYTES>(args, &tm_c, &tm_p, pu.u, pu.tm, pu.tn, taddr, quad, lane,
+                                          w + npairs >= num_work, false, false, ring, ring_ptr, eb, limit,
+                                          abort_flag);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(lead_tempty);
+        }
+        if (stop && lane == 0) give_up();
+    } else if (warp < 10) {
+        // ------------------------------ A loaders -----------------------------
+        // Warp w owns TMEM lanes 32 (w % 4) .. +31, i.e. those rows of this
+        // CTA's 128; a lane is one row.  Per 32-k block: the row's 128 bytes
+        // from the staging slot (16-byte chunks in the 128-byte swizzle, so a
+        // quarter-warp's 8 rows hit 8 distinct bank groups), the slot handed
+        // back, hi and lo written to A slot t, the slot handed to the even CTA
+        // (8 arrivals: 4 warps of each CTA).
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        uint32_t fills = 0;
+        bool stop = false;
+        for (int w = pair; w < num_work && !stop; w += npairs) {
+            const Unit u = decode_unit(w, args);
+            for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+                const int j = fills % SS, t = fills % SA;
+                const uint32_t pj = (fills / SS) & 1u, pt = (fills / SA) & 1u;
+                if (!__all_sync(0xffffffffu, wait_phase(s_full(j), pj, limit, abort_flag, args.status))) {
+                    stop = true;
+                    break;
+                }
+                const uint8_t* src = astage_ptr + j * L::STAGE_A_BYTES + row * 128;
+                float v[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 q = *reinterpret_cast<const float4*>(src + ((c ^ (row & 7)) << 4));
+                    v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+                }
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    hi[c] = __float_as_uint(v[c]) & 0xFFFFE000u;  // what the MMA reads of the raw value
+                    lo[c] = __float_as_uint(lo_part(v[c]));
+                }
+                // these generic-proxy reads before the TMA's next write of the slot
+                ptx::fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(s_empty(j));
+                // the MMAs of this slot's last use are done
+                if (!__all_sync(0xffffffffu, wait_phase(a_empty(t), pt ^ 1u, limit, abort_flag, args.status))) {
+                    stop = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t slot = tmem_base + lane_off + L::A_COL0 + (uint32_t)t * 64u;
+                ptx::tmem_st_32x32b_x32(slot, hi);
+                ptx::tmem_st_32x32b_x32(slot + 32u, lo);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(a_full(t), lead));
+            }
+        }
+        if (stop && lane == 0) give_up();
+    } else if (warp == 10) {
+        // ----------------------------- B forwarder ----------------------------
+        // The odd CTA's B stages, handed to the even CTA's MMA thread (release
+        // at cluster scope after this thread's acquire of the copies), in
+        // order; a slot is refilled only after the MMAs that needed this
+        // hand-off, so the parity wait is never a phase behind or ahead.
+        if (lane == 0 && rank == 1) {
+            uint32_t fills = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs) {
+                const Unit u = decode_unit(w, args);
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
+                    const int s = fills % SB;
+                    const uint32_t ps = (fills / SB) & 1u;
+                    if (!wait_phase(b_full(s), ps, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::mbar_arrive_cluster(ptx::mapa(b_conv(s), lead));
+                }
+            }
+            if (stop) give_up();
+        }
+    } else {
+        // ----------------------------- A producer -----------------------------
+        // Raw A of this CTA's 128 rows, one 32-k block per staging slot, in
+        // the loaders' order; rows past M and k past K read as zero.
+        if (lane == 0) {
+            pdl_wait();  // the previous kernel's writes (A) are done
+            uint32_t fills = 0;
+            bool stop = false;
+            for (int w = pair; w < num_work && !stop; w += npairs) {
+                const PairUnit pu = pair_unit(w, args, (int)rank);
+                for (int kb = pu.u.kb0; kb < pu.u.kb1; ++kb) {
+                    const int j = fills % SS;
+                    const uint32_t pj = (fills / SS) & 1u;
+                    if (!wait_phase(s_empty(j), pj ^ 1u, limit, abort_flag, args.status)) {
+                        stop = true;
+                        break;
+                    }
+                    ++fills;
+                    ptx::mbar_arrive_expect_tx(s_full(j), L::STAGE_A_BYTES);
+                    ptx::tma_load_2d(astage + j * L::STAGE_A_BYTES, &tm_a, s_full(j), kb * L::KB, pu.tm * kBM);
+                }
+            }
+            if (stop) give_up();
+            // Drain: the last fill of every slot must have landed.
+            const uint32_t total = fills;
+            for (int j = 0; j < SS && (uint32_t)j < total; ++j) {
+                const uint32_t last = (total - 1 - j) / SS * SS + j;
+                const uint32_t par = (last / SS) & 1u;
+                const long long t0 = clock64();
+                while (!ptx::mbar_try_wait(s_full(j), par))
+                    if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+            }
+        }
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    // no CTA leaves (or frees TMEM) while the pair's MMAs may still read its
+    // shared or tensor memory or its peer may still arrive on its barriers
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int NB, int NS>
+cudaError_t launch_pair_tmem(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
+                             const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
+{
+    using L = TmemALayout<NB, NS>;
+    auto kern = tc_pair_tmem_kernel<NB, NS>;
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = smem_limit_once(kern, L::SMEM_BYTES, smem_set); e != cudaSuccess) return e;
+    const int work = a.dp_tiles + a.split_tiles * a.splits;
+    const int pairs = work < st.pair_slots ? work : st.pair_slots;
+    if (pairs < 1 || a.cluster > 1) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(2 * pairs), dim3(kTmemAThreads), L::SMEM_BYTES, s, 2, ta, tbhi, tblo,
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
+                      *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
+}
+
+template <int NB, int NS>
+int pair_tmem_slots_for(int sms)
+{
+    using L = TmemALayout<NB, NS>;
+    auto kern = tc_pair_tmem_kernel<NB, NS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1));
+    cfg.blockDim = dim3(kTmemAThreads);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // Sum the K-slices of every split pair tile (its two 128-row tiles) in slice
 // order and write C (guarded).  Grid-stride over 2 x split_tiles (pairs) x 128
 // x BN/4 float4 positions; tile j = 2q + r of the split tiles is row half r of
@@ -738,6 +1148,12 @@ cudaError_t tc_pair_main(int bn, int bk, int split, const TcPlanState& st, const
     return cudaErrorInvalidValue;
 }
 
+cudaError_t tc_pair_tmem_main(const TcPlanState& st, const TcArgs& a, const CUtensorMap& ta,
+                              const CUtensorMap& tbhi, const CUtensorMap& tblo, cudaStream_t s)
+{
+    return launch_pair_tmem<5, 3>(st, a, ta, tbhi, tblo, s);
+}
+
 cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const TcArgs& a, cudaStream_t s)
 {
     const int64_t total = (int64_t)2 * a.split_tiles * kBM * (bn / 4);
@@ -752,9 +1168,10 @@ cudaError_t tc_pair_reduce(int bn, const TcPlanState& st, const TcArgs& a, cudaS
     return cudaErrorInvalidValue;
 }
 
-int tc_pair_slots(int bn, int bk, int sms)
+int tc_pair_slots(int bn, int bk, int sms, int split)
 {
-    // the same shared memory and threads for every form of the operands
+    if (split == kSplitTmemA) return bn == 256 && bk == 32 ? pair_tmem_slots_for<5, 3>(sms) : 0;
+    // the same shared memory and threads for every other form of the operands
     if (bn == 256 && bk == 32) return pair_slots_for<256, 3, 32>(sms);
     if (bn == 256 && bk == 16) return pair_slots_for<256, 6, 16>(sms);
     if (bn == 128 && bk == 32) return pair_slots_for<128, 4, 32>(sms);

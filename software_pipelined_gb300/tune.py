@@ -239,9 +239,10 @@ def effective_split(desc: str) -> int:
 
 
 def split_where(desc: str) -> int:
-    """The table's split field: 0 pre-pass, 1 in the kernel, 2 hybrid, 3 raw A."""
+    """The table's split field: 0 pre-pass, 1 in the kernel, 2 hybrid, 3 raw A,
+    4 A in tensor memory."""
     return (1 if "in-kernel-split" in desc else 2 if "hybrid-split" in desc
-            else 3 if "raw-a-split" in desc else 0)
+            else 3 if "raw-a-split" in desc else 4 if "tmem-a-split" in desc else 0)
 
 
 def write_inc(results, path):
@@ -253,7 +254,7 @@ def write_inc(results, path):
         "// tile_m (tcgen05: 256 = CTA pairs), tile_n, stages (0 = compiled default), split_k (0 = automatic",
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
         "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass,",
-        "// 3 hi of A read from A),",
+        "// 3 hi of A read from A, 4 A split into tensor memory by the CTA pair),",
         "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k and",
         "// k_slices (SIMT: K-tile depth, K-slice groups inside the CTA).",
         "struct TableRow {",

@@ -39,6 +39,7 @@ FORMS = {
     "pair_hybrid": dict(variant=TC, tile_m=256, operand_split=3),
     "pair_raw_a": dict(variant=TC, tile_m=256, operand_split=4),
     "pair_raw_a_k16": dict(variant=TC, tile_m=256, tile_n=256, operand_split=4, tile_k=16),
+    "pair_tmem_a": dict(variant=TC, tile_m=256, tile_n=256, operand_split=5),
     "split_k4": dict(variant=TC, split_k=4),
 }
 M, N, K = 300, 520, 264

@@ -135,6 +135,73 @@ def test_pair_raw_a_small_integers_padding_and_misaligned_fallback(bk):
     assert canaries and np.array_equal(C, exact), desc
 
 
+TMEMA_CASES = [
+    # M, N, K, split_k: A split by the kernel's loader warps into tensor memory,
+    # hi/lo of B by the pre-pass; 256x256 tiles, one accumulator per pair
+    (512, 512, 256, 2),
+    (300, 521, 264, 2),       # the second tile row past M; ldb = 521 (B needs no aligned rows)
+    (1024, 1024, 1024, 4),
+    (4096, 4096, 256, 0),     # 256 pair tiles: several units per pair through the one accumulator
+    (2304, 4096, 320, 0),     # partial last wave split automatically
+    (130, 33, 96, 2),         # one pair, most of it past M and N
+    (640, 768, 1000, 3),      # K not a multiple of 32: the last k-block's tail is zeros
+]
+TMEMA_IDS = [f"{m}x{n}x{k}_s{s}" for m, n, k, s in TMEMA_CASES]
+TMEMA = dict(PAIR, tile_n=256, tile_k=32, operand_split=5)
+
+
+@pytest.mark.parametrize("case", TMEMA_CASES, ids=TMEMA_IDS)
+def test_pair_tmem_a_matches_the_oracle(case):
+    M, N, K, split = case
+    A = inputs.uniform_pm1(2125, M, K)
+    B = inputs.normal(2126, K, N)
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, split_k=split, **TMEMA)
+    assert "tmem-a-split cta-pair" in desc and "tile=256x256x32" in desc, desc
+    err, ok = check_against_oracle(C, A, B)
+    assert canaries and ok, f"{desc}: {err}"
+    assert np.array_equal(outs[0], outs[1]), desc
+
+
+def test_pair_tmem_a_small_integers_padding_and_misaligned_fallback():
+    M, N, K = 520, 300, 200
+    A = inputs.small_int(2127, M, K, -4, 4)
+    B = inputs.small_int(2128, K, N, -4, 4)
+    exact = A.astype(np.float64) @ B.astype(np.float64)
+    opts = dict(TMEMA, split_k=2)
+    C, desc, canaries, _ = run_gemm(A, B, **opts)
+    assert "tmem-a-split cta-pair" in desc and canaries and np.array_equal(C, exact), desc
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 8, ldb=N + 3, ldc=N + 5, **opts)
+    assert canaries and np.array_equal(C, exact), desc
+    # A's base off a 16-byte boundary: the one-CTA pre-pass form (its own maps)
+    C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, a_off=1, **opts)
+    assert canaries and np.array_equal(C, exact), desc
+
+
+def test_pair_tmem_a_refusals_and_withheld_stage():
+    import torch
+    for kw in (dict(tile_n=128), dict(tile_k=16), dict(tile_m=128)):
+        with pytest.raises(g.GemmError):
+            g.Plan(512, 512, 512, **dict(TMEMA, **kw))
+    with pytest.raises(g.GemmError):
+        g.Plan(512, 512, 256, 257, 512, 512, **TMEMA)
+    M, N, K = 512, 512, 512
+    A = inputs.uniform_pm1(2129, M, K)
+    B = inputs.uniform_pm1(2130, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    for withhold in (1, 5):
+        with g.Plan(M, N, K, split_k=2, wait_timeout_cycles=1 << 22, debug_withhold_stage=withhold, **TMEMA) as p:
+            p.run(dA, dB, dC)
+            assert p.check() == g.ERR_TIMEOUT
+    torch.cuda.synchronize()
+    dC.fill_(float("nan"))
+    with g.Plan(M, N, K, split_k=2, **TMEMA) as p:
+        p.run(dA, dB, dC)
+        assert p.check() == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
 def test_pair_hybrid_small_integers_and_misaligned_fallback():
     M, N, K = 520, 300, 200
     A = inputs.small_int(2117, M, K, -4, 4)
@@ -286,7 +353,7 @@ def test_pair_cluster_sum_withheld_stage_times_out():
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
 
 
-@pytest.mark.parametrize("mode", [2, 3, 4], ids=["in_kernel", "hybrid", "raw_a"])
+@pytest.mark.parametrize("mode", [2, 3, 4, 5], ids=["in_kernel", "hybrid", "raw_a", "tmem_a"])
 def test_pair_run_host_blocks_ragged_with_splits(mode):
     # Ragged M and N (the last panel's second tile row and the last block's
     # columns past the edge), K-slices in every panel's last wave, padded C:
@@ -308,7 +375,7 @@ def test_pair_run_host_blocks_ragged_with_splits(mode):
             assert (C[:, N:] == 321.0).all()
 
 
-@pytest.mark.parametrize("mode", [2, 3, 4], ids=["in_kernel", "hybrid", "raw_a"])
+@pytest.mark.parametrize("mode", [2, 3, 4, 5], ids=["in_kernel", "hybrid", "raw_a", "tmem_a"])
 @pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (3, 2), (2, 3)])
 def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels, cols):
     # Without a K-split every tile is summed in the same order whichever 256-row

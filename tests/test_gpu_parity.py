@@ -739,12 +739,13 @@ NONFINITE_VARIANTS = [SIMT, TC, {"variant": g.VARIANT_TCGEN05, "operand_split": 
                       {"variant": g.VARIANT_TCGEN05, "operand_split": 4},
                       {"variant": g.VARIANT_TCGEN05, "split_k": 4},
                       {"variant": g.VARIANT_TCGEN05, "tile_m": 256, "operand_split": 3},
-                      {"variant": g.VARIANT_TCGEN05, "tile_m": 256, "operand_split": 4}]
+                      {"variant": g.VARIANT_TCGEN05, "tile_m": 256, "operand_split": 4},
+                      {"variant": g.VARIANT_TCGEN05, "tile_m": 256, "tile_n": 256, "operand_split": 5}]
 
 
 @pytest.mark.parametrize("variant", NONFINITE_VARIANTS,
                          ids=["simt", "tcgen05", "in_kernel", "in_kernel_k16", "hybrid", "raw_a", "split4",
-                              "pair_hybrid", "pair_raw_a"])
+                              "pair_hybrid", "pair_raw_a", "pair_tmem_a"])
 def test_non_finite_inputs(variant):
     M, N, K = 300, 260, 100
     A = inputs.uniform_pm1(1751, M, K)
