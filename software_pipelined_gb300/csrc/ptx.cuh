@@ -63,6 +63,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
                  " [%0], [%1, {%3, %4}], [%2];\n"
                  :: "r"(dst), "l"(tmap), "r"(bar), "r"(c0), "r"(c1) : "memory");
 }
+// The same load issued by one CTA of a CTA pair (tcgen05 cta_group::2): its
+// completion may be signalled on the mbarrier of either CTA of the pair (bar:
+// a shared::cluster address, e.g. the peer's barrier through mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4}], [%2];\n"
+                 :: "r"(dst), "l"(tmap), "r"(bar), "r"(c0), "r"(c1) : "memory");
+}
 // Store a box from shared memory (the tensor map's box and swizzle) at
 // element coordinates (c0 innermost, c1); boxes past the tensor's edge are
 // clipped.  Tracked by bulk groups (commit / wait below).

@@ -11,9 +11,10 @@
 //     transposed to hi_B / lo_B by its converters);
 //   * or, in two lighter forms, B arrives split and transposed by the operand
 //     pre-pass (hi_B and lo_B by TMA), and in the second of them lo_A too (hi
-//     of A is the raw A, which the MMA truncates): then the converter warps
-//     only hand each landed stage to the even CTA, and no conversion sits
-//     between a stage's copy and its MMAs;
+//     of A is the raw A, which the MMA truncates): then both CTAs' copies of
+//     a stage complete on the even CTA's barrier (the TMA's cta_group::2 form
+//     may signal the peer's barrier), and nothing sits between a stage's
+//     copies and its MMAs;
 //   * the even CTA's MMA thread issues M = 256, N = BN MMAs that read A rows
 //     0..127 and B columns 0..BN/2-1 from its own shared memory and the rest
 //     from its peer's, at the same addresses, and accumulate the even CTA's
@@ -25,14 +26,15 @@
 //
 // Synchronisation (every wait bounded; a CTA that gives up raises its own and
 // its peer's abort flag):
-//   full_a[s]  TMA of the CTA's raw A and B landed (local)
+//   full_a[s]  TMA of the CTA's raw A and B landed (local); in the form with
+//              nothing to convert, the even CTA's barrier counts both CTAs'
+//              copies (armed by the even CTA with the pair's bytes)
 //   rd[s]      every converter warp (of the group on that stage) holds its
 //              raw B (local)
 //   conv[s]    (even CTA) both CTAs' converters are done: counts 2 x 4 warps
 //              (one group of each CTA), the odd CTA's arriving remotely with
-//              release at cluster scope; in the form with nothing to convert,
-//              the odd CTA's forwarding thread (1 arrival), the MMA thread
-//              waiting on its own CTA's full_a[s] as well
+//              release at cluster scope (unused in the form with nothing to
+//              convert)
 //   empty[s]   the pair's MMAs of slot s completed: one commit, multicast to
 //              both CTAs
 //   tfull      accumulator complete: commit multicast to both CTAs
@@ -311,10 +313,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
             ptx::mbar_init(full_a(s), 1);
-            // one group of each CTA's converters, or (nothing to convert) the
-            // odd CTA's forwarding thread (the even CTA's MMA thread waits for
-            // its own copies on full_a itself)
-            ptx::mbar_init(conv(s), APRE ? 1 : 2 * kPairConvWarps / kConvGroups);
+            // one group of each CTA's converters
+            ptx::mbar_init(conv(s), 2 * kPairConvWarps / kConvGroups);
             ptx::mbar_init(empty(s), 1);
             ptx::mbar_init(rd(s), kPairConvWarps / kConvGroups);
         }
@@ -378,13 +378,16 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     const int kc = kh * KB;
                     const uint32_t slot = ring + s * L::SLOT_BYTES;
                     if constexpr (APRE) {
-                        // raw A (= hi_A) and lo_A, this CTA's half of hi_B and lo_B
-                        ptx::mbar_arrive_expect_tx(full_a(s), 2 * L::A_BYTES + 2 * L::B_BYTES);
-                        ptx::tma_load_2d(slot, &tm_a, full_a(s), kc, pu.tm * kBM);
-                        ptx::tma_load_2d(slot + L::A_BYTES, &tm_alo, full_a(s), kc, pu.tm * kBM);
+                        // raw A (= hi_A) and lo_A, this CTA's half of hi_B and lo_B;
+                        // both CTAs' copies complete on the even CTA's barrier, which
+                        // the even CTA's thread arms with the pair's bytes
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_a(s), 2 * (2 * L::A_BYTES + 2 * L::B_BYTES));
+                        const uint32_t fb = rank == 0 ? full_a(s) : ptx::mapa(full_a(s), lead);
+                        ptx::tma_load_2d_pair(slot, &tm_a, fb, kc, pu.tm * kBM);
+                        ptx::tma_load_2d_pair(slot + L::A_BYTES, &tm_alo, fb, kc, pu.tm * kBM);
                         const int n0 = pu.tn * BN + (int)rank * L::BH;
-                        ptx::tma_load_2d(slot + 2 * L::A_BYTES, &tm_bhi, full_a(s), kc, n0);
-                        ptx::tma_load_2d(slot + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, full_a(s), kc, n0);
+                        ptx::tma_load_2d_pair(slot + 2 * L::A_BYTES, &tm_bhi, fb, kc, n0);
+                        ptx::tma_load_2d_pair(slot + 2 * L::A_BYTES + L::B_BYTES, &tm_blo, fb, kc, n0);
                     } else if constexpr (BPRE) {
                         // raw A into the A part, this CTA's half of hi_B and lo_B
                         ptx::mbar_arrive_expect_tx(full_a(s), L::A_BYTES + 2 * L::B_BYTES);
@@ -405,15 +408,28 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
             if (stop) give_up();
-            // Drain: the last fill of every slot must have landed.
+            // Drain: the last fill of every slot must have landed.  With every
+            // piece by TMA the odd CTA's copies complete on the even CTA's
+            // barriers, so the even CTA's drain covers both CTAs (and the odd
+            // CTA leaves only after it, at the final cluster barrier); after
+            // an abort the odd CTA gives a copy it issued without a matching
+            // copy of the even CTA time to land.
             const uint32_t total = fills;
-            for (int s = 0; s < SLOTS && (uint32_t)s < total; ++s) {
-                const uint32_t last = (total - 1 - s) / SLOTS * SLOTS + s;
-                if (last + 1 == (uint32_t)args.withhold) continue;
-                const uint32_t par = (last / SLOTS) & 1u;
-                const long long t0 = clock64();
-                while (!ptx::mbar_try_wait(full_a(s), par))
-                    if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+            if (APRE && rank == 1) {
+                if (stop) {
+                    const long long t0 = clock64();
+                    while (clock64() - t0 < (1 << 20)) {
+                    }
+                }
+            } else {
+                for (int s = 0; s < SLOTS && (uint32_t)s < total; ++s) {
+                    const uint32_t last = (total - 1 - s) / SLOTS * SLOTS + s;
+                    if (last + 1 == (uint32_t)args.withhold) continue;
+                    const uint32_t par = (last / SLOTS) & 1u;
+                    const long long t0 = clock64();
+                    while (!ptx::mbar_try_wait(full_a(s), par))
+                        if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+                }
             }
         }
         __syncwarp();
@@ -437,11 +453,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
                     const int s = fills % SLOTS;
                     const uint32_t ps = (fills / SLOTS) & 1u;
-                    if (APRE && !wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
-                        stop = true;
-                        break;
-                    }
-                    if (!wait_phase_cluster(conv(s), ps, limit, abort_flag, args.status)) {
+                    if (APRE ? !wait_phase(full_a(s), ps, limit, abort_flag, args.status)
+                             : !wait_phase_cluster(conv(s), ps, limit, abort_flag, args.status)) {
                         stop = true;
                         break;
                     }
@@ -510,31 +523,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         if (stop && lane == 0) give_up();
     } else if constexpr (APRE) {
-        // ------------------------------ forwarder -----------------------------
-        // Every piece of the stage comes by TMA: one thread of the odd CTA
-        // hands each landed stage to the even CTA's MMA thread (release at
-        // cluster scope after its own acquire of the copies); the MMA thread
-        // waits for the even CTA's copies itself.  The forwarder takes the
-        // stages in order, and a slot is refilled only after the MMAs that
-        // needed this hand-off, so its parity wait is never a phase behind or
-        // ahead.
-        if (threadIdx.x == 6 * 32 && rank == 1) {
-            uint32_t fills = 0;
-            bool stop = false;
-            for (int w = pair; w < num_work && !stop; w += npairs) {
-                const Unit u = decode_unit(w, args);
-                for (int kh = u.kb0 * HALVES; kh < u.kb1 * HALVES; ++kh, ++fills) {
-                    const int s = fills % SLOTS;
-                    const uint32_t ps = (fills / SLOTS) & 1u;
-                    if (!wait_phase(full_a(s), ps, limit, abort_flag, args.status)) {
-                        stop = true;
-                        break;
-                    }
-                    ptx::mbar_arrive_cluster(ptx::mapa(conv(s), lead));
-                }
-            }
-            if (stop) give_up();
-        }
+        // nothing to convert: the converter warps idle
     } else {
         // ------------------------------ converters ----------------------------
         // Two groups of warps take alternate stages, so that one group's
@@ -649,8 +638,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 // Barriers (every wait bounded; a CTA that gives up raises both abort flags):
 //   s_full[j]   raw A of staging slot j landed (TMA, local)
 //   s_empty[j]  this CTA's 4 loader warps have read staging slot j (local)
-//   b_full[s]   this CTA's hi_B / lo_B halves of stage s landed (TMA, local)
-//   b_conv[s]   (even CTA) the odd CTA's stage s landed: its forwarding thread
+//   b_full[s]   (even CTA) both CTAs' hi_B / lo_B halves of stage s landed
+//               (TMA; the odd CTA's copies signal it directly)
 //   b_empty[s]  the pair's MMAs of B slot s completed (commit, multicast)
 //   a_full[t]   (even CTA) both CTAs' loader warps wrote A slot t: 8 arrivals
 //   a_empty[t]  the pair's MMAs of A slot t completed (commit, multicast)
@@ -664,7 +653,7 @@ struct TmemALayout {
     static constexpr int SLOT_BYTES = 2 * B_BYTES;  // hi_B, lo_B
     static constexpr int RING_BYTES = NB_SLOTS * SLOT_BYTES;
     static constexpr int STAGE_A_BYTES = kBM * KB * 4;  // raw A of one stage: 128 rows x 32
-    static constexpr int NBARS = 3 * NB_SLOTS + 2 * A_SLOTS + 2 * NA_STAGE + 3;
+    static constexpr int NBARS = 2 * NB_SLOTS + 2 * A_SLOTS + 2 * NA_STAGE + 3;
     static constexpr int BAR_BYTES = 8 * NBARS + 16;
     // B_BYTES of slack after the barriers, as in PairLayout
     static constexpr int SMEM_BYTES = 1024 + RING_BYTES + NA_STAGE * STAGE_A_BYTES + BAR_BYTES + B_BYTES;
@@ -673,8 +662,8 @@ struct TmemALayout {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(RING_BYTES >= 4 * 8 * 4096, "the ring holds the last unit's TMA-store staging");
 };
-// B producer, MMA, 4 epilogue, 4 loader warps, B forwarder, A producer
-constexpr int kTmemAThreads = 12 * 32;
+// B producer, MMA, 4 epilogue, 4 loader warps, A producer
+constexpr int kTmemAThreads = 11 * 32;
 
 template <int NB_SLOTS, int NA_STAGE>
 __global__ void __launch_bounds__(kTmemAThreads, 1)
@@ -700,15 +689,14 @@ tc_pair_tmem_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     const uint32_t rank = crank & 1u, lead = crank & ~1u;
     const uint16_t pair_mask = (uint16_t)(3u << lead);
     auto b_full = [&](int s) { return ptx::smem_u32(bars + s); };
-    auto b_conv = [&](int s) { return ptx::smem_u32(bars + SB + s); };
-    auto b_empty = [&](int s) { return ptx::smem_u32(bars + 2 * SB + s); };
-    auto a_full = [&](int t) { return ptx::smem_u32(bars + 3 * SB + t); };
-    auto a_empty = [&](int t) { return ptx::smem_u32(bars + 3 * SB + SA + t); };
-    const uint32_t tfull = ptx::smem_u32(bars + 3 * SB + 2 * SA);
-    const uint32_t tempty = ptx::smem_u32(bars + 3 * SB + 2 * SA + 1);
-    const uint32_t drain_bar = ptx::smem_u32(bars + 3 * SB + 2 * SA + 2);
-    auto s_full = [&](int j) { return ptx::smem_u32(bars + 3 * SB + 2 * SA + 3 + j); };
-    auto s_empty = [&](int j) { return ptx::smem_u32(bars + 3 * SB + 2 * SA + 3 + SS + j); };
+    auto b_empty = [&](int s) { return ptx::smem_u32(bars + SB + s); };
+    auto a_full = [&](int t) { return ptx::smem_u32(bars + 2 * SB + t); };
+    auto a_empty = [&](int t) { return ptx::smem_u32(bars + 2 * SB + SA + t); };
+    const uint32_t tfull = ptx::smem_u32(bars + 2 * SB + 2 * SA);
+    const uint32_t tempty = ptx::smem_u32(bars + 2 * SB + 2 * SA + 1);
+    const uint32_t drain_bar = ptx::smem_u32(bars + 2 * SB + 2 * SA + 2);
+    auto s_full = [&](int j) { return ptx::smem_u32(bars + 2 * SB + 2 * SA + 3 + j); };
+    auto s_empty = [&](int j) { return ptx::smem_u32(bars + 2 * SB + 2 * SA + 3 + SS + j); };
     const uint32_t peer_abort = ptx::mapa(ptx::smem_u32(const_cast<int*>(abort_flag)), crank ^ 1u);
     auto give_up = [&]() {
         *abort_flag = 1;
@@ -718,7 +706,6 @@ tc_pair_tmem_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < SB; ++s) {
             ptx::mbar_init(b_full(s), 1);
-            ptx::mbar_init(b_conv(s), 1);
             ptx::mbar_init(b_empty(s), 1);
         }
         for (int t = 0; t < SA; ++t) {
@@ -775,21 +762,34 @@ tc_pair_tmem_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
                     if (fills == (uint32_t)args.withhold) continue;
                     const uint32_t slot = ring + s * L::SLOT_BYTES;
                     const int n0 = pu.tn * BN + (int)rank * L::BH;
-                    ptx::mbar_arrive_expect_tx(b_full(s), L::SLOT_BYTES);
-                    ptx::tma_load_2d(slot, &tm_bhi, b_full(s), kb * L::KB, n0);
-                    ptx::tma_load_2d(slot + L::B_BYTES, &tm_blo, b_full(s), kb * L::KB, n0);
+                    // both CTAs' halves complete on the even CTA's barrier
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(b_full(s), 2 * L::SLOT_BYTES);
+                    const uint32_t fb = rank == 0 ? b_full(s) : ptx::mapa(b_full(s), lead);
+                    ptx::tma_load_2d_pair(slot, &tm_bhi, fb, kb * L::KB, n0);
+                    ptx::tma_load_2d_pair(slot + L::B_BYTES, &tm_blo, fb, kb * L::KB, n0);
                 }
             }
             if (stop) give_up();
-            // Drain: the last fill of every slot must have landed.
+            // Drain: the last fill of every slot must have landed (the even
+            // CTA's barriers count both CTAs' copies; after an abort the odd
+            // CTA gives a copy without a matching copy of the even CTA time to
+            // land).
             const uint32_t total = fills;
-            for (int s = 0; s < SB && (uint32_t)s < total; ++s) {
-                const uint32_t last = (total - 1 - s) / SB * SB + s;
-                if (last + 1 == (uint32_t)args.withhold) continue;
-                const uint32_t par = (last / SB) & 1u;
-                const long long t0 = clock64();
-                while (!ptx::mbar_try_wait(b_full(s), par))
-                    if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+            if (rank == 1) {
+                if (stop) {
+                    const long long t0 = clock64();
+                    while (clock64() - t0 < (1 << 20)) {
+                    }
+                }
+            } else {
+                for (int s = 0; s < SB && (uint32_t)s < total; ++s) {
+                    const uint32_t last = (total - 1 - s) / SB * SB + s;
+                    if (last + 1 == (uint32_t)args.withhold) continue;
+                    const uint32_t par = (last / SB) & 1u;
+                    const long long t0 = clock64();
+                    while (!ptx::mbar_try_wait(b_full(s), par))
+                        if (clock64() - t0 > limit) { atomicExch(args.status, kStatusTimeout); break; }
+                }
             }
         }
         __syncwarp();
@@ -812,7 +812,6 @@ tc_pair_tmem_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
                     const int s = fills % SB, t = fills % SA;
                     const uint32_t ps = (fills / SB) & 1u, pt = (fills / SA) & 1u;
                     if (!wait_phase(b_full(s), ps, limit, abort_flag, args.status) ||
-                        !wait_phase_cluster(b_conv(s), ps, limit, abort_flag, args.status) ||
                         !wait_phase_cluster(a_full(t), pt, limit, abort_flag, args.status)) {
                         stop = true;
                         break;
@@ -924,29 +923,6 @@ tc_pair_tmem_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             }
         }
         if (stop && lane == 0) give_up();
-    } else if (warp == 10) {
-        // ----------------------------- B forwarder ----------------------------
-        // The odd CTA's B stages, handed to the even CTA's MMA thread (release
-        // at cluster scope after this thread's acquire of the copies), in
-        // order; a slot is refilled only after the MMAs that needed this
-        // hand-off, so the parity wait is never a phase behind or ahead.
-        if (lane == 0 && rank == 1) {
-            uint32_t fills = 0;
-            bool stop = false;
-            for (int w = pair; w < num_work && !stop; w += npairs) {
-                const Unit u = decode_unit(w, args);
-                for (int kb = u.kb0; kb < u.kb1; ++kb, ++fills) {
-                    const int s = fills % SB;
-                    const uint32_t ps = (fills / SB) & 1u;
-                    if (!wait_phase(b_full(s), ps, limit, abort_flag, args.status)) {
-                        stop = true;
-                        break;
-                    }
-                    ptx::mbar_arrive_cluster(ptx::mapa(b_conv(s), lead));
-                }
-            }
-            if (stop) give_up();
-        }
     } else {
         // ----------------------------- A producer -----------------------------
         // Raw A of this CTA's 128 rows, one 32-k block per staging slot, in

@@ -280,6 +280,31 @@ def test_pair_withheld_stage_times_out_and_context_survives():
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
 
 
+def test_pair_raw_a_withheld_stage_times_out_and_context_survives():
+    # Every piece by TMA, both CTAs' copies completing on the even CTA's
+    # barrier: a fill withheld by both producers leaves that barrier short, the
+    # MMA thread gives up after the limit, and the next run is right.
+    import torch
+    M, N, K = 512, 512, 512
+    A = inputs.uniform_pm1(2131, M, K)
+    B = inputs.uniform_pm1(2132, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    opts = dict(PAIR, tile_n=256, split_k=2, operand_split=4)
+    for withhold in (1, 3, 6):
+        with g.Plan(M, N, K, wait_timeout_cycles=1 << 22, debug_withhold_stage=withhold, **opts) as p:
+            assert "raw-a-split cta-pair" in p.describe()
+            p.run(dA, dB, dC)
+            assert p.check() == g.ERR_TIMEOUT
+    torch.cuda.synchronize()
+    dC.fill_(float("nan"))
+    with g.Plan(M, N, K, **opts) as p:
+        p.run(dA, dB, dC)
+        assert p.check() == g.OK
+    Cref, S = oracle.gemm_f64(A, B)
+    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
 def test_pair_launch_count_and_host_run():
     import torch
     M, N, K = 1024, 1024, 1024
