@@ -160,13 +160,13 @@ int auto_split(int64_t tiles, int64_t K, int64_t min_k_per_split, int sms)
 //     below, a K-split when the tiles fill under half the SMs.
 //   * both M and N at least 1000: 256x256 tiles on CTA pairs (one
 //     tcgen05.mma across two SMs halves each CTA's B traffic).  Products of
-//     2^34 multiply-adds and more with both sides at least 2048 read lo of A
-//     and B pre-split (no conversion inside the kernel; 3072^3 229 vs 233 us,
-//     6144^3 1646 vs 1802 us for the one-CTA pre-pass form the rule took
-//     before; with a side of 1024 the pre-pass costs more than it saves:
-//     1024x4096x4096 176 vs 157 us); the others split both operands in the
-//     kernel (B by the pre-pass when its rows are not 16-byte aligned); a
-//     K-split so that the pairs fill the machine.
+//     2^33 multiply-adds and more read lo of A and B pre-split (no conversion
+//     inside the kernel, both CTAs' copies completing on one barrier; 2560^3
+//     123 vs 137 us, 4096x1024x4096 138 vs 152 us against splitting in the
+//     kernel, 2048^3 a tie); the smaller ones split both operands in the
+//     kernel (B by the pre-pass when its rows are not 16-byte aligned), where
+//     the pre-pass launch costs more than the conversion it saves; a K-split
+//     so that the pairs fill the machine.
 //   * otherwise (skinny, or under 1000 on a side): 128x128 tiles on one CTA,
 //     operands split in the kernel (B by the pre-pass when its rows are not
 //     aligned), K-split to fill the SMs (8192x256x1024 28 vs 40 us,
@@ -190,7 +190,7 @@ DispatchChoice choose_tc(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
         c.tile_m = 256;
         c.tile_n = 256;
         c.tile_k = 32;
-        c.fused = macs >= 17179869184.0 && M >= 2048 && N >= 2048 ? kSplitRawA : b_split;
+        c.fused = macs >= 8589934592.0 ? kSplitRawA : b_split;
         const int64_t ptiles = ((M + 255) / 256) * ((N + 255) / 256);
         c.split_k = ptiles >= sms / 4 ? 0 : auto_split(ptiles, K, 192, sms / 2);
         return c;
