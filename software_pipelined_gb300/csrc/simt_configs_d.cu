@@ -19,6 +19,12 @@ extern const SimtEntry kSimtPartD[] = {
     // deeper rings: a small tile's FFMAs per K-tile are too few to cover a copy
     {{32, 32, 32, 4, 4, 3, false, 4}, launch_cfg<32, 32, 32, 4, 4, 3, false, 4>},
     {{32, 32, 32, 4, 4, 4, false, 4}, launch_cfg<32, 32, 32, 4, 4, 4, false, 4>},
+    // half-height / half-width tiles: twice the CTAs, two to an SM, for grids
+    // of 32x32 tiles just over the SM count
+    {{16, 32, 32, 4, 4, 3, false, 4}, launch_cfg<16, 32, 32, 4, 4, 3, false, 4>},
+    {{16, 32, 32, 4, 4, 3, false, 2}, launch_cfg<16, 32, 32, 4, 4, 3, false, 2>},
+    {{32, 16, 32, 4, 4, 3, false, 4}, launch_cfg<32, 16, 32, 4, 4, 3, false, 4>},
+    {{32, 16, 32, 4, 4, 3, false, 2}, launch_cfg<32, 16, 32, 4, 4, 3, false, 2>},
     {{32, 32, 64, 4, 4, 3, false, 4}, launch_cfg<32, 32, 64, 4, 4, 3, false, 4>},
     {{64, 64, 16, 4, 4, 4, false, 2}, launch_cfg<64, 64, 16, 4, 4, 4, false, 2>},
     {{32, 64, 32, 4, 4, 3, false, 2}, launch_cfg<32, 64, 32, 4, 4, 3, false, 2>},

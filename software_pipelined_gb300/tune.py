@@ -37,7 +37,8 @@ from software_pipelined_gb300 import inputs  # noqa: E402
 SIMT_CFGS = [(128, 128, 2, 16), (128, 128, 3, 16), (128, 128, 1, 16), (64, 64, 2, 16), (64, 64, 3, 16),
              (64, 64, 1, 16), (64, 64, 2, 32), (32, 32, 2, 32), (32, 32, 1, 32), (128, 64, 2, 16),
              (32, 32, 3, 32), (32, 32, 1, 64), (32, 32, 2, 64), (32, 64, 2, 32), (64, 32, 2, 32),
-             (32, 32, 4, 32), (32, 32, 3, 64), (64, 64, 4, 16), (32, 64, 3, 32), (64, 32, 3, 32)]
+             (32, 32, 4, 32), (32, 32, 3, 64), (64, 64, 4, 16), (32, 64, 3, 32), (64, 32, 3, 32),
+             (16, 32, 3, 32), (32, 16, 3, 32)]
 TC_BN = [64, 128, 256]
 SPLITS = [1, 2, 3, 4, 6, 8, 12, 16]
 
