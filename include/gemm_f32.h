@@ -158,7 +158,11 @@ typedef struct {
                                slices of a tile run as one cluster of 2 or 4 CTAs and sum in
                                distributed shared memory (needs every tile split in 2 or 4,
                                all slices resident at once, tiles at most 128 wide and a ring
-                               of 128 KB or more; else UNSUPPORTED) */
+                               of 128 KB or more; else UNSUPPORTED); 4 = CTA pairs (tile_m 256,
+                               operand_split 2 to 4) only: the kernel's grid, launched
+                               cooperatively, passes a grid-wide barrier once every unit is
+                               stored and then sums the slices itself, in the reduction
+                               kernel's order (bit-identical; no reduction launch) */
     int32_t k_slices;       /* SIMT only: thread groups of a CTA that split each K-tile between
                                them and add their register tiles at the end (1, 2 or 4; 0 = the
                                dispatcher's choice): more warps per SM for small grids without a

@@ -132,7 +132,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
-    if (o.split_reduce < 0 || o.split_reduce > 3) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.split_reduce < 0 || o.split_reduce > 4) return GEMM_F32_ERR_INVALID_ARG;
     if (!(o.k_slices == 0 || o.k_slices == 1 || o.k_slices == 2 || o.k_slices == 4)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_col_blocks < 0 || o.host_col_blocks > 16) return GEMM_F32_ERR_INVALID_ARG;
     if (o.simt_fragments != 0 && o.simt_fragments != 1) return GEMM_F32_ERR_INVALID_ARG;
@@ -402,7 +402,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // the table's K-slice sum goes with its own split
             t.cluster_mode = o.split_reduce ? o.split_reduce : o.split_k ? 0 : c.reduce;
             tc_configure(t, M, N, K, c.split_k);
-            if ((o.split_reduce == 2 && t.cluster == 0) || (o.split_reduce == 3 && t.fixup == 0)) {
+            if ((o.split_reduce == 2 && t.cluster == 0) || (o.split_reduce == 3 && t.fixup == 0) ||
+                (o.split_reduce == 4 && t.gridsum == 0)) {
                 delete p;
                 return GEMM_F32_ERR_UNSUPPORTED;
             }
@@ -433,7 +434,8 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                          tcfg.split == kSplitHybrid ? "hybrid-split"
                          : tcfg.split == kSplitRawA ? "raw-a-split"
                          : tcfg.split == kSplitTmemA ? "tmem-a-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
-                         t.split_tiles, t.splits, t.cluster ? " cluster-sum" : "", t.pair_slots,
+                         t.split_tiles, t.splits, t.cluster ? " cluster-sum" : t.gridsum ? " grid-sum" : "",
+                         t.pair_slots,
                          t.tile_group > 0 ? t.tile_group : 8,
                          (long long)t.kp);
             else

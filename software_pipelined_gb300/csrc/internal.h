@@ -125,11 +125,15 @@ struct TcPlanState {
     int split_request = 0;     // the split policy tc_configure was given
     // K-slice sums (the plan's split_reduce option): 0 and 1 = the reduction
     // kernel; 2 = in a thread-block cluster where possible; 3 = the last slice
-    // to arrive sums the tile where possible
+    // to arrive sums the tile where possible; 4 = the CTA pairs' whole grid,
+    // after a grid-wide barrier
     int cluster_mode = 0;
     int cluster = 0;           // > 1: slices per tile, summed in a thread-block cluster
     int fixup = 0;             // 1: the last slice to arrive sums the tile
-    int* sem = nullptr;        // fixup arrival counters (zero between runs), sem_bytes long
+    int gridsum = 0;           // 1: CTA pairs: the whole (cooperative) grid sums the slices
+                               // after a grid-wide barrier, no reduction launch
+    int* sem = nullptr;        // fixup arrival counters or the grid barrier's count and
+                               // generation (zero between runs), sem_bytes long
     size_t sem_bytes = 0;
     // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;

@@ -43,6 +43,9 @@ struct TcArgs {
     int cluster;         // > 1: every tile split in `cluster` K-slices, one CTA each, the
                          // slices of a tile one thread-block cluster that sums them
                          // through distributed shared memory (no partial tiles)
+    int gridsum;         // 1: CTA pairs, cooperative grid: once every CTA has stored its
+                         // units, a grid-wide barrier (sem[0] count, sem[1] generation),
+                         // then every CTA sums a share of the split tiles' slices
 };
 
 // One unit of work of the persistent kernel: a whole tile, or one K-slice of a
@@ -585,15 +588,18 @@ __device__ __forceinline__ bool drain_unit(const TcArgs& args, const CUtensorMap
 // way of summing them gives the same bits), with the loads of up to four
 // slices in flight at once (the first, then three at a time).  p: slice 0;
 // STRIDE: float4 from one slice to the next.
-template <int STRIDE>
+// COHERENT: loads through L2 only (ld.global.cg), for slices written by other
+// CTAs of the same kernel; else the read-only path.
+template <int STRIDE, bool COHERENT = false>
 __device__ __forceinline__ float4 sum_slices(const float4* __restrict__ p, int splits)
 {
-    float4 acc = __ldg(p);
+    auto ld = [](const float4* q) { return COHERENT ? __ldcg(q) : __ldg(q); };
+    float4 acc = ld(p);
     for (int z = 1; z < splits; z += 3) {
         float4 t[3];
 #pragma unroll
         for (int i = 0; i < 3; ++i)
-            if (z + i < splits) t[i] = __ldg(p + (int64_t)(z + i) * STRIDE);
+            if (z + i < splits) t[i] = ld(p + (int64_t)(z + i) * STRIDE);
 #pragma unroll
         for (int i = 0; i < 3; ++i)
             if (z + i < splits) {
@@ -625,29 +631,81 @@ inline int reduce_blocks(int64_t work, int sms)
 // the previous kernel on the stream finishes, and waits for it (griddepcontrol)
 // before touching that kernel's output.  cluster > 1: thread-block clusters of
 // that many consecutive CTAs (the grid is a multiple of it).
+// cooperative: the runtime guarantees that every CTA of the grid is resident
+// at once (the launch fails otherwise), for kernels whose CTAs wait on one
+// another.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
-                       Args&&... args)
+cudaError_t launch_pdl_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
+                          bool cooperative, Args&&... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cluster > 1) {
         if (grid.x % (unsigned)cluster != 0) return cudaErrorInvalidValue;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = (unsigned)cluster;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = (unsigned)cluster;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    if (cooperative) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+        attr[cfg.numAttrs].val.cooperative = 1;
+        ++cfg.numAttrs;
     }
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
+                       Args&&... args)
+{
+    return launch_pdl_ex(kern, grid, block, smem, s, cluster, false, std::forward<Args>(args)...);
+}
+
+// A barrier across every CTA of a cooperative grid.  bar[0] counts arrivals,
+// bar[1] is the generation: a CTA reads the generation, releases its writes
+// (fence at GPU scope) and arrives; the last to arrive resets the count and
+// advances the generation; the others wait (bounded) until it moves, then
+// acquire.  The count is back at zero after every complete barrier; a barrier
+// that timed out leaves it as it stands, and the host clears it with the
+// status word.  Called by every thread of the CTA (ok_s: a word of the CTA's
+// shared memory free for the purpose); false = gave up.
+__device__ __forceinline__ bool grid_barrier(unsigned* bar, int64_t limit, int* status, volatile int* ok_s)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        volatile unsigned* gen = bar + 1;
+        const unsigned g = *gen;
+        __threadfence();
+        const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+        if (arrived == gridDim.x * gridDim.y * gridDim.z) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            const long long t0 = clock64();
+            while (*gen == g) {
+                if (clock64() - t0 > limit) {
+                    atomicExch(status, kStatusTimeout);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        *ok_s = ok;
+    }
+    __syncthreads();
+    return *ok_s != 0;
 }
 
 }  // namespace tc

@@ -284,7 +284,11 @@ void pair_configure(TcPlanState& t, int64_t M, int64_t N, int split_request)
     t.cluster = t.cluster_mode == 2 && t.dp_tiles == 0 && t.split_tiles > 0 && (t.splits == 2 || t.splits == 4)
                     ? t.splits : 0;
     t.fixup = 0;
-    t.sem_bytes = 0;
+    // With the grid sum asked for, the pairs' whole (cooperative) grid sums
+    // the slices after a grid-wide barrier (no reduction launch); not in the
+    // tensor-memory form.
+    t.gridsum = t.cluster_mode == 4 && t.split_tiles > 0 && !t.cluster && c.split != kSplitTmemA;
+    t.sem_bytes = t.gridsum ? 2 * sizeof(int) : 0;
     t.partial_bytes = t.split_tiles && !t.cluster ? size_t(2) * t.split_tiles * t.splits * kBM * c.bn * sizeof(float)
                                                  : 0;
 }
@@ -352,6 +356,7 @@ void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_req
     const bool fixup_fits = kTc[t.config_id].fixup_ok && t.split_tiles > 0 && t.splits <= 8 &&
                             t.split_tiles * t.splits <= sms && !t.cluster;
     if (fixup_fits && t.cluster_mode == 3) t.fixup = 1;
+    t.gridsum = 0;  // CTA pairs only
     t.sem_bytes = t.fixup ? size_t(t.split_tiles) * 4 * sizeof(int) : 0;
     t.partial_bytes = t.split_tiles && !t.cluster ? size_t(t.split_tiles) * t.splits * kBM * c.bn * sizeof(float)
                                                   : 0;
@@ -450,6 +455,7 @@ TcArgs make_args(const TcPlanState& st, int64_t M, int64_t N, float* C, int64_t 
     a.group = st.tile_group > 0 ? st.tile_group : 8;
     a.cluster = st.cluster;
     a.fixup = st.fixup;
+    a.gridsum = st.gridsum;
     a.sem = st.sem;
     prepare_c_map(st, C, M, N, ldc);
     a.c_tma = st.c_tma;
@@ -505,7 +511,7 @@ cudaError_t main_and_reduce(const TcPlanState& st, const Route& r, const TcArgs&
     }
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[2], s);
-    if (st.split_tiles > 0 && a.cluster <= 1 && !a.fixup) e = kTc[r.id].reduce(st, a, s);
+    if (st.split_tiles > 0 && a.cluster <= 1 && !a.fixup && !a.gridsum) e = kTc[r.id].reduce(st, a, s);
     if (ev) cudaEventRecord(ev[3], s);
     return e;
 }

@@ -259,6 +259,55 @@ __device__ bool pair_cluster_sum(const TcArgs& args, const CUtensorMap* tm_c, in
     return true;
 }
 
+// The split pair tiles' K-slices summed in slice order into C, float4 by
+// float4: indices idx0, idx0 + step, ... of 2 x split_pairs dense 128 x BN
+// partial tiles (slice z of the half h of split pair tile q at slot
+// (2q + h) x splits + z).  COHERENT: the slices were written by other CTAs of
+// the running kernel (loads through L2 only).
+template <int BN, bool COHERENT>
+__device__ __forceinline__ void pair_reduce_range(const float4* __restrict__ partial, int dp_pairs, int split_pairs,
+                                                  int splits, int tiles_m, int tiles_n, int group, int64_t M,
+                                                  int64_t N, float* __restrict__ C, int64_t ldc, int64_t idx0,
+                                                  int64_t step)
+{
+    constexpr int Q = BN / 4;
+    constexpr int PER_TILE = kBM * Q;
+    const bool vec = ((ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
+    const int64_t total = (int64_t)2 * split_pairs * PER_TILE;
+    for (int64_t idx = idx0; idx < total; idx += step) {
+        const int j = (int)(idx / PER_TILE);
+        const int rem = (int)(idx % PER_TILE);
+        const int r = rem / Q, c = (rem % Q) * 4;
+        int ptm, tn;
+        tile_coords(dp_pairs + j / 2, tiles_m / 2, tiles_n, group, ptm, tn);
+        const int64_t grow = ((int64_t)2 * ptm + (j & 1)) * kBM + r, gcol = (int64_t)tn * BN + c;
+        if (grow >= M || gcol >= N) continue;
+        const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
+        const float4 acc = sum_slices<PER_TILE, COHERENT>(p, splits);
+        float* dst = C + grow * ldc + gcol;
+        if (vec && gcol + 3 < N) {
+            *reinterpret_cast<float4*>(dst) = acc;
+        } else {
+            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int q = 0; q < 4 && gcol + q < N; ++q) dst[q] = v[q];
+        }
+    }
+}
+
+// The grid sum of a pair kernel, out of line so that its registers do not
+// weigh on the kernel's main loop: the grid-wide barrier, then this CTA's
+// share of the slices' sums.
+template <int BN>
+__device__ __noinline__ void pair_grid_sum(const TcArgs& args, volatile int* ok_word)
+{
+    ptx::fence_proxy_async_global();
+    if (grid_barrier(reinterpret_cast<unsigned*>(args.sem), args.timeout, args.status, ok_word))
+        pair_reduce_range<BN, true>(reinterpret_cast<const float4*>(args.partial), args.dp_tiles, args.split_tiles,
+                                    args.splits, args.tiles_m, args.tiles_n, args.group, args.M, args.N, args.C,
+                                    args.ldc, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                                    (int64_t)gridDim.x * blockDim.x);
+}
+
 // MODE kPairPreB: B comes split and transposed by the pre-pass (hi and lo,
 // K-major, by TMA through tm_bhi / tm_blo: this CTA's half of the tile's
 // columns) and the converters only add lo_A; kPairPreAB: lo_A comes from the
@@ -615,6 +664,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         ptx::tc_fence_after();
         ptx::tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
     }
+    // Every unit of the grid stored (the epilogues waited for their bulk
+    // stores): the split tiles' slices summed by the whole grid, in the
+    // reduction kernel's order.  The idle ring holds the barrier's word.
+    if (args.gridsum) pair_grid_sum<BN>(args, reinterpret_cast<volatile int*>(ring_ptr));
 }
 
 // ---------------------------------------------------------------------------
@@ -1025,29 +1078,8 @@ pair_reduce_kernel(const float4* __restrict__ partial, int dp_pairs, int split_p
 {
     pdl_trigger();
     pdl_wait();
-    constexpr int Q = BN / 4;
-    constexpr int PER_TILE = kBM * Q;
-    const bool vec = ((ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0);
-    const int64_t total = (int64_t)2 * split_pairs * PER_TILE;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int j = (int)(idx / PER_TILE);
-        const int rem = (int)(idx % PER_TILE);
-        const int r = rem / Q, c = (rem % Q) * 4;
-        int ptm, tn;
-        tile_coords(dp_pairs + j / 2, tiles_m / 2, tiles_n, group, ptm, tn);
-        const int64_t grow = ((int64_t)2 * ptm + (j & 1)) * kBM + r, gcol = (int64_t)tn * BN + c;
-        if (grow >= M || gcol >= N) continue;
-        const float4* p = partial + ((int64_t)j * splits * kBM + r) * Q + c / 4;
-        const float4 acc = sum_slices<PER_TILE>(p, splits);
-        float* dst = C + grow * ldc + gcol;
-        if (vec && gcol + 3 < N) {
-            *reinterpret_cast<float4*>(dst) = acc;
-        } else {
-            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-            for (int q = 0; q < 4 && gcol + q < N; ++q) dst[q] = v[q];
-        }
-    }
+    pair_reduce_range<BN, false>(partial, dp_pairs, split_pairs, splits, tiles_m, tiles_n, group, M, N, C, ldc,
+                                 (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
 }
 
 template <int BN, int SLOTS, int KB, int MODE>
@@ -1065,10 +1097,11 @@ cudaError_t launch_pair(const TcPlanState& st, const TcArgs& a, const CUtensorMa
     if (a.cluster > 1 && (a.dp_tiles != 0 || a.splits != a.cluster ||
                           PairSum<BN>::ring_bytes(a.cluster) > L::RING_BYTES))
         return cudaErrorInvalidValue;
-    return launch_pdl(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s, a.cluster > 1 ? 2 * a.cluster : 2,
-                      ta, tb, tbhi, tblo, talo,
-                      *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
-                      *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
+    // the grid sum's barrier needs every CTA resident at once
+    return launch_pdl_ex(kern, dim3(2 * pairs), dim3(kPairThreads), L::SMEM_BYTES, s,
+                         a.cluster > 1 ? 2 * a.cluster : 2, a.gridsum != 0, ta, tb, tbhi, tblo, talo,
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_c),
+                         *reinterpret_cast<const CUtensorMap*>(st.tmap_p), a);
 }
 
 template <int BN, int SLOTS, int KB>

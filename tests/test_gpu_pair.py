@@ -305,6 +305,67 @@ def test_pair_raw_a_withheld_stage_times_out_and_context_survives():
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
 
 
+GRIDSUM_CASES = [
+    # (M, N, K, operand_split, split_k, tile_n): the grid's own slice sum
+    (1024, 1024, 1024, 2, 4, 256),    # every pair tile in 4 slices, one unit per pair
+    (4096, 4096, 256, 4, 0, 256),     # raw A: whole tiles, then the last wave's split tiles
+    (300, 521, 264, 3, 2, 256),       # hybrid, ragged: the second tile row past M
+    (640, 768, 1000, 2, 3, 128),      # K not a multiple of 32, 256x128 pair tiles
+    (2560, 4096, 320, 4, 0, 256),     # several units per pair, the last wave split
+]
+GRIDSUM_IDS = [f"{m}x{n}x{k}_os{o}_s{s}_n{t}" for m, n, k, o, s, t in GRIDSUM_CASES]
+
+
+@pytest.mark.parametrize("case", GRIDSUM_CASES, ids=GRIDSUM_IDS)
+def test_pair_grid_sum_matches_the_reduction_kernel_bit_for_bit(case):
+    # The grid sums the slices after a grid-wide barrier, in the reduction
+    # kernel's order: the same bits as the reduction launch, within the bound,
+    # and the same bits on a second run (the barrier resets itself).
+    M, N, K, split, sk, tn = case
+    A = inputs.uniform_pm1(2141, M, K)
+    B = inputs.normal(2142, K, N)
+    opts = dict(PAIR, tile_n=tn, split_k=sk, operand_split=split)
+    C, desc, canaries, outs = run_gemm(A, B, repeat=2, split_reduce=4, **opts)
+    assert "grid-sum" in desc, desc
+    Cr, desc_r, canaries_r, _ = run_gemm(A, B, split_reduce=1, **opts)
+    assert "grid-sum" not in desc_r
+    assert canaries and canaries_r
+    assert np.array_equal(outs[0], outs[1]), desc
+    assert np.array_equal(C, Cr), desc
+    err, ok = check_against_oracle(C, A, B)
+    assert ok, f"{desc}: {err}"
+
+
+def test_pair_grid_sum_refusals_and_withheld_stage():
+    import torch
+    # one-CTA tiles and the tensor-memory form have no grid sum
+    for kw in (dict(tile_m=128, operand_split=2), dict(tile_m=256, tile_n=256, operand_split=5)):
+        with pytest.raises(g.GemmError):
+            g.Plan(1024, 1024, 1024, variant=g.VARIANT_TCGEN05, split_k=4, split_reduce=4, **kw)
+    M, N, K = 512, 512, 512
+    A = inputs.uniform_pm1(2143, M, K)
+    B = inputs.uniform_pm1(2144, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    opts = dict(PAIR, tile_n=256, split_k=2, split_reduce=4)
+    for split in (2, 4):
+        for withhold in (1, 3):
+            with g.Plan(M, N, K, wait_timeout_cycles=1 << 22, debug_withhold_stage=withhold, operand_split=split,
+                        **opts) as p:
+                assert "grid-sum" in p.describe()
+                p.run(dA, dB, dC)
+                # the stalled pair gives up and still meets the grid barrier
+                assert p.check() == g.ERR_TIMEOUT
+        torch.cuda.synchronize()
+        dC.fill_(float("nan"))
+        with g.Plan(M, N, K, operand_split=split, **opts) as p:
+            for _ in range(2):
+                p.run(dA, dB, dC)
+                assert p.check() == g.OK
+        Cref, S = oracle.gemm_f64(A, B)
+        assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
+
+
 def test_pair_launch_count_and_host_run():
     import torch
     M, N, K = 1024, 1024, 1024
