@@ -607,7 +607,8 @@ def run_gpu_arm(args):
                     raise g.GemmError(s, "gemm_f32_run_host")
         for w in work:
             w["plan"].trace_enable(0)
-        e2e_step()
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
         n_e2e = max(10, args.steps // 5)
         if dist:
             dist.barrier()
@@ -616,13 +617,16 @@ def run_gpu_arm(args):
             t0 = time.perf_counter()
             e2e_step()  # synchronous: the call copies C back and synchronises
             calls.append(time.perf_counter() - t0)
-        dt = max_over_ranks(sum(calls) / n_e2e, dist, "cuda")
+        # The median call: a host-side stall of one call (seen once at 39 ms
+        # against 5.5 ms for the others) does not stand for the pipeline; the
+        # mean is reported beside it.
+        dt = max_over_ranks(statistics.median(calls), dist, "cuda")
         e2e = {"value": round(whole_job_rate(flops_step, world, dt), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(sum(4 * (w["M"] * w["K"] + w["K"] * w["N"]) for w in work)),
                "d2h_bytes_per_step": int(sum(4 * w["M"] * w["N"] for w in work)),
-               "ms_per_step": round(dt * 1e3, 3), "steps": n_e2e,
+               "ms_per_step": round(dt * 1e3, 3), "statistic": f"median of {n_e2e} calls", "steps": n_e2e,
                "ms_min": round(min(calls) * 1e3, 3), "ms_median": round(statistics.median(calls) * 1e3, 3),
-               "ms_max": round(max(calls) * 1e3, 3),
+               "ms_mean": round(sum(calls) / n_e2e * 1e3, 3), "ms_max": round(max(calls) * 1e3, 3),
                "call": "gemm_f32_run_host (pinned host A, B, C; copies and sync inside the call)"}
         del hbufs
 
