@@ -128,7 +128,7 @@ gemm_f32_status validate_opts(const gemm_f32_opts& o)
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
     if (o.wait_timeout_cycles < 0 || o.debug_withhold_stage < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.separate_syncs != 0 && o.separate_syncs != 1) return GEMM_F32_ERR_INVALID_ARG;
-    if (o.operand_split < 0 || o.operand_split > 6) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.operand_split < 0 || o.operand_split > 5) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_group < 0 || o.tile_group > 64) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_k < 0) return GEMM_F32_ERR_INVALID_ARG;
     if (o.host_panels < 0 || o.host_panels > 64) return GEMM_F32_ERR_INVALID_ARG;
@@ -285,8 +285,6 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
     }
 
     size_t status_off = 0, part_off = 0, ahi_off = 0, alo_off = 0, bhi_off = 0, blo_off = 0, sem_off = 0;
-    size_t odl_off = 0, odr_off = 0;
-    std::vector<int2> od_pieces;  // the split-on-demand list, copied to the plan's scratch
     size_t bytes = align256(sizeof(int));
     status_off = 0;
 
@@ -350,12 +348,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
             // across both), operands split in the kernel only.
             // operand_split 3 (B by the pre-pass) asks for the pairs' hybrid form,
             // 4 (lo of A and B by the pre-pass) for their form without converters,
-            // 5 for their form with A in tensor memory, 6 for the form without
-            // converters whose idle warps split the pieces on demand
+            // 5 for their form with A in tensor memory
             bool pair = c.tile_m == 256;
-            bool on_demand = o.operand_split == 6 || (!o.operand_split && c.fused == kSplitRawAOnDemand);
             const int pair_split = o.operand_split == 5   ? kSplitTmemA
-                                   : o.operand_split == 4 || o.operand_split == 6 || on_demand ? kSplitRawA
+                                   : o.operand_split == 4 ? kSplitRawA
                                    : o.operand_split == 3 ? kSplitHybrid
                                    : o.operand_split      ? kSplitInKernel
                                    : (c.fused == kSplitHybrid || c.fused == kSplitRawA || c.fused == kSplitTmemA)
@@ -411,19 +407,6 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 delete p;
                 return GEMM_F32_ERR_UNSUPPORTED;
             }
-            // split on demand: raw-A pairs with 256-wide tiles of 32-k stages
-            if (on_demand) {
-                const TcConfig& oc = tc_config(t.config_id);
-                if (!pair || oc.split != kSplitRawA || oc.bn != 256 || oc.bk != 32) {
-                    if (o.operand_split == 6) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
-                    on_demand = false;
-                } else {
-                    tc_od_pieces(t, od_pieces);
-                    t.od = 1;
-                    t.od_pieces = (int)od_pieces.size();
-                    t.od_ready_bytes = (size_t((t.od_a_panels + t.od_b_panels)) * t.od_slabs + 1) * sizeof(int);
-                }
-            }
             if (pair) {
                 // a run with operands the TMA cannot take falls back to the
                 // one-CTA pre-pass form: the partial buffer holds either's slices
@@ -444,21 +427,15 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
                 sem_off = bytes;
                 bytes += align256(t.sem_bytes);
             }
-            if (t.od) {
-                odl_off = bytes;
-                bytes += align256(size_t(t.od_pieces) * sizeof(int2));
-                odr_off = bytes;
-                bytes += align256(t.od_ready_bytes);
-            }
             if (pair)
                 snprintf(p->desc, sizeof p->desc,
                          "tcgen05 3xtf32 %s cta-pair terms=%d tile=%dx%dx%d stages=%d pairs=%d "
-                         "whole=%d split=%dx%d%s%s resident=%d group=%d kp=%lld",
+                         "whole=%d split=%dx%d%s resident=%d group=%d kp=%lld",
                          tcfg.split == kSplitHybrid ? "hybrid-split"
                          : tcfg.split == kSplitRawA ? "raw-a-split"
                          : tcfg.split == kSplitTmemA ? "tmem-a-split" : "in-kernel-split", t.terms, tcfg.bm, tcfg.bn, tcfg.bk, tcfg.stages, t.tiles_m / 2 * t.tiles_n, t.dp_tiles,
                          t.split_tiles, t.splits, t.cluster ? " cluster-sum" : t.gridsum ? " grid-sum" : "",
-                         t.od ? " split-on-demand" : "", t.pair_slots,
+                         t.pair_slots,
                          t.tile_group > 0 ? t.tile_group : 8,
                          (long long)t.kp);
             else
@@ -497,12 +474,6 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         if (t.sem_bytes) {
             t.sem = reinterpret_cast<int*>(base + sem_off);
             if (e == cudaSuccess) e = cudaMemset(t.sem, 0, t.sem_bytes);
-        }
-        if (t.od) {
-            t.od_list = reinterpret_cast<int2*>(base + odl_off);
-            t.od_ready = reinterpret_cast<int*>(base + odr_off);
-            if (e == cudaSuccess && t.od_pieces)
-                e = cudaMemcpy(t.od_list, od_pieces.data(), od_pieces.size() * sizeof(int2), cudaMemcpyHostToDevice);
         }
         if (e == cudaSuccess) e = tc_prepare(t, M, N, K);
     }

@@ -1,6 +1,5 @@
 // Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
-#include <vector>
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
@@ -76,8 +75,7 @@ enum : int {
     kSplitInKernel = 1,  // raw A and B by TMA, split by converter warps
     kSplitHybrid = 2,    // raw A split in the kernel, B split by the pre-pass
     kSplitRawA = 3,      // hi of A read from A (truncated by the MMA); the pre-pass writes lo of A, hi/lo of B
-    kSplitTmemA = 4,     // CTA pairs only: A split by the kernel's loader warps into tensor memory, B by the pre-pass
-    kSplitRawAOnDemand = 5  // dispatch only: the raw-A pair kernel (kSplitRawA) splitting its pieces on demand
+    kSplitTmemA = 4      // CTA pairs only: A split by the kernel's loader warps into tensor memory, B by the pre-pass
 };
 int tc_num_configs();
 const TcConfig& tc_config(int id);
@@ -137,18 +135,6 @@ struct TcPlanState {
     int* sem = nullptr;        // fixup arrival counters or the grid barrier's count and
                                // generation (zero between runs), sem_bytes long
     size_t sem_bytes = 0;
-    // Split on demand (raw-A CTA pairs, 256-wide tiles, device runs): the main
-    // kernel's converter warps make lo of A and hi/lo of B themselves, in the
-    // order of od_list; od_ready holds a flag per (panel, 32-k slab) and the
-    // list's queue counter (zeroed before every run).  od_pieces == 0: the
-    // pre-pass makes them.
-    int od = 0;                // split on demand (od_pieces may be 0: the first wave is all)
-    int od_pieces = 0;
-    int od_a_panels = 0, od_b_panels = 0, od_slabs = 0;
-    int od_a_first = 0, od_b_first = 0;  // the first wave's panels, made by the pre-pass
-    int2* od_list = nullptr;
-    int* od_ready = nullptr;
-    size_t od_ready_bytes = 0;
     // In-kernel and hybrid split plans: the pre-split configuration of the same
     // tile width, used when a base pointer of A or B is not 16-byte aligned;
     // tensor maps over the caller's raw A and B, re-encoded when they change.
@@ -166,10 +152,6 @@ struct TcPlanState {
     mutable float* c_ptr = nullptr;
     mutable int c_tma = 0;
 };
-// Split on demand: the pieces of the operand split (32-k slabs of 128-row
-// panels of A and 128-column panels of B), in the order the plan's tile
-// schedule first needs them.  Sets od_a_panels, od_b_panels, od_slabs.
-void tc_od_pieces(TcPlanState& t, std::vector<int2>& out);
 // Work decomposition for config t.config_id: split_request 0 = automatic
 // (split the tiles of a partial last wave), 1 = none, >= 2 = every tile in that
 // many K-slices.  Sets kp, tiles, dp/split tiles, splits and partial_bytes.

@@ -174,16 +174,6 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 
 // Order this thread's async-proxy (TMA) global accesses against its generic
 // ones, both ways.
-// Load with acquire semantics at GPU scope (a flag another CTA releases).
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-// Store with release semantics at GPU scope.
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;\n" :: "l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;\n" ::: "memory");
 }

@@ -46,26 +46,6 @@ struct TcArgs {
     int gridsum;         // 1: CTA pairs, cooperative grid: once every CTA has stored its
                          // units, a grid-wide barrier (sem[0] count, sem[1] generation),
                          // then every CTA sums a share of the split tiles' slices
-    // Split on demand (CTA pairs, every piece but hi of A split, 256-wide tiles):
-    // the kernel's otherwise idle converter warps make lo of A and hi/lo of B
-    // themselves, piece by piece in the order the tile schedule needs them,
-    // and the producers wait for each piece's ready flag before its copies.
-    // A piece is one 32-k slab of one 128-row panel of A or of one 128-column
-    // panel of B; od_pieces lists them (x: bit 31 set for B, panel below;
-    // y: slab), od_ready holds a flag per (panel, slab) (A panels first),
-    // od_queue the next piece to take.  od_pieces == 0: the pre-pass made them.
-    int od_pieces;
-    int od_a_panels, od_slabs;
-    const int2* od_list;
-    int* od_ready;
-    int* od_queue;
-    const float* od_A;   // the caller's A and B
-    const float* od_B;
-    int64_t od_lda, od_ldb, od_K, od_kp;
-    float* od_a_lo;      // the split operands (kp-long rows)
-    float* od_b_hi;
-    float* od_b_lo;
-    int od_vec_b;        // B's rows 16-byte aligned
 };
 
 // One unit of work of the persistent kernel: a whole tile, or one K-slice of a
@@ -203,12 +183,12 @@ __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity
 
 // Tile order: groups of G tile-rows, column-major inside a group, so the CTAs
 // running together share A and B panels in L2.
-__host__ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int G, int& tm, int& tn)
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int G, int& tm, int& tn)
 {
     const int group_size = G * tiles_n;
     const int gid = tile / group_size;
     const int first_m = gid * G;
-    const int gsz = tiles_m - first_m < G ? tiles_m - first_m : G;
+    const int gsz = min(tiles_m - first_m, G);
     const int r = tile % group_size;
     tm = first_m + r % gsz;
     tn = r / gsz;

@@ -362,78 +362,6 @@ void tc_configure(TcPlanState& t, int64_t M, int64_t N, int64_t K, int split_req
                                                   : 0;
 }
 
-void tc_od_pieces(TcPlanState& t, std::vector<int2>& out)
-{
-    const TcConfig& c = kTc[t.config_id].cfg;
-    const int slabs = (int)(t.kp / kBK);
-    const int a_panels = t.tiles_m;                  // 128-row panels (whole pairs)
-    const int b_panels = (int)((t.tiles_n * (int64_t)c.bn + 127) / 128);
-    t.od_a_panels = a_panels;
-    t.od_b_panels = b_panels;
-    t.od_slabs = slabs;
-    // When each piece is first needed: the wave of the first unit that reads
-    // it, then the unit's k-block (the pairs take units pair, pair + P, ...
-    // and run through each unit's k-blocks in order).
-    const int P = t.pair_slots;
-    const int num_work = t.dp_tiles + t.split_tiles * t.splits;
-    const int pairs = num_work < P ? num_work : P;
-    const int group = t.tile_group > 0 ? t.tile_group : 8;
-    const int64_t never = INT64_MAX;
-    std::vector<int64_t> need_a((size_t)a_panels * slabs, never), need_b((size_t)b_panels * slabs, never);
-    for (int w = 0; w < num_work; ++w) {
-        int tile, kb0, kb1;
-        if (w < t.dp_tiles) {
-            tile = w; kb0 = 0; kb1 = slabs;
-        } else {
-            const int u = w - t.dp_tiles, z = u % t.splits;
-            tile = t.dp_tiles + u / t.splits;
-            kb0 = z * t.kb_per_split;
-            kb1 = kb0 + t.kb_per_split < slabs ? kb0 + t.kb_per_split : slabs;
-        }
-        int ptm, tn;
-        tile_coords(tile, t.tiles_m / 2, t.tiles_n, group, ptm, tn);
-        const int64_t wave = w / pairs;
-        for (int kb = kb0; kb < kb1; ++kb) {
-            const int64_t key = wave * slabs + (kb - kb0);
-            for (int h = 0; h < 2; ++h) {
-                int64_t& ka = need_a[(size_t)(2 * ptm + h) * slabs + kb];
-                if (key < ka) ka = key;
-                const int bp = (int)((tn * (int64_t)c.bn + h * (c.bn / 2)) / 128);
-                int64_t& kbb = need_b[(size_t)bp * slabs + kb];
-                if (key < kbb) kbb = key;
-            }
-        }
-    }
-    // The first wave's panels are made by the pre-pass (the kernel's own warps
-    // could not keep up with a whole wave starting at once): the A panels
-    // below od_a_first and the B panels below od_b_first, contiguous from 0 in
-    // the raster order.
-    int a_first = 0, b_first = 0;
-    for (int pnl = 0; pnl < a_panels; ++pnl)
-        for (int sl = 0; sl < slabs; ++sl)
-            if (need_a[(size_t)pnl * slabs + sl] < slabs && pnl + 1 > a_first) a_first = pnl + 1;
-    for (int pnl = 0; pnl < b_panels; ++pnl)
-        for (int sl = 0; sl < slabs; ++sl)
-            if (need_b[(size_t)pnl * slabs + sl] < slabs && pnl + 1 > b_first) b_first = pnl + 1;
-    t.od_a_first = a_first;
-    t.od_b_first = b_first;
-    struct Item { int64_t key; int2 pc; };
-    std::vector<Item> items;
-    items.reserve(need_a.size() + need_b.size());
-    for (int pnl = a_first; pnl < a_panels; ++pnl)
-        for (int sl = 0; sl < slabs; ++sl)
-            if (need_a[(size_t)pnl * slabs + sl] != never)
-                items.push_back({need_a[(size_t)pnl * slabs + sl], make_int2(pnl, sl)});
-    for (int pnl = b_first; pnl < b_panels; ++pnl)
-        for (int sl = 0; sl < slabs; ++sl)
-            if (need_b[(size_t)pnl * slabs + sl] != never)
-                items.push_back({need_b[(size_t)pnl * slabs + sl], make_int2((int)(0x80000000u | (unsigned)pnl), sl)});
-    std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) { return x.key < y.key; });
-    out.clear();
-    out.reserve(items.size());
-    for (const Item& it : items) out.push_back(it.pc);
-}
-
 cudaError_t tc_set_partial(TcPlanState& st, float* partial)
 {
     st.partial = partial;
@@ -473,7 +401,6 @@ struct Route {
     bool pre_b;      // the pre-pass splits B
     bool tmem_a;     // A read from A by the kernel's loader warps into tensor memory
     bool pair;       // a CTA-pair plan whose kernel can take these operands
-    bool on_demand;  // raw-A pairs whose kernel splits lo of A and B itself
 };
 
 Route route(const TcPlanState& st, const float* A, const float* B)
@@ -491,9 +418,6 @@ Route route(const TcPlanState& st, const float* A, const float* B)
     // a misaligned base pointer: the pre-pass form of the same tile width
     if (!r.in_kernel && !r.raw_a && !r.tmem_a && c.split != kSplitPrepass) r.id = st.fallback_config_id;
     r.pair = c.bm == 2 * kBM && (r.in_kernel || r.raw_a || r.tmem_a);
-    // split on demand: the main kernel makes every split piece itself
-    r.on_demand = r.pair && r.raw_a && st.od;
-    if (r.on_demand) r.pre_a = r.pre_b = false;
     return r;
 }
 
@@ -541,24 +465,16 @@ TcArgs make_args(const TcPlanState& st, int64_t M, int64_t N, float* C, int64_t 
 // The operand pre-pass: the A part (rows of this state, only lo with raw_a)
 // and/or the B part, one launch.
 cudaError_t prepass(const TcPlanState& st, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                    const float* B, int64_t ldb, bool do_a, bool a_lo_only, bool do_b, cudaStream_t s,
-                    bool od_init = false)
+                    const float* B, int64_t ldb, bool do_a, bool a_lo_only, bool do_b, cudaStream_t s)
 {
     const int vec_a = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
     const int vec_b = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
     const int a_blocks = do_a ? grid_cap(M * (st.kp / 4), st.num_sms) : 0;
     const int64_t b_blocks = do_b ? (st.kp / kSplitBK) * ((N + kSplitBN - 1) / kSplitBN) : 0;
-    // split on demand: the first wave's panels here, their flags set, the rest cleared
-    const int64_t nflags = od_init ? (int64_t)(st.od_a_panels + st.od_b_panels) * st.od_slabs : 0;
-    const int64_t a_made = od_init ? (int64_t)st.od_a_first * st.od_slabs : 0;
-    const int64_t b_first = od_init ? (int64_t)st.od_a_panels * st.od_slabs : 0;
-    const int64_t b_end = od_init ? b_first + (int64_t)st.od_b_first * st.od_slabs : 0;
-    if (a_blocks + b_blocks == 0 && !od_init) return cudaSuccess;
-    const int64_t blocks = a_blocks + b_blocks > 0 ? a_blocks + b_blocks : 1;
-    split_operands_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+    if (a_blocks + b_blocks == 0) return cudaSuccess;
+    split_operands_kernel<<<(unsigned)(a_blocks + b_blocks), 256, 0, s>>>(
         A, M, K, lda, vec_a, B, N, ldb, vec_b, st.kp, reinterpret_cast<float4*>(st.a_hi),
-        reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks, a_lo_only ? 1 : 0,
-        od_init ? st.od_ready : nullptr, nflags, a_made, b_first, b_end);
+        reinterpret_cast<float4*>(st.a_lo), st.b_hi, st.b_lo, a_blocks, a_lo_only ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -635,38 +551,10 @@ cudaError_t tc_launch(const TcPlanState& st, int64_t M, int64_t N, int64_t K, co
         st.raw_b = B;
     }
     // 1. The pre-pass into the plan's scratch (what the route needs of it).
-    // Split on demand: the first wave's panels (rows below od_a_first x 128,
-    // columns below od_b_first x 128) by the pre-pass, which also sets their
-    // flags and clears the others; the main kernel makes the rest.
-    if (r.on_demand)
-        e = prepass(st, std::min<int64_t>(M, (int64_t)st.od_a_first * kBM), std::min<int64_t>(N, (int64_t)st.od_b_first * 128),
-                    K, A, lda, B, ldb, st.od_a_first > 0, true, st.od_b_first > 0, s, true);
-    else
-        e = prepass(st, M, N, K, A, lda, B, ldb, r.pre_a, r.raw_a, r.pre_b, s);
-    if (e != cudaSuccess) return e;
-    TcArgs a = make_args(st, M, N, C, ldc, status);
-    if (r.on_demand) {
-        const int flags = (st.od_a_panels + st.od_b_panels) * st.od_slabs;
-        a.od_pieces = st.od_pieces;
-        a.od_a_panels = st.od_a_panels;
-        a.od_slabs = st.od_slabs;
-        a.od_list = st.od_list;
-        a.od_ready = st.od_ready;
-        a.od_queue = st.od_ready + flags;
-        a.od_A = A;
-        a.od_B = B;
-        a.od_lda = lda;
-        a.od_ldb = ldb;
-        a.od_K = K;
-        a.od_kp = st.kp;
-        a.od_a_lo = st.a_lo;
-        a.od_b_hi = st.b_hi;
-        a.od_b_lo = st.b_lo;
-        a.od_vec_b = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0);
-    }
+    if ((e = prepass(st, M, N, K, A, lda, B, ldb, r.pre_a, r.raw_a, r.pre_b, s)) != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[1], s);
     // 2. The pipelined tensor-core GEMM and 3. the split tiles' reduction.
-    return main_and_reduce(st, r, a, ev, s);
+    return main_and_reduce(st, r, make_args(st, M, N, C, ldc, status), ev, s);
 }
 
 cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, int64_t N, int64_t K,
@@ -677,8 +565,6 @@ cudaError_t tc_panel_prepare(const TcPlanState& full, int64_t r0, int64_t mp, in
     tc_configure(out, mp, N, K, full.split_request);
     out.partial = nullptr;
     out.sem = nullptr;
-    out.od = 0;
-    out.od_pieces = 0;
     out.c_ptr = nullptr;
     out.c_tma = 0;
     out.a_hi = full.a_hi + r0 * full.kp;
@@ -716,8 +602,7 @@ cudaError_t tc_split_b(const TcPlanState& full, int64_t N, int64_t K, const floa
                        int64_t ldb, cudaStream_t s)
 {
     const Route r = route(full, A, B);
-    // the panels of a split-on-demand plan read B split by the pre-pass
-    return r.pre_b || r.on_demand ? prepass(full, 0, N, K, A, 1, B, ldb, false, false, true, s) : cudaSuccess;
+    return r.pre_b ? prepass(full, 0, N, K, A, 1, B, ldb, false, false, true, s) : cudaSuccess;
 }
 
 cudaError_t tc_panel_run(const TcPlanState& panel, int64_t mp, int64_t N, int64_t K, const float* A_panel,

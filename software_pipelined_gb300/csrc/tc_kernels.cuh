@@ -69,22 +69,12 @@ constexpr int kSplitBN = 128;   // n columns per B tile
 // (K x N, ldb), stage it in shared memory and write it transposed to b_hi,
 // b_lo (N x kp): reads are coalesced along n, writes along k.  The last thing
 // each block does is allow the dependent GEMM launch to start its prologue.
-// With od_flags (a CTA-pair plan that splits the rest of its pieces on
-// demand): the pieces this launch makes (the first wave's panels) are marked
-// made, every other flag and the list's queue counter (at od_nflags) cleared.
 __global__ void __launch_bounds__(256)
 split_operands_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t lda, int vec_a,
                       const float* __restrict__ B, int64_t N, int64_t ldb, int vec_b, int64_t kp,
                       float4* __restrict__ a_hi, float4* __restrict__ a_lo,
-                      float* __restrict__ b_hi, float* __restrict__ b_lo, int a_blocks, int a_lo_only,
-                      int* __restrict__ od_flags, int64_t od_nflags, int64_t od_a_made, int64_t od_b_first,
-                      int64_t od_b_end)
+                      float* __restrict__ b_hi, float* __restrict__ b_lo, int a_blocks, int a_lo_only)
 {
-    if (od_flags) {
-        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= od_nflags;
-             i += (int64_t)gridDim.x * blockDim.x)
-            od_flags[i] = i < od_nflags && (i < od_a_made || (i >= od_b_first && i < od_b_end)) ? 1 : 0;
-    }
     if ((int)blockIdx.x < a_blocks) {
         const int64_t kp4 = kp / 4;
         const int64_t total = M * kp4;

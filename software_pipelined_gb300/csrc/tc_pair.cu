@@ -294,87 +294,6 @@ __device__ __forceinline__ void pair_reduce_range(const float4* __restrict__ par
     }
 }
 
-// Split on demand: one piece by one warp.  A piece of A is a 32-k slab of a
-// 128-row panel: lo = lo_part(a) of every element (hi of A is A itself), a
-// warp instruction covering 4 rows x 128 bytes, 8 float4 loads of each lane
-// in flight at once.  A piece of B is a 32-k slab of a 128-column panel,
-// written transposed (K-major): lane = k, hi and lo by split3, the stores of
-// a column coalesced along k.  Elements past M, N or K are not written (rows
-// and columns) or written as zeros (k up to the padded kp), as the pre-pass
-// writes them; the arithmetic is the pre-pass's, so the split operands are
-// the same bits.
-__device__ __noinline__ void od_split_piece(const TcArgs& a, int2 pc, int lane)
-{
-    const int panel = pc.x & 0x7FFFFFFF, slab = pc.y;
-    const int64_t k0 = (int64_t)slab * kBK;
-    if (!(pc.x & 0x80000000)) {
-        const int64_t r0 = (int64_t)panel * kBM;
-#pragma unroll 1
-        for (int i0 = 0; i0 < 32; i0 += 16) {
-            float4 v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int q = lane + 32 * (i0 + j);
-                const int64_t row = r0 + q / 8, k = k0 + (q % 8) * 4;
-                v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (row < a.M) {
-                    const float* src = a.od_A + row * a.od_lda + k;
-                    if (k + 3 < a.od_K) {
-                        v[j] = __ldg(reinterpret_cast<const float4*>(src));
-                    } else {
-                        float t[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int e = 0; e < 4; ++e)
-                            if (k + e < a.od_K) t[e] = __ldg(src + e);
-                        v[j] = make_float4(t[0], t[1], t[2], t[3]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int q = lane + 32 * (i0 + j);
-                const int64_t row = r0 + q / 8, k = k0 + (q % 8) * 4;
-                if (row < a.M)
-                    *reinterpret_cast<float4*>(a.od_a_lo + row * a.od_kp + k) =
-                        make_float4(lo_part(v[j].x), lo_part(v[j].y), lo_part(v[j].z), lo_part(v[j].w));
-            }
-        }
-    } else {
-        const int64_t n0 = (int64_t)panel * 128, k = k0 + lane;
-        const bool kin = k < a.od_K;
-        const float* row = a.od_B + (kin ? k : 0) * a.od_ldb;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int64_t n = n0 + c0 + 4 * j;
-                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kin && n < a.N) {
-                    if (a.od_vec_b && n + 3 < a.N) {
-                        t = __ldg(reinterpret_cast<const float4*>(row + n));
-                    } else {
-                        float u[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int e = 0; e < 4; ++e)
-                            if (n + e < a.N) u[e] = __ldg(row + n + e);
-                        t = make_float4(u[0], u[1], u[2], u[3]);
-                    }
-                }
-                v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int64_t n = n0 + c0 + j;
-                if (n < a.N) {
-                    float h, l;
-                    split3(v[j], h, l);
-                    a.od_b_hi[n * a.od_kp + k] = h;
-                    a.od_b_lo[n * a.od_kp + k] = l;
-                }
-            }
-        }
-    }
-}
-
 // The grid sum of a pair kernel, out of line so that its registers do not
 // weigh on the kernel's main loop: the grid-wide barrier, then this CTA's
 // share of the slices' sums.
@@ -496,7 +415,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             bool stop = false;
             for (int w = pair; w < num_work && !stop; w += npairs) {
                 const PairUnit pu = pair_unit(w, args, (int)rank);
-                int od_ready_to = pu.u.kb0;  // split on demand: slabs of this unit known made
                 for (int kh = pu.u.kb0 * HALVES; kh < pu.u.kb1 * HALVES; ++kh) {
                     const int s = fills % SLOTS;
                     const uint32_t ps = (fills / SLOTS) & 1u;
@@ -509,29 +427,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     const int kc = kh * KB;
                     const uint32_t slot = ring + s * L::SLOT_BYTES;
                     if constexpr (APRE) {
-                        if (args.od_pieces > 0 && kh / HALVES >= od_ready_to) {
-                            // split on demand: this CTA's pieces of the next slabs of the
-                            // unit (up to 2) are made: acquire their flags, then one fence
-                            // orders the copies of all of them after those loads
-                            const int slab0 = kh / HALVES;
-                            const int slab1 = min(slab0 + 2, pu.u.kb1);  // slabs are 32-k blocks
-                            const int bpanel = (pu.tn * BN + (int)rank * L::BH) / 128;
-                            const int* fa = args.od_ready + (int64_t)pu.tm * args.od_slabs;
-                            const int* fb = args.od_ready + ((int64_t)args.od_a_panels + bpanel) * args.od_slabs;
-                            const long long t0 = clock64();
-                            for (int sl = slab0; sl < slab1 && !stop; ++sl) {
-                                while (!ptx::ld_acquire_gpu(fa + sl) || !ptx::ld_acquire_gpu(fb + sl)) {
-                                    if (*abort_flag || clock64() - t0 > limit) {
-                                        if (!*abort_flag) atomicExch(args.status, kStatusTimeout);
-                                        stop = true;
-                                        break;
-                                    }
-                                }
-                            }
-                            if (stop) break;
-                            ptx::fence_proxy_async_global();
-                            od_ready_to = slab1;
-                        }
                         // raw A (= hi_A) and lo_A, this CTA's half of hi_B and lo_B;
                         // both CTAs' copies complete on the even CTA's barrier, which
                         // the even CTA's thread arms with the pair's bytes
@@ -677,27 +572,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         if (stop && lane == 0) give_up();
     } else if constexpr (APRE) {
-        // Split on demand: each converter warp takes the next piece of the
-        // list, makes it and releases its flag (every lane's stores ordered
-        // before it at GPU scope); the producers of both CTAs wait on the flags.
-        if (args.od_pieces > 0) {
-            pdl_wait();  // the previous kernel's writes (A, B, the split buffers' readers) are done
-            for (;;) {
-                int idx = 0;
-                if (lane == 0) idx = atomicAdd(args.od_queue, 1);
-                idx = __shfl_sync(0xffffffffu, idx, 0);
-                if (idx >= args.od_pieces || *abort_flag) break;
-                const int2 pc = args.od_list[idx];
-                od_split_piece(args, pc, lane);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) {
-                    const int64_t f = ((pc.x & 0x80000000) ? (int64_t)args.od_a_panels + (pc.x & 0x7FFFFFFF)
-                                                           : (int64_t)pc.x) * args.od_slabs + pc.y;
-                    ptx::st_release_gpu(args.od_ready + f, 1);
-                }
-            }
-        }
+        // nothing to convert: the converter warps idle
     } else {
         // ------------------------------ converters ----------------------------
         // Two groups of warps take alternate stages, so that one group's

@@ -366,73 +366,6 @@ def test_pair_grid_sum_refusals_and_withheld_stage():
         assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
 
 
-ONDEMAND_CASES = [
-    # (M, N, K, split_k, lda pad, ldb pad): split on demand against the pre-pass
-    (4096, 4096, 256, 0, 0, 0),      # several units per pair, the last wave split
-    (1024, 1024, 1024, 4, 0, 0),     # every tile in 4 slices: pieces needed from mid-K
-    (300, 520, 264, 2, 0, 0),        # ragged: rows past M, columns past N, K past its last slab
-    (640, 768, 1000, 3, 4, 1),       # padded lda, ldb off a 16-byte row (scalar B loads)
-    (2560, 4096, 320, 0, 0, 0),      # partial last wave, 3.x waves
-]
-ONDEMAND_IDS = [f"{m}x{n}x{k}_s{s}_pa{pa}_pb{pb}" for m, n, k, s, pa, pb in ONDEMAND_CASES]
-
-
-@pytest.mark.parametrize("case", ONDEMAND_CASES, ids=ONDEMAND_IDS)
-def test_pair_split_on_demand_bit_identical_to_the_pre_pass(case):
-    # The kernel's own warps make lo of A and hi/lo of B with the pre-pass's
-    # arithmetic, so the product is the same bits as with the pre-pass; twice
-    # (the flags start at zero every run), within the bound.
-    M, N, K, sk, pa, pb = case
-    A = inputs.uniform_pm1(2151, M, K)
-    B = inputs.normal(2152, K, N)
-    opts = dict(PAIR, tile_n=256, split_k=sk)
-    lds = dict(lda=K + pa if pa else None, ldb=N + pb if pb else None)
-    C, desc, canaries, outs = run_gemm(A, B, repeat=2, operand_split=6, **lds, **opts)
-    assert "raw-a-split" in desc and "split-on-demand" in desc, desc
-    Cp, desc_p, canaries_p, _ = run_gemm(A, B, operand_split=4, **lds, **opts)
-    assert "split-on-demand" not in desc_p
-    assert canaries and canaries_p
-    assert np.array_equal(outs[0], outs[1]), desc
-    assert np.array_equal(C, Cp), desc
-    err, ok = check_against_oracle(C, A, B)
-    assert ok, f"{desc}: {err}"
-
-
-def test_pair_split_on_demand_small_integers_refusals_and_withheld_stage():
-    import torch
-    M, N, K = 520, 300, 200
-    A = inputs.small_int(2153, M, K, -4, 4)
-    B = inputs.small_int(2154, K, N, -4, 4)
-    exact = A.astype(np.float64) @ B.astype(np.float64)
-    C, desc, canaries, _ = run_gemm(A, B, tile_n=256, split_k=2, operand_split=6, **PAIR)
-    assert "split-on-demand" in desc and canaries and np.array_equal(C, exact), desc
-    # A's base off a 16-byte boundary: the one-CTA pre-pass form
-    C, desc, canaries, _ = run_gemm(A, B, lda=K + 4, a_off=1, tile_n=256, split_k=2, operand_split=6, **PAIR)
-    assert canaries and np.array_equal(C, exact), desc
-    # 256-wide tiles of 32-k stages only
-    for kw in (dict(tile_n=128), dict(tile_n=256, tile_k=16), dict(tile_m=128, tile_n=256)):
-        with pytest.raises(g.GemmError):
-            g.Plan(512, 512, 512, **dict(PAIR, operand_split=6, **kw))
-    M, N, K = 512, 512, 512
-    A = inputs.uniform_pm1(2155, M, K)
-    B = inputs.uniform_pm1(2156, K, N)
-    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
-    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    opts = dict(PAIR, tile_n=256, split_k=2, operand_split=6)
-    for withhold in (1, 3):
-        with g.Plan(M, N, K, wait_timeout_cycles=1 << 22, debug_withhold_stage=withhold, **opts) as p:
-            p.run(dA, dB, dC)
-            assert p.check() == g.ERR_TIMEOUT
-    torch.cuda.synchronize()
-    dC.fill_(float("nan"))
-    with g.Plan(M, N, K, **opts) as p:
-        for _ in range(2):
-            p.run(dA, dB, dC)
-            assert p.check() == g.OK
-    Cref, S = oracle.gemm_f64(A, B)
-    assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
-
-
 def test_pair_launch_count_and_host_run():
     import torch
     M, N, K = 1024, 1024, 1024
@@ -506,7 +439,7 @@ def test_pair_cluster_sum_withheld_stage_times_out():
     assert oracle.within_bound(dC.cpu().numpy(), Cref, S, K)
 
 
-@pytest.mark.parametrize("mode", [2, 3, 4, 5, 6], ids=["in_kernel", "hybrid", "raw_a", "tmem_a", "on_demand"])
+@pytest.mark.parametrize("mode", [2, 3, 4, 5], ids=["in_kernel", "hybrid", "raw_a", "tmem_a"])
 def test_pair_run_host_blocks_ragged_with_splits(mode):
     # Ragged M and N (the last panel's second tile row and the last block's
     # columns past the edge), K-slices in every panel's last wave, padded C:
@@ -528,7 +461,7 @@ def test_pair_run_host_blocks_ragged_with_splits(mode):
             assert (C[:, N:] == 321.0).all()
 
 
-@pytest.mark.parametrize("mode", [2, 3, 4, 5, 6], ids=["in_kernel", "hybrid", "raw_a", "tmem_a", "on_demand"])
+@pytest.mark.parametrize("mode", [2, 3, 4, 5], ids=["in_kernel", "hybrid", "raw_a", "tmem_a"])
 @pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (3, 2), (2, 3)])
 def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels, cols):
     # Without a K-split every tile is summed in the same order whichever 256-row
