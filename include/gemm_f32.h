@@ -146,7 +146,8 @@ typedef struct {
                                pipelined over (A panel copies, panel GEMMs and C panel
                                copies overlap); 0 = the dispatcher's choice, 1 = none,
                                n = n panels of whole tiles (128 rows; 256 for CTA-pair plans;
-                               at most 64) */
+                               at most 64); with column blocks on a GEMM of 8 waves or more
+                               the first panel takes two shares of the tile rows */
     int32_t split_reduce;   /* TC only: how the K-slices of split tiles are summed.  0 = the
                                dispatcher's choice (1: measured fastest); 1 = a
                                reduction kernel over partial tiles in scratch; 3 = no extra
@@ -173,7 +174,7 @@ typedef struct {
                                its columns of B have landed (the GEMM starts after a fraction
                                of B instead of all of it).  0 = the dispatcher's choice, 1 =
                                none, at most 16; only for plans that split A inside the GEMM
-                               kernel or read hi of A from A (operand_split 2, 3 or 4),
+                               kernel or read hi of A from A (operand_split 2 to 5),
                                otherwise as 1 */
     int32_t simt_fragments;  /* SIMT only: how each thread's register fragments come from the
                                staged tiles.  0 = 16-byte shared-memory loads that lanes

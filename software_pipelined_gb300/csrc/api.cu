@@ -521,7 +521,9 @@ int host_col_request(const gemm_f32_plan_s* p)
     const TcConfig& c = tc_config(p->tc.config_id);
     if (c.split == kSplitPrepass) return 1;
     const int q = p->opts.host_col_blocks;
-    return q != 0 ? q : p->N >= 6144 ? 3 : p->N >= 2048 ? 2 : 1;
+    // 4 blocks from N = 6144 (8192^3 with its first panel of two shares: 4.38
+    // against 4.49 ms with 3), 2 from N = 2048
+    return q != 0 ? q : p->N >= 6144 ? 4 : p->N >= 2048 ? 2 : 1;
 }
 
 // Row panels of the pipelined host-buffer run: the option's count, else a
@@ -577,11 +579,26 @@ cudaError_t make_panels(gemm_f32_plan_s* p, int count, int64_t width)
 {
     if (!p->panels.empty() && p->panel_count == count && p->block_width == width) return cudaSuccess;
     drop_panels(p);
-    const int64_t rows = round_up((p->M + count - 1) / count, tc_config(p->tc.config_id).bm);
+    const int64_t bm = tc_config(p->tc.config_id).bm;
+    int64_t rows = round_up((p->M + count - 1) / count, bm);
+    // With column blocks on a GEMM of many waves (copies shorter than the
+    // GEMM), the first panel takes two shares of the tile rows: its blocks'
+    // GEMMs then last about as long as the copy of the next block of B, so
+    // the GEMM does not wait between them.
+    int64_t first = rows;
+    const int64_t waves = int64_t(p->tc.tiles_m) * p->tc.tiles_n / (p->num_sms > 0 ? p->num_sms : 1);
+    if (width > 0 && count > 2 && waves >= 8) {
+        const int64_t tile_rows = (p->M + bm - 1) / bm, share = tile_rows / (count + 1);
+        if (share >= 1) {
+            rows = share * bm;
+            first = (tile_rows - share * (count - 1)) * bm;
+        }
+    }
     size_t need = 0;
     cudaError_t e = cudaSuccess;
-    for (int64_t r0 = 0; r0 < p->M; r0 += rows) {
-        const int64_t mp = p->M - r0 < rows ? p->M - r0 : rows;
+    for (int64_t r0 = 0; r0 < p->M; r0 += r0 == 0 ? first : rows) {
+        const int64_t step = r0 == 0 ? first : rows;
+        const int64_t mp = p->M - r0 < step ? p->M - r0 : step;
         TcPlanState ps;
         if ((e = tc_panel_prepare(p->tc, r0, mp, p->N, p->K, p->hA, p->lda, p->hB, p->ldb, ps)) != cudaSuccess) {
             drop_panels(p);

@@ -461,6 +461,25 @@ def test_pair_run_host_blocks_ragged_with_splits(mode):
             assert (C[:, N:] == 321.0).all()
 
 
+def test_pair_run_host_first_panel_of_two_shares_bit_identical_to_device_run():
+    # A GEMM of many waves with column blocks: the first row panel takes two
+    # shares of the tile rows (8192 x 4096: 12 pair-rows, then 4 panels of 5).
+    # Without a K-split the panel pipeline reproduces the device run bit for bit.
+    import torch
+    M, N, K = 8192, 4096, 128
+    A = inputs.normal(2161, M, K)
+    B = inputs.normal(2162, K, N)
+    hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+    hC = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    opts = dict(PAIR, tile_n=256, split_k=1, operand_split=4)
+    with g.Plan(M, N, K, host_panels=5, host_col_blocks=3, **opts) as p:
+        for _ in range(2):
+            assert p.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), 0) == g.OK
+    C, desc, canaries, _ = run_gemm(A, B, host_panels=1, **opts)
+    assert canaries
+    assert np.array_equal(hC.numpy().astype(np.float64), C), desc
+
+
 @pytest.mark.parametrize("mode", [2, 3, 4, 5], ids=["in_kernel", "hybrid", "raw_a", "tmem_a"])
 @pytest.mark.parametrize("panels,cols", [(2, 1), (3, 1), (3, 2), (2, 3)])
 def test_pair_run_host_panels_bit_identical_to_device_run(mode, panels, cols):
