@@ -627,6 +627,7 @@ def run_gpu_arm(args):
                "ms_per_step": round(dt * 1e3, 3), "statistic": f"median of {n_e2e} calls", "steps": n_e2e,
                "ms_min": round(min(calls) * 1e3, 3), "ms_median": round(statistics.median(calls) * 1e3, 3),
                "ms_mean": round(sum(calls) / n_e2e * 1e3, 3), "ms_max": round(max(calls) * 1e3, 3),
+               "ms_calls": [round(c * 1e3, 2) for c in calls],
                "call": "gemm_f32_run_host (pinned host A, B, C; copies and sync inside the call)"}
         del hbufs
 
