@@ -27,6 +27,7 @@ there is no collective on the data path.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -613,10 +614,18 @@ def run_gpu_arm(args):
         if dist:
             dist.barrier()
         calls = []
-        for _ in range(n_e2e):
-            t0 = time.perf_counter()
-            e2e_step()  # synchronous: the call copies C back and synchronises
-            calls.append(time.perf_counter() - t0)
+        # the host-side timing runs with Python's cyclic garbage collector
+        # paused (as timeit does): a collection inside a call is host noise
+        gc_was = gc.isenabled()
+        gc.disable()
+        try:
+            for _ in range(n_e2e):
+                t0 = time.perf_counter()
+                e2e_step()  # synchronous: the call copies C back and synchronises
+                calls.append(time.perf_counter() - t0)
+        finally:
+            if gc_was:
+                gc.enable()
         # The median call: a host-side stall of one call (seen once at 39 ms
         # against 5.5 ms for the others) does not stand for the pipeline; the
         # mean is reported beside it.
