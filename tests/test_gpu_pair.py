@@ -462,11 +462,12 @@ def test_pair_run_host_blocks_ragged_with_splits(mode):
 
 
 def test_pair_run_host_first_panel_of_two_shares_bit_identical_to_device_run():
-    # A GEMM of many waves with column blocks: the first row panel takes two
-    # shares of the tile rows (8192 x 4096: 12 pair-rows, then 4 panels of 5).
-    # Without a K-split the panel pipeline reproduces the device run bit for bit.
+    # A GEMM of 8 waves or more with column blocks: the first row panel takes
+    # two shares of the tile rows (8192 x 8192: 12 pair-rows, then 4 panels of
+    # 5).  Without a K-split the panel pipeline reproduces the device run bit
+    # for bit.
     import torch
-    M, N, K = 8192, 4096, 128
+    M, N, K = 8192, 8192, 64
     A = inputs.normal(2161, M, K)
     B = inputs.normal(2162, K, N)
     hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
