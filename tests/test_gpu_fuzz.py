@@ -14,7 +14,7 @@ from gpu_util import check_against_oracle, run_gemm
 pytestmark = pytest.mark.gpu
 
 
-def _cases(n=48, seed=20261202):
+def _cases(n=96, seed=20261202):
     rng = np.random.default_rng(seed)
     forms = [
         dict(variant=g.VARIANT_SIMT),
@@ -27,6 +27,11 @@ def _cases(n=48, seed=20261202):
         dict(variant=g.VARIANT_TCGEN05, tile_m=256, tile_n=256, operand_split=4),
         dict(variant=g.VARIANT_TCGEN05, tile_m=256, tile_n=128, operand_split=4),
         dict(variant=g.VARIANT_AUTO),
+        # the other ways of summing K-slices, and A split into tensor memory
+        dict(variant=g.VARIANT_TCGEN05, tile_m=256, tile_n=256, operand_split=5),
+        dict(variant=g.VARIANT_TCGEN05, tile_m=256, tile_n=256, operand_split=4, split_reduce=4),
+        dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=128, operand_split=2, split_reduce=2),
+        dict(variant=g.VARIANT_TCGEN05, tile_m=128, tile_n=128, operand_split=1, split_reduce=3),
     ]
     out = []
     for i in range(n):
