@@ -30,9 +30,9 @@ constexpr int64_t kTcFusedMinK = 32;
 struct DispatchChoice {
     int variant;   // GEMM_F32_VARIANT_SIMT / _TCGEN05
     int tile_m, tile_n, stages, split_k;
-    int fused;     // TC: where the split happens (kSplitPrepass / kSplitInKernel / kSplitHybrid)
+    int fused;     // TC: where the split happens (kSplitPrepass .. kSplitTmemA)
     int group;     // TC: tile-rows per raster group (0 = default)
-    int tile_k;    // SIMT: K-tile depth (0 = compiled default)
+    int tile_k;    // SIMT: K-tile depth; TC: k per stage, 32 or 16 (0 = compiled default)
     int k_slices;  // SIMT: K-slice groups inside the CTA (0 = 1)
     int reduce;    // TC: how split tiles' K-slices are summed (the split_reduce option; 0 = kernel)
 };

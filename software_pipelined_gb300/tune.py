@@ -256,8 +256,9 @@ def write_inc(results, path):
         "// last-wave split, 1 = none, >= 2 = every tile in that many K-slices),",
         "// split (tcgen05: 0 pre-pass, 1 inside the kernel, 2 A inside and B by the pre-pass,",
         "// 3 hi of A read from A, 4 A split into tensor memory by the CTA pair),",
-        "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k and",
-        "// k_slices (SIMT: K-tile depth, K-slice groups inside the CTA).",
+        "// tile_group (tcgen05: tile-rows per raster group, 0 = default), tile_k (SIMT:",
+        "// K-tile depth; tcgen05: k per stage, 32 or 16; 0 = default), k_slices (SIMT:",
+        "// K-slice groups inside the CTA) and split_reduce (0 = the reduction kernel).",
         "struct TableRow {",
         "    int64_t M, N, K;",
         "    DispatchChoice c;",
@@ -270,10 +271,10 @@ def write_inc(results, path):
         split = effective_split(r["best"]["plan"])
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {{{o['variant']}, {o['tile_m']}, {o['tile_n']}, "
                      f"{o['stages']}, {split}, {split_where(r['best']['plan'])}, {o.get('tile_group', 0)}, "
-                     f"{o.get('tile_k', 0)}, {o.get('k_slices', 0)}}}}},"
+                     f"{o.get('tile_k', 0)}, {o.get('k_slices', 0)}, {o.get('split_reduce', 0)}}}}},"
                      f"  // {r['best']['us']} us")
     lines += [
-        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel",
+        "    {0, 0, 0, {0, 0, 0, 0, 0, 0, 0, 0, 0, 0}},  // sentinel",
         "};",
         "",
         "bool table_lookup(int64_t M, int64_t N, int64_t K, DispatchChoice& out)",
