@@ -147,7 +147,10 @@ typedef struct {
                                copies overlap); 0 = the dispatcher's choice, 1 = none,
                                n = n panels of whole tiles (128 rows; 256 for CTA-pair plans;
                                at most 64); with column blocks on a GEMM of 8 waves or more
-                               the first panel takes two shares of the tile rows */
+                               the first panel takes two shares of the tile rows; with column
+                               blocks and three panels or more, the last panel runs as two
+                               column halves when each half holds a wave of tiles, the first
+                               half's C copied back while the second half's GEMM runs */
     int32_t split_reduce;   /* TC only: how the K-slices of split tiles are summed.  0 = the
                                dispatcher's choice (1: measured fastest); 1 = a
                                reduction kernel over partial tiles in scratch; 3 = no extra
