@@ -790,3 +790,31 @@ def test_very_tall(variant):
     C, desc, canaries, _ = run_gemm(A, B, **variant)
     err, ok = check_against_oracle(C, A, B)
     assert canaries and ok, f"{desc}: {err}"
+
+
+def test_plans_on_several_streams_at_once():
+    # Different plans on different streams share nothing: two CTA-pair plans
+    # (one split in K, one of whole tiles) and a SIMT plan, queued back to back
+    # on three streams ten times, give the same bits as each run alone.
+    import torch
+    shapes = [(1024, 1024, 1024), (2048, 2048, 512), (513, 257, 129)]
+    runs = []
+    for i, (M, N, K) in enumerate(shapes):
+        A = inputs.uniform_pm1(2301 + 2 * i, M, K)
+        B = inputs.normal(2302 + 2 * i, K, N)
+        ref, desc, ok, _ = run_gemm(A, B)
+        assert ok, desc
+        runs.append((g.Plan(M, N, K), torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(),
+                     torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda"), ref, torch.cuda.Stream()))
+    try:
+        torch.cuda.synchronize()
+        for _ in range(10):
+            for p, dA, dB, dC, _, st in runs:
+                assert p.run_ptr(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), st.cuda_stream) == g.OK
+        for p, _, _, dC, ref, st in runs:
+            st.synchronize()
+            assert p.check() == g.OK
+            assert np.array_equal(dC.cpu().numpy().astype(np.float64), ref), p.describe()
+    finally:
+        for r in runs:
+            r[0].close()
