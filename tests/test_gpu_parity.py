@@ -818,3 +818,39 @@ def test_plans_on_several_streams_at_once():
     finally:
         for r in runs:
             r[0].close()
+
+
+@pytest.mark.parametrize("shape,opts", [
+    ((1024, 1024, 1024), {}),                                                   # CTA pairs, 4 K-slices
+    ((4096, 4096, 256), {}),                                                    # raw-A pairs: pre-pass, split last wave
+    ((768, 768, 768), dict(variant=g.VARIANT_TCGEN05, tile_m=128, split_k=4)),  # one CTA per tile
+    ((513, 257, 129), dict(variant=g.VARIANT_SIMT, split_k=2)),                 # SIMT with its reduction
+], ids=["pairs", "raw_a_pairs", "one_cta", "simt_split"])
+def test_runs_captured_in_a_cuda_graph(shape, opts):
+    # Every launch of a run is stream-ordered and allocation-free, so runs can
+    # be captured in a CUDA graph: replays give the bits of a plain run.
+    import torch
+    M, N, K = shape
+    A = inputs.uniform_pm1(2311, M, K)
+    B = inputs.normal(2312, K, N)
+    ref, desc, ok, _ = run_gemm(A, B, **opts)
+    assert ok, desc
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    with g.Plan(M, N, K, **opts) as p:
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            p.run_ptr(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), st.cuda_stream)  # warm (attributes, maps)
+        st.synchronize()
+        dC.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            for _ in range(2):
+                p.run_ptr(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), st.cuda_stream)
+        with torch.cuda.stream(st):
+            for _ in range(3):
+                graph.replay()
+        st.synchronize()
+        assert p.check() == g.OK
+        assert np.array_equal(dC.cpu().numpy().astype(np.float64), ref), p.describe()
