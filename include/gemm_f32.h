@@ -56,6 +56,11 @@
  *   - A plan is bound to the CUDA device that was current when it was made and
  *     must run with that device current.  One plan may be used from one stream
  *     at a time: it owns scratch memory (split-K partials, split operands).
+ *     Different plans may run on different streams at once.
+ *   - gemm_f32_run only enqueues kernels on the stream and allocates nothing,
+ *     so its runs can be captured in a CUDA graph (after one plain run of the
+ *     plan, which sets the kernels' attributes); gemm_f32_run_host and
+ *     gemm_f32_check synchronise and cannot.
  */
 #ifndef GEMM_F32_H_
 #define GEMM_F32_H_
