@@ -231,6 +231,22 @@ DispatchChoice choose_simt(int64_t M, int64_t N, int64_t K, int sms)
     if ((tiles > sms && tiles <= sms + sms / 4) || tiles <= sms / 8) c.tile_n = 16;
     const int64_t ctas = ((M + 31) / 32) * ((N + c.tile_n - 1) / c.tile_n);
     c.split_k = ctas >= sms / 2 ? 1 : auto_split(ctas, K, 128, sms);
+    // Many output tiles over a short K (up to 32): storing C and each CTA's
+    // setup dominate, and big tiles without K-slices win: 128x64 while they
+    // still give every SM a CTA, else 64x64; 16-deep K-tiles, two stages (the
+    // 64x64 tiles a single one when K fits it) (8192x8192x16 78 against 269 us with 32x32 sliced tiles,
+    // 16384^2 x 16 300 against 1147, 1024^2 x 16 2.9 against 5.2, 640^2 x 24
+    // 2.4 against 2.8).
+    const int64_t t64 = ((M + 63) / 64) * ((N + 63) / 64);
+    if (K <= 32 && t64 >= sms / 2) {
+        const int64_t t128 = ((M + 127) / 128) * ((N + 63) / 64);
+        c.tile_m = t128 >= sms ? 128 : 64;
+        c.tile_n = 64;
+        c.tile_k = 16;
+        c.stages = c.tile_m == 64 && K <= 16 ? 1 : 2;
+        c.k_slices = 1;
+        c.split_k = 1;
+    }
     return c;
 }
 
@@ -242,6 +258,9 @@ DispatchChoice choose(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     // enough to amortise the operand split; SIMT below that.
     const double macs = double(M) * double(N) * double(K);
     if (macs >= 6.0e7 && K >= 32) return choose_tc(M, N, K, lda, ldb, sms);  // K >= kTcMinK with margin
+    // a short K on a large product: the pre-pass form of the tensor cores
+    // (8192x2048x24 26 against 31 us on SIMT tiles, 3000x5000x20 27 against 29)
+    if (macs >= 2.5e8 && K >= 20) return choose_tc(M, N, K, lda, ldb, sms);
     return choose_simt(M, N, K, sms);
 }
 

@@ -122,6 +122,11 @@ RULE_SHAPES = [
     (96, 96, 1024, None, None), (33, 65, 129, None, None), (300, 40, 700, None, None),
     (1023, 1025, 1027, None, None), (2049, 2047, 2051, None, None), (1024, 1024, 1024, 1027, 1029),
     (4096, 4096, 4096, 4097, 4099),
+    # many output tiles over a short K
+    (1024, 1024, 16, None, None), (2048, 2048, 16, None, None), (4096, 4096, 16, None, None),
+    (3000, 5000, 20, None, None), (8192, 2048, 24, None, None), (1500, 1500, 31, None, None),
+    (800, 800, 16, None, None), (800, 800, 64, None, None), (640, 640, 24, None, None),
+    (16384, 4096, 20, None, None), (4096, 4096, 24, None, None), (2048, 8192, 28, None, None),
 ]
 
 
@@ -130,7 +135,10 @@ def rule_sweep(args):
     import torch
     stream = torch.cuda.current_stream()
     results = []
+    only = set(args.rule_shapes.split(",")) if args.rule_shapes else None
     for (M, N, K, lda, ldb) in RULE_SHAPES:
+        if only and f"{M}x{N}x{K}" not in only:
+            continue
         lda, ldb = lda or K, ldb or N
         A = inputs.uniform_pm1(8001, M, K, ld=lda if lda != K else None)
         B = inputs.uniform_pm1(8002, K, N, ld=ldb if ldb != N else None)
@@ -181,6 +189,7 @@ def main():
     ap.add_argument("--inc", default=None)
     ap.add_argument("--workloads", default="tiny_32,small_ragged,tall_skinny,square_1024,large_squares")
     ap.add_argument("--rule-sweep", action="store_true")
+    ap.add_argument("--rule-shapes", default=None, help="with --rule-sweep: only these MxNxK, comma-separated")
     ap.add_argument("--md", action="store_true")
     args = ap.parse_args()
     g.load()

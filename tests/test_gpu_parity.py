@@ -854,3 +854,18 @@ def test_runs_captured_in_a_cuda_graph(shape, opts):
         st.synchronize()
         assert p.check() == g.OK
         assert np.array_equal(dC.cpu().numpy().astype(np.float64), ref), p.describe()
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 16), (2048, 2048, 8), (700, 900, 5), (640, 640, 24),
+                                   (1500, 1500, 31), (2048, 4096, 1)])
+def test_short_k_over_many_tiles(shape):
+    # Many output tiles over a short K take big SIMT tiles without K-slices
+    # (the dispatcher's rule); checked element by element against the oracle.
+    M, N, K = shape
+    A = inputs.uniform_pm1(2321, M, K)
+    B = inputs.normal(2322, K, N)
+    C, desc, ok, _ = run_gemm(A, B)
+    assert ok, desc
+    assert desc.startswith("simt") and (("tile=128x64x16" in desc) or ("tile=64x64x16" in desc)), desc
+    err, okb = check_against_oracle(C, A, B)
+    assert okb, f"{desc}: {err}"
