@@ -19,7 +19,9 @@ using namespace gemm_f32;
 
 namespace {
 
-enum PlanKind : int { kNoop = 0, kZeroFill = 1, kSimt = 2, kTc = 3 };
+enum PlanKind : int { kNoop = 0, kZeroFill = 1, kSimt = 2, kTc = 3, kRows = 4 };
+// The short-M kernel (rows.cu).
+constexpr int kVariantRows = GEMM_F32_VARIANT_SHORT_M;
 
 // Smallest K the tensor-core path accepts (accuracy of the 3xTF32 split):
 // 16 with the round-to-nearest split of the pre-pass, 32 with the truncating
@@ -127,7 +129,7 @@ static_assert(sizeof(gemm_f32_opts) == 72, "gemm_f32_opts layout");
 
 gemm_f32_status validate_opts(const gemm_f32_opts& o)
 {
-    if (o.variant < 0 || o.variant > GEMM_F32_VARIANT_TCGEN05) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.variant < 0 || o.variant > GEMM_F32_VARIANT_SHORT_M) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_m < 0 || o.tile_n < 0 || o.stages < 0 || o.split_k < 0 || o.split_k > 64)
         return GEMM_F32_ERR_INVALID_ARG;
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
@@ -254,6 +256,17 @@ DispatchChoice choose(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
 {
     DispatchChoice c{};
     if (table_lookup(M, N, K, c)) return c;
+    // A short A (up to 8 rows) against a large B (2^24 elements or more): the
+    // product is bound by reading B, which the short-M kernel streams once
+    // (1x8192x8192 49 against 112 us on 128-row tensor-core tiles, whose rows
+    // are mostly padding; 8x8192x8192 63 against 112).  With 16 rows its
+    // registers cap it under the tensor cores (16x8192x8192 123 against 111),
+    // and with a small B its blocks' chain of loads is exposed (1x1024x1024
+    // 8.4 against 6.1 us on SIMT tiles).
+    if (M <= 8 && double(N) * double(K) >= 16777216.0) {
+        c.variant = kVariantRows;
+        return c;
+    }
     // Shapes outside the measured table: tensor cores once the product is big
     // enough to amortise the operand split; SIMT below that.
     const double macs = double(M) * double(N) * double(K);
@@ -319,8 +332,21 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         DispatchChoice c = choose(M, N, K, lda, ldb, p->num_sms);
         if (o.variant != GEMM_F32_VARIANT_AUTO && o.variant != c.variant) {
             // A forced variant starts from that variant's own rule.
-            c = o.variant == GEMM_F32_VARIANT_SIMT ? choose_simt(M, N, K, p->num_sms)
-                                                   : choose_tc(M, N, K, lda, ldb, p->num_sms);
+            if (o.variant == kVariantRows) {
+                if (M > kRowsMaxM) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+                c = DispatchChoice{};
+                c.variant = kVariantRows;
+            } else {
+                c = o.variant == GEMM_F32_VARIANT_SIMT ? choose_simt(M, N, K, p->num_sms)
+                                                       : choose_tc(M, N, K, lda, ldb, p->num_sms);
+            }
+        }
+        // Options of the SIMT kernel's shape turn the dispatcher's short-M choice
+        // into a SIMT plan (a forced short-M variant takes none of them).
+        if (c.variant == kVariantRows && (o.tile_m || o.tile_n || o.stages || o.split_k || o.k_slices || o.tile_k ||
+                                          o.separate_syncs || o.simt_fragments)) {
+            if (o.variant == kVariantRows) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            c = choose_simt(M, N, K, p->num_sms);
         }
         // A forced tile or ring replaces the choice, so the table's K-tile depth
         // and tile order (tuned for its own tile) no longer apply.
@@ -330,7 +356,19 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         if (o.stages) c.stages = o.stages;
         if (o.split_k) c.split_k = o.split_k;
 
-        if (c.variant == GEMM_F32_VARIANT_SIMT) {
+        if (c.variant == kVariantRows) {
+            p->kind = kRows;
+            const int64_t chunk = rows_range(N, K, p->num_sms);
+            p->split_k = (int)((K + chunk - 1) / chunk);
+            p->k_chunk = chunk;
+            if (p->split_k > 1) {
+                p->ldp = round_up(N, 4);
+                part_off = bytes;
+                bytes += align256(size_t(p->split_k) * size_t(M) * size_t(p->ldp) * sizeof(float));
+            }
+            snprintf(p->desc, sizeof p->desc, "simt short-m rows=%lld cols-per-block=256 k-range=%lld split_k=%d",
+                     (long long)M, (long long)chunk, p->split_k);
+        } else if (c.variant == GEMM_F32_VARIANT_SIMT) {
             p->kind = kSimt;
             const int ksl = o.k_slices ? o.k_slices : c.k_slices ? c.k_slices : 1;
             p->simt_id = simt_find_config(c.tile_m, c.tile_n, c.stages, o.separate_syncs != 0,
@@ -487,7 +525,7 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
     char* base = static_cast<char*>(p->ws);
     p->d_status = reinterpret_cast<int*>(base + status_off);
     e = cudaMemset(p->d_status, 0, sizeof(int));
-    if (p->kind == kSimt && p->split_k > 1) p->partial = reinterpret_cast<float*>(base + part_off);
+    if ((p->kind == kSimt || p->kind == kRows) && p->split_k > 1) p->partial = reinterpret_cast<float*>(base + part_off);
     if (p->kind == kTc) {
         TcPlanState& t = p->tc;
         t.a_hi = reinterpret_cast<float*>(base + ahi_off);
@@ -939,6 +977,20 @@ gemm_f32_status gemm_f32_run(gemm_f32_plan_t p, const float* A, const float* B, 
         if (ev) cudaEventRecord(ev[3], s);
         break;
     }
+    case kRows: {
+        RowsArgs a{};
+        a.M = p->M; a.N = p->N; a.K = p->K;
+        a.A = A; a.lda = p->lda; a.B = B; a.ldb = p->ldb; a.C = C; a.ldc = p->ldc;
+        a.partial = p->partial; a.ldp = p->ldp;
+        a.range = p->k_chunk;
+        if (ev) { cudaEventRecord(ev[0], s); cudaEventRecord(ev[1], s); }
+        e = rows_launch(a, s);
+        if (ev) cudaEventRecord(ev[2], s);
+        if (e == cudaSuccess && p->split_k > 1)
+            e = splitk_reduce_launch(p->partial, p->split_k, p->M, p->N, p->ldp, C, p->ldc, s);
+        if (ev) cudaEventRecord(ev[3], s);
+        break;
+    }
     case kTc:
         e = tc_launch(p->tc, p->M, p->N, p->K, A, p->lda, B, p->ldb, C, p->ldc, p->d_status, s, ev);
         break;
@@ -1077,6 +1129,7 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
     switch (p->kind) {
     case kZeroFill: return (int)p->batch;
     case kSimt: return p->split_k > 1 ? 2 : 1;
+    case kRows: return p->split_k > 1 ? 2 : 1;
     case kTc: {
         // the pre-pass (unless both operands are split in the kernel), the GEMM,
         // and the reduction of split tiles

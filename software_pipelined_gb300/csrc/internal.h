@@ -56,6 +56,23 @@ struct SimtArgs {
 };
 cudaError_t simt_launch(int config_id, const SimtArgs& a, cudaStream_t s);
 
+// ---- short-M kernel (rows.cu) ----------------------------------------------
+// C = A*B for M <= kRowsMaxM, streaming B once; K in ranges of `range` rows
+// (rows_range: a multiple of 256), each range's partial written to `partial`
+// (range z at partial + z*M*ldp) for the split-K reduction when K spans more
+// than one range, else C directly.
+constexpr int64_t kRowsMaxM = 16;
+struct RowsArgs {
+    int64_t M, N, K;
+    const float* A; int64_t lda;
+    const float* B; int64_t ldb;
+    float* C; int64_t ldc;
+    float* partial; int64_t ldp;
+    int64_t range;
+};
+int64_t rows_range(int64_t N, int64_t K, int sms);
+cudaError_t rows_launch(const RowsArgs& a, cudaStream_t s);
+
 // Deterministic split-K reduction: C[i][j] = sum_{z=0}^{splits-1} P[z][i][j]
 // in ascending z (splitk_reduce.cu).
 cudaError_t splitk_reduce_launch(const float* P, int splits, int64_t M, int64_t N, int64_t ldp,

@@ -869,3 +869,45 @@ def test_short_k_over_many_tiles(shape):
     assert desc.startswith("simt") and (("tile=128x64x16" in desc) or ("tile=64x64x16" in desc)), desc
     err, okb = check_against_oracle(C, A, B)
     assert okb, f"{desc}: {err}"
+
+
+SHORT_M = [
+    # (M, N, K, lda, ldb, ldc): a short A against B, the short-M kernel forced
+    (1, 8192, 8192, None, None, None),       # the dispatcher's choice too
+    (16, 4096, 4096, None, None, None),
+    (5, 1000, 3000, None, None, None),       # N past the last whole block
+    (13, 777, 1500, 1503, 781, 790),         # B rows not 16-byte aligned: scalar loads
+    (3, 2049, 513, None, None, None),        # K past the last whole piece, N past a quad
+    (16, 256, 65536, None, None, None),      # several pieces per block's K-range
+    (1, 300, 4096, 4100, None, None),
+    (7, 33, 40, None, None, None),           # one block, one piece, one range: C written directly
+]
+
+
+@pytest.mark.parametrize("case", SHORT_M, ids=[f"{c[0]}x{c[1]}x{c[2]}" for c in SHORT_M])
+def test_short_m_against_the_oracle(case):
+    M, N, K, lda, ldb, ldc = case
+    A = inputs.uniform_pm1(2331, M, K)
+    B = inputs.normal(2332, K, N)
+    C, desc, ok, outs = run_gemm(A, B, lda=lda, ldb=ldb, ldc=ldc, repeat=2, variant=g.VARIANT_SHORT_M)
+    assert desc.startswith("simt short-m"), desc
+    assert ok, desc
+    assert np.array_equal(outs[0], outs[1]), desc
+    err, okb = check_against_oracle(C, A, B)
+    assert okb, f"{desc}: {err}"
+    with g.Plan(M, N, K, variant=g.VARIANT_SHORT_M) as p:
+        splits = int(p.describe().split("split_k=")[1].split()[0])
+        assert p.kernel_launches == (2 if splits > 1 else 1)
+    # the dispatcher takes it for up to 8 rows against 2^24 elements of B or more
+    chosen = M <= 8 and N * K >= 2 ** 24
+    with g.Plan(M, N, K) as p:
+        assert p.describe().startswith("simt short-m") == chosen, p.describe()
+    # there, options of the SIMT kernel's shape give an ordinary SIMT plan;
+    # forced together with the short-M variant, or past 16 rows, it is refused
+    if chosen:
+        with g.Plan(M, N, K, tile_m=32, tile_n=32) as p:
+            assert p.describe().startswith("simt tile=32x32"), p.describe()
+    with pytest.raises(g.GemmError):
+        g.Plan(M, N, K, variant=g.VARIANT_SHORT_M, tile_m=32, tile_n=32)
+    with pytest.raises(g.GemmError):
+        g.Plan(17, N, K, variant=g.VARIANT_SHORT_M)
