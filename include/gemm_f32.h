@@ -98,10 +98,14 @@ typedef enum {
     GEMM_F32_VARIANT_AUTO = 0,     /* dispatcher's choice */
     GEMM_F32_VARIANT_SIMT = 1,     /* FFMA, cp.async multi-stage */
     GEMM_F32_VARIANT_TCGEN05 = 2,  /* tcgen05 3xTF32 with TMA/mbarrier pipeline */
-    GEMM_F32_VARIANT_SHORT_M = 3   /* FFMA for M <= 16 (else UNSUPPORTED): B streamed once in
+    GEMM_F32_VARIANT_SHORT_M = 3,  /* FFMA for M <= 16 (else UNSUPPORTED): B streamed once in
                                       256-column blocks over ranges of K, the ranges' sums
                                       added by the split-K reduction; the dispatcher takes it
                                       for M <= 8 with K x N at least 2^24 */
+    GEMM_F32_VARIANT_SHORT_N = 4   /* FFMA for N <= 16 (else UNSUPPORTED): a warp per row of C
+                                      streams that row of A once, its lanes' sums added in a
+                                      fixed order; fast for N = 1 only, where the dispatcher
+                                      takes it (M at least 4096, M x K at least 2^24) */
 } gemm_f32_variant;
 
 /* Options for gemm_f32_plan_ex.  Zero means "dispatcher's choice" for every

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgemm_f32.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM = range(6)
-VARIANT_AUTO, VARIANT_SIMT, VARIANT_TCGEN05, VARIANT_SHORT_M = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_TCGEN05, VARIANT_SHORT_M, VARIANT_SHORT_N = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "OOM"}
 
 EXPORTED = ("gemm_f32_opts_init", "gemm_f32_plan", "gemm_f32_plan_ex", "gemm_f32_run",

@@ -19,9 +19,10 @@ using namespace gemm_f32;
 
 namespace {
 
-enum PlanKind : int { kNoop = 0, kZeroFill = 1, kSimt = 2, kTc = 3, kRows = 4 };
-// The short-M kernel (rows.cu).
+enum PlanKind : int { kNoop = 0, kZeroFill = 1, kSimt = 2, kTc = 3, kRows = 4, kCols = 5 };
+// The short-M and short-N kernels (rows.cu).
 constexpr int kVariantRows = GEMM_F32_VARIANT_SHORT_M;
+constexpr int kVariantCols = GEMM_F32_VARIANT_SHORT_N;
 
 // Smallest K the tensor-core path accepts (accuracy of the 3xTF32 split):
 // 16 with the round-to-nearest split of the pre-pass, 32 with the truncating
@@ -129,7 +130,7 @@ static_assert(sizeof(gemm_f32_opts) == 72, "gemm_f32_opts layout");
 
 gemm_f32_status validate_opts(const gemm_f32_opts& o)
 {
-    if (o.variant < 0 || o.variant > GEMM_F32_VARIANT_SHORT_M) return GEMM_F32_ERR_INVALID_ARG;
+    if (o.variant < 0 || o.variant > GEMM_F32_VARIANT_SHORT_N) return GEMM_F32_ERR_INVALID_ARG;
     if (o.tile_m < 0 || o.tile_n < 0 || o.stages < 0 || o.split_k < 0 || o.split_k > 64)
         return GEMM_F32_ERR_INVALID_ARG;
     if (!(o.tf32_terms == 0 || o.tf32_terms == 1 || o.tf32_terms == 3)) return GEMM_F32_ERR_INVALID_ARG;
@@ -267,6 +268,14 @@ DispatchChoice choose(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
         c.variant = kVariantRows;
         return c;
     }
+    // The mirror case, a single column of B against a large A with rows enough
+    // for a warp on each: the short-N kernel (8192x1x8192 66 against 103 us on
+    // tensor-core tiles, 65536x1x512 30 against 74).  From two columns its
+    // loads of B's rows through L1 bound it (8192x4x8192 588 against 111).
+    if (N == 1 && M >= 4096 && double(M) * double(K) >= 16777216.0) {
+        c.variant = kVariantCols;
+        return c;
+    }
     // Shapes outside the measured table: tensor cores once the product is big
     // enough to amortise the operand split; SIMT below that.
     const double macs = double(M) * double(N) * double(K);
@@ -332,10 +341,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         DispatchChoice c = choose(M, N, K, lda, ldb, p->num_sms);
         if (o.variant != GEMM_F32_VARIANT_AUTO && o.variant != c.variant) {
             // A forced variant starts from that variant's own rule.
-            if (o.variant == kVariantRows) {
-                if (M > kRowsMaxM) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+            if (o.variant == kVariantRows || o.variant == kVariantCols) {
+                if (o.variant == kVariantRows ? M > kRowsMaxM : N > kColsMaxN) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
                 c = DispatchChoice{};
-                c.variant = kVariantRows;
+                c.variant = o.variant;
             } else {
                 c = o.variant == GEMM_F32_VARIANT_SIMT ? choose_simt(M, N, K, p->num_sms)
                                                        : choose_tc(M, N, K, lda, ldb, p->num_sms);
@@ -343,9 +352,10 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         }
         // Options of the SIMT kernel's shape turn the dispatcher's short-M choice
         // into a SIMT plan (a forced short-M variant takes none of them).
-        if (c.variant == kVariantRows && (o.tile_m || o.tile_n || o.stages || o.split_k || o.k_slices || o.tile_k ||
-                                          o.separate_syncs || o.simt_fragments)) {
-            if (o.variant == kVariantRows) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
+        if ((c.variant == kVariantRows || c.variant == kVariantCols) &&
+            (o.tile_m || o.tile_n || o.stages || o.split_k || o.k_slices || o.tile_k || o.separate_syncs ||
+             o.simt_fragments)) {
+            if (o.variant == kVariantRows || o.variant == kVariantCols) { delete p; return GEMM_F32_ERR_UNSUPPORTED; }
             c = choose_simt(M, N, K, p->num_sms);
         }
         // A forced tile or ring replaces the choice, so the table's K-tile depth
@@ -356,7 +366,11 @@ gemm_f32_status make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
         if (o.stages) c.stages = o.stages;
         if (o.split_k) c.split_k = o.split_k;
 
-        if (c.variant == kVariantRows) {
+        if (c.variant == kVariantCols) {
+            p->kind = kCols;
+            p->split_k = 1;
+            snprintf(p->desc, sizeof p->desc, "simt short-n cols=%lld warp-per-row", (long long)N);
+        } else if (c.variant == kVariantRows) {
             p->kind = kRows;
             const int64_t chunk = rows_range(N, K, p->num_sms);
             p->split_k = (int)((K + chunk - 1) / chunk);
@@ -977,6 +991,15 @@ gemm_f32_status gemm_f32_run(gemm_f32_plan_t p, const float* A, const float* B, 
         if (ev) cudaEventRecord(ev[3], s);
         break;
     }
+    case kCols: {
+        ColsArgs a{};
+        a.M = p->M; a.N = p->N; a.K = p->K;
+        a.A = A; a.lda = p->lda; a.B = B; a.ldb = p->ldb; a.C = C; a.ldc = p->ldc;
+        if (ev) { cudaEventRecord(ev[0], s); cudaEventRecord(ev[1], s); }
+        e = cols_launch(a, p->num_sms, s);
+        if (ev) { cudaEventRecord(ev[2], s); cudaEventRecord(ev[3], s); }
+        break;
+    }
     case kRows: {
         RowsArgs a{};
         a.M = p->M; a.N = p->N; a.K = p->K;
@@ -1130,6 +1153,7 @@ int gemm_f32_plan_kernel_launches(gemm_f32_plan_t p)
     case kZeroFill: return (int)p->batch;
     case kSimt: return p->split_k > 1 ? 2 : 1;
     case kRows: return p->split_k > 1 ? 2 : 1;
+    case kCols: return 1;
     case kTc: {
         // the pre-pass (unless both operands are split in the kernel), the GEMM,
         // and the reduction of split tiles

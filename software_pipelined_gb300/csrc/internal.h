@@ -72,6 +72,15 @@ struct RowsArgs {
 };
 int64_t rows_range(int64_t N, int64_t K, int sms);
 cudaError_t rows_launch(const RowsArgs& a, cudaStream_t s);
+// C = A*B for N <= kColsMaxN, streaming A once (a warp per row of C; rows.cu).
+constexpr int64_t kColsMaxN = 16;
+struct ColsArgs {
+    int64_t M, N, K;
+    const float* A; int64_t lda;
+    const float* B; int64_t ldb;
+    float* C; int64_t ldc;
+};
+cudaError_t cols_launch(const ColsArgs& a, int sms, cudaStream_t s);
 
 // Deterministic split-K reduction: C[i][j] = sum_{z=0}^{splits-1} P[z][i][j]
 // in ascending z (splitk_reduce.cu).

@@ -150,3 +150,92 @@ cudaError_t rows_launch(const RowsArgs& a, cudaStream_t s)
 }
 
 }  // namespace gemm_f32
+
+// Products with a short B (N up to 16 columns) against a large A: the mirror
+// case, bound by reading A once.  Each warp computes whole rows of C (a
+// grid-stride loop over rows): its lanes stream the row of A with 16-byte
+// loads (512 contiguous bytes a step, four steps in flight), take B's rows for
+// their k through L1 (B is K x N, small), keep NR FP32 sums each, and add the
+// 32 lanes' sums in a fixed butterfly order.  Every output is summed in one
+// order, run after run.
+namespace gemm_f32 {
+namespace {
+
+constexpr int kColsThreads = 256;
+constexpr int kColsUnroll = 4;
+
+template <int NR>
+__global__ void __launch_bounds__(kColsThreads)
+cols_kernel(const float* __restrict__ A, int64_t lda, const float* __restrict__ B, int64_t ldb,
+            float* __restrict__ C, int64_t ldc, int64_t M, int64_t N, int64_t K, int vec_a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t wpb = kColsThreads / 32;
+    for (int64_t i = (int64_t)blockIdx.x * wpb + threadIdx.x / 32; i < M; i += (int64_t)gridDim.x * wpb) {
+        const float* arow = A + i * lda;
+        float acc[NR];
+#pragma unroll
+        for (int j = 0; j < NR; ++j) acc[j] = 0.f;
+        for (int64_t k0 = 4 * lane; k0 < K; k0 += 128 * kColsUnroll) {
+            float a[kColsUnroll][4];
+#pragma unroll
+            for (int u = 0; u < kColsUnroll; ++u) {
+                const int64_t k = k0 + 128 * u;
+                if (vec_a && k + 3 < K) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(arow + k));
+                    a[u][0] = v.x; a[u][1] = v.y; a[u][2] = v.z; a[u][3] = v.w;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a[u][c] = k + c < K ? __ldg(arow + k + c) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kColsUnroll; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int64_t k = k0 + 128 * u + c;
+                    if (k < K) {
+                        const float* brow = B + k * ldb;
+#pragma unroll
+                        for (int j = 0; j < NR; ++j)
+                            if (j < N) acc[j] = fmaf(a[u][c], __ldg(brow + j), acc[j]);
+                    }
+                }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < NR; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+                if (j < N) C[i * ldc + j] = acc[j];
+    }
+}
+
+template <int NR>
+cudaError_t launch_cols(const ColsArgs& a, int sms, cudaStream_t s)
+{
+    const int64_t wpb = kColsThreads / 32;
+    int64_t blocks = (a.M + wpb - 1) / wpb;
+    const int64_t cap = (int64_t)sms * 16;
+    if (blocks > cap) blocks = cap;
+    const int vec_a = (a.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(a.A) % 16 == 0);
+    cols_kernel<NR><<<(unsigned)blocks, kColsThreads, 0, s>>>(a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.M, a.N, a.K,
+                                                              vec_a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t cols_launch(const ColsArgs& a, int sms, cudaStream_t s)
+{
+    if (a.M < 1 || a.N < 1 || a.N > kColsMaxN || a.K < 1 || sms < 1) return cudaErrorInvalidValue;
+    if (a.N <= 1) return launch_cols<1>(a, sms, s);
+    if (a.N <= 2) return launch_cols<2>(a, sms, s);
+    if (a.N <= 4) return launch_cols<4>(a, sms, s);
+    if (a.N <= 8) return launch_cols<8>(a, sms, s);
+    return launch_cols<16>(a, sms, s);
+}
+
+}  // namespace gemm_f32

@@ -68,7 +68,7 @@ def test_plan_rejects_bad_dims(lib, dims):
 
 
 def test_plan_rejects_bad_options(lib):
-    for field, value in [("variant", 7), ("split_k", 65), ("tf32_terms", 2), ("stages", -1),
+    for field, value in [("variant", 7), ("variant", 5), ("split_k", 65), ("tf32_terms", 2), ("stages", -1),
                          ("wait_timeout_cycles", -5), ("operand_split", 6), ("tile_group", 65),
                          ("host_panels", 65), ("host_panels", -1), ("split_reduce", 5), ("split_reduce", -1), ("k_slices", 3), ("k_slices", 8),
                          ("host_col_blocks", -1), ("host_col_blocks", 17), ("simt_fragments", 2)]:

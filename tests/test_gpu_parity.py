@@ -911,3 +911,30 @@ def test_short_m_against_the_oracle(case):
         g.Plan(M, N, K, variant=g.VARIANT_SHORT_M, tile_m=32, tile_n=32)
     with pytest.raises(g.GemmError):
         g.Plan(17, N, K, variant=g.VARIANT_SHORT_M)
+
+
+SHORT_N = [
+    # (M, N, K, lda, ldb, ldc): a short B against A, the short-N kernel forced
+    (8192, 1, 8192, None, None, None),       # the dispatcher's choice too
+    (4096, 4, 4100, None, None, None),        # K past a 512-element step
+    (300, 16, 4096, None, None, None),
+    (5000, 3, 1001, 1003, 5, 7),            # A rows not 16-byte aligned: scalar loads
+    (33, 7, 40, None, None, None),
+]
+
+
+@pytest.mark.parametrize("case", SHORT_N, ids=[f"{c[0]}x{c[1]}x{c[2]}" for c in SHORT_N])
+def test_short_n_against_the_oracle(case):
+    M, N, K, lda, ldb, ldc = case
+    A = inputs.uniform_pm1(2341, M, K)
+    B = inputs.normal(2342, K, N)
+    C, desc, ok, outs = run_gemm(A, B, lda=lda, ldb=ldb, ldc=ldc, repeat=2, variant=g.VARIANT_SHORT_N)
+    assert desc.startswith("simt short-n"), desc
+    assert ok, desc
+    assert np.array_equal(outs[0], outs[1]), desc
+    err, okb = check_against_oracle(C, A, B)
+    assert okb, f"{desc}: {err}"
+    with g.Plan(M, N, K) as p:
+        assert p.describe().startswith("simt short-n") == (N == 1 and M >= 4096 and M * K >= 2 ** 24), p.describe()
+    with pytest.raises(g.GemmError):
+        g.Plan(M, 17, K, variant=g.VARIANT_SHORT_N)
