@@ -49,7 +49,7 @@
  *     stay finite through the split.  The two pieces carry 22 significand
  *     bits, whose per-product error of about 3*2^-22*|a||b| meets the first
  *     term only for K of about 10 and up, so the tensor-core path takes
- *     K >= 16 only; smaller K always runs on the SIMT kernel.  With
+ *     K >= 16 only; smaller K always runs on an FFMA kernel.  With
  *     non-finite inputs the affected outputs are non-finite, but not
  *     necessarily the IEEE value (the 3xTF32 split turns +-Inf into NaN).
  *   - Errors are returned as status codes; nothing calls exit or abort.
